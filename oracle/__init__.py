@@ -1,0 +1,246 @@
+"""Reference oracle (fp64, CPU) for the speculative-decoding verification step.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package.  The
+product path (``sampling_row_online_gb300``) never imports it, and the two share
+no code.  The arithmetic lives in ``oracle.c`` (plain C, fp64, left-to-right
+loops); this module only marshals arrays through ctypes.
+
+Inputs are CPU tensors (``torch.float32`` / ``torch.bfloat16``) or numpy arrays
+(``float32``; ``uint16``/``int16`` holding bfloat16 bit patterns).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lib = None
+
+F32, BF16 = 0, 1
+OK, ERR_ARG, ERR_TOKEN, ERR_PARENT = 0, 1, 2, 3
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        c_p = ctypes.c_void_p
+        i32, u32, u64, f64 = ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_double
+        lib.oracle_philox4x32_10.argtypes = [c_p, c_p, c_p]
+        lib.oracle_philox4x32_10.restype = None
+        lib.oracle_uniform.argtypes = [u64, u32, u32, u32]
+        lib.oracle_uniform.restype = f64
+        lib.oracle_row_stats.argtypes = [c_p, i32, i32, f64, c_p, c_p]
+        lib.oracle_row_stats.restype = None
+        lib.oracle_argmax.argtypes = [c_p, i32, i32]
+        lib.oracle_argmax.restype = i32
+        lib.oracle_accept.argtypes = [c_p, c_p, i32, i32, f64, i32, f64, c_p, c_p]
+        lib.oracle_accept.restype = i32
+        lib.oracle_target_sample.argtypes = [c_p, i32, i32, f64, f64, c_p]
+        lib.oracle_target_sample.restype = i32
+        lib.oracle_residual_sample.argtypes = [c_p, c_p, i32, i32, f64, f64, c_p, c_p]
+        lib.oracle_residual_sample.restype = i32
+        lib.oracle_verify_chain.argtypes = [c_p, c_p, c_p, i32, i32, i32, i32, f64, u64,
+                                            c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, c_p, i32]
+        lib.oracle_verify_chain.restype = i32
+        lib.oracle_tree_max_depth.argtypes = [c_p, i32]
+        lib.oracle_tree_max_depth.restype = i32
+        lib.oracle_tree_mask.argtypes = [c_p, i32, c_p, c_p]
+        lib.oracle_tree_mask.restype = i32
+        lib.oracle_verify_tree_greedy.argtypes = [c_p, c_p, c_p, i32, i32, i32, i32, i32,
+                                                  c_p, c_p, i32]
+        lib.oracle_verify_tree_greedy.restype = i32
+        lib.oracle_max_threads.argtypes = []
+        lib.oracle_max_threads.restype = i32
+        _lib = lib
+    return _lib
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+# ----------------------------------------------------------------------------
+# array marshalling
+# ----------------------------------------------------------------------------
+def _logits(z):
+    """Return (contiguous numpy array holding the raw element bits, dtype code)."""
+    try:
+        import torch
+    except ImportError:  # pragma: no cover
+        torch = None
+    if torch is not None and isinstance(z, torch.Tensor):
+        z = z.detach()
+        if z.device.type != "cpu":
+            raise ValueError("oracle inputs must be CPU tensors")
+        z = z.contiguous()
+        if z.dtype == torch.float32:
+            return z.numpy(), F32
+        if z.dtype == torch.bfloat16:
+            return z.view(torch.int16).numpy(), BF16
+        raise TypeError(f"unsupported logits dtype {z.dtype}")
+    a = np.ascontiguousarray(z)
+    if a.dtype == np.float32:
+        return a, F32
+    if a.dtype in (np.uint16, np.int16):
+        return a, BF16
+    if a.dtype == np.float64:
+        raise TypeError("pass float32 (or bfloat16 bits); the oracle widens exactly itself")
+    raise TypeError(f"unsupported logits dtype {a.dtype}")
+
+
+def _i32(a):
+    try:
+        import torch
+        if isinstance(a, torch.Tensor):
+            a = a.detach().cpu().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(a), dtype=np.int32)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ----------------------------------------------------------------------------
+# public helpers
+# ----------------------------------------------------------------------------
+def philox4x32_10(ctr, key):
+    """Philox4x32-10 block: 4 counter words, 2 key words -> 4 output words."""
+    c = np.asarray(ctr, dtype=np.uint32).copy()
+    k = np.asarray(key, dtype=np.uint32).copy()
+    out = np.zeros(4, dtype=np.uint32)
+    _load().oracle_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return [int(v) for v in out]
+
+
+def uniform(seed: int, b: int, position: int, slot: int) -> float:
+    """u = (word0 >> 8) * 2^-24 of Philox(counter=(b, position, slot, 0), key=seed)."""
+    return float(_load().oracle_uniform(seed, b, position, slot))
+
+
+def row_stats(z, T: float):
+    """(m, S) = (max z, sum exp((z - m) / T)) of one row, in fp64."""
+    a, dt = _logits(z)
+    m, S = ctypes.c_double(), ctypes.c_double()
+    _load().oracle_row_stats(_ptr(a), dt, a.size, float(T), ctypes.byref(m), ctypes.byref(S))
+    return m.value, S.value
+
+
+def argmax(z) -> int:
+    a, dt = _logits(z)
+    return int(_load().oracle_argmax(_ptr(a), dt, a.size))
+
+
+def accept(zt, zd, x: int, T: float, u: float):
+    """(accepted, r = p(x)/q(x), near) for one draft token under uniform u."""
+    a, dt = _logits(zt)
+    d, dt2 = _logits(zd)
+    assert dt == dt2 and a.size == d.size
+    r, near = ctypes.c_double(), ctypes.c_int()
+    ok = _load().oracle_accept(_ptr(a), _ptr(d), dt, a.size, float(T), int(x), float(u),
+                               ctypes.byref(r), ctypes.byref(near))
+    return bool(ok), r.value, bool(near.value)
+
+
+def target_sample(zt, T: float, u: float):
+    """(token, near) drawn from p = softmax(zt / T) by inverse CDF at uniform u."""
+    a, dt = _logits(zt)
+    near = ctypes.c_int()
+    tok = _load().oracle_target_sample(_ptr(a), dt, a.size, float(T), float(u), ctypes.byref(near))
+    return int(tok), bool(near.value)
+
+
+def residual_sample(zt, zd, T: float, u: float):
+    """(token, near, fallback) drawn from norm(max(0, p - q)) at uniform u."""
+    a, dt = _logits(zt)
+    d, _ = _logits(zd)
+    near, fb = ctypes.c_int(), ctypes.c_int()
+    tok = _load().oracle_residual_sample(_ptr(a), _ptr(d), dt, a.size, float(T), float(u),
+                                         ctypes.byref(near), ctypes.byref(fb))
+    return int(tok), bool(near.value), bool(fb.value)
+
+
+def verify_chain(zt, zd, draft_tokens, T: float, seed: int, *, b_ids=None, u_acc=None,
+                 u_samp=None, want_stats=False, nthreads=1):
+    """Chain verification of nb sequences.
+
+    zt: [nb, K+1, V]; zd: [nb, K, V] (may be None when T == 0); draft_tokens: [nb, K].
+    Returns a dict with tokens [nb, K+1], n_accepted [nb], near [nb], fallback [nb],
+    status, and (want_stats) row_max / row_sumexp [nb, 2K+1].
+    """
+    zt_a, dt = _logits(zt)
+    nb, K1, V = zt_a.shape
+    K = K1 - 1
+    zd_a = None
+    if zd is not None and K > 0:
+        zd_a, dt2 = _logits(zd)
+        assert dt2 == dt and zd_a.shape == (nb, K, V)
+    elif T > 0 and K > 0:
+        raise ValueError("draft logits are required when T > 0")
+    x = _i32(draft_tokens).reshape(nb, K)
+    bi = None if b_ids is None else _i32(b_ids).reshape(nb)
+    ua = None if u_acc is None else np.ascontiguousarray(u_acc, dtype=np.float64).reshape(nb, K)
+    us = None if u_samp is None else np.ascontiguousarray(u_samp, dtype=np.float64).reshape(nb, K + 1)
+    tokens = np.zeros((nb, K + 1), dtype=np.int32)
+    n = np.zeros(nb, dtype=np.int32)
+    near = np.zeros(nb, dtype=np.int32)
+    fb = np.zeros(nb, dtype=np.int32)
+    m = S = None
+    if want_stats:
+        m = np.zeros((nb, 2 * K + 1), dtype=np.float64)
+        S = np.zeros((nb, 2 * K + 1), dtype=np.float64)
+    st = _load().oracle_verify_chain(_ptr(zt_a), _ptr(zd_a), _ptr(x), nb, K, V, dt, float(T),
+                                     int(seed) & ((1 << 64) - 1), _ptr(bi), _ptr(ua), _ptr(us),
+                                     _ptr(tokens), _ptr(n), _ptr(near), _ptr(fb), _ptr(m),
+                                     _ptr(S), int(nthreads))
+    if st == ERR_ARG:
+        raise ValueError("oracle_verify_chain: invalid arguments")
+    out = dict(tokens=tokens, n_accepted=n, near=near.astype(bool), fallback=fb.astype(bool),
+               status=st)
+    if want_stats:
+        out["row_max"] = m
+        out["row_sumexp"] = S
+    return out
+
+
+def tree_max_depth(parent) -> int:
+    p = _i32(parent)
+    return int(_load().oracle_tree_max_depth(_ptr(p), p.size))
+
+
+def tree_mask(parent):
+    """(mask [N, N] uint8, depth [N]) of the tree given by parent[]."""
+    p = _i32(parent)
+    N = p.size
+    mask = np.zeros((N, N), dtype=np.uint8)
+    depth = np.zeros(N, dtype=np.int32)
+    st = _load().oracle_tree_mask(_ptr(p), N, _ptr(mask), _ptr(depth))
+    if st != OK:
+        raise ValueError("invalid parent array")
+    return mask, depth
+
+
+def verify_tree_greedy(zt, parent, node_tokens, *, max_depth=None, nthreads=1):
+    """Greedy tree verification; returns (path [nb, D+1], length [nb], status)."""
+    zt_a, dt = _logits(zt)
+    nb, N, V = zt_a.shape
+    p = _i32(parent).reshape(N)
+    tok = _i32(node_tokens).reshape(nb, N)
+    D = tree_max_depth(p) if max_depth is None else int(max_depth)
+    if D < 0:
+        raise ValueError("invalid parent array")
+    path = np.zeros((nb, D + 1), dtype=np.int32)
+    length = np.zeros(nb, dtype=np.int32)
+    st = _load().oracle_verify_tree_greedy(_ptr(zt_a), _ptr(p), _ptr(tok), nb, N, V, dt, D,
+                                           _ptr(path), _ptr(length), int(nthreads))
+    if st in (ERR_ARG, ERR_PARENT):
+        raise ValueError("oracle_verify_tree_greedy: invalid arguments")
+    return path, length, st

@@ -1,0 +1,18 @@
+"""GB300-native verification step of speculative decoding.
+
+The compute path is the C-ABI library ``libspec_verify.so`` (hand-written CUDA
+for sm_103a); this package is its thin Python binding (argument marshalling
+only).  The library is loaded on first use; importing the package (or its
+``workloads`` input generator) does not touch CUDA.
+"""
+from __future__ import annotations
+
+__all__ = ["spec_verify", "spec_verify_ex", "spec_verify_tree_greedy", "spec_verify_host",
+           "spec_tree_mask", "spec_tree_max_depth", "spec_get_status", "SpecError", "library"]
+
+
+def __getattr__(name):
+    if name in __all__:
+        from . import binding
+        return getattr(binding, name)
+    raise AttributeError(name)
