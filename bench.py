@@ -1,0 +1,378 @@
+#!/usr/bin/env python3
+"""Benchmark of the verification step: verified draft positions per second and
+achieved HBM bandwidth on GB300, one JSON line on stdout (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c1] [--impl reference]
+
+A step is one call of the verification on one batch of the workload
+(default c1: chain, B=64, K=5, V=128256, bf16 logits, T=0.7), inputs resident
+in HBM.  Consecutive steps rotate through input copies whose total exceeds
+twice the L2, so no step finds its logits in L2.  Under torchrun each rank
+verifies its own batch (weak scaling, no collective on the data path); the
+time is the max over ranks.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (the
+reference arm): each step verifies one sequence of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import glob
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft positions/sec and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
+UNIT = "positions/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _source_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "sampling_row_online_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _profile_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    m_h = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_b or not m_h or m_h.group(1) != _source_hash():
+        return None
+    return int(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, period_ms: int = 50):
+        self.proc = None
+        self.err = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception as e:  # pragma: no cover
+            self.err = str(e)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "error": self.err}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:  # pragma: no cover
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        return parse_clock_samples(out)
+
+
+def parse_clock_samples(text: str):
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in text.strip().splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 8:
+            continue
+        try:
+            sm.append(float(parts[0]))
+            smax.append(float(parts[1]))
+        except ValueError:
+            continue
+        for nm, v in zip(names, parts[4:8]):
+            if v.lower().startswith("active"):
+                reasons.add(nm)
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, backend_device=None) -> float:
+    """Max of a float over all ranks (identity without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64,
+                     device=backend_device if backend_device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------
+# oracle timing (cpu_baseline and the reference arm)
+# ----------------------------------------------------------------------------
+def time_oracle(w, n_sequences: int, host_inputs=None, nthreads=None):
+    """Verifies n_sequences sequences of workload w with the oracle (cycling through
+    the batch, all host cores); returns (seconds, threads, description)."""
+    import numpy as np
+    import torch
+    import oracle
+    from sampling_row_online_gb300.workloads import make_chain, make_tree
+    nthreads = nthreads or max(1, os.cpu_count() or 1)
+    if host_inputs is None:
+        host_inputs = (make_tree(w, device="cpu") if w.kind == "tree"
+                       else make_chain(w, device="cpu"))
+    done = 0
+    t0 = time.perf_counter()
+    while done < n_sequences:
+        nb = min(w.B, n_sequences - done)
+        if w.kind == "tree":
+            zt, parent, tok = host_inputs
+            oracle.verify_tree_greedy(zt[:nb], parent, tok[:nb], nthreads=nthreads)
+        else:
+            zt, zd, x = host_inputs
+            oracle.verify_chain(zt[:nb], None if zd is None else zd[:nb], x[:nb], w.T,
+                                w.verify_seed, b_ids=np.arange(nb), nthreads=nthreads)
+        done += nb
+    return time.perf_counter() - t0, nthreads
+
+
+def run_reference(args, w):
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    from sampling_row_online_gb300.workloads import describe, make_chain, make_tree
+    host = make_tree(w, device="cpu") if w.kind == "tree" else make_chain(w, device="cpu")
+    per_seq_positions = (w.K - 1) if w.kind == "tree" else w.K
+    if args.warmup > 0:
+        time_oracle(w, min(args.warmup, w.B), host)
+    secs, threads = time_oracle(w, args.steps, host)
+    value = args.steps * per_seq_positions / secs
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{w.name}: {describe(w)}", "step": "one sequence of the batch"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{args.steps} sequences of {w.name} (cycling through its "
+                                   f"batch of {w.B}), fp64 oracle, {threads} OpenMP threads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def run_gpu(args, w):
+    import torch
+    import torch.distributed as dist
+    from sampling_row_online_gb300 import binding
+    from sampling_row_online_gb300.workloads import (describe, input_copies_for_cold_l2,
+                                                     make_chain, make_tree)
+    ws, rank, local = _dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    lib = binding.library()
+    stream = torch.cuda.current_stream()
+    sp = ctypes.c_void_p(stream.cuda_stream)
+
+    # inputs (rank-specific seed: each rank verifies its own batch)
+    wr = w.scaled(data_seed=w.data_seed + 7919 * rank)
+    first = make_tree(wr, device=dev) if w.kind == "tree" else make_chain(wr, device=dev)
+    per_copy = w.algorithmic_bytes
+    ncopies = input_copies_for_cold_l2(per_copy)
+    copies = [first] + [tuple(t.clone() if t.dim() >= 2 and t.numel() * t.element_size() > 1 << 20
+                              else t for t in first) for _ in range(ncopies - 1)]
+    B, V = w.B, w.V
+    dt = 0 if w.dtype == "f32" else 1
+    if w.kind == "tree":
+        D = binding.spec_tree_max_depth(first[1].cpu())
+        out_a = torch.empty((B, D + 1), dtype=torch.int32, device=dev)
+    else:
+        D = 0
+        out_a = torch.empty((B, w.K + 1), dtype=torch.int32, device=dev)
+    out_b = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def make_call(c):
+        if w.kind == "tree":
+            zt, parent, tok = c
+            a = (ctypes.c_void_p(zt.data_ptr()), ctypes.c_void_p(parent.data_ptr()),
+                 ctypes.c_void_p(tok.data_ptr()), B, w.K, V, dt, D,
+                 ctypes.c_void_p(out_a.data_ptr()), ctypes.c_void_p(out_b.data_ptr()), sp)
+            return lambda: lib.spec_verify_tree_greedy(*a)
+        zt, zd, x = c
+        a = (ctypes.c_void_p(zt.data_ptr()),
+             ctypes.c_void_p(zd.data_ptr()) if zd is not None else None,
+             ctypes.c_void_p(x.data_ptr()), B, w.K, V, dt, ctypes.c_float(w.T),
+             ctypes.c_uint64(w.verify_seed), ctypes.c_void_p(out_a.data_ptr()),
+             ctypes.c_void_p(out_b.data_ptr()), sp)
+        return lambda: lib.spec_verify(*a)
+
+    calls = [make_call(c) for c in copies]
+    for k in range(max(3, args.warmup)):
+        st = calls[k % ncopies]()
+        if st != 0:
+            raise SystemExit(f"spec call failed: {st} {lib.spec_last_error_message().decode()}")
+    torch.cuda.synchronize()
+    if lib.spec_get_status(sp) != 0:
+        raise SystemExit("device status error during warm-up")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.25 if clocks else 0)
+    wall0 = time.perf_counter()
+    t_start.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        calls[k % ncopies]()
+        ev[k][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    status = lib.spec_get_status(sp)
+    if status != 0:
+        raise SystemExit(f"device status error in the timed region: {status}")
+    region_ms = t_start.elapsed_time(t_end)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    region_ms = max_over_ranks(region_ms, dev)
+    avg_launch_ms = statistics.fmean(launch_ms)
+    positions = w.positions * args.steps * ws
+    value = positions / (region_ms / 1e3)
+
+    # end to end through the host-buffer entry point (copies in the timed region)
+    e2e = None
+    if w.kind == "chain":
+        zt, zd, x = first
+        hzt, hzd, hx = (zt.cpu().pin_memory(), None if zd is None else zd.cpu().pin_memory(),
+                        x.cpu().pin_memory())
+        hout = torch.empty((B, w.K + 1), dtype=torch.int32, pin_memory=True)
+        hn = torch.empty((B,), dtype=torch.int32, pin_memory=True)
+        e_args = (ctypes.c_void_p(hzt.data_ptr()),
+                  ctypes.c_void_p(hzd.data_ptr()) if hzd is not None else None,
+                  ctypes.c_void_p(hx.data_ptr()), B, w.K, V, dt, ctypes.c_float(w.T),
+                  ctypes.c_uint64(w.verify_seed), ctypes.c_void_p(hout.data_ptr()),
+                  ctypes.c_void_p(hn.data_ptr()), sp)
+        e_steps = max(5, min(args.steps, 30))
+        for _ in range(3):
+            lib.spec_verify_host(*e_args)
+        if ws > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e_steps):
+            st = lib.spec_verify_host(*e_args)
+            if st != 0:
+                raise SystemExit(f"spec_verify_host failed: {st}")
+        e_sec = max_over_ranks(time.perf_counter() - t0, dev)
+        h2d = hzt.numel() * hzt.element_size() + (0 if hzd is None else hzd.numel() * hzd.element_size()) \
+            + hx.numel() * 4
+        d2h = hout.numel() * 4 + hn.numel() * 4
+        e2e = {"value": w.positions * e_steps * ws / e_sec, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = _peaks()
+    kernel = "argmax_kernel" if (w.kind == "tree" or w.T == 0) else "sample_kernel"
+    achieved = w.algorithmic_bytes / (avg_launch_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                "traffic": _profile_traffic(kernel, w.name), "kernel": kernel,
+                "algorithmic_bytes_per_launch": w.algorithmic_bytes,
+                "avg_launch_us": avg_launch_ms * 1e3}
+    # CPU baseline: the oracle as it stands on the host cores, bounded sample
+    cpu = None
+    if not args.no_cpu_baseline:
+        nseq = w.B
+        secs, threads = time_oracle(w, nseq)
+        reps = 1
+        while secs * reps < 3.0 and reps < 8:
+            more, _ = time_oracle(w, nseq)
+            secs += more
+            reps += 1
+        per_seq = (w.K - 1) if w.kind == "tree" else w.K
+        cpu = {"value": nseq * reps * per_seq / secs, "unit": UNIT, "cores": threads,
+               "kind": "oracle",
+               "sample": f"{reps} pass(es) over the {nseq} sequences of {w.name}, fp64 oracle"}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {describe(w)}", "logits": w.dtype,
+                   "per_rank_batch": w.B, "parallelism": f"replicas x{ws} (sequences sharded, no collective)",
+                   "l2": f"rotating {ncopies} input copies ({ncopies * per_copy / 1e6:.0f} MB > 2x L2)"},
+        "roofline": roofline,
+        "achieved_hbm_gbs": achieved,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4"])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    from sampling_row_online_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

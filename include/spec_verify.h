@@ -1,0 +1,218 @@
+/*
+ * spec_verify.h — C ABI of the GB300 (sm_103a) verification step of
+ * speculative decoding.
+ *
+ * One library, libspec_verify.so, with hand-written CUDA kernels behind plain
+ * C entry points: pointers, sizes and a CUDA stream passed as void*.  No
+ * C++ types, no exceptions and no torch types cross this boundary.
+ *
+ * Pages this interface restates:
+ *   [Oscine]  blog.oscine.io, "投机解码：让大模型「猜」着跑的数学魔术"
+ *   [Anhtu]   anhtu.dev, "Speculative Decoding: Cách LLM Sinh Văn Bản Nhanh
+ *             Gấp 2–3 Lần"
+ *   [Infra53] infra-guide, "5.3 Medusa, EAGLE và MTP"
+ *   [Glukhov] glukhov.org, "Спекулятивное декодирование: ускорение
+ *             инференса LLM на 20–50%"
+ *
+ * Common conventions
+ *   - Logit tensors are contiguous, row-major, vocabulary innermost, either
+ *     IEEE fp32 (SPEC_F32) or bfloat16 (SPEC_BF16).  Rows are read once.
+ *   - Every tensor argument is a DEVICE pointer owned by the caller unless a
+ *     function says otherwise; the library never frees or keeps them.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, NULL = the legacy
+ *     default stream) unless stated otherwise.  Argument errors are reported
+ *     by the return value before anything is launched.  Errors found on the
+ *     device (a token id outside [0, V), a malformed tree) are recorded per
+ *     stream and returned by spec_get_status(); the affected sequence's
+ *     count output is set to -1 and its token outputs to -1.
+ *   - The fast path reads logits with TMA bulk copies and needs 16-byte
+ *     aligned logits pointers and V * element_size divisible by 16; other
+ *     layouts are accepted and take a slower path with plain loads.
+ *   - Each row must hold at least one finite logit.  -inf entries (masked
+ *     vocabulary) are allowed; NaN and +inf are not.
+ *   - The library keeps one grow-only device workspace per (device, stream)
+ *     pair (a few ints per sequence).  Growing it calls cudaMalloc, so the
+ *     first call of a new size on a stream should not be inside a CUDA graph
+ *     capture.  Two calls that overlap on the GPU must use different streams.
+ *     spec_shutdown() frees every workspace.
+ *   - Identical inputs and seed give identical outputs, bit for bit.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum {
+  SPEC_OK = 0,
+  SPEC_ERR_ARG = 1,          /* null pointer, size out of range, bad temperature */
+  SPEC_ERR_DTYPE = 2,        /* unknown dtype code */
+  SPEC_ERR_ALIGN = 3,        /* reserved: misaligned inputs take the slow path */
+  SPEC_ERR_TOKEN_RANGE = 4,  /* (device) a draft/node token outside [0, V) */
+  SPEC_ERR_CUDA = 5,         /* a CUDA runtime error; see spec_last_error_message */
+  SPEC_ERR_TIMEOUT = 6,      /* (device) a bounded wait ran out */
+  SPEC_ERR_PARENT = 7,       /* parent[] is not a tree: parent[0] != -1 or parent[c] >= c */
+  SPEC_ERR_UNSUPPORTED = 8   /* no usable GPU / cluster launch not possible */
+};
+
+/* Logit element types. */
+enum { SPEC_F32 = 0, SPEC_BF16 = 1 };
+
+/* Size limits. */
+#define SPEC_MAX_DRAFTS 255      /* K of a chain */
+#define SPEC_MAX_TREE_NODES 1024 /* N of a tree */
+
+/* Counters a caller may ask spec_verify_ex to accumulate (device memory,
+ * zeroed by the caller, added to atomically by every call that receives it).
+ * They mirror the acceptance monitoring the pages recommend ([Glukhov]
+ * §"Мониторинг в производстве": acceptance rate per request). */
+typedef struct {
+  unsigned long long sequences;          /* sequences verified without error */
+  unsigned long long accepted;           /* sum of n_accepted */
+  unsigned long long bonus;              /* sequences that accepted all K and drew a bonus */
+  unsigned long long resampled;          /* sequences that stopped at a reject */
+  unsigned long long residual_fallbacks; /* rejects whose residual mass was 0 in fp32 */
+  unsigned long long errors;             /* sequences with an out-of-range token */
+} spec_stats_t;
+
+/*
+ * spec_verify — chain verification of B sequences with K drafts each.
+ *
+ * For temperature T > 0 ([Oscine] §"验收标准的精确数学", eq. α(x);
+ * §"拒绝之后怎么办？——残差分布", eq. p_resid; §"多 Token 验证：左到右，遇错即停"):
+ *   p_i = softmax(target_logits[b, i, :] / T), i = 0..K,
+ *   q_i = softmax(draft_logits[b, i, :] / T),  i = 0..K-1;
+ *   draft x_i = draft_tokens[b, i] is accepted iff u_i < p_i(x_i) / q_i(x_i),
+ *   scanning i = 0, 1, ... and stopping at the first reject j; the token at j
+ *   is then drawn from norm(max(0, p_j - q_j)); if all K are accepted a bonus
+ *   token is drawn from p_K ([Anhtu] §"Toán học của sự miễn phí").
+ * For T == 0 the rule is greedy matching ([Infra53] §9.1): x_i is kept iff it
+ * equals argmax p_i (lowest index on ties); the first mismatch emits
+ * argmax p_j, a full match emits argmax p_K.  draft_logits is not read.
+ *
+ * Uniforms: u = (w >> 8) * 2^-24, w = word 0 of Philox4x32-10 with key
+ * (seed mod 2^32, seed >> 32) and counter (b, position, slot, 0); slot 0 is
+ * the acceptance test at position i, slot 1 the residual draw at position j
+ * or the bonus draw at position K.  Draws invert the CDF in vocabulary order
+ * (smallest v with C(v) > u * Z).
+ *
+ * Arguments
+ *   target_logits   [B, K+1, V], dtype
+ *   draft_logits    [B, K, V], dtype; may be NULL iff T == 0 or K == 0
+ *   draft_tokens    [B, K] int32; may be NULL iff K == 0
+ *   B >= 0 (B == 0 is a no-op), 0 <= K <= SPEC_MAX_DRAFTS, V >= 1
+ *   dtype           SPEC_F32 or SPEC_BF16
+ *   temperature     T >= 0, finite
+ *   seed            64-bit Philox key
+ *   out_tokens      [B, K+1] int32: accepted drafts, then the new token,
+ *                   then -1 padding
+ *   out_n_accepted  [B] int32: number of accepted drafts n (0..K), -1 on a
+ *                   device-detected error in that sequence
+ *   stream          cudaStream_t as void*
+ * Returns SPEC_OK or an error code (nothing is launched on an error).
+ */
+int spec_verify(const void *target_logits, const void *draft_logits,
+                const int32_t *draft_tokens, int B, int K, int V, int dtype,
+                float temperature, uint64_t seed, int32_t *out_tokens,
+                int32_t *out_n_accepted, void *stream);
+
+/*
+ * spec_verify_ex — spec_verify plus optional observability outputs.
+ *   out_row_max     [B, 2K+1] float or NULL: max logit of each row
+ *   out_row_sumexp  [B, 2K+1] float or NULL: S = sum_v exp((z_v - max)/T)
+ *                   (NaN when T == 0).  Row order: target rows 0..K, then
+ *                   draft rows 0..K-1 (draft rows are NaN when T == 0).
+ *   stats           spec_stats_t* in device memory or NULL (accumulated)
+ */
+int spec_verify_ex(const void *target_logits, const void *draft_logits,
+                   const int32_t *draft_tokens, int B, int K, int V, int dtype,
+                   float temperature, uint64_t seed, int32_t *out_tokens,
+                   int32_t *out_n_accepted, float *out_row_max,
+                   float *out_row_sumexp, spec_stats_t *stats, void *stream);
+
+/*
+ * spec_verify_host — spec_verify on HOST buffers, end to end and synchronous:
+ * copies the inputs to a library-owned device staging area (grow-only, per
+ * device and stream), verifies, copies the outputs back and waits.  Page-
+ * locked host buffers give the fastest copies.  Returns SPEC_OK, an argument
+ * error, or the device status of this call (as spec_get_status).
+ */
+int spec_verify_host(const void *target_logits, const void *draft_logits,
+                     const int32_t *draft_tokens, int B, int K, int V, int dtype,
+                     float temperature, uint64_t seed, int32_t *out_tokens,
+                     int32_t *out_n_accepted, void *stream);
+
+/*
+ * spec_verify_tree_greedy — greedy verification of a draft tree
+ * ([Infra53] §3: every node sees only its ancestors, one path is
+ * committed; [Anhtu] §"Token tree": the deepest accepted branch is the
+ * output).  Row n of target_logits is the target's distribution after node
+ * n.  Node c >= 1 is accepted iff its parent is accepted and
+ * node_tokens[b, c] == argmax(target_logits[b, parent[c], :]) (lowest index
+ * on ties); node 0 (the root, already committed) is always accepted.  The
+ * deepest accepted node d* (lowest index among equals) is committed.
+ *
+ *   target_logits  [B, N, V], dtype
+ *   parent         [N] int32 (device): parent[0] = -1, 0 <= parent[c] < c
+ *   node_tokens    [B, N] int32; entry 0 is ignored
+ *   B >= 0, 1 <= N <= SPEC_MAX_TREE_NODES, V >= 1
+ *   max_depth      D = spec_tree_max_depth(parent) (from a host copy)
+ *   out_path       [B, D+1] int32: tokens of the committed path (root
+ *                  excluded), then the bonus argmax(row d*), then -1 padding
+ *   out_len        [B] int32: depth(d*) + 1, or -1 on a device error
+ * A parent[] that is not a tree, or deeper than max_depth, is reported as
+ * SPEC_ERR_PARENT by spec_get_status and sets every out_len to -1.
+ */
+int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent,
+                            const int32_t *node_tokens, int B, int N, int V,
+                            int dtype, int max_depth, int32_t *out_path,
+                            int32_t *out_len, void *stream);
+
+/*
+ * spec_tree_max_depth — HOST helper: the largest node depth of parent[]
+ * (HOST pointer), or -SPEC_ERR_PARENT if parent[] is not a tree
+ * ([Infra53] §3.2: position IDs follow tree depth).
+ */
+int spec_tree_max_depth(const int32_t *parent_host, int N);
+
+/*
+ * spec_tree_mask — tree-attention mask and depth position IDs of B trees
+ * ([Infra53] §3.1–§3.2 and the example of §8: node n sees exactly its
+ * ancestors and itself; its position ID is its depth).
+ *   parent     [B, N] int32 (device), each row a tree as above
+ *   out_mask   [B, N, W] uint32 with W = ceil(N / 32): bit (a mod 32) of
+ *              word a / 32 of row n is set iff a is an ancestor-or-self of n
+ *   out_depth  [B, N] int32
+ * A malformed tree is reported by spec_get_status (SPEC_ERR_PARENT) and its
+ * rows are zeroed with depth -1.
+ */
+int spec_tree_mask(const int32_t *parent, int B, int N, uint32_t *out_mask,
+                   int32_t *out_depth, void *stream);
+
+/*
+ * spec_get_status — waits for `stream`, then returns (and clears) the first
+ * device-side error recorded by calls on it: SPEC_OK, SPEC_ERR_TOKEN_RANGE,
+ * SPEC_ERR_PARENT, SPEC_ERR_TIMEOUT, or SPEC_ERR_CUDA for an asynchronous
+ * CUDA error.
+ */
+int spec_get_status(void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *spec_error_string(int status);
+
+/* Detail of the last error returned on the calling host thread. */
+const char *spec_last_error_message(void);
+
+/* Frees every workspace and staging buffer the library holds.  No call may
+ * be in flight. */
+void spec_shutdown(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,249 @@
+"""Thin ctypes binding of libspec_verify.so (argument marshalling only).
+
+Every step of the verification runs in the library's CUDA kernels; this module
+checks tensor shapes, dtypes and devices, passes raw device pointers and the
+current CUDA stream, and raises ``SpecError`` on a non-zero status.  There is
+no fallback: if the library is missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+SPEC_OK = 0
+SPEC_F32, SPEC_BF16 = 0, 1
+STATUS_NAMES = {
+    0: "SPEC_OK", 1: "SPEC_ERR_ARG", 2: "SPEC_ERR_DTYPE", 3: "SPEC_ERR_ALIGN",
+    4: "SPEC_ERR_TOKEN_RANGE", 5: "SPEC_ERR_CUDA", 6: "SPEC_ERR_TIMEOUT",
+    7: "SPEC_ERR_PARENT", 8: "SPEC_ERR_UNSUPPORTED",
+}
+
+_lib = None
+
+
+class SpecError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        name = STATUS_NAMES.get(abs(status), f"status {status}")
+        super().__init__(f"{where}: {name}" + (f" ({detail})" if detail else ""))
+
+
+class StatsStruct(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_ulonglong) for n in
+                ("sequences", "accepted", "bonus", "resampled", "residual_fallbacks", "errors")]
+
+
+def library():
+    """Loads libspec_verify.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        path = _build.build()
+    lib = ctypes.CDLL(path)
+    vp, i32, u64, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_float
+    lib.spec_verify.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, u64, vp, vp, vp]
+    lib.spec_verify_ex.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, u64, vp, vp, vp, vp, vp, vp]
+    lib.spec_verify_host.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, u64, vp, vp, vp]
+    lib.spec_verify_tree_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.spec_tree_max_depth.argtypes = [vp, i32]
+    lib.spec_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp]
+    lib.spec_get_status.argtypes = [vp]
+    lib.spec_error_string.argtypes = [i32]
+    lib.spec_error_string.restype = ctypes.c_char_p
+    lib.spec_last_error_message.argtypes = []
+    lib.spec_last_error_message.restype = ctypes.c_char_p
+    lib.spec_shutdown.argtypes = []
+    lib.spec_shutdown.restype = None
+    for name in ("spec_verify", "spec_verify_ex", "spec_verify_host", "spec_verify_tree_greedy",
+                 "spec_tree_max_depth", "spec_tree_mask", "spec_get_status"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(status: int, where: str):
+    if status != SPEC_OK:
+        detail = library().spec_last_error_message().decode(errors="replace")
+        raise SpecError(status, where, detail)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _dev(t, name, dtype=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _chain_shapes(target_logits, draft_logits, draft_tokens):
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, K+1, V]")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    if draft_tokens is not None and tuple(draft_tokens.shape) != (B, K):
+        raise ValueError(f"draft_tokens must be [B, K] = [{B}, {K}]")
+    if draft_logits is not None and K > 0:
+        if tuple(draft_logits.shape) != (B, K, V) or draft_logits.dtype != target_logits.dtype:
+            raise ValueError(f"draft_logits must be [B, K, V] = [{B}, {K}, {V}] of the target dtype")
+    return B, K, V
+
+
+def spec_verify(target_logits, draft_logits, draft_tokens, temperature, seed, *,
+                out_tokens=None, out_n_accepted=None, stream=None):
+    """Chain verification; returns (out_tokens [B, K+1] int32, n_accepted [B] int32)."""
+    return spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature, seed,
+                          out_tokens=out_tokens, out_n_accepted=out_n_accepted,
+                          stream=stream)[:2]
+
+
+def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature, seed, *,
+                   out_tokens=None, out_n_accepted=None, want_row_stats=False, stats=None,
+                   stream=None):
+    """Chain verification with optional per-row (max, sumexp) [B, 2K+1] outputs and a
+    device ``stats`` tensor (6 int64 counters, accumulated).  Returns
+    (out_tokens, n_accepted, row_max or None, row_sumexp or None)."""
+    lib = library()
+    _dev(target_logits, "target_logits")
+    B, K, V = _chain_shapes(target_logits, draft_logits, draft_tokens)
+    _dev(draft_logits, "draft_logits")
+    _dev(draft_tokens, "draft_tokens", torch.int32)
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if out_n_accepted is None:
+        out_n_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _dev(out_tokens, "out_tokens", torch.int32)
+    _dev(out_n_accepted, "out_n_accepted", torch.int32)
+    row_max = row_sumexp = None
+    if want_row_stats:
+        row_max = torch.empty((B, 2 * K + 1), dtype=torch.float32, device=dev)
+        row_sumexp = torch.empty((B, 2 * K + 1), dtype=torch.float32, device=dev)
+    if stats is not None:
+        _dev(stats, "stats", torch.int64)
+        if stats.numel() != 6:
+            raise ValueError("stats must hold 6 int64 counters")
+    with torch.cuda.device(dev):
+        st = lib.spec_verify_ex(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens),
+                                B, K, V, _dtype_code(target_logits), float(temperature),
+                                int(seed) & (2 ** 64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
+                                _ptr(row_max), _ptr(row_sumexp), _ptr(stats), _stream(stream))
+    _check(st, "spec_verify")
+    return out_tokens, out_n_accepted, row_max, row_sumexp
+
+
+def spec_verify_host(target_logits, draft_logits, draft_tokens, temperature, seed, *,
+                     out_tokens=None, out_n_accepted=None, device=None, stream=None):
+    """End-to-end chain verification on HOST (CPU) tensors: the library copies the
+    inputs to the GPU, verifies, copies the outputs back and waits.  Pinned host
+    tensors give the fastest copies.  Returns (out_tokens, n_accepted) on the host."""
+    lib = library()
+    for t, name in ((target_logits, "target_logits"), (draft_logits, "draft_logits"),
+                    (draft_tokens, "draft_tokens")):
+        if t is not None and (t.device.type != "cpu" or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    B, K, V = _chain_shapes(target_logits, draft_logits, draft_tokens)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, pin_memory=True)
+    if out_n_accepted is None:
+        out_n_accepted = torch.empty((B,), dtype=torch.int32, pin_memory=True)
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(device):
+        st = lib.spec_verify_host(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens),
+                                  B, K, V, _dtype_code(target_logits), float(temperature),
+                                  int(seed) & (2 ** 64 - 1), _ptr(out_tokens),
+                                  _ptr(out_n_accepted), _stream(stream))
+    _check(st, "spec_verify_host")
+    return out_tokens, out_n_accepted
+
+
+def spec_tree_max_depth(parent) -> int:
+    """Largest node depth of parent[] (host data)."""
+    p = torch.as_tensor(parent, dtype=torch.int32).contiguous().cpu()
+    d = library().spec_tree_max_depth(_ptr(p), p.numel())
+    if d < 0:
+        _check(-d, "spec_tree_max_depth")
+    return d
+
+
+def spec_verify_tree_greedy(target_logits, parent, node_tokens, *, max_depth=None,
+                            out_path=None, out_len=None, stream=None):
+    """Greedy tree verification; returns (out_path [B, D+1] int32, out_len [B] int32)."""
+    lib = library()
+    _dev(target_logits, "target_logits")
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, N, V]")
+    B, N, V = target_logits.shape
+    _dev(parent, "parent", torch.int32)
+    _dev(node_tokens, "node_tokens", torch.int32)
+    if parent.numel() != N or tuple(node_tokens.shape) != (B, N):
+        raise ValueError("parent must be [N] and node_tokens [B, N]")
+    if max_depth is None:
+        max_depth = spec_tree_max_depth(parent.cpu())
+    dev = target_logits.device
+    if out_path is None:
+        out_path = torch.empty((B, max_depth + 1), dtype=torch.int32, device=dev)
+    if out_len is None:
+        out_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.spec_verify_tree_greedy(_ptr(target_logits), _ptr(parent), _ptr(node_tokens),
+                                         B, N, V, _dtype_code(target_logits), int(max_depth),
+                                         _ptr(out_path), _ptr(out_len), _stream(stream))
+    _check(st, "spec_verify_tree_greedy")
+    return out_path, out_len
+
+
+def spec_tree_mask(parent, *, stream=None):
+    """Tree-attention masks and depth position IDs of B trees.
+
+    parent: [B, N] int32 CUDA tensor.  Returns (mask [B, N, ceil(N/32)] int32 bit
+    words, depth [B, N] int32)."""
+    lib = library()
+    _dev(parent, "parent", torch.int32)
+    if parent.dim() == 1:
+        parent = parent.unsqueeze(0)
+    B, N = parent.shape
+    W = (N + 31) // 32
+    mask = torch.empty((B, N, W), dtype=torch.int32, device=parent.device)
+    depth = torch.empty((B, N), dtype=torch.int32, device=parent.device)
+    with torch.cuda.device(parent.device):
+        st = lib.spec_tree_mask(_ptr(parent), B, N, _ptr(mask), _ptr(depth), _stream(stream))
+    _check(st, "spec_tree_mask")
+    return mask, depth
+
+
+def spec_get_status(stream=None) -> int:
+    """Waits for the stream; returns (and clears) the device-side status code."""
+    return int(library().spec_get_status(_stream(stream)))
+
+
+def raise_on_device_error(stream=None):
+    st = spec_get_status(stream)
+    _check(st, "device")

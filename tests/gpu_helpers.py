@@ -1,0 +1,65 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI
+and the fp64 oracle on the same input bytes, and compare under the parity rule.
+
+Parity rule (stochastic chain): out_n_accepted and every emitted token equal
+the oracle's, except for sequences the oracle flags as near a decision
+boundary (|u - r| <= 1e-5 max(r, 2^-24) at an acceptance test, or t within
+1e-5 Z of a CDF boundary of the draw).  Flagged sequences are counted; the
+count must stay below 1e-4 of the verified positions (a test with fewer than
+10^4 positions tolerates one).  Greedy and tree results are bit-exact.
+Normalisers: the row max exactly, the sum of exponentials to 1e-5 relative.
+"""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+
+import oracle
+from sampling_row_online_gb300 import binding
+
+NTHREADS = max(1, os.cpu_count() or 1)
+S_RTOL = 1e-5
+
+
+def gpu_chain(zt, zd, x, T, seed, want_row_stats=True, stats=None):
+    out, n, rmax, rsum = binding.spec_verify_ex(zt, zd, x, T, seed, want_row_stats=want_row_stats,
+                                                stats=stats)
+    torch.cuda.synchronize()
+    return (out.cpu().numpy(), n.cpu().numpy(),
+            None if rmax is None else rmax.cpu().numpy(),
+            None if rsum is None else rsum.cpu().numpy())
+
+
+def oracle_chain(zt, zd, x, T, seed, b_ids=None, want_stats=True):
+    return oracle.verify_chain(zt.cpu(), None if zd is None else zd.cpu(), x.cpu(), T, seed,
+                               b_ids=b_ids, want_stats=want_stats, nthreads=NTHREADS)
+
+
+def compare_chain(gpu_tokens, gpu_n, ref, positions, rows=None):
+    """Asserts the parity rule; returns the number of excluded (near) sequences."""
+    near = ref["near"]
+    sel = np.arange(len(gpu_n)) if rows is None else np.asarray(rows)
+    g_tok, g_n = gpu_tokens[sel], gpu_n[sel]
+    ok = (g_n == ref["n_accepted"]) & np.all(g_tok == ref["tokens"], axis=1)
+    bad = np.where(~ok & ~near)[0]
+    assert bad.size == 0, (
+        f"{bad.size} sequences differ from the oracle away from any boundary; first: "
+        f"b={sel[bad[0]]} gpu n={g_n[bad[0]]} tokens={g_tok[bad[0]].tolist()} "
+        f"oracle n={ref['n_accepted'][bad[0]]} tokens={ref['tokens'][bad[0]].tolist()}")
+    n_near = int(near.sum())
+    assert n_near <= max(1, 1e-4 * positions), f"{n_near} near-boundary sequences of {positions}"
+    return n_near
+
+
+def compare_row_stats(g_max, g_sum, ref, T, rows=None):
+    sel = slice(None) if rows is None else np.asarray(rows)
+    o_max, o_sum = ref["row_max"], ref["row_sumexp"]
+    gm, gs = g_max[sel], g_sum[sel]
+    fin = np.isfinite(o_max)
+    assert np.array_equal(np.isnan(gm), np.isnan(o_max))
+    assert np.all(gm[fin] == o_max[fin].astype(np.float32)), "row max must be exact"
+    if T > 0:
+        rel = np.abs(gs[fin].astype(np.float64) - o_sum[fin]) / o_sum[fin]
+        assert rel.max() <= S_RTOL, f"sumexp relative error {rel.max():.3e}"

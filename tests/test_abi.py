@@ -1,0 +1,98 @@
+"""The C-ABI library loads, exports every symbol its header declares, and
+rejects bad arguments on the host before touching CUDA (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "spec_verify.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(spec_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sampling_row_online_gb300 import build, binding
+    build.build()
+    return binding.library()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("spec_verify", "spec_verify_tree_greedy", "spec_verify_ex", "spec_verify_host",
+                     "spec_tree_max_depth", "spec_tree_mask", "spec_get_status",
+                     "spec_error_string", "spec_last_error_message", "spec_shutdown"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def _verify(lib, **kw):
+    a = dict(zt=ctypes.c_void_p(16), zd=ctypes.c_void_p(16), x=ctypes.c_void_p(16), B=2, K=3,
+             V=100, dtype=1, T=1.0, seed=0, out=ctypes.c_void_p(16), n=ctypes.c_void_p(16),
+             stream=None)
+    a.update(kw)
+    return lib.spec_verify(a["zt"], a["zd"], a["x"], a["B"], a["K"], a["V"], a["dtype"], a["T"],
+                           a["seed"], a["out"], a["n"], a["stream"])
+
+
+def test_argument_validation_without_gpu(lib):
+    ARG, DTYPE = 1, 2
+    assert _verify(lib, B=0) == 0                       # empty batch: no-op
+    assert _verify(lib, B=-1) == ARG
+    assert _verify(lib, V=0) == ARG
+    assert _verify(lib, K=-1) == ARG
+    assert _verify(lib, K=256) == ARG
+    assert _verify(lib, dtype=7) == DTYPE
+    assert _verify(lib, T=-0.5) == ARG
+    assert _verify(lib, T=float("nan")) == ARG
+    assert _verify(lib, T=float("inf")) == ARG
+    assert _verify(lib, T=1e-40) == ARG                  # 1/T overflows fp32
+    assert _verify(lib, zt=None) == ARG
+    assert _verify(lib, zd=None) == ARG                  # T > 0 needs draft logits
+    assert _verify(lib, x=None) == ARG
+    assert _verify(lib, out=None) == ARG
+    assert _verify(lib, n=None) == ARG
+    msg = lib.spec_last_error_message().decode()
+    assert "NULL" in msg
+    assert lib.spec_error_string(ARG) == b"SPEC_ERR_ARG"
+    assert lib.spec_error_string(0) == b"SPEC_OK"
+
+
+def test_tree_validation_without_gpu(lib):
+    vp = ctypes.c_void_p(16)
+    assert lib.spec_verify_tree_greedy(vp, vp, vp, 2, 0, 10, 1, 0, vp, vp, None) == 1     # N = 0
+    assert lib.spec_verify_tree_greedy(vp, vp, vp, 2, 5, 10, 1, 5, vp, vp, None) == 1     # depth >= N
+    assert lib.spec_verify_tree_greedy(vp, vp, vp, 0, 5, 10, 1, 2, vp, vp, None) == 0     # empty
+    assert lib.spec_tree_mask(vp, 1, 0, vp, vp, None) == 1
+
+
+@pytest.mark.parametrize("parent,depth", [([-1], 0), ([-1, 0, 0, 1, 2], 2),
+                                          ([-1, 0, 1, 2, 3], 4), ([-1, 0, 0, 0], 1)])
+def test_tree_max_depth_host(lib, parent, depth):
+    p = np.array(parent, dtype=np.int32)
+    assert lib.spec_tree_max_depth(p.ctypes.data_as(ctypes.c_void_p), p.size) == depth
+
+
+@pytest.mark.parametrize("parent", [[0], [-1, 1], [-1, 0, 3], [-1, -1]])
+def test_tree_max_depth_rejects_non_trees(lib, parent):
+    p = np.array(parent, dtype=np.int32)
+    assert lib.spec_tree_max_depth(p.ctypes.data_as(ctypes.c_void_p), p.size) == -7
+
+
+def test_binding_matches_oracle_tree_depth(lib):
+    import oracle
+    from sampling_row_online_gb300 import binding
+    from sampling_row_online_gb300.workloads import tree_parents
+    parent = tree_parents((4, 3, 2, 2, 1), 63)
+    assert binding.spec_tree_max_depth(parent) == oracle.tree_max_depth(parent) == 4
