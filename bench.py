@@ -282,7 +282,7 @@ def run_gpu(args, w):
 
     # end to end through the host-buffer entry point (copies in the timed region)
     e2e = None
-    if w.kind == "chain":
+    if w.kind == "chain" and not args.no_e2e:
         zt, zd, x = first
         hzt, hzd, hx = (zt.cpu().pin_memory(), None if zd is None else zd.cpu().pin_memory(),
                         x.cpu().pin_memory())
@@ -366,6 +366,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
     from sampling_row_online_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]

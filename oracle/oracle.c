@@ -367,9 +367,10 @@ int oracle_verify_chain(const void *zt, const void *zd, const int32_t *x,
     if (out_m || out_S) {
       int R = 2 * K + 1;
       for (int r = 0; r < R; ++r) {
+        /* draft rows are not part of greedy matching: NaN when T == 0 */
         const void *row = r <= K ? row_ptr(zt_seq, dtype, r, V)
-                                 : (zd_seq ? row_ptr(zd_seq, dtype, r - K - 1, V)
-                                           : NULL);
+                                 : (zd_seq && T > 0.0 ? row_ptr(zd_seq, dtype, r - K - 1, V)
+                                                      : NULL);
         double m = NAN, S = NAN;
         if (row) {
           if (T > 0.0) {

@@ -4,10 +4,12 @@ and the fp64 oracle on the same input bytes, and compare under the parity rule.
 Parity rule (stochastic chain): out_n_accepted and every emitted token equal
 the oracle's, except for sequences the oracle flags as near a decision
 boundary (|u - r| <= 1e-5 max(r, 2^-24) at an acceptance test, or t within
-1e-5 Z of a CDF boundary of the draw).  Flagged sequences are counted; the
-count must stay below 1e-4 of the verified positions (a test with fewer than
-10^4 positions tolerates one).  Greedy and tree results are bit-exact.
-Normalisers: the row max exactly, the sum of exponentials to 1e-5 relative.
+1e-5 Z of a CDF boundary of the draw).  A flagged sequence may differ; such
+excused differences are counted and must stay below 1e-4 of the verified
+positions (a test with fewer than 10^4 positions tolerates one).  Flags
+without a difference are only reported.  Greedy and tree results are
+bit-exact.  Normalisers: the row max exactly, the sum of exponentials to 1e-5
+relative.
 """
 from __future__ import annotations
 
@@ -38,7 +40,7 @@ def oracle_chain(zt, zd, x, T, seed, b_ids=None, want_stats=True):
 
 
 def compare_chain(gpu_tokens, gpu_n, ref, positions, rows=None):
-    """Asserts the parity rule; returns the number of excluded (near) sequences."""
+    """Asserts the parity rule; returns (excused differences, near-flagged sequences)."""
     near = ref["near"]
     sel = np.arange(len(gpu_n)) if rows is None else np.asarray(rows)
     g_tok, g_n = gpu_tokens[sel], gpu_n[sel]
@@ -48,9 +50,10 @@ def compare_chain(gpu_tokens, gpu_n, ref, positions, rows=None):
         f"{bad.size} sequences differ from the oracle away from any boundary; first: "
         f"b={sel[bad[0]]} gpu n={g_n[bad[0]]} tokens={g_tok[bad[0]].tolist()} "
         f"oracle n={ref['n_accepted'][bad[0]]} tokens={ref['tokens'][bad[0]].tolist()}")
-    n_near = int(near.sum())
-    assert n_near <= max(1, 1e-4 * positions), f"{n_near} near-boundary sequences of {positions}"
-    return n_near
+    n_excused = int((~ok & near).sum())
+    assert n_excused <= max(1, 1e-4 * positions), (
+        f"{n_excused} near-boundary differences in {positions} positions")
+    return n_excused, int(near.sum())
 
 
 def compare_row_stats(g_max, g_sum, ref, T, rows=None):
