@@ -62,8 +62,10 @@ struct Params {
   uint64_t seed;
   int slice;                // vocabulary elements per CTA (multiple of the vector width)
   int tile;                 // elements per tile and row
-  int stages;               // shared-memory stages
-  int resident;             // 1: every tile of a slice stays in shared memory
+  int stages;               // shared-memory stages of the tile ring
+  int ncl;                  // clusters launched (persistent)
+  int njobs;                // jobs in total
+  int emit_off;             // byte offset of the emission scratch in dynamic smem
   int max_depth;            // tree output width - 1
   int32_t *out_tokens;      // chain [B, K+1]; tree [B, max_depth+1]
   int32_t *out_n;           // chain n_accepted [B]; tree length [B]
@@ -233,63 +235,114 @@ __device__ __forceinline__ int block_reduce_max_int(int v, int *sh) {
   return r;
 }
 
-// Exclusive prefix sum over the threads of the block, in thread order.
-__device__ __forceinline__ float block_exclusive_scan(float v, float *sh) {
+// Exclusive prefix sum over the threads of the block, in thread order; the
+// block total is returned in *total (every thread).  sh: NWARP + 1 floats.
+__device__ __forceinline__ float block_exclusive_scan(float v, float *sh, float *total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float inc = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
     const float n = __shfl_up_sync(0xFFFFFFFFu, inc, off);
-    if (lane >= off) inc += n;
+    if (lane >= off) inc = __fadd_rn(inc, n);
   }
   if (lane == 31) sh[warp] = inc;
   __syncthreads();
   float base = 0.f;
-  for (int w = 0; w < warp; ++w) base += sh[w];
+  for (int w = 0; w < warp; ++w) base = __fadd_rn(base, sh[w]);
+  const float excl = __fadd_rn(base, __fsub_rn(inc, v));
+  if (threadIdx.x == NT - 1) sh[NWARP] = __fadd_rn(excl, v);
   __syncthreads();
-  return base + inc - v;
+  *total = sh[NWARP];
+  __syncthreads();
+  return excl;
 }
 
-// -------------------------------------------------------- tile pipeline
-// Streams the tiles of one CTA's vocabulary slice (1 or 2 rows) through a
-// ring of shared-memory stages.  TMA path: thread 0 issues one bulk copy per
-// row and tile, completion is tracked by one mbarrier per stage.  Plain path
-// (rows not 16-byte aligned): all threads copy element by element and pad
-// the last vector with -inf.
+// -------------------------------------------------------- job stream
+// The kernels are persistent: cluster `cl` handles jobs q = cl, cl + ncl,
+// cl + 2 ncl, ...  Every CTA of the cluster streams the tiles of its
+// vocabulary slice of those jobs, in order, through a ring of S shared-memory
+// stages, so the copies of the next job are in flight while the current job
+// is combined and decided.  TMA path: thread 0 issues one bulk copy per row
+// and tile, one mbarrier per stage tracks completion.  Plain path (rows not
+// 16-byte aligned): all threads copy element by element and pad the last
+// vector with -inf.
+
+// Job q -> (sequence b, row i).  Stochastic chain: the K row pairs in
+// position-major order (so earlier positions of a sequence tend to be decided
+// first), then the K+1-th target rows.  Argmax kinds: rows position-major.
+__device__ __forceinline__ void decode_job(const Params &p, int q, int &b, int &i) {
+  if (p.kind == KIND_SAMPLE) {
+    const int npair = p.B * p.K;
+    if (q < npair) {
+      i = q / p.B;
+      b = q - i * p.B;
+    } else {
+      i = p.K;
+      b = q - npair;
+    }
+  } else {
+    i = q / p.B;
+    b = q - i * p.B;
+  }
+}
+
 template <int DT, bool TMA>
-struct Pipe {
+struct Stream {
   using E = Elem<DT>;
+  const Params *p;
   unsigned char *buf;
   uint64_t *full;
-  const unsigned char *src[2];  // row bytes at the slice start
-  int nrows, stages, tile, len, ntile;
-  uint32_t parity;
+  int cl, lo, len, nt, S, srows;
   bool timed_out;
 
-  __device__ __forceinline__ int tile_len(int k) const { return min(tile, len - k * tile); }
+  __device__ __forceinline__ int tile_len(int k) const { return min(p->tile, len - k * p->tile); }
   __device__ __forceinline__ unsigned char *stage_row(int s, int r) const {
-    return buf + static_cast<size_t>(s * nrows + r) * tile * E::BYTES;
+    return buf + static_cast<size_t>(s * srows + r) * p->tile * E::BYTES;
+  }
+  // target and (for a pair) draft row of job q; returns the row count
+  __device__ __forceinline__ int rows_of(int q, const unsigned char *&rt,
+                                         const unsigned char *&rd) const {
+    int b, i;
+    decode_job(*p, q, b, i);
+    rt = static_cast<const unsigned char *>(p->zt) +
+         (static_cast<size_t>(b) * p->J + i) * p->V * E::BYTES;
+    if (p->kind == KIND_SAMPLE && i < p->K) {
+      rd = static_cast<const unsigned char *>(p->zd) +
+           (static_cast<size_t>(b) * p->K + i) * p->V * E::BYTES;
+      return 2;
+    }
+    rd = nullptr;
+    return 1;
   }
 
-  // TMA only, thread 0 only.
-  __device__ __forceinline__ void issue(int k, int s) {
+  // TMA, thread 0: issue tile `seq` of this CTA's stream, if it exists.
+  __device__ __forceinline__ void produce(int seq) {
+    if (nt == 0) return;
+    const int n = seq / nt, k = seq - n * nt;
+    const int q = cl + n * p->ncl;
+    if (q >= p->njobs) return;
+    const unsigned char *rt, *rd;
+    const int nr = rows_of(q, rt, rd);
+    const int s = seq % S;
     const uint32_t bytes = static_cast<uint32_t>(tile_len(k)) * E::BYTES;
-    mbar_arrive_expect_tx(&full[s], bytes * nrows);
-    for (int r = 0; r < nrows; ++r)
-      bulk_g2s(stage_row(s, r), src[r] + static_cast<size_t>(k) * tile * E::BYTES, bytes, &full[s]);
+    const size_t off = (static_cast<size_t>(lo) + static_cast<size_t>(k) * p->tile) * E::BYTES;
+    mbar_arrive_expect_tx(&full[s], bytes * nr);
+    bulk_g2s(stage_row(s, 0), rt + off, bytes, &full[s]);
+    if (nr == 2) bulk_g2s(stage_row(s, 1), rd + off, bytes, &full[s]);
   }
 
   __device__ __forceinline__ void prologue() {
-    if (TMA && threadIdx.x == 0) {
-      const int n = min(stages, ntile);
-      for (int k = 0; k < n; ++k) issue(k, k);
-    }
+    if (TMA && threadIdx.x == 0)
+      for (int s = 0; s < S; ++s) produce(s);
   }
 
-  // Makes tile k available in stage s (called by every thread).
-  __device__ __forceinline__ void acquire(int k, int s) {
+  // Every thread: tile `seq` (tile k of the current job, rows rt/rd) is in
+  // stage seq % S on return.
+  __device__ __forceinline__ void acquire(int seq, int k, const unsigned char *rt,
+                                          const unsigned char *rd) {
+    const int s = seq % S;
     if (TMA) {
-      const uint32_t par = (parity >> s) & 1u;
+      const uint32_t par = static_cast<uint32_t>(seq / S) & 1u;
       if (!mbar_try_wait(&full[s], par)) {
         const uint64_t t0 = clock_ns();
         while (!mbar_try_wait(&full[s], par)) {
@@ -299,13 +352,13 @@ struct Pipe {
           }
         }
       }
-      parity ^= 1u << s;
     } else {
       __syncthreads();
       const int n = tile_len(k);
       const int npad = (n + E::VE - 1) / E::VE * E::VE;
-      for (int r = 0; r < nrows; ++r) {
-        const unsigned char *g = src[r] + static_cast<size_t>(k) * tile * E::BYTES;
+      const size_t off = (static_cast<size_t>(lo) + static_cast<size_t>(k) * p->tile) * E::BYTES;
+      for (int r = 0; r < (rd ? 2 : 1); ++r) {
+        const unsigned char *g = (r ? rd : rt) + off;
         unsigned char *d = stage_row(s, r);
         for (int e = threadIdx.x; e < npad; e += NT) {
           if (e < n)
@@ -318,20 +371,21 @@ struct Pipe {
     }
   }
 
-  // After consuming tile k from stage s: refill the stage with tile k + stages.
-  __device__ __forceinline__ void release(int k, int s) {
-    if (TMA && k + stages < ntile) {
+  // After every thread consumed tile `seq`: refill its stage with tile seq + S.
+  __device__ __forceinline__ void release(int seq) {
+    if (TMA) {
       __syncthreads();
-      if (threadIdx.x == 0) issue(k + stages, s);
+      if (threadIdx.x == 0) produce(seq + S);
     }
   }
 
   // Bounded drain of copies that may still be in flight after a timeout.
-  __device__ __forceinline__ void drain_after_timeout() {
+  __device__ __forceinline__ void drain_after_timeout(int seq_end) {
     if (!TMA) return;
     const uint64_t t0 = clock_ns();
-    for (int s = 0; s < stages; ++s)
-      while (!mbar_try_wait(&full[s], (parity >> s) & 1u) && clock_ns() - t0 < WAIT_LIMIT_NS) {
+    for (int seq = seq_end; seq < seq_end + S; ++seq)
+      while (!mbar_try_wait(&full[seq % S], static_cast<uint32_t>(seq / S) & 1u) &&
+             clock_ns() - t0 < WAIT_LIMIT_NS) {
       }
   }
 };
@@ -356,399 +410,67 @@ __device__ __forceinline__ void online_update(const float (&f)[VE], float c, flo
   }
 }
 
+// Weight of one vocabulary entry in the second pass: the residual
+// max(0, p - q) of a rejected pair, or the unnormalised p of a draw from p.
+// Explicit roundings, so the summation and the search compute identical bits.
+struct Weights {
+  float c, mtc, mdc, inv_st, inv_sd;
+  bool resid;
+  __device__ __forceinline__ float operator()(float zt, float zd) const {
+    const float et = ex2(fmaf(zt, c, -mtc));
+    if (!resid) return et;
+    const float ed = ex2(fmaf(zd, c, -mdc));
+    return fmaxf(__fsub_rn(__fmul_rn(et, inv_st), __fmul_rn(ed, inv_sd)), 0.f);
+  }
+};
+
 // --------------------------------------------------------- shared state
 struct SharedSmall {
   uint64_t full[MAX_STAGES];
   float red_m[2][NWARP];
   float red_s[2][NWARP];
-  float part[6];      // exchanged through DSMEM: m_t, s_t, m_d, s_d, hint (int bits), argmax idx
-  float zpart[2];     // exchanged: residual / fallback mass of this CTA's slice
-  int tok;            // rank 0: the drawn token
-  float tsum[MAX_TILES];
-  float f[8];
-  int i[8];
+  // exchanged through DSMEM, double-buffered by job parity:
+  float part[2][6];   // m_t, s_t, m_d, s_d, hint (int bits), argmax index (int bits)
+  float zpart[2][2];  // slice mass, round 0 (residual) and 1 (fallback)
+  // per-job values of this CTA, double-buffered by job parity:
+  float gz[2][2];     // z_t[x], z_d[x]
+  int gok[2];         // draft token in range
+  float bf[8];        // broadcast floats
+  int bi[8];          // broadcast ints
   int scratch[NWARP];
-  float fscratch[NWARP];
+  float fscratch[NWARP + 1];
 };
 
-// Emission by the last job of sequence b (rank 0 CTA of that cluster).
-// Returns true in every thread of the CTA if this CTA is the last.
+// Ticket of sequence b: true in every thread of the CTA that finished the
+// sequence's last job.  Call from every thread of one CTA.
 __device__ __forceinline__ bool take_ticket(const Params &p, int b, SharedSmall &sh) {
+  __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
     const int old = atomicAdd(&p.ticket[b], 1);
-    sh.i[7] = (old == p.J - 1);
+    sh.bi[7] = (old == p.J - 1);
     if (old == p.J - 1) __threadfence();
   }
   __syncthreads();
-  return sh.i[7] != 0;
+  return sh.bi[7] != 0;
 }
 
-// ======================================================================
-// Stochastic chain: rows statistics, acceptance test, residual/bonus draw.
-// ======================================================================
-template <int DT, bool TMA>
-__global__ void __launch_bounds__(NT) sample_kernel(const Params p) {
-  using E = Elem<DT>;
-  constexpr int VE = E::VE;
-  constexpr int CH = VE * VECS_PER_THREAD;  // contiguous elements per thread in a tile scan
-  extern __shared__ __align__(128) unsigned char dyn[];
-  __shared__ SharedSmall sh;
-
-  const int tid = threadIdx.x;
-  const uint32_t rank = cluster_rank();
-  const uint32_t C = cluster_size();
-  const int job = blockIdx.x / C;
-  const int b = job / p.J;
-  const int i = job - b * p.J;
-  const bool pair = i < p.K;
-  const float c = p.c;
-
-  const int lo = static_cast<int>(rank) * p.slice;
-  const int len = max(0, min(p.V, lo + p.slice) - lo);
-
-  const unsigned char *rowt = static_cast<const unsigned char *>(p.zt) +
-                              (static_cast<size_t>(b) * p.J + i) * p.V * E::BYTES;
-  const unsigned char *rowd =
-      pair ? static_cast<const unsigned char *>(p.zd) + (static_cast<size_t>(b) * p.K + i) * p.V * E::BYTES
-           : nullptr;
-
-  Pipe<DT, TMA> pipe;
-  pipe.buf = dyn;
-  pipe.full = sh.full;
-  pipe.src[0] = rowt + static_cast<size_t>(lo) * E::BYTES;
-  pipe.src[1] = pair ? rowd + static_cast<size_t>(lo) * E::BYTES : nullptr;
-  pipe.nrows = pair ? 2 : 1;
-  pipe.stages = p.stages;
-  pipe.tile = p.tile;
-  pipe.len = len;
-  pipe.ntile = (len + p.tile - 1) / p.tile;
-  pipe.parity = 0;
-  pipe.timed_out = false;
-
-  if (tid == 0) {
-    for (int s = 0; s < p.stages; ++s) mbar_init(&sh.full[s], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-  pipe.prologue();
-
-  // gather the draft token's two logits (another warp, overlapping the copies)
-  if (tid == 32 || (NT <= 32 && tid == 0)) {
-    int ok = 1, x = 0;
-    float zx_t = 0.f, zx_d = 0.f;
-    if (pair) {
-      x = __ldg(p.tokens + static_cast<size_t>(b) * p.K + i);
-      ok = (x >= 0 && x < p.V);
-      if (ok) {
-        zx_t = E::load(rowt, x);
-        zx_d = E::load(rowd, x);
-      }
-    }
-    sh.i[0] = ok;
-    sh.f[0] = zx_t;
-    sh.f[1] = zx_d;
-    // hint: lowest rejected position already published for this sequence
-    if (rank == 0) {
-      const int hint = *reinterpret_cast<volatile int *>(p.first_rej + b);
-      sh.part[4] = __int_as_float(hint);
-    }
-  }
-
-  // ---- pass 1: online max / sum-exp of the slice, both rows at once
-  float mt = -INFINITY, st = 0.f, mtc = 0.f;
-  float md = -INFINITY, sd = 0.f, mdc = 0.f;
-  for (int k = 0; k < pipe.ntile; ++k) {
-    const int s = k % p.stages;
-    pipe.acquire(k, s);
-    const int nv = (pipe.tile_len(k) + VE - 1) / VE;
-    const unsigned char *bt = pipe.stage_row(s, 0);
-    if (pair) {
-      const unsigned char *bd = pipe.stage_row(s, 1);
-      for (int j = tid; j < nv; j += NT) {
-        float f[VE];
-        E::unpack(lds128(bt + j * 16), f);
-        online_update<VE>(f, c, mt, st, mtc);
-        E::unpack(lds128(bd + j * 16), f);
-        online_update<VE>(f, c, md, sd, mdc);
-      }
-    } else {
-      for (int j = tid; j < nv; j += NT) {
-        float f[VE];
-        E::unpack(lds128(bt + j * 16), f);
-        online_update<VE>(f, c, mt, st, mtc);
-      }
-    }
-    if (!p.resident) pipe.release(k, s);
-  }
-  block_reduce_ms(mt, st, c, sh.red_m[0], sh.red_s[0]);
-  if (pair) block_reduce_ms(md, sd, c, sh.red_m[1], sh.red_s[1]);
-  if (tid == 0) {
-    sh.part[0] = mt;
-    sh.part[1] = st;
-    sh.part[2] = md;
-    sh.part[3] = sd;
-  }
-  cluster_sync();  // #1: partial statistics visible cluster-wide
-
-  // ---- combine the slices (rank order) and take the acceptance decision
-  if (tid == 0) {
-    float Mt = -INFINITY, St = 0.f, Md = -INFINITY, Sd = 0.f;
-    for (uint32_t r = 0; r < C; ++r) {
-      ms_combine(Mt, St, dsmem_ld_f32(dsmem_addr(&sh.part[0], r)),
-                 dsmem_ld_f32(dsmem_addr(&sh.part[1], r)), c);
-      if (pair)
-        ms_combine(Md, Sd, dsmem_ld_f32(dsmem_addr(&sh.part[2], r)),
-                   dsmem_ld_f32(dsmem_addr(&sh.part[3], r)), c);
-    }
-    const int hint = __float_as_int(dsmem_ld_f32(dsmem_addr(&sh.part[4], 0)));
-    const int ok = sh.i[0];
-    int accept = 1;
-    if (pair && ok) {
-      const float a = fmaf(sh.f[0], c, -(Mt * c));
-      const float d = fmaf(sh.f[1], c, -(Md * c));
-      const float ratio = ex2(a - d) * (Sd / St);  // p_i(x_i) / q_i(x_i)
-      const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
-      accept = u < ratio;
-    }
-    const int need = pair ? (ok && !accept) : 1;
-    const int superseded = pair ? (hint < i) : (hint < p.K);
-    sh.i[1] = accept;
-    sh.i[2] = need && !superseded;
-    sh.f[2] = Mt;
-    sh.f[3] = St;
-    sh.f[4] = Md;
-    sh.f[5] = Sd;
-    if (rank == 0) {
-      const int R = 2 * p.K + 1;
-      if (p.out_row_max) {
-        p.out_row_max[static_cast<size_t>(b) * R + i] = Mt;
-        if (pair) p.out_row_max[static_cast<size_t>(b) * R + p.K + 1 + i] = Md;
-      }
-      if (p.out_row_sumexp) {
-        p.out_row_sumexp[static_cast<size_t>(b) * R + i] = St;
-        if (pair) p.out_row_sumexp[static_cast<size_t>(b) * R + p.K + 1 + i] = Sd;
-      }
-      if (pair && !ok) {
-        atomicOr(p.seq_err + b, 1);
-        atomicOr(p.status, ST_TOKEN);
-      }
-      if (pair && ok && !accept) atomicMin(p.first_rej + b, i);
-    }
-  }
-  __syncthreads();
-  const int do_draw = sh.i[2];
-  const float Mt = sh.f[2], St = sh.f[3], Md = sh.f[4], Sd = sh.f[5];
-  const float mtc_g = Mt * c, mdc_g = Md * c;
-  const float inv_st = 1.f / St, inv_sd = 1.f / Sd;
-
-  // ---- pass 2 (only for a reject or the bonus row): weights, slice mass,
-  // owner slice and tile, then a block scan inside the owner tile.
-  int fallback = 0;
-  if (do_draw) {
-    // weights: residual max(0, p - q) on a pair, p (unnormalised) otherwise
-    bool resid = pair;
-    float t_local = 0.f;
-    int owner = 0, pick_last = 0;
-    for (int round = 0; round < 2; ++round) {
-      if (!p.resident) {
-        __syncthreads();
-        pipe.prologue();
-      }
-      for (int k = 0; k < pipe.ntile; ++k) {
-        const int s = k % p.stages;
-        if (!p.resident) pipe.acquire(k, s);
-        const int nv = (pipe.tile_len(k) + VE - 1) / VE;
-        float acc = 0.f;
-        const unsigned char *bt = pipe.stage_row(s, 0);
-        if (resid) {
-          const unsigned char *bd = pipe.stage_row(s, 1);
-          for (int j = tid; j < nv; j += NT) {
-            float ft[VE], fd[VE];
-            E::unpack(lds128(bt + j * 16), ft);
-            E::unpack(lds128(bd + j * 16), fd);
-#pragma unroll
-            for (int e = 0; e < VE; ++e) {
-              const float w = ex2(fmaf(ft[e], c, -mtc_g)) * inv_st - ex2(fmaf(fd[e], c, -mdc_g)) * inv_sd;
-              acc += fmaxf(w, 0.f);
-            }
-          }
-        } else {
-          for (int j = tid; j < nv; j += NT) {
-            float ft[VE];
-            E::unpack(lds128(bt + j * 16), ft);
-#pragma unroll
-            for (int e = 0; e < VE; ++e) acc += ex2(fmaf(ft[e], c, -mtc_g));
-          }
-        }
-        const float tsum = block_reduce_sum(acc, sh.fscratch);
-        if (tid == 0) sh.tsum[k] = tsum;
-        if (!p.resident) pipe.release(k, s);
-      }
-      if (tid == 0) {
-        float z = 0.f;
-        for (int k = 0; k < pipe.ntile; ++k) z += sh.tsum[k];
-        sh.zpart[round] = z;
-      }
-      cluster_sync();  // #2: slice masses visible cluster-wide
-      if (tid == 0) {
-        float Z = 0.f;
-        for (uint32_t r = 0; r < C; ++r) Z += dsmem_ld_f32(dsmem_addr(&sh.zpart[round], r));
-        int again = 0;
-        if (resid && !(Z > 0.f)) {
-          again = 1;  // no residual mass in fp32: draw from p at this position
-        } else {
-          const uint32_t pos = static_cast<uint32_t>(pair ? i : p.K);
-          const float t = philox_uniform(p.seed, static_cast<uint32_t>(b), pos, 1u) * Z;
-          float P = 0.f, Pown = 0.f, Plast = 0.f;
-          int own = -1, last = -1;
-          for (uint32_t r = 0; r < C; ++r) {
-            const float zr = dsmem_ld_f32(dsmem_addr(&sh.zpart[round], r));
-            if (own < 0 && P + zr > t) {
-              own = static_cast<int>(r);
-              Pown = P;
-            }
-            if (zr > 0.f) {
-              last = static_cast<int>(r);
-              Plast = P;
-            }
-            P += zr;
-          }
-          int pl = 0;
-          if (own < 0) {
-            own = last < 0 ? 0 : last;
-            Pown = Plast;
-            pl = 1;
-          }
-          sh.i[3] = own;
-          sh.i[4] = pl;
-          sh.f[6] = t - Pown;
-        }
-        sh.i[5] = again;
-      }
-      __syncthreads();
-      if (sh.i[5] && round == 0) {
-        resid = false;
-        fallback = 1;
-        continue;
-      }
-      owner = sh.i[3];
-      pick_last = sh.i[4];
-      t_local = sh.f[6];
-      break;
-    }
-
-    if (static_cast<int>(rank) == owner) {
-      // owner tile: first tile whose running mass passes t_local
-      if (tid == 0) {
-        float TP = 0.f, TPk = 0.f, TPlast = 0.f;
-        int kk = -1, klast = -1;
-        for (int k = 0; k < pipe.ntile; ++k) {
-          const float ts = sh.tsum[k];
-          if (kk < 0 && TP + ts > t_local) {
-            kk = k;
-            TPk = TP;
-          }
-          if (ts > 0.f) {
-            klast = k;
-            TPlast = TP;
-          }
-          TP += ts;
-        }
-        int pl = pick_last;
-        if (pl || kk < 0) {
-          kk = klast < 0 ? 0 : klast;
-          TPk = TPlast;
-          pl = 1;
-        }
-        sh.i[3] = kk;
-        sh.i[4] = pl;
-        sh.f[6] = t_local - TPk;
-      }
-      __syncthreads();
-      const int kk = sh.i[3];
-      const int pl = sh.i[4];
-      const float tl = sh.f[6];
-      int s = kk;
-      if (!p.resident) {
-        __syncthreads();
-        s = 0;
-        if (TMA && tid == 0) pipe.issue(kk, 0);
-        pipe.acquire(kk, 0);
-      }
-      const int n = pipe.len > 0 ? pipe.tile_len(kk) : 0;
-      // contiguous chunk of this thread inside the tile
-      const int e0 = tid * CH;
-      float w[CH];
-      float sum = 0.f;
-      const unsigned char *bt = pipe.stage_row(s, 0);
-      const unsigned char *bd = resid ? pipe.stage_row(s, 1) : nullptr;
-#pragma unroll
-      for (int v = 0; v < VECS_PER_THREAD; ++v) {
-        const int base = e0 + v * VE;
-        float ft[VE], fd[VE];
-        if (base < n) {
-          E::unpack(lds128(bt + base * E::BYTES), ft);
-          if (resid) E::unpack(lds128(bd + base * E::BYTES), fd);
-        }
-#pragma unroll
-        for (int e = 0; e < VE; ++e) {
-          float x = 0.f;
-          if (base + e < n) {
-            if (resid)
-              x = fmaxf(ex2(fmaf(ft[e], c, -mtc_g)) * inv_st - ex2(fmaf(fd[e], c, -mdc_g)) * inv_sd, 0.f);
-            else
-              x = ex2(fmaf(ft[e], c, -mtc_g));
-          }
-          w[v * VE + e] = x;
-          sum += x;
-        }
-      }
-      const float excl = block_exclusive_scan(sum, sh.fscratch);
-      int pick = INT_MAX;
-      if (!pl) {
-        float run = excl;
-#pragma unroll
-        for (int e = 0; e < CH; ++e) {
-          run += w[e];
-          if (pick == INT_MAX && run > tl && w[e] > 0.f) pick = e0 + e;
-        }
-      }
-      pick = block_reduce_min_int(pick, sh.scratch);
-      if (pick == INT_MAX) {
-        int lastpos = -1;
-#pragma unroll
-        for (int e = 0; e < CH; ++e)
-          if (w[e] > 0.f) lastpos = e0 + e;
-        pick = block_reduce_max_int(lastpos, sh.scratch);
-        if (pick < 0) pick = 0;
-      }
-      if (tid == 0) dsmem_st_s32(dsmem_addr(&sh.tok, 0), lo + kk * p.tile + pick);
-    }
-  }
-  cluster_sync();  // #3: token delivered to rank 0; no DSMEM access after this
-  if (pipe.timed_out) {
-    atomicOr(p.status, ST_TIMEOUT);
-    pipe.drain_after_timeout();
-  }
-  if (rank != 0) return;
-  if (tid == 0 && do_draw) p.cand[static_cast<size_t>(b) * p.J + i] = sh.tok | (fallback ? CAND_FALLBACK : 0);
-
-  // ---- emission by the last job of the sequence
-  if (!take_ticket(p, b, sh)) return;
+// Outputs of stochastic-chain sequence b, once all its jobs are done.
+__device__ __forceinline__ void emit_chain_sample(const Params &p, int b) {
   const int err = __ldcg(p.seq_err + b);
   const int n = min(__ldcg(p.first_rej + b), p.K);
-  for (int e = tid; e <= p.K; e += NT) {
+  const int cn = __ldcg(p.cand + static_cast<size_t>(b) * p.J + n);
+  for (int e = threadIdx.x; e <= p.K; e += NT) {
     int v = -1;
     if (!err) {
       if (e < n)
         v = __ldg(p.tokens + static_cast<size_t>(b) * p.K + e);
       else if (e == n)
-        v = __ldcg(p.cand + static_cast<size_t>(b) * p.J + n) & ~CAND_FALLBACK;
+        v = cn & ~CAND_FALLBACK;
     }
     p.out_tokens[static_cast<size_t>(b) * (p.K + 1) + e] = v;
   }
-  if (tid == 0) {
+  if (threadIdx.x == 0) {
     p.out_n[b] = err ? -1 : n;
     if (p.stats) {
       if (err) {
@@ -756,12 +478,8 @@ __global__ void __launch_bounds__(NT) sample_kernel(const Params p) {
       } else {
         atomicAdd(&p.stats->sequences, 1ull);
         atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(n));
-        if (n == p.K)
-          atomicAdd(&p.stats->bonus, 1ull);
-        else
-          atomicAdd(&p.stats->resampled, 1ull);
-        if (n < p.K && (__ldcg(p.cand + static_cast<size_t>(b) * p.J + n) & CAND_FALLBACK))
-          atomicAdd(&p.stats->residual_fallbacks, 1ull);
+        atomicAdd(n == p.K ? &p.stats->bonus : &p.stats->resampled, 1ull);
+        if (n < p.K && (cn & CAND_FALLBACK)) atomicAdd(&p.stats->residual_fallbacks, 1ull);
       }
     }
     p.ticket[b] = 0;
@@ -771,10 +489,10 @@ __global__ void __launch_bounds__(NT) sample_kernel(const Params p) {
 }
 
 // ======================================================================
-// Greedy chain (T = 0) and greedy tree: per-row argmax, then the walk.
+// Stochastic chain: row statistics, acceptance test, residual/bonus draw.
 // ======================================================================
 template <int DT, bool TMA>
-__global__ void __launch_bounds__(NT) argmax_kernel(const Params p) {
+__global__ void __launch_bounds__(NT, 2) sample_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
   extern __shared__ __align__(128) unsigned char dyn[];
@@ -783,170 +501,455 @@ __global__ void __launch_bounds__(NT) argmax_kernel(const Params p) {
   const int tid = threadIdx.x;
   const uint32_t rank = cluster_rank();
   const uint32_t C = cluster_size();
-  const int job = blockIdx.x / C;
-  const int b = job / p.J;
-  const int i = job - b * p.J;
-  const int lo = static_cast<int>(rank) * p.slice;
-  const int len = max(0, min(p.V, lo + p.slice) - lo);
-  const unsigned char *row = static_cast<const unsigned char *>(p.zt) +
-                             (static_cast<size_t>(b) * p.J + i) * p.V * E::BYTES;
+  const float c = p.c;
 
-  Pipe<DT, TMA> pipe;
-  pipe.buf = dyn;
-  pipe.full = sh.full;
-  pipe.src[0] = row + static_cast<size_t>(lo) * E::BYTES;
-  pipe.src[1] = nullptr;
-  pipe.nrows = 1;
-  pipe.stages = p.stages;
-  pipe.tile = p.tile;
-  pipe.len = len;
-  pipe.ntile = (len + p.tile - 1) / p.tile;
-  pipe.parity = 0;
-  pipe.timed_out = false;
+  Stream<DT, TMA> st;
+  st.p = &p;
+  st.buf = dyn;
+  st.full = sh.full;
+  st.cl = blockIdx.x / C;
+  st.lo = static_cast<int>(rank) * p.slice;
+  st.len = max(0, min(p.V, st.lo + p.slice) - st.lo);
+  st.nt = (st.len + p.tile - 1) / p.tile;
+  st.S = p.stages;
+  st.srows = p.K > 0 ? 2 : 1;
+  st.timed_out = false;
+  const int lo = st.lo, len = st.len;
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) mbar_init(&sh.full[s], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  pipe.prologue();
+  st.prologue();
 
-  float best = -INFINITY;
-  int bidx = INT_MAX;
-  for (int k = 0; k < pipe.ntile; ++k) {
-    const int s = k % p.stages;
-    pipe.acquire(k, s);
-    const int nv = (pipe.tile_len(k) + VE - 1) / VE;
-    const unsigned char *bt = pipe.stage_row(s, 0);
-    const int base = lo + k * p.tile;
-    for (int j = tid; j < nv; j += NT) {
-      float f[VE];
-      E::unpack(lds128(bt + j * 16), f);
-      float vm = f[0];
-#pragma unroll
-      for (int e = 1; e < VE; ++e) vm = fmaxf(vm, f[e]);
-      if (vm > best) {  // rare after the first few vectors
-        best = vm;
-#pragma unroll
-        for (int e = VE - 1; e >= 0; --e)
-          if (f[e] == vm) bidx = base + j * VE + e;
+  // contiguous chunk of this thread in the second pass
+  const int E2 = ((len + NT - 1) / NT + VE - 1) / VE * VE;
+  const int e0 = min(len, tid * E2), e1 = min(len, e0 + E2);
+
+  int seq = 0;
+  for (int n = 0;; ++n) {
+    const int q = st.cl + n * p.ncl;
+    if (q >= p.njobs) break;
+    const int par = n & 1;
+    int b, i;
+    decode_job(p, q, b, i);
+    const bool pair = i < p.K;
+    const unsigned char *rt, *rd;
+    st.rows_of(q, rt, rd);
+
+    // draft token and its two logits (another warp, overlapping pass 1)
+    if (tid == 32) {
+      int ok = 1;
+      float zx_t = 0.f, zx_d = 0.f;
+      if (pair) {
+        const int x = __ldg(p.tokens + static_cast<size_t>(b) * p.K + i);
+        ok = (x >= 0 && x < p.V);
+        if (ok) {
+          zx_t = E::load(rt, x);
+          zx_d = E::load(rd, x);
+        }
+      }
+      sh.gok[par] = ok;
+      sh.gz[par][0] = zx_t;
+      sh.gz[par][1] = zx_d;
+      if (rank == 0) {  // lowest rejected position already published
+        const int hint = *reinterpret_cast<volatile int *>(p.first_rej + b);
+        sh.part[par][4] = __int_as_float(hint);
       }
     }
-    pipe.release(k, s);
-  }
-  block_reduce_argmax(best, bidx, sh.fscratch, sh.scratch);
-  if (tid == 0) {
-    sh.part[0] = best;
-    sh.part[5] = __int_as_float(bidx);
-  }
-  cluster_sync();  // #1
-  if (rank == 0 && tid == 0) {
-    float v = -INFINITY;
-    int idx = INT_MAX;
-    for (uint32_t r = 0; r < C; ++r)
-      am_combine(v, idx, dsmem_ld_f32(dsmem_addr(&sh.part[0], r)),
-                 __float_as_int(dsmem_ld_f32(dsmem_addr(&sh.part[5], r))));
-    if (idx == INT_MAX) idx = 0;  // every logit is -inf: first index
-    p.cand[static_cast<size_t>(b) * p.J + i] = idx;
-    if (p.kind == KIND_GREEDY_CHAIN) {
-      const int R = 2 * p.K + 1;
-      if (p.out_row_max) {
-        p.out_row_max[static_cast<size_t>(b) * R + i] = v;
-        if (i < p.K) p.out_row_max[static_cast<size_t>(b) * R + p.K + 1 + i] = NAN;
+
+    // ---- pass 1: online max / sum-exp of both rows of this slice
+    float mt = -INFINITY, s_t = 0.f, mtc = 0.f;
+    float md = -INFINITY, s_d = 0.f, mdc = 0.f;
+    for (int k = 0; k < st.nt; ++k, ++seq) {
+      st.acquire(seq, k, rt, rd);
+      const int s = seq % st.S;
+      const int nv = (st.tile_len(k) + VE - 1) / VE;
+      const unsigned char *bt = st.stage_row(s, 0);
+      if (pair) {
+        const unsigned char *bd = st.stage_row(s, 1);
+        for (int j = tid; j < nv; j += NT) {
+          float f[VE];
+          E::unpack(lds128(bt + j * 16), f);
+          online_update<VE>(f, c, mt, s_t, mtc);
+          E::unpack(lds128(bd + j * 16), f);
+          online_update<VE>(f, c, md, s_d, mdc);
+        }
+      } else {
+        for (int j = tid; j < nv; j += NT) {
+          float f[VE];
+          E::unpack(lds128(bt + j * 16), f);
+          online_update<VE>(f, c, mt, s_t, mtc);
+        }
       }
-      if (p.out_row_sumexp) {
-        p.out_row_sumexp[static_cast<size_t>(b) * R + i] = NAN;
-        if (i < p.K) p.out_row_sumexp[static_cast<size_t>(b) * R + p.K + 1 + i] = NAN;
+      st.release(seq);
+    }
+    block_reduce_ms(mt, s_t, c, sh.red_m[0], sh.red_s[0]);
+    if (pair) block_reduce_ms(md, s_d, c, sh.red_m[1], sh.red_s[1]);
+    if (tid == 0) {
+      sh.part[par][0] = mt;
+      sh.part[par][1] = s_t;
+      sh.part[par][2] = md;
+      sh.part[par][3] = s_d;
+    }
+    cluster_sync();  // partial statistics of job n visible cluster-wide
+
+    // ---- combine the slices (rank order) and take the acceptance decision
+    if (tid == 0) {
+      float Mt = -INFINITY, St = 0.f, Md = -INFINITY, Sd = 0.f;
+      for (uint32_t r = 0; r < C; ++r) {
+        ms_combine(Mt, St, dsmem_ld_f32(dsmem_addr(&sh.part[par][0], r)),
+                   dsmem_ld_f32(dsmem_addr(&sh.part[par][1], r)), c);
+        if (pair)
+          ms_combine(Md, Sd, dsmem_ld_f32(dsmem_addr(&sh.part[par][2], r)),
+                     dsmem_ld_f32(dsmem_addr(&sh.part[par][3], r)), c);
+      }
+      const int hint = __float_as_int(dsmem_ld_f32(dsmem_addr(&sh.part[par][4], 0)));
+      const int ok = sh.gok[par];
+      int accept = 1;
+      if (pair && ok) {
+        const float a = fmaf(sh.gz[par][0], c, -(Mt * c));
+        const float d = fmaf(sh.gz[par][1], c, -(Md * c));
+        const float ratio = ex2(a - d) * (Sd / St);  // p_i(x_i) / q_i(x_i)
+        const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
+        accept = u < ratio;
+      }
+      const int need = pair ? (ok && !accept) : 1;
+      const int superseded = pair ? (hint < i) : (hint < p.K);
+      sh.bi[0] = need && !superseded;
+      sh.bf[0] = Mt;
+      sh.bf[1] = St;
+      sh.bf[2] = Md;
+      sh.bf[3] = Sd;
+      if (rank == 0) {
+        const int R = 2 * p.K + 1;
+        if (p.out_row_max) {
+          p.out_row_max[static_cast<size_t>(b) * R + i] = Mt;
+          if (pair) p.out_row_max[static_cast<size_t>(b) * R + p.K + 1 + i] = Md;
+        }
+        if (p.out_row_sumexp) {
+          p.out_row_sumexp[static_cast<size_t>(b) * R + i] = St;
+          if (pair) p.out_row_sumexp[static_cast<size_t>(b) * R + p.K + 1 + i] = Sd;
+        }
+        if (pair && !ok) {
+          atomicOr(p.seq_err + b, 1);
+          atomicOr(p.status, ST_TOKEN);
+        }
+        if (pair && ok && !accept) atomicMin(p.first_rej + b, i);
       }
     }
+    __syncthreads();
+
+    int taker = 0;  // the CTA that records the job and takes its ticket
+    if (sh.bi[0]) {
+      // ---- pass 2 (a reject or the bonus row), from the slice just read
+      // (L2-resident): per-thread contiguous chunks, block scan, slice mass,
+      // cluster exchange, owner slice, then one thread walks its chunk.
+      Weights W;
+      W.c = c;
+      W.mtc = sh.bf[0] * c;
+      W.mdc = sh.bf[2] * c;
+      W.inv_st = 1.f / sh.bf[1];
+      W.inv_sd = 1.f / sh.bf[3];
+      W.resid = pair;
+      int fallback = 0, owner = 0, pl = 0;
+      float tl = 0.f, excl = 0.f, sum = 0.f;
+      for (int round = 0; round < 2; ++round) {
+        sum = 0.f;
+        if (TMA) {
+          for (int e = e0; e < e1; e += VE) {
+            const size_t off = static_cast<size_t>(lo + e) * E::BYTES;
+            float ft[VE], fd[VE];
+            E::unpack(__ldg(reinterpret_cast<const uint4 *>(rt + off)), ft);
+            if (W.resid) E::unpack(__ldg(reinterpret_cast<const uint4 *>(rd + off)), fd);
+#pragma unroll
+            for (int j = 0; j < VE; ++j) sum = __fadd_rn(sum, W(ft[j], W.resid ? fd[j] : 0.f));
+          }
+        } else {
+          for (int e = e0; e < e1; ++e)
+            sum = __fadd_rn(sum, W(E::load(rt, lo + e), W.resid ? E::load(rd, lo + e) : 0.f));
+        }
+        float total;
+        excl = block_exclusive_scan(sum, sh.fscratch, &total);
+        if (tid == 0) sh.zpart[par][round] = total;
+        cluster_sync();  // slice masses visible cluster-wide
+        if (tid == 0) {
+          float Z = 0.f;
+          for (uint32_t r = 0; r < C; ++r) Z += dsmem_ld_f32(dsmem_addr(&sh.zpart[par][round], r));
+          int again = 0;
+          if (W.resid && !(Z > 0.f)) {
+            again = 1;  // no residual mass in fp32: draw from p at this position
+          } else {
+            const uint32_t pos = static_cast<uint32_t>(pair ? i : p.K);
+            const float t = philox_uniform(p.seed, static_cast<uint32_t>(b), pos, 1u) * Z;
+            float P = 0.f, Pown = 0.f, Plast = 0.f;
+            int own = -1, last = -1;
+            for (uint32_t r = 0; r < C; ++r) {
+              const float zr = dsmem_ld_f32(dsmem_addr(&sh.zpart[par][round], r));
+              if (own < 0 && P + zr > t) {
+                own = static_cast<int>(r);
+                Pown = P;
+              }
+              if (zr > 0.f) {
+                last = static_cast<int>(r);
+                Plast = P;
+              }
+              P += zr;
+            }
+            int lastmode = 0;
+            if (own < 0) {
+              own = last < 0 ? 0 : last;
+              Pown = Plast;
+              lastmode = 1;
+            }
+            sh.bi[1] = own;
+            sh.bi[2] = lastmode;
+            sh.bf[4] = t - Pown;
+          }
+          sh.bi[3] = again;
+        }
+        __syncthreads();
+        if (sh.bi[3] && round == 0) {
+          W.resid = false;
+          fallback = 1;
+          continue;
+        }
+        owner = sh.bi[1];
+        pl = sh.bi[2];
+        tl = sh.bf[4];
+        break;
+      }
+      taker = owner;
+      if (static_cast<int>(rank) == owner) {
+        // the thread whose chunk holds the crossing (or the last positive one)
+        int who;
+        if (!pl)
+          who = block_reduce_min_int((sum > 0.f && __fadd_rn(excl, sum) > tl) ? tid : INT_MAX,
+                                     sh.scratch);
+        else
+          who = block_reduce_max_int(sum > 0.f ? tid : -1, sh.scratch);
+        if (who == INT_MAX || who < 0) {
+          // rounding left no crossing in this slice: last positive entry
+          pl = 1;
+          who = block_reduce_max_int(sum > 0.f ? tid : -1, sh.scratch);
+          if (who < 0) who = 0;
+        }
+        if (tid == who) {
+          float run = 0.f;
+          int pick = -1;
+          for (int e = e0; e < e1; ++e) {
+            const float w = W(E::load(rt, lo + e), W.resid ? E::load(rd, lo + e) : 0.f);
+            run = __fadd_rn(run, w);
+            if (w > 0.f) {
+              if (!pl && __fadd_rn(excl, run) > tl) {
+                pick = e;
+                break;
+              }
+              pick = e;
+            }
+          }
+          if (pick < 0) pick = e0;
+          p.cand[static_cast<size_t>(b) * p.J + i] = (lo + pick) | (fallback ? CAND_FALLBACK : 0);
+          __threadfence();
+        }
+      }
+    }
+    if (static_cast<int>(rank) == taker) {
+      if (take_ticket(p, b, sh)) emit_chain_sample(p, b);
+    }
   }
-  cluster_sync();  // #2: no DSMEM access after this
-  if (pipe.timed_out) {
+  if (st.timed_out) {
     atomicOr(p.status, ST_TIMEOUT);
-    pipe.drain_after_timeout();
+    st.drain_after_timeout(seq);
   }
-  if (rank != 0) return;
-  if (!take_ticket(p, b, sh)) return;
+  // keep this CTA's shared memory alive until no peer can read it
+  cluster_sync();
+}
 
-  // ---- emission: all rows of sequence b have their argmax in cand[b, :]
-  int *s_amax = reinterpret_cast<int *>(dyn);
-  int *s_tok = s_amax + p.J;
-  for (int e = tid; e < p.J; e += NT) s_amax[e] = __ldcg(p.cand + static_cast<size_t>(b) * p.J + e);
-  if (p.kind == KIND_GREEDY_CHAIN) {
-    for (int e = tid; e < p.K; e += NT) s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * p.K + e);
+// ======================================================================
+// Greedy chain (T = 0) and greedy tree: per-row argmax, then the walk.
+// ======================================================================
+template <int DT, bool TMA>
+__global__ void __launch_bounds__(NT, 2) argmax_kernel(const Params p) {
+  using E = Elem<DT>;
+  constexpr int VE = E::VE;
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ SharedSmall sh;
+
+  const int tid = threadIdx.x;
+  const uint32_t rank = cluster_rank();
+  const uint32_t C = cluster_size();
+
+  Stream<DT, TMA> st;
+  st.p = &p;
+  st.buf = dyn;
+  st.full = sh.full;
+  st.cl = blockIdx.x / C;
+  st.lo = static_cast<int>(rank) * p.slice;
+  st.len = max(0, min(p.V, st.lo + p.slice) - st.lo);
+  st.nt = (st.len + p.tile - 1) / p.tile;
+  st.S = p.stages;
+  st.srows = 1;
+  st.timed_out = false;
+
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) mbar_init(&sh.full[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  st.prologue();
+
+  int seq = 0;
+  for (int n = 0;; ++n) {
+    const int q = st.cl + n * p.ncl;
+    if (q >= p.njobs) break;
+    const int par = n & 1;
+    int b, i;
+    decode_job(p, q, b, i);
+    const unsigned char *rt, *rd;
+    st.rows_of(q, rt, rd);
+
+    float best = -INFINITY;
+    int bidx = INT_MAX;
+    for (int k = 0; k < st.nt; ++k, ++seq) {
+      st.acquire(seq, k, rt, nullptr);
+      const int s = seq % st.S;
+      const int nv = (st.tile_len(k) + VE - 1) / VE;
+      const unsigned char *bt = st.stage_row(s, 0);
+      const int base = st.lo + k * p.tile;
+      for (int j = tid; j < nv; j += NT) {
+        float f[VE];
+        E::unpack(lds128(bt + j * 16), f);
+        float vm = f[0];
+#pragma unroll
+        for (int e = 1; e < VE; ++e) vm = fmaxf(vm, f[e]);
+        if (vm > best) {  // rare after the first few vectors
+          best = vm;
+#pragma unroll
+          for (int e = VE - 1; e >= 0; --e)
+            if (f[e] == vm) bidx = base + j * VE + e;
+        }
+      }
+      st.release(seq);
+    }
+    block_reduce_argmax(best, bidx, sh.fscratch, sh.scratch);
+    if (tid == 0) {
+      sh.part[par][0] = best;
+      sh.part[par][5] = __int_as_float(bidx);
+    }
+    cluster_sync();  // partial maxima of job n visible cluster-wide
+    if (rank != 0) continue;
+    if (tid == 0) {
+      float v = -INFINITY;
+      int idx = INT_MAX;
+      for (uint32_t r = 0; r < C; ++r)
+        am_combine(v, idx, dsmem_ld_f32(dsmem_addr(&sh.part[par][0], r)),
+                   __float_as_int(dsmem_ld_f32(dsmem_addr(&sh.part[par][5], r))));
+      if (idx == INT_MAX) idx = 0;  // every logit is -inf: first index
+      p.cand[static_cast<size_t>(b) * p.J + i] = idx;
+      if (p.kind == KIND_GREEDY_CHAIN) {
+        const int R = 2 * p.K + 1;
+        if (p.out_row_max) {
+          p.out_row_max[static_cast<size_t>(b) * R + i] = v;
+          if (i < p.K) p.out_row_max[static_cast<size_t>(b) * R + p.K + 1 + i] = NAN;
+        }
+        if (p.out_row_sumexp) {
+          p.out_row_sumexp[static_cast<size_t>(b) * R + i] = NAN;
+          if (i < p.K) p.out_row_sumexp[static_cast<size_t>(b) * R + p.K + 1 + i] = NAN;
+        }
+      }
+    }
+    if (!take_ticket(p, b, sh)) continue;
+
+    // ---- emission: every row of sequence b has its argmax in cand[b, :]
+    int *s_amax = reinterpret_cast<int *>(dyn + p.emit_off);
+    int *s_tok = s_amax + p.J;
+    for (int e = tid; e < p.J; e += NT) s_amax[e] = __ldcg(p.cand + static_cast<size_t>(b) * p.J + e);
+    if (p.kind == KIND_GREEDY_CHAIN) {
+      for (int e = tid; e < p.K; e += NT) s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * p.K + e);
+      __syncthreads();
+      if (tid == 0) {
+        int nacc = p.K, err = 0;
+        for (int e = 0; e < p.K; ++e) {
+          const int x = s_tok[e];
+          if (x < 0 || x >= p.V) err = 1;
+          if (nacc == p.K && x != s_amax[e]) nacc = e;
+        }
+        int32_t *out = p.out_tokens + static_cast<size_t>(b) * (p.K + 1);
+        for (int e = 0; e <= p.K; ++e)
+          out[e] = err ? -1 : (e < nacc ? s_tok[e] : (e == nacc ? s_amax[nacc] : -1));
+        p.out_n[b] = err ? -1 : nacc;
+        if (err) atomicOr(p.status, ST_TOKEN);
+        if (p.stats) {
+          if (err) {
+            atomicAdd(&p.stats->errors, 1ull);
+          } else {
+            atomicAdd(&p.stats->sequences, 1ull);
+            atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(nacc));
+            atomicAdd(nacc == p.K ? &p.stats->bonus : &p.stats->resampled, 1ull);
+          }
+        }
+        p.ticket[b] = 0;
+      }
+      __syncthreads();
+      continue;
+    }
+
+    // tree: N = J nodes
+    const int N = p.J;
+    int *s_par = s_tok + N;
+    int *s_depth = s_par + N;
+    unsigned char *s_acc = reinterpret_cast<unsigned char *>(s_depth + N);
+    for (int e = tid; e < N; e += NT) {
+      s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * N + e);
+      s_par[e] = __ldg(p.parent + e);
+    }
     __syncthreads();
     if (tid == 0) {
-      int n = p.K, err = 0;
-      for (int e = 0; e < p.K; ++e) {
-        const int x = s_tok[e];
-        if (x < 0 || x >= p.V) err = 1;
-        if (n == p.K && x != s_amax[e]) n = e;
-      }
-      int32_t *out = p.out_tokens + static_cast<size_t>(b) * (p.K + 1);
-      for (int e = 0; e <= p.K; ++e) out[e] = err ? -1 : (e < n ? s_tok[e] : (e == n ? s_amax[n] : -1));
-      p.out_n[b] = err ? -1 : n;
-      if (err) atomicOr(p.status, ST_TOKEN);
-      if (p.stats) {
-        if (err) {
-          atomicAdd(&p.stats->errors, 1ull);
-        } else {
-          atomicAdd(&p.stats->sequences, 1ull);
-          atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(n));
-          atomicAdd(n == p.K ? &p.stats->bonus : &p.stats->resampled, 1ull);
+      const int W = p.max_depth + 1;
+      int32_t *path = p.out_tokens + static_cast<size_t>(b) * W;
+      int bad_parent = s_par[0] != -1, bad_tok = 0;
+      s_depth[0] = 0;
+      s_acc[0] = 1;
+      int bestn = 0;
+      for (int c2 = 1; c2 < N && !bad_parent; ++c2) {
+        const int pc = s_par[c2];
+        if (pc < 0 || pc >= c2) {
+          bad_parent = 1;
+          break;
         }
+        const int d = s_depth[pc] + 1;
+        if (d > p.max_depth) {
+          bad_parent = 1;
+          break;
+        }
+        const int x = s_tok[c2];
+        if (x < 0 || x >= p.V) bad_tok = 1;
+        s_depth[c2] = d;
+        s_acc[c2] = s_acc[pc] && x == s_amax[pc];
+        if (s_acc[c2] && d > s_depth[bestn]) bestn = c2;
+      }
+      if (bad_parent || bad_tok) {
+        for (int e = 0; e < W; ++e) path[e] = -1;
+        p.out_n[b] = -1;
+        atomicOr(p.status, bad_parent ? ST_PARENT : ST_TOKEN);
+      } else {
+        const int d = s_depth[bestn];
+        for (int e = d + 1; e < W; ++e) path[e] = -1;
+        path[d] = s_amax[bestn];
+        for (int n2 = bestn, e = d - 1; n2 != 0; n2 = s_par[n2], --e) path[e] = s_tok[n2];
+        p.out_n[b] = d + 1;
       }
       p.ticket[b] = 0;
     }
-    return;
+    __syncthreads();
   }
-
-  // tree: N = J nodes
-  const int N = p.J;
-  int *s_par = s_tok + N;
-  int *s_depth = s_par + N;
-  unsigned char *s_acc = reinterpret_cast<unsigned char *>(s_depth + N);
-  for (int e = tid; e < N; e += NT) {
-    s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * N + e);
-    s_par[e] = __ldg(p.parent + e);
+  if (st.timed_out) {
+    atomicOr(p.status, ST_TIMEOUT);
+    st.drain_after_timeout(seq);
   }
-  __syncthreads();
-  if (tid == 0) {
-    const int W = p.max_depth + 1;
-    int32_t *path = p.out_tokens + static_cast<size_t>(b) * W;
-    int bad_parent = s_par[0] != -1, bad_tok = 0;
-    s_depth[0] = 0;
-    s_acc[0] = 1;
-    int best = 0;
-    for (int c2 = 1; c2 < N && !bad_parent; ++c2) {
-      const int pc = s_par[c2];
-      if (pc < 0 || pc >= c2) {
-        bad_parent = 1;
-        break;
-      }
-      const int d = s_depth[pc] + 1;
-      if (d > p.max_depth) {
-        bad_parent = 1;
-        break;
-      }
-      const int x = s_tok[c2];
-      if (x < 0 || x >= p.V) bad_tok = 1;
-      s_depth[c2] = d;
-      s_acc[c2] = s_acc[pc] && x == s_amax[pc];
-      if (s_acc[c2] && d > s_depth[best]) best = c2;
-    }
-    if (bad_parent || bad_tok) {
-      for (int e = 0; e < W; ++e) path[e] = -1;
-      p.out_n[b] = -1;
-      atomicOr(p.status, bad_parent ? ST_PARENT : ST_TOKEN);
-    } else {
-      const int d = s_depth[best];
-      for (int e = d + 1; e < W; ++e) path[e] = -1;
-      path[d] = s_amax[best];
-      for (int n2 = best, e = d - 1; n2 != 0; n2 = s_par[n2], --e) path[e] = s_tok[n2];
-      p.out_n[b] = d + 1;
-    }
-    p.ticket[b] = 0;
-  }
+  cluster_sync();
 }
 
 // ======================================================================

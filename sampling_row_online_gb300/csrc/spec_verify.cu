@@ -7,6 +7,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -106,19 +107,44 @@ void bind_ws(Params &p, const Workspace *w) {
 }
 
 // ------------------------------------------------------------ geometry
-constexpr int SLICE_TARGET_BYTES = 16 * 1024;   // per row and CTA
-constexpr int RESIDENT_LIMIT_BYTES = 64 * 1024; // keep a slice on chip up to this
-constexpr int STREAM_STAGES = 4;
+constexpr int SLICE_TARGET_BYTES = 16 * 1024;  // vocabulary bytes per row and CTA
+constexpr int DEFAULT_STAGES = 4;               // tile ring depth
+
+int env_int(const char *name, int dflt, int lo, int hi) {
+  const char *v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  const int x = std::atoi(v);
+  return (x >= lo && x <= hi) ? x : dflt;
+}
 
 struct KernelCache {
   const void *fn;
   int device;
   int smem_set;
-  int cluster_ok[17];  // -1 unknown, 0 no, 1 yes
+  int C, smem, max_clusters;  // last occupancy query
 };
 std::vector<KernelCache> g_kc;
 
-int prepare_kernel(const void *fn, int smem, int *C_inout) {
+cudaLaunchConfig_t cluster_config(const void *fn, int C, int grid_clusters, int smem,
+                                  cudaStream_t stream, cudaLaunchAttribute *attr) {
+  (void)fn;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(C * grid_clusters), 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr->id = cudaLaunchAttributeClusterDimension;
+  attr->val.clusterDim.x = C;
+  attr->val.clusterDim.y = 1;
+  attr->val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Sets the kernel's attributes once per device and returns how many clusters
+// of size C with `smem` bytes can be resident at once (0: none).
+int prepare_kernel(const void *fn, int C, int smem, int *max_clusters) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -131,7 +157,7 @@ int prepare_kernel(const void *fn, int smem, int *C_inout) {
     k.fn = fn;
     k.device = dev;
     k.smem_set = -1;
-    for (int &v : k.cluster_ok) v = -1;
+    k.C = -1;
     g_kc.push_back(k);
     kc = &g_kc.back();
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -141,51 +167,22 @@ int prepare_kernel(const void *fn, int smem, int *C_inout) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
     kc->smem_set = smem;
-    for (int &v : kc->cluster_ok) v = -1;
+    kc->C = -1;
   }
-  // largest cluster size <= requested that can be resident at all
-  int C = *C_inout;
-  while (C > 1) {
-    if (kc->cluster_ok[C] < 0) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(C, 1, 1);
-      cfg.blockDim = dim3(NT, 1, 1);
-      cfg.dynamicSmemBytes = smem;
-      cudaLaunchAttribute attr;
-      attr.id = cudaLaunchAttributeClusterDimension;
-      attr.val.clusterDim.x = C;
-      attr.val.clusterDim.y = 1;
-      attr.val.clusterDim.z = 1;
-      cfg.attrs = &attr;
-      cfg.numAttrs = 1;
-      int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
-      if (e != cudaSuccess) cudaGetLastError();
-      kc->cluster_ok[C] = (e == cudaSuccess && n > 0) ? 1 : 0;
+  if (kc->C != C || kc->smem != smem) {
+    cudaLaunchAttribute attr;
+    cudaLaunchConfig_t cfg = cluster_config(fn, C, 1, smem, nullptr, &attr);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
     }
-    if (kc->cluster_ok[C] == 1) break;
-    C = C > 8 ? 8 : C / 2;
+    kc->C = C;
+    kc->smem = smem;
+    kc->max_clusters = n;
   }
-  *C_inout = std::max(C, 1);
-  return SPEC_OK;
-}
-
-int launch(const void *fn, int C, long long jobs, int smem, cudaStream_t stream, Params &p) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(C * jobs), 1, 1);
-  cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = C;
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  void *args[] = {&p};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
-  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  *max_clusters = kc->max_clusters;
   return SPEC_OK;
 }
 
@@ -207,48 +204,56 @@ const void *pick_argmax_kernel(int dtype, bool tma) {
              : reinterpret_cast<const void *>(&argmax_kernel<1, false>);
 }
 
-// Geometry of one launch: cluster size, slice, tile, stages, residency.
+// Launch geometry: cluster size C (CTAs sharing one row), slice per CTA,
+// tile, ring depth, dynamic shared memory, clusters launched.
 struct Geometry {
-  int C, slice, tile, stages, resident, smem;
+  int C, slice, tile, stages, smem, emit_off, ncl;
 };
 
-// Slices of ~16 KB per row and CTA (cluster size up to 16), tiles of
-// NT x 2 vectors, and either every tile of the slice resident in shared
-// memory (stochastic chain, up to 64 KB) or a 4-stage ring.
-int geometry_for(int C, int V, int dtype, int nrows, bool sample, int min_smem, Geometry *g) {
+// Slices of about 16 KB per row and CTA (cluster size up to 16), tiles of
+// NT threads x 2 vectors of 16 bytes, a ring of `stages` tiles (each stage
+// holds `srows` rows), then as many clusters as can be resident, capped by
+// the number of jobs.
+int plan(const void *fn, int V, int dtype, int srows, int emit_bytes, long long njobs,
+         Geometry *g) {
   const int esz = dtype == SPEC_F32 ? 4 : 2;
   const int VE = 16 / esz;
-  g->C = C;
-  g->tile = NT * VE * VECS_PER_THREAD;
-  const int per = (V + C - 1) / C;
-  g->slice = (per + VE - 1) / VE * VE;
-  const int ntile = (g->slice + g->tile - 1) / g->tile;
-  if (ntile > MAX_TILES) return fail(SPEC_ERR_ARG, "vocabulary too large");
-  if (sample) {
-    const long long bytes = static_cast<long long>(ntile) * nrows * g->tile * esz;
-    g->resident = ntile <= MAX_STAGES && bytes <= RESIDENT_LIMIT_BYTES;
-    g->stages = g->resident ? ntile : std::min(ntile, STREAM_STAGES);
-  } else {
-    g->stages = std::min(ntile, STREAM_STAGES);
-    g->resident = ntile <= g->stages;
-  }
-  g->smem = std::max(g->stages * nrows * g->tile * esz, min_smem);
-  return SPEC_OK;
-}
-
-int plan(const void *fn, int V, int dtype, int nrows, bool sample, int min_smem, Geometry *g) {
-  const int esz = dtype == SPEC_F32 ? 4 : 2;
   const long long row_bytes = static_cast<long long>(V) * esz;
   int C = static_cast<int>(std::min<long long>(
       16, std::max<long long>(1, (row_bytes + SLICE_TARGET_BYTES - 1) / SLICE_TARGET_BYTES)));
+  C = env_int("SPEC_VERIFY_CLUSTER", C, 1, 16);
+  g->stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
+  g->tile = NT * VE * VECS_PER_THREAD;
   for (;;) {
-    int st = geometry_for(C, V, dtype, nrows, sample, min_smem, g);
+    const int per = (V + C - 1) / C;
+    g->slice = (per + VE - 1) / VE * VE;
+    g->emit_off = g->stages * srows * g->tile * esz;
+    g->smem = g->emit_off + emit_bytes;
+    int maxc = 0;
+    int st = prepare_kernel(fn, C, g->smem, &maxc);
     if (st) return st;
-    int C2 = C;
-    if ((st = prepare_kernel(fn, g->smem, &C2))) return st;
-    if (C2 == C) return SPEC_OK;
-    C = C2;  // fewer CTAs per cluster fit: re-plan the slices
+    if (maxc > 0) {
+      g->C = C;
+      g->ncl = static_cast<int>(std::min<long long>(njobs, maxc));
+      return SPEC_OK;
+    }
+    if (C == 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster of this size fits on the device");
+    C = C > 8 ? 8 : C / 2;
   }
+}
+
+int launch(const void *fn, const Geometry &g, cudaStream_t stream, Params &p) {
+  cudaLaunchAttribute attr;
+  cudaLaunchConfig_t cfg = cluster_config(fn, g.C, g.ncl, g.smem, stream, &attr);
+  p.slice = g.slice;
+  p.tile = g.tile;
+  p.stages = g.stages;
+  p.ncl = g.ncl;
+  p.emit_off = g.emit_off;
+  void *args[] = {&p};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return SPEC_OK;
 }
 
 int check_common(const void *zt, int B, int V, int dtype) {
@@ -280,8 +285,9 @@ int verify_chain(const void *zt, const void *zd, const int32_t *x, int B, int K,
   const bool tma = (static_cast<long long>(V) * esz) % 16 == 0 && aligned16(zt) &&
                    (!sample || K == 0 || aligned16(zd));
   const void *fn = sample ? pick_sample_kernel(dtype, tma) : pick_argmax_kernel(dtype, tma);
+  const long long njobs = static_cast<long long>(B) * (K + 1);
   Geometry g;
-  if ((st = plan(fn, V, dtype, sample && K > 0 ? 2 : 1, sample, sample ? 0 : 8 * (2 * K + 2), &g)))
+  if ((st = plan(fn, V, dtype, sample && K > 0 ? 2 : 1, sample ? 0 : 8 * (2 * K + 2), njobs, &g)))
     return st;
   Workspace *w = nullptr;
   if ((st = get_ws(stream, B, K + 1, &w))) return st;
@@ -298,10 +304,7 @@ int verify_chain(const void *zt, const void *zd, const int32_t *x, int B, int K,
   p.kind = sample ? KIND_SAMPLE : KIND_GREEDY_CHAIN;
   p.c = static_cast<float>(cd);
   p.seed = seed;
-  p.slice = g.slice;
-  p.tile = g.tile;
-  p.stages = g.stages;
-  p.resident = g.resident;
+  p.njobs = static_cast<int>(njobs);
   p.max_depth = 0;
   p.out_tokens = out_tokens;
   p.out_n = out_n;
@@ -309,7 +312,7 @@ int verify_chain(const void *zt, const void *zd, const int32_t *x, int B, int K,
   p.out_row_sumexp = row_sumexp;
   p.stats = reinterpret_cast<Stats *>(stats);
   bind_ws(p, w);
-  return launch(fn, g.C, static_cast<long long>(B) * (K + 1), g.smem, stream, p);
+  return launch(fn, g, stream, p);
 }
 
 int tree_depth_host(const int32_t *parent, int N) {
@@ -361,8 +364,9 @@ int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent,
   const bool tma = (static_cast<long long>(V) * esz) % 16 == 0 && aligned16(target_logits);
   const int emit_smem = 17 * N + 64;
   const void *fn = pick_argmax_kernel(dtype, tma);
+  const long long njobs = static_cast<long long>(B) * N;
   Geometry g;
-  if ((st = plan(fn, V, dtype, 1, false, emit_smem, &g))) return st;
+  if ((st = plan(fn, V, dtype, 1, emit_smem, njobs, &g))) return st;
   Workspace *w = nullptr;
   if ((st = get_ws(stream, B, N, &w))) return st;
   Params p = {};
@@ -374,15 +378,12 @@ int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent,
   p.V = V;
   p.J = N;
   p.kind = KIND_TREE;
-  p.slice = g.slice;
-  p.tile = g.tile;
-  p.stages = g.stages;
-  p.resident = g.resident;
+  p.njobs = static_cast<int>(njobs);
   p.max_depth = max_depth;
   p.out_tokens = out_path;
   p.out_n = out_len;
   bind_ws(p, w);
-  return launch(fn, g.C, static_cast<long long>(B) * N, g.smem, stream, p);
+  return launch(fn, g, stream, p);
 }
 
 int spec_tree_max_depth(const int32_t *parent_host, int N) {
