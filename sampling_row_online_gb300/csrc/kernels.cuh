@@ -38,6 +38,7 @@ constexpr int NWARP = NT / 32;
 constexpr int VECS_PER_THREAD = 2;      // 16-byte vectors per thread per tile
 constexpr int MAX_STAGES = 8;
 constexpr int MAX_TILES = 64;
+constexpr int MAX_CLUSTER = 16;
 constexpr int FIRST_REJ_NONE = 0x7F7F7F7F;  // also the byte pattern the workspace is memset to
 constexpr int CAND_FALLBACK = 1 << 30;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s bound on any wait
@@ -429,10 +430,13 @@ struct SharedSmall {
   uint64_t full[MAX_STAGES];
   float red_m[2][NWARP];
   float red_s[2][NWARP];
-  // exchanged through DSMEM, double-buffered by job parity:
-  float part[2][6];   // m_t, s_t, m_d, s_d, hint (int bits), argmax index (int bits)
-  float zpart[2][2];  // slice mass, round 0 (residual) and 1 (fallback)
-  // per-job values of this CTA, double-buffered by job parity:
+  // Pushed by every CTA of the cluster into every CTA's copy (st.shared::cluster
+  // before the cluster barrier), double-buffered by job parity, so combines
+  // read local shared memory only:
+  alignas(16) float xs[2][MAX_CLUSTER][4];  // per rank: (m_t, s_t, m_d, s_d) or (max, index bits)
+  float xz[2][2][MAX_CLUSTER];              // per rank: slice mass of the draw (round 0 / 1)
+  int xhint[2];                             // rank 0: lowest rejected position seen
+  // per-job values of this CTA
   float gz[2][2];     // z_t[x], z_d[x]
   int gok[2];         // draft token in range
   float bf[8];        // broadcast floats
@@ -492,7 +496,7 @@ __device__ __forceinline__ void emit_chain_sample(const Params &p, int b) {
 // Stochastic chain: row statistics, acceptance test, residual/bonus draw.
 // ======================================================================
 template <int DT, bool TMA>
-__global__ void __launch_bounds__(NT, 2) sample_kernel(const Params p) {
+__global__ void __launch_bounds__(NT, 3) sample_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
   extern __shared__ __align__(128) unsigned char dyn[];
@@ -527,6 +531,15 @@ __global__ void __launch_bounds__(NT, 2) sample_kernel(const Params p) {
   const int E2 = ((len + NT - 1) / NT + VE - 1) / VE * VE;
   const int e0 = min(len, tid * E2), e1 = min(len, e0 + E2);
 
+  // draft token of the next job, loaded one job ahead by thread 32
+  auto token_of = [&](int q) -> int {
+    if (q >= p.njobs) return 0;
+    int b, i;
+    decode_job(p, q, b, i);
+    return i < p.K ? __ldg(p.tokens + static_cast<size_t>(b) * p.K + i) : 0;
+  };
+  int x_next = (tid == 32) ? token_of(st.cl) : 0;
+
   int seq = 0;
   for (int n = 0;; ++n) {
     const int q = st.cl + n * p.ncl;
@@ -538,25 +551,21 @@ __global__ void __launch_bounds__(NT, 2) sample_kernel(const Params p) {
     const unsigned char *rt, *rd;
     st.rows_of(q, rt, rd);
 
-    // draft token and its two logits (another warp, overlapping pass 1)
+    // draft token's two logits and the rejection hint: loads issued now by
+    // thread 32, consumed after pass 1
+    int g_ok = 1, g_hint = 0;
+    float g_zt = 0.f, g_zd = 0.f;
     if (tid == 32) {
-      int ok = 1;
-      float zx_t = 0.f, zx_d = 0.f;
+      const int x = x_next;
       if (pair) {
-        const int x = __ldg(p.tokens + static_cast<size_t>(b) * p.K + i);
-        ok = (x >= 0 && x < p.V);
-        if (ok) {
-          zx_t = E::load(rt, x);
-          zx_d = E::load(rd, x);
+        g_ok = (x >= 0 && x < p.V);
+        if (g_ok) {
+          g_zt = E::load(rt, x);
+          g_zd = E::load(rd, x);
         }
       }
-      sh.gok[par] = ok;
-      sh.gz[par][0] = zx_t;
-      sh.gz[par][1] = zx_d;
-      if (rank == 0) {  // lowest rejected position already published
-        const int hint = *reinterpret_cast<volatile int *>(p.first_rej + b);
-        sh.part[par][4] = __int_as_float(hint);
-      }
+      if (rank == 0) g_hint = *reinterpret_cast<volatile int *>(p.first_rej + b);
+      x_next = token_of(q + p.ncl);
     }
 
     // ---- pass 1: online max / sum-exp of both rows of this slice
@@ -587,11 +596,16 @@ __global__ void __launch_bounds__(NT, 2) sample_kernel(const Params p) {
     }
     block_reduce_ms(mt, s_t, c, sh.red_m[0], sh.red_s[0]);
     if (pair) block_reduce_ms(md, s_d, c, sh.red_m[1], sh.red_s[1]);
-    if (tid == 0) {
-      sh.part[par][0] = mt;
-      sh.part[par][1] = s_t;
-      sh.part[par][2] = md;
-      sh.part[par][3] = s_d;
+    if (tid < 32) {  // push this slice's statistics into every CTA of the cluster
+      const float a0 = __shfl_sync(0xFFFFFFFFu, mt, 0), a1 = __shfl_sync(0xFFFFFFFFu, s_t, 0);
+      const float a2 = __shfl_sync(0xFFFFFFFFu, md, 0), a3 = __shfl_sync(0xFFFFFFFFu, s_d, 0);
+      if (tid < static_cast<int>(C)) dsmem_st_v4f32(dsmem_addr(&sh.xs[par][rank][0], tid), a0, a1, a2, a3);
+    } else if (tid == 32) {
+      sh.gok[par] = g_ok;
+      sh.gz[par][0] = g_zt;
+      sh.gz[par][1] = g_zd;
+      if (rank == 0)
+        for (uint32_t r = 0; r < C; ++r) dsmem_st_s32(dsmem_addr(&sh.xhint[par], r), g_hint);
     }
     cluster_sync();  // partial statistics of job n visible cluster-wide
 
@@ -599,13 +613,10 @@ __global__ void __launch_bounds__(NT, 2) sample_kernel(const Params p) {
     if (tid == 0) {
       float Mt = -INFINITY, St = 0.f, Md = -INFINITY, Sd = 0.f;
       for (uint32_t r = 0; r < C; ++r) {
-        ms_combine(Mt, St, dsmem_ld_f32(dsmem_addr(&sh.part[par][0], r)),
-                   dsmem_ld_f32(dsmem_addr(&sh.part[par][1], r)), c);
-        if (pair)
-          ms_combine(Md, Sd, dsmem_ld_f32(dsmem_addr(&sh.part[par][2], r)),
-                     dsmem_ld_f32(dsmem_addr(&sh.part[par][3], r)), c);
+        ms_combine(Mt, St, sh.xs[par][r][0], sh.xs[par][r][1], c);
+        if (pair) ms_combine(Md, Sd, sh.xs[par][r][2], sh.xs[par][r][3], c);
       }
-      const int hint = __float_as_int(dsmem_ld_f32(dsmem_addr(&sh.part[par][4], 0)));
+      const int hint = sh.xhint[par];
       const int ok = sh.gok[par];
       int accept = 1;
       if (pair && ok) {
@@ -658,6 +669,7 @@ __global__ void __launch_bounds__(NT, 2) sample_kernel(const Params p) {
       for (int round = 0; round < 2; ++round) {
         sum = 0.f;
         if (TMA) {
+#pragma unroll 4
           for (int e = e0; e < e1; e += VE) {
             const size_t off = static_cast<size_t>(lo + e) * E::BYTES;
             float ft[VE], fd[VE];
@@ -672,11 +684,11 @@ __global__ void __launch_bounds__(NT, 2) sample_kernel(const Params p) {
         }
         float total;
         excl = block_exclusive_scan(sum, sh.fscratch, &total);
-        if (tid == 0) sh.zpart[par][round] = total;
+        if (tid < static_cast<int>(C)) dsmem_st_f32(dsmem_addr(&sh.xz[par][round][rank], tid), total);
         cluster_sync();  // slice masses visible cluster-wide
         if (tid == 0) {
           float Z = 0.f;
-          for (uint32_t r = 0; r < C; ++r) Z += dsmem_ld_f32(dsmem_addr(&sh.zpart[par][round], r));
+          for (uint32_t r = 0; r < C; ++r) Z += sh.xz[par][round][r];
           int again = 0;
           if (W.resid && !(Z > 0.f)) {
             again = 1;  // no residual mass in fp32: draw from p at this position
@@ -686,7 +698,7 @@ __global__ void __launch_bounds__(NT, 2) sample_kernel(const Params p) {
             float P = 0.f, Pown = 0.f, Plast = 0.f;
             int own = -1, last = -1;
             for (uint32_t r = 0; r < C; ++r) {
-              const float zr = dsmem_ld_f32(dsmem_addr(&sh.zpart[par][round], r));
+              const float zr = sh.xz[par][round][r];
               if (own < 0 && P + zr > t) {
                 own = static_cast<int>(r);
                 Pown = P;
@@ -735,21 +747,25 @@ __global__ void __launch_bounds__(NT, 2) sample_kernel(const Params p) {
           who = block_reduce_max_int(sum > 0.f ? tid : -1, sh.scratch);
           if (who < 0) who = 0;
         }
-        if (tid == who) {
-          float run = 0.f;
-          int pick = -1;
-          for (int e = e0; e < e1; ++e) {
-            const float w = W(E::load(rt, lo + e), W.resid ? E::load(rd, lo + e) : 0.f);
-            run = __fadd_rn(run, w);
-            if (w > 0.f) {
-              if (!pl && __fadd_rn(excl, run) > tl) {
-                pick = e;
-                break;
-              }
-              pick = e;
-            }
-          }
-          if (pick < 0) pick = e0;
+        // the whole CTA walks the chosen chunk: one entry per thread, a block
+        // scan, and the first entry whose running mass passes tl
+        const int w0 = min(len, who * E2), w1 = min(len, w0 + E2);
+        const float wexcl = __shfl_sync(0xFFFFFFFFu, excl, who & 31);
+        if ((tid & 31) == 0) sh.fscratch[tid >> 5] = wexcl;
+        __syncthreads();
+        const float base = sh.fscratch[who >> 5];
+        __syncthreads();
+        float w = 0.f;
+        const int e = w0 + tid;
+        if (e < w1) w = W(E::load(rt, lo + e), W.resid ? E::load(rd, lo + e) : 0.f);
+        float tot_unused;
+        const float before = block_exclusive_scan(w, sh.fscratch, &tot_unused);
+        const float run = __fadd_rn(base, __fadd_rn(before, w));
+        int pick = INT_MAX;
+        if (!pl) pick = block_reduce_min_int((w > 0.f && run > tl) ? e : INT_MAX, sh.scratch);
+        if (pick == INT_MAX) pick = block_reduce_max_int(w > 0.f ? e : -1, sh.scratch);
+        if (pick < 0) pick = w0;
+        if (tid == 0) {
           p.cand[static_cast<size_t>(b) * p.J + i] = (lo + pick) | (fallback ? CAND_FALLBACK : 0);
           __threadfence();
         }
@@ -771,7 +787,7 @@ __global__ void __launch_bounds__(NT, 2) sample_kernel(const Params p) {
 // Greedy chain (T = 0) and greedy tree: per-row argmax, then the walk.
 // ======================================================================
 template <int DT, bool TMA>
-__global__ void __launch_bounds__(NT, 2) argmax_kernel(const Params p) {
+__global__ void __launch_bounds__(NT, 3) argmax_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
   extern __shared__ __align__(128) unsigned char dyn[];
@@ -834,18 +850,14 @@ __global__ void __launch_bounds__(NT, 2) argmax_kernel(const Params p) {
       st.release(seq);
     }
     block_reduce_argmax(best, bidx, sh.fscratch, sh.scratch);
-    if (tid == 0) {
-      sh.part[par][0] = best;
-      sh.part[par][5] = __int_as_float(bidx);
-    }
+    if (tid == 0)  // push this slice's (max, index) into rank 0
+      dsmem_st_v4f32(dsmem_addr(&sh.xs[par][rank][0], 0), best, __int_as_float(bidx), 0.f, 0.f);
     cluster_sync();  // partial maxima of job n visible cluster-wide
     if (rank != 0) continue;
     if (tid == 0) {
       float v = -INFINITY;
       int idx = INT_MAX;
-      for (uint32_t r = 0; r < C; ++r)
-        am_combine(v, idx, dsmem_ld_f32(dsmem_addr(&sh.part[par][0], r)),
-                   __float_as_int(dsmem_ld_f32(dsmem_addr(&sh.part[par][5], r))));
+      for (uint32_t r = 0; r < C; ++r) am_combine(v, idx, sh.xs[par][r][0], __float_as_int(sh.xs[par][r][1]));
       if (idx == INT_MAX) idx = 0;  // every logit is -inf: first index
       p.cand[static_cast<size_t>(b) * p.J + i] = idx;
       if (p.kind == KIND_GREEDY_CHAIN) {

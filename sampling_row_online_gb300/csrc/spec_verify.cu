@@ -227,6 +227,9 @@ int plan(const void *fn, int V, int dtype, int srows, int emit_bytes, long long 
   for (;;) {
     const int per = (V + C - 1) / C;
     g->slice = (per + VE - 1) / VE * VE;
+    // the draw's per-thread chunk must fit one block-wide pass (slice <= NT^2)
+    if (g->slice > NT * NT || (g->slice + g->tile - 1) / g->tile > MAX_TILES * 64)
+      return fail(SPEC_ERR_ARG, "vocabulary too large (V <= 1048576)");
     g->emit_off = g->stages * srows * g->tile * esz;
     g->smem = g->emit_off + emit_bytes;
     int maxc = 0;
