@@ -316,11 +316,12 @@ def run_gpu(args, w):
         return 0
 
     peak, peak_kind = _peaks()
-    kernel = "argmax_kernel" if (w.kind == "tree" or w.T == 0) else "sample_kernel"
+    kernel = "row_kernel"
     achieved = w.algorithmic_bytes / (avg_launch_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                 "traffic": _profile_traffic(kernel, w.name), "kernel": kernel,
+                "timed": "whole call (row_kernel + decision kernel), events around each call",
                 "algorithmic_bytes_per_launch": w.algorithmic_bytes,
                 "avg_launch_us": avg_launch_ms * 1e3}
     # CPU baseline: the oracle as it stands on the host cores, bounded sample

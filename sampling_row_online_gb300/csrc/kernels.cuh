@@ -1,18 +1,29 @@
 // Verification kernels for sm_103a.
 //
-// One thread-block cluster per "job", one job per logit row (or row pair):
-//   chain, T > 0 : job i < K reads target row i and draft row i together,
-//                  job K reads the bonus target row K;
-//   chain, T = 0 : job i reads target row i (argmax only);
-//   tree         : job n reads target row n (argmax only).
-// The C CTAs of a cluster split the vocabulary into C slices; each CTA
-// streams its slice from HBM into shared memory with TMA bulk copies
-// (cp.async.bulk + mbarrier), reduces it, and the cluster combines the
-// partial results through distributed shared memory.  Everything a job
-// needs after the row statistics (the acceptance test, the residual or bonus
-// draw) runs on the data still held on chip, so each logit is read from HBM
-// once.  The last job of a sequence to finish (an atomic ticket) writes the
-// sequence's outputs.
+// Two launches per call, back to back on the caller's stream:
+//
+//  A. row_kernel — a streaming reduction over every logit row the step needs.
+//     Work item = (job, vocabulary slice): a job is a target/draft row pair
+//     (stochastic chain, positions i < K), the bonus target row K, or one
+//     target row (greedy chain, tree).  Persistent CTAs take items round-robin
+//     and stream their tiles from HBM into shared memory with TMA bulk copies
+//     (cp.async.bulk + one mbarrier per stage) through a ring that runs across
+//     item boundaries.  Each item ends in one 16-byte partial: (max, sum of
+//     2^((z - max) log2e / T)) for both rows, or (max, first index of max).
+//     No CTA ever waits for another.
+//
+//  B. draw_kernel (stochastic chain) — one thread-block cluster per sequence.
+//     Every CTA combines the partials of all 2K+1 rows (fixed order, so every
+//     CTA holds the same bits), takes the K acceptance decisions left to
+//     right, and the cluster draws the single token the sequence needs: the
+//     residual at the first reject, or the bonus from row K.  The draw
+//     re-reads one row pair (L2-resident when possible) split over the
+//     cluster: per-thread chunk masses, a block scan, slice masses pushed to
+//     every CTA through distributed shared memory, the owner slice, and a
+//     block-wide walk of the owner chunk.  The owner CTA writes the outputs.
+//
+//     finish_kernel (greedy chain, tree) — one CTA per sequence: argmax per
+//     row from the partials, then the left-to-right match or the tree walk.
 //
 // Method (pages cited by title and section):
 //   blog.oscine.io "投机解码：让大模型「猜」着跑的数学魔术":
@@ -37,10 +48,7 @@ constexpr int NT = 256;                 // threads per CTA
 constexpr int NWARP = NT / 32;
 constexpr int VECS_PER_THREAD = 2;      // 16-byte vectors per thread per tile
 constexpr int MAX_STAGES = 8;
-constexpr int MAX_TILES = 64;
 constexpr int MAX_CLUSTER = 16;
-constexpr int FIRST_REJ_NONE = 0x7F7F7F7F;  // also the byte pattern the workspace is memset to
-constexpr int CAND_FALLBACK = 1 << 30;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s bound on any wait
 
 // device status bits (per stream)
@@ -61,22 +69,18 @@ struct Params {
   int kind;
   float c;                  // log2(e) / T
   uint64_t seed;
-  int slice;                // vocabulary elements per CTA (multiple of the vector width)
+  int C;                    // vocabulary slices per row (= cluster size of the draw)
+  int slice;                // elements per slice (multiple of the vector width)
   int tile;                 // elements per tile and row
   int stages;               // shared-memory stages of the tile ring
-  int ncl;                  // clusters launched (persistent)
-  int njobs;                // jobs in total
-  int emit_off;             // byte offset of the emission scratch in dynamic smem
+  int njobs;                // jobs in total; items = njobs * C
   int max_depth;            // tree output width - 1
+  float4 *partials;         // [njobs * C]
   int32_t *out_tokens;      // chain [B, K+1]; tree [B, max_depth+1]
   int32_t *out_n;           // chain n_accepted [B]; tree length [B]
   float *out_row_max;       // [B, 2K+1] or null
   float *out_row_sumexp;    // [B, 2K+1] or null
   Stats *stats;             // or null
-  int32_t *ticket;          // [B] jobs finished (reset by the last one)
-  int32_t *first_rej;       // [B] lowest rejected position (reset by the last job)
-  int32_t *seq_err;         // [B] error flags (reset by the last job)
-  int32_t *cand;            // [B, J] per-job result token
   int32_t *status;          // device status bits
 };
 
@@ -133,6 +137,8 @@ struct Elem<1> {  // bfloat16: the upper half of an fp32
 
 // ------------------------------------------------------------- reductions
 // (max, sum of 2^((z - max) c)) pairs; an empty side has max = -inf, sum = 0.
+// Commutative bit for bit (IEEE + and * are), so butterfly reductions give
+// the same bits in every lane.
 __device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s2, float c) {
   const float M = fmaxf(m, m2);
   if (M == -INFINITY) {
@@ -140,12 +146,31 @@ __device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s
     s = 0.f;
     return;
   }
-  s = s * ex2((m - M) * c) + s2 * ex2((m2 - M) * c);
+  s = __fadd_rn(__fmul_rn(s, ex2((m - M) * c)), __fmul_rn(s2, ex2((m2 - M) * c)));
   m = M;
 }
 
+// Online (max, sum 2^((z - max) c)) over one vector of logits.
+template <int VE>
+__device__ __forceinline__ void online_vec(const float (&f)[VE], float c, float &m, float &s,
+                                           float &mc) {
+  float vm = f[0];
+#pragma unroll
+  for (int k = 1; k < VE; ++k) vm = fmaxf(vm, f[k]);
+  if (vm > m) {
+    s *= ex2((m - vm) * c);
+    m = vm;
+    mc = m * c;
+  }
+  if (m > -INFINITY) {
+    float a = 0.f;
+#pragma unroll
+    for (int k = 0; k < VE; ++k) a += ex2(fmaf(f[k], c, -mc));
+    s += a;
+  }
+}
+
 // Block-wide (max, sumexp) reduction; the result is valid in thread 0.
-// Fixed combination order, so the result is deterministic.
 __device__ __forceinline__ void block_reduce_ms(float &m, float &s, float c, float *sh_m,
                                                 float *sh_s) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -168,22 +193,8 @@ __device__ __forceinline__ void block_reduce_ms(float &m, float &s, float c, flo
   __syncthreads();
 }
 
-__device__ __forceinline__ float block_reduce_sum(float v, float *sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_down_sync(0xFFFFFFFFu, v, off);
-  if (lane == 0) sh[warp] = v;
-  __syncthreads();
-  float r = 0.f;
-  if (threadIdx.x == 0) {
-    r = sh[0];
-    for (int w = 1; w < NWARP; ++w) r += sh[w];
-  }
-  __syncthreads();
-  return r;
-}
-
 // (value, index) maximum with ties to the lower index; index INT_MAX = none.
+// Commutative.
 __device__ __forceinline__ void am_combine(float &v, int &i, float v2, int i2) {
   if (v2 > v || (v2 == v && i2 < i)) {
     v = v2;
@@ -258,19 +269,10 @@ __device__ __forceinline__ float block_exclusive_scan(float v, float *sh, float 
   return excl;
 }
 
-// -------------------------------------------------------- job stream
-// The kernels are persistent: cluster `cl` handles jobs q = cl, cl + ncl,
-// cl + 2 ncl, ...  Every CTA of the cluster streams the tiles of its
-// vocabulary slice of those jobs, in order, through a ring of S shared-memory
-// stages, so the copies of the next job are in flight while the current job
-// is combined and decided.  TMA path: thread 0 issues one bulk copy per row
-// and tile, one mbarrier per stage tracks completion.  Plain path (rows not
-// 16-byte aligned): all threads copy element by element and pad the last
-// vector with -inf.
-
+// ------------------------------------------------------------ job layout
 // Job q -> (sequence b, row i).  Stochastic chain: the K row pairs in
-// position-major order (so earlier positions of a sequence tend to be decided
-// first), then the K+1-th target rows.  Argmax kinds: rows position-major.
+// position-major order, then the K+1-th target rows.  Argmax kinds: rows
+// position-major.
 __device__ __forceinline__ void decode_job(const Params &p, int q, int &b, int &i) {
   if (p.kind == KIND_SAMPLE) {
     const int npair = p.B * p.K;
@@ -287,133 +289,221 @@ __device__ __forceinline__ void decode_job(const Params &p, int q, int &b, int &
   }
 }
 
-template <int DT, bool TMA>
-struct Stream {
+__device__ __forceinline__ int job_of(const Params &p, int b, int i) {
+  if (p.kind == KIND_SAMPLE && i == p.K) return p.B * p.K + b;
+  return i * p.B + b;
+}
+
+template <int DT>
+__device__ __forceinline__ const unsigned char *target_row(const Params &p, int b, int i) {
+  return static_cast<const unsigned char *>(p.zt) +
+         (static_cast<size_t>(b) * p.J + i) * p.V * Elem<DT>::BYTES;
+}
+
+template <int DT>
+__device__ __forceinline__ const unsigned char *draft_row(const Params &p, int b, int i) {
+  return static_cast<const unsigned char *>(p.zd) +
+         (static_cast<size_t>(b) * p.K + i) * p.V * Elem<DT>::BYTES;
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ======================================================================
+// A. row_kernel: streaming per-(job, slice) statistics.
+// ======================================================================
+// Item it = job * C + slice; a CTA takes items blockIdx.x, + gridDim.x, ...
+// and streams their tiles through a ring of `stages` shared-memory stages
+// (each stage holds one tile of up to two rows).
+template <int DT, bool ARGMAX>
+struct ItemCursor {
   using E = Elem<DT>;
-  const Params *p;
-  unsigned char *buf;
-  uint64_t *full;
-  int cl, lo, len, nt, S, srows;
-  bool timed_out;
+  int item, k, nt, lo, len, nrows, tile;
+  const unsigned char *rt, *rd;
 
-  __device__ __forceinline__ int tile_len(int k) const { return min(p->tile, len - k * p->tile); }
-  __device__ __forceinline__ unsigned char *stage_row(int s, int r) const {
-    return buf + static_cast<size_t>(s * srows + r) * p->tile * E::BYTES;
-  }
-  // target and (for a pair) draft row of job q; returns the row count
-  __device__ __forceinline__ int rows_of(int q, const unsigned char *&rt,
-                                         const unsigned char *&rd) const {
+  __device__ __forceinline__ void set(const Params &p, int it) {
+    item = it;
+    k = 0;
+    tile = p.tile;
+    if (it >= p.njobs * p.C) {
+      nt = 0;
+      return;
+    }
+    const int q = it / p.C, s = it - q * p.C;
+    lo = s * p.slice;
+    len = max(0, min(p.V, lo + p.slice) - lo);
+    nt = (len + p.tile - 1) / p.tile;
     int b, i;
-    decode_job(*p, q, b, i);
-    rt = static_cast<const unsigned char *>(p->zt) +
-         (static_cast<size_t>(b) * p->J + i) * p->V * E::BYTES;
-    if (p->kind == KIND_SAMPLE && i < p->K) {
-      rd = static_cast<const unsigned char *>(p->zd) +
-           (static_cast<size_t>(b) * p->K + i) * p->V * E::BYTES;
-      return 2;
-    }
-    rd = nullptr;
-    return 1;
-  }
-
-  // TMA, thread 0: issue tile `seq` of this CTA's stream, if it exists.
-  __device__ __forceinline__ void produce(int seq) {
-    if (nt == 0) return;
-    const int n = seq / nt, k = seq - n * nt;
-    const int q = cl + n * p->ncl;
-    if (q >= p->njobs) return;
-    const unsigned char *rt, *rd;
-    const int nr = rows_of(q, rt, rd);
-    const int s = seq % S;
-    const uint32_t bytes = static_cast<uint32_t>(tile_len(k)) * E::BYTES;
-    const size_t off = (static_cast<size_t>(lo) + static_cast<size_t>(k) * p->tile) * E::BYTES;
-    mbar_arrive_expect_tx(&full[s], bytes * nr);
-    bulk_g2s(stage_row(s, 0), rt + off, bytes, &full[s]);
-    if (nr == 2) bulk_g2s(stage_row(s, 1), rd + off, bytes, &full[s]);
-  }
-
-  __device__ __forceinline__ void prologue() {
-    if (TMA && threadIdx.x == 0)
-      for (int s = 0; s < S; ++s) produce(s);
-  }
-
-  // Every thread: tile `seq` (tile k of the current job, rows rt/rd) is in
-  // stage seq % S on return.
-  __device__ __forceinline__ void acquire(int seq, int k, const unsigned char *rt,
-                                          const unsigned char *rd) {
-    const int s = seq % S;
-    if (TMA) {
-      const uint32_t par = static_cast<uint32_t>(seq / S) & 1u;
-      if (!mbar_try_wait(&full[s], par)) {
-        const uint64_t t0 = clock_ns();
-        while (!mbar_try_wait(&full[s], par)) {
-          if (clock_ns() - t0 > WAIT_LIMIT_NS) {
-            timed_out = true;
-            break;
-          }
-        }
-      }
+    decode_job(p, q, b, i);
+    rt = target_row<DT>(p, b, i) + static_cast<size_t>(lo) * E::BYTES;
+    if (!ARGMAX && i < p.K) {
+      rd = draft_row<DT>(p, b, i) + static_cast<size_t>(lo) * E::BYTES;
+      nrows = 2;
     } else {
-      __syncthreads();
-      const int n = tile_len(k);
-      const int npad = (n + E::VE - 1) / E::VE * E::VE;
-      const size_t off = (static_cast<size_t>(lo) + static_cast<size_t>(k) * p->tile) * E::BYTES;
-      for (int r = 0; r < (rd ? 2 : 1); ++r) {
-        const unsigned char *g = (r ? rd : rt) + off;
-        unsigned char *d = stage_row(s, r);
-        for (int e = threadIdx.x; e < npad; e += NT) {
-          if (e < n)
-            E::copy_elem(d + e * E::BYTES, g + e * E::BYTES);
-          else
-            E::store_neg_inf(d + e * E::BYTES);
-        }
-      }
-      __syncthreads();
+      rd = nullptr;
+      nrows = 1;
     }
   }
-
-  // After every thread consumed tile `seq`: refill its stage with tile seq + S.
-  __device__ __forceinline__ void release(int seq) {
-    if (TMA) {
-      __syncthreads();
-      if (threadIdx.x == 0) produce(seq + S);
-    }
-  }
-
-  // Bounded drain of copies that may still be in flight after a timeout.
-  __device__ __forceinline__ void drain_after_timeout(int seq_end) {
-    if (!TMA) return;
-    const uint64_t t0 = clock_ns();
-    for (int seq = seq_end; seq < seq_end + S; ++seq)
-      while (!mbar_try_wait(&full[seq % S], static_cast<uint32_t>(seq / S) & 1u) &&
-             clock_ns() - t0 < WAIT_LIMIT_NS) {
-      }
-  }
+  __device__ __forceinline__ int tile_len(int kk) const { return min(tile, len - kk * tile); }
 };
 
-// Online (max, sum 2^((z - max) c)) over one vector of logits.
-template <int VE>
-__device__ __forceinline__ void online_update(const float (&f)[VE], float c, float &m, float &s,
-                                              float &mc) {
-  float vm = f[0];
-#pragma unroll
-  for (int k = 1; k < VE; ++k) vm = fmaxf(vm, f[k]);
-  if (vm > m) {
-    s *= ex2((m - vm) * c);
-    m = vm;
-    mc = m * c;
+template <int DT, bool TMA, bool ARGMAX>
+__global__ void __launch_bounds__(NT, 3) row_kernel(const Params p) {
+  using E = Elem<DT>;
+  constexpr int VE = E::VE;
+  constexpr int SROWS = ARGMAX ? 1 : 2;
+  extern __shared__ __align__(128) unsigned char dyn[];
+  __shared__ uint64_t full[MAX_STAGES];
+  __shared__ float red_a[2][NWARP], red_b[2][NWARP];
+  __shared__ int red_i[NWARP];
+
+  const int tid = threadIdx.x;
+  const int S = p.stages;
+  const int nitems = p.njobs * p.C;
+  const float c = p.c;
+  const size_t stage_bytes = static_cast<size_t>(SROWS) * p.tile * E::BYTES;
+  auto stage_row = [&](int s, int r) -> unsigned char * {
+    return dyn + static_cast<size_t>(s) * stage_bytes + static_cast<size_t>(r) * p.tile * E::BYTES;
+  };
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    fence_mbar_init();
   }
-  if (m > -INFINITY) {
-    float a = 0.f;
+  __syncthreads();
+
+  // producer cursor (thread 0 only): issues the next tile of this CTA's stream
+  ItemCursor<DT, ARGMAX> pc;
+  pc.item = nitems;
+  pc.k = pc.nt = 0;
+  int pseq = 0;
+  auto produce_one = [&]() {
+    while (pc.k >= pc.nt) {
+      if (pc.item >= nitems) return;
+      pc.set(p, pc.item + gridDim.x);
+    }
+    const int s = pseq % S;
+    const uint32_t bytes = static_cast<uint32_t>(pc.tile_len(pc.k)) * E::BYTES;
+    const size_t off = static_cast<size_t>(pc.k) * p.tile * E::BYTES;
+    mbar_arrive_expect_tx(&full[s], bytes * pc.nrows);
+    bulk_g2s(stage_row(s, 0), pc.rt + off, bytes, &full[s]);
+    if (pc.nrows == 2) bulk_g2s(stage_row(s, 1), pc.rd + off, bytes, &full[s]);
+    ++pc.k;
+    ++pseq;
+  };
+  if (TMA && tid == 0) {
+    pc.set(p, blockIdx.x);
+    for (int s = 0; s < S; ++s) produce_one();
+  }
+
+  bool timed_out = false;
+  int seq = 0;
+  ItemCursor<DT, ARGMAX> cc;
+  for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+    cc.set(p, it);
+    float a0 = -INFINITY, a1 = 0.f, a2 = -INFINITY, a3 = 0.f;  // (m_t, s_t, m_d, s_d)
+    float ac0 = 0.f, ac2 = 0.f;                                // m * c
+    int aidx = INT_MAX;                                        // argmax index
+    for (int k = 0; k < cc.nt; ++k, ++seq) {
+      const int s = seq % S;
+      const int n = cc.tile_len(k);
+      if (TMA) {
+        const uint32_t par = static_cast<uint32_t>(seq / S) & 1u;
+        if (!mbar_try_wait(&full[s], par)) {
+          const uint64_t t0 = clock_ns();
+          while (!mbar_try_wait(&full[s], par)) {
+            if (clock_ns() - t0 > WAIT_LIMIT_NS) {
+              timed_out = true;
+              break;
+            }
+          }
+        }
+      } else {
+        __syncthreads();
+        const int npad = (n + VE - 1) / VE * VE;
+        const size_t off = static_cast<size_t>(k) * p.tile * E::BYTES;
+        for (int r = 0; r < cc.nrows; ++r) {
+          const unsigned char *g = (r ? cc.rd : cc.rt) + off;
+          unsigned char *d = stage_row(s, r);
+          for (int e = tid; e < npad; e += NT) {
+            if (e < n)
+              E::copy_elem(d + e * E::BYTES, g + e * E::BYTES);
+            else
+              E::store_neg_inf(d + e * E::BYTES);
+          }
+        }
+        __syncthreads();
+      }
+      const int nv = (n + VE - 1) / VE;
+      const unsigned char *bt = stage_row(s, 0);
+      if (ARGMAX) {
+        const int base = cc.lo + k * p.tile;
+        for (int j = tid; j < nv; j += NT) {
+          float f[VE];
+          E::unpack(lds128(bt + j * 16), f);
+          float vm = f[0];
 #pragma unroll
-    for (int k = 0; k < VE; ++k) a += ex2(fmaf(f[k], c, -mc));
-    s += a;
+          for (int e = 1; e < VE; ++e) vm = fmaxf(vm, f[e]);
+          if (vm > a0) {  // rare after the first few vectors
+            a0 = vm;
+#pragma unroll
+            for (int e = VE - 1; e >= 0; --e)
+              if (f[e] == vm) aidx = base + j * VE + e;
+          }
+        }
+      } else if (cc.nrows == 2) {
+        const unsigned char *bd = stage_row(s, 1);
+        for (int j = tid; j < nv; j += NT) {
+          float f[VE];
+          E::unpack(lds128(bt + j * 16), f);
+          online_vec<VE>(f, c, a0, a1, ac0);
+          E::unpack(lds128(bd + j * 16), f);
+          online_vec<VE>(f, c, a2, a3, ac2);
+        }
+      } else {
+        for (int j = tid; j < nv; j += NT) {
+          float f[VE];
+          E::unpack(lds128(bt + j * 16), f);
+          online_vec<VE>(f, c, a0, a1, ac0);
+        }
+      }
+      if (TMA) {
+        __syncthreads();  // stage s fully consumed
+        if (tid == 0) produce_one();
+      }
+    }
+    // item partial
+    if (ARGMAX) {
+      block_reduce_argmax(a0, aidx, red_a[0], red_i);
+      if (tid == 0) p.partials[it] = make_float4(a0, __int_as_float(aidx), 0.f, 0.f);
+    } else {
+      block_reduce_ms(a0, a1, c, red_a[0], red_b[0]);
+      if (cc.nrows == 2) block_reduce_ms(a2, a3, c, red_a[1], red_b[1]);
+      if (tid == 0) p.partials[it] = make_float4(a0, a1, a2, a3);
+    }
+  }
+  pdl_launch_dependents();
+  if (timed_out) {
+    atomicOr(p.status, ST_TIMEOUT);
+    // bounded drain of any copy still in flight
+    if (TMA && tid == 0) {
+      const uint64_t t0 = clock_ns();
+      for (int q = seq; q < seq + S; ++q)
+        while (!mbar_try_wait(&full[q % S], static_cast<uint32_t>(q / S) & 1u) &&
+               clock_ns() - t0 < WAIT_LIMIT_NS) {
+        }
+    }
   }
 }
 
-// Weight of one vocabulary entry in the second pass: the residual
-// max(0, p - q) of a rejected pair, or the unnormalised p of a draw from p.
-// Explicit roundings, so the summation and the search compute identical bits.
+// ======================================================================
+// B. draw_kernel: decisions and the one draw of each sequence.
+// ======================================================================
+// Weight of one vocabulary entry in the draw: the residual max(0, p - q) of a
+// rejected pair, or the unnormalised p of a draw from p.  Explicit roundings,
+// so the summation and the walk compute identical bits.
 struct Weights {
   float c, mtc, mdc, inv_st, inv_sd;
   bool resid;
@@ -425,543 +515,358 @@ struct Weights {
   }
 };
 
-// --------------------------------------------------------- shared state
-struct SharedSmall {
-  uint64_t full[MAX_STAGES];
-  float red_m[2][NWARP];
-  float red_s[2][NWARP];
-  // Pushed by every CTA of the cluster into every CTA's copy (st.shared::cluster
-  // before the cluster barrier), double-buffered by job parity, so combines
-  // read local shared memory only:
-  alignas(16) float xs[2][MAX_CLUSTER][4];  // per rank: (m_t, s_t, m_d, s_d) or (max, index bits)
-  float xz[2][2][MAX_CLUSTER];              // per rank: slice mass of the draw (round 0 / 1)
-  int xhint[2];                             // rank 0: lowest rejected position seen
-  // per-job values of this CTA
-  float gz[2][2];     // z_t[x], z_d[x]
-  int gok[2];         // draft token in range
-  float bf[8];        // broadcast floats
-  int bi[8];          // broadcast ints
+struct DrawShared {
+  float xz[2][MAX_CLUSTER];  // slice masses pushed by every CTA (round 0 / 1)
+  float bf[8];
+  int bi[8];
   int scratch[NWARP];
   float fscratch[NWARP + 1];
 };
 
-// Ticket of sequence b: true in every thread of the CTA that finished the
-// sequence's last job.  Call from every thread of one CTA.
-__device__ __forceinline__ bool take_ticket(const Params &p, int b, SharedSmall &sh) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const int old = atomicAdd(&p.ticket[b], 1);
-    sh.bi[7] = (old == p.J - 1);
-    if (old == p.J - 1) __threadfence();
+// Combined (max, sumexp) of one row from its C slice partials, by warp:
+// lane s < C holds slice s; butterfly, so every lane ends with the same bits.
+__device__ __forceinline__ void warp_row_stats(const float4 *parts, int C, bool draft, float c,
+                                               float &m, float &s) {
+  const int lane = threadIdx.x & 31;
+  m = -INFINITY;
+  s = 0.f;
+  if (lane < C) {
+    const float4 v = __ldcg(parts + lane);
+    m = draft ? v.z : v.x;
+    s = draft ? v.w : v.y;
   }
-  __syncthreads();
-  return sh.bi[7] != 0;
-}
-
-// Outputs of stochastic-chain sequence b, once all its jobs are done.
-__device__ __forceinline__ void emit_chain_sample(const Params &p, int b) {
-  const int err = __ldcg(p.seq_err + b);
-  const int n = min(__ldcg(p.first_rej + b), p.K);
-  const int cn = __ldcg(p.cand + static_cast<size_t>(b) * p.J + n);
-  for (int e = threadIdx.x; e <= p.K; e += NT) {
-    int v = -1;
-    if (!err) {
-      if (e < n)
-        v = __ldg(p.tokens + static_cast<size_t>(b) * p.K + e);
-      else if (e == n)
-        v = cn & ~CAND_FALLBACK;
-    }
-    p.out_tokens[static_cast<size_t>(b) * (p.K + 1) + e] = v;
-  }
-  if (threadIdx.x == 0) {
-    p.out_n[b] = err ? -1 : n;
-    if (p.stats) {
-      if (err) {
-        atomicAdd(&p.stats->errors, 1ull);
-      } else {
-        atomicAdd(&p.stats->sequences, 1ull);
-        atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(n));
-        atomicAdd(n == p.K ? &p.stats->bonus : &p.stats->resampled, 1ull);
-        if (n < p.K && (cn & CAND_FALLBACK)) atomicAdd(&p.stats->residual_fallbacks, 1ull);
-      }
-    }
-    p.ticket[b] = 0;
-    p.first_rej[b] = FIRST_REJ_NONE;
-    p.seq_err[b] = 0;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, off);
+    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, off);
+    ms_combine(m, s, m2, s2, c);
   }
 }
 
-// ======================================================================
-// Stochastic chain: row statistics, acceptance test, residual/bonus draw.
-// ======================================================================
 template <int DT, bool TMA>
-__global__ void __launch_bounds__(NT, 3) sample_kernel(const Params p) {
+__global__ void __launch_bounds__(NT) draw_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
-  extern __shared__ __align__(128) unsigned char dyn[];
-  __shared__ SharedSmall sh;
+  extern __shared__ __align__(16) float dsh[];  // row max [R], row sumexp [R], logits at x [2K], ok [K]
+  __shared__ DrawShared sh;
 
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_rank();
   const uint32_t C = cluster_size();
+  const int b = blockIdx.x / C;
+  const int K = p.K;
+  const int R = 2 * K + 1;
   const float c = p.c;
+  float *rmax = dsh, *rsum = dsh + R, *gx = dsh + 2 * R;
+  int *gok = reinterpret_cast<int *>(dsh + 2 * R + 2 * K);
 
-  Stream<DT, TMA> st;
-  st.p = &p;
-  st.buf = dyn;
-  st.full = sh.full;
-  st.cl = blockIdx.x / C;
-  st.lo = static_cast<int>(rank) * p.slice;
-  st.len = max(0, min(p.V, st.lo + p.slice) - st.lo);
-  st.nt = (st.len + p.tile - 1) / p.tile;
-  st.S = p.stages;
-  st.srows = p.K > 0 ? 2 : 1;
-  st.timed_out = false;
-  const int lo = st.lo, len = st.len;
+  // every CTA of the cluster must be running before any DSMEM store: arrive
+  // now, wait before the first push
+  cluster_arrive_relaxed();
+  pdl_wait();  // the row partials of the first launch are complete and visible
 
-  if (tid == 0) {
-    for (int s = 0; s < p.stages; ++s) mbar_init(&sh.full[s], 1);
-    fence_mbar_init();
+  // ---- normalisers of the 2K+1 rows (target 0..K, then draft 0..K-1)
+  for (int r = warp; r < R; r += NWARP) {
+    const bool draft = r > K;
+    const int i = draft ? r - K - 1 : r;
+    float m, s;
+    warp_row_stats(p.partials + static_cast<size_t>(job_of(p, b, i)) * p.C, p.C, draft, c, m, s);
+    if (lane == 0) {
+      rmax[r] = m;
+      rsum[r] = s;
+    }
+  }
+  // ---- draft tokens and their two logits
+  for (int i = tid; i < K; i += NT) {
+    const int x = __ldg(p.tokens + static_cast<size_t>(b) * K + i);
+    const int ok = x >= 0 && x < p.V;
+    gok[i] = ok;
+    gx[2 * i] = ok ? E::load(target_row<DT>(p, b, i), x) : 0.f;
+    gx[2 * i + 1] = ok ? E::load(draft_row<DT>(p, b, i), x) : 0.f;
   }
   __syncthreads();
-  st.prologue();
 
-  // contiguous chunk of this thread in the second pass
-  const int E2 = ((len + NT - 1) / NT + VE - 1) / VE * VE;
-  const int e0 = min(len, tid * E2), e1 = min(len, e0 + E2);
-
-  // draft token of the next job, loaded one job ahead by thread 32
-  auto token_of = [&](int q) -> int {
-    if (q >= p.njobs) return 0;
-    int b, i;
-    decode_job(p, q, b, i);
-    return i < p.K ? __ldg(p.tokens + static_cast<size_t>(b) * p.K + i) : 0;
-  };
-  int x_next = (tid == 32) ? token_of(st.cl) : 0;
-
-  int seq = 0;
-  for (int n = 0;; ++n) {
-    const int q = st.cl + n * p.ncl;
-    if (q >= p.njobs) break;
-    const int par = n & 1;
-    int b, i;
-    decode_job(p, q, b, i);
-    const bool pair = i < p.K;
-    const unsigned char *rt, *rd;
-    st.rows_of(q, rt, rd);
-
-    // draft token's two logits and the rejection hint: loads issued now by
-    // thread 32, consumed after pass 1
-    int g_ok = 1, g_hint = 0;
-    float g_zt = 0.f, g_zd = 0.f;
-    if (tid == 32) {
-      const int x = x_next;
-      if (pair) {
-        g_ok = (x >= 0 && x < p.V);
-        if (g_ok) {
-          g_zt = E::load(rt, x);
-          g_zd = E::load(rd, x);
-        }
-      }
-      if (rank == 0) g_hint = *reinterpret_cast<volatile int *>(p.first_rej + b);
-      x_next = token_of(q + p.ncl);
-    }
-
-    // ---- pass 1: online max / sum-exp of both rows of this slice
-    float mt = -INFINITY, s_t = 0.f, mtc = 0.f;
-    float md = -INFINITY, s_d = 0.f, mdc = 0.f;
-    for (int k = 0; k < st.nt; ++k, ++seq) {
-      st.acquire(seq, k, rt, rd);
-      const int s = seq % st.S;
-      const int nv = (st.tile_len(k) + VE - 1) / VE;
-      const unsigned char *bt = st.stage_row(s, 0);
-      if (pair) {
-        const unsigned char *bd = st.stage_row(s, 1);
-        for (int j = tid; j < nv; j += NT) {
-          float f[VE];
-          E::unpack(lds128(bt + j * 16), f);
-          online_update<VE>(f, c, mt, s_t, mtc);
-          E::unpack(lds128(bd + j * 16), f);
-          online_update<VE>(f, c, md, s_d, mdc);
-        }
-      } else {
-        for (int j = tid; j < nv; j += NT) {
-          float f[VE];
-          E::unpack(lds128(bt + j * 16), f);
-          online_update<VE>(f, c, mt, s_t, mtc);
-        }
-      }
-      st.release(seq);
-    }
-    block_reduce_ms(mt, s_t, c, sh.red_m[0], sh.red_s[0]);
-    if (pair) block_reduce_ms(md, s_d, c, sh.red_m[1], sh.red_s[1]);
-    if (tid < 32) {  // push this slice's statistics into every CTA of the cluster
-      const float a0 = __shfl_sync(0xFFFFFFFFu, mt, 0), a1 = __shfl_sync(0xFFFFFFFFu, s_t, 0);
-      const float a2 = __shfl_sync(0xFFFFFFFFu, md, 0), a3 = __shfl_sync(0xFFFFFFFFu, s_d, 0);
-      if (tid < static_cast<int>(C)) dsmem_st_v4f32(dsmem_addr(&sh.xs[par][rank][0], tid), a0, a1, a2, a3);
-    } else if (tid == 32) {
-      sh.gok[par] = g_ok;
-      sh.gz[par][0] = g_zt;
-      sh.gz[par][1] = g_zd;
-      if (rank == 0)
-        for (uint32_t r = 0; r < C; ++r) dsmem_st_s32(dsmem_addr(&sh.xhint[par], r), g_hint);
-    }
-    cluster_sync();  // partial statistics of job n visible cluster-wide
-
-    // ---- combine the slices (rank order) and take the acceptance decision
-    if (tid == 0) {
-      float Mt = -INFINITY, St = 0.f, Md = -INFINITY, Sd = 0.f;
-      for (uint32_t r = 0; r < C; ++r) {
-        ms_combine(Mt, St, sh.xs[par][r][0], sh.xs[par][r][1], c);
-        if (pair) ms_combine(Md, Sd, sh.xs[par][r][2], sh.xs[par][r][3], c);
-      }
-      const int hint = sh.xhint[par];
-      const int ok = sh.gok[par];
-      int accept = 1;
-      if (pair && ok) {
-        const float a = fmaf(sh.gz[par][0], c, -(Mt * c));
-        const float d = fmaf(sh.gz[par][1], c, -(Md * c));
-        const float ratio = ex2(a - d) * (Sd / St);  // p_i(x_i) / q_i(x_i)
-        const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
-        accept = u < ratio;
-      }
-      const int need = pair ? (ok && !accept) : 1;
-      const int superseded = pair ? (hint < i) : (hint < p.K);
-      sh.bi[0] = need && !superseded;
-      sh.bf[0] = Mt;
-      sh.bf[1] = St;
-      sh.bf[2] = Md;
-      sh.bf[3] = Sd;
-      if (rank == 0) {
-        const int R = 2 * p.K + 1;
-        if (p.out_row_max) {
-          p.out_row_max[static_cast<size_t>(b) * R + i] = Mt;
-          if (pair) p.out_row_max[static_cast<size_t>(b) * R + p.K + 1 + i] = Md;
-        }
-        if (p.out_row_sumexp) {
-          p.out_row_sumexp[static_cast<size_t>(b) * R + i] = St;
-          if (pair) p.out_row_sumexp[static_cast<size_t>(b) * R + p.K + 1 + i] = Sd;
-        }
-        if (pair && !ok) {
-          atomicOr(p.seq_err + b, 1);
-          atomicOr(p.status, ST_TOKEN);
-        }
-        if (pair && ok && !accept) atomicMin(p.first_rej + b, i);
-      }
-    }
-    __syncthreads();
-
-    int taker = 0;  // the CTA that records the job and takes its ticket
-    if (sh.bi[0]) {
-      // ---- pass 2 (a reject or the bonus row), from the slice just read
-      // (L2-resident): per-thread contiguous chunks, block scan, slice mass,
-      // cluster exchange, owner slice, then one thread walks its chunk.
-      Weights W;
-      W.c = c;
-      W.mtc = sh.bf[0] * c;
-      W.mdc = sh.bf[2] * c;
-      W.inv_st = 1.f / sh.bf[1];
-      W.inv_sd = 1.f / sh.bf[3];
-      W.resid = pair;
-      int fallback = 0, owner = 0, pl = 0;
-      float tl = 0.f, excl = 0.f, sum = 0.f;
-      for (int round = 0; round < 2; ++round) {
-        sum = 0.f;
-        if (TMA) {
-#pragma unroll 4
-          for (int e = e0; e < e1; e += VE) {
-            const size_t off = static_cast<size_t>(lo + e) * E::BYTES;
-            float ft[VE], fd[VE];
-            E::unpack(__ldg(reinterpret_cast<const uint4 *>(rt + off)), ft);
-            if (W.resid) E::unpack(__ldg(reinterpret_cast<const uint4 *>(rd + off)), fd);
-#pragma unroll
-            for (int j = 0; j < VE; ++j) sum = __fadd_rn(sum, W(ft[j], W.resid ? fd[j] : 0.f));
-          }
-        } else {
-          for (int e = e0; e < e1; ++e)
-            sum = __fadd_rn(sum, W(E::load(rt, lo + e), W.resid ? E::load(rd, lo + e) : 0.f));
-        }
-        float total;
-        excl = block_exclusive_scan(sum, sh.fscratch, &total);
-        if (tid < static_cast<int>(C)) dsmem_st_f32(dsmem_addr(&sh.xz[par][round][rank], tid), total);
-        cluster_sync();  // slice masses visible cluster-wide
-        if (tid == 0) {
-          float Z = 0.f;
-          for (uint32_t r = 0; r < C; ++r) Z += sh.xz[par][round][r];
-          int again = 0;
-          if (W.resid && !(Z > 0.f)) {
-            again = 1;  // no residual mass in fp32: draw from p at this position
-          } else {
-            const uint32_t pos = static_cast<uint32_t>(pair ? i : p.K);
-            const float t = philox_uniform(p.seed, static_cast<uint32_t>(b), pos, 1u) * Z;
-            float P = 0.f, Pown = 0.f, Plast = 0.f;
-            int own = -1, last = -1;
-            for (uint32_t r = 0; r < C; ++r) {
-              const float zr = sh.xz[par][round][r];
-              if (own < 0 && P + zr > t) {
-                own = static_cast<int>(r);
-                Pown = P;
-              }
-              if (zr > 0.f) {
-                last = static_cast<int>(r);
-                Plast = P;
-              }
-              P += zr;
-            }
-            int lastmode = 0;
-            if (own < 0) {
-              own = last < 0 ? 0 : last;
-              Pown = Plast;
-              lastmode = 1;
-            }
-            sh.bi[1] = own;
-            sh.bi[2] = lastmode;
-            sh.bf[4] = t - Pown;
-          }
-          sh.bi[3] = again;
-        }
-        __syncthreads();
-        if (sh.bi[3] && round == 0) {
-          W.resid = false;
-          fallback = 1;
-          continue;
-        }
-        owner = sh.bi[1];
-        pl = sh.bi[2];
-        tl = sh.bf[4];
+  // ---- left-to-right acceptance: the first reject n (or K)
+  if (tid == 0) {
+    int n = K, err = 0;
+    for (int i = 0; i < K; ++i)
+      if (!gok[i]) err = 1;
+    for (int i = 0; i < K && !err; ++i) {
+      const float a = fmaf(gx[2 * i], c, -(rmax[i] * c));
+      const float d = fmaf(gx[2 * i + 1], c, -(rmax[K + 1 + i] * c));
+      const float ratio = ex2(a - d) * (rsum[K + 1 + i] / rsum[i]);  // p_i(x_i) / q_i(x_i)
+      const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
+      if (!(u < ratio)) {
+        n = i;
         break;
       }
-      taker = owner;
-      if (static_cast<int>(rank) == owner) {
-        // the thread whose chunk holds the crossing (or the last positive one)
-        int who;
-        if (!pl)
-          who = block_reduce_min_int((sum > 0.f && __fadd_rn(excl, sum) > tl) ? tid : INT_MAX,
-                                     sh.scratch);
-        else
-          who = block_reduce_max_int(sum > 0.f ? tid : -1, sh.scratch);
-        if (who == INT_MAX || who < 0) {
-          // rounding left no crossing in this slice: last positive entry
-          pl = 1;
-          who = block_reduce_max_int(sum > 0.f ? tid : -1, sh.scratch);
-          if (who < 0) who = 0;
+    }
+    sh.bi[0] = n;
+    sh.bi[1] = err;
+  }
+  __syncthreads();
+  const int n = sh.bi[0];
+  const int err = sh.bi[1];
+  if (rank == 0) {
+    for (int r = tid; r < R; r += NT) {
+      if (p.out_row_max) p.out_row_max[static_cast<size_t>(b) * R + r] = rmax[r];
+      if (p.out_row_sumexp) p.out_row_sumexp[static_cast<size_t>(b) * R + r] = rsum[r];
+    }
+    if (err) {
+      for (int e = tid; e <= K; e += NT) p.out_tokens[static_cast<size_t>(b) * (K + 1) + e] = -1;
+      if (tid == 0) {
+        p.out_n[b] = -1;
+        atomicOr(p.status, ST_TOKEN);
+        if (p.stats) atomicAdd(&p.stats->errors, 1ull);
+      }
+    }
+  }
+
+  if (err) cluster_wait();
+  if (!err) {
+    // ---- the draw: residual at n < K, or the bonus from row K
+    const bool pair = n < K;
+    const unsigned char *rt = target_row<DT>(p, b, n);
+    const unsigned char *rd = pair ? draft_row<DT>(p, b, n) : nullptr;
+    const int lo = static_cast<int>(rank) * p.slice;
+    const int len = max(0, min(p.V, lo + p.slice) - lo);
+    const int E2 = ((len + NT - 1) / NT + VE - 1) / VE * VE;
+    const int e0 = min(len, tid * E2), e1 = min(len, e0 + E2);
+    Weights W;
+    W.c = c;
+    W.mtc = rmax[n] * c;
+    W.mdc = pair ? rmax[K + 1 + n] * c : 0.f;
+    W.inv_st = 1.f / rsum[n];
+    W.inv_sd = pair ? 1.f / rsum[K + 1 + n] : 0.f;
+    W.resid = pair;
+    cluster_wait();
+    int fallback = 0, owner = 0, pl = 0;
+    float tl = 0.f, excl = 0.f, sum = 0.f;
+    for (int round = 0; round < 2; ++round) {
+      sum = 0.f;
+      if (TMA) {
+#pragma unroll 4
+        for (int e = e0; e < e1; e += VE) {
+          const size_t off = static_cast<size_t>(lo + e) * E::BYTES;
+          float ft[VE], fd[VE];
+          E::unpack(__ldcg(reinterpret_cast<const uint4 *>(rt + off)), ft);
+          if (W.resid) E::unpack(__ldcg(reinterpret_cast<const uint4 *>(rd + off)), fd);
+#pragma unroll
+          for (int j = 0; j < VE; ++j) sum = __fadd_rn(sum, W(ft[j], W.resid ? fd[j] : 0.f));
         }
-        // the whole CTA walks the chosen chunk: one entry per thread, a block
-        // scan, and the first entry whose running mass passes tl
-        const int w0 = min(len, who * E2), w1 = min(len, w0 + E2);
-        const float wexcl = __shfl_sync(0xFFFFFFFFu, excl, who & 31);
-        if ((tid & 31) == 0) sh.fscratch[tid >> 5] = wexcl;
-        __syncthreads();
-        const float base = sh.fscratch[who >> 5];
-        __syncthreads();
-        float w = 0.f;
-        const int e = w0 + tid;
-        if (e < w1) w = W(E::load(rt, lo + e), W.resid ? E::load(rd, lo + e) : 0.f);
-        float tot_unused;
-        const float before = block_exclusive_scan(w, sh.fscratch, &tot_unused);
-        const float run = __fadd_rn(base, __fadd_rn(before, w));
-        int pick = INT_MAX;
-        if (!pl) pick = block_reduce_min_int((w > 0.f && run > tl) ? e : INT_MAX, sh.scratch);
-        if (pick == INT_MAX) pick = block_reduce_max_int(w > 0.f ? e : -1, sh.scratch);
-        if (pick < 0) pick = w0;
-        if (tid == 0) {
-          p.cand[static_cast<size_t>(b) * p.J + i] = (lo + pick) | (fallback ? CAND_FALLBACK : 0);
-          __threadfence();
+      } else {
+        for (int e = e0; e < e1; ++e)
+          sum = __fadd_rn(sum, W(E::load(rt, lo + e), W.resid ? E::load(rd, lo + e) : 0.f));
+      }
+      float total;
+      excl = block_exclusive_scan(sum, sh.fscratch, &total);
+      if (tid < static_cast<int>(C)) dsmem_st_f32(dsmem_addr(&sh.xz[round][rank], tid), total);
+      cluster_sync();  // slice masses visible cluster-wide
+      if (tid == 0) {
+        float Z = 0.f;
+        for (uint32_t r = 0; r < C; ++r) Z = __fadd_rn(Z, sh.xz[round][r]);
+        int again = 0;
+        if (W.resid && !(Z > 0.f)) {
+          again = 1;  // no residual mass in fp32: draw from p at this position
+        } else {
+          const float t = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(n), 1u) * Z;
+          float P = 0.f, Pown = 0.f, Plast = 0.f;
+          int own = -1, last = -1;
+          for (uint32_t r = 0; r < C; ++r) {
+            const float zr = sh.xz[round][r];
+            if (own < 0 && __fadd_rn(P, zr) > t) {
+              own = static_cast<int>(r);
+              Pown = P;
+            }
+            if (zr > 0.f) {
+              last = static_cast<int>(r);
+              Plast = P;
+            }
+            P = __fadd_rn(P, zr);
+          }
+          int lastmode = 0;
+          if (own < 0) {
+            own = last < 0 ? 0 : last;
+            Pown = Plast;
+            lastmode = 1;
+          }
+          sh.bi[2] = own;
+          sh.bi[3] = lastmode;
+          sh.bf[0] = t - Pown;
+        }
+        sh.bi[4] = again;
+      }
+      __syncthreads();
+      if (sh.bi[4] && round == 0) {
+        W.resid = false;
+        fallback = 1;
+        continue;
+      }
+      owner = sh.bi[2];
+      pl = sh.bi[3];
+      tl = sh.bf[0];
+      break;
+    }
+    if (static_cast<int>(rank) == owner) {
+      // the thread whose chunk holds the crossing (or the last positive one)
+      int who;
+      if (!pl)
+        who = block_reduce_min_int((sum > 0.f && __fadd_rn(excl, sum) > tl) ? tid : INT_MAX, sh.scratch);
+      else
+        who = block_reduce_max_int(sum > 0.f ? tid : -1, sh.scratch);
+      if (who == INT_MAX || who < 0) {  // rounding left no crossing: last positive entry
+        pl = 1;
+        who = block_reduce_max_int(sum > 0.f ? tid : -1, sh.scratch);
+        if (who < 0) who = 0;
+      }
+      // the whole CTA walks that chunk: one entry per thread, a block scan,
+      // and the first entry whose running mass passes tl
+      const int w0 = min(len, who * E2), w1 = min(len, w0 + E2);
+      const float wexcl = __shfl_sync(0xFFFFFFFFu, excl, who & 31);
+      if (lane == 0) sh.fscratch[warp] = wexcl;
+      __syncthreads();
+      const float base = sh.fscratch[who >> 5];
+      __syncthreads();
+      float w = 0.f;
+      const int e = w0 + tid;
+      if (e < w1) w = W(E::load(rt, lo + e), W.resid ? E::load(rd, lo + e) : 0.f);
+      float tot_unused;
+      const float before = block_exclusive_scan(w, sh.fscratch, &tot_unused);
+      const float run = __fadd_rn(base, __fadd_rn(before, w));
+      int pick = INT_MAX;
+      if (!pl) pick = block_reduce_min_int((w > 0.f && run > tl) ? e : INT_MAX, sh.scratch);
+      if (pick == INT_MAX) pick = block_reduce_max_int(w > 0.f ? e : -1, sh.scratch);
+      if (pick < 0) pick = w0;
+      const int token = lo + pick;
+      // ---- outputs of sequence b
+      int32_t *out = p.out_tokens + static_cast<size_t>(b) * (K + 1);
+      for (int j = tid; j <= K; j += NT)
+        out[j] = j < n ? __ldg(p.tokens + static_cast<size_t>(b) * K + j) : (j == n ? token : -1);
+      if (tid == 0) {
+        p.out_n[b] = n;
+        if (p.stats) {
+          atomicAdd(&p.stats->sequences, 1ull);
+          atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(n));
+          atomicAdd(n == K ? &p.stats->bonus : &p.stats->resampled, 1ull);
+          if (fallback) atomicAdd(&p.stats->residual_fallbacks, 1ull);
         }
       }
     }
-    if (static_cast<int>(rank) == taker) {
-      if (take_ticket(p, b, sh)) emit_chain_sample(p, b);
-    }
   }
-  if (st.timed_out) {
-    atomicOr(p.status, ST_TIMEOUT);
-    st.drain_after_timeout(seq);
-  }
-  // keep this CTA's shared memory alive until no peer can read it
-  cluster_sync();
+  cluster_sync();  // no CTA leaves while a peer may still write its shared memory
 }
 
 // ======================================================================
-// Greedy chain (T = 0) and greedy tree: per-row argmax, then the walk.
+// B'. finish_kernel: greedy chain and greedy tree, one CTA per sequence.
 // ======================================================================
-template <int DT, bool TMA>
-__global__ void __launch_bounds__(NT, 3) argmax_kernel(const Params p) {
-  using E = Elem<DT>;
-  constexpr int VE = E::VE;
-  extern __shared__ __align__(128) unsigned char dyn[];
-  __shared__ SharedSmall sh;
+__global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
+  extern __shared__ __align__(16) int ish[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.x;
+  const int J = p.J;
+  int *s_amax = ish;                                        // [J]
+  int *s_tok = ish + J;                                     // [J]
+  float *s_vmax = reinterpret_cast<float *>(ish + 2 * J);  // [J]
 
-  const int tid = threadIdx.x;
-  const uint32_t rank = cluster_rank();
-  const uint32_t C = cluster_size();
-
-  Stream<DT, TMA> st;
-  st.p = &p;
-  st.buf = dyn;
-  st.full = sh.full;
-  st.cl = blockIdx.x / C;
-  st.lo = static_cast<int>(rank) * p.slice;
-  st.len = max(0, min(p.V, st.lo + p.slice) - st.lo);
-  st.nt = (st.len + p.tile - 1) / p.tile;
-  st.S = p.stages;
-  st.srows = 1;
-  st.timed_out = false;
-
-  if (tid == 0) {
-    for (int s = 0; s < p.stages; ++s) mbar_init(&sh.full[s], 1);
-    fence_mbar_init();
+  pdl_wait();
+  for (int r = warp; r < J; r += NWARP) {
+    float v = -INFINITY;
+    int idx = INT_MAX;
+    if (lane < p.C) {
+      const float4 a = __ldcg(p.partials + static_cast<size_t>(job_of(p, b, r)) * p.C + lane);
+      v = a.x;
+      idx = __float_as_int(a.y);
+    }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, off);
+      const int i2 = __shfl_xor_sync(0xFFFFFFFFu, idx, off);
+      am_combine(v, idx, v2, i2);
+    }
+    if (lane == 0) {
+      s_amax[r] = idx == INT_MAX ? 0 : idx;  // every logit -inf: first index
+      s_vmax[r] = v;
+    }
   }
+  const int ntok = p.kind == KIND_TREE ? J : p.K;
+  for (int e = tid; e < ntok; e += NT) s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * ntok + e);
   __syncthreads();
-  st.prologue();
 
-  int seq = 0;
-  for (int n = 0;; ++n) {
-    const int q = st.cl + n * p.ncl;
-    if (q >= p.njobs) break;
-    const int par = n & 1;
-    int b, i;
-    decode_job(p, q, b, i);
-    const unsigned char *rt, *rd;
-    st.rows_of(q, rt, rd);
-
-    float best = -INFINITY;
-    int bidx = INT_MAX;
-    for (int k = 0; k < st.nt; ++k, ++seq) {
-      st.acquire(seq, k, rt, nullptr);
-      const int s = seq % st.S;
-      const int nv = (st.tile_len(k) + VE - 1) / VE;
-      const unsigned char *bt = st.stage_row(s, 0);
-      const int base = st.lo + k * p.tile;
-      for (int j = tid; j < nv; j += NT) {
-        float f[VE];
-        E::unpack(lds128(bt + j * 16), f);
-        float vm = f[0];
-#pragma unroll
-        for (int e = 1; e < VE; ++e) vm = fmaxf(vm, f[e]);
-        if (vm > best) {  // rare after the first few vectors
-          best = vm;
-#pragma unroll
-          for (int e = VE - 1; e >= 0; --e)
-            if (f[e] == vm) bidx = base + j * VE + e;
-        }
+  if (p.kind == KIND_GREEDY_CHAIN) {
+    const int K = p.K, R = 2 * K + 1;
+    if (p.out_row_max || p.out_row_sumexp)
+      for (int r = tid; r < R; r += NT) {
+        if (p.out_row_max) p.out_row_max[static_cast<size_t>(b) * R + r] = r <= K ? s_vmax[r] : NAN;
+        if (p.out_row_sumexp) p.out_row_sumexp[static_cast<size_t>(b) * R + r] = NAN;
       }
-      st.release(seq);
-    }
-    block_reduce_argmax(best, bidx, sh.fscratch, sh.scratch);
-    if (tid == 0)  // push this slice's (max, index) into rank 0
-      dsmem_st_v4f32(dsmem_addr(&sh.xs[par][rank][0], 0), best, __int_as_float(bidx), 0.f, 0.f);
-    cluster_sync();  // partial maxima of job n visible cluster-wide
-    if (rank != 0) continue;
     if (tid == 0) {
-      float v = -INFINITY;
-      int idx = INT_MAX;
-      for (uint32_t r = 0; r < C; ++r) am_combine(v, idx, sh.xs[par][r][0], __float_as_int(sh.xs[par][r][1]));
-      if (idx == INT_MAX) idx = 0;  // every logit is -inf: first index
-      p.cand[static_cast<size_t>(b) * p.J + i] = idx;
-      if (p.kind == KIND_GREEDY_CHAIN) {
-        const int R = 2 * p.K + 1;
-        if (p.out_row_max) {
-          p.out_row_max[static_cast<size_t>(b) * R + i] = v;
-          if (i < p.K) p.out_row_max[static_cast<size_t>(b) * R + p.K + 1 + i] = NAN;
-        }
-        if (p.out_row_sumexp) {
-          p.out_row_sumexp[static_cast<size_t>(b) * R + i] = NAN;
-          if (i < p.K) p.out_row_sumexp[static_cast<size_t>(b) * R + p.K + 1 + i] = NAN;
+      int nacc = K, err = 0;
+      for (int e = 0; e < K; ++e) {
+        const int x = s_tok[e];
+        if (x < 0 || x >= p.V) err = 1;
+        if (nacc == K && x != s_amax[e]) nacc = e;
+      }
+      int32_t *out = p.out_tokens + static_cast<size_t>(b) * (K + 1);
+      for (int e = 0; e <= K; ++e)
+        out[e] = err ? -1 : (e < nacc ? s_tok[e] : (e == nacc ? s_amax[nacc] : -1));
+      p.out_n[b] = err ? -1 : nacc;
+      if (err) atomicOr(p.status, ST_TOKEN);
+      if (p.stats) {
+        if (err) {
+          atomicAdd(&p.stats->errors, 1ull);
+        } else {
+          atomicAdd(&p.stats->sequences, 1ull);
+          atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(nacc));
+          atomicAdd(nacc == K ? &p.stats->bonus : &p.stats->resampled, 1ull);
         }
       }
     }
-    if (!take_ticket(p, b, sh)) continue;
-
-    // ---- emission: every row of sequence b has its argmax in cand[b, :]
-    int *s_amax = reinterpret_cast<int *>(dyn + p.emit_off);
-    int *s_tok = s_amax + p.J;
-    for (int e = tid; e < p.J; e += NT) s_amax[e] = __ldcg(p.cand + static_cast<size_t>(b) * p.J + e);
-    if (p.kind == KIND_GREEDY_CHAIN) {
-      for (int e = tid; e < p.K; e += NT) s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * p.K + e);
-      __syncthreads();
-      if (tid == 0) {
-        int nacc = p.K, err = 0;
-        for (int e = 0; e < p.K; ++e) {
-          const int x = s_tok[e];
-          if (x < 0 || x >= p.V) err = 1;
-          if (nacc == p.K && x != s_amax[e]) nacc = e;
-        }
-        int32_t *out = p.out_tokens + static_cast<size_t>(b) * (p.K + 1);
-        for (int e = 0; e <= p.K; ++e)
-          out[e] = err ? -1 : (e < nacc ? s_tok[e] : (e == nacc ? s_amax[nacc] : -1));
-        p.out_n[b] = err ? -1 : nacc;
-        if (err) atomicOr(p.status, ST_TOKEN);
-        if (p.stats) {
-          if (err) {
-            atomicAdd(&p.stats->errors, 1ull);
-          } else {
-            atomicAdd(&p.stats->sequences, 1ull);
-            atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(nacc));
-            atomicAdd(nacc == p.K ? &p.stats->bonus : &p.stats->resampled, 1ull);
-          }
-        }
-        p.ticket[b] = 0;
-      }
-      __syncthreads();
-      continue;
-    }
-
-    // tree: N = J nodes
-    const int N = p.J;
-    int *s_par = s_tok + N;
-    int *s_depth = s_par + N;
-    unsigned char *s_acc = reinterpret_cast<unsigned char *>(s_depth + N);
-    for (int e = tid; e < N; e += NT) {
-      s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * N + e);
-      s_par[e] = __ldg(p.parent + e);
-    }
-    __syncthreads();
-    if (tid == 0) {
-      const int W = p.max_depth + 1;
-      int32_t *path = p.out_tokens + static_cast<size_t>(b) * W;
-      int bad_parent = s_par[0] != -1, bad_tok = 0;
-      s_depth[0] = 0;
-      s_acc[0] = 1;
-      int bestn = 0;
-      for (int c2 = 1; c2 < N && !bad_parent; ++c2) {
-        const int pc = s_par[c2];
-        if (pc < 0 || pc >= c2) {
-          bad_parent = 1;
-          break;
-        }
-        const int d = s_depth[pc] + 1;
-        if (d > p.max_depth) {
-          bad_parent = 1;
-          break;
-        }
-        const int x = s_tok[c2];
-        if (x < 0 || x >= p.V) bad_tok = 1;
-        s_depth[c2] = d;
-        s_acc[c2] = s_acc[pc] && x == s_amax[pc];
-        if (s_acc[c2] && d > s_depth[bestn]) bestn = c2;
-      }
-      if (bad_parent || bad_tok) {
-        for (int e = 0; e < W; ++e) path[e] = -1;
-        p.out_n[b] = -1;
-        atomicOr(p.status, bad_parent ? ST_PARENT : ST_TOKEN);
-      } else {
-        const int d = s_depth[bestn];
-        for (int e = d + 1; e < W; ++e) path[e] = -1;
-        path[d] = s_amax[bestn];
-        for (int n2 = bestn, e = d - 1; n2 != 0; n2 = s_par[n2], --e) path[e] = s_tok[n2];
-        p.out_n[b] = d + 1;
-      }
-      p.ticket[b] = 0;
-    }
-    __syncthreads();
+    return;
   }
-  if (st.timed_out) {
-    atomicOr(p.status, ST_TIMEOUT);
-    st.drain_after_timeout(seq);
+
+  // tree: J = N nodes
+  const int N = J;
+  int *s_par = ish + 3 * J;
+  int *s_depth = s_par + N;
+  unsigned char *s_acc = reinterpret_cast<unsigned char *>(s_depth + N);
+  for (int e = tid; e < N; e += NT) s_par[e] = __ldg(p.parent + e);
+  __syncthreads();
+  if (tid == 0) {
+    const int W = p.max_depth + 1;
+    int32_t *path = p.out_tokens + static_cast<size_t>(b) * W;
+    int bad_parent = s_par[0] != -1, bad_tok = 0;
+    s_depth[0] = 0;
+    s_acc[0] = 1;
+    int bestn = 0;
+    for (int c2 = 1; c2 < N && !bad_parent; ++c2) {
+      const int pc = s_par[c2];
+      if (pc < 0 || pc >= c2) {
+        bad_parent = 1;
+        break;
+      }
+      const int d = s_depth[pc] + 1;
+      if (d > p.max_depth) {
+        bad_parent = 1;
+        break;
+      }
+      const int x = s_tok[c2];
+      if (x < 0 || x >= p.V) bad_tok = 1;
+      s_depth[c2] = d;
+      s_acc[c2] = s_acc[pc] && x == s_amax[pc];
+      if (s_acc[c2] && d > s_depth[bestn]) bestn = c2;
+    }
+    if (bad_parent || bad_tok) {
+      for (int e = 0; e < W; ++e) path[e] = -1;
+      p.out_n[b] = -1;
+      atomicOr(p.status, bad_parent ? ST_PARENT : ST_TOKEN);
+    } else {
+      const int d = s_depth[bestn];
+      for (int e = d + 1; e < W; ++e) path[e] = -1;
+      path[d] = s_amax[bestn];
+      for (int n2 = bestn, e = d - 1; n2 != 0; n2 = s_par[n2], --e) path[e] = s_tok[n2];
+      p.out_n[b] = d + 1;
+    }
   }
-  cluster_sync();
 }
 
 // ======================================================================

@@ -74,6 +74,14 @@ __device__ __forceinline__ void cluster_sync() {
           : "memory");
 }
 
+// Split cluster barrier: arrive (relaxed: orders nothing) and wait.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait;" ::: "memory");
+}
+
 // Address of the same shared variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank) {
   uint32_t r;

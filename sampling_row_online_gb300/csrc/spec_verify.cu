@@ -32,14 +32,15 @@ int cuda_fail(cudaError_t e, const char *what) {
 }
 
 // ------------------------------------------------------------ workspaces
-// Per (device, stream): [status][ticket B][first_rej B][seq_err B][cand B*J]
-// plus a staging area for the host-buffer entry point.
+// Per (device, stream): the status word (never reallocated), the row
+// partials of the current call (float4 per job and slice, grow-only), and a
+// staging area for the host-buffer entry point.
 struct Workspace {
   int device = -1;
   cudaStream_t stream = nullptr;
-  int32_t *status = nullptr;  // 1 word, never reallocated
-  int32_t *ints = nullptr;
-  size_t cap_seq = 0, cap_cand = 0;
+  int32_t *status = nullptr;
+  float4 *partials = nullptr;
+  size_t cap_parts = 0;
   unsigned char *stage = nullptr;
   size_t stage_cap = 0;
 };
@@ -58,8 +59,7 @@ Workspace *find_ws(int device, cudaStream_t stream, bool create) {
   return w;
 }
 
-// Returns SPEC_OK and the workspace holding at least B sequences and B*J jobs.
-int get_ws(cudaStream_t stream, size_t B, size_t J, Workspace **out) {
+int get_ws(cudaStream_t stream, size_t nparts, Workspace **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -71,43 +71,23 @@ int get_ws(cudaStream_t stream, size_t B, size_t J, Workspace **out) {
     e = cudaMemsetAsync(w->status, 0, sizeof(int32_t), stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
   }
-  const size_t need_seq = std::max<size_t>(B, 1), need_cand = std::max<size_t>(B * J, 1);
-  if (w->cap_seq < need_seq || w->cap_cand < need_cand) {
-    const size_t seq = std::max(need_seq, w->cap_seq), cand = std::max(need_cand, w->cap_cand);
-    if (w->ints) {
-      e = cudaFree(w->ints);  // synchronises the device: no call still uses it
-      w->ints = nullptr;
-      w->cap_seq = w->cap_cand = 0;
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+  if (w->cap_parts < nparts) {
+    if (w->partials) {
+      e = cudaFree(w->partials);  // synchronises the device: no call still uses it
+      w->partials = nullptr;
+      w->cap_parts = 0;
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFree(partials)");
     }
-    int32_t *p = nullptr;
-    e = cudaMalloc(&p, sizeof(int32_t) * (3 * seq + cand));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
-    // ticket = 0, first_rej = "none" (0x7F7F7F7F), seq_err = 0, cand = 0
-    if ((e = cudaMemsetAsync(p, 0, sizeof(int32_t) * seq, stream)) != cudaSuccess ||
-        (e = cudaMemsetAsync(p + seq, 0x7F, sizeof(int32_t) * seq, stream)) != cudaSuccess ||
-        (e = cudaMemsetAsync(p + 2 * seq, 0, sizeof(int32_t) * (seq + cand), stream)) != cudaSuccess) {
-      cudaFree(p);
-      return cuda_fail(e, "cudaMemsetAsync(workspace)");
-    }
-    w->ints = p;
-    w->cap_seq = seq;
-    w->cap_cand = cand;
+    e = cudaMalloc(&w->partials, sizeof(float4) * nparts);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(partials)");
+    w->cap_parts = nparts;
   }
   *out = w;
   return SPEC_OK;
 }
 
-void bind_ws(Params &p, const Workspace *w) {
-  p.status = w->status;
-  p.ticket = w->ints;
-  p.first_rej = w->ints + w->cap_seq;
-  p.seq_err = w->ints + 2 * w->cap_seq;
-  p.cand = w->ints + 3 * w->cap_seq;
-}
-
 // ------------------------------------------------------------ geometry
-constexpr int SLICE_TARGET_BYTES = 16 * 1024;  // vocabulary bytes per row and CTA
+constexpr int SLICE_TARGET_BYTES = 16 * 1024;  // vocabulary bytes per row and slice
 constexpr int DEFAULT_STAGES = 4;               // tile ring depth
 
 int env_int(const char *name, int dflt, int lo, int hi) {
@@ -120,31 +100,15 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 struct KernelCache {
   const void *fn;
   int device;
-  int smem_set;
-  int C, smem, max_clusters;  // last occupancy query
+  int smem_set;   // largest dynamic smem attribute set so far
+  int q_smem, q_C;  // last occupancy query
+  int q_result;
 };
 std::vector<KernelCache> g_kc;
 
-cudaLaunchConfig_t cluster_config(const void *fn, int C, int grid_clusters, int smem,
-                                  cudaStream_t stream, cudaLaunchAttribute *attr) {
-  (void)fn;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(C * grid_clusters), 1, 1);
-  cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  attr->id = cudaLaunchAttributeClusterDimension;
-  attr->val.clusterDim.x = C;
-  attr->val.clusterDim.y = 1;
-  attr->val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cfg;
-}
-
-// Sets the kernel's attributes once per device and returns how many clusters
-// of size C with `smem` bytes can be resident at once (0: none).
-int prepare_kernel(const void *fn, int C, int smem, int *max_clusters) {
+// Dynamic-smem attribute once per (kernel, device) and size, then either the
+// resident blocks per SM (C == 0) or the resident clusters of size C.
+int occupancy(const void *fn, int smem, int C, int *result) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -157,105 +121,171 @@ int prepare_kernel(const void *fn, int C, int smem, int *max_clusters) {
     k.fn = fn;
     k.device = dev;
     k.smem_set = -1;
-    k.C = -1;
+    k.q_smem = -1;
     g_kc.push_back(k);
     kc = &g_kc.back();
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster)");
+    if (C > 0) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster)");
+    }
   }
   if (smem > kc->smem_set) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
     kc->smem_set = smem;
-    kc->C = -1;
+    kc->q_smem = -1;
   }
-  if (kc->C != C || kc->smem != smem) {
-    cudaLaunchAttribute attr;
-    cudaLaunchConfig_t cfg = cluster_config(fn, C, 1, smem, nullptr, &attr);
+  if (kc->q_smem != smem || kc->q_C != C) {
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    if (C == 0) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, NT, smem);
+    } else {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(C, 1, 1);
+      cfg.blockDim = dim3(NT, 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = C;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    }
     if (e != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
-    kc->C = C;
-    kc->smem = smem;
-    kc->max_clusters = n;
+    kc->q_smem = smem;
+    kc->q_C = C;
+    kc->q_result = n;
   }
-  *max_clusters = kc->max_clusters;
+  *result = kc->q_result;
   return SPEC_OK;
+}
+
+int num_sms() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (!sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = n > 0 ? n : 1;
+  }
+  return sms[dev];
 }
 
 bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-const void *pick_sample_kernel(int dtype, bool tma) {
+template <bool ARGMAX>
+const void *pick_row_kernel(int dtype, bool tma) {
   if (dtype == SPEC_F32)
-    return tma ? reinterpret_cast<const void *>(&sample_kernel<0, true>)
-               : reinterpret_cast<const void *>(&sample_kernel<0, false>);
-  return tma ? reinterpret_cast<const void *>(&sample_kernel<1, true>)
-             : reinterpret_cast<const void *>(&sample_kernel<1, false>);
+    return tma ? reinterpret_cast<const void *>(&row_kernel<0, true, ARGMAX>)
+               : reinterpret_cast<const void *>(&row_kernel<0, false, ARGMAX>);
+  return tma ? reinterpret_cast<const void *>(&row_kernel<1, true, ARGMAX>)
+             : reinterpret_cast<const void *>(&row_kernel<1, false, ARGMAX>);
 }
 
-const void *pick_argmax_kernel(int dtype, bool tma) {
+const void *pick_draw_kernel(int dtype, bool tma) {
   if (dtype == SPEC_F32)
-    return tma ? reinterpret_cast<const void *>(&argmax_kernel<0, true>)
-               : reinterpret_cast<const void *>(&argmax_kernel<0, false>);
-  return tma ? reinterpret_cast<const void *>(&argmax_kernel<1, true>)
-             : reinterpret_cast<const void *>(&argmax_kernel<1, false>);
+    return tma ? reinterpret_cast<const void *>(&draw_kernel<0, true>)
+               : reinterpret_cast<const void *>(&draw_kernel<0, false>);
+  return tma ? reinterpret_cast<const void *>(&draw_kernel<1, true>)
+             : reinterpret_cast<const void *>(&draw_kernel<1, false>);
 }
 
-// Launch geometry: cluster size C (CTAs sharing one row), slice per CTA,
-// tile, ring depth, dynamic shared memory, clusters launched.
-struct Geometry {
-  int C, slice, tile, stages, smem, emit_off, ncl;
-};
-
-// Slices of about 16 KB per row and CTA (cluster size up to 16), tiles of
-// NT threads x 2 vectors of 16 bytes, a ring of `stages` tiles (each stage
-// holds `srows` rows), then as many clusters as can be resident, capped by
-// the number of jobs.
-int plan(const void *fn, int V, int dtype, int srows, int emit_bytes, long long njobs,
-         Geometry *g) {
+// The whole step: A (row statistics, persistent grid) then B (per-sequence
+// decisions and outputs, launched as a programmatic dependent of A).
+int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws_out) {
   const int esz = dtype == SPEC_F32 ? 4 : 2;
   const int VE = 16 / esz;
-  const long long row_bytes = static_cast<long long>(V) * esz;
+  const bool argmax = p.kind != KIND_SAMPLE;
+  const int srows = argmax ? 1 : 2;
+  const long long row_bytes = static_cast<long long>(p.V) * esz;
   int C = static_cast<int>(std::min<long long>(
-      16, std::max<long long>(1, (row_bytes + SLICE_TARGET_BYTES - 1) / SLICE_TARGET_BYTES)));
-  C = env_int("SPEC_VERIFY_CLUSTER", C, 1, 16);
-  g->stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
-  g->tile = NT * VE * VECS_PER_THREAD;
+      MAX_CLUSTER, std::max<long long>(1, (row_bytes + SLICE_TARGET_BYTES - 1) / SLICE_TARGET_BYTES)));
+  C = env_int("SPEC_VERIFY_SLICES", C, 1, MAX_CLUSTER);
+  const int stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
+  const int tile = NT * VE * VECS_PER_THREAD;
+  const void *fa = argmax ? pick_row_kernel<true>(dtype, tma) : pick_row_kernel<false>(dtype, tma);
+  const void *fb = argmax ? reinterpret_cast<const void *>(&finish_kernel) : pick_draw_kernel(dtype, tma);
+  int smem_b = 0;
+  if (argmax)
+    smem_b = 4 * (3 * p.J) + (p.kind == KIND_TREE ? 9 * p.J : 0) + 16;
+  else
+    smem_b = 4 * (7 * p.K + 2) + 16;
+  const int smem_a = stages * srows * tile * esz;
+  int st;
+  // the draw needs clusters of C CTAs: shrink C until such a cluster fits
   for (;;) {
-    const int per = (V + C - 1) / C;
-    g->slice = (per + VE - 1) / VE * VE;
-    // the draw's per-thread chunk must fit one block-wide pass (slice <= NT^2)
-    if (g->slice > NT * NT || (g->slice + g->tile - 1) / g->tile > MAX_TILES * 64)
-      return fail(SPEC_ERR_ARG, "vocabulary too large (V <= 1048576)");
-    g->emit_off = g->stages * srows * g->tile * esz;
-    g->smem = g->emit_off + emit_bytes;
-    int maxc = 0;
-    int st = prepare_kernel(fn, C, g->smem, &maxc);
-    if (st) return st;
-    if (maxc > 0) {
-      g->C = C;
-      g->ncl = static_cast<int>(std::min<long long>(njobs, maxc));
-      return SPEC_OK;
-    }
-    if (C == 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster of this size fits on the device");
+    if (argmax) break;
+    int nclus = 0;
+    if ((st = occupancy(fb, smem_b, C, &nclus))) return st;
+    if (nclus > 0) break;
+    if (C == 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster fits on the device");
     C = C > 8 ? 8 : C / 2;
   }
-}
+  const int per = (p.V + C - 1) / C;
+  const int slice = (per + VE - 1) / VE * VE;
+  // the draw walks one thread's chunk with one entry per thread: slice <= NT^2
+  if (slice > NT * NT) return fail(SPEC_ERR_ARG, "vocabulary too large for the slice count");
+  const long long nitems = static_cast<long long>(p.njobs) * C;
+  if (nitems > INT_MAX) return fail(SPEC_ERR_ARG, "too many rows");
+  int per_sm = 0;
+  if ((st = occupancy(fa, smem_a, 0, &per_sm))) return st;
+  if (per_sm < 1) return fail(SPEC_ERR_UNSUPPORTED, "row kernel does not fit on an SM");
+  const int grid_a = static_cast<int>(std::min<long long>(nitems, static_cast<long long>(per_sm) * num_sms()));
 
-int launch(const void *fn, const Geometry &g, cudaStream_t stream, Params &p) {
-  cudaLaunchAttribute attr;
-  cudaLaunchConfig_t cfg = cluster_config(fn, g.C, g.ncl, g.smem, stream, &attr);
-  p.slice = g.slice;
-  p.tile = g.tile;
-  p.stages = g.stages;
-  p.ncl = g.ncl;
-  p.emit_off = g.emit_off;
-  void *args[] = {&p};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
-  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  Workspace *w = nullptr;
+  if ((st = get_ws(stream, static_cast<size_t>(nitems), &w))) return st;
+  p.C = C;
+  p.slice = slice;
+  p.tile = tile;
+  p.stages = stages;
+  p.partials = w->partials;
+  p.status = w->status;
+  *ws_out = w;
+
+  cudaError_t e;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_a), 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = smem_a;
+    cfg.stream = stream;
+    void *args[] = {&p};
+    e = cudaLaunchKernelExC(&cfg, fa, args);
+    if (e != cudaSuccess) return cuda_fail(e, "row kernel launch");
+  }
+  {
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = smem_b;
+    cfg.stream = stream;
+    if (argmax) {
+      cfg.gridDim = dim3(static_cast<unsigned>(p.B), 1, 1);
+      if ((st = occupancy(fb, smem_b, 0, &per_sm))) return st;
+    } else {
+      cfg.gridDim = dim3(static_cast<unsigned>(p.B * C), 1, 1);
+      attr[na].id = cudaLaunchAttributeClusterDimension;
+      attr[na].val.clusterDim.x = C;
+      attr[na].val.clusterDim.y = 1;
+      attr[na].val.clusterDim.z = 1;
+      ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    void *args[] = {&p};
+    e = cudaLaunchKernelExC(&cfg, fb, args);
+    if (e != cudaSuccess) return cuda_fail(e, "decision kernel launch");
+  }
   return SPEC_OK;
 }
 
@@ -280,21 +310,12 @@ int verify_chain(const void *zt, const void *zd, const int32_t *x, int B, int K,
   if (!out_tokens || !out_n) return fail(SPEC_ERR_ARG, "output pointer is NULL");
   if (K > 0 && !x) return fail(SPEC_ERR_ARG, "draft_tokens is NULL");
   if (K > 0 && T > 0.f && !zd) return fail(SPEC_ERR_ARG, "draft_logits is NULL with T > 0");
-  if (static_cast<long long>(B) * (K + 1) > INT_MAX / 16) return fail(SPEC_ERR_ARG, "B*(K+1) too large");
+  if (static_cast<long long>(B) * (K + 1) * MAX_CLUSTER > INT_MAX) return fail(SPEC_ERR_ARG, "B*(K+1) too large");
 
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const int esz = dtype == SPEC_F32 ? 4 : 2;
   const bool sample = T > 0.f;
   const bool tma = (static_cast<long long>(V) * esz) % 16 == 0 && aligned16(zt) &&
                    (!sample || K == 0 || aligned16(zd));
-  const void *fn = sample ? pick_sample_kernel(dtype, tma) : pick_argmax_kernel(dtype, tma);
-  const long long njobs = static_cast<long long>(B) * (K + 1);
-  Geometry g;
-  if ((st = plan(fn, V, dtype, sample && K > 0 ? 2 : 1, sample ? 0 : 8 * (2 * K + 2), njobs, &g)))
-    return st;
-  Workspace *w = nullptr;
-  if ((st = get_ws(stream, B, K + 1, &w))) return st;
-
   Params p = {};
   p.zt = zt;
   p.zd = zd;
@@ -307,15 +328,15 @@ int verify_chain(const void *zt, const void *zd, const int32_t *x, int B, int K,
   p.kind = sample ? KIND_SAMPLE : KIND_GREEDY_CHAIN;
   p.c = static_cast<float>(cd);
   p.seed = seed;
-  p.njobs = static_cast<int>(njobs);
+  p.njobs = B * (K + 1);
   p.max_depth = 0;
   p.out_tokens = out_tokens;
   p.out_n = out_n;
   p.out_row_max = row_max;
   p.out_row_sumexp = row_sumexp;
   p.stats = reinterpret_cast<Stats *>(stats);
-  bind_ws(p, w);
-  return launch(fn, g, stream, p);
+  Workspace *w = nullptr;
+  return run_step(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr), &w);
 }
 
 int tree_depth_host(const int32_t *parent, int N) {
@@ -361,17 +382,9 @@ int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent,
   if (max_depth < 0 || max_depth >= N) return fail(SPEC_ERR_ARG, "max_depth out of range [0, N)");
   if (B == 0) return SPEC_OK;
   if (!parent || !node_tokens || !out_path || !out_len) return fail(SPEC_ERR_ARG, "NULL pointer");
-  if (static_cast<long long>(B) * N > INT_MAX / 16) return fail(SPEC_ERR_ARG, "B*N too large");
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  if (static_cast<long long>(B) * N * MAX_CLUSTER > INT_MAX) return fail(SPEC_ERR_ARG, "B*N too large");
   const int esz = dtype == SPEC_F32 ? 4 : 2;
   const bool tma = (static_cast<long long>(V) * esz) % 16 == 0 && aligned16(target_logits);
-  const int emit_smem = 17 * N + 64;
-  const void *fn = pick_argmax_kernel(dtype, tma);
-  const long long njobs = static_cast<long long>(B) * N;
-  Geometry g;
-  if ((st = plan(fn, V, dtype, 1, emit_smem, njobs, &g))) return st;
-  Workspace *w = nullptr;
-  if ((st = get_ws(stream, B, N, &w))) return st;
   Params p = {};
   p.zt = target_logits;
   p.tokens = node_tokens;
@@ -381,12 +394,12 @@ int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent,
   p.V = V;
   p.J = N;
   p.kind = KIND_TREE;
-  p.njobs = static_cast<int>(njobs);
+  p.njobs = B * N;
   p.max_depth = max_depth;
   p.out_tokens = out_path;
   p.out_n = out_len;
-  bind_ws(p, w);
-  return launch(fn, g, stream, p);
+  Workspace *w = nullptr;
+  return run_step(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr), &w);
 }
 
 int spec_tree_max_depth(const int32_t *parent_host, int N) {
@@ -403,7 +416,7 @@ int spec_tree_mask(const int32_t *parent, int B, int N, uint32_t *out_mask, int3
   if (!parent || !out_mask || !out_depth) return fail(SPEC_ERR_ARG, "NULL pointer");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   Workspace *w = nullptr;
-  int st = get_ws(stream, 1, 1, &w);
+  int st = get_ws(stream, 1, &w);
   if (st) return st;
   const int W = (N + 31) / 32;
   tree_mask_kernel<<<B, NT, 0, stream>>>(parent, N, W, out_mask, out_depth, w->status);
@@ -513,7 +526,7 @@ void spec_shutdown(void) {
   for (Workspace *w : g_ws) {
     cudaSetDevice(w->device);
     if (w->status) cudaFree(w->status);
-    if (w->ints) cudaFree(w->ints);
+    if (w->partials) cudaFree(w->partials);
     if (w->stage) cudaFree(w->stage);
     delete w;
   }
