@@ -314,23 +314,27 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 // ======================================================================
 // A. row_kernel: streaming per-(job, slice) statistics.
 // ======================================================================
-// Item it = job * C + slice; a CTA takes items blockIdx.x, + gridDim.x, ...
-// and streams their tiles through a ring of `stages` shared-memory stages
-// (each stage holds one tile of up to two rows).
+// Warp-specialised: NCW consumer warps and one producer warp.  Item it =
+// job * C + slice; a CTA takes items blockIdx.x, + gridDim.x, ...  The
+// producer streams their tiles (up to two rows each) into a ring of `stages`
+// shared-memory stages: it waits for a stage to be empty (every consumer warp
+// arrived), then issues the bulk copies that complete the stage's `full`
+// barrier.  Consumers wait on `full`, reduce, and arrive on `empty`.  At the
+// end of an item every consumer warp writes its own 16-byte partial, so no
+// barrier spans the CTA.
+constexpr int NCW = 8;                  // consumer warps
+constexpr int NT_ROW = (NCW + 1) * 32;  // + the producer warp
+
 template <int DT, bool ARGMAX>
 struct ItemCursor {
   using E = Elem<DT>;
-  int item, k, nt, lo, len, nrows, tile;
+  int item, lo, len, nt, nrows;
   const unsigned char *rt, *rd;
 
   __device__ __forceinline__ void set(const Params &p, int it) {
     item = it;
-    k = 0;
-    tile = p.tile;
-    if (it >= p.njobs * p.C) {
-      nt = 0;
-      return;
-    }
+    nt = 0;
+    if (it >= p.njobs * p.C) return;
     const int q = it / p.C, s = it - q * p.C;
     lo = s * p.slice;
     len = max(0, min(p.V, lo + p.slice) - lo);
@@ -346,101 +350,127 @@ struct ItemCursor {
       nrows = 1;
     }
   }
-  __device__ __forceinline__ int tile_len(int kk) const { return min(tile, len - kk * tile); }
 };
 
+// Bounded wait on an mbarrier phase; false if it ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = clock_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (clock_ns() - t0 > WAIT_LIMIT_NS) return false;
+  return true;
+}
+
+// Online (max, sum 2^((z - max) c)) over one vector.  mc = max(m c, -FLT_MAX)
+// keeps -inf entries at weight 0 before any finite entry was seen.
+template <int VE>
+__device__ __forceinline__ void online_vec2(const float (&f)[VE], float c, float &m, float &s,
+                                            float &mc) {
+  float vm = f[0];
+#pragma unroll
+  for (int k = 1; k < VE; ++k) vm = fmaxf(vm, f[k]);
+  if (vm > m) {
+    s *= ex2((m - vm) * c);
+    m = vm;
+    mc = fmaxf(m * c, -FLT_MAX);
+  }
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int k = 0; k < VE; k += 2) {
+    a0 += ex2(fmaf(f[k], c, -mc));
+    a1 += ex2(fmaf(f[k + 1], c, -mc));
+  }
+  s += a0 + a1;
+}
+
 template <int DT, bool TMA, bool ARGMAX>
-__global__ void __launch_bounds__(NT, 3) row_kernel(const Params p) {
+__global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
   constexpr int SROWS = ARGMAX ? 1 : 2;
+  constexpr int NC = NCW * 32;  // consumer threads
   extern __shared__ __align__(128) unsigned char dyn[];
-  __shared__ uint64_t full[MAX_STAGES];
-  __shared__ float red_a[2][NWARP], red_b[2][NWARP];
-  __shared__ int red_i[NWARP];
+  __shared__ uint64_t full[MAX_STAGES], empty[MAX_STAGES];
 
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.stages;
   const int nitems = p.njobs * p.C;
   const float c = p.c;
-  const size_t stage_bytes = static_cast<size_t>(SROWS) * p.tile * E::BYTES;
+  const size_t row_bytes = static_cast<size_t>(p.tile) * E::BYTES;
   auto stage_row = [&](int s, int r) -> unsigned char * {
-    return dyn + static_cast<size_t>(s) * stage_bytes + static_cast<size_t>(r) * p.tile * E::BYTES;
+    return dyn + (static_cast<size_t>(s) * SROWS + r) * row_bytes;
   };
 
   if (tid == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NCW);
+    }
     fence_mbar_init();
   }
   __syncthreads();
 
-  // producer cursor (thread 0 only): issues the next tile of this CTA's stream
-  ItemCursor<DT, ARGMAX> pc;
-  pc.item = nitems;
-  pc.k = pc.nt = 0;
-  int pseq = 0;
-  auto produce_one = [&]() {
-    while (pc.k >= pc.nt) {
-      if (pc.item >= nitems) return;
-      pc.set(p, pc.item + gridDim.x);
+  if (warp == NCW) {
+    // ------------------------------------------------------------ producer
+    ItemCursor<DT, ARGMAX> pc;
+    int pseq = 0;
+    bool tmo = false;
+    for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+      pc.set(p, it);
+      for (int k = 0; k < pc.nt; ++k, ++pseq) {
+        const int s = pseq % S;
+        const uint32_t round = static_cast<uint32_t>(pseq / S);
+        if (!mbar_wait_bounded(&empty[s], (round & 1u) ^ 1u)) tmo = true;
+        const int n = min(p.tile, pc.len - k * p.tile);
+        const size_t off = static_cast<size_t>(k) * row_bytes;
+        if (TMA) {
+          if (lane == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(n) * E::BYTES;
+            mbar_arrive_expect_tx(&full[s], bytes * pc.nrows);
+            bulk_g2s(stage_row(s, 0), pc.rt + off, bytes, &full[s]);
+            if (pc.nrows == 2) bulk_g2s(stage_row(s, 1), pc.rd + off, bytes, &full[s]);
+          }
+        } else {
+          const int npad = (n + VE - 1) / VE * VE;
+          for (int r = 0; r < pc.nrows; ++r) {
+            const unsigned char *g = (r ? pc.rd : pc.rt) + off;
+            unsigned char *d = stage_row(s, r);
+            for (int e = lane; e < npad; e += 32) {
+              if (e < n)
+                E::copy_elem(d + e * E::BYTES, g + e * E::BYTES);
+              else
+                E::store_neg_inf(d + e * E::BYTES);
+            }
+          }
+          __threadfence_block();  // the lanes' copies are visible before the arrival
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[s]);
+        }
+      }
     }
-    const int s = pseq % S;
-    const uint32_t bytes = static_cast<uint32_t>(pc.tile_len(pc.k)) * E::BYTES;
-    const size_t off = static_cast<size_t>(pc.k) * p.tile * E::BYTES;
-    mbar_arrive_expect_tx(&full[s], bytes * pc.nrows);
-    bulk_g2s(stage_row(s, 0), pc.rt + off, bytes, &full[s]);
-    if (pc.nrows == 2) bulk_g2s(stage_row(s, 1), pc.rd + off, bytes, &full[s]);
-    ++pc.k;
-    ++pseq;
-  };
-  if (TMA && tid == 0) {
-    pc.set(p, blockIdx.x);
-    for (int s = 0; s < S; ++s) produce_one();
+    if (tmo && lane == 0) atomicOr(p.status, ST_TIMEOUT);
+    pdl_launch_dependents();
+    return;
   }
 
-  bool timed_out = false;
-  int seq = 0;
+  // -------------------------------------------------------------- consumers
   ItemCursor<DT, ARGMAX> cc;
+  int seq = 0;
+  bool tmo = false;
   for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
     cc.set(p, it);
     float a0 = -INFINITY, a1 = 0.f, a2 = -INFINITY, a3 = 0.f;  // (m_t, s_t, m_d, s_d)
-    float ac0 = 0.f, ac2 = 0.f;                                // m * c
+    float ac0 = -FLT_MAX, ac2 = -FLT_MAX;                      // max(m c, -FLT_MAX)
     int aidx = INT_MAX;                                        // argmax index
     for (int k = 0; k < cc.nt; ++k, ++seq) {
       const int s = seq % S;
-      const int n = cc.tile_len(k);
-      if (TMA) {
-        const uint32_t par = static_cast<uint32_t>(seq / S) & 1u;
-        if (!mbar_try_wait(&full[s], par)) {
-          const uint64_t t0 = clock_ns();
-          while (!mbar_try_wait(&full[s], par)) {
-            if (clock_ns() - t0 > WAIT_LIMIT_NS) {
-              timed_out = true;
-              break;
-            }
-          }
-        }
-      } else {
-        __syncthreads();
-        const int npad = (n + VE - 1) / VE * VE;
-        const size_t off = static_cast<size_t>(k) * p.tile * E::BYTES;
-        for (int r = 0; r < cc.nrows; ++r) {
-          const unsigned char *g = (r ? cc.rd : cc.rt) + off;
-          unsigned char *d = stage_row(s, r);
-          for (int e = tid; e < npad; e += NT) {
-            if (e < n)
-              E::copy_elem(d + e * E::BYTES, g + e * E::BYTES);
-            else
-              E::store_neg_inf(d + e * E::BYTES);
-          }
-        }
-        __syncthreads();
-      }
+      if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(seq / S) & 1u)) tmo = true;
+      const int n = min(p.tile, cc.len - k * p.tile);
       const int nv = (n + VE - 1) / VE;
       const unsigned char *bt = stage_row(s, 0);
       if (ARGMAX) {
         const int base = cc.lo + k * p.tile;
-        for (int j = tid; j < nv; j += NT) {
+        for (int j = tid; j < nv; j += NC) {
           float f[VE];
           E::unpack(lds128(bt + j * 16), f);
           float vm = f[0];
@@ -455,47 +485,46 @@ __global__ void __launch_bounds__(NT, 3) row_kernel(const Params p) {
         }
       } else if (cc.nrows == 2) {
         const unsigned char *bd = stage_row(s, 1);
-        for (int j = tid; j < nv; j += NT) {
-          float f[VE];
+        for (int j = tid; j < nv; j += NC) {
+          float f[VE], g[VE];
           E::unpack(lds128(bt + j * 16), f);
-          online_vec<VE>(f, c, a0, a1, ac0);
-          E::unpack(lds128(bd + j * 16), f);
-          online_vec<VE>(f, c, a2, a3, ac2);
+          E::unpack(lds128(bd + j * 16), g);
+          online_vec2<VE>(f, c, a0, a1, ac0);
+          online_vec2<VE>(g, c, a2, a3, ac2);
         }
       } else {
-        for (int j = tid; j < nv; j += NT) {
+        for (int j = tid; j < nv; j += NC) {
           float f[VE];
           E::unpack(lds128(bt + j * 16), f);
-          online_vec<VE>(f, c, a0, a1, ac0);
+          online_vec2<VE>(f, c, a0, a1, ac0);
         }
       }
-      if (TMA) {
-        __syncthreads();  // stage s fully consumed
-        if (tid == 0) produce_one();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with stage s
+    }
+    // per-warp partial of the item (butterfly: same bits in every lane)
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      if (ARGMAX) {
+        const float v2 = __shfl_xor_sync(0xFFFFFFFFu, a0, off);
+        const int i2 = __shfl_xor_sync(0xFFFFFFFFu, aidx, off);
+        am_combine(a0, aidx, v2, i2);
+      } else {
+        float m2 = __shfl_xor_sync(0xFFFFFFFFu, a0, off), s2 = __shfl_xor_sync(0xFFFFFFFFu, a1, off);
+        ms_combine(a0, a1, m2, s2, c);
+        if (cc.nrows == 2) {
+          m2 = __shfl_xor_sync(0xFFFFFFFFu, a2, off);
+          s2 = __shfl_xor_sync(0xFFFFFFFFu, a3, off);
+          ms_combine(a2, a3, m2, s2, c);
+        }
       }
     }
-    // item partial
-    if (ARGMAX) {
-      block_reduce_argmax(a0, aidx, red_a[0], red_i);
-      if (tid == 0) p.partials[it] = make_float4(a0, __int_as_float(aidx), 0.f, 0.f);
-    } else {
-      block_reduce_ms(a0, a1, c, red_a[0], red_b[0]);
-      if (cc.nrows == 2) block_reduce_ms(a2, a3, c, red_a[1], red_b[1]);
-      if (tid == 0) p.partials[it] = make_float4(a0, a1, a2, a3);
-    }
+    if (lane == 0)
+      p.partials[static_cast<size_t>(it) * NCW + warp] =
+          ARGMAX ? make_float4(a0, __int_as_float(aidx), 0.f, 0.f) : make_float4(a0, a1, a2, a3);
   }
   pdl_launch_dependents();
-  if (timed_out) {
-    atomicOr(p.status, ST_TIMEOUT);
-    // bounded drain of any copy still in flight
-    if (TMA && tid == 0) {
-      const uint64_t t0 = clock_ns();
-      for (int q = seq; q < seq + S; ++q)
-        while (!mbar_try_wait(&full[q % S], static_cast<uint32_t>(q / S) & 1u) &&
-               clock_ns() - t0 < WAIT_LIMIT_NS) {
-        }
-    }
-  }
+  if (tmo) atomicOr(p.status, ST_TIMEOUT);
 }
 
 // ======================================================================
@@ -523,17 +552,18 @@ struct DrawShared {
   float fscratch[NWARP + 1];
 };
 
-// Combined (max, sumexp) of one row from its C slice partials, by warp:
-// lane s < C holds slice s; butterfly, so every lane ends with the same bits.
-__device__ __forceinline__ void warp_row_stats(const float4 *parts, int C, bool draft, float c,
-                                               float &m, float &s) {
+// Combined (max, sumexp) of one row from its C x NCW partials (one per
+// slice and consumer warp), by one warp: lane l folds partials l, l+32, ...
+// in order, then a butterfly, so every lane (and every CTA) ends with the
+// same bits.
+__device__ __forceinline__ void warp_row_stats(const float4 *parts, int nparts, bool draft,
+                                               float c, float &m, float &s) {
   const int lane = threadIdx.x & 31;
   m = -INFINITY;
   s = 0.f;
-  if (lane < C) {
-    const float4 v = __ldcg(parts + lane);
-    m = draft ? v.z : v.x;
-    s = draft ? v.w : v.y;
+  for (int j = lane; j < nparts; j += 32) {
+    const float4 v = __ldcg(parts + j);
+    ms_combine(m, s, draft ? v.z : v.x, draft ? v.w : v.y, c);
   }
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -570,7 +600,8 @@ __global__ void __launch_bounds__(NT) draw_kernel(const Params p) {
     const bool draft = r > K;
     const int i = draft ? r - K - 1 : r;
     float m, s;
-    warp_row_stats(p.partials + static_cast<size_t>(job_of(p, b, i)) * p.C, p.C, draft, c, m, s);
+    warp_row_stats(p.partials + static_cast<size_t>(job_of(p, b, i)) * p.C * NCW, p.C * NCW, draft,
+                   c, m, s);
     if (lane == 0) {
       rmax[r] = m;
       rsum[r] = s;
@@ -772,10 +803,10 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
   for (int r = warp; r < J; r += NWARP) {
     float v = -INFINITY;
     int idx = INT_MAX;
-    if (lane < p.C) {
-      const float4 a = __ldcg(p.partials + static_cast<size_t>(job_of(p, b, r)) * p.C + lane);
-      v = a.x;
-      idx = __float_as_int(a.y);
+    const float4 *parts = p.partials + static_cast<size_t>(job_of(p, b, r)) * p.C * NCW;
+    for (int j = lane; j < p.C * NCW; j += 32) {
+      const float4 a = __ldcg(parts + j);
+      am_combine(v, idx, a.x, __float_as_int(a.y));
     }
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {

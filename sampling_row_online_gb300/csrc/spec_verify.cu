@@ -88,7 +88,8 @@ int get_ws(cudaStream_t stream, size_t nparts, Workspace **out) {
 
 // ------------------------------------------------------------ geometry
 constexpr int SLICE_TARGET_BYTES = 16 * 1024;  // vocabulary bytes per row and slice
-constexpr int DEFAULT_STAGES = 4;               // tile ring depth
+constexpr int DEFAULT_STAGES = 3;               // tile ring depth
+constexpr int TILE_MAX_BYTES = 16 * 1024;       // tile width per row
 
 int env_int(const char *name, int dflt, int lo, int hi) {
   const char *v = std::getenv(name);
@@ -137,8 +138,8 @@ int occupancy(const void *fn, int smem, int C, int *result) {
   }
   if (kc->q_smem != smem || kc->q_C != C) {
     int n = 0;
-    if (C == 0) {
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, NT, smem);
+    if (C <= 0) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, C == -1 ? NT_ROW : NT, smem);
     } else {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(C, 1, 1);
@@ -208,7 +209,6 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
       MAX_CLUSTER, std::max<long long>(1, (row_bytes + SLICE_TARGET_BYTES - 1) / SLICE_TARGET_BYTES)));
   C = env_int("SPEC_VERIFY_SLICES", C, 1, MAX_CLUSTER);
   const int stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
-  const int tile = NT * VE * VECS_PER_THREAD;
   const void *fa = argmax ? pick_row_kernel<true>(dtype, tma) : pick_row_kernel<false>(dtype, tma);
   const void *fb = argmax ? reinterpret_cast<const void *>(&finish_kernel) : pick_draw_kernel(dtype, tma);
   int smem_b = 0;
@@ -216,7 +216,6 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
     smem_b = 4 * (3 * p.J) + (p.kind == KIND_TREE ? 9 * p.J : 0) + 16;
   else
     smem_b = 4 * (7 * p.K + 2) + 16;
-  const int smem_a = stages * srows * tile * esz;
   int st;
   // the draw needs clusters of C CTAs: shrink C until such a cluster fits
   for (;;) {
@@ -229,17 +228,20 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
   }
   const int per = (p.V + C - 1) / C;
   const int slice = (per + VE - 1) / VE * VE;
+  // tiles of up to 16 KB per row, never wider than a slice
+  const int tile = std::min(TILE_MAX_BYTES / esz, slice);
+  const int smem_a = stages * srows * tile * esz;
   // the draw walks one thread's chunk with one entry per thread: slice <= NT^2
   if (slice > NT * NT) return fail(SPEC_ERR_ARG, "vocabulary too large for the slice count");
   const long long nitems = static_cast<long long>(p.njobs) * C;
   if (nitems > INT_MAX) return fail(SPEC_ERR_ARG, "too many rows");
   int per_sm = 0;
-  if ((st = occupancy(fa, smem_a, 0, &per_sm))) return st;
+  if ((st = occupancy(fa, smem_a, -1, &per_sm))) return st;
   if (per_sm < 1) return fail(SPEC_ERR_UNSUPPORTED, "row kernel does not fit on an SM");
   const int grid_a = static_cast<int>(std::min<long long>(nitems, static_cast<long long>(per_sm) * num_sms()));
 
   Workspace *w = nullptr;
-  if ((st = get_ws(stream, static_cast<size_t>(nitems), &w))) return st;
+  if ((st = get_ws(stream, static_cast<size_t>(nitems) * NCW, &w))) return st;
   p.C = C;
   p.slice = slice;
   p.tile = tile;
@@ -252,7 +254,7 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_a), 1, 1);
-    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.blockDim = dim3(NT_ROW, 1, 1);
     cfg.dynamicSmemBytes = smem_a;
     cfg.stream = stream;
     void *args[] = {&p};
