@@ -150,26 +150,6 @@ __device__ __forceinline__ void ms_combine(float &m, float &s, float m2, float s
   m = M;
 }
 
-// Online (max, sum 2^((z - max) c)) over one vector of logits.
-template <int VE>
-__device__ __forceinline__ void online_vec(const float (&f)[VE], float c, float &m, float &s,
-                                           float &mc) {
-  float vm = f[0];
-#pragma unroll
-  for (int k = 1; k < VE; ++k) vm = fmaxf(vm, f[k]);
-  if (vm > m) {
-    s *= ex2((m - vm) * c);
-    m = vm;
-    mc = m * c;
-  }
-  if (m > -INFINITY) {
-    float a = 0.f;
-#pragma unroll
-    for (int k = 0; k < VE; ++k) a += ex2(fmaf(f[k], c, -mc));
-    s += a;
-  }
-}
-
 // Block-wide (max, sumexp) reduction; the result is valid in thread 0.
 __device__ __forceinline__ void block_reduce_ms(float &m, float &s, float c, float *sh_m,
                                                 float *sh_s) {
@@ -352,35 +332,63 @@ struct ItemCursor {
   }
 };
 
-// Bounded wait on an mbarrier phase; false if it ran out.
+// Bounded wait on an mbarrier phase; false if it ran out.  The warp sleeps
+// in hardware between polls.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
   const uint64_t t0 = clock_ns();
-  while (!mbar_try_wait(bar, parity))
+  while (!mbar_try_wait_sleep(bar, parity, 20000u))
     if (clock_ns() - t0 > WAIT_LIMIT_NS) return false;
   return true;
 }
 
-// Online (max, sum 2^((z - max) c)) over one vector.  mc = max(m c, -FLT_MAX)
+// Online (max, sum 2^((z - max) c)) state of one row in one thread; the sum
+// is kept as two lanes for the packed fp32x2 adds.  mc = max(m c, -FLT_MAX)
 // keeps -inf entries at weight 0 before any finite entry was seen.
-template <int VE>
-__device__ __forceinline__ void online_vec2(const float (&f)[VE], float c, float &m, float &s,
-                                            float &mc) {
-  float vm = f[0];
-#pragma unroll
-  for (int k = 1; k < VE; ++k) vm = fmaxf(vm, f[k]);
-  if (vm > m) {
-    s *= ex2((m - vm) * c);
-    m = vm;
-    mc = fmaxf(m * c, -FLT_MAX);
+struct Online {
+  float m, mc;
+  float2 s;
+  __device__ __forceinline__ void init() {
+    m = -INFINITY;
+    mc = -FLT_MAX;
+    s = make_float2(0.f, 0.f);
   }
-  float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-  for (int k = 0; k < VE; k += 2) {
-    a0 += ex2(fmaf(f[k], c, -mc));
-    a1 += ex2(fmaf(f[k + 1], c, -mc));
+  __device__ __forceinline__ void rescale(float vm, float c) {
+    if (vm > m) {
+      const float r = ex2((m - vm) * c);
+      s.x *= r;
+      s.y *= r;
+      m = vm;
+      mc = fmaxf(vm * c, -FLT_MAX);
+    }
   }
-  s += a0 + a1;
+  // f: an even number of logits
+  template <int N>
+  __device__ __forceinline__ void accumulate(const float (&f)[N], float c) {
+    const float2 cc = make_float2(c, c), nm = make_float2(-mc, -mc);
+#pragma unroll
+    for (int k = 0; k < N; k += 2) {
+      const float2 y = __ffma2_rn(make_float2(f[k], f[k + 1]), cc, nm);
+      s = __fadd2_rn(s, make_float2(ex2(y.x), ex2(y.y)));
+    }
+  }
+  __device__ __forceinline__ float sum() const { return s.x + s.y; }
+};
+
+// One 16-byte vector of logits into the online state.
+template <int DT>
+__device__ __forceinline__ void online_vec16(const uint4 w, float c, Online &st) {
+  float f[Elem<DT>::VE];
+  Elem<DT>::unpack(w, f);
+  float vm;
+  if (DT == 1) {  // bf16: packed maximum of the 8 values
+    const uint32_t mx = bf16x2_max(bf16x2_max(w.x, w.y), bf16x2_max(w.z, w.w));
+    vm = fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u));
+  } else {
+    vm = fmaxf(fmaxf(f[0], f[1]), fmaxf(f[2], f[3]));
+  }
+  st.rescale(vm, c);
+  st.accumulate(f, c);
 }
 
 template <int DT, bool TMA, bool ARGMAX>
@@ -459,9 +467,11 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
   bool tmo = false;
   for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
     cc.set(p, it);
-    float a0 = -INFINITY, a1 = 0.f, a2 = -INFINITY, a3 = 0.f;  // (m_t, s_t, m_d, s_d)
-    float ac0 = -FLT_MAX, ac2 = -FLT_MAX;                      // max(m c, -FLT_MAX)
-    int aidx = INT_MAX;                                        // argmax index
+    Online ot, od;  // target and draft row states
+    ot.init();
+    od.init();
+    float a0 = -INFINITY;  // argmax value
+    int aidx = INT_MAX;    // argmax index
     for (int k = 0; k < cc.nt; ++k, ++seq) {
       const int s = seq % S;
       if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(seq / S) & 1u)) tmo = true;
@@ -486,18 +496,12 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
       } else if (cc.nrows == 2) {
         const unsigned char *bd = stage_row(s, 1);
         for (int j = tid; j < nv; j += NC) {
-          float f[VE], g[VE];
-          E::unpack(lds128(bt + j * 16), f);
-          E::unpack(lds128(bd + j * 16), g);
-          online_vec2<VE>(f, c, a0, a1, ac0);
-          online_vec2<VE>(g, c, a2, a3, ac2);
+          const uint4 wt = lds128(bt + j * 16), wd = lds128(bd + j * 16);
+          online_vec16<DT>(wt, c, ot);
+          online_vec16<DT>(wd, c, od);
         }
       } else {
-        for (int j = tid; j < nv; j += NC) {
-          float f[VE];
-          E::unpack(lds128(bt + j * 16), f);
-          online_vec2<VE>(f, c, a0, a1, ac0);
-        }
+        for (int j = tid; j < nv; j += NC) online_vec16<DT>(lds128(bt + j * 16), c, ot);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with stage s
@@ -509,19 +513,24 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
         const float v2 = __shfl_xor_sync(0xFFFFFFFFu, a0, off);
         const int i2 = __shfl_xor_sync(0xFFFFFFFFu, aidx, off);
         am_combine(a0, aidx, v2, i2);
-      } else {
-        float m2 = __shfl_xor_sync(0xFFFFFFFFu, a0, off), s2 = __shfl_xor_sync(0xFFFFFFFFu, a1, off);
-        ms_combine(a0, a1, m2, s2, c);
+      }
+    }
+    float m_t = ot.m, s_t = ot.sum(), m_d = od.m, s_d = od.sum();
+    if (!ARGMAX) {
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        float m2 = __shfl_xor_sync(0xFFFFFFFFu, m_t, off), s2 = __shfl_xor_sync(0xFFFFFFFFu, s_t, off);
+        ms_combine(m_t, s_t, m2, s2, c);
         if (cc.nrows == 2) {
-          m2 = __shfl_xor_sync(0xFFFFFFFFu, a2, off);
-          s2 = __shfl_xor_sync(0xFFFFFFFFu, a3, off);
-          ms_combine(a2, a3, m2, s2, c);
+          m2 = __shfl_xor_sync(0xFFFFFFFFu, m_d, off);
+          s2 = __shfl_xor_sync(0xFFFFFFFFu, s_d, off);
+          ms_combine(m_d, s_d, m2, s2, c);
         }
       }
     }
     if (lane == 0)
       p.partials[static_cast<size_t>(it) * NCW + warp] =
-          ARGMAX ? make_float4(a0, __int_as_float(aidx), 0.f, 0.f) : make_float4(a0, a1, a2, a3);
+          ARGMAX ? make_float4(a0, __int_as_float(aidx), 0.f, 0.f) : make_float4(m_t, s_t, m_d, s_d);
   }
   pdl_launch_dependents();
   if (tmo) atomicOr(p.status, ST_TIMEOUT);
