@@ -391,6 +391,29 @@ __device__ __forceinline__ void online_vec16(const uint4 w, float c, Online &st)
   st.accumulate(f, c);
 }
 
+// What the producer tells the consumers about the tile in a stage.
+struct StageMeta {
+  int item;   // item index, or -1: end of this CTA's stream
+  int n;      // elements per row in the tile
+  int nrows;  // 1 or 2
+  int last;   // 1: last tile of the item
+  int base;   // vocabulary index of the tile's first element (argmax)
+  int pad[3];
+};
+
+// Warp-wide (max, sumexp) of per-lane online states: max butterfly, one
+// rescale per lane, sum butterfly.  Every lane ends with the same bits.
+__device__ __forceinline__ void warp_ms(float &m, float &s, float c) {
+  float M = m;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, off));
+  float t = (M == -INFINITY) ? 0.f : __fmul_rn(s, ex2((m - M) * c));
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) t = __fadd_rn(t, __shfl_xor_sync(0xFFFFFFFFu, t, off));
+  m = M;
+  s = t;
+}
+
 template <int DT, bool TMA, bool ARGMAX>
 __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
   using E = Elem<DT>;
@@ -399,10 +422,10 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
   constexpr int NC = NCW * 32;  // consumer threads
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ uint64_t full[MAX_STAGES], empty[MAX_STAGES];
+  __shared__ __align__(16) StageMeta meta[MAX_STAGES];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.stages;
-  const int nitems = p.njobs * p.C;
   const float c = p.c;
   const size_t row_bytes = static_cast<size_t>(p.tile) * E::BYTES;
   auto stage_row = [&](int s, int r) -> unsigned char * {
@@ -420,17 +443,31 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
 
   if (warp == NCW) {
     // ------------------------------------------------------------ producer
+    const int nitems = p.njobs * p.C;
     ItemCursor<DT, ARGMAX> pc;
     int pseq = 0;
     bool tmo = false;
+    auto next_stage = [&]() -> int {  // wait until the next stage is free
+      const int s = pseq % S;
+      const uint32_t round = static_cast<uint32_t>(pseq / S);
+      if (!mbar_wait_bounded(&empty[s], (round & 1u) ^ 1u)) tmo = true;
+      return s;
+    };
     for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
       pc.set(p, it);
       for (int k = 0; k < pc.nt; ++k, ++pseq) {
-        const int s = pseq % S;
-        const uint32_t round = static_cast<uint32_t>(pseq / S);
-        if (!mbar_wait_bounded(&empty[s], (round & 1u) ^ 1u)) tmo = true;
+        const int s = next_stage();
         const int n = min(p.tile, pc.len - k * p.tile);
         const size_t off = static_cast<size_t>(k) * row_bytes;
+        if (lane == 0) {
+          StageMeta m;
+          m.item = it;
+          m.n = n;
+          m.nrows = pc.nrows;
+          m.last = (k == pc.nt - 1);
+          m.base = pc.lo + k * p.tile;
+          meta[s] = m;
+        }
         if (TMA) {
           if (lane == 0) {
             const uint32_t bytes = static_cast<uint32_t>(n) * E::BYTES;
@@ -455,6 +492,18 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
           if (lane == 0) mbar_arrive(&full[s]);
         }
       }
+      if (pc.nt == 0 && lane == 0) {  // an empty slice still gets its (neutral) partial
+        for (int w = 0; w < NCW; ++w)
+          p.partials[static_cast<size_t>(it) * NCW + w] =
+              ARGMAX ? make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f)
+                     : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+      }
+    }
+    // end of stream
+    const int s = next_stage();
+    if (lane == 0) {
+      meta[s].item = -1;
+      mbar_arrive(&full[s]);
     }
     if (tmo && lane == 0) atomicOr(p.status, ST_TIMEOUT);
     pdl_launch_dependents();
@@ -462,75 +511,67 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
   }
 
   // -------------------------------------------------------------- consumers
-  ItemCursor<DT, ARGMAX> cc;
-  int seq = 0;
   bool tmo = false;
-  for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
-    cc.set(p, it);
-    Online ot, od;  // target and draft row states
-    ot.init();
-    od.init();
-    float a0 = -INFINITY;  // argmax value
-    int aidx = INT_MAX;    // argmax index
-    for (int k = 0; k < cc.nt; ++k, ++seq) {
-      const int s = seq % S;
-      if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(seq / S) & 1u)) tmo = true;
-      const int n = min(p.tile, cc.len - k * p.tile);
-      const int nv = (n + VE - 1) / VE;
-      const unsigned char *bt = stage_row(s, 0);
-      if (ARGMAX) {
-        const int base = cc.lo + k * p.tile;
-        for (int j = tid; j < nv; j += NC) {
-          float f[VE];
-          E::unpack(lds128(bt + j * 16), f);
-          float vm = f[0];
+  Online ot, od;  // target and draft row states
+  ot.init();
+  od.init();
+  float av = -INFINITY;  // argmax value
+  int aidx = INT_MAX;    // argmax index
+  for (int seq = 0;; ++seq) {
+    const int s = seq % S;
+    if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(seq / S) & 1u)) tmo = true;
+    const StageMeta m = meta[s];
+    if (m.item < 0) break;
+    const int nv = (m.n + VE - 1) / VE;
+    const unsigned char *bt = stage_row(s, 0);
+    if (ARGMAX) {
+      for (int j = tid; j < nv; j += NC) {
+        float f[VE];
+        E::unpack(lds128(bt + j * 16), f);
+        float vm = f[0];
 #pragma unroll
-          for (int e = 1; e < VE; ++e) vm = fmaxf(vm, f[e]);
-          if (vm > a0) {  // rare after the first few vectors
-            a0 = vm;
+        for (int e = 1; e < VE; ++e) vm = fmaxf(vm, f[e]);
+        if (vm > av) {  // rare after the first few vectors
+          av = vm;
 #pragma unroll
-            for (int e = VE - 1; e >= 0; --e)
-              if (f[e] == vm) aidx = base + j * VE + e;
-          }
+          for (int e = VE - 1; e >= 0; --e)
+            if (f[e] == vm) aidx = m.base + j * VE + e;
         }
-      } else if (cc.nrows == 2) {
-        const unsigned char *bd = stage_row(s, 1);
-        for (int j = tid; j < nv; j += NC) {
-          const uint4 wt = lds128(bt + j * 16), wd = lds128(bd + j * 16);
-          online_vec16<DT>(wt, c, ot);
-          online_vec16<DT>(wd, c, od);
-        }
-      } else {
-        for (int j = tid; j < nv; j += NC) online_vec16<DT>(lds128(bt + j * 16), c, ot);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with stage s
-    }
-    // per-warp partial of the item (butterfly: same bits in every lane)
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      if (ARGMAX) {
-        const float v2 = __shfl_xor_sync(0xFFFFFFFFu, a0, off);
-        const int i2 = __shfl_xor_sync(0xFFFFFFFFu, aidx, off);
-        am_combine(a0, aidx, v2, i2);
+    } else if (m.nrows == 2) {
+      const unsigned char *bd = stage_row(s, 1);
+      for (int j = tid; j < nv; j += NC) {
+        const uint4 wt = lds128(bt + j * 16), wd = lds128(bd + j * 16);
+        online_vec16<DT>(wt, c, ot);
+        online_vec16<DT>(wd, c, od);
       }
+    } else {
+      for (int j = tid; j < nv; j += NC) online_vec16<DT>(lds128(bt + j * 16), c, ot);
     }
-    float m_t = ot.m, s_t = ot.sum(), m_d = od.m, s_d = od.sum();
-    if (!ARGMAX) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with stage s
+    if (!m.last) continue;
+    // end of the item: one partial per warp
+    float4 out;
+    if (ARGMAX) {
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
-        float m2 = __shfl_xor_sync(0xFFFFFFFFu, m_t, off), s2 = __shfl_xor_sync(0xFFFFFFFFu, s_t, off);
-        ms_combine(m_t, s_t, m2, s2, c);
-        if (cc.nrows == 2) {
-          m2 = __shfl_xor_sync(0xFFFFFFFFu, m_d, off);
-          s2 = __shfl_xor_sync(0xFFFFFFFFu, s_d, off);
-          ms_combine(m_d, s_d, m2, s2, c);
-        }
+        const float v2 = __shfl_xor_sync(0xFFFFFFFFu, av, off);
+        const int i2 = __shfl_xor_sync(0xFFFFFFFFu, aidx, off);
+        am_combine(av, aidx, v2, i2);
       }
+      out = make_float4(av, __int_as_float(aidx), 0.f, 0.f);
+      av = -INFINITY;
+      aidx = INT_MAX;
+    } else {
+      float m_t = ot.m, s_t = ot.sum(), m_d = od.m, s_d = od.sum();
+      warp_ms(m_t, s_t, c);
+      if (m.nrows == 2) warp_ms(m_d, s_d, c);
+      out = make_float4(m_t, s_t, m_d, s_d);
+      ot.init();
+      od.init();
     }
-    if (lane == 0)
-      p.partials[static_cast<size_t>(it) * NCW + warp] =
-          ARGMAX ? make_float4(a0, __int_as_float(aidx), 0.f, 0.f) : make_float4(m_t, s_t, m_d, s_d);
+    if (lane == 0) p.partials[static_cast<size_t>(m.item) * NCW + warp] = out;
   }
   pdl_launch_dependents();
   if (tmo) atomicOr(p.status, ST_TIMEOUT);
