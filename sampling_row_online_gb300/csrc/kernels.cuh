@@ -602,29 +602,42 @@ struct DrawShared {
   float fscratch[NWARP + 1];
 };
 
-// Combined (max, sumexp) of one row from its C x NCW partials (one per
-// slice and consumer warp), by one warp: lane l folds partials l, l+32, ...
-// in order, then a butterfly, so every lane (and every CTA) ends with the
-// same bits.
-__device__ __forceinline__ void warp_row_stats(const float4 *parts, int nparts, bool draft,
-                                               float c, float &m, float &s) {
+// Combined (max, sumexp) of rows from their C x NCW partials (one per slice
+// and consumer warp), by one warp: every load of the warp's rows is issued
+// before any is used; lane l folds partials l, l+32, l+64, l+96 in order,
+// then a butterfly, so every lane (and every CTA) ends with the same bits.
+constexpr int PARTS_PER_LANE = MAX_CLUSTER * NCW / 32;
+
+__device__ __forceinline__ void warp_row_stats2(const float4 *pa, bool da, const float4 *pb, bool db,
+                                                int nparts, float c, float &ma, float &sa,
+                                                float &mb, float &sb) {
   const int lane = threadIdx.x & 31;
-  m = -INFINITY;
-  s = 0.f;
-  for (int j = lane; j < nparts; j += 32) {
-    const float4 v = __ldcg(parts + j);
-    ms_combine(m, s, draft ? v.z : v.x, draft ? v.w : v.y, c);
+  float4 va[PARTS_PER_LANE], vb[PARTS_PER_LANE];
+#pragma unroll
+  for (int k = 0; k < PARTS_PER_LANE; ++k) {
+    const int j = lane + 32 * k;
+    va[k] = (pa && j < nparts) ? __ldcg(pa + j) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+    vb[k] = (pb && j < nparts) ? __ldcg(pb + j) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+  }
+  ma = mb = -INFINITY;
+  sa = sb = 0.f;
+#pragma unroll
+  for (int k = 0; k < PARTS_PER_LANE; ++k) {
+    ms_combine(ma, sa, da ? va[k].z : va[k].x, da ? va[k].w : va[k].y, c);
+    ms_combine(mb, sb, db ? vb[k].z : vb[k].x, db ? vb[k].w : vb[k].y, c);
   }
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, off);
-    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, off);
-    ms_combine(m, s, m2, s2, c);
+    float m2 = __shfl_xor_sync(0xFFFFFFFFu, ma, off), s2 = __shfl_xor_sync(0xFFFFFFFFu, sa, off);
+    ms_combine(ma, sa, m2, s2, c);
+    m2 = __shfl_xor_sync(0xFFFFFFFFu, mb, off);
+    s2 = __shfl_xor_sync(0xFFFFFFFFu, sb, off);
+    ms_combine(mb, sb, m2, s2, c);
   }
 }
 
 template <int DT, bool TMA>
-__global__ void __launch_bounds__(NT) draw_kernel(const Params p) {
+__global__ void __launch_bounds__(NT, 2) draw_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
   extern __shared__ __align__(16) float dsh[];  // row max [R], row sumexp [R], logits at x [2K], ok [K]
@@ -639,31 +652,44 @@ __global__ void __launch_bounds__(NT) draw_kernel(const Params p) {
   const float c = p.c;
   float *rmax = dsh, *rsum = dsh + R, *gx = dsh + 2 * R;
   int *gok = reinterpret_cast<int *>(dsh + 2 * R + 2 * K);
+  float *gu = dsh + 2 * R + 3 * K;  // acceptance uniforms [K]
 
   // every CTA of the cluster must be running before any DSMEM store: arrive
   // now, wait before the first push
   cluster_arrive_relaxed();
-  pdl_wait();  // the row partials of the first launch are complete and visible
 
-  // ---- normalisers of the 2K+1 rows (target 0..K, then draft 0..K-1)
-  for (int r = warp; r < R; r += NWARP) {
-    const bool draft = r > K;
-    const int i = draft ? r - K - 1 : r;
-    float m, s;
-    warp_row_stats(p.partials + static_cast<size_t>(job_of(p, b, i)) * p.C * NCW, p.C * NCW, draft,
-                   c, m, s);
-    if (lane == 0) {
-      rmax[r] = m;
-      rsum[r] = s;
-    }
-  }
-  // ---- draft tokens and their two logits
+  // ---- inputs that do not depend on the first launch: draft tokens, their
+  // two logits, the acceptance uniforms (overlaps the first launch's tail)
   for (int i = tid; i < K; i += NT) {
     const int x = __ldg(p.tokens + static_cast<size_t>(b) * K + i);
     const int ok = x >= 0 && x < p.V;
     gok[i] = ok;
     gx[2 * i] = ok ? E::load(target_row<DT>(p, b, i), x) : 0.f;
     gx[2 * i + 1] = ok ? E::load(draft_row<DT>(p, b, i), x) : 0.f;
+    gu[i] = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
+  }
+
+  pdl_wait();  // the row partials of the first launch are complete and visible
+
+  // ---- normalisers of the 2K+1 rows (target 0..K, then draft 0..K-1), two
+  // rows per warp per round
+  const int nparts = p.C * NCW;
+  for (int r = warp; r < R; r += 2 * NWARP) {
+    const int r2 = r + NWARP;
+    const bool da = r > K, db = r2 > K;
+    const float4 *pa = p.partials + static_cast<size_t>(job_of(p, b, da ? r - K - 1 : r)) * nparts;
+    const float4 *pb = r2 < R ? p.partials + static_cast<size_t>(job_of(p, b, db ? r2 - K - 1 : r2)) * nparts
+                              : nullptr;
+    float ma, sa, mb, sb;
+    warp_row_stats2(pa, da, pb, db, nparts, c, ma, sa, mb, sb);
+    if (lane == 0) {
+      rmax[r] = ma;
+      rsum[r] = sa;
+      if (r2 < R) {
+        rmax[r2] = mb;
+        rsum[r2] = sb;
+      }
+    }
   }
   __syncthreads();
 
@@ -676,8 +702,7 @@ __global__ void __launch_bounds__(NT) draw_kernel(const Params p) {
       const float a = fmaf(gx[2 * i], c, -(rmax[i] * c));
       const float d = fmaf(gx[2 * i + 1], c, -(rmax[K + 1 + i] * c));
       const float ratio = ex2(a - d) * (rsum[K + 1 + i] / rsum[i]);  // p_i(x_i) / q_i(x_i)
-      const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
-      if (!(u < ratio)) {
+      if (!(gu[i] < ratio)) {
         n = i;
         break;
       }
@@ -849,15 +874,21 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
   int *s_tok = ish + J;                                     // [J]
   float *s_vmax = reinterpret_cast<float *>(ish + 2 * J);  // [J]
 
+  const int ntok = p.kind == KIND_TREE ? J : p.K;
+  for (int e = tid; e < ntok; e += NT) s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * ntok + e);
   pdl_wait();
+  const int nparts = p.C * NCW;
   for (int r = warp; r < J; r += NWARP) {
     float v = -INFINITY;
     int idx = INT_MAX;
-    const float4 *parts = p.partials + static_cast<size_t>(job_of(p, b, r)) * p.C * NCW;
-    for (int j = lane; j < p.C * NCW; j += 32) {
-      const float4 a = __ldcg(parts + j);
-      am_combine(v, idx, a.x, __float_as_int(a.y));
-    }
+    const float4 *parts = p.partials + static_cast<size_t>(job_of(p, b, r)) * nparts;
+    float4 a[PARTS_PER_LANE];
+#pragma unroll
+    for (int k = 0; k < PARTS_PER_LANE; ++k)
+      a[k] = lane + 32 * k < nparts ? __ldcg(parts + lane + 32 * k)
+                                    : make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < PARTS_PER_LANE; ++k) am_combine(v, idx, a[k].x, __float_as_int(a[k].y));
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, off);
@@ -869,8 +900,6 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
       s_vmax[r] = v;
     }
   }
-  const int ntok = p.kind == KIND_TREE ? J : p.K;
-  for (int e = tid; e < ntok; e += NT) s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * ntok + e);
   __syncthreads();
 
   if (p.kind == KIND_GREEDY_CHAIN) {

@@ -215,7 +215,7 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
   if (argmax)
     smem_b = 4 * (3 * p.J) + (p.kind == KIND_TREE ? 9 * p.J : 0) + 16;
   else
-    smem_b = 4 * (7 * p.K + 2) + 16;
+    smem_b = 4 * (8 * p.K + 2) + 16;
   int st;
   // the draw needs clusters of C CTAs: shrink C until such a cluster fits
   for (;;) {
