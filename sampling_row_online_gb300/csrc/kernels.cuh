@@ -69,8 +69,9 @@ struct Params {
   int kind;
   float c;                  // log2(e) / T
   uint64_t seed;
-  int C;                    // vocabulary slices per row (= cluster size of the draw)
+  int C;                    // vocabulary slices per row in the streaming kernel
   int slice;                // elements per slice (multiple of the vector width)
+  int slice_d;              // elements per CTA in the draw (multiple of the vector width)
   int tile;                 // elements per tile and row
   int stages;               // shared-memory stages of the tile ring
   int njobs;                // jobs in total; items = njobs * C
@@ -596,6 +597,7 @@ struct Weights {
 
 struct DrawShared {
   float xz[2][MAX_CLUSTER];  // slice masses pushed by every CTA (round 0 / 1)
+  alignas(16) float dec[8];  // rank 0's decision, pushed: n, err, m_t, S_t, m_d, S_d
   float bf[8];
   int bi[8];
   int scratch[NWARP];
@@ -636,17 +638,22 @@ __device__ __forceinline__ void warp_row_stats2(const float4 *pa, bool da, const
   }
 }
 
+// Rank 0 of the cluster combines the partials of all 2K+1 rows and takes
+// the left-to-right decisions; every CTA then draws over its own slice of
+// the vocabulary (slice_d elements, independent of the streaming kernel's
+// slices).
 template <int DT, bool TMA>
 __global__ void __launch_bounds__(NT, 2) draw_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
-  extern __shared__ __align__(16) float dsh[];  // row max [R], row sumexp [R], logits at x [2K], ok [K]
+  constexpr int BATCH = 8;  // 16-byte vectors per row loaded before use
+  extern __shared__ __align__(16) float dsh[];  // row max [R], row sumexp [R], logits at x [2K], ok [K], u [K]
   __shared__ DrawShared sh;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_rank();
-  const uint32_t C = cluster_size();
-  const int b = blockIdx.x / C;
+  const uint32_t CD = cluster_size();
+  const int b = blockIdx.x / CD;
   const int K = p.K;
   const int R = 2 * K + 1;
   const float c = p.c;
@@ -655,65 +662,62 @@ __global__ void __launch_bounds__(NT, 2) draw_kernel(const Params p) {
   float *gu = dsh + 2 * R + 3 * K;  // acceptance uniforms [K]
 
   // every CTA of the cluster must be running before any DSMEM store: arrive
-  // now, wait before the first push
+  // now, wait before the first store
   cluster_arrive_relaxed();
 
-  // ---- inputs that do not depend on the first launch: draft tokens, their
-  // two logits, the acceptance uniforms (overlaps the first launch's tail)
-  for (int i = tid; i < K; i += NT) {
-    const int x = __ldg(p.tokens + static_cast<size_t>(b) * K + i);
-    const int ok = x >= 0 && x < p.V;
-    gok[i] = ok;
-    gx[2 * i] = ok ? E::load(target_row<DT>(p, b, i), x) : 0.f;
-    gx[2 * i + 1] = ok ? E::load(draft_row<DT>(p, b, i), x) : 0.f;
-    gu[i] = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
+  if (rank == 0) {
+    // ---- inputs that do not depend on the first launch (overlaps its tail)
+    for (int i = tid; i < K; i += NT) {
+      const int x = __ldg(p.tokens + static_cast<size_t>(b) * K + i);
+      const int ok = x >= 0 && x < p.V;
+      gok[i] = ok;
+      gx[2 * i] = ok ? E::load(target_row<DT>(p, b, i), x) : 0.f;
+      gx[2 * i + 1] = ok ? E::load(draft_row<DT>(p, b, i), x) : 0.f;
+      gu[i] = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
+    }
   }
-
   pdl_wait();  // the row partials of the first launch are complete and visible
 
-  // ---- normalisers of the 2K+1 rows (target 0..K, then draft 0..K-1), two
-  // rows per warp per round
-  const int nparts = p.C * NCW;
-  for (int r = warp; r < R; r += 2 * NWARP) {
-    const int r2 = r + NWARP;
-    const bool da = r > K, db = r2 > K;
-    const float4 *pa = p.partials + static_cast<size_t>(job_of(p, b, da ? r - K - 1 : r)) * nparts;
-    const float4 *pb = r2 < R ? p.partials + static_cast<size_t>(job_of(p, b, db ? r2 - K - 1 : r2)) * nparts
-                              : nullptr;
-    float ma, sa, mb, sb;
-    warp_row_stats2(pa, da, pb, db, nparts, c, ma, sa, mb, sb);
-    if (lane == 0) {
-      rmax[r] = ma;
-      rsum[r] = sa;
-      if (r2 < R) {
-        rmax[r2] = mb;
-        rsum[r2] = sb;
-      }
-    }
-  }
-  __syncthreads();
-
-  // ---- left-to-right acceptance: the first reject n (or K)
-  if (tid == 0) {
-    int n = K, err = 0;
-    for (int i = 0; i < K; ++i)
-      if (!gok[i]) err = 1;
-    for (int i = 0; i < K && !err; ++i) {
-      const float a = fmaf(gx[2 * i], c, -(rmax[i] * c));
-      const float d = fmaf(gx[2 * i + 1], c, -(rmax[K + 1 + i] * c));
-      const float ratio = ex2(a - d) * (rsum[K + 1 + i] / rsum[i]);  // p_i(x_i) / q_i(x_i)
-      if (!(gu[i] < ratio)) {
-        n = i;
-        break;
-      }
-    }
-    sh.bi[0] = n;
-    sh.bi[1] = err;
-  }
-  __syncthreads();
-  const int n = sh.bi[0];
-  const int err = sh.bi[1];
   if (rank == 0) {
+    // ---- normalisers of the 2K+1 rows (target 0..K, then draft 0..K-1)
+    const int nparts = p.C * NCW;
+    for (int r = warp; r < R; r += 2 * NWARP) {
+      const int r2 = r + NWARP;
+      const bool da = r > K, db = r2 > K;
+      const float4 *pa = p.partials + static_cast<size_t>(job_of(p, b, da ? r - K - 1 : r)) * nparts;
+      const float4 *pb =
+          r2 < R ? p.partials + static_cast<size_t>(job_of(p, b, db ? r2 - K - 1 : r2)) * nparts : nullptr;
+      float ma, sa, mb, sb;
+      warp_row_stats2(pa, da, pb, db, nparts, c, ma, sa, mb, sb);
+      if (lane == 0) {
+        rmax[r] = ma;
+        rsum[r] = sa;
+        if (r2 < R) {
+          rmax[r2] = mb;
+          rsum[r2] = sb;
+        }
+      }
+    }
+    __syncthreads();
+    // ---- left-to-right acceptance: the first reject n (or K)
+    if (tid == 0) {
+      int n = K, err = 0;
+      for (int i = 0; i < K; ++i)
+        if (!gok[i]) err = 1;
+      for (int i = 0; i < K && !err; ++i) {
+        const float a = fmaf(gx[2 * i], c, -(rmax[i] * c));
+        const float d = fmaf(gx[2 * i + 1], c, -(rmax[K + 1 + i] * c));
+        const float ratio = ex2(a - d) * (rsum[K + 1 + i] / rsum[i]);  // p_i(x_i) / q_i(x_i)
+        if (!(gu[i] < ratio)) {
+          n = i;
+          break;
+        }
+      }
+      sh.bi[0] = n;
+      sh.bi[1] = err;
+    }
+    __syncthreads();
+    const int n = sh.bi[0], err = sh.bi[1];
     for (int r = tid; r < R; r += NT) {
       if (p.out_row_max) p.out_row_max[static_cast<size_t>(b) * R + r] = rmax[r];
       if (p.out_row_sumexp) p.out_row_sumexp[static_cast<size_t>(b) * R + r] = rsum[r];
@@ -726,39 +730,61 @@ __global__ void __launch_bounds__(NT, 2) draw_kernel(const Params p) {
         if (p.stats) atomicAdd(&p.stats->errors, 1ull);
       }
     }
+    cluster_wait();  // every peer is running
+    if (tid < static_cast<int>(CD)) {  // push the decision into every CTA
+      const bool pair = n < K;
+      dsmem_st_v4f32(dsmem_addr(&sh.dec[0], tid), __int_as_float(n), __int_as_float(err), rmax[n],
+                     rsum[n]);
+      dsmem_st_f32(dsmem_addr(&sh.dec[4], tid), pair ? rmax[K + 1 + n] : 0.f);
+      dsmem_st_f32(dsmem_addr(&sh.dec[5], tid), pair ? rsum[K + 1 + n] : 1.f);
+    }
+  } else {
+    cluster_wait();
   }
+  cluster_sync();  // the decision is visible in every CTA
+  const int n = __float_as_int(sh.dec[0]);
+  const int err = __float_as_int(sh.dec[1]);
 
-  if (err) cluster_wait();
   if (!err) {
     // ---- the draw: residual at n < K, or the bonus from row K
     const bool pair = n < K;
     const unsigned char *rt = target_row<DT>(p, b, n);
     const unsigned char *rd = pair ? draft_row<DT>(p, b, n) : nullptr;
-    const int lo = static_cast<int>(rank) * p.slice;
-    const int len = max(0, min(p.V, lo + p.slice) - lo);
+    const int lo = static_cast<int>(rank) * p.slice_d;
+    const int len = max(0, min(p.V, lo + p.slice_d) - lo);
     const int E2 = ((len + NT - 1) / NT + VE - 1) / VE * VE;
     const int e0 = min(len, tid * E2), e1 = min(len, e0 + E2);
     Weights W;
     W.c = c;
-    W.mtc = rmax[n] * c;
-    W.mdc = pair ? rmax[K + 1 + n] * c : 0.f;
-    W.inv_st = 1.f / rsum[n];
-    W.inv_sd = pair ? 1.f / rsum[K + 1 + n] : 0.f;
+    W.mtc = sh.dec[2] * c;
+    W.mdc = sh.dec[4] * c;
+    W.inv_st = 1.f / sh.dec[3];
+    W.inv_sd = 1.f / sh.dec[5];
     W.resid = pair;
-    cluster_wait();
     int fallback = 0, owner = 0, pl = 0;
     float tl = 0.f, excl = 0.f, sum = 0.f;
     for (int round = 0; round < 2; ++round) {
       sum = 0.f;
       if (TMA) {
-#pragma unroll 4
-        for (int e = e0; e < e1; e += VE) {
-          const size_t off = static_cast<size_t>(lo + e) * E::BYTES;
-          float ft[VE], fd[VE];
-          E::unpack(__ldcg(reinterpret_cast<const uint4 *>(rt + off)), ft);
-          if (W.resid) E::unpack(__ldcg(reinterpret_cast<const uint4 *>(rd + off)), fd);
+        for (int e = e0; e < e1; e += BATCH * VE) {
+          uint4 vt[BATCH], vd[BATCH];
 #pragma unroll
-          for (int j = 0; j < VE; ++j) sum = __fadd_rn(sum, W(ft[j], W.resid ? fd[j] : 0.f));
+          for (int k = 0; k < BATCH; ++k) {
+            const int ek = e + k * VE;
+            const size_t off = static_cast<size_t>(lo + ek) * E::BYTES;
+            vt[k] = ek < e1 ? __ldcg(reinterpret_cast<const uint4 *>(rt + off)) : make_uint4(0, 0, 0, 0);
+            vd[k] = (ek < e1 && W.resid) ? __ldcg(reinterpret_cast<const uint4 *>(rd + off))
+                                         : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int k = 0; k < BATCH; ++k) {
+            if (e + k * VE >= e1) break;
+            float ft[VE], fd[VE];
+            E::unpack(vt[k], ft);
+            E::unpack(vd[k], fd);
+#pragma unroll
+            for (int j = 0; j < VE; ++j) sum = __fadd_rn(sum, W(ft[j], fd[j]));
+          }
         }
       } else {
         for (int e = e0; e < e1; ++e)
@@ -766,11 +792,11 @@ __global__ void __launch_bounds__(NT, 2) draw_kernel(const Params p) {
       }
       float total;
       excl = block_exclusive_scan(sum, sh.fscratch, &total);
-      if (tid < static_cast<int>(C)) dsmem_st_f32(dsmem_addr(&sh.xz[round][rank], tid), total);
+      if (tid < static_cast<int>(CD)) dsmem_st_f32(dsmem_addr(&sh.xz[round][rank], tid), total);
       cluster_sync();  // slice masses visible cluster-wide
       if (tid == 0) {
         float Z = 0.f;
-        for (uint32_t r = 0; r < C; ++r) Z = __fadd_rn(Z, sh.xz[round][r]);
+        for (uint32_t r = 0; r < CD; ++r) Z = __fadd_rn(Z, sh.xz[round][r]);
         int again = 0;
         if (W.resid && !(Z > 0.f)) {
           again = 1;  // no residual mass in fp32: draw from p at this position
@@ -778,7 +804,7 @@ __global__ void __launch_bounds__(NT, 2) draw_kernel(const Params p) {
           const float t = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(n), 1u) * Z;
           float P = 0.f, Pown = 0.f, Plast = 0.f;
           int own = -1, last = -1;
-          for (uint32_t r = 0; r < C; ++r) {
+          for (uint32_t r = 0; r < CD; ++r) {
             const float zr = sh.xz[round][r];
             if (own < 0 && __fadd_rn(P, zr) > t) {
               own = static_cast<int>(r);

@@ -90,6 +90,7 @@ int get_ws(cudaStream_t stream, size_t nparts, Workspace **out) {
 constexpr int SLICE_TARGET_BYTES = 16 * 1024;  // vocabulary bytes per row and slice
 constexpr int DEFAULT_STAGES = 3;               // tile ring depth
 constexpr int TILE_MAX_BYTES = 16 * 1024;       // tile width per row
+constexpr int DRAW_CLUSTER = 8;                 // CTAs per sequence in the draw
 
 int env_int(const char *name, int dflt, int lo, int hi) {
   const char *v = std::getenv(name);
@@ -217,22 +218,26 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
   else
     smem_b = 4 * (8 * p.K + 2) + 16;
   int st;
-  // the draw needs clusters of C CTAs: shrink C until such a cluster fits
+  // the draw: clusters of CD CTAs, each CTA walking one thread's chunk with
+  // one entry per thread, so a draw slice holds at most NT^2 entries
+  int CD = env_int("SPEC_VERIFY_DRAW_CLUSTER", DRAW_CLUSTER, 1, MAX_CLUSTER);
+  while (CD < MAX_CLUSTER && (p.V + CD - 1) / CD > NT * NT - VE) CD *= 2;
   for (;;) {
     if (argmax) break;
     int nclus = 0;
-    if ((st = occupancy(fb, smem_b, C, &nclus))) return st;
+    if ((st = occupancy(fb, smem_b, CD, &nclus))) return st;
     if (nclus > 0) break;
-    if (C == 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster fits on the device");
-    C = C > 8 ? 8 : C / 2;
+    if (CD == 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster fits on the device");
+    CD = CD > 8 ? 8 : CD / 2;
   }
+  const int per_d = (p.V + CD - 1) / CD;
+  const int slice_d = (per_d + VE - 1) / VE * VE;
+  if (!argmax && slice_d > NT * NT) return fail(SPEC_ERR_ARG, "vocabulary too large");
   const int per = (p.V + C - 1) / C;
   const int slice = (per + VE - 1) / VE * VE;
   // tiles of up to 16 KB per row, never wider than a slice
   const int tile = std::min(TILE_MAX_BYTES / esz, slice);
   const int smem_a = stages * srows * tile * esz;
-  // the draw walks one thread's chunk with one entry per thread: slice <= NT^2
-  if (slice > NT * NT) return fail(SPEC_ERR_ARG, "vocabulary too large for the slice count");
   const long long nitems = static_cast<long long>(p.njobs) * C;
   if (nitems > INT_MAX) return fail(SPEC_ERR_ARG, "too many rows");
   int per_sm = 0;
@@ -244,6 +249,7 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
   if ((st = get_ws(stream, static_cast<size_t>(nitems) * NCW, &w))) return st;
   p.C = C;
   p.slice = slice;
+  p.slice_d = slice_d;
   p.tile = tile;
   p.stages = stages;
   p.partials = w->partials;
@@ -275,9 +281,9 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
       cfg.gridDim = dim3(static_cast<unsigned>(p.B), 1, 1);
       if ((st = occupancy(fb, smem_b, 0, &per_sm))) return st;
     } else {
-      cfg.gridDim = dim3(static_cast<unsigned>(p.B * C), 1, 1);
+      cfg.gridDim = dim3(static_cast<unsigned>(p.B * CD), 1, 1);
       attr[na].id = cudaLaunchAttributeClusterDimension;
-      attr[na].val.clusterDim.x = C;
+      attr[na].val.clusterDim.x = CD;
       attr[na].val.clusterDim.y = 1;
       attr[na].val.clusterDim.z = 1;
       ++na;
