@@ -72,6 +72,8 @@ struct Params {
   int C;                    // vocabulary slices per row in the streaming kernel
   int slice;                // elements per slice (multiple of the vector width)
   int slice_d;              // elements per CTA in the draw (multiple of the vector width)
+  int draw_staged;          // 1: the draw stages its slice in shared memory
+  int draw_stage_off;       // byte offset of that staging area in dynamic smem
   int tile;                 // elements per tile and row
   int stages;               // shared-memory stages of the tile ring
   int njobs;                // jobs in total; items = njobs * C
@@ -102,6 +104,9 @@ struct Elem<0> {  // fp32
   __device__ static __forceinline__ float load(const unsigned char *row, int i) {
     return __ldg(reinterpret_cast<const float *>(row) + i);
   }
+  __device__ static __forceinline__ float load_shared(const unsigned char *row, int i) {
+    return reinterpret_cast<const float *>(row)[i];
+  }
   __device__ static __forceinline__ void store_neg_inf(unsigned char *p) {
     *reinterpret_cast<uint32_t *>(p) = 0xFF800000u;
   }
@@ -127,6 +132,9 @@ struct Elem<1> {  // bfloat16: the upper half of an fp32
   __device__ static __forceinline__ float load(const unsigned char *row, int i) {
     const unsigned short h = __ldg(reinterpret_cast<const unsigned short *>(row) + i);
     return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  }
+  __device__ static __forceinline__ float load_shared(const unsigned char *row, int i) {
+    return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t *>(row)[i]) << 16);
   }
   __device__ static __forceinline__ void store_neg_inf(unsigned char *p) {
     *reinterpret_cast<uint16_t *>(p) = 0xFF80u;
@@ -596,6 +604,7 @@ struct Weights {
 };
 
 struct DrawShared {
+  uint64_t bar;              // completion of the slice's bulk copies
   float xz[2][MAX_CLUSTER];  // slice masses pushed by every CTA (round 0 / 1)
   alignas(16) float dec[8];  // rank 0's decision, pushed: n, err, m_t, S_t, m_d, S_d
   float bf[8];
@@ -643,10 +652,9 @@ __device__ __forceinline__ void warp_row_stats2(const float4 *pa, bool da, const
 // the vocabulary (slice_d elements, independent of the streaming kernel's
 // slices).
 template <int DT, bool TMA>
-__global__ void __launch_bounds__(NT, 2) draw_kernel(const Params p) {
+__global__ void __launch_bounds__(NT, 3) draw_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
-  constexpr int BATCH = 8;  // 16-byte vectors per row loaded before use
   extern __shared__ __align__(16) float dsh[];  // row max [R], row sumexp [R], logits at x [2K], ok [K], u [K]
   __shared__ DrawShared sh;
 
@@ -661,6 +669,11 @@ __global__ void __launch_bounds__(NT, 2) draw_kernel(const Params p) {
   int *gok = reinterpret_cast<int *>(dsh + 2 * R + 2 * K);
   float *gu = dsh + 2 * R + 3 * K;  // acceptance uniforms [K]
 
+  if (tid == 0) {
+    mbar_init(&sh.bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
   // every CTA of the cluster must be running before any DSMEM store: arrive
   // now, wait before the first store
   cluster_arrive_relaxed();
@@ -754,6 +767,36 @@ __global__ void __launch_bounds__(NT, 2) draw_kernel(const Params p) {
     const int len = max(0, min(p.V, lo + p.slice_d) - lo);
     const int E2 = ((len + NT - 1) / NT + VE - 1) / VE * VE;
     const int e0 = min(len, tid * E2), e1 = min(len, e0 + E2);
+    // This CTA's slice of the row(s) in shared memory when it fits: one bulk
+    // copy per row (TMA path) or a cooperative copy.
+    unsigned char *st_t = reinterpret_cast<unsigned char *>(dsh) + p.draw_stage_off;
+    unsigned char *st_d = st_t + static_cast<size_t>(p.slice_d) * E::BYTES;
+    const bool staged = p.draw_staged;
+    if (staged && len > 0) {
+      if (TMA) {
+        if (tid == 0) {
+          const uint32_t bytes = static_cast<uint32_t>(len) * E::BYTES;
+          mbar_arrive_expect_tx(&sh.bar, bytes * (pair ? 2 : 1));
+          bulk_g2s(st_t, rt + static_cast<size_t>(lo) * E::BYTES, bytes, &sh.bar);
+          if (pair) bulk_g2s(st_d, rd + static_cast<size_t>(lo) * E::BYTES, bytes, &sh.bar);
+        }
+        if (!mbar_wait_bounded(&sh.bar, 0u)) atomicOr(p.status, ST_TIMEOUT);
+      } else {
+        for (int e = tid; e < len; e += NT) {
+          E::copy_elem(st_t + e * E::BYTES, rt + static_cast<size_t>(lo + e) * E::BYTES);
+          if (pair) E::copy_elem(st_d + e * E::BYTES, rd + static_cast<size_t>(lo + e) * E::BYTES);
+        }
+        __syncthreads();
+      }
+    }
+    auto zt_at = [&](int e) -> float {
+      if (staged) return E::load_shared(st_t, e);
+      return E::load(rt, lo + e);
+    };
+    auto zd_at = [&](int e) -> float {
+      if (staged) return E::load_shared(st_d, e);
+      return E::load(rd, lo + e);
+    };
     Weights W;
     W.c = c;
     W.mtc = sh.dec[2] * c;
@@ -765,30 +808,20 @@ __global__ void __launch_bounds__(NT, 2) draw_kernel(const Params p) {
     float tl = 0.f, excl = 0.f, sum = 0.f;
     for (int round = 0; round < 2; ++round) {
       sum = 0.f;
-      if (TMA) {
-        for (int e = e0; e < e1; e += BATCH * VE) {
-          uint4 vt[BATCH], vd[BATCH];
+      if (staged) {
+        for (int e = e0; e < e1; e += VE) {
+          // e is a multiple of VE and the staging rows hold slice_d >= e1
+          // entries (rounded up to VE), so the 16-byte reads stay in bounds;
+          // entries past e1 are skipped below
+          float ft[VE], fd[VE];
+          E::unpack(lds128(st_t + e * E::BYTES), ft);
+          if (W.resid) E::unpack(lds128(st_d + e * E::BYTES), fd);
 #pragma unroll
-          for (int k = 0; k < BATCH; ++k) {
-            const int ek = e + k * VE;
-            const size_t off = static_cast<size_t>(lo + ek) * E::BYTES;
-            vt[k] = ek < e1 ? __ldcg(reinterpret_cast<const uint4 *>(rt + off)) : make_uint4(0, 0, 0, 0);
-            vd[k] = (ek < e1 && W.resid) ? __ldcg(reinterpret_cast<const uint4 *>(rd + off))
-                                         : make_uint4(0, 0, 0, 0);
-          }
-#pragma unroll
-          for (int k = 0; k < BATCH; ++k) {
-            if (e + k * VE >= e1) break;
-            float ft[VE], fd[VE];
-            E::unpack(vt[k], ft);
-            E::unpack(vd[k], fd);
-#pragma unroll
-            for (int j = 0; j < VE; ++j) sum = __fadd_rn(sum, W(ft[j], fd[j]));
-          }
+          for (int j = 0; j < VE; ++j)
+            if (e + j < e1) sum = __fadd_rn(sum, W(ft[j], W.resid ? fd[j] : 0.f));
         }
       } else {
-        for (int e = e0; e < e1; ++e)
-          sum = __fadd_rn(sum, W(E::load(rt, lo + e), W.resid ? E::load(rd, lo + e) : 0.f));
+        for (int e = e0; e < e1; ++e) sum = __fadd_rn(sum, W(zt_at(e), W.resid ? zd_at(e) : 0.f));
       }
       float total;
       excl = block_exclusive_scan(sum, sh.fscratch, &total);
@@ -861,7 +894,7 @@ __global__ void __launch_bounds__(NT, 2) draw_kernel(const Params p) {
       __syncthreads();
       float w = 0.f;
       const int e = w0 + tid;
-      if (e < w1) w = W(E::load(rt, lo + e), W.resid ? E::load(rd, lo + e) : 0.f);
+      if (e < w1) w = W(zt_at(e), W.resid ? zd_at(e) : 0.f);
       float tot_unused;
       const float before = block_exclusive_scan(w, sh.fscratch, &tot_unused);
       const float run = __fadd_rn(base, __fadd_rn(before, w));

@@ -90,7 +90,8 @@ int get_ws(cudaStream_t stream, size_t nparts, Workspace **out) {
 constexpr int SLICE_TARGET_BYTES = 16 * 1024;  // vocabulary bytes per row and slice
 constexpr int DEFAULT_STAGES = 3;               // tile ring depth
 constexpr int TILE_MAX_BYTES = 16 * 1024;       // tile width per row
-constexpr int DRAW_CLUSTER = 8;                 // CTAs per sequence in the draw
+constexpr int DRAW_SLICE_BYTES = 32 * 1024;     // draw: bytes of each row per CTA
+constexpr int DRAW_STAGE_LIMIT = 200 * 1024;    // draw: largest staged shared memory
 
 int env_int(const char *name, int dflt, int lo, int hi) {
   const char *v = std::getenv(name);
@@ -216,22 +217,35 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
   if (argmax)
     smem_b = 4 * (3 * p.J) + (p.kind == KIND_TREE ? 9 * p.J : 0) + 16;
   else
-    smem_b = 4 * (8 * p.K + 2) + 16;
+    smem_b = (4 * (8 * p.K + 2) + 15) / 16 * 16;  // normalisers, logits at x, uniforms
   int st;
   // the draw: clusters of CD CTAs, each CTA walking one thread's chunk with
   // one entry per thread, so a draw slice holds at most NT^2 entries
-  int CD = env_int("SPEC_VERIFY_DRAW_CLUSTER", DRAW_CLUSTER, 1, MAX_CLUSTER);
-  while (CD < MAX_CLUSTER && (p.V + CD - 1) / CD > NT * NT - VE) CD *= 2;
+  // draw: about 32 KB of each row per CTA (staged in shared memory)
+  int CD = static_cast<int>(std::min<long long>(
+      MAX_CLUSTER, std::max<long long>(1, (row_bytes + DRAW_SLICE_BYTES - 1) / DRAW_SLICE_BYTES)));
+  CD = env_int("SPEC_VERIFY_DRAW_CLUSTER", CD, 1, MAX_CLUSTER);
+  while (CD < MAX_CLUSTER && (p.V + CD - 1) / CD > NT * NT - VE) ++CD;
+  const int smem_base = smem_b;
+  int slice_d = 0, draw_stage_off = smem_base;
+  bool draw_staged = false;
+  bool allow_stage = true;
   for (;;) {
+    const int per_d = (p.V + CD - 1) / CD;
+    slice_d = (per_d + VE - 1) / VE * VE;
+    draw_staged = !argmax && allow_stage && 2LL * slice_d * esz + smem_base <= DRAW_STAGE_LIMIT;
+    smem_b = smem_base + (draw_staged ? 2 * slice_d * esz : 0);
     if (argmax) break;
     int nclus = 0;
     if ((st = occupancy(fb, smem_b, CD, &nclus))) return st;
     if (nclus > 0) break;
+    if (draw_staged) {  // first give up the staging, then shrink the cluster
+      allow_stage = false;
+      continue;
+    }
     if (CD == 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster fits on the device");
     CD = CD > 8 ? 8 : CD / 2;
   }
-  const int per_d = (p.V + CD - 1) / CD;
-  const int slice_d = (per_d + VE - 1) / VE * VE;
   if (!argmax && slice_d > NT * NT) return fail(SPEC_ERR_ARG, "vocabulary too large");
   const int per = (p.V + C - 1) / C;
   const int slice = (per + VE - 1) / VE * VE;
@@ -250,6 +264,8 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
   p.C = C;
   p.slice = slice;
   p.slice_d = slice_d;
+  p.draw_staged = draw_staged ? 1 : 0;
+  p.draw_stage_off = draw_stage_off;
   p.tile = tile;
   p.stages = stages;
   p.partials = w->partials;
