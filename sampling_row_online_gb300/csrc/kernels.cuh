@@ -259,18 +259,20 @@ __device__ __forceinline__ float block_exclusive_scan(float v, float *sh, float 
 }
 
 // ------------------------------------------------------------ job layout
-// Job q -> (sequence b, row i).  Stochastic chain: the K row pairs in
-// position-major order, then the K+1-th target rows.  Argmax kinds: rows
-// position-major.
+// Job q -> (sequence b, row i).  Stochastic chain: the B bonus rows first,
+// then the row pairs from position K-1 down to 0, so the rows a residual draw
+// most often needs (the early positions) are the last ones streamed and are
+// still in L2 when the draw runs.  Argmax kinds: rows position-major.
 __device__ __forceinline__ void decode_job(const Params &p, int q, int &b, int &i) {
   if (p.kind == KIND_SAMPLE) {
-    const int npair = p.B * p.K;
-    if (q < npair) {
-      i = q / p.B;
-      b = q - i * p.B;
-    } else {
+    if (q < p.B) {
       i = p.K;
-      b = q - npair;
+      b = q;
+    } else {
+      const int r = q - p.B;
+      const int k = r / p.B;
+      i = p.K - 1 - k;
+      b = r - k * p.B;
     }
   } else {
     i = q / p.B;
@@ -279,7 +281,7 @@ __device__ __forceinline__ void decode_job(const Params &p, int q, int &b, int &
 }
 
 __device__ __forceinline__ int job_of(const Params &p, int b, int i) {
-  if (p.kind == KIND_SAMPLE && i == p.K) return p.B * p.K + b;
+  if (p.kind == KIND_SAMPLE) return i == p.K ? b : p.B + (p.K - 1 - i) * p.B + b;
   return i * p.B + b;
 }
 
@@ -428,7 +430,6 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
   constexpr int SROWS = ARGMAX ? 1 : 2;
-  constexpr int NC = NCW * 32;  // consumer threads
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ uint64_t full[MAX_STAGES], empty[MAX_STAGES];
   __shared__ __align__(16) StageMeta meta[MAX_STAGES];
@@ -531,10 +532,13 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
     if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(seq / S) & 1u)) tmo = true;
     const StageMeta m = meta[s];
     if (m.item < 0) break;
+    // this warp's contiguous share of the tile's vectors (lanes interleaved)
     const int nv = (m.n + VE - 1) / VE;
+    const int nvw = (nv + NCW - 1) / NCW;
+    const int j0 = warp * nvw + lane, j1 = min(nv, (warp + 1) * nvw);
     const unsigned char *bt = stage_row(s, 0);
     if (ARGMAX) {
-      for (int j = tid; j < nv; j += NC) {
+      for (int j = j0; j < j1; j += 32) {
         float f[VE];
         E::unpack(lds128(bt + j * 16), f);
         float vm = f[0];
@@ -549,13 +553,13 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
       }
     } else if (m.nrows == 2) {
       const unsigned char *bd = stage_row(s, 1);
-      for (int j = tid; j < nv; j += NC) {
+      for (int j = j0; j < j1; j += 32) {
         const uint4 wt = lds128(bt + j * 16), wd = lds128(bd + j * 16);
         online_vec16<DT>(wt, c, ot);
         online_vec16<DT>(wd, c, od);
       }
     } else {
-      for (int j = tid; j < nv; j += NC) online_vec16<DT>(lds128(bt + j * 16), c, ot);
+      for (int j = j0; j < j1; j += 32) online_vec16<DT>(lds128(bt + j * 16), c, ot);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with stage s
@@ -613,29 +617,31 @@ struct DrawShared {
   float fscratch[NWARP + 1];
 };
 
-// Combined (max, sumexp) of rows from their C x NCW partials (one per slice
-// and consumer warp), by one warp: every load of the warp's rows is issued
-// before any is used; lane l folds partials l, l+32, l+64, l+96 in order,
-// then a butterfly, so every lane (and every CTA) ends with the same bits.
-constexpr int PARTS_PER_LANE = MAX_CLUSTER * NCW / 32;
+// Combined (max, sumexp) of two rows from their C x NCW partials (one per
+// slice and consumer warp), by one warp: loads are issued PARTS_PER_LANE per
+// lane and row at a time; lane l folds partials l, l+32, ... in order, then
+// a butterfly, so every lane (and every CTA) ends with the same bits.
+constexpr int PARTS_PER_LANE = 4;
 
 __device__ __forceinline__ void warp_row_stats2(const float4 *pa, bool da, const float4 *pb, bool db,
                                                 int nparts, float c, float &ma, float &sa,
                                                 float &mb, float &sb) {
   const int lane = threadIdx.x & 31;
-  float4 va[PARTS_PER_LANE], vb[PARTS_PER_LANE];
-#pragma unroll
-  for (int k = 0; k < PARTS_PER_LANE; ++k) {
-    const int j = lane + 32 * k;
-    va[k] = (pa && j < nparts) ? __ldcg(pa + j) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-    vb[k] = (pb && j < nparts) ? __ldcg(pb + j) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-  }
   ma = mb = -INFINITY;
   sa = sb = 0.f;
+  for (int base = 0; base < nparts; base += 32 * PARTS_PER_LANE) {
+    float4 va[PARTS_PER_LANE], vb[PARTS_PER_LANE];
 #pragma unroll
-  for (int k = 0; k < PARTS_PER_LANE; ++k) {
-    ms_combine(ma, sa, da ? va[k].z : va[k].x, da ? va[k].w : va[k].y, c);
-    ms_combine(mb, sb, db ? vb[k].z : vb[k].x, db ? vb[k].w : vb[k].y, c);
+    for (int k = 0; k < PARTS_PER_LANE; ++k) {
+      const int j = base + lane + 32 * k;
+      va[k] = (pa && j < nparts) ? __ldcg(pa + j) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+      vb[k] = (pb && j < nparts) ? __ldcg(pb + j) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < PARTS_PER_LANE; ++k) {
+      ms_combine(ma, sa, da ? va[k].z : va[k].x, da ? va[k].w : va[k].y, c);
+      ms_combine(mb, sb, db ? vb[k].z : vb[k].x, db ? vb[k].w : vb[k].y, c);
+    }
   }
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -645,6 +651,114 @@ __device__ __forceinline__ void warp_row_stats2(const float4 *pa, bool da, const
     s2 = __shfl_xor_sync(0xFFFFFFFFu, sb, off);
     ms_combine(mb, sb, m2, s2, c);
   }
+}
+
+// Draw from p (unnormalised weights 2^((z - M) c)) of one target row using
+// its streaming partials: the partial of (slice s, warp w) is the mass of a
+// contiguous vocabulary range, so the range holding u * Z is found from the
+// partials alone and only that range (at most 1024 entries) is read.  Called
+// by every thread of one CTA; returns the token in every thread.
+template <int DT>
+__device__ __forceinline__ int draw_p_from_partials(const Params &p, const float4 *parts,
+                                                    const unsigned char *row, float M, float u,
+                                                    int *scratch, float *fscratch, float *bcast) {
+  using E = Elem<DT>;
+  constexpr int VE = E::VE;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const float c = p.c, Mc = M * c;
+  const int nparts = p.C * NCW;
+  // 1. range masses, scanned in order by warp 0 (lane l: a contiguous run)
+  if (tid < 32) {
+    const int per = (nparts + 31) / 32;
+    const int j0 = min(nparts, lane * per), j1 = min(nparts, j0 + per);
+    float sum = 0.f;
+    for (int j = j0; j < j1; ++j) {
+      const float4 v = __ldcg(parts + j);
+      sum = __fadd_rn(sum, v.x == -INFINITY ? 0.f : __fmul_rn(v.y, ex2(v.x * c - Mc)));
+    }
+    float inc = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float n = __shfl_up_sync(0xFFFFFFFFu, inc, off);
+      if (lane >= off) inc = __fadd_rn(inc, n);
+    }
+    const float excl = __fsub_rn(inc, sum);
+    const float Z = __shfl_sync(0xFFFFFFFFu, inc, 31);
+    const float t = u * Z;
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, sum > 0.f && inc > t);
+    const unsigned pos = __ballot_sync(0xFFFFFFFFu, sum > 0.f);
+    const int who = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+    const bool lastmode = hit == 0;
+    if (lane == who) {
+      float run = excl;
+      int own = j0, ownlast = j0;
+      float P = excl, Plast = excl;
+      bool found = false;
+      for (int j = j0; j < j1; ++j) {
+        const float4 v = __ldcg(parts + j);
+        const float mj = v.x == -INFINITY ? 0.f : __fmul_rn(v.y, ex2(v.x * c - Mc));
+        if (mj > 0.f) {
+          if (!lastmode && !found && __fadd_rn(run, mj) > t) {
+            own = j;
+            P = run;
+            found = true;
+          }
+          ownlast = j;
+          Plast = run;
+        }
+        run = __fadd_rn(run, mj);
+      }
+      if (!found) {
+        own = ownlast;
+        P = Plast;
+      }
+      scratch[0] = own;
+      scratch[1] = found ? 0 : 1;
+      fscratch[0] = t;
+      fscratch[1] = P;
+    }
+  }
+  __syncthreads();
+  const int own = scratch[0];
+  const int pl = scratch[1];
+  const float t = fscratch[0], P = fscratch[1];
+  __syncthreads();
+  // 2. the owner range: slice s, warp w of the streaming kernel's split
+  const int sl = own / NCW, w = own - sl * NCW;
+  const int lo_s = sl * p.slice;
+  const int len_s = max(0, min(p.V, lo_s + p.slice) - lo_s);
+  const int nv = (len_s + VE - 1) / VE, nvw = (nv + NCW - 1) / NCW;
+  const int r0 = lo_s + min(len_s, w * nvw * VE);
+  const int r1 = lo_s + min(len_s, (w + 1) * nvw * VE);
+  // 3. walk it: a few consecutive entries per thread, block scan
+  const int per = (r1 - r0 + NT - 1) / NT;
+  const int a0 = min(r1, r0 + tid * per), a1 = min(r1, a0 + per);
+  float sum = 0.f;
+  for (int v = a0; v < a1; ++v) sum = __fadd_rn(sum, ex2(fmaf(E::load(row, v), c, -Mc)));
+  float total;
+  const float excl = __fadd_rn(P, block_exclusive_scan(sum, fscratch, &total));
+  int pick = INT_MAX;
+  if (!pl && sum > 0.f && __fadd_rn(excl, sum) > t) {
+    float run = excl;
+    for (int v = a0; v < a1; ++v) {
+      const float x = ex2(fmaf(E::load(row, v), c, -Mc));
+      run = __fadd_rn(run, x);
+      if (x > 0.f && run > t) {
+        pick = v;
+        break;
+      }
+    }
+  }
+  pick = block_reduce_min_int(pick, scratch);
+  if (pick == INT_MAX) {
+    int last = -1;
+    for (int v = a0; v < a1; ++v)
+      if (ex2(fmaf(E::load(row, v), c, -Mc)) > 0.f) last = v;
+    pick = block_reduce_max_int(last, scratch);
+    if (pick < 0) pick = r0;
+  }
+  (void)bcast;
+  return pick;
 }
 
 // Rank 0 of the cluster combines the partials of all 2K+1 rows and takes
@@ -758,7 +872,25 @@ __global__ void __launch_bounds__(NT, 3) draw_kernel(const Params p) {
   const int n = __float_as_int(sh.dec[0]);
   const int err = __float_as_int(sh.dec[1]);
 
-  if (!err) {
+  if (!err && n == K) {
+    // ---- bonus: rank 0 draws from p_K using the streaming partials
+    if (rank == 0) {
+      const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(K), 1u);
+      const int token = draw_p_from_partials<DT>(
+          p, p.partials + static_cast<size_t>(job_of(p, b, K)) * p.C * NCW, target_row<DT>(p, b, K),
+          sh.dec[2], u, sh.scratch, sh.fscratch, sh.bf);
+      int32_t *out = p.out_tokens + static_cast<size_t>(b) * (K + 1);
+      for (int j = tid; j <= K; j += NT) out[j] = j < K ? __ldg(p.tokens + static_cast<size_t>(b) * K + j) : token;
+      if (tid == 0) {
+        p.out_n[b] = K;
+        if (p.stats) {
+          atomicAdd(&p.stats->sequences, 1ull);
+          atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(K));
+          atomicAdd(&p.stats->bonus, 1ull);
+        }
+      }
+    }
+  } else if (!err) {
     // ---- the draw: residual at n < K, or the bonus from row K
     const bool pair = n < K;
     const unsigned char *rt = target_row<DT>(p, b, n);
@@ -941,13 +1073,16 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
     float v = -INFINITY;
     int idx = INT_MAX;
     const float4 *parts = p.partials + static_cast<size_t>(job_of(p, b, r)) * nparts;
-    float4 a[PARTS_PER_LANE];
+    for (int base = 0; base < nparts; base += 32 * PARTS_PER_LANE) {
+      float4 a[PARTS_PER_LANE];
 #pragma unroll
-    for (int k = 0; k < PARTS_PER_LANE; ++k)
-      a[k] = lane + 32 * k < nparts ? __ldcg(parts + lane + 32 * k)
-                                    : make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f);
+      for (int k = 0; k < PARTS_PER_LANE; ++k) {
+        const int j = base + lane + 32 * k;
+        a[k] = j < nparts ? __ldcg(parts + j) : make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f);
+      }
 #pragma unroll
-    for (int k = 0; k < PARTS_PER_LANE; ++k) am_combine(v, idx, a[k].x, __float_as_int(a[k].y));
+      for (int k = 0; k < PARTS_PER_LANE; ++k) am_combine(v, idx, a[k].x, __float_as_int(a[k].y));
+    }
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, off);

@@ -87,7 +87,6 @@ int get_ws(cudaStream_t stream, size_t nparts, Workspace **out) {
 }
 
 // ------------------------------------------------------------ geometry
-constexpr int SLICE_TARGET_BYTES = 16 * 1024;  // vocabulary bytes per row and slice
 constexpr int DEFAULT_STAGES = 3;               // tile ring depth
 constexpr int TILE_MAX_BYTES = 16 * 1024;       // tile width per row
 constexpr int DRAW_SLICE_BYTES = 32 * 1024;     // draw: bytes of each row per CTA
@@ -207,9 +206,9 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
   const bool argmax = p.kind != KIND_SAMPLE;
   const int srows = argmax ? 1 : 2;
   const long long row_bytes = static_cast<long long>(p.V) * esz;
-  int C = static_cast<int>(std::min<long long>(
-      MAX_CLUSTER, std::max<long long>(1, (row_bytes + SLICE_TARGET_BYTES - 1) / SLICE_TARGET_BYTES)));
-  C = env_int("SPEC_VERIFY_SLICES", C, 1, MAX_CLUSTER);
+  // streaming items are single tiles of at most 16 KB per row
+  const int C_min = static_cast<int>(std::max<long long>(1, (row_bytes + TILE_MAX_BYTES - 1) / TILE_MAX_BYTES));
+  const int C = std::max(C_min, env_int("SPEC_VERIFY_SLICES", C_min, 1, 1 << 16));
   const int stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
   const void *fa = argmax ? pick_row_kernel<true>(dtype, tma) : pick_row_kernel<false>(dtype, tma);
   const void *fb = argmax ? reinterpret_cast<const void *>(&finish_kernel) : pick_draw_kernel(dtype, tma);
