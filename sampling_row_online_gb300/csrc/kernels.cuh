@@ -610,7 +610,6 @@ struct Weights {
 struct DrawShared {
   uint64_t bar;              // completion of the slice's bulk copies
   float xz[2][MAX_CLUSTER];  // slice masses pushed by every CTA (round 0 / 1)
-  alignas(16) float dec[8];  // rank 0's decision, pushed: n, err, m_t, S_t, m_d, S_d
   float bf[8];
   int bi[8];
   int scratch[NWARP];
@@ -792,64 +791,78 @@ __global__ void __launch_bounds__(NT, 3) draw_kernel(const Params p) {
   // now, wait before the first store
   cluster_arrive_relaxed();
 
-  if (rank == 0) {
-    // ---- inputs that do not depend on the first launch (overlaps its tail)
-    for (int i = tid; i < K; i += NT) {
-      const int x = __ldg(p.tokens + static_cast<size_t>(b) * K + i);
-      const int ok = x >= 0 && x < p.V;
-      gok[i] = ok;
-      gx[2 * i] = ok ? E::load(target_row<DT>(p, b, i), x) : 0.f;
-      gx[2 * i + 1] = ok ? E::load(draft_row<DT>(p, b, i), x) : 0.f;
-      gu[i] = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
-    }
+  // ---- inputs that do not depend on the first launch (overlaps its tail)
+  for (int i = tid; i < K; i += NT) {
+    const int x = __ldg(p.tokens + static_cast<size_t>(b) * K + i);
+    const int ok = x >= 0 && x < p.V;
+    gok[i] = ok;
+    gx[2 * i] = ok ? E::load(target_row<DT>(p, b, i), x) : 0.f;
+    gx[2 * i + 1] = ok ? E::load(draft_row<DT>(p, b, i), x) : 0.f;
+    gu[i] = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
   }
   pdl_wait();  // the row partials of the first launch are complete and visible
 
+  // ---- normalisers of the 2K+1 rows (target 0..K, then draft 0..K-1): this
+  // CTA combines rows rank, rank + CD, ... (two per warp per round) and
+  // pushes them into every CTA of the cluster
+  const int nparts = p.C * NCW;
+  const int nmine = static_cast<int>(rank) < R ? (R - static_cast<int>(rank) + CD - 1) / CD : 0;
+  for (int k = 2 * warp; k < nmine; k += 2 * NWARP) {
+    const int r = static_cast<int>(rank) + CD * k;
+    const int r2 = k + 1 < nmine ? r + CD : R;
+    const bool da = r > K, db = r2 > K;
+    const float4 *pa = p.partials + static_cast<size_t>(job_of(p, b, da ? r - K - 1 : r)) * nparts;
+    const float4 *pb =
+        r2 < R ? p.partials + static_cast<size_t>(job_of(p, b, db ? r2 - K - 1 : r2)) * nparts : nullptr;
+    float ma, sa, mb, sb;
+    warp_row_stats2(pa, da, pb, db, nparts, c, ma, sa, mb, sb);
+    if (lane == 0) {
+      rmax[r] = ma;
+      rsum[r] = sa;
+      if (r2 < R) {
+        rmax[r2] = mb;
+        rsum[r2] = sb;
+      }
+    }
+  }
+  __syncthreads();
+  cluster_wait();  // every peer is running: DSMEM stores are allowed
+  for (int t = tid; t < nmine * static_cast<int>(CD); t += NT) {
+    const int k = t / CD;
+    const uint32_t dst = static_cast<uint32_t>(t - k * CD);
+    if (dst == rank) continue;
+    const int r = static_cast<int>(rank) + CD * k;
+    dsmem_st_f32(dsmem_addr(&rmax[r], dst), rmax[r]);
+    dsmem_st_f32(dsmem_addr(&rsum[r], dst), rsum[r]);
+  }
+  cluster_sync();  // every row's normalisers are in every CTA
+
+  // ---- left-to-right acceptance: the first reject n (or K); every CTA
+  // takes the same decision from the same bits
+  if (tid == 0) {
+    int n = K, err = 0;
+    for (int i = 0; i < K; ++i)
+      if (!gok[i]) err = 1;
+    for (int i = 0; i < K && !err; ++i) {
+      const float a = fmaf(gx[2 * i], c, -(rmax[i] * c));
+      const float d = fmaf(gx[2 * i + 1], c, -(rmax[K + 1 + i] * c));
+      const float ratio = ex2(a - d) * (rsum[K + 1 + i] / rsum[i]);  // p_i(x_i) / q_i(x_i)
+      if (!(gu[i] < ratio)) {
+        n = i;
+        break;
+      }
+    }
+    sh.bi[0] = n;
+    sh.bi[1] = err;
+  }
+  __syncthreads();
   if (rank == 0) {
-    // ---- normalisers of the 2K+1 rows (target 0..K, then draft 0..K-1)
-    const int nparts = p.C * NCW;
-    for (int r = warp; r < R; r += 2 * NWARP) {
-      const int r2 = r + NWARP;
-      const bool da = r > K, db = r2 > K;
-      const float4 *pa = p.partials + static_cast<size_t>(job_of(p, b, da ? r - K - 1 : r)) * nparts;
-      const float4 *pb =
-          r2 < R ? p.partials + static_cast<size_t>(job_of(p, b, db ? r2 - K - 1 : r2)) * nparts : nullptr;
-      float ma, sa, mb, sb;
-      warp_row_stats2(pa, da, pb, db, nparts, c, ma, sa, mb, sb);
-      if (lane == 0) {
-        rmax[r] = ma;
-        rsum[r] = sa;
-        if (r2 < R) {
-          rmax[r2] = mb;
-          rsum[r2] = sb;
-        }
-      }
-    }
-    __syncthreads();
-    // ---- left-to-right acceptance: the first reject n (or K)
-    if (tid == 0) {
-      int n = K, err = 0;
-      for (int i = 0; i < K; ++i)
-        if (!gok[i]) err = 1;
-      for (int i = 0; i < K && !err; ++i) {
-        const float a = fmaf(gx[2 * i], c, -(rmax[i] * c));
-        const float d = fmaf(gx[2 * i + 1], c, -(rmax[K + 1 + i] * c));
-        const float ratio = ex2(a - d) * (rsum[K + 1 + i] / rsum[i]);  // p_i(x_i) / q_i(x_i)
-        if (!(gu[i] < ratio)) {
-          n = i;
-          break;
-        }
-      }
-      sh.bi[0] = n;
-      sh.bi[1] = err;
-    }
-    __syncthreads();
-    const int n = sh.bi[0], err = sh.bi[1];
+    const int n0 = sh.bi[0];
     for (int r = tid; r < R; r += NT) {
       if (p.out_row_max) p.out_row_max[static_cast<size_t>(b) * R + r] = rmax[r];
       if (p.out_row_sumexp) p.out_row_sumexp[static_cast<size_t>(b) * R + r] = rsum[r];
     }
-    if (err) {
+    if (sh.bi[1]) {
       for (int e = tid; e <= K; e += NT) p.out_tokens[static_cast<size_t>(b) * (K + 1) + e] = -1;
       if (tid == 0) {
         p.out_n[b] = -1;
@@ -857,20 +870,10 @@ __global__ void __launch_bounds__(NT, 3) draw_kernel(const Params p) {
         if (p.stats) atomicAdd(&p.stats->errors, 1ull);
       }
     }
-    cluster_wait();  // every peer is running
-    if (tid < static_cast<int>(CD)) {  // push the decision into every CTA
-      const bool pair = n < K;
-      dsmem_st_v4f32(dsmem_addr(&sh.dec[0], tid), __int_as_float(n), __int_as_float(err), rmax[n],
-                     rsum[n]);
-      dsmem_st_f32(dsmem_addr(&sh.dec[4], tid), pair ? rmax[K + 1 + n] : 0.f);
-      dsmem_st_f32(dsmem_addr(&sh.dec[5], tid), pair ? rsum[K + 1 + n] : 1.f);
-    }
-  } else {
-    cluster_wait();
+    (void)n0;
   }
-  cluster_sync();  // the decision is visible in every CTA
-  const int n = __float_as_int(sh.dec[0]);
-  const int err = __float_as_int(sh.dec[1]);
+  const int n = sh.bi[0];
+  const int err = sh.bi[1];
 
   if (!err && n == K) {
     // ---- bonus: rank 0 draws from p_K using the streaming partials
@@ -878,7 +881,7 @@ __global__ void __launch_bounds__(NT, 3) draw_kernel(const Params p) {
       const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(K), 1u);
       const int token = draw_p_from_partials<DT>(
           p, p.partials + static_cast<size_t>(job_of(p, b, K)) * p.C * NCW, target_row<DT>(p, b, K),
-          sh.dec[2], u, sh.scratch, sh.fscratch, sh.bf);
+          rmax[K], u, sh.scratch, sh.fscratch, sh.bf);
       int32_t *out = p.out_tokens + static_cast<size_t>(b) * (K + 1);
       for (int j = tid; j <= K; j += NT) out[j] = j < K ? __ldg(p.tokens + static_cast<size_t>(b) * K + j) : token;
       if (tid == 0) {
@@ -931,10 +934,10 @@ __global__ void __launch_bounds__(NT, 3) draw_kernel(const Params p) {
     };
     Weights W;
     W.c = c;
-    W.mtc = sh.dec[2] * c;
-    W.mdc = sh.dec[4] * c;
-    W.inv_st = 1.f / sh.dec[3];
-    W.inv_sd = 1.f / sh.dec[5];
+    W.mtc = rmax[n] * c;
+    W.mdc = pair ? rmax[K + 1 + n] * c : 0.f;
+    W.inv_st = 1.f / rsum[n];
+    W.inv_sd = pair ? 1.f / rsum[K + 1 + n] : 0.f;
     W.resid = pair;
     int fallback = 0, owner = 0, pl = 0;
     float tl = 0.f, excl = 0.f, sum = 0.f;
@@ -951,6 +954,29 @@ __global__ void __launch_bounds__(NT, 3) draw_kernel(const Params p) {
 #pragma unroll
           for (int j = 0; j < VE; ++j)
             if (e + j < e1) sum = __fadd_rn(sum, W(ft[j], W.resid ? fd[j] : 0.f));
+        }
+      } else if (TMA) {
+        // rows 16-byte aligned: 16-byte loads, four per row in flight
+        constexpr int BATCH = 4;
+        for (int e = e0; e < e1; e += BATCH * VE) {
+          uint4 vt[BATCH], vd[BATCH];
+#pragma unroll
+          for (int k = 0; k < BATCH; ++k) {
+            const int ek = e + k * VE;
+            const size_t off = static_cast<size_t>(lo + ek) * E::BYTES;
+            vt[k] = ek < e1 ? __ldcg(reinterpret_cast<const uint4 *>(rt + off)) : make_uint4(0, 0, 0, 0);
+            vd[k] = (ek < e1 && W.resid) ? __ldcg(reinterpret_cast<const uint4 *>(rd + off))
+                                         : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int k = 0; k < BATCH; ++k) {
+            if (e + k * VE >= e1) break;
+            float ft[VE], fd[VE];
+            E::unpack(vt[k], ft);
+            E::unpack(vd[k], fd);
+#pragma unroll
+            for (int j = 0; j < VE; ++j) sum = __fadd_rn(sum, W(ft[j], W.resid ? fd[j] : 0.f));
+          }
         }
       } else {
         for (int e = e0; e < e1; ++e) sum = __fadd_rn(sum, W(zt_at(e), W.resid ? zd_at(e) : 0.f));

@@ -87,10 +87,10 @@ int get_ws(cudaStream_t stream, size_t nparts, Workspace **out) {
 }
 
 // ------------------------------------------------------------ geometry
-constexpr int DEFAULT_STAGES = 3;               // tile ring depth
+constexpr int DEFAULT_STAGES = 2;               // tile ring depth
 constexpr int TILE_MAX_BYTES = 16 * 1024;       // tile width per row
 constexpr int DRAW_SLICE_BYTES = 32 * 1024;     // draw: bytes of each row per CTA
-constexpr int DRAW_STAGE_LIMIT = 200 * 1024;    // draw: largest staged shared memory
+constexpr int DRAW_STAGE_LIMIT = 72 * 1024;     // draw: largest staged shared memory
 
 int env_int(const char *name, int dflt, int lo, int hi) {
   const char *v = std::getenv(name);
