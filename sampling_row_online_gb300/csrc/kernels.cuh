@@ -765,7 +765,7 @@ __device__ __forceinline__ int draw_p_from_partials(const Params &p, const float
 // the vocabulary (slice_d elements, independent of the streaming kernel's
 // slices).
 template <int DT, bool TMA>
-__global__ void __launch_bounds__(NT, 3) draw_kernel(const Params p) {
+__global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
   extern __shared__ __align__(16) float dsh[];  // row max [R], row sumexp [R], logits at x [2K], ok [K], u [K]

@@ -232,7 +232,8 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
   for (;;) {
     const int per_d = (p.V + CD - 1) / CD;
     slice_d = (per_d + VE - 1) / VE * VE;
-    draw_staged = !argmax && allow_stage && 2LL * slice_d * esz + smem_base <= DRAW_STAGE_LIMIT;
+    draw_staged = !argmax && allow_stage && env_int("SPEC_VERIFY_DRAW_STAGE", 0, 0, 1) &&
+                  2LL * slice_d * esz + smem_base <= DRAW_STAGE_LIMIT;
     smem_b = smem_base + (draw_staged ? 2 * slice_d * esz : 0);
     if (argmax) break;
     int nclus = 0;
