@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "verified draft positions/sec and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
 UNIT = "positions/s"
+LAUNCHES_PER_CALL = 2  # the streaming row kernel and the per-sequence decision kernel
 
 
 def _peaks():
@@ -349,7 +350,7 @@ def run_gpu(args, w):
         "achieved_hbm_gbs": achieved,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * LAUNCHES_PER_CALL,
         "clocks": clk,
         "wall_s": wall,
     }
