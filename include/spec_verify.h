@@ -147,6 +147,37 @@ int spec_verify_host(const void *target_logits, const void *draft_logits,
                      int32_t *out_n_accepted, void *stream);
 
 /*
+ * spec_verify_noalloc — spec_verify for callers that cannot allocate device
+ * memory while they run: a serving engine that hands nearly all of HBM to
+ * its own memory pool at start-up, or a latency-critical loop that cannot
+ * afford cudaMalloc/cudaFree (cudaFree can synchronise the whole device).
+ * The pages describe no such interface; it exists for integration only.
+ *
+ * Same arguments, outputs and results as spec_verify (temperature > 0 and
+ * T == 0 alike), but the scratch space comes from a fixed array compiled into
+ * the library (8 MiB of row partials plus a status word), which every GPU
+ * that loads the library keeps until the process exits.  Nothing is
+ * allocated by the call.
+ *
+ *   - Size limit: B * (K+1) * ceil(V * element_size / 16384) <= 65536
+ *     (e.g. B = 64, K = 5, V = 128256 bf16 uses 6144).  Larger calls return
+ *     SPEC_ERR_ARG with an explanation and launch nothing.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array: two calls that overlap on the GPU
+ *     (different streams, or different host threads) race and corrupt each
+ *     other's results.  Serialise them.
+ *   - Errors found on the device (a draft token outside [0, V)) show in the
+ *     outputs (n_accepted = -1, tokens -1); they are not reported by
+ *     spec_get_status.
+ */
+int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
+                        const int32_t *draft_tokens, int B, int K, int V, int dtype,
+                        float temperature, uint64_t seed, int32_t *out_tokens,
+                        int32_t *out_n_accepted, void *stream);
+
+/*
  * spec_verify_tree_greedy — greedy verification of a draft tree
  * ([Infra53] §3: every node sees only its ancestors, one path is
  * committed; [Anhtu] §"Token tree": the deepest accepted branch is the

@@ -313,6 +313,124 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
   return SPEC_OK;
 }
 
+// The same two launches as run_step, on scratch the caller provides
+// (partials with room for cap_parts entries, and a status word); nothing is
+// allocated.  Used by the no-allocation entry point below.
+int run_step_on(Params &p, int dtype, bool tma, cudaStream_t stream, float4 *partials,
+                size_t cap_parts, int32_t *status) {
+  const int esz = dtype == SPEC_F32 ? 4 : 2;
+  const int VE = 16 / esz;
+  const bool argmax = p.kind != KIND_SAMPLE;
+  const int srows = argmax ? 1 : 2;
+  const long long row_bytes = static_cast<long long>(p.V) * esz;
+  // streaming items are single tiles of at most 16 KB per row
+  const int C_min = static_cast<int>(std::max<long long>(1, (row_bytes + TILE_MAX_BYTES - 1) / TILE_MAX_BYTES));
+  const int C = std::max(C_min, env_int("SPEC_VERIFY_SLICES", C_min, 1, 1 << 16));
+  const int stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
+  const void *fa = argmax ? pick_row_kernel<true>(dtype, tma) : pick_row_kernel<false>(dtype, tma);
+  const void *fb = argmax ? reinterpret_cast<const void *>(&finish_kernel) : pick_draw_kernel(dtype, tma);
+  int smem_b = 0;
+  if (argmax)
+    smem_b = 4 * (3 * p.J) + (p.kind == KIND_TREE ? 9 * p.J : 0) + 16;
+  else
+    smem_b = (4 * (8 * p.K + 2) + 15) / 16 * 16;  // normalisers, logits at x, uniforms
+  int st;
+  // the draw: clusters of CD CTAs, each CTA walking one thread's chunk with
+  // one entry per thread, so a draw slice holds at most NT^2 entries
+  // draw: about 32 KB of each row per CTA (staged in shared memory)
+  int CD = static_cast<int>(std::min<long long>(
+      MAX_CLUSTER, std::max<long long>(1, (row_bytes + DRAW_SLICE_BYTES - 1) / DRAW_SLICE_BYTES)));
+  CD = env_int("SPEC_VERIFY_DRAW_CLUSTER", CD, 1, MAX_CLUSTER);
+  while (CD < MAX_CLUSTER && (p.V + CD - 1) / CD > NT * NT - VE) ++CD;
+  const int smem_base = smem_b;
+  int slice_d = 0, draw_stage_off = smem_base;
+  bool draw_staged = false;
+  bool allow_stage = true;
+  for (;;) {
+    const int per_d = (p.V + CD - 1) / CD;
+    slice_d = (per_d + VE - 1) / VE * VE;
+    draw_staged = !argmax && allow_stage && env_int("SPEC_VERIFY_DRAW_STAGE", 0, 0, 1) &&
+                  2LL * slice_d * esz + smem_base <= DRAW_STAGE_LIMIT;
+    smem_b = smem_base + (draw_staged ? 2 * slice_d * esz : 0);
+    if (argmax) break;
+    int nclus = 0;
+    if ((st = occupancy(fb, smem_b, CD, &nclus))) return st;
+    if (nclus > 0) break;
+    if (draw_staged) {  // first give up the staging, then shrink the cluster
+      allow_stage = false;
+      continue;
+    }
+    if (CD == 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster fits on the device");
+    CD = CD > 8 ? 8 : CD / 2;
+  }
+  if (!argmax && slice_d > NT * NT) return fail(SPEC_ERR_ARG, "vocabulary too large");
+  const int per = (p.V + C - 1) / C;
+  const int slice = (per + VE - 1) / VE * VE;
+  // tiles of up to 16 KB per row, never wider than a slice
+  const int tile = std::min(TILE_MAX_BYTES / esz, slice);
+  const int smem_a = stages * srows * tile * esz;
+  const long long nitems = static_cast<long long>(p.njobs) * C;
+  if (nitems > INT_MAX) return fail(SPEC_ERR_ARG, "too many rows");
+  int per_sm = 0;
+  if ((st = occupancy(fa, smem_a, -1, &per_sm))) return st;
+  if (per_sm < 1) return fail(SPEC_ERR_UNSUPPORTED, "row kernel does not fit on an SM");
+  const int grid_a = static_cast<int>(std::min<long long>(nitems, static_cast<long long>(per_sm) * num_sms()));
+
+  if (static_cast<size_t>(nitems) * NCW > cap_parts)
+    return fail(SPEC_ERR_ARG, "call too large for the fixed scratch of spec_verify_noalloc: "
+                              "B * (K+1) * ceil(V * element size / 16384) must not exceed " +
+                                  std::to_string(cap_parts / NCW));
+  p.C = C;
+  p.slice = slice;
+  p.slice_d = slice_d;
+  p.draw_staged = draw_staged ? 1 : 0;
+  p.draw_stage_off = draw_stage_off;
+  p.tile = tile;
+  p.stages = stages;
+  p.partials = partials;
+  p.status = status;
+
+  cudaError_t e;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_a), 1, 1);
+    cfg.blockDim = dim3(NT_ROW, 1, 1);
+    cfg.dynamicSmemBytes = smem_a;
+    cfg.stream = stream;
+    void *args[] = {&p};
+    e = cudaLaunchKernelExC(&cfg, fa, args);
+    if (e != cudaSuccess) return cuda_fail(e, "row kernel launch");
+  }
+  {
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = smem_b;
+    cfg.stream = stream;
+    if (argmax) {
+      cfg.gridDim = dim3(static_cast<unsigned>(p.B), 1, 1);
+      if ((st = occupancy(fb, smem_b, 0, &per_sm))) return st;
+    } else {
+      cfg.gridDim = dim3(static_cast<unsigned>(p.B * CD), 1, 1);
+      attr[na].id = cudaLaunchAttributeClusterDimension;
+      attr[na].val.clusterDim.x = CD;
+      attr[na].val.clusterDim.y = 1;
+      attr[na].val.clusterDim.z = 1;
+      ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    void *args[] = {&p};
+    e = cudaLaunchKernelExC(&cfg, fb, args);
+    if (e != cudaSuccess) return cuda_fail(e, "decision kernel launch");
+  }
+  return SPEC_OK;
+}
+
 int check_common(const void *zt, int B, int V, int dtype) {
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return fail(SPEC_ERR_DTYPE, "dtype must be SPEC_F32 or SPEC_BF16");
   if (B < 0) return fail(SPEC_ERR_ARG, "B must be >= 0");
@@ -560,3 +678,86 @@ void spec_shutdown(void) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------
+// spec_verify_noalloc: spec_verify on a fixed scratch area compiled into the
+// library.  Some callers cannot allocate device memory at call time: a
+// serving engine that reserves nearly all HBM for its own pool at start-up,
+// or a latency-critical loop that cannot pay for cudaMalloc/cudaFree (which
+// may synchronise the whole device).  This entry point serves them: its
+// scratch is the static array below, resident on every GPU that loads the
+// library until the process exits, and the call allocates nothing.
+namespace spec {
+namespace {
+
+// status word (256-byte slot) followed by the row partials
+constexpr size_t NOALLOC_MAX_PARTIALS = size_t(1) << 19;  // float4 entries: 8 MiB
+constexpr size_t NOALLOC_BYTES = 256 + NOALLOC_MAX_PARTIALS * sizeof(float4);
+static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+std::mutex g_noalloc_mu;
+unsigned char *g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {nullptr};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the array's host-side name is only a stand-in).
+int noalloc_scratch(unsigned char **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return fail(SPEC_ERR_UNSUPPORTED, "device index too large");
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_noalloc_ptr[dev] = static_cast<unsigned char *>(ptr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return SPEC_OK;
+}
+
+}  // namespace
+}  // namespace spec
+
+extern "C" int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
+                                   const int32_t *draft_tokens, int B, int K, int V, int dtype,
+                                   float temperature, uint64_t seed, int32_t *out_tokens,
+                                   int32_t *out_n_accepted, void *stream_ptr) {
+  using namespace spec;
+  int st = check_common(target_logits, B, V, dtype);
+  if (st) return st;
+  if (K < 0 || K > SPEC_MAX_DRAFTS) return fail(SPEC_ERR_ARG, "K out of range [0, 255]");
+  const float T = temperature;
+  if (!(T >= 0.f) || !std::isfinite(T)) return fail(SPEC_ERR_ARG, "temperature must be finite and >= 0");
+  const double cd = T > 0.f ? 1.4426950408889634 / static_cast<double>(T) : 0.0;
+  if (T > 0.f && !(cd < 1e30)) return fail(SPEC_ERR_ARG, "temperature too small");
+  if (B == 0) return SPEC_OK;
+  if (!out_tokens || !out_n_accepted) return fail(SPEC_ERR_ARG, "output pointer is NULL");
+  if (K > 0 && !draft_tokens) return fail(SPEC_ERR_ARG, "draft_tokens is NULL");
+  if (K > 0 && T > 0.f && !draft_logits) return fail(SPEC_ERR_ARG, "draft_logits is NULL with T > 0");
+  if (static_cast<long long>(B) * (K + 1) * MAX_CLUSTER > INT_MAX) return fail(SPEC_ERR_ARG, "B*(K+1) too large");
+  unsigned char *scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch))) return st;
+  const int esz = dtype == SPEC_F32 ? 4 : 2;
+  const bool sample = T > 0.f;
+  const bool tma = (static_cast<long long>(V) * esz) % 16 == 0 && aligned16(target_logits) &&
+                   (!sample || K == 0 || aligned16(draft_logits));
+  Params p = {};
+  p.zt = target_logits;
+  p.zd = draft_logits;
+  p.tokens = draft_tokens;
+  p.B = B;
+  p.K = K;
+  p.V = V;
+  p.J = K + 1;
+  p.kind = sample ? KIND_SAMPLE : KIND_GREEDY_CHAIN;
+  p.c = static_cast<float>(cd);
+  p.seed = seed;
+  p.njobs = B * (K + 1);
+  p.out_tokens = out_tokens;
+  p.out_n = out_n_accepted;
+  return run_step_on(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr),
+                     reinterpret_cast<float4 *>(scratch + 256), NOALLOC_MAX_PARTIALS,
+                     reinterpret_cast<int32_t *>(scratch));
+}
