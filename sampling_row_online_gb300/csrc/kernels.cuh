@@ -386,42 +386,6 @@ struct Online {
   __device__ __forceinline__ float sum() const { return s.x + s.y; }
 };
 
-// Maximum of one 16-byte vector of logits.
-template <int DT>
-__device__ __forceinline__ float vec16_max(const uint4 w) {
-  if (DT == 1) {  // bf16: packed maximum of the 8 values
-    const uint32_t mx = bf16x2_max(bf16x2_max(w.x, w.y), bf16x2_max(w.z, w.w));
-    return fmaxf(__uint_as_float(mx << 16), __uint_as_float(mx & 0xFFFF0000u));
-  }
-  return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
-               fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
-}
-
-// Sum of 2^(z c - mc) over one 16-byte vector into a two-lane accumulator.
-template <int DT>
-__device__ __forceinline__ void vec16_expsum(const uint4 w, float c, float mc, float2 &acc) {
-  float f[Elem<DT>::VE];
-  Elem<DT>::unpack(w, f);
-  const float2 cc = make_float2(c, c), nm = make_float2(-mc, -mc);
-#pragma unroll
-  for (int k = 0; k < Elem<DT>::VE; k += 2) {
-    const float2 y = __ffma2_rn(make_float2(f[k], f[k + 1]), cc, nm);
-    acc = __fadd2_rn(acc, make_float2(ex2(y.x), ex2(y.y)));
-  }
-}
-
-// One tile share of one row into the online state: the maximum of the
-// share first, then every exponential against it (one rescale per tile
-// instead of a running-maximum test per vector).
-template <int DT>
-__device__ __forceinline__ void online_share(const unsigned char *row, int j0, int j1, float c,
-                                             Online &st) {
-  float vm = -INFINITY;
-  for (int j = j0; j < j1; j += 32) vm = fmaxf(vm, vec16_max<DT>(lds128(row + j * 16)));
-  st.rescale(vm, c);
-  for (int j = j0; j < j1; j += 32) vec16_expsum<DT>(lds128(row + j * 16), c, st.mc, st.s);
-}
-
 // One 16-byte vector of logits into the online state.
 template <int DT>
 __device__ __forceinline__ void online_vec16(const uint4 w, float c, Online &st) {
@@ -588,10 +552,14 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
         }
       }
     } else if (m.nrows == 2) {
-      online_share<DT>(bt, j0, j1, c, ot);
-      online_share<DT>(stage_row(s, 1), j0, j1, c, od);
+      const unsigned char *bd = stage_row(s, 1);
+      for (int j = j0; j < j1; j += 32) {
+        const uint4 wt = lds128(bt + j * 16), wd = lds128(bd + j * 16);
+        online_vec16<DT>(wt, c, ot);
+        online_vec16<DT>(wd, c, od);
+      }
     } else {
-      online_share<DT>(bt, j0, j1, c, ot);
+      for (int j = j0; j < j1; j += 32) online_vec16<DT>(lds128(bt + j * 16), c, ot);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);  // this warp is done with stage s
