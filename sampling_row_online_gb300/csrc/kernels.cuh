@@ -60,6 +60,25 @@ struct Stats {  // layout-compatible with spec_stats_t
   unsigned long long sequences, accepted, bonus, resampled, residual_fallbacks, errors;
 };
 
+// Control words of one stochastic-chain call (verify_kernel).  Every word is
+// zero between calls: the last thread that uses one in a call puts it back.
+struct Control {
+  int item_cursor;  // next streaming item
+  int res_cursor;   // next residual-task ticket
+  int ready_tail;   // sequences published for a residual draw
+  int determined;   // sequences whose outcome is known
+  int exited;       // CTAs that have finished
+  int pad[3];
+};
+
+// A sequence published for its residual draw at position n: the weights of
+// max(0, p_n - q_n) (see Weights).
+struct ReadyRec {
+  int b, n;
+  float mtc, mdc, inv_st, inv_sd;
+  int pad[2];
+};
+
 struct Params {
   const void *zt;           // [B, J, V] target rows (J = K+1 chain, N tree)
   const void *zd;           // [B, K, V] draft rows (sampling only)
@@ -85,6 +104,18 @@ struct Params {
   float *out_row_sumexp;    // [B, 2K+1] or null
   Stats *stats;             // or null
   int32_t *status;          // device status bits
+  // stochastic chain (verify_kernel): zero-at-rest control words ...
+  Control *ctl;
+  int *job_done;                 // [B*(K+1)] slices completed per job
+  unsigned long long *seq_mask;  // [B] decided bits 0..K, rejected bits 32..32+K-1 (K <= 31)
+  int *dec_count;                // [B] positions decided (K > 31)
+  int *pos_state;                // [B*(K+1)] 1 accepted / row done, 2 rejected (K > 31)
+  int *res_done;                 // [B] residual slices completed
+  int *ready_flag;               // [B] ready slot -> b + 1 once its record is written
+  // ... and data written before it is read in the same call
+  float4 *norms;                 // [B*(K+1)] (max, sumexp) of target and draft row
+  ReadyRec *ready;               // [B]
+  float *rmass;                  // [B * C * NCW] residual mass of each range
 };
 
 // ------------------------------------------------------------------ elements
