@@ -561,10 +561,29 @@ __global__ void __launch_bounds__(NT_V, 2) verify_kernel(const Params p) {
     };
 
     // lane 0 holds the tickets: the next streaming item and one residual task
+    // (task index held = slot * C + slice).  Streaming items come from this
+    // CTA's shard first, then from the others once it is used up; residual
+    // tickets always from this CTA's shard.
+    const int ns = p.nshard;
+    const int rshard = static_cast<int>(blockIdx.x) % ns;
+    int ishard = rshard, iempty = 0;
+    auto take_item = [&]() -> int {
+      while (iempty < ns) {
+        const long long it =
+            static_cast<long long>(atomicAdd(&p.ctl->item[ishard * SHARD_STRIDE], 1)) * ns + ishard;
+        if (it < nitems) return static_cast<int>(it);
+        ++iempty;
+        ishard = ishard + 1 == ns ? 0 : ishard + 1;
+      }
+      return nitems;
+    };
+    auto take_task = [&]() -> int {
+      return atomicAdd(&p.ctl->res[rshard * SHARD_STRIDE], 1) * ns + rshard;
+    };
     int item = 0, held = 0, flag = 0;
     if (lane == 0) {
-      item = atomicAdd(&p.ctl->item_cursor, 1);
-      held = atomicAdd(&p.ctl->res_cursor, 1);
+      item = take_item();
+      held = take_task();
     }
     bool finished = false;
     while (!finished && !tmo) {
@@ -612,7 +631,7 @@ __global__ void __launch_bounds__(NT_V, 2) verify_kernel(const Params p) {
           issue(s, target_row<DT>(p, b, n) + off, draft_row<DT>(p, b, n) + off, len, 2);
         }
         if (lane == 0) {
-          held = atomicAdd(&p.ctl->res_cursor, 1);
+          held = take_task();
           flag = 0;  // polled after the next fill, once the new ticket is in
         }
         continue;
@@ -620,7 +639,7 @@ __global__ void __launch_bounds__(NT_V, 2) verify_kernel(const Params p) {
       if (act == 2) {
         // -------- a streaming item: slice sl of job q = i * B + b
         const int it = __shfl_sync(0xFFFFFFFFu, item, 0);
-        if (lane == 0) item = atomicAdd(&p.ctl->item_cursor, 1);
+        if (lane == 0) item = take_item();
         const int q = it / C, sl = it - q * C;
         const int i = q / B, b = q - i * B;
         const int lo = sl * p.slice, len = max(0, min(p.V, lo + p.slice) - lo);
@@ -806,8 +825,10 @@ __global__ void __launch_bounds__(NT_V, 2) verify_kernel(const Params p) {
     __threadfence();
     if (atomicAdd(&p.ctl->exited, 1) == static_cast<int>(gridDim.x) - 1) {
       __threadfence();
-      p.ctl->item_cursor = 0;
-      p.ctl->res_cursor = 0;
+      for (int k = 0; k < p.nshard; ++k) {
+        p.ctl->item[k * SHARD_STRIDE] = 0;
+        p.ctl->res[k * SHARD_STRIDE] = 0;
+      }
       p.ctl->ready_tail = 0;
       p.ctl->determined = 0;
       p.ctl->exited = 0;

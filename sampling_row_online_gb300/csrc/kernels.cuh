@@ -62,13 +62,19 @@ struct Stats {  // layout-compatible with spec_stats_t
 
 // Control words of one stochastic-chain call (verify_kernel).  Every word is
 // zero between calls: the last thread that uses one in a call puts it back.
+// The tickets are sharded over up to NSHARD counters, one per 128-byte line,
+// so that no single address takes every CTA's atomics.
+constexpr int NSHARD = 32;
+constexpr int SHARD_STRIDE = 32;  // ints
 struct Control {
-  int item_cursor;  // next streaming item
-  int res_cursor;   // next residual-task ticket
-  int ready_tail;   // sequences published for a residual draw
-  int determined;   // sequences whose outcome is known
-  int exited;       // CTAs that have finished
-  int pad[3];
+  int item[NSHARD * SHARD_STRIDE];  // streaming items: shard k hands out k, k + ns, k + 2 ns, ...
+  int res[NSHARD * SHARD_STRIDE];   // residual tasks: likewise over (slot * C + slice)
+  int ready_tail;                   // sequences published for a residual draw
+  int pad0[SHARD_STRIDE - 1];
+  int determined;                   // sequences whose outcome is known
+  int pad1[SHARD_STRIDE - 1];
+  int exited;                       // CTAs that have finished
+  int pad2[SHARD_STRIDE - 1];
 };
 
 // A sequence published for its residual draw at position n: the weights of
@@ -96,6 +102,7 @@ struct Params {
   int tile;                 // elements per tile and row
   int stages;               // shared-memory stages of the tile ring
   int njobs;                // jobs in total; items = njobs * C
+  int nshard;               // ticket shards in use (verify_kernel)
   int max_depth;            // tree output width - 1
   float4 *partials;         // [njobs * C]
   int32_t *out_tokens;      // chain [B, K+1]; tree [B, max_depth+1]

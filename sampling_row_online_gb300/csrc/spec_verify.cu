@@ -304,9 +304,10 @@ int launch_step(Params &p, int dtype, bool tma, cudaStream_t stream, const Plan 
     const int smem = pl.stages * 2 * pl.tile * esz;
     if ((st = occupancy(fn, NT_V, smem, &per_sm))) return st;
     if (per_sm < 1) return fail(SPEC_ERR_UNSUPPORTED, "verify kernel does not fit on an SM");
-    const int grid = static_cast<int>(std::min<long long>(pl.nitems, static_cast<long long>(per_sm) * num_sms()));
+    const int grid = std::max(1, static_cast<int>(std::min<long long>(pl.nitems, static_cast<long long>(per_sm) * num_sms())));
+    p.nshard = std::min(NSHARD, grid);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(std::max(1, grid)), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(NT_V, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
