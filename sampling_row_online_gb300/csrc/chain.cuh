@@ -513,9 +513,18 @@ __global__ void __launch_bounds__(NT_V, 2) verify_kernel(const Params p) {
     // ------------------------------------------------------------ producer
     const int nitems = p.njobs * C;
     int pseq = 0, pdone = 0, cseq = 0;  // fills issued, fills handed in, FIFO entries
+    // Only lane 0 waits on the producer's barriers and only lane 0 arrives on
+    // them; the warp learns the outcome through the shuffle.  (Were every
+    // lane to wait, a lane that polls after lane 0 has already acted could
+    // find the next phase complete and wait for a parity that never returns.)
+    auto wait0 = [&](uint64_t *bar, uint32_t parity) {
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(bar, parity);
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) tmo = true;
+    };
     auto ctl_push = [&](int kind, int t0, int t1) {
       const int f = cseq % CTL_FIFO;
-      if (!mbar_wait_bounded(&sh.cfree[f], ((cseq / CTL_FIFO) & 1) ^ 1)) tmo = true;
+      wait0(&sh.cfree[f], ((cseq / CTL_FIFO) & 1) ^ 1);
       if (lane == 0) {
         sh.fifo[f] = make_int4(kind, t0, t1, 0);
         mbar_arrive(&sh.cfull[f]);
@@ -525,7 +534,7 @@ __global__ void __launch_bounds__(NT_V, 2) verify_kernel(const Params p) {
     };
     auto observe = [&]() {  // the oldest fill in flight is released: hand it in
       const int s = pdone % S;
-      if (!mbar_wait_bounded(&sh.empty[s], (pdone / S) & 1)) tmo = true;
+      wait0(&sh.empty[s], (pdone / S) & 1);
       ctl_push(sh.meta[s].kind, sh.meta[s].tag0, sh.meta[s].tag1);
       ++pdone;
     };
@@ -677,7 +686,7 @@ __global__ void __launch_bounds__(NT_V, 2) verify_kernel(const Params p) {
       // wait for the held residual task or for the end of the call
       while (pdone < pseq && !tmo) observe();
       const uint64_t t0 = clock_ns();
-      for (;;) {
+      for (int polls = 0;; ++polls) {
         int st = 0;
         if (lane == 0) {
           const int slot = held / C;
@@ -697,7 +706,7 @@ __global__ void __launch_bounds__(NT_V, 2) verify_kernel(const Params p) {
           finished = true;
           break;
         }
-        if (clock_ns() - t0 > WAIT_LIMIT_NS) {
+        if (clock_ns() - t0 > WAIT_LIMIT_NS || polls > (1 << 22)) {
           tmo = true;
           break;
         }
@@ -720,7 +729,9 @@ __global__ void __launch_bounds__(NT_V, 2) verify_kernel(const Params p) {
     int k = 0;
     bool done = false;
     while (!done) {
-      if (!mbar_wait_bounded(&sh.cfull[k % CTL_FIFO], (k / CTL_FIFO) & 1)) {
+      // every lane waits (acquiring the entry); the outcome is decided warp-wide
+      const bool ok = mbar_wait_bounded(&sh.cfull[k % CTL_FIFO], (k / CTL_FIFO) & 1);
+      if (!__all_sync(0xFFFFFFFFu, ok)) {
         tmo = true;
         break;
       }
@@ -768,7 +779,10 @@ __global__ void __launch_bounds__(NT_V, 2) verify_kernel(const Params p) {
     od.init();
     for (int seq = 0;; ++seq) {
       const int s = seq % S;
-      if (!mbar_wait_bounded(&sh.full[s], (seq / S) & 1)) {
+      // every lane waits (the TMA writes become visible to it); a timeout ends
+      // the loop for the whole warp
+      const bool ok = mbar_wait_bounded(&sh.full[s], (seq / S) & 1);
+      if (!__all_sync(0xFFFFFFFFu, ok)) {
         tmo = true;
         break;
       }

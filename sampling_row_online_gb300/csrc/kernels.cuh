@@ -383,11 +383,14 @@ struct ItemCursor {
 
 // Bounded wait on an mbarrier phase; false if it ran out.  The warp sleeps
 // in hardware between polls.
+// Also bounded in polls (each suspends at most ~20 us), should the clock
+// not advance.
+constexpr int WAIT_LIMIT_POLLS = 1 << 17;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
   if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
   const uint64_t t0 = clock_ns();
-  while (!mbar_try_wait_sleep(bar, parity, 20000u))
-    if (clock_ns() - t0 > WAIT_LIMIT_NS) return false;
+  for (int polls = 0; !mbar_try_wait_sleep(bar, parity, 20000u); ++polls)
+    if (clock_ns() - t0 > WAIT_LIMIT_NS || polls > WAIT_LIMIT_POLLS) return false;
   return true;
 }
 
@@ -496,15 +499,19 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
     int pseq = 0;
     bool tmo = false;
     auto next_stage = [&]() -> int {  // wait until the next stage is free
+      // lane 0 alone waits (it alone issues the copies); see verify_kernel
       const int s = pseq % S;
       const uint32_t round = static_cast<uint32_t>(pseq / S);
-      if (!mbar_wait_bounded(&empty[s], (round & 1u) ^ 1u)) tmo = true;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(&empty[s], (round & 1u) ^ 1u);
+      if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) tmo = true;
       return s;
     };
-    for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+    for (int it = blockIdx.x; it < nitems && !tmo; it += gridDim.x) {
       pc.set(p, it);
       for (int k = 0; k < pc.nt; ++k, ++pseq) {
         const int s = next_stage();
+        if (tmo) break;  // a wait ran out: stop (the consumers stop on their own)
         const int n = min(p.tile, pc.len - k * p.tile);
         const size_t off = static_cast<size_t>(k) * row_bytes;
         if (lane == 0) {
@@ -549,7 +556,7 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
     }
     // end of stream
     const int s = next_stage();
-    if (lane == 0) {
+    if (!tmo && lane == 0) {
       meta[s].item = -1;
       mbar_arrive(&full[s]);
     }
@@ -567,7 +574,11 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
   int aidx = INT_MAX;    // argmax index
   for (int seq = 0;; ++seq) {
     const int s = seq % S;
-    if (!mbar_wait_bounded(&full[s], static_cast<uint32_t>(seq / S) & 1u)) tmo = true;
+    const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>(seq / S) & 1u);
+    if (!__all_sync(0xFFFFFFFFu, ok)) {
+      tmo = true;
+      break;
+    }
     const StageMeta m = meta[s];
     if (m.item < 0) break;
     // this warp's contiguous share of the tile's vectors (lanes interleaved)
