@@ -33,15 +33,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "verified draft positions/sec and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
 UNIT = "positions/s"
-# kernels one call launches: the stochastic chain is one persistent kernel;
-# greedy chains and trees are the streaming argmax kernel plus the per-sequence
-# finish kernel
-def launches_per_call(w) -> int:
-    return 2 if (w.kind == "tree" or w.T == 0) else 1
-
-
-def timed_kernel(w) -> str:
-    return "row_kernel" if (w.kind == "tree" or w.T == 0) else "verify_kernel"
+LAUNCHES_PER_CALL = 2  # the streaming row kernel and the per-sequence decision kernel
 
 
 def _peaks():
@@ -325,14 +317,12 @@ def run_gpu(args, w):
         return 0
 
     peak, peak_kind = _peaks()
-    kernel = timed_kernel(w)
+    kernel = "row_kernel"
     achieved = w.algorithmic_bytes / (avg_launch_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
                 "traffic": _profile_traffic(kernel, w.name), "kernel": kernel,
-                "timed": ("whole call (verify_kernel, one launch), events around each call"
-                          if launches_per_call(w) == 1 else
-                          "whole call (row_kernel + finish_kernel), events around each call"),
+                "timed": "whole call (row_kernel + decision kernel), events around each call",
                 "algorithmic_bytes_per_launch": w.algorithmic_bytes,
                 "avg_launch_us": avg_launch_ms * 1e3}
     # CPU baseline: the oracle as it stands on the host cores, bounded sample
@@ -360,7 +350,7 @@ def run_gpu(args, w):
         "achieved_hbm_gbs": achieved,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * launches_per_call(w),
+        "gpu_launches": args.steps * LAUNCHES_PER_CALL,
         "clocks": clk,
         "wall_s": wall,
     }

@@ -60,31 +60,6 @@ struct Stats {  // layout-compatible with spec_stats_t
   unsigned long long sequences, accepted, bonus, resampled, residual_fallbacks, errors;
 };
 
-// Control words of one stochastic-chain call (verify_kernel).  Every word is
-// zero between calls: the last thread that uses one in a call puts it back.
-// The tickets are sharded over up to NSHARD counters, one per 128-byte line,
-// so that no single address takes every CTA's atomics.
-constexpr int NSHARD = 32;
-constexpr int SHARD_STRIDE = 32;  // ints
-struct Control {
-  int item[NSHARD * SHARD_STRIDE];  // streaming items: shard k hands out k, k + ns, k + 2 ns, ...
-  int res[NSHARD * SHARD_STRIDE];   // residual tasks: likewise over (slot * C + slice)
-  int ready_tail;                   // sequences published for a residual draw
-  int pad0[SHARD_STRIDE - 1];
-  int determined;                   // sequences whose outcome is known
-  int pad1[SHARD_STRIDE - 1];
-  int exited;                       // CTAs that have finished
-  int pad2[SHARD_STRIDE - 1];
-};
-
-// A sequence published for its residual draw at position n: the weights of
-// max(0, p_n - q_n) (see Weights).
-struct ReadyRec {
-  int b, n;
-  float mtc, mdc, inv_st, inv_sd;
-  int pad[2];
-};
-
 struct Params {
   const void *zt;           // [B, J, V] target rows (J = K+1 chain, N tree)
   const void *zd;           // [B, K, V] draft rows (sampling only)
@@ -102,7 +77,6 @@ struct Params {
   int tile;                 // elements per tile and row
   int stages;               // shared-memory stages of the tile ring
   int njobs;                // jobs in total; items = njobs * C
-  int nshard;               // ticket shards in use (verify_kernel)
   int max_depth;            // tree output width - 1
   float4 *partials;         // [njobs * C]
   int32_t *out_tokens;      // chain [B, K+1]; tree [B, max_depth+1]
@@ -111,18 +85,6 @@ struct Params {
   float *out_row_sumexp;    // [B, 2K+1] or null
   Stats *stats;             // or null
   int32_t *status;          // device status bits
-  // stochastic chain (verify_kernel): zero-at-rest control words ...
-  Control *ctl;
-  int *job_done;                 // [B*(K+1)] slices completed per job
-  unsigned long long *seq_mask;  // [B] decided bits 0..K, rejected bits 32..32+K-1 (K <= 31)
-  int *dec_count;                // [B] positions decided (K > 31)
-  int *pos_state;                // [B*(K+1)] 1 accepted / row done, 2 rejected (K > 31)
-  int *res_done;                 // [B] residual slices completed
-  int *ready_flag;               // [B] ready slot -> b + 1 once its record is written
-  // ... and data written before it is read in the same call
-  float4 *norms;                 // [B*(K+1)] (max, sumexp) of target and draft row
-  ReadyRec *ready;               // [B]
-  float *rmass;                  // [B * C * NCW] residual mass of each range
 };
 
 // ------------------------------------------------------------------ elements
@@ -499,7 +461,10 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
     int pseq = 0;
     bool tmo = false;
     auto next_stage = [&]() -> int {  // wait until the next stage is free
-      // lane 0 alone waits (it alone issues the copies); see verify_kernel
+      // Lane 0 alone waits (it alone issues the copies) and the warp learns
+      // the outcome through the shuffle.  Were every lane to wait, a lane
+      // polling after lane 0 had refilled the stage could find the next
+      // phase complete and wait for a parity that never comes back.
       const int s = pseq % S;
       const uint32_t round = static_cast<uint32_t>(pseq / S);
       int ok = 1;
@@ -574,6 +539,8 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
   int aidx = INT_MAX;    // argmax index
   for (int seq = 0;; ++seq) {
     const int s = seq % S;
+    // every lane waits (the bulk-copied bytes become visible to it); a
+    // timeout ends the loop for the whole warp
     const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>(seq / S) & 1u);
     if (!__all_sync(0xFFFFFFFFu, ok)) {
       tmo = true;

@@ -61,49 +61,6 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
   return done != 0;
 }
 
-// Non-blocking probe of an mbarrier phase: true iff the phase with the given
-// parity has completed.
-__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// ------------------------------------------------ GPU-scope synchronisation
-// Atomic add with acquire-release semantics at GPU scope: the caller's
-// earlier writes are visible to whoever observes this update, and writes
-// released by the earlier updates of the counter are visible to the caller.
-__device__ __forceinline__ int atom_add_acq_rel(int *p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
-__device__ __forceinline__ unsigned long long atom_or_acq_rel(unsigned long long *p,
-                                                              unsigned long long v) {
-  unsigned long long old;
-  asm volatile("atom.acq_rel.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
-  return old;
-}
-
-// Relaxed (morally strong) load and store at GPU scope, for flags polled by
-// other CTAs; pair them with __threadfence() for ordering.
-__device__ __forceinline__ int ld_relaxed(const int *p) {
-  int v;
-  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_relaxed(int *p, int v) {
-  asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // Packed bf16 maximum of two pairs.
 __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
   uint32_t r;

@@ -13,7 +13,7 @@
 #include <string>
 #include <vector>
 
-#include "chain.cuh"
+#include "kernels.cuh"
 #include "spec_verify.h"
 
 namespace spec {
@@ -31,64 +31,16 @@ int cuda_fail(cudaError_t e, const char *what) {
   return SPEC_ERR_CUDA;
 }
 
-// ------------------------------------------------------------ scratch
-// Device scratch of one call: the status word, the row partials (float4 per
-// job, slice and consumer warp), the control words of the stochastic chain
-// (zero between calls) and its per-call data.
-struct Scratch {
-  int32_t *status = nullptr;
-  float4 *partials = nullptr;
-  size_t cap_parts = 0;
-  unsigned char *zero = nullptr;  // zero-at-rest control words
-  size_t zero_cap = 0;
-  unsigned char *data = nullptr;  // written before read within a call
-  size_t data_cap = 0;
-};
-
-// Byte offsets of the stochastic chain's arrays inside Scratch::zero and
-// Scratch::data for B sequences, K drafts and C slices per row.
-struct ChainLayout {
-  size_t ctl, job_done, seq_mask, dec_count, pos_state, res_done, ready_flag, zero_bytes;
-  size_t norms, ready, rmass, data_bytes;
-};
-
-ChainLayout chain_layout(long long B, long long K, long long C) {
-  auto up = [](long long x) { return static_cast<size_t>((x + 255) / 256 * 256); };
-  ChainLayout L;
-  size_t o = 0;
-  L.ctl = o;
-  o += up(sizeof(Control));
-  L.job_done = o;
-  o += up(4 * B * (K + 1));
-  L.seq_mask = o;
-  o += up(8 * B);
-  L.dec_count = o;
-  o += up(4 * B);
-  L.pos_state = o;
-  o += up(4 * B * (K + 1));
-  L.res_done = o;
-  o += up(4 * B);
-  L.ready_flag = o;
-  o += up(4 * B);
-  L.zero_bytes = o;
-  o = 0;
-  L.norms = o;
-  o += up(16 * B * (K + 1));
-  L.ready = o;
-  o += up(static_cast<long long>(sizeof(ReadyRec)) * B);
-  L.rmass = o;
-  o += up(4 * B * C * NCW);
-  L.data_bytes = o;
-  return L;
-}
-
 // ------------------------------------------------------------ workspaces
-// Per (device, stream): a Scratch whose regions only grow, and a staging
-// area for the host-buffer entry point.
+// Per (device, stream): the status word (never reallocated), the row
+// partials of the current call (float4 per job and slice, grow-only), and a
+// staging area for the host-buffer entry point.
 struct Workspace {
   int device = -1;
   cudaStream_t stream = nullptr;
-  Scratch sc;
+  int32_t *status = nullptr;
+  float4 *partials = nullptr;
+  size_t cap_parts = 0;
   unsigned char *stage = nullptr;
   size_t stage_cap = 0;
 };
@@ -107,54 +59,38 @@ Workspace *find_ws(int device, cudaStream_t stream, bool create) {
   return w;
 }
 
-// Grows one region (cudaFree synchronises the device, so no call still uses
-// the old one); a new control region is zeroed on `stream`.
-template <class T>
-int grow(T **ptr, size_t *cap, size_t need, bool zero, cudaStream_t stream, const char *what) {
-  if (*cap >= need) return SPEC_OK;
-  cudaError_t e;
-  if (*ptr) {
-    e = cudaFree(*ptr);
-    *ptr = nullptr;
-    *cap = 0;
-    if (e != cudaSuccess) return cuda_fail(e, what);
-  }
-  void *q = nullptr;
-  if ((e = cudaMalloc(&q, need)) != cudaSuccess) return cuda_fail(e, what);
-  if (zero && (e = cudaMemsetAsync(q, 0, need, stream)) != cudaSuccess) {
-    cudaFree(q);
-    return cuda_fail(e, what);
-  }
-  *ptr = static_cast<T *>(q);
-  *cap = need;
-  return SPEC_OK;
-}
-
-int get_ws(cudaStream_t stream, size_t nparts, size_t zero_bytes, size_t data_bytes, Workspace **out) {
+int get_ws(cudaStream_t stream, size_t nparts, Workspace **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   std::lock_guard<std::mutex> lock(g_mu);
   Workspace *w = find_ws(dev, stream, true);
-  Scratch &sc = w->sc;
-  if (!sc.status) {
-    if ((e = cudaMalloc(&sc.status, sizeof(int32_t))) != cudaSuccess) return cuda_fail(e, "cudaMalloc(status)");
-    if ((e = cudaMemsetAsync(sc.status, 0, sizeof(int32_t), stream)) != cudaSuccess)
-      return cuda_fail(e, "cudaMemsetAsync(status)");
+  if (!w->status) {
+    e = cudaMalloc(&w->status, sizeof(int32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status)");
+    e = cudaMemsetAsync(w->status, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
   }
-  size_t cap = sc.cap_parts * sizeof(float4);
-  int st;
-  if ((st = grow(&sc.partials, &cap, nparts * sizeof(float4), false, stream, "cudaMalloc(partials)"))) return st;
-  sc.cap_parts = cap / sizeof(float4);
-  if ((st = grow(&sc.zero, &sc.zero_cap, zero_bytes, true, stream, "cudaMalloc(control)"))) return st;
-  if ((st = grow(&sc.data, &sc.data_cap, data_bytes, false, stream, "cudaMalloc(chain data)"))) return st;
+  if (w->cap_parts < nparts) {
+    if (w->partials) {
+      e = cudaFree(w->partials);  // synchronises the device: no call still uses it
+      w->partials = nullptr;
+      w->cap_parts = 0;
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFree(partials)");
+    }
+    e = cudaMalloc(&w->partials, sizeof(float4) * nparts);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(partials)");
+    w->cap_parts = nparts;
+  }
   *out = w;
   return SPEC_OK;
 }
 
 // ------------------------------------------------------------ geometry
-constexpr int DEFAULT_STAGES = 2;          // tile ring depth
-constexpr int TILE_MAX_BYTES = 16 * 1024;  // tile width per row
+constexpr int DEFAULT_STAGES = 2;               // tile ring depth
+constexpr int TILE_MAX_BYTES = 16 * 1024;       // tile width per row
+constexpr int DRAW_SLICE_BYTES = 32 * 1024;     // draw: bytes of each row per CTA
+constexpr int DRAW_STAGE_LIMIT = 72 * 1024;     // draw: largest staged shared memory
 
 int env_int(const char *name, int dflt, int lo, int hi) {
   const char *v = std::getenv(name);
@@ -166,15 +102,15 @@ int env_int(const char *name, int dflt, int lo, int hi) {
 struct KernelCache {
   const void *fn;
   int device;
-  int smem_set;     // largest dynamic smem attribute set so far
-  int q_smem, q_nt;  // last occupancy query
+  int smem_set;   // largest dynamic smem attribute set so far
+  int q_smem, q_C;  // last occupancy query
   int q_result;
 };
 std::vector<KernelCache> g_kc;
 
-// Dynamic-smem attribute once per (kernel, device) and size, then the
-// resident blocks of `nt` threads per SM.
-int occupancy(const void *fn, int nt, int smem, int *result) {
+// Dynamic-smem attribute once per (kernel, device) and size, then either the
+// resident blocks per SM (C == 0) or the resident clusters of size C.
+int occupancy(const void *fn, int smem, int C, int *result) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -190,6 +126,10 @@ int occupancy(const void *fn, int nt, int smem, int *result) {
     k.q_smem = -1;
     g_kc.push_back(k);
     kc = &g_kc.back();
+    if (C > 0) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster)");
+    }
   }
   if (smem > kc->smem_set) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -197,15 +137,30 @@ int occupancy(const void *fn, int nt, int smem, int *result) {
     kc->smem_set = smem;
     kc->q_smem = -1;
   }
-  if (kc->q_smem != smem || kc->q_nt != nt) {
+  if (kc->q_smem != smem || kc->q_C != C) {
     int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, nt, smem);
+    if (C <= 0) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, C == -1 ? NT_ROW : NT, smem);
+    } else {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(C, 1, 1);
+      cfg.blockDim = dim3(NT, 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = C;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+    }
     if (e != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
     kc->q_smem = smem;
-    kc->q_nt = nt;
+    kc->q_C = C;
     kc->q_result = n;
   }
   *result = kc->q_result;
@@ -226,101 +181,98 @@ int num_sms() {
 
 bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
+template <bool ARGMAX>
 const void *pick_row_kernel(int dtype, bool tma) {
   if (dtype == SPEC_F32)
-    return tma ? reinterpret_cast<const void *>(&row_kernel<0, true, true>)
-               : reinterpret_cast<const void *>(&row_kernel<0, false, true>);
-  return tma ? reinterpret_cast<const void *>(&row_kernel<1, true, true>)
-             : reinterpret_cast<const void *>(&row_kernel<1, false, true>);
+    return tma ? reinterpret_cast<const void *>(&row_kernel<0, true, ARGMAX>)
+               : reinterpret_cast<const void *>(&row_kernel<0, false, ARGMAX>);
+  return tma ? reinterpret_cast<const void *>(&row_kernel<1, true, ARGMAX>)
+             : reinterpret_cast<const void *>(&row_kernel<1, false, ARGMAX>);
 }
 
-const void *pick_verify_kernel(int dtype, bool tma) {
+const void *pick_draw_kernel(int dtype, bool tma) {
   if (dtype == SPEC_F32)
-    return tma ? reinterpret_cast<const void *>(&verify_kernel<0, true>)
-               : reinterpret_cast<const void *>(&verify_kernel<0, false>);
-  return tma ? reinterpret_cast<const void *>(&verify_kernel<1, true>)
-             : reinterpret_cast<const void *>(&verify_kernel<1, false>);
+    return tma ? reinterpret_cast<const void *>(&draw_kernel<0, true>)
+               : reinterpret_cast<const void *>(&draw_kernel<0, false>);
+  return tma ? reinterpret_cast<const void *>(&draw_kernel<1, true>)
+             : reinterpret_cast<const void *>(&draw_kernel<1, false>);
 }
 
-// Streaming geometry: single-tile items of at most 16 KB per row.
-struct Plan {
-  int C, slice, tile, stages;
-  long long nitems;
-};
-
-int make_plan(const Params &p, int dtype, Plan *pl) {
+// The whole step: A (row statistics, persistent grid) then B (per-sequence
+// decisions and outputs, launched as a programmatic dependent of A).
+int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws_out) {
   const int esz = dtype == SPEC_F32 ? 4 : 2;
   const int VE = 16 / esz;
+  const bool argmax = p.kind != KIND_SAMPLE;
+  const int srows = argmax ? 1 : 2;
   const long long row_bytes = static_cast<long long>(p.V) * esz;
+  // streaming items are single tiles of at most 16 KB per row
   const int C_min = static_cast<int>(std::max<long long>(1, (row_bytes + TILE_MAX_BYTES - 1) / TILE_MAX_BYTES));
-  pl->C = std::max(C_min, env_int("SPEC_VERIFY_SLICES", C_min, 1, 1 << 16));
-  pl->stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
-  const int per = (p.V + pl->C - 1) / pl->C;
-  pl->slice = (per + VE - 1) / VE * VE;
-  pl->tile = std::min(TILE_MAX_BYTES / esz, pl->slice);
-  pl->nitems = static_cast<long long>(p.njobs) * pl->C;
-  if (pl->nitems * NCW > INT_MAX) return fail(SPEC_ERR_ARG, "too many rows");
-  return SPEC_OK;
-}
-
-// Scratch bytes a call needs: partials, control words, chain data.
-void scratch_needs(const Params &p, const Plan &pl, size_t *nparts, size_t *zero_bytes, size_t *data_bytes) {
-  *nparts = static_cast<size_t>(pl.nitems) * NCW;
-  if (p.kind == KIND_SAMPLE) {
-    const ChainLayout L = chain_layout(p.B, p.K, pl.C);
-    *zero_bytes = L.zero_bytes;
-    *data_bytes = L.data_bytes;
-  } else {
-    *zero_bytes = *data_bytes = 0;
+  const int C = std::max(C_min, env_int("SPEC_VERIFY_SLICES", C_min, 1, 1 << 16));
+  const int stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
+  const void *fa = argmax ? pick_row_kernel<true>(dtype, tma) : pick_row_kernel<false>(dtype, tma);
+  const void *fb = argmax ? reinterpret_cast<const void *>(&finish_kernel) : pick_draw_kernel(dtype, tma);
+  int smem_b = 0;
+  if (argmax)
+    smem_b = 4 * (3 * p.J) + (p.kind == KIND_TREE ? 9 * p.J : 0) + 16;
+  else
+    smem_b = (4 * (8 * p.K + 2) + 15) / 16 * 16;  // normalisers, logits at x, uniforms
+  int st;
+  // the draw: clusters of CD CTAs, each CTA walking one thread's chunk with
+  // one entry per thread, so a draw slice holds at most NT^2 entries
+  // draw: about 32 KB of each row per CTA (staged in shared memory)
+  int CD = static_cast<int>(std::min<long long>(
+      MAX_CLUSTER, std::max<long long>(1, (row_bytes + DRAW_SLICE_BYTES - 1) / DRAW_SLICE_BYTES)));
+  CD = env_int("SPEC_VERIFY_DRAW_CLUSTER", CD, 1, MAX_CLUSTER);
+  while (CD < MAX_CLUSTER && (p.V + CD - 1) / CD > NT * NT - VE) ++CD;
+  const int smem_base = smem_b;
+  int slice_d = 0, draw_stage_off = smem_base;
+  bool draw_staged = false;
+  bool allow_stage = true;
+  for (;;) {
+    const int per_d = (p.V + CD - 1) / CD;
+    slice_d = (per_d + VE - 1) / VE * VE;
+    draw_staged = !argmax && allow_stage && env_int("SPEC_VERIFY_DRAW_STAGE", 0, 0, 1) &&
+                  2LL * slice_d * esz + smem_base <= DRAW_STAGE_LIMIT;
+    smem_b = smem_base + (draw_staged ? 2 * slice_d * esz : 0);
+    if (argmax) break;
+    int nclus = 0;
+    if ((st = occupancy(fb, smem_b, CD, &nclus))) return st;
+    if (nclus > 0) break;
+    if (draw_staged) {  // first give up the staging, then shrink the cluster
+      allow_stage = false;
+      continue;
+    }
+    if (CD == 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster fits on the device");
+    CD = CD > 8 ? 8 : CD / 2;
   }
-}
-
-// The whole step on scratch `sc`.  Stochastic chain: verify_kernel, one
-// launch.  Greedy chain and tree: row_kernel (argmax partials), then
-// finish_kernel as its programmatic dependent.
-int launch_step(Params &p, int dtype, bool tma, cudaStream_t stream, const Plan &pl, const Scratch &sc) {
-  const int esz = dtype == SPEC_F32 ? 4 : 2;
-  p.C = pl.C;
-  p.slice = pl.slice;
-  p.tile = pl.tile;
-  p.stages = pl.stages;
-  p.partials = sc.partials;
-  p.status = sc.status;
-  int st, per_sm = 0;
-  cudaError_t e;
-  if (p.kind == KIND_SAMPLE) {
-    const ChainLayout L = chain_layout(p.B, p.K, pl.C);
-    p.ctl = reinterpret_cast<Control *>(sc.zero + L.ctl);
-    p.job_done = reinterpret_cast<int *>(sc.zero + L.job_done);
-    p.seq_mask = reinterpret_cast<unsigned long long *>(sc.zero + L.seq_mask);
-    p.dec_count = reinterpret_cast<int *>(sc.zero + L.dec_count);
-    p.pos_state = reinterpret_cast<int *>(sc.zero + L.pos_state);
-    p.res_done = reinterpret_cast<int *>(sc.zero + L.res_done);
-    p.ready_flag = reinterpret_cast<int *>(sc.zero + L.ready_flag);
-    p.norms = reinterpret_cast<float4 *>(sc.data + L.norms);
-    p.ready = reinterpret_cast<ReadyRec *>(sc.data + L.ready);
-    p.rmass = reinterpret_cast<float *>(sc.data + L.rmass);
-    const void *fn = pick_verify_kernel(dtype, tma);
-    const int smem = pl.stages * 2 * pl.tile * esz;
-    if ((st = occupancy(fn, NT_V, smem, &per_sm))) return st;
-    if (per_sm < 1) return fail(SPEC_ERR_UNSUPPORTED, "verify kernel does not fit on an SM");
-    const int grid = std::max(1, static_cast<int>(std::min<long long>(pl.nitems, static_cast<long long>(per_sm) * num_sms())));
-    p.nshard = std::min(NSHARD, grid);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-    cfg.blockDim = dim3(NT_V, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    void *args[] = {&p};
-    e = cudaLaunchKernelExC(&cfg, fn, args);
-    if (e != cudaSuccess) return cuda_fail(e, "verify kernel launch");
-    return SPEC_OK;
-  }
-  const void *fa = pick_row_kernel(dtype, tma);
-  const int smem_a = pl.stages * pl.tile * esz;
-  if ((st = occupancy(fa, NT_ROW, smem_a, &per_sm))) return st;
+  if (!argmax && slice_d > NT * NT) return fail(SPEC_ERR_ARG, "vocabulary too large");
+  const int per = (p.V + C - 1) / C;
+  const int slice = (per + VE - 1) / VE * VE;
+  // tiles of up to 16 KB per row, never wider than a slice
+  const int tile = std::min(TILE_MAX_BYTES / esz, slice);
+  const int smem_a = stages * srows * tile * esz;
+  const long long nitems = static_cast<long long>(p.njobs) * C;
+  if (nitems > INT_MAX) return fail(SPEC_ERR_ARG, "too many rows");
+  int per_sm = 0;
+  if ((st = occupancy(fa, smem_a, -1, &per_sm))) return st;
   if (per_sm < 1) return fail(SPEC_ERR_UNSUPPORTED, "row kernel does not fit on an SM");
-  const int grid_a = static_cast<int>(std::min<long long>(pl.nitems, static_cast<long long>(per_sm) * num_sms()));
+  const int grid_a = static_cast<int>(std::min<long long>(nitems, static_cast<long long>(per_sm) * num_sms()));
+
+  Workspace *w = nullptr;
+  if ((st = get_ws(stream, static_cast<size_t>(nitems) * NCW, &w))) return st;
+  p.C = C;
+  p.slice = slice;
+  p.slice_d = slice_d;
+  p.draw_staged = draw_staged ? 1 : 0;
+  p.draw_stage_off = draw_stage_off;
+  p.tile = tile;
+  p.stages = stages;
+  p.partials = w->partials;
+  p.status = w->status;
+  *ws_out = w;
+
+  cudaError_t e;
   {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid_a), 1, 1);
@@ -331,35 +283,152 @@ int launch_step(Params &p, int dtype, bool tma, cudaStream_t stream, const Plan 
     e = cudaLaunchKernelExC(&cfg, fa, args);
     if (e != cudaSuccess) return cuda_fail(e, "row kernel launch");
   }
-  const int smem_b = 4 * (3 * p.J) + (p.kind == KIND_TREE ? 9 * p.J : 0) + 16;
-  const void *fb = reinterpret_cast<const void *>(&finish_kernel);
-  if ((st = occupancy(fb, NT, smem_b, &per_sm))) return st;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.B), 1, 1);
-  cfg.blockDim = dim3(NT, 1, 1);
-  cfg.dynamicSmemBytes = smem_b;
-  cfg.stream = stream;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  void *args[] = {&p};
-  e = cudaLaunchKernelExC(&cfg, fb, args);
-  if (e != cudaSuccess) return cuda_fail(e, "finish kernel launch");
+  {
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = smem_b;
+    cfg.stream = stream;
+    if (argmax) {
+      cfg.gridDim = dim3(static_cast<unsigned>(p.B), 1, 1);
+      if ((st = occupancy(fb, smem_b, 0, &per_sm))) return st;
+    } else {
+      cfg.gridDim = dim3(static_cast<unsigned>(p.B * CD), 1, 1);
+      attr[na].id = cudaLaunchAttributeClusterDimension;
+      attr[na].val.clusterDim.x = CD;
+      attr[na].val.clusterDim.y = 1;
+      attr[na].val.clusterDim.z = 1;
+      ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    void *args[] = {&p};
+    e = cudaLaunchKernelExC(&cfg, fb, args);
+    if (e != cudaSuccess) return cuda_fail(e, "decision kernel launch");
+  }
   return SPEC_OK;
 }
 
-// The step on this stream's workspace.
-int run_step(Params &p, int dtype, bool tma, cudaStream_t stream) {
-  Plan pl;
-  int st = make_plan(p, dtype, &pl);
-  if (st) return st;
-  size_t nparts, zb, db;
-  scratch_needs(p, pl, &nparts, &zb, &db);
-  Workspace *w = nullptr;
-  if ((st = get_ws(stream, nparts, zb, db, &w))) return st;
-  return launch_step(p, dtype, tma, stream, pl, w->sc);
+// The same two launches as run_step, on scratch the caller provides
+// (partials with room for cap_parts entries, and a status word); nothing is
+// allocated.  Used by the no-allocation entry point below.
+int run_step_on(Params &p, int dtype, bool tma, cudaStream_t stream, float4 *partials,
+                size_t cap_parts, int32_t *status) {
+  const int esz = dtype == SPEC_F32 ? 4 : 2;
+  const int VE = 16 / esz;
+  const bool argmax = p.kind != KIND_SAMPLE;
+  const int srows = argmax ? 1 : 2;
+  const long long row_bytes = static_cast<long long>(p.V) * esz;
+  // streaming items are single tiles of at most 16 KB per row
+  const int C_min = static_cast<int>(std::max<long long>(1, (row_bytes + TILE_MAX_BYTES - 1) / TILE_MAX_BYTES));
+  const int C = std::max(C_min, env_int("SPEC_VERIFY_SLICES", C_min, 1, 1 << 16));
+  const int stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
+  const void *fa = argmax ? pick_row_kernel<true>(dtype, tma) : pick_row_kernel<false>(dtype, tma);
+  const void *fb = argmax ? reinterpret_cast<const void *>(&finish_kernel) : pick_draw_kernel(dtype, tma);
+  int smem_b = 0;
+  if (argmax)
+    smem_b = 4 * (3 * p.J) + (p.kind == KIND_TREE ? 9 * p.J : 0) + 16;
+  else
+    smem_b = (4 * (8 * p.K + 2) + 15) / 16 * 16;  // normalisers, logits at x, uniforms
+  int st;
+  // the draw: clusters of CD CTAs, each CTA walking one thread's chunk with
+  // one entry per thread, so a draw slice holds at most NT^2 entries
+  // draw: about 32 KB of each row per CTA (staged in shared memory)
+  int CD = static_cast<int>(std::min<long long>(
+      MAX_CLUSTER, std::max<long long>(1, (row_bytes + DRAW_SLICE_BYTES - 1) / DRAW_SLICE_BYTES)));
+  CD = env_int("SPEC_VERIFY_DRAW_CLUSTER", CD, 1, MAX_CLUSTER);
+  while (CD < MAX_CLUSTER && (p.V + CD - 1) / CD > NT * NT - VE) ++CD;
+  const int smem_base = smem_b;
+  int slice_d = 0, draw_stage_off = smem_base;
+  bool draw_staged = false;
+  bool allow_stage = true;
+  for (;;) {
+    const int per_d = (p.V + CD - 1) / CD;
+    slice_d = (per_d + VE - 1) / VE * VE;
+    draw_staged = !argmax && allow_stage && env_int("SPEC_VERIFY_DRAW_STAGE", 0, 0, 1) &&
+                  2LL * slice_d * esz + smem_base <= DRAW_STAGE_LIMIT;
+    smem_b = smem_base + (draw_staged ? 2 * slice_d * esz : 0);
+    if (argmax) break;
+    int nclus = 0;
+    if ((st = occupancy(fb, smem_b, CD, &nclus))) return st;
+    if (nclus > 0) break;
+    if (draw_staged) {  // first give up the staging, then shrink the cluster
+      allow_stage = false;
+      continue;
+    }
+    if (CD == 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster fits on the device");
+    CD = CD > 8 ? 8 : CD / 2;
+  }
+  if (!argmax && slice_d > NT * NT) return fail(SPEC_ERR_ARG, "vocabulary too large");
+  const int per = (p.V + C - 1) / C;
+  const int slice = (per + VE - 1) / VE * VE;
+  // tiles of up to 16 KB per row, never wider than a slice
+  const int tile = std::min(TILE_MAX_BYTES / esz, slice);
+  const int smem_a = stages * srows * tile * esz;
+  const long long nitems = static_cast<long long>(p.njobs) * C;
+  if (nitems > INT_MAX) return fail(SPEC_ERR_ARG, "too many rows");
+  int per_sm = 0;
+  if ((st = occupancy(fa, smem_a, -1, &per_sm))) return st;
+  if (per_sm < 1) return fail(SPEC_ERR_UNSUPPORTED, "row kernel does not fit on an SM");
+  const int grid_a = static_cast<int>(std::min<long long>(nitems, static_cast<long long>(per_sm) * num_sms()));
+
+  if (static_cast<size_t>(nitems) * NCW > cap_parts)
+    return fail(SPEC_ERR_ARG, "call too large for the fixed scratch of spec_verify_noalloc: "
+                              "B * (K+1) * ceil(V * element size / 16384) must not exceed " +
+                                  std::to_string(cap_parts / NCW));
+  p.C = C;
+  p.slice = slice;
+  p.slice_d = slice_d;
+  p.draw_staged = draw_staged ? 1 : 0;
+  p.draw_stage_off = draw_stage_off;
+  p.tile = tile;
+  p.stages = stages;
+  p.partials = partials;
+  p.status = status;
+
+  cudaError_t e;
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_a), 1, 1);
+    cfg.blockDim = dim3(NT_ROW, 1, 1);
+    cfg.dynamicSmemBytes = smem_a;
+    cfg.stream = stream;
+    void *args[] = {&p};
+    e = cudaLaunchKernelExC(&cfg, fa, args);
+    if (e != cudaSuccess) return cuda_fail(e, "row kernel launch");
+  }
+  {
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = smem_b;
+    cfg.stream = stream;
+    if (argmax) {
+      cfg.gridDim = dim3(static_cast<unsigned>(p.B), 1, 1);
+      if ((st = occupancy(fb, smem_b, 0, &per_sm))) return st;
+    } else {
+      cfg.gridDim = dim3(static_cast<unsigned>(p.B * CD), 1, 1);
+      attr[na].id = cudaLaunchAttributeClusterDimension;
+      attr[na].val.clusterDim.x = CD;
+      attr[na].val.clusterDim.y = 1;
+      attr[na].val.clusterDim.z = 1;
+      ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    void *args[] = {&p};
+    e = cudaLaunchKernelExC(&cfg, fb, args);
+    if (e != cudaSuccess) return cuda_fail(e, "decision kernel launch");
+  }
+  return SPEC_OK;
 }
 
 int check_common(const void *zt, int B, int V, int dtype) {
@@ -383,7 +452,7 @@ int verify_chain(const void *zt, const void *zd, const int32_t *x, int B, int K,
   if (!out_tokens || !out_n) return fail(SPEC_ERR_ARG, "output pointer is NULL");
   if (K > 0 && !x) return fail(SPEC_ERR_ARG, "draft_tokens is NULL");
   if (K > 0 && T > 0.f && !zd) return fail(SPEC_ERR_ARG, "draft_logits is NULL with T > 0");
-  if (static_cast<long long>(B) * (K + 1) > INT_MAX / (64 * NCW)) return fail(SPEC_ERR_ARG, "B*(K+1) too large");
+  if (static_cast<long long>(B) * (K + 1) * MAX_CLUSTER > INT_MAX) return fail(SPEC_ERR_ARG, "B*(K+1) too large");
 
   const int esz = dtype == SPEC_F32 ? 4 : 2;
   const bool sample = T > 0.f;
@@ -408,7 +477,8 @@ int verify_chain(const void *zt, const void *zd, const int32_t *x, int B, int K,
   p.out_row_max = row_max;
   p.out_row_sumexp = row_sumexp;
   p.stats = reinterpret_cast<Stats *>(stats);
-  return run_step(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr));
+  Workspace *w = nullptr;
+  return run_step(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr), &w);
 }
 
 int tree_depth_host(const int32_t *parent, int N) {
@@ -454,7 +524,7 @@ int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent,
   if (max_depth < 0 || max_depth >= N) return fail(SPEC_ERR_ARG, "max_depth out of range [0, N)");
   if (B == 0) return SPEC_OK;
   if (!parent || !node_tokens || !out_path || !out_len) return fail(SPEC_ERR_ARG, "NULL pointer");
-  if (static_cast<long long>(B) * N > INT_MAX / (64 * NCW)) return fail(SPEC_ERR_ARG, "B*N too large");
+  if (static_cast<long long>(B) * N * MAX_CLUSTER > INT_MAX) return fail(SPEC_ERR_ARG, "B*N too large");
   const int esz = dtype == SPEC_F32 ? 4 : 2;
   const bool tma = (static_cast<long long>(V) * esz) % 16 == 0 && aligned16(target_logits);
   Params p = {};
@@ -470,7 +540,8 @@ int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent,
   p.max_depth = max_depth;
   p.out_tokens = out_path;
   p.out_n = out_len;
-  return run_step(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr));
+  Workspace *w = nullptr;
+  return run_step(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr), &w);
 }
 
 int spec_tree_max_depth(const int32_t *parent_host, int N) {
@@ -487,10 +558,10 @@ int spec_tree_mask(const int32_t *parent, int B, int N, uint32_t *out_mask, int3
   if (!parent || !out_mask || !out_depth) return fail(SPEC_ERR_ARG, "NULL pointer");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   Workspace *w = nullptr;
-  int st = get_ws(stream, 1, 0, 0, &w);
+  int st = get_ws(stream, 1, &w);
   if (st) return st;
   const int W = (N + 31) / 32;
-  tree_mask_kernel<<<B, NT, 0, stream>>>(parent, N, W, out_mask, out_depth, w->sc.status);
+  tree_mask_kernel<<<B, NT, 0, stream>>>(parent, N, W, out_mask, out_depth, w->status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "tree_mask_kernel launch");
   return SPEC_OK;
@@ -507,18 +578,13 @@ int spec_get_status(void *stream_ptr) {
     std::lock_guard<std::mutex> lock(g_mu);
     w = find_ws(dev, stream, false);
   }
-  if (!w || !w->sc.status) return SPEC_OK;
+  if (!w || !w->status) return SPEC_OK;
   int32_t bits = 0;
-  if ((e = cudaMemcpy(&bits, w->sc.status, sizeof bits, cudaMemcpyDeviceToHost)) != cudaSuccess)
+  if ((e = cudaMemcpy(&bits, w->status, sizeof bits, cudaMemcpyDeviceToHost)) != cudaSuccess)
     return cuda_fail(e, "cudaMemcpy(status)");
   if (bits == 0) return SPEC_OK;
-  if ((e = cudaMemset(w->sc.status, 0, sizeof(int32_t))) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
-  if (bits & ST_TIMEOUT) {
-    // an interrupted call leaves its control words behind: start from zero
-    if (w->sc.zero && (e = cudaMemset(w->sc.zero, 0, w->sc.zero_cap)) != cudaSuccess)
-      return cuda_fail(e, "cudaMemset(control)");
-    return fail(SPEC_ERR_TIMEOUT, "a bounded wait on the device ran out");
-  }
+  if ((e = cudaMemset(w->status, 0, sizeof(int32_t))) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+  if (bits & ST_TIMEOUT) return fail(SPEC_ERR_TIMEOUT, "a bounded wait on the device ran out");
   if (bits & ST_PARENT) return fail(SPEC_ERR_PARENT, "parent[] is not a tree of the given depth");
   return fail(SPEC_ERR_TOKEN_RANGE, "a draft or node token is outside [0, V)");
 }
@@ -601,10 +667,8 @@ void spec_shutdown(void) {
   cudaGetDevice(&cur);
   for (Workspace *w : g_ws) {
     cudaSetDevice(w->device);
-    if (w->sc.status) cudaFree(w->sc.status);
-    if (w->sc.partials) cudaFree(w->sc.partials);
-    if (w->sc.zero) cudaFree(w->sc.zero);
-    if (w->sc.data) cudaFree(w->sc.data);
+    if (w->status) cudaFree(w->status);
+    if (w->partials) cudaFree(w->partials);
     if (w->stage) cudaFree(w->stage);
     delete w;
   }
@@ -626,14 +690,9 @@ void spec_shutdown(void) {
 namespace spec {
 namespace {
 
-// Layout: status word (256-byte slot), control words (zero at rest; a static
-// array starts zeroed and every call leaves them zero), chain data, row
-// partials.  The limit B * (K+1) * C <= 65536 bounds every region.
-constexpr size_t NOALLOC_MAX_UNITS = size_t(1) << 16;                   // B * (K+1) * C
-constexpr size_t NOALLOC_MAX_PARTIALS = NOALLOC_MAX_UNITS * NCW;         // float4 entries: 8 MiB
-constexpr size_t NOALLOC_ZERO_BYTES = size_t(2) << 20;
-constexpr size_t NOALLOC_DATA_BYTES = size_t(6) << 20;
-constexpr size_t NOALLOC_BYTES = 256 + NOALLOC_ZERO_BYTES + NOALLOC_DATA_BYTES + NOALLOC_MAX_PARTIALS * sizeof(float4);
+// status word (256-byte slot) followed by the row partials
+constexpr size_t NOALLOC_MAX_PARTIALS = size_t(1) << 19;  // float4 entries: 8 MiB
+constexpr size_t NOALLOC_BYTES = 256 + NOALLOC_MAX_PARTIALS * sizeof(float4);
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
 
 constexpr int NOALLOC_MAX_DEVICES = 64;
@@ -677,7 +736,7 @@ extern "C" int spec_verify_noalloc(const void *target_logits, const void *draft_
   if (!out_tokens || !out_n_accepted) return fail(SPEC_ERR_ARG, "output pointer is NULL");
   if (K > 0 && !draft_tokens) return fail(SPEC_ERR_ARG, "draft_tokens is NULL");
   if (K > 0 && T > 0.f && !draft_logits) return fail(SPEC_ERR_ARG, "draft_logits is NULL with T > 0");
-  if (static_cast<long long>(B) * (K + 1) > INT_MAX / (64 * NCW)) return fail(SPEC_ERR_ARG, "B*(K+1) too large");
+  if (static_cast<long long>(B) * (K + 1) * MAX_CLUSTER > INT_MAX) return fail(SPEC_ERR_ARG, "B*(K+1) too large");
   unsigned char *scratch = nullptr;
   if ((st = noalloc_scratch(&scratch))) return st;
   const int esz = dtype == SPEC_F32 ? 4 : 2;
@@ -698,21 +757,7 @@ extern "C" int spec_verify_noalloc(const void *target_logits, const void *draft_
   p.njobs = B * (K + 1);
   p.out_tokens = out_tokens;
   p.out_n = out_n_accepted;
-  Plan pl;
-  if ((st = make_plan(p, dtype, &pl))) return st;
-  size_t nparts, zb, db;
-  scratch_needs(p, pl, &nparts, &zb, &db);
-  if (nparts > NOALLOC_MAX_PARTIALS || zb > NOALLOC_ZERO_BYTES || db > NOALLOC_DATA_BYTES)
-    return fail(SPEC_ERR_ARG, "call too large for the fixed scratch of spec_verify_noalloc: "
-                              "B * (K+1) * ceil(V * element size / 16384) must not exceed " +
-                                  std::to_string(NOALLOC_MAX_UNITS));
-  Scratch sc;
-  sc.status = reinterpret_cast<int32_t *>(scratch);
-  sc.zero = scratch + 256;
-  sc.zero_cap = NOALLOC_ZERO_BYTES;
-  sc.data = scratch + 256 + NOALLOC_ZERO_BYTES;
-  sc.data_cap = NOALLOC_DATA_BYTES;
-  sc.partials = reinterpret_cast<float4 *>(scratch + 256 + NOALLOC_ZERO_BYTES + NOALLOC_DATA_BYTES);
-  sc.cap_parts = NOALLOC_MAX_PARTIALS;
-  return launch_step(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr), pl, sc);
+  return run_step_on(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr),
+                     reinterpret_cast<float4 *>(scratch + 256), NOALLOC_MAX_PARTIALS,
+                     reinterpret_cast<int32_t *>(scratch));
 }
