@@ -72,8 +72,7 @@ struct Params {
   int C;                    // vocabulary slices per row in the streaming kernel
   int slice;                // elements per slice (multiple of the vector width)
   int slice_d;              // elements per CTA in the draw (multiple of the vector width)
-  int draw_staged;          // 1: the draw stages its slice in shared memory
-  int draw_stage_off;       // byte offset of that staging area in dynamic smem
+  int wbuf_off;             // draw: byte offset of the walk buffer in dynamic smem
   int tile;                 // elements per tile and row
   int stages;               // shared-memory stages of the tile ring
   int njobs;                // jobs in total; items = njobs * C
@@ -609,6 +608,23 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
 // ======================================================================
 // B. draw_kernel: decisions and the one draw of each sequence.
 // ======================================================================
+// One thread-block cluster of CD CTAs per sequence; CTA `rank` owns the
+// vocabulary slice [rank * slice_d, (rank + 1) * slice_d) of the draw.
+//
+//  1. Before the dependent-launch wait (inputs only): the draft tokens, their
+//     target and draft logits, the acceptance uniforms.
+//  2. Every CTA combines the partials of all 2K+1 rows itself (the same
+//     fixed order everywhere, so every CTA holds the same bits) and takes the
+//     K decisions left to right: no exchange is needed for them.
+//  3. n == K: rank 0 draws the bonus token from row K's partials.
+//     n < K: every warp weighs a contiguous range of its CTA's slice of the
+//     row pair (lane-strided, coalesced loads, several in flight per lane)
+//     and sums it with shuffles; each CTA's mass goes to every CTA of the
+//     cluster through distributed shared memory; after one cluster barrier
+//     every CTA knows Z and the CTA holding u * Z.  That CTA finds the warp
+//     range holding it, weighs the range into shared memory, and one warp
+//     walks its CDF.
+//
 // Weight of one vocabulary entry in the draw: the residual max(0, p - q) of a
 // rejected pair, or the unnormalised p of a draw from p.  Explicit roundings,
 // so the summation and the walk compute identical bits.
@@ -624,167 +640,208 @@ struct Weights {
 };
 
 struct DrawShared {
-  uint64_t bar;              // completion of the slice's bulk copies
-  float xz[2][MAX_CLUSTER];  // slice masses pushed by every CTA (round 0 / 1)
+  float xz[2][MAX_CLUSTER];  // CTA masses pushed by every CTA (round 0 / 1)
+  float wmass[NWARP];        // this CTA's warp-range masses
   float bf[8];
   int bi[8];
-  int scratch[NWARP];
-  float fscratch[NWARP + 1];
 };
 
-// Combined (max, sumexp) of two rows from their C x NCW partials (one per
-// slice and consumer warp), by one warp: loads are issued PARTS_PER_LANE per
-// lane and row at a time; lane l folds partials l, l+32, ... in order, then
-// a butterfly, so every lane (and every CTA) ends with the same bits.
 constexpr int PARTS_PER_LANE = 4;
 
-__device__ __forceinline__ void warp_row_stats2(const float4 *pa, bool da, const float4 *pb, bool db,
-                                                int nparts, float c, float &ma, float &sa,
-                                                float &mb, float &sb) {
+// (max, sumexp) of the target row (and of the draft row if `pair`) of one job
+// from its C x NCW partials, by one warp: lane l folds partials l, l + 32, ...
+// in order (PARTS_PER_LANE loads in flight per lane), then a butterfly, so
+// every lane (and every CTA) ends with the same bits.
+__device__ __forceinline__ void warp_norms(const float4 *parts, int nparts, float c, bool pair,
+                                           float &mt, float &st, float &md, float &sd) {
   const int lane = threadIdx.x & 31;
-  ma = mb = -INFINITY;
-  sa = sb = 0.f;
+  mt = md = -INFINITY;
+  st = sd = 0.f;
   for (int base = 0; base < nparts; base += 32 * PARTS_PER_LANE) {
-    float4 va[PARTS_PER_LANE], vb[PARTS_PER_LANE];
+    float4 v[PARTS_PER_LANE];
 #pragma unroll
     for (int k = 0; k < PARTS_PER_LANE; ++k) {
       const int j = base + lane + 32 * k;
-      va[k] = (pa && j < nparts) ? __ldcg(pa + j) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-      vb[k] = (pb && j < nparts) ? __ldcg(pb + j) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+      v[k] = j < nparts ? __ldcg(parts + j) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
     }
 #pragma unroll
     for (int k = 0; k < PARTS_PER_LANE; ++k) {
-      ms_combine(ma, sa, da ? va[k].z : va[k].x, da ? va[k].w : va[k].y, c);
-      ms_combine(mb, sb, db ? vb[k].z : vb[k].x, db ? vb[k].w : vb[k].y, c);
+      ms_combine(mt, st, v[k].x, v[k].y, c);
+      if (pair) ms_combine(md, sd, v[k].z, v[k].w, c);
     }
   }
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    float m2 = __shfl_xor_sync(0xFFFFFFFFu, ma, off), s2 = __shfl_xor_sync(0xFFFFFFFFu, sa, off);
-    ms_combine(ma, sa, m2, s2, c);
-    m2 = __shfl_xor_sync(0xFFFFFFFFu, mb, off);
-    s2 = __shfl_xor_sync(0xFFFFFFFFu, sb, off);
-    ms_combine(mb, sb, m2, s2, c);
+    float m2 = __shfl_xor_sync(0xFFFFFFFFu, mt, off), s2 = __shfl_xor_sync(0xFFFFFFFFu, st, off);
+    ms_combine(mt, st, m2, s2, c);
+    if (pair) {
+      m2 = __shfl_xor_sync(0xFFFFFFFFu, md, off);
+      s2 = __shfl_xor_sync(0xFFFFFFFFu, sd, off);
+      ms_combine(md, sd, m2, s2, c);
+    }
   }
 }
 
-// Draw from p (unnormalised weights 2^((z - M) c)) of one target row using
-// its streaming partials: the partial of (slice s, warp w) is the mass of a
-// contiguous vocabulary range, so the range holding u * Z is found from the
-// partials alone and only that range (at most 1024 entries) is read.  Called
-// by every thread of one CTA; returns the token in every thread.
+// Exclusive prefix sum over the lanes; *total = the warp's sum (every lane).
+__device__ __forceinline__ float warp_excl_scan(float v, float *total) {
+  const int lane = threadIdx.x & 31;
+  float inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float n = __shfl_up_sync(0xFFFFFFFFu, inc, off);
+    if (lane >= off) inc = __fadd_rn(inc, n);
+  }
+  *total = __shfl_sync(0xFFFFFFFFu, inc, 31);
+  const float ex = __shfl_up_sync(0xFFFFFFFFu, inc, 1);
+  return lane ? ex : 0.f;
+}
+
+// Butterfly sum: the same bits in every lane.
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xFFFFFFFFu, v, off));
+  return v;
+}
+
+// Inverse-CDF walk of the weights wbuf[0, len) of one range whose preceding
+// mass is P, by one warp: the smallest entry e whose running mass P + C(e)
+// passes t, else (or if `lastmode`) the last entry of positive weight.  Lane
+// l holds a contiguous chunk; the chunk test and the walk inside the chunk
+// compare the same sums (the chunk's prefix from zero, added to the same
+// base), so a chunk chosen by its total always yields an entry.  Returns the
+// entry index in every lane (0 if the range has no positive weight).
+__device__ __forceinline__ int warp_walk(const float *wbuf, int len, float P, float t, bool lastmode) {
+  const int lane = threadIdx.x & 31;
+  const int cper = (len + 31) / 32;
+  const int a0 = min(len, lane * cper), a1 = min(len, a0 + cper);
+  float csum = 0.f;
+  for (int e = a0; e < a1; ++e) csum = __fadd_rn(csum, wbuf[e]);
+  float ctot;
+  const float E0 = __fadd_rn(P, warp_excl_scan(csum, &ctot));
+  int pick = -1;
+  const unsigned hit = lastmode ? 0u : __ballot_sync(0xFFFFFFFFu, csum > 0.f && __fadd_rn(E0, csum) > t);
+  if (hit) {
+    const int who = __ffs(hit) - 1;
+    if (lane == who) {
+      float pre = 0.f;
+      for (int e = a0; e < a1; ++e) {
+        const float x = wbuf[e];
+        pre = __fadd_rn(pre, x);
+        if (x > 0.f && __fadd_rn(E0, pre) > t) {
+          pick = e;
+          break;
+        }
+      }
+    }
+    pick = __shfl_sync(0xFFFFFFFFu, pick, who);
+  }
+  if (pick < 0) {  // the last entry of positive weight
+    int lastp = -1;
+    for (int e = a0; e < a1; ++e)
+      if (wbuf[e] > 0.f) lastp = e;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) lastp = max(lastp, __shfl_xor_sync(0xFFFFFFFFu, lastp, off));
+    pick = lastp < 0 ? 0 : lastp;
+  }
+  return pick;
+}
+
+// Bonus draw from p (unnormalised weights 2^((z - M) c)) of one target row,
+// by one CTA, from the row's streaming partials: the partial of (slice s,
+// consumer warp w) is the mass of a contiguous vocabulary range, so warp 0
+// finds the range holding u * Z from the partials alone; the CTA weighs that
+// range (at most one streaming tile's warp share) into `wbuf` and warp 0
+// walks it.  Returns the token in thread 0.
 template <int DT>
 __device__ __forceinline__ int draw_p_from_partials(const Params &p, const float4 *parts,
                                                     const unsigned char *row, float M, float u,
-                                                    int *scratch, float *fscratch, float *bcast) {
+                                                    float *wbuf, DrawShared &sh) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
   const int tid = threadIdx.x, lane = tid & 31;
   const float c = p.c, Mc = M * c;
   const int nparts = p.C * NCW;
-  // 1. range masses, scanned in order by warp 0 (lane l: a contiguous run)
+  auto mass = [&](int j) -> float {
+    const float4 v = __ldcg(parts + j);
+    return v.x == -INFINITY ? 0.f : __fmul_rn(v.y, ex2(fmaf(v.x, c, -Mc)));
+  };
   if (tid < 32) {
+    // range masses; lane l holds a contiguous run of them
+    constexpr int BATCH = 4;
     const int per = (nparts + 31) / 32;
     const int j0 = min(nparts, lane * per), j1 = min(nparts, j0 + per);
     float sum = 0.f;
-    for (int j = j0; j < j1; ++j) {
-      const float4 v = __ldcg(parts + j);
-      sum = __fadd_rn(sum, v.x == -INFINITY ? 0.f : __fmul_rn(v.y, ex2(v.x * c - Mc)));
-    }
-    float inc = sum;
+    for (int j = j0; j < j1; j += BATCH) {
+      float v[BATCH];
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float n = __shfl_up_sync(0xFFFFFFFFu, inc, off);
-      if (lane >= off) inc = __fadd_rn(inc, n);
+      for (int k = 0; k < BATCH; ++k) v[k] = j + k < j1 ? mass(j + k) : 0.f;
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) sum = __fadd_rn(sum, v[k]);
     }
-    const float excl = __fsub_rn(inc, sum);
-    const float Z = __shfl_sync(0xFFFFFFFFu, inc, 31);
+    float Z;
+    const float excl = warp_excl_scan(sum, &Z);
     const float t = u * Z;
-    const unsigned hit = __ballot_sync(0xFFFFFFFFu, sum > 0.f && inc > t);
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, sum > 0.f && __fadd_rn(excl, sum) > t);
     const unsigned pos = __ballot_sync(0xFFFFFFFFu, sum > 0.f);
+    int lastmode = hit == 0;
     const int who = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
-    const bool lastmode = hit == 0;
     if (lane == who) {
-      float run = excl;
-      int own = j0, ownlast = j0;
-      float P = excl, Plast = excl;
-      bool found = false;
-      for (int j = j0; j < j1; ++j) {
-        const float4 v = __ldcg(parts + j);
-        const float mj = v.x == -INFINITY ? 0.f : __fmul_rn(v.y, ex2(v.x * c - Mc));
-        if (mj > 0.f) {
-          if (!lastmode && !found && __fadd_rn(run, mj) > t) {
-            own = j;
-            P = run;
-            found = true;
+      float pre = 0.f, P = excl, Plast = excl;
+      int own = -1, lastj = j0;
+      for (int j = j0; j < j1; j += BATCH) {
+        float v[BATCH];
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) v[k] = j + k < j1 ? mass(j + k) : 0.f;
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) {
+          const float before = __fadd_rn(excl, pre);
+          pre = __fadd_rn(pre, v[k]);
+          if (v[k] > 0.f) {
+            if (!lastmode && own < 0 && __fadd_rn(excl, pre) > t) {
+              own = j + k;
+              P = before;
+            }
+            lastj = j + k;
+            Plast = before;
           }
-          ownlast = j;
-          Plast = run;
         }
-        run = __fadd_rn(run, mj);
       }
-      if (!found) {
-        own = ownlast;
+      if (own < 0) {
+        own = lastj;
         P = Plast;
+        lastmode = 1;
       }
-      scratch[0] = own;
-      scratch[1] = found ? 0 : 1;
-      fscratch[0] = t;
-      fscratch[1] = P;
+      sh.bi[4] = own;
+      sh.bi[5] = lastmode;
+      sh.bf[4] = P;
+      sh.bf[5] = t;
     }
   }
   __syncthreads();
-  const int own = scratch[0];
-  const int pl = scratch[1];
-  const float t = fscratch[0], P = fscratch[1];
-  __syncthreads();
-  // 2. the owner range: slice s, warp w of the streaming kernel's split
+  const int own = sh.bi[4];
+  const bool lastmode = sh.bi[5] != 0;
+  const float P = sh.bf[4], t = sh.bf[5];
+  // the owner range: slice s, consumer warp w of the streaming split
   const int sl = own / NCW, w = own - sl * NCW;
   const int lo_s = sl * p.slice;
   const int len_s = max(0, min(p.V, lo_s + p.slice) - lo_s);
   const int nv = (len_s + VE - 1) / VE, nvw = (nv + NCW - 1) / NCW;
   const int r0 = lo_s + min(len_s, w * nvw * VE);
-  const int r1 = lo_s + min(len_s, (w + 1) * nvw * VE);
-  // 3. walk it: a few consecutive entries per thread, block scan
-  const int per = (r1 - r0 + NT - 1) / NT;
-  const int a0 = min(r1, r0 + tid * per), a1 = min(r1, a0 + per);
-  float sum = 0.f;
-  for (int v = a0; v < a1; ++v) sum = __fadd_rn(sum, ex2(fmaf(E::load(row, v), c, -Mc)));
-  float total;
-  const float excl = __fadd_rn(P, block_exclusive_scan(sum, fscratch, &total));
-  int pick = INT_MAX;
-  if (!pl && sum > 0.f && __fadd_rn(excl, sum) > t) {
-    float run = excl;
-    for (int v = a0; v < a1; ++v) {
-      const float x = ex2(fmaf(E::load(row, v), c, -Mc));
-      run = __fadd_rn(run, x);
-      if (x > 0.f && run > t) {
-        pick = v;
-        break;
-      }
-    }
-  }
-  pick = block_reduce_min_int(pick, scratch);
-  if (pick == INT_MAX) {
-    int last = -1;
-    for (int v = a0; v < a1; ++v)
-      if (ex2(fmaf(E::load(row, v), c, -Mc)) > 0.f) last = v;
-    pick = block_reduce_max_int(last, scratch);
-    if (pick < 0) pick = r0;
-  }
-  (void)bcast;
-  return pick;
+  const int len = lo_s + min(len_s, (w + 1) * nvw * VE) - r0;
+  for (int e = tid; e < len; e += NT) wbuf[e] = ex2(fmaf(E::load(row, r0 + e), c, -Mc));
+  __syncthreads();
+  int token = 0;
+  if (tid < 32) token = r0 + warp_walk(wbuf, len, P, t, lastmode);
+  return token;
 }
 
-// Rank 0 of the cluster combines the partials of all 2K+1 rows and takes
-// the left-to-right decisions; every CTA then draws over its own slice of
-// the vocabulary (slice_d elements, independent of the streaming kernel's
-// slices).
 template <int DT, bool TMA>
 __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
-  extern __shared__ __align__(16) float dsh[];  // row max [R], row sumexp [R], logits at x [2K], ok [K], u [K]
+  // dynamic: row max [R], row sumexp [R], logits at x [2K], ok [K], u [K],
+  // then (16-byte aligned) the walk buffer
+  extern __shared__ __align__(16) float dsh[];
   __shared__ DrawShared sh;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -796,72 +853,42 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   const float c = p.c;
   float *rmax = dsh, *rsum = dsh + R, *gx = dsh + 2 * R;
   int *gok = reinterpret_cast<int *>(dsh + 2 * R + 2 * K);
-  float *gu = dsh + 2 * R + 3 * K;  // acceptance uniforms [K]
+  float *gu = dsh + 2 * R + 3 * K;
+  float *wbuf = dsh + p.wbuf_off / 4;
 
-  if (tid == 0) {
-    mbar_init(&sh.bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
   // every CTA of the cluster must be running before any DSMEM store: arrive
   // now, wait before the first store
   cluster_arrive_relaxed();
 
-  // ---- inputs that do not depend on the first launch: the draft tokens now;
-  // their logits are gathered below, in flight together with the partials
-  int gx_tok = 0;
+  // ---- inputs (not produced by the first launch): tokens, their logits, uniforms
   for (int i = tid; i < K; i += NT) {
-    gx_tok = __ldg(p.tokens + static_cast<size_t>(b) * K + i);
+    const int x = __ldg(p.tokens + static_cast<size_t>(b) * K + i);
+    const int ok = x >= 0 && x < p.V;
+    gok[i] = ok;
+    gx[2 * i] = ok ? E::load(target_row<DT>(p, b, i), x) : 0.f;
+    gx[2 * i + 1] = ok ? E::load(draft_row<DT>(p, b, i), x) : 0.f;
     gu[i] = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
   }
   pdl_wait();  // the row partials of the first launch are complete and visible
-  if (K <= NT) {
-    for (int i = tid; i < K; i += NT) {
-      const int x = gx_tok;
-      const int ok = x >= 0 && x < p.V;
-      gok[i] = ok;
-      gx[2 * i] = ok ? E::load(target_row<DT>(p, b, i), x) : 0.f;
-      gx[2 * i + 1] = ok ? E::load(draft_row<DT>(p, b, i), x) : 0.f;
-    }
-  }
 
-  // ---- normalisers of the 2K+1 rows (target 0..K, then draft 0..K-1): this
-  // CTA combines rows rank, rank + CD, ... (two per warp per round) and
-  // pushes them into every CTA of the cluster
+  // ---- normalisers of all 2K+1 rows (target 0..K, draft 0..K-1), one job
+  // (row pair, or the bonus row) per warp
   const int nparts = p.C * NCW;
-  const int nmine = static_cast<int>(rank) < R ? (R - static_cast<int>(rank) + CD - 1) / CD : 0;
-  for (int k = 2 * warp; k < nmine; k += 2 * NWARP) {
-    const int r = static_cast<int>(rank) + CD * k;
-    const int r2 = k + 1 < nmine ? r + CD : R;
-    const bool da = r > K, db = r2 > K;
-    const float4 *pa = p.partials + static_cast<size_t>(job_of(p, b, da ? r - K - 1 : r)) * nparts;
-    const float4 *pb =
-        r2 < R ? p.partials + static_cast<size_t>(job_of(p, b, db ? r2 - K - 1 : r2)) * nparts : nullptr;
-    float ma, sa, mb, sb;
-    warp_row_stats2(pa, da, pb, db, nparts, c, ma, sa, mb, sb);
+  for (int i = warp; i <= K; i += NWARP) {
+    float mt, st, md, sd;
+    warp_norms(p.partials + static_cast<size_t>(job_of(p, b, i)) * nparts, nparts, c, i < K, mt, st, md, sd);
     if (lane == 0) {
-      rmax[r] = ma;
-      rsum[r] = sa;
-      if (r2 < R) {
-        rmax[r2] = mb;
-        rsum[r2] = sb;
+      rmax[i] = mt;
+      rsum[i] = st;
+      if (i < K) {
+        rmax[K + 1 + i] = md;
+        rsum[K + 1 + i] = sd;
       }
     }
   }
   __syncthreads();
-  cluster_wait();  // every peer is running: DSMEM stores are allowed
-  for (int t = tid; t < nmine * static_cast<int>(CD); t += NT) {
-    const int k = t / CD;
-    const uint32_t dst = static_cast<uint32_t>(t - k * CD);
-    if (dst == rank) continue;
-    const int r = static_cast<int>(rank) + CD * k;
-    dsmem_st_f32(dsmem_addr(&rmax[r], dst), rmax[r]);
-    dsmem_st_f32(dsmem_addr(&rsum[r], dst), rsum[r]);
-  }
-  cluster_sync();  // every row's normalisers are in every CTA
 
-  // ---- left-to-right acceptance: the first reject n (or K); every CTA
-  // takes the same decision from the same bits
+  // ---- left-to-right acceptance: the first reject n (or K)
   if (tid == 0) {
     int n = K, err = 0;
     for (int i = 0; i < K; ++i)
@@ -879,228 +906,197 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
     sh.bi[1] = err;
   }
   __syncthreads();
+  const int n = sh.bi[0];
+  const int err = sh.bi[1];
+  int32_t *out = p.out_tokens + static_cast<size_t>(b) * (K + 1);
   if (rank == 0) {
-    const int n0 = sh.bi[0];
     for (int r = tid; r < R; r += NT) {
       if (p.out_row_max) p.out_row_max[static_cast<size_t>(b) * R + r] = rmax[r];
       if (p.out_row_sumexp) p.out_row_sumexp[static_cast<size_t>(b) * R + r] = rsum[r];
     }
-    if (sh.bi[1]) {
-      for (int e = tid; e <= K; e += NT) p.out_tokens[static_cast<size_t>(b) * (K + 1) + e] = -1;
+    if (err) {
+      for (int e = tid; e <= K; e += NT) out[e] = -1;
       if (tid == 0) {
         p.out_n[b] = -1;
         atomicOr(p.status, ST_TOKEN);
         if (p.stats) atomicAdd(&p.stats->errors, 1ull);
       }
     }
-    (void)n0;
   }
-  const int n = sh.bi[0];
-  const int err = sh.bi[1];
+  cluster_wait();  // every peer is running (pairs with the arrive above)
+  if (err) return;
 
-  if (!err && n == K) {
+  if (n == K) {
     // ---- bonus: rank 0 draws from p_K using the streaming partials
     if (rank == 0) {
       const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(K), 1u);
       const int token = draw_p_from_partials<DT>(
-          p, p.partials + static_cast<size_t>(job_of(p, b, K)) * p.C * NCW, target_row<DT>(p, b, K),
-          rmax[K], u, sh.scratch, sh.fscratch, sh.bf);
-      int32_t *out = p.out_tokens + static_cast<size_t>(b) * (K + 1);
-      for (int j = tid; j <= K; j += NT) out[j] = j < K ? __ldg(p.tokens + static_cast<size_t>(b) * K + j) : token;
-      if (tid == 0) {
-        p.out_n[b] = K;
-        if (p.stats) {
-          atomicAdd(&p.stats->sequences, 1ull);
-          atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(K));
-          atomicAdd(&p.stats->bonus, 1ull);
+          p, p.partials + static_cast<size_t>(job_of(p, b, K)) * nparts, target_row<DT>(p, b, K), rmax[K], u,
+          wbuf, sh);
+      if (tid < 32) {
+        const int tk = __shfl_sync(0xFFFFFFFFu, token, 0);
+        for (int j = lane; j <= K; j += 32)
+          out[j] = j < K ? __ldg(p.tokens + static_cast<size_t>(b) * K + j) : tk;
+        if (lane == 0) {
+          p.out_n[b] = K;
+          if (p.stats) {
+            atomicAdd(&p.stats->sequences, 1ull);
+            atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(K));
+            atomicAdd(&p.stats->bonus, 1ull);
+          }
         }
       }
     }
-  } else if (!err) {
-    // ---- the draw: residual at n < K, or the bonus from row K
-    const bool pair = n < K;
-    const unsigned char *rt = target_row<DT>(p, b, n);
-    const unsigned char *rd = pair ? draft_row<DT>(p, b, n) : nullptr;
-    const int lo = static_cast<int>(rank) * p.slice_d;
-    const int len = max(0, min(p.V, lo + p.slice_d) - lo);
-    const int E2 = ((len + NT - 1) / NT + VE - 1) / VE * VE;
-    const int e0 = min(len, tid * E2), e1 = min(len, e0 + E2);
-    // This CTA's slice of the row(s) in shared memory when it fits: one bulk
-    // copy per row (TMA path) or a cooperative copy.
-    unsigned char *st_t = reinterpret_cast<unsigned char *>(dsh) + p.draw_stage_off;
-    unsigned char *st_d = st_t + static_cast<size_t>(p.slice_d) * E::BYTES;
-    const bool staged = p.draw_staged;
-    if (staged && len > 0) {
-      if (TMA) {
-        if (tid == 0) {
-          const uint32_t bytes = static_cast<uint32_t>(len) * E::BYTES;
-          mbar_arrive_expect_tx(&sh.bar, bytes * (pair ? 2 : 1));
-          bulk_g2s(st_t, rt + static_cast<size_t>(lo) * E::BYTES, bytes, &sh.bar);
-          if (pair) bulk_g2s(st_d, rd + static_cast<size_t>(lo) * E::BYTES, bytes, &sh.bar);
+    return;
+  }
+
+  // ---- the residual draw at position n
+  const unsigned char *rt = target_row<DT>(p, b, n);
+  const unsigned char *rd = draft_row<DT>(p, b, n);
+  const int lo = static_cast<int>(rank) * p.slice_d;
+  const int len = max(0, min(p.V, lo + p.slice_d) - lo);
+  const int nv = (len + VE - 1) / VE, nvw = (nv + NWARP - 1) / NWARP;
+  Weights W;
+  W.c = c;
+  W.mtc = rmax[n] * c;
+  W.mdc = rmax[K + 1 + n] * c;
+  W.inv_st = 1.f / rsum[n];
+  W.inv_sd = 1.f / rsum[K + 1 + n];
+  W.resid = true;
+  const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(n), 1u);
+  int fallback = 0;
+  for (int round = 0; round < 2; ++round) {
+    // warp `warp` weighs vectors [v0, v1) of the slice, lanes strided
+    const int v0 = warp * nvw, v1 = min(nv, v0 + nvw);
+    float acc = 0.f;
+    if (TMA) {  // rows 16-byte aligned, V a multiple of the vector width
+      constexpr int BATCH = 4;
+      for (int j = v0 + lane; j < v1; j += 32 * BATCH) {
+        uint4 vt[BATCH], vd[BATCH];
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) {
+          const int jj = j + 32 * k;
+          const size_t off = static_cast<size_t>(lo + jj * VE) * E::BYTES;
+          vt[k] = jj < v1 ? __ldcg(reinterpret_cast<const uint4 *>(rt + off)) : make_uint4(0, 0, 0, 0);
+          vd[k] = (jj < v1 && W.resid) ? __ldcg(reinterpret_cast<const uint4 *>(rd + off)) : make_uint4(0, 0, 0, 0);
         }
-        if (!mbar_wait_bounded(&sh.bar, 0u)) atomicOr(p.status, ST_TIMEOUT);
-      } else {
-        for (int e = tid; e < len; e += NT) {
-          E::copy_elem(st_t + e * E::BYTES, rt + static_cast<size_t>(lo + e) * E::BYTES);
-          if (pair) E::copy_elem(st_d + e * E::BYTES, rd + static_cast<size_t>(lo + e) * E::BYTES);
-        }
-        __syncthreads();
-      }
-    }
-    auto zt_at = [&](int e) -> float {
-      if (staged) return E::load_shared(st_t, e);
-      return E::load(rt, lo + e);
-    };
-    auto zd_at = [&](int e) -> float {
-      if (staged) return E::load_shared(st_d, e);
-      return E::load(rd, lo + e);
-    };
-    Weights W;
-    W.c = c;
-    W.mtc = rmax[n] * c;
-    W.mdc = pair ? rmax[K + 1 + n] * c : 0.f;
-    W.inv_st = 1.f / rsum[n];
-    W.inv_sd = pair ? 1.f / rsum[K + 1 + n] : 0.f;
-    W.resid = pair;
-    int fallback = 0, owner = 0, pl = 0;
-    float tl = 0.f, excl = 0.f, sum = 0.f;
-    for (int round = 0; round < 2; ++round) {
-      sum = 0.f;
-      if (staged) {
-        for (int e = e0; e < e1; e += VE) {
-          // e is a multiple of VE and the staging rows hold slice_d >= e1
-          // entries (rounded up to VE), so the 16-byte reads stay in bounds;
-          // entries past e1 are skipped below
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) {
+          if (j + 32 * k >= v1) break;
           float ft[VE], fd[VE];
-          E::unpack(lds128(st_t + e * E::BYTES), ft);
-          if (W.resid) E::unpack(lds128(st_d + e * E::BYTES), fd);
+          E::unpack(vt[k], ft);
+          E::unpack(vd[k], fd);
 #pragma unroll
-          for (int j = 0; j < VE; ++j)
-            if (e + j < e1) sum = __fadd_rn(sum, W(ft[j], W.resid ? fd[j] : 0.f));
+          for (int e = 0; e < VE; ++e) acc = __fadd_rn(acc, W(ft[e], fd[e]));
         }
-      } else if (TMA) {
-        // rows 16-byte aligned: 16-byte loads, four per row in flight
-        constexpr int BATCH = 4;
-        for (int e = e0; e < e1; e += BATCH * VE) {
-          uint4 vt[BATCH], vd[BATCH];
-#pragma unroll
-          for (int k = 0; k < BATCH; ++k) {
-            const int ek = e + k * VE;
-            const size_t off = static_cast<size_t>(lo + ek) * E::BYTES;
-            vt[k] = ek < e1 ? __ldcg(reinterpret_cast<const uint4 *>(rt + off)) : make_uint4(0, 0, 0, 0);
-            vd[k] = (ek < e1 && W.resid) ? __ldcg(reinterpret_cast<const uint4 *>(rd + off))
-                                         : make_uint4(0, 0, 0, 0);
-          }
-#pragma unroll
-          for (int k = 0; k < BATCH; ++k) {
-            if (e + k * VE >= e1) break;
-            float ft[VE], fd[VE];
-            E::unpack(vt[k], ft);
-            E::unpack(vd[k], fd);
-#pragma unroll
-            for (int j = 0; j < VE; ++j) sum = __fadd_rn(sum, W(ft[j], W.resid ? fd[j] : 0.f));
-          }
-        }
-      } else {
-        for (int e = e0; e < e1; ++e) sum = __fadd_rn(sum, W(zt_at(e), W.resid ? zd_at(e) : 0.f));
       }
-      float total;
-      excl = block_exclusive_scan(sum, sh.fscratch, &total);
-      if (tid < static_cast<int>(CD)) dsmem_st_f32(dsmem_addr(&sh.xz[round][rank], tid), total);
-      cluster_sync();  // slice masses visible cluster-wide
-      if (tid == 0) {
-        float Z = 0.f;
-        for (uint32_t r = 0; r < CD; ++r) Z = __fadd_rn(Z, sh.xz[round][r]);
-        int again = 0;
-        if (W.resid && !(Z > 0.f)) {
-          again = 1;  // no residual mass in fp32: draw from p at this position
-        } else {
-          const float t = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(n), 1u) * Z;
-          float P = 0.f, Pown = 0.f, Plast = 0.f;
-          int own = -1, last = -1;
-          for (uint32_t r = 0; r < CD; ++r) {
-            const float zr = sh.xz[round][r];
-            if (own < 0 && __fadd_rn(P, zr) > t) {
-              own = static_cast<int>(r);
-              Pown = P;
-            }
-            if (zr > 0.f) {
-              last = static_cast<int>(r);
-              Plast = P;
-            }
-            P = __fadd_rn(P, zr);
-          }
-          int lastmode = 0;
-          if (own < 0) {
-            own = last < 0 ? 0 : last;
-            Pown = Plast;
-            lastmode = 1;
-          }
-          sh.bi[2] = own;
-          sh.bi[3] = lastmode;
-          sh.bf[0] = t - Pown;
-        }
-        sh.bi[4] = again;
-      }
-      __syncthreads();
-      if (sh.bi[4] && round == 0) {
-        W.resid = false;
-        fallback = 1;
-        continue;
-      }
-      owner = sh.bi[2];
-      pl = sh.bi[3];
-      tl = sh.bf[0];
-      break;
+    } else {
+      const int e0 = min(len, v0 * VE), e1 = min(len, v1 * VE);
+      for (int e = e0 + lane; e < e1; e += 32)
+        acc = __fadd_rn(acc, W(E::load(rt, lo + e), W.resid ? E::load(rd, lo + e) : 0.f));
     }
-    if (static_cast<int>(rank) == owner) {
-      // the thread whose chunk holds the crossing (or the last positive one)
-      int who;
-      if (!pl)
-        who = block_reduce_min_int((sum > 0.f && __fadd_rn(excl, sum) > tl) ? tid : INT_MAX, sh.scratch);
-      else
-        who = block_reduce_max_int(sum > 0.f ? tid : -1, sh.scratch);
-      if (who == INT_MAX || who < 0) {  // rounding left no crossing: last positive entry
-        pl = 1;
-        who = block_reduce_max_int(sum > 0.f ? tid : -1, sh.scratch);
-        if (who < 0) who = 0;
-      }
-      // the whole CTA walks that chunk: one entry per thread, a block scan,
-      // and the first entry whose running mass passes tl
-      const int w0 = min(len, who * E2), w1 = min(len, w0 + E2);
-      const float wexcl = __shfl_sync(0xFFFFFFFFu, excl, who & 31);
-      if (lane == 0) sh.fscratch[warp] = wexcl;
-      __syncthreads();
-      const float base = sh.fscratch[who >> 5];
-      __syncthreads();
-      float w = 0.f;
-      const int e = w0 + tid;
-      if (e < w1) w = W(zt_at(e), W.resid ? zd_at(e) : 0.f);
-      float tot_unused;
-      const float before = block_exclusive_scan(w, sh.fscratch, &tot_unused);
-      const float run = __fadd_rn(base, __fadd_rn(before, w));
-      int pick = INT_MAX;
-      if (!pl) pick = block_reduce_min_int((w > 0.f && run > tl) ? e : INT_MAX, sh.scratch);
-      if (pick == INT_MAX) pick = block_reduce_max_int(w > 0.f ? e : -1, sh.scratch);
-      if (pick < 0) pick = w0;
-      const int token = lo + pick;
-      // ---- outputs of sequence b
-      int32_t *out = p.out_tokens + static_cast<size_t>(b) * (K + 1);
-      for (int j = tid; j <= K; j += NT)
-        out[j] = j < n ? __ldg(p.tokens + static_cast<size_t>(b) * K + j) : (j == n ? token : -1);
-      if (tid == 0) {
-        p.out_n[b] = n;
-        if (p.stats) {
-          atomicAdd(&p.stats->sequences, 1ull);
-          atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(n));
-          atomicAdd(n == K ? &p.stats->bonus : &p.stats->resampled, 1ull);
-          if (fallback) atomicAdd(&p.stats->residual_fallbacks, 1ull);
+    acc = warp_sum(acc);
+    if (lane == 0) sh.wmass[warp] = acc;
+    __syncthreads();
+    // this CTA's mass, pushed into every CTA of the cluster
+    if (tid < static_cast<int>(CD)) {
+      float cm = 0.f;
+      for (int w = 0; w < NWARP; ++w) cm = __fadd_rn(cm, sh.wmass[w]);
+      dsmem_st_f32(dsmem_addr(&sh.xz[round][rank], static_cast<uint32_t>(tid)), cm);
+    }
+    cluster_sync();  // every CTA's mass is in every CTA
+    if (tid == 0) {
+      float Z = 0.f;
+      for (uint32_t r = 0; r < CD; ++r) Z = __fadd_rn(Z, sh.xz[round][r]);
+      int again = 0;
+      if (W.resid && !(Z > 0.f)) {
+        again = 1;  // no residual mass in fp32: draw from p at this position
+      } else {
+        const float t = u * Z;
+        float P = 0.f, Pown = 0.f, Plast = 0.f;
+        int own = -1, last = -1;
+        for (uint32_t r = 0; r < CD; ++r) {
+          const float zr = sh.xz[round][r];
+          if (own < 0 && zr > 0.f && __fadd_rn(P, zr) > t) {
+            own = static_cast<int>(r);
+            Pown = P;
+          }
+          if (zr > 0.f) {
+            last = static_cast<int>(r);
+            Plast = P;
+          }
+          P = __fadd_rn(P, zr);
         }
+        int lastmode = 0;
+        if (own < 0) {
+          own = last < 0 ? 0 : last;
+          Pown = Plast;
+          lastmode = 1;
+        }
+        sh.bi[2] = own;
+        sh.bi[3] = lastmode;
+        sh.bf[0] = Pown;
+        sh.bf[1] = t;
+      }
+      sh.bi[4] = again;
+    }
+    __syncthreads();
+    if (sh.bi[4] && round == 0) {
+      W.resid = false;
+      fallback = 1;
+      continue;
+    }
+    break;
+  }
+  // No DSMEM access follows the last exchange, so only the owner CTA goes on.
+  if (static_cast<int>(rank) != sh.bi[2]) return;
+  if (tid == 0) {  // the warp range holding t
+    const float t = sh.bf[1];
+    int lastmode = sh.bi[3];
+    float P = sh.bf[0], Pown = P, Plast = P;
+    int ow = -1, last = -1;
+    for (int w = 0; w < NWARP; ++w) {
+      const float m = sh.wmass[w];
+      if (!lastmode && ow < 0 && m > 0.f && __fadd_rn(P, m) > t) {
+        ow = w;
+        Pown = P;
+      }
+      if (m > 0.f) {
+        last = w;
+        Plast = P;
+      }
+      P = __fadd_rn(P, m);
+    }
+    if (ow < 0) {
+      ow = last < 0 ? 0 : last;
+      Pown = Plast;
+      lastmode = 1;
+    }
+    sh.bi[6] = ow;
+    sh.bi[7] = lastmode;
+    sh.bf[2] = Pown;
+  }
+  __syncthreads();
+  const int ow = sh.bi[6];
+  const int r0 = min(len, ow * nvw * VE);
+  const int rlen = min(len, (ow + 1) * nvw * VE) - r0;
+  for (int e = tid; e < rlen; e += NT)
+    wbuf[e] = W(E::load(rt, lo + r0 + e), W.resid ? E::load(rd, lo + r0 + e) : 0.f);
+  __syncthreads();
+  if (tid < 32) {
+    const int token = lo + r0 + warp_walk(wbuf, rlen, sh.bf[2], sh.bf[1], sh.bi[7] != 0);
+    for (int j = lane; j <= K; j += 32)
+      out[j] = j < n ? __ldg(p.tokens + static_cast<size_t>(b) * K + j) : (j == n ? token : -1);
+    if (lane == 0) {
+      p.out_n[b] = n;
+      if (p.stats) {
+        atomicAdd(&p.stats->sequences, 1ull);
+        atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(n));
+        atomicAdd(&p.stats->resampled, 1ull);
+        if (fallback) atomicAdd(&p.stats->residual_fallbacks, 1ull);
       }
     }
   }
-  // No DSMEM access follows the last exchange (each is followed by a cluster
-  // barrier), so CTAs may leave independently.
 }
 
 // ======================================================================

@@ -90,7 +90,6 @@ int get_ws(cudaStream_t stream, size_t nparts, Workspace **out) {
 constexpr int DEFAULT_STAGES = 2;               // tile ring depth
 constexpr int TILE_MAX_BYTES = 16 * 1024;       // tile width per row
 constexpr int DRAW_SLICE_BYTES = 32 * 1024;     // draw: bytes of each row per CTA
-constexpr int DRAW_STAGE_LIMIT = 72 * 1024;     // draw: largest staged shared memory
 
 int env_int(const char *name, int dflt, int lo, int hi) {
   const char *v = std::getenv(name);
@@ -109,7 +108,8 @@ struct KernelCache {
 std::vector<KernelCache> g_kc;
 
 // Dynamic-smem attribute once per (kernel, device) and size, then either the
-// resident blocks per SM (C == 0) or the resident clusters of size C.
+// resident blocks per SM (C == -1: row kernel blocks, C == 0: NT-thread
+// blocks) or the resident clusters of size C.
 int occupancy(const void *fn, int smem, int C, int *result) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -198,9 +198,16 @@ const void *pick_draw_kernel(int dtype, bool tma) {
              : reinterpret_cast<const void *>(&draw_kernel<1, false>);
 }
 
-// The whole step: A (row statistics, persistent grid) then B (per-sequence
-// decisions and outputs, launched as a programmatic dependent of A).
-int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws_out) {
+// Launch geometry of one call.
+struct Geometry {
+  const void *fa, *fb;   // row kernel, decision kernel
+  int C, slice, tile, stages;
+  int CD, slice_d, wbuf_off;
+  int smem_a, smem_b, grid_a;
+  long long nitems;
+};
+
+int plan(Params &p, int dtype, bool tma, Geometry *g) {
   const int esz = dtype == SPEC_F32 ? 4 : 2;
   const int VE = 16 / esz;
   const bool argmax = p.kind != KIND_SAMPLE;
@@ -208,227 +215,128 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
   const long long row_bytes = static_cast<long long>(p.V) * esz;
   // streaming items are single tiles of at most 16 KB per row
   const int C_min = static_cast<int>(std::max<long long>(1, (row_bytes + TILE_MAX_BYTES - 1) / TILE_MAX_BYTES));
-  const int C = std::max(C_min, env_int("SPEC_VERIFY_SLICES", C_min, 1, 1 << 16));
-  const int stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
-  const void *fa = argmax ? pick_row_kernel<true>(dtype, tma) : pick_row_kernel<false>(dtype, tma);
-  const void *fb = argmax ? reinterpret_cast<const void *>(&finish_kernel) : pick_draw_kernel(dtype, tma);
-  int smem_b = 0;
-  if (argmax)
-    smem_b = 4 * (3 * p.J) + (p.kind == KIND_TREE ? 9 * p.J : 0) + 16;
-  else
-    smem_b = (4 * (8 * p.K + 2) + 15) / 16 * 16;  // normalisers, logits at x, uniforms
-  int st;
-  // the draw: clusters of CD CTAs, each CTA walking one thread's chunk with
-  // one entry per thread, so a draw slice holds at most NT^2 entries
-  // draw: about 32 KB of each row per CTA (staged in shared memory)
+  g->C = std::max(C_min, env_int("SPEC_VERIFY_SLICES", C_min, 1, 1 << 16));
+  g->stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
+  g->fa = argmax ? pick_row_kernel<true>(dtype, tma) : pick_row_kernel<false>(dtype, tma);
+  g->fb = argmax ? reinterpret_cast<const void *>(&finish_kernel) : pick_draw_kernel(dtype, tma);
+  const int per = (p.V + g->C - 1) / g->C;
+  g->slice = (per + VE - 1) / VE * VE;
+  g->tile = std::min(TILE_MAX_BYTES / esz, g->slice);
+  g->smem_a = g->stages * srows * g->tile * esz;
+  g->nitems = static_cast<long long>(p.njobs) * g->C;
+  if (g->nitems * NCW > INT_MAX) return fail(SPEC_ERR_ARG, "too many rows");
+  int st, per_sm = 0;
+  if ((st = occupancy(g->fa, g->smem_a, -1, &per_sm))) return st;
+  if (per_sm < 1) return fail(SPEC_ERR_UNSUPPORTED, "row kernel does not fit on an SM");
+  g->grid_a = static_cast<int>(std::min<long long>(g->nitems, static_cast<long long>(per_sm) * num_sms()));
+  g->CD = 1;
+  g->slice_d = 0;
+  g->wbuf_off = 0;
+  if (argmax) {
+    g->smem_b = 4 * (3 * p.J) + (p.kind == KIND_TREE ? 9 * p.J : 0) + 16;
+    return SPEC_OK;
+  }
+  // the draw: clusters of CD CTAs, about 32 KB of each row per CTA; the walk
+  // buffer holds one warp range of a CTA slice or of a streaming tile
+  const int base = (4 * (8 * p.K + 2) + 15) / 16 * 16;  // normalisers, logits at x, uniforms
   int CD = static_cast<int>(std::min<long long>(
       MAX_CLUSTER, std::max<long long>(1, (row_bytes + DRAW_SLICE_BYTES - 1) / DRAW_SLICE_BYTES)));
   CD = env_int("SPEC_VERIFY_DRAW_CLUSTER", CD, 1, MAX_CLUSTER);
-  while (CD < MAX_CLUSTER && (p.V + CD - 1) / CD > NT * NT - VE) ++CD;
-  const int smem_base = smem_b;
-  int slice_d = 0, draw_stage_off = smem_base;
-  bool draw_staged = false;
-  bool allow_stage = true;
   for (;;) {
     const int per_d = (p.V + CD - 1) / CD;
-    slice_d = (per_d + VE - 1) / VE * VE;
-    draw_staged = !argmax && allow_stage && env_int("SPEC_VERIFY_DRAW_STAGE", 0, 0, 1) &&
-                  2LL * slice_d * esz + smem_base <= DRAW_STAGE_LIMIT;
-    smem_b = smem_base + (draw_staged ? 2 * slice_d * esz : 0);
-    if (argmax) break;
+    const int slice_d = (per_d + VE - 1) / VE * VE;
+    if (slice_d > NT * NT) return fail(SPEC_ERR_ARG, "vocabulary too large");
+    const auto range = [&](int sl) { return ((sl + VE - 1) / VE + NWARP - 1) / NWARP * VE; };
+    const int wlen = std::max(range(slice_d), range(g->slice));
+    g->slice_d = slice_d;
+    g->wbuf_off = base;
+    g->smem_b = base + 4 * wlen;
     int nclus = 0;
-    if ((st = occupancy(fb, smem_b, CD, &nclus))) return st;
+    if ((st = occupancy(g->fb, g->smem_b, CD, &nclus))) return st;
     if (nclus > 0) break;
-    if (draw_staged) {  // first give up the staging, then shrink the cluster
-      allow_stage = false;
-      continue;
-    }
     if (CD == 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster fits on the device");
     CD = CD > 8 ? 8 : CD / 2;
   }
-  if (!argmax && slice_d > NT * NT) return fail(SPEC_ERR_ARG, "vocabulary too large");
-  const int per = (p.V + C - 1) / C;
-  const int slice = (per + VE - 1) / VE * VE;
-  // tiles of up to 16 KB per row, never wider than a slice
-  const int tile = std::min(TILE_MAX_BYTES / esz, slice);
-  const int smem_a = stages * srows * tile * esz;
-  const long long nitems = static_cast<long long>(p.njobs) * C;
-  if (nitems > INT_MAX) return fail(SPEC_ERR_ARG, "too many rows");
-  int per_sm = 0;
-  if ((st = occupancy(fa, smem_a, -1, &per_sm))) return st;
-  if (per_sm < 1) return fail(SPEC_ERR_UNSUPPORTED, "row kernel does not fit on an SM");
-  const int grid_a = static_cast<int>(std::min<long long>(nitems, static_cast<long long>(per_sm) * num_sms()));
-
-  Workspace *w = nullptr;
-  if ((st = get_ws(stream, static_cast<size_t>(nitems) * NCW, &w))) return st;
-  p.C = C;
-  p.slice = slice;
-  p.slice_d = slice_d;
-  p.draw_staged = draw_staged ? 1 : 0;
-  p.draw_stage_off = draw_stage_off;
-  p.tile = tile;
-  p.stages = stages;
-  p.partials = w->partials;
-  p.status = w->status;
-  *ws_out = w;
-
-  cudaError_t e;
-  {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid_a), 1, 1);
-    cfg.blockDim = dim3(NT_ROW, 1, 1);
-    cfg.dynamicSmemBytes = smem_a;
-    cfg.stream = stream;
-    void *args[] = {&p};
-    e = cudaLaunchKernelExC(&cfg, fa, args);
-    if (e != cudaSuccess) return cuda_fail(e, "row kernel launch");
-  }
-  {
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(NT, 1, 1);
-    cfg.dynamicSmemBytes = smem_b;
-    cfg.stream = stream;
-    if (argmax) {
-      cfg.gridDim = dim3(static_cast<unsigned>(p.B), 1, 1);
-      if ((st = occupancy(fb, smem_b, 0, &per_sm))) return st;
-    } else {
-      cfg.gridDim = dim3(static_cast<unsigned>(p.B * CD), 1, 1);
-      attr[na].id = cudaLaunchAttributeClusterDimension;
-      attr[na].val.clusterDim.x = CD;
-      attr[na].val.clusterDim.y = 1;
-      attr[na].val.clusterDim.z = 1;
-      ++na;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    void *args[] = {&p};
-    e = cudaLaunchKernelExC(&cfg, fb, args);
-    if (e != cudaSuccess) return cuda_fail(e, "decision kernel launch");
-  }
+  g->CD = CD;
   return SPEC_OK;
 }
 
-// The same two launches as run_step, on scratch the caller provides
-// (partials with room for cap_parts entries, and a status word); nothing is
-// allocated.  Used by the no-allocation entry point below.
-int run_step_on(Params &p, int dtype, bool tma, cudaStream_t stream, float4 *partials,
-                size_t cap_parts, int32_t *status) {
-  const int esz = dtype == SPEC_F32 ? 4 : 2;
-  const int VE = 16 / esz;
-  const bool argmax = p.kind != KIND_SAMPLE;
-  const int srows = argmax ? 1 : 2;
-  const long long row_bytes = static_cast<long long>(p.V) * esz;
-  // streaming items are single tiles of at most 16 KB per row
-  const int C_min = static_cast<int>(std::max<long long>(1, (row_bytes + TILE_MAX_BYTES - 1) / TILE_MAX_BYTES));
-  const int C = std::max(C_min, env_int("SPEC_VERIFY_SLICES", C_min, 1, 1 << 16));
-  const int stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
-  const void *fa = argmax ? pick_row_kernel<true>(dtype, tma) : pick_row_kernel<false>(dtype, tma);
-  const void *fb = argmax ? reinterpret_cast<const void *>(&finish_kernel) : pick_draw_kernel(dtype, tma);
-  int smem_b = 0;
-  if (argmax)
-    smem_b = 4 * (3 * p.J) + (p.kind == KIND_TREE ? 9 * p.J : 0) + 16;
-  else
-    smem_b = (4 * (8 * p.K + 2) + 15) / 16 * 16;  // normalisers, logits at x, uniforms
-  int st;
-  // the draw: clusters of CD CTAs, each CTA walking one thread's chunk with
-  // one entry per thread, so a draw slice holds at most NT^2 entries
-  // draw: about 32 KB of each row per CTA (staged in shared memory)
-  int CD = static_cast<int>(std::min<long long>(
-      MAX_CLUSTER, std::max<long long>(1, (row_bytes + DRAW_SLICE_BYTES - 1) / DRAW_SLICE_BYTES)));
-  CD = env_int("SPEC_VERIFY_DRAW_CLUSTER", CD, 1, MAX_CLUSTER);
-  while (CD < MAX_CLUSTER && (p.V + CD - 1) / CD > NT * NT - VE) ++CD;
-  const int smem_base = smem_b;
-  int slice_d = 0, draw_stage_off = smem_base;
-  bool draw_staged = false;
-  bool allow_stage = true;
-  for (;;) {
-    const int per_d = (p.V + CD - 1) / CD;
-    slice_d = (per_d + VE - 1) / VE * VE;
-    draw_staged = !argmax && allow_stage && env_int("SPEC_VERIFY_DRAW_STAGE", 0, 0, 1) &&
-                  2LL * slice_d * esz + smem_base <= DRAW_STAGE_LIMIT;
-    smem_b = smem_base + (draw_staged ? 2 * slice_d * esz : 0);
-    if (argmax) break;
-    int nclus = 0;
-    if ((st = occupancy(fb, smem_b, CD, &nclus))) return st;
-    if (nclus > 0) break;
-    if (draw_staged) {  // first give up the staging, then shrink the cluster
-      allow_stage = false;
-      continue;
-    }
-    if (CD == 1) return fail(SPEC_ERR_UNSUPPORTED, "no cluster fits on the device");
-    CD = CD > 8 ? 8 : CD / 2;
-  }
-  if (!argmax && slice_d > NT * NT) return fail(SPEC_ERR_ARG, "vocabulary too large");
-  const int per = (p.V + C - 1) / C;
-  const int slice = (per + VE - 1) / VE * VE;
-  // tiles of up to 16 KB per row, never wider than a slice
-  const int tile = std::min(TILE_MAX_BYTES / esz, slice);
-  const int smem_a = stages * srows * tile * esz;
-  const long long nitems = static_cast<long long>(p.njobs) * C;
-  if (nitems > INT_MAX) return fail(SPEC_ERR_ARG, "too many rows");
-  int per_sm = 0;
-  if ((st = occupancy(fa, smem_a, -1, &per_sm))) return st;
-  if (per_sm < 1) return fail(SPEC_ERR_UNSUPPORTED, "row kernel does not fit on an SM");
-  const int grid_a = static_cast<int>(std::min<long long>(nitems, static_cast<long long>(per_sm) * num_sms()));
-
-  if (static_cast<size_t>(nitems) * NCW > cap_parts)
-    return fail(SPEC_ERR_ARG, "call too large for the fixed scratch of spec_verify_noalloc: "
-                              "B * (K+1) * ceil(V * element size / 16384) must not exceed " +
-                                  std::to_string(cap_parts / NCW));
-  p.C = C;
-  p.slice = slice;
-  p.slice_d = slice_d;
-  p.draw_staged = draw_staged ? 1 : 0;
-  p.draw_stage_off = draw_stage_off;
-  p.tile = tile;
-  p.stages = stages;
+// The two launches of a call: A (row statistics, persistent grid) then B
+// (per-sequence decisions and outputs) as a programmatic dependent of A.
+int launch(Params &p, const Geometry &g, cudaStream_t stream, float4 *partials, int32_t *status) {
+  p.C = g.C;
+  p.slice = g.slice;
+  p.slice_d = g.slice_d;
+  p.wbuf_off = g.wbuf_off;
+  p.tile = g.tile;
+  p.stages = g.stages;
   p.partials = partials;
   p.status = status;
-
+  const bool argmax = p.kind != KIND_SAMPLE;
   cudaError_t e;
   {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid_a), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(g.grid_a), 1, 1);
     cfg.blockDim = dim3(NT_ROW, 1, 1);
-    cfg.dynamicSmemBytes = smem_a;
+    cfg.dynamicSmemBytes = g.smem_a;
     cfg.stream = stream;
     void *args[] = {&p};
-    e = cudaLaunchKernelExC(&cfg, fa, args);
+    e = cudaLaunchKernelExC(&cfg, g.fa, args);
     if (e != cudaSuccess) return cuda_fail(e, "row kernel launch");
   }
-  {
-    cudaLaunchAttribute attr[2];
-    int na = 0;
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = g.smem_b;
+  cfg.stream = stream;
+  if (argmax) {
+    int per_sm = 0, st;
+    if ((st = occupancy(g.fb, g.smem_b, 0, &per_sm))) return st;
+    cfg.gridDim = dim3(static_cast<unsigned>(p.B), 1, 1);
+  } else {
+    cfg.gridDim = dim3(static_cast<unsigned>(p.B * g.CD), 1, 1);
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = g.CD;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
     ++na;
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(NT, 1, 1);
-    cfg.dynamicSmemBytes = smem_b;
-    cfg.stream = stream;
-    if (argmax) {
-      cfg.gridDim = dim3(static_cast<unsigned>(p.B), 1, 1);
-      if ((st = occupancy(fb, smem_b, 0, &per_sm))) return st;
-    } else {
-      cfg.gridDim = dim3(static_cast<unsigned>(p.B * CD), 1, 1);
-      attr[na].id = cudaLaunchAttributeClusterDimension;
-      attr[na].val.clusterDim.x = CD;
-      attr[na].val.clusterDim.y = 1;
-      attr[na].val.clusterDim.z = 1;
-      ++na;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    void *args[] = {&p};
-    e = cudaLaunchKernelExC(&cfg, fb, args);
-    if (e != cudaSuccess) return cuda_fail(e, "decision kernel launch");
   }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  void *args[] = {&p};
+  e = cudaLaunchKernelExC(&cfg, g.fb, args);
+  if (e != cudaSuccess) return cuda_fail(e, "decision kernel launch");
   return SPEC_OK;
+}
+
+// The step on this stream's workspace.
+int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws_out) {
+  Geometry g;
+  int st = plan(p, dtype, tma, &g);
+  if (st) return st;
+  Workspace *w = nullptr;
+  if ((st = get_ws(stream, static_cast<size_t>(g.nitems) * NCW, &w))) return st;
+  *ws_out = w;
+  return launch(p, g, stream, w->partials, w->status);
+}
+
+// The step on scratch the caller provides (partials with room for cap_parts
+// entries, and a status word); nothing is allocated.  Used by the
+// no-allocation entry point below.
+int run_step_on(Params &p, int dtype, bool tma, cudaStream_t stream, float4 *partials,
+                size_t cap_parts, int32_t *status) {
+  Geometry g;
+  int st = plan(p, dtype, tma, &g);
+  if (st) return st;
+  if (static_cast<size_t>(g.nitems) * NCW > cap_parts)
+    return fail(SPEC_ERR_ARG, "call too large for the fixed scratch of spec_verify_noalloc: "
+                              "B * (K+1) * ceil(V * element size / 16384) must not exceed " +
+                                  std::to_string(cap_parts / NCW));
+  return launch(p, g, stream, partials, status);
 }
 
 int check_common(const void *zt, int B, int V, int dtype) {
