@@ -51,6 +51,11 @@ constexpr int MAX_STAGES = 8;
 constexpr int MAX_CLUSTER = 16;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s bound on any wait
 
+// Streaming items are handed out by NSHARD ticket counters, one per 128-byte
+// line: shard k hands out items k, k + ns, k + 2 ns, ...
+constexpr int NSHARD = 32;
+constexpr int TICKET_STRIDE = 32;  // ints
+
 // device status bits (per stream)
 constexpr int ST_TOKEN = 1, ST_PARENT = 2, ST_TIMEOUT = 4;
 
@@ -84,6 +89,9 @@ struct Params {
   float *out_row_sumexp;    // [B, 2K+1] or null
   Stats *stats;             // or null
   int32_t *status;          // device status bits
+  int *tickets;             // item tickets, shard k at tickets[k * TICKET_STRIDE]; zero
+                            // between calls (the decision kernel puts them back)
+  int nshard;               // ticket shards in use
 };
 
 // ------------------------------------------------------------------ elements
@@ -471,7 +479,30 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) tmo = true;
       return s;
     };
-    for (int it = blockIdx.x; it < nitems && !tmo; it += gridDim.x) {
+    // Items come from the ticket counters (this CTA's shard first, then the
+    // others once it is used up), so CTAs that finish early take more and
+    // all CTAs end together.  Lane 0 holds the next ticket, fetched one item
+    // ahead so its latency hides behind the current item.
+    const int ns = p.nshard;
+    int ishard = static_cast<int>(blockIdx.x) % ns, iempty = 0, tk = 0;
+    if (lane == 0) tk = atomicAdd(&p.tickets[ishard * TICKET_STRIDE], 1);
+    for (;;) {
+      int it = nitems;
+      if (lane == 0) {
+        for (;;) {
+          const long long cand = static_cast<long long>(tk) * ns + ishard;
+          if (cand < nitems) {
+            it = static_cast<int>(cand);
+            break;
+          }
+          if (++iempty >= ns) break;
+          ishard = ishard + 1 == ns ? 0 : ishard + 1;
+          tk = atomicAdd(&p.tickets[ishard * TICKET_STRIDE], 1);
+        }
+        if (it < nitems) tk = atomicAdd(&p.tickets[ishard * TICKET_STRIDE], 1);
+      }
+      it = __shfl_sync(0xFFFFFFFFu, it, 0);
+      if (it >= nitems || tmo) break;
       pc.set(p, it);
       for (int k = 0; k < pc.nt; ++k, ++pseq) {
         const int s = next_stage();
@@ -644,6 +675,9 @@ struct DrawShared {
   float wmass[NWARP];        // this CTA's warp-range masses
   float bf[8];
   int bi[8];
+  float scan[NWARP + 1];     // block scan scratch
+  int ired[NWARP];           // block reduction scratch
+  int pick;                  // walk result
 };
 
 constexpr int PARTS_PER_LANE = 4;
@@ -704,25 +738,27 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Inverse-CDF walk of the weights wbuf[0, len) of one range whose preceding
-// mass is P, by one warp: the smallest entry e whose running mass P + C(e)
-// passes t, else (or if `lastmode`) the last entry of positive weight.  Lane
-// l holds a contiguous chunk; the chunk test and the walk inside the chunk
-// compare the same sums (the chunk's prefix from zero, added to the same
-// base), so a chunk chosen by its total always yields an entry.  Returns the
-// entry index in every lane (0 if the range has no positive weight).
-__device__ __forceinline__ int warp_walk(const float *wbuf, int len, float P, float t, bool lastmode) {
-  const int lane = threadIdx.x & 31;
-  const int cper = (len + 31) / 32;
-  const int a0 = min(len, lane * cper), a1 = min(len, a0 + cper);
+// mass is P, by the whole CTA: the smallest entry e whose running mass
+// P + C(e) passes t, else (or if `lastmode`) the last entry of positive
+// weight.  Each thread holds a contiguous chunk; the chunk test and the walk
+// inside the chunk compare the same sums (the chunk's prefix from zero added
+// to the same base), so a chunk chosen by its total always yields an entry.
+// Returns the entry index in every thread (0 if the range has no positive
+// weight).
+__device__ __forceinline__ int block_walk(const float *wbuf, int len, float P, float t, bool lastmode,
+                                          DrawShared &sh) {
+  const int tid = threadIdx.x;
+  const int cper = (len + NT - 1) / NT;
+  const int a0 = min(len, tid * cper), a1 = min(len, a0 + cper);
   float csum = 0.f;
   for (int e = a0; e < a1; ++e) csum = __fadd_rn(csum, wbuf[e]);
-  float ctot;
-  const float E0 = __fadd_rn(P, warp_excl_scan(csum, &ctot));
+  float tot;
+  const float E0 = __fadd_rn(P, block_exclusive_scan(csum, sh.scan, &tot));
+  const int who = block_reduce_min_int(
+      (!lastmode && csum > 0.f && __fadd_rn(E0, csum) > t) ? tid : INT_MAX, sh.ired);
   int pick = -1;
-  const unsigned hit = lastmode ? 0u : __ballot_sync(0xFFFFFFFFu, csum > 0.f && __fadd_rn(E0, csum) > t);
-  if (hit) {
-    const int who = __ffs(hit) - 1;
-    if (lane == who) {
+  if (who != INT_MAX) {
+    if (tid == who) {
       float pre = 0.f;
       for (int e = a0; e < a1; ++e) {
         const float x = wbuf[e];
@@ -732,15 +768,17 @@ __device__ __forceinline__ int warp_walk(const float *wbuf, int len, float P, fl
           break;
         }
       }
+      sh.pick = pick;
     }
-    pick = __shfl_sync(0xFFFFFFFFu, pick, who);
+    __syncthreads();
+    pick = sh.pick;
+    __syncthreads();
   }
   if (pick < 0) {  // the last entry of positive weight
     int lastp = -1;
     for (int e = a0; e < a1; ++e)
       if (wbuf[e] > 0.f) lastp = e;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) lastp = max(lastp, __shfl_xor_sync(0xFFFFFFFFu, lastp, off));
+    lastp = block_reduce_max_int(lastp, sh.ired);
     pick = lastp < 0 ? 0 : lastp;
   }
   return pick;
@@ -830,9 +868,7 @@ __device__ __forceinline__ int draw_p_from_partials(const Params &p, const float
   const int len = lo_s + min(len_s, (w + 1) * nvw * VE) - r0;
   for (int e = tid; e < len; e += NT) wbuf[e] = ex2(fmaf(E::load(row, r0 + e), c, -Mc));
   __syncthreads();
-  int token = 0;
-  if (tid < 32) token = r0 + warp_walk(wbuf, len, P, t, lastmode);
-  return token;
+  return r0 + block_walk(wbuf, len, P, t, lastmode, sh);
 }
 
 template <int DT, bool TMA>
@@ -870,6 +906,7 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
     gu[i] = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
   }
   pdl_wait();  // the row partials of the first launch are complete and visible
+  if (blockIdx.x == 0 && tid < p.nshard) p.tickets[tid * TICKET_STRIDE] = 0;  // for the next call
 
   // ---- normalisers of all 2K+1 rows (target 0..K, draft 0..K-1), one job
   // (row pair, or the bonus row) per warp
@@ -934,9 +971,8 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
           p, p.partials + static_cast<size_t>(job_of(p, b, K)) * nparts, target_row<DT>(p, b, K), rmax[K], u,
           wbuf, sh);
       if (tid < 32) {
-        const int tk = __shfl_sync(0xFFFFFFFFu, token, 0);
         for (int j = lane; j <= K; j += 32)
-          out[j] = j < K ? __ldg(p.tokens + static_cast<size_t>(b) * K + j) : tk;
+          out[j] = j < K ? __ldg(p.tokens + static_cast<size_t>(b) * K + j) : token;
         if (lane == 0) {
           p.out_n[b] = K;
           if (p.stats) {
@@ -1082,9 +1118,11 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   const int rlen = min(len, (ow + 1) * nvw * VE) - r0;
   for (int e = tid; e < rlen; e += NT)
     wbuf[e] = W(E::load(rt, lo + r0 + e), W.resid ? E::load(rd, lo + r0 + e) : 0.f);
+  const float Pw = sh.bf[2], tw = sh.bf[1];
+  const bool lastw = sh.bi[7] != 0;
   __syncthreads();
+  const int token = lo + r0 + block_walk(wbuf, rlen, Pw, tw, lastw, sh);
   if (tid < 32) {
-    const int token = lo + r0 + warp_walk(wbuf, rlen, sh.bf[2], sh.bf[1], sh.bi[7] != 0);
     for (int j = lane; j <= K; j += 32)
       out[j] = j < n ? __ldg(p.tokens + static_cast<size_t>(b) * K + j) : (j == n ? token : -1);
     if (lane == 0) {
@@ -1114,6 +1152,7 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
   const int ntok = p.kind == KIND_TREE ? J : p.K;
   for (int e = tid; e < ntok; e += NT) s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * ntok + e);
   pdl_wait();
+  if (b == 0 && tid < p.nshard) p.tickets[tid * TICKET_STRIDE] = 0;  // for the next call
   const int nparts = p.C * NCW;
   for (int r = warp; r < J; r += NWARP) {
     float v = -INFINITY;

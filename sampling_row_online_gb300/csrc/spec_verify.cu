@@ -31,6 +31,12 @@ int cuda_fail(cudaError_t e, const char *what) {
   return SPEC_ERR_CUDA;
 }
 
+// Status word (one 256-byte slot) followed by the item tickets.
+constexpr size_t CONTROL_BYTES = 256 + sizeof(int) * NSHARD * TICKET_STRIDE;
+inline int *tickets_of(int32_t *status) {
+  return reinterpret_cast<int *>(reinterpret_cast<unsigned char *>(status) + 256);
+}
+
 // ------------------------------------------------------------ workspaces
 // Per (device, stream): the status word (never reallocated), the row
 // partials of the current call (float4 per job and slice, grow-only), and a
@@ -38,7 +44,7 @@ int cuda_fail(cudaError_t e, const char *what) {
 struct Workspace {
   int device = -1;
   cudaStream_t stream = nullptr;
-  int32_t *status = nullptr;
+  int32_t *status = nullptr;  // status word, then the item tickets (zeroed once)
   float4 *partials = nullptr;
   size_t cap_parts = 0;
   unsigned char *stage = nullptr;
@@ -66,9 +72,9 @@ int get_ws(cudaStream_t stream, size_t nparts, Workspace **out) {
   std::lock_guard<std::mutex> lock(g_mu);
   Workspace *w = find_ws(dev, stream, true);
   if (!w->status) {
-    e = cudaMalloc(&w->status, sizeof(int32_t));
+    e = cudaMalloc(&w->status, CONTROL_BYTES);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status)");
-    e = cudaMemsetAsync(w->status, 0, sizeof(int32_t), stream);
+    e = cudaMemsetAsync(w->status, 0, CONTROL_BYTES, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
   }
   if (w->cap_parts < nparts) {
@@ -264,6 +270,8 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
 // The two launches of a call: A (row statistics, persistent grid) then B
 // (per-sequence decisions and outputs) as a programmatic dependent of A.
 int launch(Params &p, const Geometry &g, cudaStream_t stream, float4 *partials, int32_t *status) {
+  p.tickets = tickets_of(status);
+  p.nshard = std::min(NSHARD, g.grid_a);
   p.C = g.C;
   p.slice = g.slice;
   p.slice_d = g.slice_d;
@@ -309,7 +317,11 @@ int launch(Params &p, const Geometry &g, cudaStream_t stream, float4 *partials, 
   cfg.numAttrs = na;
   void *args[] = {&p};
   e = cudaLaunchKernelExC(&cfg, g.fb, args);
-  if (e != cudaSuccess) return cuda_fail(e, "decision kernel launch");
+  if (e != cudaSuccess) {
+    // the decision kernel puts the tickets back to zero; without it, do it here
+    cudaMemsetAsync(p.tickets, 0, sizeof(int) * NSHARD * TICKET_STRIDE, stream);
+    return cuda_fail(e, "decision kernel launch");
+  }
   return SPEC_OK;
 }
 
@@ -598,9 +610,11 @@ void spec_shutdown(void) {
 namespace spec {
 namespace {
 
-// status word (256-byte slot) followed by the row partials
+// status word and item tickets (zero-initialised, and zero again after every
+// call), then the row partials
 constexpr size_t NOALLOC_MAX_PARTIALS = size_t(1) << 19;  // float4 entries: 8 MiB
-constexpr size_t NOALLOC_BYTES = 256 + NOALLOC_MAX_PARTIALS * sizeof(float4);
+constexpr size_t NOALLOC_PARTS_OFF = (CONTROL_BYTES + 255) / 256 * 256;
+constexpr size_t NOALLOC_BYTES = NOALLOC_PARTS_OFF + NOALLOC_MAX_PARTIALS * sizeof(float4);
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
 
 constexpr int NOALLOC_MAX_DEVICES = 64;
@@ -666,6 +680,6 @@ extern "C" int spec_verify_noalloc(const void *target_logits, const void *draft_
   p.out_tokens = out_tokens;
   p.out_n = out_n_accepted;
   return run_step_on(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr),
-                     reinterpret_cast<float4 *>(scratch + 256), NOALLOC_MAX_PARTIALS,
+                     reinterpret_cast<float4 *>(scratch + NOALLOC_PARTS_OFF), NOALLOC_MAX_PARTIALS,
                      reinterpret_cast<int32_t *>(scratch));
 }
