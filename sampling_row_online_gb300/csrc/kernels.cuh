@@ -51,8 +51,9 @@ constexpr int MAX_STAGES = 8;
 constexpr int MAX_CLUSTER = 16;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;  // 1 s bound on any wait
 
-// Streaming items are handed out by NSHARD ticket counters, one per 128-byte
-// line: shard k hands out items k, k + ns, k + 2 ns, ...
+// Streaming items are handed out by up to NSHARD ticket counters, one per
+// 128-byte line: shard k hands out items k, k + ns, k + 2 ns, ... to the CTAs
+// k, k + ns, ... of the row kernel.
 constexpr int NSHARD = 32;
 constexpr int TICKET_STRIDE = 32;  // ints
 
@@ -479,27 +480,23 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
       if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) tmo = true;
       return s;
     };
-    // Items come from the ticket counters (this CTA's shard first, then the
-    // others once it is used up), so CTAs that finish early take more and
-    // all CTAs end together.  Lane 0 holds the next ticket, fetched one item
-    // ahead so its latency hides behind the current item.
+    // Items come from this CTA's ticket shard (the grid is a multiple of the
+    // shard count, so every shard has as many CTAs as items / ns needs):
+    // CTAs that run ahead take more items and all CTAs end together.  Lane 0
+    // holds the next ticket, fetched one item ahead so its latency hides
+    // behind the current item.
     const int ns = p.nshard;
-    int ishard = static_cast<int>(blockIdx.x) % ns, iempty = 0, tk = 0;
-    if (lane == 0) tk = atomicAdd(&p.tickets[ishard * TICKET_STRIDE], 1);
+    const int shard = static_cast<int>(blockIdx.x) % ns;
+    int tk = 0;
+    if (lane == 0) tk = atomicAdd(&p.tickets[shard * TICKET_STRIDE], 1);
     for (;;) {
       int it = nitems;
       if (lane == 0) {
-        for (;;) {
-          const long long cand = static_cast<long long>(tk) * ns + ishard;
-          if (cand < nitems) {
-            it = static_cast<int>(cand);
-            break;
-          }
-          if (++iempty >= ns) break;
-          ishard = ishard + 1 == ns ? 0 : ishard + 1;
-          tk = atomicAdd(&p.tickets[ishard * TICKET_STRIDE], 1);
+        const long long cand = static_cast<long long>(tk) * ns + shard;
+        if (cand < nitems) {
+          it = static_cast<int>(cand);
+          tk = atomicAdd(&p.tickets[shard * TICKET_STRIDE], 1);
         }
-        if (it < nitems) tk = atomicAdd(&p.tickets[ishard * TICKET_STRIDE], 1);
       }
       it = __shfl_sync(0xFFFFFFFFu, it, 0);
       if (it >= nitems || tmo) break;

@@ -209,7 +209,7 @@ struct Geometry {
   const void *fa, *fb;   // row kernel, decision kernel
   int C, slice, tile, stages;
   int CD, slice_d, wbuf_off;
-  int smem_a, smem_b, grid_a;
+  int smem_a, smem_b, grid_a, nshard;
   long long nitems;
 };
 
@@ -235,6 +235,19 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
   if ((st = occupancy(g->fa, g->smem_a, -1, &per_sm))) return st;
   if (per_sm < 1) return fail(SPEC_ERR_UNSUPPORTED, "row kernel does not fit on an SM");
   g->grid_a = static_cast<int>(std::min<long long>(g->nitems, static_cast<long long>(per_sm) * num_sms()));
+  // ticket shards: a divisor of the grid (every shard the same number of
+  // CTAs), at most NSHARD; a large grid with no divisor in [8, NSHARD] is
+  // trimmed to a multiple of 8
+  g->nshard = 1;
+  for (int d = std::min(NSHARD, g->grid_a); d >= 1; --d)
+    if (g->grid_a % d == 0) {
+      g->nshard = d;
+      break;
+    }
+  if (g->nshard < 8 && g->grid_a >= 64) {
+    g->grid_a = g->grid_a / 8 * 8;
+    g->nshard = 8;
+  }
   g->CD = 1;
   g->slice_d = 0;
   g->wbuf_off = 0;
@@ -271,7 +284,7 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
 // (per-sequence decisions and outputs) as a programmatic dependent of A.
 int launch(Params &p, const Geometry &g, cudaStream_t stream, float4 *partials, int32_t *status) {
   p.tickets = tickets_of(status);
-  p.nshard = std::min(NSHARD, g.grid_a);
+  p.nshard = g.nshard;
   p.C = g.C;
   p.slice = g.slice;
   p.slice_d = g.slice_d;
