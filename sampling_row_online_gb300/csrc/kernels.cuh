@@ -461,6 +461,10 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
     fence_mbar_init();
   }
   __syncthreads();
+  // When launched as a dependent of the previous kernel on the stream, the
+  // CTAs above were set up while that kernel finished; nothing in global
+  // memory is touched before it has completed.
+  pdl_wait();
 
   if (warp == NCW) {
     // ------------------------------------------------------------ producer
@@ -873,7 +877,7 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
   // dynamic: row max [R], row sumexp [R], logits at x [2K], ok [K], u [K],
-  // then (16-byte aligned) the walk buffer
+  // tokens [K], then (16-byte aligned) the walk buffer
   extern __shared__ __align__(16) float dsh[];
   __shared__ DrawShared sh;
 
@@ -887,16 +891,21 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   float *rmax = dsh, *rsum = dsh + R, *gx = dsh + 2 * R;
   int *gok = reinterpret_cast<int *>(dsh + 2 * R + 2 * K);
   float *gu = dsh + 2 * R + 3 * K;
+  int *gtok = reinterpret_cast<int *>(dsh + 2 * R + 4 * K);
   float *wbuf = dsh + p.wbuf_off / 4;
 
   // every CTA of the cluster must be running before any DSMEM store: arrive
   // now, wait before the first store
   cluster_arrive_relaxed();
+  // the next kernel on the stream may start its set-up (it waits for this
+  // grid to complete before touching memory)
+  pdl_launch_dependents();
 
   // ---- inputs (not produced by the first launch): tokens, their logits, uniforms
   for (int i = tid; i < K; i += NT) {
     const int x = __ldg(p.tokens + static_cast<size_t>(b) * K + i);
     const int ok = x >= 0 && x < p.V;
+    gtok[i] = x;
     gok[i] = ok;
     gx[2 * i] = ok ? E::load(target_row<DT>(p, b, i), x) : 0.f;
     gx[2 * i + 1] = ok ? E::load(draft_row<DT>(p, b, i), x) : 0.f;
@@ -922,26 +931,19 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   }
   __syncthreads();
 
-  // ---- left-to-right acceptance: the first reject n (or K)
-  if (tid == 0) {
-    int n = K, err = 0;
-    for (int i = 0; i < K; ++i)
-      if (!gok[i]) err = 1;
-    for (int i = 0; i < K && !err; ++i) {
-      const float a = fmaf(gx[2 * i], c, -(rmax[i] * c));
-      const float d = fmaf(gx[2 * i + 1], c, -(rmax[K + 1 + i] * c));
-      const float ratio = ex2(a - d) * (rsum[K + 1 + i] / rsum[i]);  // p_i(x_i) / q_i(x_i)
-      if (!(gu[i] < ratio)) {
-        n = i;
-        break;
-      }
-    }
-    sh.bi[0] = n;
-    sh.bi[1] = err;
-  }
+  // ---- the K acceptance tests (one thread each); n = the first reject, or K
+  if (tid == 0) sh.bi[0] = K;
   __syncthreads();
+  int bad = 0;
+  for (int i = tid; i < K; i += NT) {
+    bad |= !gok[i];
+    const float a = fmaf(gx[2 * i], c, -(rmax[i] * c));
+    const float d = fmaf(gx[2 * i + 1], c, -(rmax[K + 1 + i] * c));
+    const float ratio = ex2(a - d) * (rsum[K + 1 + i] / rsum[i]);  // p_i(x_i) / q_i(x_i)
+    if (!(gu[i] < ratio)) atomicMin(&sh.bi[0], i);
+  }
+  const int err = __syncthreads_or(bad);
   const int n = sh.bi[0];
-  const int err = sh.bi[1];
   int32_t *out = p.out_tokens + static_cast<size_t>(b) * (K + 1);
   if (rank == 0) {
     for (int r = tid; r < R; r += NT) {
@@ -969,7 +971,7 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
           wbuf, sh);
       if (tid < 32) {
         for (int j = lane; j <= K; j += 32)
-          out[j] = j < K ? __ldg(p.tokens + static_cast<size_t>(b) * K + j) : token;
+          out[j] = j < K ? gtok[j] : token;
         if (lane == 0) {
           p.out_n[b] = K;
           if (p.stats) {
@@ -1121,7 +1123,7 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   const int token = lo + r0 + block_walk(wbuf, rlen, Pw, tw, lastw, sh);
   if (tid < 32) {
     for (int j = lane; j <= K; j += 32)
-      out[j] = j < n ? __ldg(p.tokens + static_cast<size_t>(b) * K + j) : (j == n ? token : -1);
+      out[j] = j < n ? gtok[j] : (j == n ? token : -1);
     if (lane == 0) {
       p.out_n[b] = n;
       if (p.stats) {
@@ -1147,6 +1149,7 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
   float *s_vmax = reinterpret_cast<float *>(ish + 2 * J);  // [J]
 
   const int ntok = p.kind == KIND_TREE ? J : p.K;
+  pdl_launch_dependents();  // the next kernel may start its set-up
   for (int e = tid; e < ntok; e += NT) s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * ntok + e);
   pdl_wait();
   if (b == 0 && tid < p.nshard) p.tickets[tid * TICKET_STRIDE] = 0;  // for the next call

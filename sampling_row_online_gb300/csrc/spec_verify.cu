@@ -257,7 +257,7 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
   }
   // the draw: clusters of CD CTAs, about 32 KB of each row per CTA; the walk
   // buffer holds one warp range of a CTA slice or of a streaming tile
-  const int base = (4 * (8 * p.K + 2) + 15) / 16 * 16;  // normalisers, logits at x, uniforms
+  const int base = (4 * (9 * p.K + 2) + 15) / 16 * 16;  // normalisers, logits at x, uniforms, tokens
   int CD = static_cast<int>(std::min<long long>(
       MAX_CLUSTER, std::max<long long>(1, (row_bytes + DRAW_SLICE_BYTES - 1) / DRAW_SLICE_BYTES)));
   CD = env_int("SPEC_VERIFY_DRAW_CLUSTER", CD, 1, MAX_CLUSTER);
@@ -296,11 +296,18 @@ int launch(Params &p, const Geometry &g, cudaStream_t stream, float4 *partials, 
   const bool argmax = p.kind != KIND_SAMPLE;
   cudaError_t e;
   {
+    // a programmatic dependent of whatever precedes it on the stream: its
+    // CTAs may be set up early, and it waits for that work before reading
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(g.grid_a), 1, 1);
     cfg.blockDim = dim3(NT_ROW, 1, 1);
     cfg.dynamicSmemBytes = g.smem_a;
     cfg.stream = stream;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
     void *args[] = {&p};
     e = cudaLaunchKernelExC(&cfg, g.fa, args);
     if (e != cudaSuccess) return cuda_fail(e, "row kernel launch");
