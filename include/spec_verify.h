@@ -30,6 +30,10 @@
  *     layouts are accepted and take a slower path with plain loads.
  *   - Each row must hold at least one finite logit.  -inf entries (masked
  *     vocabulary) are allowed; NaN and +inf are not.
+ *   - The first kernel of a call is a programmatic dependent launch of
+ *     whatever precedes it on the stream: its blocks may be set up while
+ *     that work drains, and they wait for it to complete before reading
+ *     anything, so stream order is unchanged.
  *   - The library keeps one grow-only device workspace per (device, stream)
  *     pair (a few ints per sequence).  Growing it calls cudaMalloc, so the
  *     first call of a new size on a stream should not be inside a CUDA graph
@@ -155,7 +159,8 @@ int spec_verify_host(const void *target_logits, const void *draft_logits,
  *
  * Same arguments, outputs and results as spec_verify (temperature > 0 and
  * T == 0 alike), but the scratch space comes from a fixed array compiled into
- * the library (8 MiB of row partials plus a status word), which every GPU
+ * the library (a status word, the streaming kernel's item counters, which
+ * every call leaves at zero, and 8 MiB of row partials), which every GPU
  * that loads the library keeps until the process exits.  Nothing is
  * allocated by the call.
  *
