@@ -1,26 +1,29 @@
 // Verification kernels for sm_103a.
 //
-// Two launches per call, back to back on the caller's stream:
+// Two launches per call on the caller's stream; the second is a programmatic
+// dependent of the first, the first of whatever precedes it.
 //
 //  A. row_kernel — a streaming reduction over every logit row the step needs.
 //     Work item = (job, vocabulary slice): a job is a target/draft row pair
 //     (stochastic chain, positions i < K), the bonus target row K, or one
-//     target row (greedy chain, tree).  Persistent CTAs take items round-robin
-//     and stream their tiles from HBM into shared memory with TMA bulk copies
-//     (cp.async.bulk + one mbarrier per stage) through a ring that runs across
-//     item boundaries.  Each item ends in one 16-byte partial: (max, sum of
-//     2^((z - max) log2e / T)) for both rows, or (max, first index of max).
+//     target row (greedy chain, tree).  Persistent CTAs take items from
+//     sharded ticket counters and stream their tiles from HBM into shared
+//     memory with TMA bulk copies (cp.async.bulk + one mbarrier per stage)
+//     through a ring that runs across item boundaries.  Each consumer warp
+//     ends an item with one 16-byte partial: (max, sum of 2^((z - max) log2e
+//     / T)) for both rows, or (max, first index of max); for the stochastic
+//     chain the item's last warp also writes the item's combined partial.
 //     No CTA ever waits for another.
 //
 //  B. draw_kernel (stochastic chain) — one thread-block cluster per sequence.
-//     Every CTA combines the partials of all 2K+1 rows (fixed order, so every
-//     CTA holds the same bits), takes the K acceptance decisions left to
-//     right, and the cluster draws the single token the sequence needs: the
-//     residual at the first reject, or the bonus from row K.  The draw
+//     Every CTA combines the per-item partials of all 2K+1 rows (fixed
+//     order, so every CTA holds the same bits), takes the K acceptance tests,
+//     and the cluster draws the single token the sequence needs: the residual
+//     at the first reject, or the bonus from row K.  The residual draw
 //     re-reads one row pair (L2-resident when possible) split over the
-//     cluster: per-thread chunk masses, a block scan, slice masses pushed to
-//     every CTA through distributed shared memory, the owner slice, and a
-//     block-wide walk of the owner chunk.  The owner CTA writes the outputs.
+//     cluster: warp-range masses, CTA masses pushed to every CTA through
+//     distributed shared memory, the owner CTA, its owner warp range, and a
+//     block-wide walk of that range.  The owner CTA writes the outputs.
 //
 //     finish_kernel (greedy chain, tree) — one CTA per sequence: argmax per
 //     row from the partials, then the left-to-right match or the tree walk.
@@ -83,7 +86,8 @@ struct Params {
   int stages;               // shared-memory stages of the tile ring
   int njobs;                // jobs in total; items = njobs * C
   int max_depth;            // tree output width - 1
-  float4 *partials;         // [njobs * C]
+  float4 *partials;         // [njobs * C * NCW] per consumer warp
+  float4 *item_parts;       // [njobs * C] per item (stochastic chain)
   int32_t *out_tokens;      // chain [B, K+1]; tree [B, max_depth+1]
   int32_t *out_n;           // chain n_accepted [B]; tree length [B]
   float *out_row_max;       // [B, 2K+1] or null
@@ -267,21 +271,17 @@ __device__ __forceinline__ float block_exclusive_scan(float v, float *sh, float 
 }
 
 // ------------------------------------------------------------ job layout
-// Job q -> (sequence b, row i).  Stochastic chain: the B bonus rows first,
-// then the row pairs from position K-1 down to 0, so the rows a residual draw
-// most often needs (the early positions) are the last ones streamed and are
-// still in L2 when the draw runs.  Argmax kinds: rows position-major.
+// Job q -> (sequence b, row i).  Stochastic chain: the row pairs from
+// position K-1 down to 0, so the rows a residual draw most often needs (the
+// early positions) are streamed late and are still in L2 when the draw runs,
+// then the B bonus rows (single-row items, half the size, end the stream:
+// the last items finish close together; a bonus draw reads no row again).
+// Argmax kinds: rows position-major.
 __device__ __forceinline__ void decode_job(const Params &p, int q, int &b, int &i) {
   if (p.kind == KIND_SAMPLE) {
-    if (q < p.B) {
-      i = p.K;
-      b = q;
-    } else {
-      const int r = q - p.B;
-      const int k = r / p.B;
-      i = p.K - 1 - k;
-      b = r - k * p.B;
-    }
+    const int k = q / p.B;
+    b = q - k * p.B;
+    i = k < p.K ? p.K - 1 - k : p.K;
   } else {
     i = q / p.B;
     b = q - i * p.B;
@@ -289,7 +289,7 @@ __device__ __forceinline__ void decode_job(const Params &p, int q, int &b, int &
 }
 
 __device__ __forceinline__ int job_of(const Params &p, int b, int i) {
-  if (p.kind == KIND_SAMPLE) return i == p.K ? b : p.B + (p.K - 1 - i) * p.B + b;
+  if (p.kind == KIND_SAMPLE) return (i == p.K ? p.K : p.K - 1 - i) * p.B + b;
   return i * p.B + b;
 }
 
@@ -444,6 +444,10 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ uint64_t full[MAX_STAGES], empty[MAX_STAGES];
   __shared__ __align__(16) StageMeta meta[MAX_STAGES];
+  // per-item combine of the consumer warps' partials (stochastic chain):
+  // 2 * MAX_STAGES slot sets, so a set is never rewritten before it is read
+  __shared__ __align__(16) float4 cparts[ARGMAX ? 1 : 2 * MAX_STAGES][NCW];
+  __shared__ int ccount[ARGMAX ? 1 : 2 * MAX_STAGES];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.stages;
@@ -458,6 +462,8 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], NCW);
     }
+    if (!ARGMAX)
+      for (int k = 0; k < 2 * S; ++k) ccount[k] = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -543,11 +549,12 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
           if (lane == 0) mbar_arrive(&full[s]);
         }
       }
-      if (pc.nt == 0 && lane == 0) {  // an empty slice still gets its (neutral) partial
+      if (pc.nt == 0 && lane == 0) {  // an empty slice still gets its (neutral) partials
         for (int w = 0; w < NCW; ++w)
           p.partials[static_cast<size_t>(it) * NCW + w] =
               ARGMAX ? make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f)
                      : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+        if (!ARGMAX) p.item_parts[it] = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
       }
     }
     // end of stream
@@ -632,6 +639,28 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
       od.init();
     }
     if (lane == 0) p.partials[static_cast<size_t>(m.item) * NCW + warp] = out;
+    if (!ARGMAX) {
+      // the item's 8 warp partials, combined by the warp that finishes last
+      // (slots in a fixed order, so the result does not depend on which)
+      const int cs = seq % (2 * S);
+      int last = 0;
+      if (lane == 0) {
+        cparts[cs][warp] = out;
+        __threadfence_block();
+        last = atomicAdd(&ccount[cs], 1) == NCW - 1;
+      }
+      if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+        __threadfence_block();
+        const float4 v = lane < NCW ? cparts[cs][lane] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+        float mt = v.x, st = v.y, md = v.z, sd = v.w;
+        warp_ms(mt, st, c);
+        warp_ms(md, sd, c);
+        if (lane == 0) {
+          ccount[cs] = 0;
+          p.item_parts[m.item] = make_float4(mt, st, md, sd);
+        }
+      }
+    }
   }
   pdl_launch_dependents();
   if (tmo) atomicOr(p.status, ST_TIMEOUT);
@@ -645,7 +674,7 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
 //
 //  1. Before the dependent-launch wait (inputs only): the draft tokens, their
 //     target and draft logits, the acceptance uniforms.
-//  2. Every CTA combines the partials of all 2K+1 rows itself (the same
+//  2. Every CTA combines the per-item partials of all 2K+1 rows itself (the same
 //     fixed order everywhere, so every CTA holds the same bits) and takes the
 //     K decisions left to right: no exchange is needed for them.
 //  3. n == K: rank 0 draws the bonus token from row K's partials.
@@ -715,6 +744,52 @@ __device__ __forceinline__ void warp_norms(const float4 *parts, int nparts, floa
       ms_combine(md, sd, m2, s2, c);
     }
   }
+}
+
+// (max, sumexp) of the target row (and of the draft row if `pair`) of one job
+// from its C per-item partials, by one warp.  Up to 32 * PARTS_PER_LANE
+// partials: the maximum first (lane maximum, butterfly), one rescale per
+// partial, then a sum butterfly; more: the partials folded in order.  Either
+// way every lane (and every CTA) ends with the same bits.
+__device__ __forceinline__ void warp_job_norms(const float4 *ip, int C, float c, bool pair, float &mt,
+                                               float &st, float &md, float &sd) {
+  if (C > 32 * PARTS_PER_LANE) {
+    warp_norms(ip, C, c, pair, mt, st, md, sd);
+    return;
+  }
+  const int lane = threadIdx.x & 31;
+  float4 v[PARTS_PER_LANE];
+#pragma unroll
+  for (int k = 0; k < PARTS_PER_LANE; ++k) {
+    const int j = lane + 32 * k;
+    v[k] = j < C ? __ldcg(ip + j) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+  }
+  float Mt = -INFINITY, Md = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < PARTS_PER_LANE; ++k) {
+    Mt = fmaxf(Mt, v[k].x);
+    Md = fmaxf(Md, v[k].z);
+  }
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    Mt = fmaxf(Mt, __shfl_xor_sync(0xFFFFFFFFu, Mt, off));
+    Md = fmaxf(Md, __shfl_xor_sync(0xFFFFFFFFu, Md, off));
+  }
+  float a = 0.f, d = 0.f;
+#pragma unroll
+  for (int k = 0; k < PARTS_PER_LANE; ++k) {
+    if (Mt != -INFINITY && v[k].y != 0.f) a = __fadd_rn(a, __fmul_rn(v[k].y, ex2((v[k].x - Mt) * c)));
+    if (pair && Md != -INFINITY && v[k].w != 0.f) d = __fadd_rn(d, __fmul_rn(v[k].w, ex2((v[k].z - Md) * c)));
+  }
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    a = __fadd_rn(a, __shfl_xor_sync(0xFFFFFFFFu, a, off));
+    d = __fadd_rn(d, __shfl_xor_sync(0xFFFFFFFFu, d, off));
+  }
+  mt = Mt;
+  st = a;
+  md = pair ? Md : -INFINITY;
+  sd = pair ? d : 0.f;
 }
 
 // Exclusive prefix sum over the lanes; *total = the warp's sum (every lane).
@@ -919,7 +994,7 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   const int nparts = p.C * NCW;
   for (int i = warp; i <= K; i += NWARP) {
     float mt, st, md, sd;
-    warp_norms(p.partials + static_cast<size_t>(job_of(p, b, i)) * nparts, nparts, c, i < K, mt, st, md, sd);
+    warp_job_norms(p.item_parts + static_cast<size_t>(job_of(p, b, i)) * p.C, p.C, c, i < K, mt, st, md, sd);
     if (lane == 0) {
       rmax[i] = mt;
       rsum[i] = st;
