@@ -160,7 +160,7 @@ int spec_verify_host(const void *target_logits, const void *draft_logits,
  * Same arguments, outputs and results as spec_verify (temperature > 0 and
  * T == 0 alike), but the scratch space comes from a fixed array compiled into
  * the library (a status word, the streaming kernel's item counters, which
- * every call leaves at zero, and 9 MiB of row partials), which every GPU
+ * every call leaves at zero, and 8 MiB of row partials), which every GPU
  * that loads the library keeps until the process exits.  Nothing is
  * allocated by the call.
  *

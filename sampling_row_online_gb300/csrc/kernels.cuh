@@ -11,12 +11,11 @@
 //     memory with TMA bulk copies (cp.async.bulk + one mbarrier per stage)
 //     through a ring that runs across item boundaries.  Each consumer warp
 //     ends an item with one 16-byte partial: (max, sum of 2^((z - max) log2e
-//     / T)) for both rows, or (max, first index of max); for the stochastic
-//     chain the item's last warp also writes the item's combined partial.
-//     No CTA ever waits for another.
+//     / T)) for both rows, or (max, first index of max).  No CTA ever waits
+//     for another.
 //
 //  B. draw_kernel (stochastic chain) — one thread-block cluster per sequence.
-//     Every CTA combines the per-item partials of all 2K+1 rows (fixed
+//     Every CTA combines the partials of all 2K+1 rows (fixed
 //     order, so every CTA holds the same bits), takes the K acceptance tests,
 //     and the cluster draws the single token the sequence needs: the residual
 //     at the first reject, or the bonus from row K.  The residual draw
@@ -86,8 +85,7 @@ struct Params {
   int stages;               // shared-memory stages of the tile ring
   int njobs;                // jobs in total; items = njobs * C
   int max_depth;            // tree output width - 1
-  float4 *partials;         // [njobs * C * NCW] per consumer warp
-  float4 *item_parts;       // [njobs * C] per item (stochastic chain)
+  float4 *partials;         // [njobs * C * NCW], one per consumer warp
   int32_t *out_tokens;      // chain [B, K+1]; tree [B, max_depth+1]
   int32_t *out_n;           // chain n_accepted [B]; tree length [B]
   float *out_row_max;       // [B, 2K+1] or null
@@ -444,10 +442,6 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
   extern __shared__ __align__(128) unsigned char dyn[];
   __shared__ uint64_t full[MAX_STAGES], empty[MAX_STAGES];
   __shared__ __align__(16) StageMeta meta[MAX_STAGES];
-  // per-item combine of the consumer warps' partials (stochastic chain):
-  // 2 * MAX_STAGES slot sets, so a set is never rewritten before it is read
-  __shared__ __align__(16) float4 cparts[ARGMAX ? 1 : 2 * MAX_STAGES][NCW];
-  __shared__ int ccount[ARGMAX ? 1 : 2 * MAX_STAGES];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.stages;
@@ -462,8 +456,6 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], NCW);
     }
-    if (!ARGMAX)
-      for (int k = 0; k < 2 * S; ++k) ccount[k] = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -554,7 +546,6 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
           p.partials[static_cast<size_t>(it) * NCW + w] =
               ARGMAX ? make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f)
                      : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-        if (!ARGMAX) p.item_parts[it] = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
       }
     }
     // end of stream
@@ -639,28 +630,6 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
       od.init();
     }
     if (lane == 0) p.partials[static_cast<size_t>(m.item) * NCW + warp] = out;
-    if (!ARGMAX) {
-      // the item's 8 warp partials, combined by the warp that finishes last
-      // (slots in a fixed order, so the result does not depend on which)
-      const int cs = seq % (2 * S);
-      int last = 0;
-      if (lane == 0) {
-        cparts[cs][warp] = out;
-        __threadfence_block();
-        last = atomicAdd(&ccount[cs], 1) == NCW - 1;
-      }
-      if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
-        __threadfence_block();
-        const float4 v = lane < NCW ? cparts[cs][lane] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-        float mt = v.x, st = v.y, md = v.z, sd = v.w;
-        warp_ms(mt, st, c);
-        warp_ms(md, sd, c);
-        if (lane == 0) {
-          ccount[cs] = 0;
-          p.item_parts[m.item] = make_float4(mt, st, md, sd);
-        }
-      }
-    }
   }
   pdl_launch_dependents();
   if (tmo) atomicOr(p.status, ST_TIMEOUT);
@@ -674,7 +643,7 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
 //
 //  1. Before the dependent-launch wait (inputs only): the draft tokens, their
 //     target and draft logits, the acceptance uniforms.
-//  2. Every CTA combines the per-item partials of all 2K+1 rows itself (the same
+//  2. Every CTA combines the partials of all 2K+1 rows itself (the same
 //     fixed order everywhere, so every CTA holds the same bits) and takes the
 //     K decisions left to right: no exchange is needed for them.
 //  3. n == K: rank 0 draws the bonus token from row K's partials.
@@ -747,26 +716,27 @@ __device__ __forceinline__ void warp_norms(const float4 *parts, int nparts, floa
 }
 
 // (max, sumexp) of the target row (and of the draft row if `pair`) of one job
-// from its C per-item partials, by one warp.  Up to 32 * PARTS_PER_LANE
-// partials: the maximum first (lane maximum, butterfly), one rescale per
-// partial, then a sum butterfly; more: the partials folded in order.  Either
-// way every lane (and every CTA) ends with the same bits.
-__device__ __forceinline__ void warp_job_norms(const float4 *ip, int C, float c, bool pair, float &mt,
+// from its n partials, by one warp.  Up to 32 * JOB_PARTS_PER_LANE partials
+// (all loads in flight at once): the maximum first (lane maximum, butterfly),
+// one rescale per partial, then a sum butterfly; more: the partials folded
+// in order.  Either way every lane (and every CTA) ends with the same bits.
+constexpr int JOB_PARTS_PER_LANE = 8;
+__device__ __forceinline__ void warp_job_norms(const float4 *ip, int n, float c, bool pair, float &mt,
                                                float &st, float &md, float &sd) {
-  if (C > 32 * PARTS_PER_LANE) {
-    warp_norms(ip, C, c, pair, mt, st, md, sd);
+  if (n > 32 * JOB_PARTS_PER_LANE) {
+    warp_norms(ip, n, c, pair, mt, st, md, sd);
     return;
   }
   const int lane = threadIdx.x & 31;
-  float4 v[PARTS_PER_LANE];
+  float4 v[JOB_PARTS_PER_LANE];
 #pragma unroll
-  for (int k = 0; k < PARTS_PER_LANE; ++k) {
+  for (int k = 0; k < JOB_PARTS_PER_LANE; ++k) {
     const int j = lane + 32 * k;
-    v[k] = j < C ? __ldcg(ip + j) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+    v[k] = j < n ? __ldcg(ip + j) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
   }
   float Mt = -INFINITY, Md = -INFINITY;
 #pragma unroll
-  for (int k = 0; k < PARTS_PER_LANE; ++k) {
+  for (int k = 0; k < JOB_PARTS_PER_LANE; ++k) {
     Mt = fmaxf(Mt, v[k].x);
     Md = fmaxf(Md, v[k].z);
   }
@@ -777,7 +747,7 @@ __device__ __forceinline__ void warp_job_norms(const float4 *ip, int C, float c,
   }
   float a = 0.f, d = 0.f;
 #pragma unroll
-  for (int k = 0; k < PARTS_PER_LANE; ++k) {
+  for (int k = 0; k < JOB_PARTS_PER_LANE; ++k) {
     if (Mt != -INFINITY && v[k].y != 0.f) a = __fadd_rn(a, __fmul_rn(v[k].y, ex2((v[k].x - Mt) * c)));
     if (pair && Md != -INFINITY && v[k].w != 0.f) d = __fadd_rn(d, __fmul_rn(v[k].w, ex2((v[k].z - Md) * c)));
   }
@@ -994,7 +964,7 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   const int nparts = p.C * NCW;
   for (int i = warp; i <= K; i += NWARP) {
     float mt, st, md, sd;
-    warp_job_norms(p.item_parts + static_cast<size_t>(job_of(p, b, i)) * p.C, p.C, c, i < K, mt, st, md, sd);
+    warp_job_norms(p.partials + static_cast<size_t>(job_of(p, b, i)) * nparts, nparts, c, i < K, mt, st, md, sd);
     if (lane == 0) {
       rmax[i] = mt;
       rsum[i] = st;

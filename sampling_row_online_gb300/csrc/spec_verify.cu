@@ -291,8 +291,7 @@ int launch(Params &p, const Geometry &g, cudaStream_t stream, float4 *partials, 
   p.wbuf_off = g.wbuf_off;
   p.tile = g.tile;
   p.stages = g.stages;
-  p.partials = partials;                           // nitems * NCW per-warp partials,
-  p.item_parts = partials + g.nitems * NCW;         // then nitems per-item partials
+  p.partials = partials;
   p.status = status;
   const bool argmax = p.kind != KIND_SAMPLE;
   cudaError_t e;
@@ -352,7 +351,7 @@ int run_step(Params &p, int dtype, bool tma, cudaStream_t stream, Workspace **ws
   int st = plan(p, dtype, tma, &g);
   if (st) return st;
   Workspace *w = nullptr;
-  if ((st = get_ws(stream, static_cast<size_t>(g.nitems) * (NCW + 1), &w))) return st;
+  if ((st = get_ws(stream, static_cast<size_t>(g.nitems) * NCW, &w))) return st;
   *ws_out = w;
   return launch(p, g, stream, w->partials, w->status);
 }
@@ -365,10 +364,10 @@ int run_step_on(Params &p, int dtype, bool tma, cudaStream_t stream, float4 *par
   Geometry g;
   int st = plan(p, dtype, tma, &g);
   if (st) return st;
-  if (static_cast<size_t>(g.nitems) * (NCW + 1) > cap_parts)
+  if (static_cast<size_t>(g.nitems) * NCW > cap_parts)
     return fail(SPEC_ERR_ARG, "call too large for the fixed scratch of spec_verify_noalloc: "
                               "B * (K+1) * ceil(V * element size / 16384) must not exceed " +
-                                  std::to_string(cap_parts / (NCW + 1)));
+                                  std::to_string(cap_parts / NCW));
   return launch(p, g, stream, partials, status);
 }
 
@@ -633,7 +632,7 @@ namespace {
 
 // status word and item tickets (zero-initialised, and zero again after every
 // call), then the row partials
-constexpr size_t NOALLOC_MAX_PARTIALS = (size_t(1) << 16) * (NCW + 1);  // float4 entries: 9 MiB
+constexpr size_t NOALLOC_MAX_PARTIALS = (size_t(1) << 16) * NCW;  // float4 entries: 8 MiB
 constexpr size_t NOALLOC_PARTS_OFF = (CONTROL_BYTES + 255) / 256 * 256;
 constexpr size_t NOALLOC_BYTES = NOALLOC_PARTS_OFF + NOALLOC_MAX_PARTIALS * sizeof(float4);
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
