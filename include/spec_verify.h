@@ -237,6 +237,20 @@ int spec_tree_mask(const int32_t *parent, int B, int N, uint32_t *out_mask,
  */
 int spec_get_status(void *stream);
 
+/*
+ * spec_arm_rows_event — measurement hook.  The next verification call that
+ * launches (spec_verify, spec_verify_ex, spec_verify_noalloc or
+ * spec_verify_tree_greedy) made by the calling host thread records `event`
+ * (a cudaEvent_t created by the caller, passed as void*) on its stream right
+ * after launching its streaming kernel (the row statistics) and before its
+ * decision kernel; the hook is then disarmed.  An event the caller records
+ * just before that call and this one bracket the streaming kernel alone.
+ * The decision kernel of that call then starts only after the event, so
+ * calls timed this way are for measurement, not for the fastest throughput.
+ * Always returns SPEC_OK.
+ */
+int spec_arm_rows_event(void *event);
+
 /* Static, human-readable name of a status code. */
 const char *spec_error_string(int status);
 

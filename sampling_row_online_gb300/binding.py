@@ -50,6 +50,7 @@ def library():
     lib.spec_verify.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, u64, vp, vp, vp]
     lib.spec_verify_ex.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, u64, vp, vp, vp, vp, vp, vp]
     lib.spec_verify_host.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, u64, vp, vp, vp]
+    lib.spec_arm_rows_event.argtypes = [vp]
     lib.spec_verify_tree_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.spec_tree_max_depth.argtypes = [vp, i32]
     lib.spec_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp]

@@ -282,7 +282,13 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
 
 // The two launches of a call: A (row statistics, persistent grid) then B
 // (per-sequence decisions and outputs) as a programmatic dependent of A.
+// One-shot measurement hook (spec_arm_rows_event): recorded on the stream
+// between the two launches of the next call on this host thread.
+thread_local cudaEvent_t g_rows_event = nullptr;
+
 int launch(Params &p, const Geometry &g, cudaStream_t stream, float4 *partials, int32_t *status) {
+  const cudaEvent_t ev_rows = g_rows_event;
+  g_rows_event = nullptr;
   p.tickets = tickets_of(status);
   p.nshard = g.nshard;
   p.C = g.C;
@@ -312,6 +318,7 @@ int launch(Params &p, const Geometry &g, cudaStream_t stream, float4 *partials, 
     e = cudaLaunchKernelExC(&cfg, g.fa, args);
     if (e != cudaSuccess) return cuda_fail(e, "row kernel launch");
   }
+  if (ev_rows && (e = cudaEventRecord(ev_rows, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   cudaLaunchAttribute attr[2];
   int na = 0;
   attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -504,6 +511,11 @@ int spec_tree_mask(const int32_t *parent, int B, int N, uint32_t *out_mask, int3
   tree_mask_kernel<<<B, NT, 0, stream>>>(parent, N, W, out_mask, out_depth, w->status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "tree_mask_kernel launch");
+  return SPEC_OK;
+}
+
+int spec_arm_rows_event(void *event) {
+  g_rows_event = static_cast<cudaEvent_t>(event);
   return SPEC_OK;
 }
 
