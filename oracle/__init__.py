@@ -56,6 +56,10 @@ def _load():
         lib.oracle_verify_tree_greedy.argtypes = [c_p, c_p, c_p, i32, i32, i32, i32, i32,
                                                   c_p, c_p, i32]
         lib.oracle_verify_tree_greedy.restype = i32
+        lib.oracle_verify_tree_sample.argtypes = [c_p, c_p, c_p, c_p, i32, i32, i32, i32, f64,
+                                                  u64, i32, c_p, c_p, c_p, c_p, c_p, c_p, c_p,
+                                                  i32]
+        lib.oracle_verify_tree_sample.restype = i32
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         _lib = lib
@@ -244,3 +248,38 @@ def verify_tree_greedy(zt, parent, node_tokens, *, max_depth=None, nthreads=1):
     if st in (ERR_ARG, ERR_PARENT):
         raise ValueError("oracle_verify_tree_greedy: invalid arguments")
     return path, length, st
+
+
+def verify_tree_sample(zt, zd, parent, node_tokens, T: float, seed: int, *, max_depth=None,
+                       b_ids=None, u_acc=None, u_samp=None, nthreads=1):
+    """Stochastic tree verification (candidates tried sibling by sibling with
+    the residual updated after each reject).
+
+    zt, zd: [nb, N, V]; parent: [N]; node_tokens: [nb, N]; u_acc / u_samp: optional
+    [nb, N] uniforms (test of child c / draw at node u).  Returns a dict with
+    path [nb, D+1], length [nb], near [nb], fallback [nb], status.
+    """
+    zt_a, dt = _logits(zt)
+    zd_a, dt2 = _logits(zd)
+    nb, N, V = zt_a.shape
+    assert dt2 == dt and zd_a.shape == (nb, N, V)
+    p = _i32(parent).reshape(N)
+    tok = _i32(node_tokens).reshape(nb, N)
+    D = tree_max_depth(p) if max_depth is None else int(max_depth)
+    if D < 0:
+        raise ValueError("invalid parent array")
+    bi = None if b_ids is None else _i32(b_ids).reshape(nb)
+    ua = None if u_acc is None else np.ascontiguousarray(u_acc, dtype=np.float64).reshape(nb, N)
+    us = None if u_samp is None else np.ascontiguousarray(u_samp, dtype=np.float64).reshape(nb, N)
+    path = np.zeros((nb, D + 1), dtype=np.int32)
+    length = np.zeros(nb, dtype=np.int32)
+    near = np.zeros(nb, dtype=np.int32)
+    fb = np.zeros(nb, dtype=np.int32)
+    st = _load().oracle_verify_tree_sample(_ptr(zt_a), _ptr(zd_a), _ptr(p), _ptr(tok), nb, N, V,
+                                           dt, float(T), int(seed) & ((1 << 64) - 1), D,
+                                           _ptr(bi), _ptr(ua), _ptr(us), _ptr(path),
+                                           _ptr(length), _ptr(near), _ptr(fb), int(nthreads))
+    if st in (ERR_ARG, ERR_PARENT):
+        raise ValueError("oracle_verify_tree_sample: invalid arguments")
+    return dict(path=path, length=length, near=near.astype(bool), fallback=fb.astype(bool),
+                status=st)

@@ -489,6 +489,164 @@ int oracle_verify_tree_greedy(const void *zt, const int32_t *parent,
   return status;
 }
 
+/* ------------------------------------------------------------------ */
+/* Stochastic tree verification.  The pages give the chain rule          */
+/* ([Oscine] §"验收标准的精确数学" and §"拒绝之后怎么办？——残差分布") and    */
+/* warn that verifying a tree does not by itself keep the output          */
+/* lossless ([Infra53] §9); the rule for several children of one node is  */
+/* not given.  Reading taken, the lossless extension of the chain rule:   */
+/* the children of a node are candidates drawn independently from the     */
+/* draft's distribution q at that node and are tried in index order.      */
+/* With r the current target distribution at the node (r = p at first), */
+/* candidate x is accepted with probability min(1, r(x)/q(x)); on a       */
+/* reject r becomes norm(max(0, r - q)) and the next candidate is tried.  */
+/* An accepted candidate becomes the current node; a node whose           */
+/* candidates are all rejected emits a draw from r; an accepted node with */
+/* no children emits a bonus draw from its own p.                         */
+/* After k rejects at a node r = max(0, p - a_k q) / W_k with a_0 = 0,     */
+/* W_0 = 1, a_{k+1} = a_k + W_k and W_{k+1} = sum_v max(0, p - a_{k+1} q) */
+/* (max(0, r - q) = max(0, p - (a_k + W_k) q) / W_k).                     */
+/* Uniforms: the test of child c uses (b, c - 1, slot 0), the draw at     */
+/* node u uses (b, u, slot 1); on a chain-shaped tree (parent[c] = c - 1) */
+/* this is exactly the chain verification of the same rows.               */
+/* A residual that vanishes after a reject (W == 0, through rounding      */
+/* only) ends the node: the draw falls back to p there (*fallback).       */
+/*   zt, zd: [nb, N, V] (row u: target / draft distribution at node u;    */
+/*   leaves' draft rows are not read), node_tokens: [nb, N] (entry 0      */
+/*   ignored), u_acc / u_samp: [nb, N] optional injected uniforms (test   */
+/*   of child c, draw at node u), out_path: [nb, max_depth + 1] (accepted */
+/*   tokens, then the emitted token, -1 padding), out_len: [nb] (accepted */
+/*   + 1, or -1 on a token outside [0, V)).                               */
+/* ------------------------------------------------------------------ */
+static int verify_tree_one(const void *zt_seq, const void *zd_seq,
+                           const int32_t *parent, const int32_t *tok, int N,
+                           int V, int dtype, double T, uint64_t seed,
+                           uint32_t b, const double *u_acc,
+                           const double *u_samp, int32_t *path, int W,
+                           int *near_out, int *fallback_out) {
+  int near = 0, fallback = 0, len = 0;
+  for (int k = 0; k < W; ++k) path[k] = -1;
+  for (int c = 1; c < N; ++c)
+    if (tok[c] < 0 || tok[c] >= V) {
+      *near_out = 0;
+      *fallback_out = 0;
+      return -1;
+    }
+  double *w = (double *)malloc(sizeof(double) * (size_t)V);
+  int u = 0, emitted = -1;
+  for (;;) {
+    const void *zt = row_ptr(zt_seq, dtype, u, V);
+    double mt, St;
+    oracle_row_stats(zt, dtype, V, T, &mt, &St);
+    int first = -1;
+    for (int c = u + 1; c < N; ++c)
+      if (parent[c] == u) {
+        first = c;
+        break;
+      }
+    double us = u_samp ? u_samp[u] : oracle_uniform(seed, b, (uint32_t)u, 1u);
+    if (first < 0) {  /* a leaf: the bonus token from p */
+      int ns = 0;
+      emitted = oracle_target_sample(zt, dtype, V, T, us, &ns);
+      near |= ns;
+      break;
+    }
+    const void *zd = row_ptr(zd_seq, dtype, u, V);
+    double md, Sd;
+    oracle_row_stats(zd, dtype, V, T, &md, &Sd);
+    double a = 0.0, Wk = 1.0;
+    int next = -1, vanished = 0;
+    for (int c = first; c < N; ++c) {
+      if (parent[c] != u) continue;
+      int x = tok[c];
+      double px = prob_at(zt, dtype, x, T, mt, St);
+      double qx = prob_at(zd, dtype, x, T, md, Sd);
+      double rx = px - a * qx;
+      if (rx < 0.0) rx = 0.0;
+      rx /= Wk;
+      double ratio;
+      if (qx > 0.0)
+        ratio = rx / qx;
+      else
+        ratio = rx > 0.0 ? INFINITY : 0.0;
+      double uc = u_acc ? u_acc[c] : oracle_uniform(seed, b, (uint32_t)(c - 1), 0u);
+      double scale = ratio > 0x1p-24 ? ratio : 0x1p-24;
+      if (isfinite(ratio) && fabs(uc - ratio) <= 1e-5 * scale) near = 1;
+      if (uc < ratio) {
+        next = c;
+        break;
+      }
+      /* reject: r <- norm(max(0, r - q)) */
+      a += Wk;
+      double Z = 0.0;
+      for (int v = 0; v < V; ++v) {
+        double d = prob_at(zt, dtype, v, T, mt, St) - a * prob_at(zd, dtype, v, T, md, Sd);
+        w[v] = d > 0.0 ? d : 0.0;
+        Z += w[v];
+      }
+      Wk = Z;
+      if (!(Wk > 0.0)) {
+        vanished = 1;
+        break;
+      }
+    }
+    if (next >= 0) {
+      path[len++] = tok[next];
+      u = next;
+      continue;
+    }
+    int ns = 0;
+    if (vanished || a == 0.0) {  /* a == 0 cannot happen: u has a child */
+      emitted = oracle_target_sample(zt, dtype, V, T, us, &ns);
+      fallback |= vanished;
+    } else {
+      emitted = inverse_cdf(w, V, Wk, us, &ns);
+    }
+    near |= ns;
+    break;
+  }
+  free(w);
+  path[len] = emitted;
+  *near_out = near;
+  *fallback_out = fallback;
+  return len + 1;
+}
+
+int oracle_verify_tree_sample(const void *zt, const void *zd,
+                              const int32_t *parent, const int32_t *node_tokens,
+                              int nb, int N, int V, int dtype, double T,
+                              uint64_t seed, int max_depth,
+                              const int32_t *b_ids, const double *u_acc,
+                              const double *u_samp, int32_t *out_path,
+                              int32_t *out_len, int32_t *out_near,
+                              int32_t *out_fallback, int nthreads) {
+  if (nb < 0 || N <= 0 || V <= 0 || (dtype != 0 && dtype != 1) || !(T > 0.0))
+    return ORC_ERR_ARG;
+  int D = oracle_tree_max_depth(parent, N);
+  if (D < 0) return ORC_ERR_PARENT;
+  if (max_depth < D) return ORC_ERR_ARG;
+  int W = max_depth + 1;
+  int status = ORC_OK;
+  if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) \
+    reduction(max : status)
+  for (int s = 0; s < nb; ++s) {
+    uint32_t b = b_ids ? (uint32_t)b_ids[s] : (uint32_t)s;
+    int near = 0, fb = 0;
+    int len = verify_tree_one(row_ptr(zt, dtype, (int64_t)s * N, V),
+                              row_ptr(zd, dtype, (int64_t)s * N, V), parent,
+                              node_tokens + (size_t)s * N, N, V, dtype, T,
+                              seed, b, u_acc ? u_acc + (size_t)s * N : NULL,
+                              u_samp ? u_samp + (size_t)s * N : NULL,
+                              out_path + (size_t)s * W, W, &near, &fb);
+    out_len[s] = len;
+    if (len < 0) status = ORC_ERR_TOKEN;
+    if (out_near) out_near[s] = near;
+    if (out_fallback) out_fallback[s] = fb;
+  }
+  return status;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
