@@ -138,17 +138,24 @@ def max_over_ranks(value: float, backend_device=None) -> float:
 # ----------------------------------------------------------------------------
 # oracle timing (cpu_baseline and the reference arm)
 # ----------------------------------------------------------------------------
+def make_inputs(w, device):
+    from sampling_row_online_gb300.workloads import make_chain, make_tree, make_tree_sample
+    if w.kind == "tree":
+        return make_tree(w, device=device)
+    if w.kind == "tree_sample":
+        return make_tree_sample(w, device=device)
+    return make_chain(w, device=device)
+
+
 def time_oracle(w, n_sequences: int, host_inputs=None, nthreads=None):
     """Verifies n_sequences sequences of workload w with the oracle (cycling through
     the batch, all host cores); returns (seconds, threads, description)."""
     import numpy as np
     import torch
     import oracle
-    from sampling_row_online_gb300.workloads import make_chain, make_tree
     nthreads = nthreads or max(1, os.cpu_count() or 1)
     if host_inputs is None:
-        host_inputs = (make_tree(w, device="cpu") if w.kind == "tree"
-                       else make_chain(w, device="cpu"))
+        host_inputs = make_inputs(w, "cpu")
     done = 0
     t0 = time.perf_counter()
     while done < n_sequences:
@@ -156,6 +163,10 @@ def time_oracle(w, n_sequences: int, host_inputs=None, nthreads=None):
         if w.kind == "tree":
             zt, parent, tok = host_inputs
             oracle.verify_tree_greedy(zt[:nb], parent, tok[:nb], nthreads=nthreads)
+        elif w.kind == "tree_sample":
+            zt, zd, parent, tok = host_inputs
+            oracle.verify_tree_sample(zt[:nb], zd[:nb], parent, tok[:nb], w.T, w.verify_seed,
+                                      b_ids=np.arange(nb), nthreads=nthreads)
         else:
             zt, zd, x = host_inputs
             oracle.verify_chain(zt[:nb], None if zd is None else zd[:nb], x[:nb], w.T,
@@ -168,9 +179,9 @@ def run_reference(args, w):
     ws, rank, _ = _dist_env()
     if rank != 0:
         return 0
-    from sampling_row_online_gb300.workloads import describe, make_chain, make_tree
-    host = make_tree(w, device="cpu") if w.kind == "tree" else make_chain(w, device="cpu")
-    per_seq_positions = (w.K - 1) if w.kind == "tree" else w.K
+    from sampling_row_online_gb300.workloads import describe
+    host = make_inputs(w, "cpu")
+    per_seq_positions = w.positions // w.B
     if args.warmup > 0:
         time_oracle(w, min(args.warmup, w.B), host)
     secs, threads = time_oracle(w, args.steps, host)
@@ -197,8 +208,7 @@ def run_gpu(args, w):
     import torch
     import torch.distributed as dist
     from sampling_row_online_gb300 import binding
-    from sampling_row_online_gb300.workloads import (describe, input_copies_for_cold_l2,
-                                                     make_chain, make_tree)
+    from sampling_row_online_gb300.workloads import describe, input_copies_for_cold_l2
     ws, rank, local = _dist_env()
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU")
@@ -212,15 +222,15 @@ def run_gpu(args, w):
 
     # inputs (rank-specific seed: each rank verifies its own batch)
     wr = w.scaled(data_seed=w.data_seed + 7919 * rank)
-    first = make_tree(wr, device=dev) if w.kind == "tree" else make_chain(wr, device=dev)
+    first = make_inputs(wr, dev)
     per_copy = w.algorithmic_bytes
     ncopies = input_copies_for_cold_l2(per_copy)
     copies = [first] + [tuple(t.clone() if t.dim() >= 2 and t.numel() * t.element_size() > 1 << 20
                               else t for t in first) for _ in range(ncopies - 1)]
     B, V = w.B, w.V
     dt = 0 if w.dtype == "f32" else 1
-    if w.kind == "tree":
-        D = binding.spec_tree_max_depth(first[1].cpu())
+    if w.kind in ("tree", "tree_sample"):
+        D = binding.spec_tree_max_depth(first[-2].cpu())
         out_a = torch.empty((B, D + 1), dtype=torch.int32, device=dev)
     else:
         D = 0
@@ -228,6 +238,13 @@ def run_gpu(args, w):
     out_b = torch.empty((B,), dtype=torch.int32, device=dev)
 
     def make_call(c):
+        if w.kind == "tree_sample":
+            zt, zd, parent, tok = c
+            a = (ctypes.c_void_p(zt.data_ptr()), ctypes.c_void_p(zd.data_ptr()),
+                 ctypes.c_void_p(parent.data_ptr()), ctypes.c_void_p(tok.data_ptr()), B, w.K, V, dt,
+                 ctypes.c_float(w.T), ctypes.c_uint64(w.verify_seed), D,
+                 ctypes.c_void_p(out_a.data_ptr()), ctypes.c_void_p(out_b.data_ptr()), sp)
+            return lambda: lib.spec_verify_tree(*a)
         if w.kind == "tree":
             zt, parent, tok = c
             a = (ctypes.c_void_p(zt.data_ptr()), ctypes.c_void_p(parent.data_ptr()),
@@ -354,7 +371,7 @@ def run_gpu(args, w):
             more, _ = time_oracle(w, nseq)
             secs += more
             reps += 1
-        per_seq = (w.K - 1) if w.kind == "tree" else w.K
+        per_seq = w.positions // w.B
         cpu = {"value": nseq * reps * per_seq / secs, "unit": UNIT, "cores": threads,
                "kind": "oracle",
                "sample": f"{reps} pass(es) over the {nseq} sequences of {w.name}, fp64 oracle"}
@@ -384,7 +401,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4"])
+    ap.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4", "c3s"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -209,6 +209,44 @@ int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent,
                             int32_t *out_len, void *stream);
 
 /*
+ * spec_verify_tree — stochastic verification of a draft tree at temperature
+ * T > 0 (T == 0 is greedy matching, as spec_verify_tree_greedy).  The pages
+ * give the chain rule ([Oscine] §"验收标准的精确数学", §"拒绝之后怎么办？——
+ * 残差分布") and warn that verifying a tree does not by itself keep the
+ * output lossless ([Infra53] §9); the rule for several children of a node is
+ * not given, and this reading is the lossless extension of the chain rule:
+ * the children of a node are candidates drawn independently from the
+ * draft's distribution q at that node, tried in index order.  With r the
+ * current target distribution at the node (r = p at first), candidate x is
+ * accepted iff u < r(x)/q(x); a reject replaces r by norm(max(0, r - q)).
+ * An accepted candidate becomes the current node; a node whose candidates
+ * are all rejected emits a token drawn from r; an accepted node without
+ * children emits a bonus token drawn from its p.  Only one path is
+ * committed ([Infra53] §3).  Uniforms: the test of child c uses counter
+ * (b, c - 1, slot 0), the draw at node u uses (b, u, slot 1); a chain-shaped
+ * tree (parent[c] = c - 1) therefore gives exactly spec_verify's result.
+ *
+ *   target_logits  [B, N, V], dtype: row u = target distribution at node u
+ *   draft_logits   [B, N, V], dtype: row u = draft distribution at node u,
+ *                  from which u's children were drawn (rows of nodes
+ *                  without children are not read)
+ *   parent         [N] int32 (device): parent[0] = -1, 0 <= parent[c] < c
+ *   node_tokens    [B, N] int32; entry 0 is ignored
+ *   B >= 0, 1 <= N <= SPEC_MAX_TREE_NODES, V >= 1, T >= 0, seed as spec_verify
+ *   max_depth      D = spec_tree_max_depth(parent) (from a host copy)
+ *   out_path       [B, D+1] int32: tokens of the accepted path (root
+ *                  excluded), then the emitted token, then -1 padding
+ *   out_len        [B] int32: accepted + 1, or -1 on a device error
+ * A token outside [0, V) is reported as SPEC_ERR_TOKEN_RANGE, a parent[]
+ * that is not a tree of depth <= max_depth as SPEC_ERR_PARENT (both by
+ * spec_get_status); the sequence's outputs are -1.
+ */
+int spec_verify_tree(const void *target_logits, const void *draft_logits,
+                     const int32_t *parent, const int32_t *node_tokens, int B, int N,
+                     int V, int dtype, float temperature, uint64_t seed, int max_depth,
+                     int32_t *out_path, int32_t *out_len, void *stream);
+
+/*
  * spec_tree_max_depth — HOST helper: the largest node depth of parent[]
  * (HOST pointer), or -SPEC_ERR_PARENT if parent[] is not a tree
  * ([Infra53] §3.2: position IDs follow tree depth).

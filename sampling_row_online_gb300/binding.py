@@ -52,6 +52,7 @@ def library():
     lib.spec_verify_host.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, u64, vp, vp, vp]
     lib.spec_arm_rows_event.argtypes = [vp]
     lib.spec_verify_tree_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.spec_verify_tree.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, u64, i32, vp, vp, vp]
     lib.spec_tree_max_depth.argtypes = [vp, i32]
     lib.spec_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp]
     lib.spec_get_status.argtypes = [vp]
@@ -218,6 +219,39 @@ def spec_verify_tree_greedy(target_logits, parent, node_tokens, *, max_depth=Non
                                          B, N, V, _dtype_code(target_logits), int(max_depth),
                                          _ptr(out_path), _ptr(out_len), _stream(stream))
     _check(st, "spec_verify_tree_greedy")
+    return out_path, out_len
+
+
+def spec_verify_tree(target_logits, draft_logits, parent, node_tokens, temperature, seed, *,
+                     max_depth=None, out_path=None, out_len=None, stream=None):
+    """Stochastic tree verification (T > 0; T == 0 is greedy matching); returns
+    (out_path [B, D+1] int32, out_len [B] int32)."""
+    lib = library()
+    _dev(target_logits, "target_logits")
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, N, V]")
+    B, N, V = target_logits.shape
+    if draft_logits is not None:
+        _dev(draft_logits, "draft_logits", target_logits.dtype)
+        if tuple(draft_logits.shape) != (B, N, V):
+            raise ValueError("draft_logits must be [B, N, V]")
+    _dev(parent, "parent", torch.int32)
+    _dev(node_tokens, "node_tokens", torch.int32)
+    if parent.numel() != N or tuple(node_tokens.shape) != (B, N):
+        raise ValueError("parent must be [N] and node_tokens [B, N]")
+    if max_depth is None:
+        max_depth = spec_tree_max_depth(parent.cpu())
+    dev = target_logits.device
+    if out_path is None:
+        out_path = torch.empty((B, max_depth + 1), dtype=torch.int32, device=dev)
+    if out_len is None:
+        out_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.spec_verify_tree(_ptr(target_logits), _ptr(draft_logits), _ptr(parent),
+                                  _ptr(node_tokens), B, N, V, _dtype_code(target_logits),
+                                  ctypes.c_float(temperature), ctypes.c_uint64(int(seed) & ((1 << 64) - 1)),
+                                  int(max_depth), _ptr(out_path), _ptr(out_len), _stream(stream))
+    _check(st, "spec_verify_tree")
     return out_path, out_len
 
 

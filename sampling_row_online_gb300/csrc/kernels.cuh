@@ -62,7 +62,8 @@ constexpr int TICKET_STRIDE = 32;  // ints
 // device status bits (per stream)
 constexpr int ST_TOKEN = 1, ST_PARENT = 2, ST_TIMEOUT = 4;
 
-enum Kind : int { KIND_SAMPLE = 0, KIND_GREEDY_CHAIN = 1, KIND_TREE = 2 };
+enum Kind : int { KIND_SAMPLE = 0, KIND_GREEDY_CHAIN = 1, KIND_TREE = 2, KIND_TREE_SAMPLE = 3 };
+constexpr int MAX_TREE_NODES = 1024;
 
 struct Stats {  // layout-compatible with spec_stats_t
   unsigned long long sequences, accepted, bonus, resampled, residual_fallbacks, errors;
@@ -327,6 +328,7 @@ struct ItemCursor {
   using E = Elem<DT>;
   int item, lo, len, nt, nrows;
   const unsigned char *rt, *rd;
+  const uint32_t *tree_internal;  // stochastic tree: bit u set iff node u has children
 
   __device__ __forceinline__ void set(const Params &p, int it) {
     item = it;
@@ -339,7 +341,8 @@ struct ItemCursor {
     int b, i;
     decode_job(p, q, b, i);
     rt = target_row<DT>(p, b, i) + static_cast<size_t>(lo) * E::BYTES;
-    if (!ARGMAX && i < p.K) {
+    const bool pair = p.kind == KIND_TREE_SAMPLE ? ((tree_internal[i >> 5] >> (i & 31)) & 1u) != 0 : i < p.K;
+    if (!ARGMAX && pair) {
       rd = draft_row<DT>(p, b, i) + static_cast<size_t>(lo) * E::BYTES;
       nrows = 2;
     } else {
@@ -468,6 +471,18 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
     // ------------------------------------------------------------ producer
     const int nitems = p.njobs * p.C;
     ItemCursor<DT, ARGMAX> pc;
+    __shared__ uint32_t tree_internal[ARGMAX ? 1 : MAX_TREE_NODES / 32];
+    pc.tree_internal = tree_internal;
+    if (!ARGMAX && p.kind == KIND_TREE_SAMPLE) {
+      // stochastic tree: nodes with children stream their draft row too
+      for (int w = lane; w < MAX_TREE_NODES / 32; w += 32) tree_internal[w] = 0u;
+      __syncwarp();
+      for (int cn = 1 + lane; cn < p.K; cn += 32) {
+        const int u = __ldg(p.parent + cn);
+        if (u >= 0 && u < p.K) atomicOr(&tree_internal[u >> 5], 1u << (u & 31));
+      }
+      __syncwarp();
+    }
     int pseq = 0;
     bool tmo = false;
     auto next_stage = [&]() -> int {  // wait until the next stage is free
@@ -917,6 +932,151 @@ __device__ __forceinline__ int draw_p_from_partials(const Params &p, const float
   return r0 + block_walk(wbuf, len, P, t, lastmode, sh);
 }
 
+// This CTA's share of a cluster-wide draw: slice [lo, lo + len) of the
+// vocabulary, NWARP contiguous warp ranges of nvw 16-byte vectors each.
+struct DrawSlice {
+  int lo, len, nv, nvw;
+  __device__ __forceinline__ void set(int rank, int slice_d, int V, int VE) {
+    lo = rank * slice_d;
+    len = max(0, min(V, lo + slice_d) - lo);
+    nv = (len + VE - 1) / VE;
+    nvw = (nv + NWARP - 1) / NWARP;
+  }
+};
+
+// One cluster-wide weighing of the row pair (rt, rd) under W, by every CTA
+// of the cluster over its slice: each warp sums its range (lane-strided,
+// coalesced 16-byte loads, four per row in flight per lane) into
+// sh.wmass[warp]; each CTA's mass goes into sh.xz[slot][rank] of every CTA;
+// after the cluster barrier every thread of every CTA gets the same total Z.
+template <int DT, bool TMA>
+__device__ __forceinline__ float cluster_weigh(const unsigned char *rt, const unsigned char *rd, const Weights &W,
+                                               const DrawSlice &ds, int slot, uint32_t rank, uint32_t CD,
+                                               DrawShared &sh) {
+  using E = Elem<DT>;
+  constexpr int VE = E::VE;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int v0 = warp * ds.nvw, v1 = min(ds.nv, v0 + ds.nvw);
+  float acc = 0.f;
+  if (TMA) {  // rows 16-byte aligned, V a multiple of the vector width
+    constexpr int BATCH = 4;
+    for (int j = v0 + lane; j < v1; j += 32 * BATCH) {
+      uint4 vt[BATCH], vd[BATCH];
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) {
+        const int jj = j + 32 * k;
+        const size_t off = static_cast<size_t>(ds.lo + jj * VE) * E::BYTES;
+        vt[k] = jj < v1 ? __ldcg(reinterpret_cast<const uint4 *>(rt + off)) : make_uint4(0, 0, 0, 0);
+        vd[k] = (jj < v1 && W.resid) ? __ldcg(reinterpret_cast<const uint4 *>(rd + off)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) {
+        if (j + 32 * k >= v1) break;
+        float ft[VE], fd[VE];
+        E::unpack(vt[k], ft);
+        E::unpack(vd[k], fd);
+#pragma unroll
+        for (int e = 0; e < VE; ++e) acc = __fadd_rn(acc, W(ft[e], fd[e]));
+      }
+    }
+  } else {
+    const int e0 = min(ds.len, v0 * VE), e1 = min(ds.len, v1 * VE);
+    for (int e = e0 + lane; e < e1; e += 32)
+      acc = __fadd_rn(acc, W(E::load(rt, ds.lo + e), W.resid ? E::load(rd, ds.lo + e) : 0.f));
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) sh.wmass[warp] = acc;
+  __syncthreads();
+  if (tid < static_cast<int>(CD)) {  // this CTA's mass, into every CTA of the cluster
+    float cm = 0.f;
+    for (int w = 0; w < NWARP; ++w) cm = __fadd_rn(cm, sh.wmass[w]);
+    dsmem_st_f32(dsmem_addr(&sh.xz[slot][rank], static_cast<uint32_t>(tid)), cm);
+  }
+  cluster_sync();  // every CTA's mass is in every CTA
+  float Z = 0.f;
+  for (uint32_t r = 0; r < CD; ++r) Z = __fadd_rn(Z, sh.xz[slot][r]);
+  return Z;
+}
+
+// The CTA whose slice holds t = u * Z (the first with positive mass whose
+// running total passes t; else the last with positive mass), found by
+// thread 0 from sh.xz[slot]: sh.bi[2] = that CTA, sh.bi[3] = last-entry mode,
+// sh.bf[0] = the mass before it, sh.bf[1] = t.  The caller synchronises.
+__device__ __forceinline__ void find_owner_cta(float u, float Z, int slot, uint32_t CD, DrawShared &sh) {
+  const float t = u * Z;
+  float P = 0.f, Pown = 0.f, Plast = 0.f;
+  int own = -1, last = -1;
+  for (uint32_t r = 0; r < CD; ++r) {
+    const float zr = sh.xz[slot][r];
+    if (own < 0 && zr > 0.f && __fadd_rn(P, zr) > t) {
+      own = static_cast<int>(r);
+      Pown = P;
+    }
+    if (zr > 0.f) {
+      last = static_cast<int>(r);
+      Plast = P;
+    }
+    P = __fadd_rn(P, zr);
+  }
+  int lastmode = 0;
+  if (own < 0) {
+    own = last < 0 ? 0 : last;
+    Pown = Plast;
+    lastmode = 1;
+  }
+  sh.bi[2] = own;
+  sh.bi[3] = lastmode;
+  sh.bf[0] = Pown;
+  sh.bf[1] = t;
+}
+
+// In the owner CTA (after find_owner_cta): the warp range holding t, its
+// weights into wbuf, and the block-wide walk.  Returns the token in every
+// thread.  sh.wmass must still hold this CTA's warp masses of the same W.
+template <int DT>
+__device__ __forceinline__ int owner_walk(const unsigned char *rt, const unsigned char *rd, const Weights &W,
+                                          const DrawSlice &ds, float *wbuf, DrawShared &sh) {
+  using E = Elem<DT>;
+  constexpr int VE = E::VE;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    const float t = sh.bf[1];
+    int lastmode = sh.bi[3];
+    float P = sh.bf[0], Pown = P, Plast = P;
+    int ow = -1, last = -1;
+    for (int w = 0; w < NWARP; ++w) {
+      const float m = sh.wmass[w];
+      if (!lastmode && ow < 0 && m > 0.f && __fadd_rn(P, m) > t) {
+        ow = w;
+        Pown = P;
+      }
+      if (m > 0.f) {
+        last = w;
+        Plast = P;
+      }
+      P = __fadd_rn(P, m);
+    }
+    if (ow < 0) {
+      ow = last < 0 ? 0 : last;
+      Pown = Plast;
+      lastmode = 1;
+    }
+    sh.bi[6] = ow;
+    sh.bi[7] = lastmode;
+    sh.bf[2] = Pown;
+  }
+  __syncthreads();
+  const int ow = sh.bi[6];
+  const int r0 = min(ds.len, ow * ds.nvw * VE);
+  const int rlen = min(ds.len, (ow + 1) * ds.nvw * VE) - r0;
+  for (int e = tid; e < rlen; e += NT)
+    wbuf[e] = W(E::load(rt, ds.lo + r0 + e), W.resid ? E::load(rd, ds.lo + r0 + e) : 0.f);
+  const float Pw = sh.bf[2], tw = sh.bf[1];
+  const bool lastw = sh.bi[7] != 0;
+  __syncthreads();
+  return ds.lo + r0 + block_walk(wbuf, rlen, Pw, tw, lastw, sh);
+}
+
 template <int DT, bool TMA>
 __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   using E = Elem<DT>;
@@ -1033,9 +1193,8 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   // ---- the residual draw at position n
   const unsigned char *rt = target_row<DT>(p, b, n);
   const unsigned char *rd = draft_row<DT>(p, b, n);
-  const int lo = static_cast<int>(rank) * p.slice_d;
-  const int len = max(0, min(p.V, lo + p.slice_d) - lo);
-  const int nv = (len + VE - 1) / VE, nvw = (nv + NWARP - 1) / NWARP;
+  DrawSlice ds;
+  ds.set(static_cast<int>(rank), p.slice_d, p.V, VE);
   Weights W;
   W.c = c;
   W.mtc = rmax[n] * c;
@@ -1044,128 +1203,19 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   W.inv_sd = 1.f / rsum[K + 1 + n];
   W.resid = true;
   const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(n), 1u);
-  int fallback = 0;
-  for (int round = 0; round < 2; ++round) {
-    // warp `warp` weighs vectors [v0, v1) of the slice, lanes strided
-    const int v0 = warp * nvw, v1 = min(nv, v0 + nvw);
-    float acc = 0.f;
-    if (TMA) {  // rows 16-byte aligned, V a multiple of the vector width
-      constexpr int BATCH = 4;
-      for (int j = v0 + lane; j < v1; j += 32 * BATCH) {
-        uint4 vt[BATCH], vd[BATCH];
-#pragma unroll
-        for (int k = 0; k < BATCH; ++k) {
-          const int jj = j + 32 * k;
-          const size_t off = static_cast<size_t>(lo + jj * VE) * E::BYTES;
-          vt[k] = jj < v1 ? __ldcg(reinterpret_cast<const uint4 *>(rt + off)) : make_uint4(0, 0, 0, 0);
-          vd[k] = (jj < v1 && W.resid) ? __ldcg(reinterpret_cast<const uint4 *>(rd + off)) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int k = 0; k < BATCH; ++k) {
-          if (j + 32 * k >= v1) break;
-          float ft[VE], fd[VE];
-          E::unpack(vt[k], ft);
-          E::unpack(vd[k], fd);
-#pragma unroll
-          for (int e = 0; e < VE; ++e) acc = __fadd_rn(acc, W(ft[e], fd[e]));
-        }
-      }
-    } else {
-      const int e0 = min(len, v0 * VE), e1 = min(len, v1 * VE);
-      for (int e = e0 + lane; e < e1; e += 32)
-        acc = __fadd_rn(acc, W(E::load(rt, lo + e), W.resid ? E::load(rd, lo + e) : 0.f));
-    }
-    acc = warp_sum(acc);
-    if (lane == 0) sh.wmass[warp] = acc;
-    __syncthreads();
-    // this CTA's mass, pushed into every CTA of the cluster
-    if (tid < static_cast<int>(CD)) {
-      float cm = 0.f;
-      for (int w = 0; w < NWARP; ++w) cm = __fadd_rn(cm, sh.wmass[w]);
-      dsmem_st_f32(dsmem_addr(&sh.xz[round][rank], static_cast<uint32_t>(tid)), cm);
-    }
-    cluster_sync();  // every CTA's mass is in every CTA
-    if (tid == 0) {
-      float Z = 0.f;
-      for (uint32_t r = 0; r < CD; ++r) Z = __fadd_rn(Z, sh.xz[round][r]);
-      int again = 0;
-      if (W.resid && !(Z > 0.f)) {
-        again = 1;  // no residual mass in fp32: draw from p at this position
-      } else {
-        const float t = u * Z;
-        float P = 0.f, Pown = 0.f, Plast = 0.f;
-        int own = -1, last = -1;
-        for (uint32_t r = 0; r < CD; ++r) {
-          const float zr = sh.xz[round][r];
-          if (own < 0 && zr > 0.f && __fadd_rn(P, zr) > t) {
-            own = static_cast<int>(r);
-            Pown = P;
-          }
-          if (zr > 0.f) {
-            last = static_cast<int>(r);
-            Plast = P;
-          }
-          P = __fadd_rn(P, zr);
-        }
-        int lastmode = 0;
-        if (own < 0) {
-          own = last < 0 ? 0 : last;
-          Pown = Plast;
-          lastmode = 1;
-        }
-        sh.bi[2] = own;
-        sh.bi[3] = lastmode;
-        sh.bf[0] = Pown;
-        sh.bf[1] = t;
-      }
-      sh.bi[4] = again;
-    }
-    __syncthreads();
-    if (sh.bi[4] && round == 0) {
-      W.resid = false;
-      fallback = 1;
-      continue;
-    }
-    break;
+  int fallback = 0, slot = 0;
+  float Z = cluster_weigh<DT, TMA>(rt, rd, W, ds, slot, rank, CD, sh);
+  if (!(Z > 0.f)) {  // no residual mass in fp32: draw from p at this position
+    W.resid = false;
+    fallback = 1;
+    slot = 1;
+    Z = cluster_weigh<DT, TMA>(rt, rd, W, ds, slot, rank, CD, sh);
   }
+  if (tid == 0) find_owner_cta(u, Z, slot, CD, sh);
+  __syncthreads();
   // No DSMEM access follows the last exchange, so only the owner CTA goes on.
   if (static_cast<int>(rank) != sh.bi[2]) return;
-  if (tid == 0) {  // the warp range holding t
-    const float t = sh.bf[1];
-    int lastmode = sh.bi[3];
-    float P = sh.bf[0], Pown = P, Plast = P;
-    int ow = -1, last = -1;
-    for (int w = 0; w < NWARP; ++w) {
-      const float m = sh.wmass[w];
-      if (!lastmode && ow < 0 && m > 0.f && __fadd_rn(P, m) > t) {
-        ow = w;
-        Pown = P;
-      }
-      if (m > 0.f) {
-        last = w;
-        Plast = P;
-      }
-      P = __fadd_rn(P, m);
-    }
-    if (ow < 0) {
-      ow = last < 0 ? 0 : last;
-      Pown = Plast;
-      lastmode = 1;
-    }
-    sh.bi[6] = ow;
-    sh.bi[7] = lastmode;
-    sh.bf[2] = Pown;
-  }
-  __syncthreads();
-  const int ow = sh.bi[6];
-  const int r0 = min(len, ow * nvw * VE);
-  const int rlen = min(len, (ow + 1) * nvw * VE) - r0;
-  for (int e = tid; e < rlen; e += NT)
-    wbuf[e] = W(E::load(rt, lo + r0 + e), W.resid ? E::load(rd, lo + r0 + e) : 0.f);
-  const float Pw = sh.bf[2], tw = sh.bf[1];
-  const bool lastw = sh.bi[7] != 0;
-  __syncthreads();
-  const int token = lo + r0 + block_walk(wbuf, rlen, Pw, tw, lastw, sh);
+  const int token = owner_walk<DT>(rt, rd, W, ds, wbuf, sh);
   if (tid < 32) {
     for (int j = lane; j <= K; j += 32)
       out[j] = j < n ? gtok[j] : (j == n ? token : -1);
@@ -1178,6 +1228,197 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
         if (fallback) atomicAdd(&p.stats->residual_fallbacks, 1ull);
       }
     }
+  }
+}
+
+// ======================================================================
+// B''. tree_draw_kernel: stochastic tree verification, one cluster per tree.
+// ======================================================================
+// The candidates (children) of a node are tried in index order.  With r the
+// current target distribution at the node (r = p at first), candidate x is
+// accepted iff u < r(x)/q(x); on a reject r becomes max(0, p - a q)/W with
+// a += W and W = the mass of max(0, p - a q), weighed over the node's row
+// pair by the whole cluster.  An accepted candidate becomes the current
+// node; if every candidate is rejected the token is drawn from r with the
+// masses of that last weighing; an accepted leaf draws a bonus token from its
+// own p, from its streaming partials.  Uniforms: the test of child c uses
+// (b, c - 1, slot 0), the draw at node u uses (b, u, slot 1), so that a
+// chain-shaped tree is exactly the chain verification.  Every CTA of the
+// cluster takes the same decisions from the same bits.
+// Pages: the chain rule of blog.oscine.io "投机解码：让大模型「猜」着跑的数学魔术"
+// (§"验收标准的精确数学", §"拒绝之后怎么办？——残差分布") applied sibling by
+// sibling; infra-guide "5.3 Medusa, EAGLE và MTP" §9 (a tree is not lossless
+// by itself) and §3 (one committed path).
+template <int DT, bool TMA>
+__global__ void __launch_bounds__(NT, 4) tree_draw_kernel(const Params p) {
+  using E = Elem<DT>;
+  constexpr int VE = E::VE;
+  // dynamic: parent [N], tokens [N], each node's logits at its token in its
+  // parent's target and draft rows [N] + [N], acceptance uniforms [N], the
+  // current node's children [N], then (16-byte aligned) the walk buffer
+  extern __shared__ __align__(16) float dsh[];
+  __shared__ DrawShared sh;
+  __shared__ float nrm[4];  // the current node's (max, sumexp) of target and draft
+  __shared__ int tst[2];    // error bits, number of children of the current node
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t rank = cluster_rank();
+  const uint32_t CD = cluster_size();
+  const int b = blockIdx.x / CD;
+  const int N = p.K;
+  const float c = p.c;
+  int *s_par = reinterpret_cast<int *>(dsh);
+  int *s_tok = s_par + N;
+  float *s_gt = reinterpret_cast<float *>(s_tok + N);
+  float *s_gd = s_gt + N;
+  float *s_u = s_gd + N;
+  int *s_kids = reinterpret_cast<int *>(s_u + N);
+  float *wbuf = dsh + p.wbuf_off / 4;
+
+  cluster_arrive_relaxed();  // every peer must run before any DSMEM store
+  pdl_launch_dependents();
+  if (tid == 0) tst[0] = 0;
+  __syncthreads();
+  // ---- inputs: the tree, the node tokens, their logits, the uniforms
+  for (int cn = tid; cn < N; cn += NT) {
+    const int pu = __ldg(p.parent + cn);
+    const int x = __ldg(p.tokens + static_cast<size_t>(b) * N + cn);
+    int bad = 0;
+    if (cn == 0) {
+      bad = pu != -1 ? 2 : 0;
+    } else {
+      if (pu < 0 || pu >= cn) bad |= 2;
+      if (x < 0 || x >= p.V) bad |= 1;
+    }
+    s_par[cn] = pu;
+    s_tok[cn] = x;
+    s_gt[cn] = (cn > 0 && !bad) ? E::load(target_row<DT>(p, b, pu), x) : 0.f;
+    s_gd[cn] = (cn > 0 && !bad) ? E::load(draft_row<DT>(p, b, pu), x) : 0.f;
+    s_u[cn] = cn > 0 ? philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(cn - 1), 0u) : 0.f;
+    if (bad) atomicOr(&tst[0], bad);
+  }
+  __syncthreads();
+  if (!(tst[0] & 2)) {  // every node within max_depth of the root
+    for (int cn = tid; cn < N; cn += NT) {
+      int d = 0;
+      for (int a = cn; a > 0 && d <= p.max_depth; a = s_par[a]) ++d;
+      if (d > p.max_depth) atomicOr(&tst[0], 2);
+    }
+  }
+  __syncthreads();
+  pdl_wait();  // the row partials of the first launch are complete and visible
+  if (blockIdx.x == 0 && tid < p.nshard) p.tickets[tid * TICKET_STRIDE] = 0;  // for the next call
+  const int err = tst[0];
+  const int W1 = p.max_depth + 1;
+  int32_t *path = p.out_tokens + static_cast<size_t>(b) * W1;
+  cluster_wait();  // pairs with the arrive above
+  if (err) {
+    if (rank == 0) {
+      for (int j = tid; j < W1; j += NT) path[j] = -1;
+      if (tid == 0) {
+        p.out_n[b] = -1;
+        atomicOr(p.status, (err & 2) ? ST_PARENT : ST_TOKEN);
+      }
+    }
+    return;
+  }
+
+  const int nparts = p.C * NCW;
+  DrawSlice ds;
+  ds.set(static_cast<int>(rank), p.slice_d, p.V, VE);
+  int node = 0, len = 0, slot = 0;
+  for (;;) {
+    // ---- the children of `node` in index order, and its normalisers
+    if (warp == 0) {
+      int cnt = 0;
+      for (int base = node + 1; base < N; base += 32) {
+        const int cn = base + lane;
+        const bool is = cn < N && s_par[cn] == node;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, is);
+        if (is) s_kids[cnt + __popc(m & ((1u << lane) - 1u))] = cn;
+        cnt += __popc(m);
+      }
+      float mt, st, md, sd;
+      warp_job_norms(p.partials + static_cast<size_t>(job_of(p, b, node)) * nparts, nparts, c, cnt > 0, mt,
+                     st, md, sd);
+      if (lane == 0) {
+        nrm[0] = mt;
+        nrm[1] = st;
+        nrm[2] = md;
+        nrm[3] = sd;
+        tst[1] = cnt;
+      }
+    }
+    __syncthreads();
+    const int nk = tst[1];
+    const float mt = nrm[0], st = nrm[1], md = nrm[2], sd = nrm[3];
+    const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(node), 1u);
+    if (nk == 0) {  // an accepted leaf: the bonus token from p (rank 0)
+      if (rank == 0) {
+        const int token = draw_p_from_partials<DT>(
+            p, p.partials + static_cast<size_t>(job_of(p, b, node)) * nparts, target_row<DT>(p, b, node), mt, u,
+            wbuf, sh);
+        for (int j = tid; j < W1; j += NT)
+          if (j >= len) path[j] = j == len ? token : -1;
+        if (tid == 0) p.out_n[b] = len + 1;
+      }
+      return;
+    }
+    const unsigned char *rt = target_row<DT>(p, b, node), *rd = draft_row<DT>(p, b, node);
+    Weights W;
+    W.c = c;
+    W.mtc = mt * c;
+    W.mdc = md * c;
+    W.inv_st = 1.f / st;
+    W.resid = true;
+    const float inv_sd = 1.f / sd;
+    float a = 0.f, Wk = 1.f;
+    int next = -1, vanished = 0, last_slot = 0;
+    for (int k = 0; k < nk; ++k) {
+      const int cn = s_kids[k];
+      const float at = fmaf(s_gt[cn], c, -(mt * c));
+      const float ad = fmaf(s_gd[cn], c, -(md * c));
+      const float rho = ex2(at - ad) * (sd / st);  // p(x) / q(x)
+      const float ratio = k == 0 ? rho : fmaxf(rho - a, 0.f) / Wk;  // r(x) / q(x)
+      if (s_u[cn] < ratio) {
+        next = cn;
+        break;
+      }
+      // reject: r <- norm(max(0, r - q)) = max(0, p - a q) / W
+      a = __fadd_rn(a, Wk);
+      W.inv_sd = __fmul_rn(a, inv_sd);
+      last_slot = slot;
+      Wk = cluster_weigh<DT, TMA>(rt, rd, W, ds, slot, rank, CD, sh);
+      slot ^= 1;
+      if (!(Wk > 0.f)) {
+        vanished = 1;
+        break;
+      }
+    }
+    if (next >= 0) {
+      if (rank == 0 && tid == 0) path[len] = s_tok[next];
+      ++len;
+      node = next;
+      __syncthreads();  // s_kids, nrm and tst are rewritten for the next node
+      continue;
+    }
+    // ---- every candidate rejected: the draw at this node
+    int token;
+    if (vanished) {  // no residual mass in fp32: draw from p at this node (rank 0)
+      if (rank != 0) return;
+      token = draw_p_from_partials<DT>(p, p.partials + static_cast<size_t>(job_of(p, b, node)) * nparts, rt, mt,
+                                       u, wbuf, sh);
+    } else {
+      if (tid == 0) find_owner_cta(u, Wk, last_slot, CD, sh);
+      __syncthreads();
+      // no DSMEM access follows the last exchange: only the owner CTA goes on
+      if (static_cast<int>(rank) != sh.bi[2]) return;
+      token = owner_walk<DT>(rt, rd, W, ds, wbuf, sh);
+    }
+    for (int j = tid; j < W1; j += NT)
+      if (j >= len) path[j] = j == len ? token : -1;
+    if (tid == 0) p.out_n[b] = len + 1;
+    return;
   }
 }
 

@@ -196,6 +196,14 @@ const void *pick_row_kernel(int dtype, bool tma) {
              : reinterpret_cast<const void *>(&row_kernel<1, false, ARGMAX>);
 }
 
+const void *pick_tree_draw_kernel(int dtype, bool tma) {
+  if (dtype == SPEC_F32)
+    return tma ? reinterpret_cast<const void *>(&tree_draw_kernel<0, true>)
+               : reinterpret_cast<const void *>(&tree_draw_kernel<0, false>);
+  return tma ? reinterpret_cast<const void *>(&tree_draw_kernel<1, true>)
+             : reinterpret_cast<const void *>(&tree_draw_kernel<1, false>);
+}
+
 const void *pick_draw_kernel(int dtype, bool tma) {
   if (dtype == SPEC_F32)
     return tma ? reinterpret_cast<const void *>(&draw_kernel<0, true>)
@@ -216,7 +224,7 @@ struct Geometry {
 int plan(Params &p, int dtype, bool tma, Geometry *g) {
   const int esz = dtype == SPEC_F32 ? 4 : 2;
   const int VE = 16 / esz;
-  const bool argmax = p.kind != KIND_SAMPLE;
+  const bool argmax = p.kind == KIND_GREEDY_CHAIN || p.kind == KIND_TREE;
   const int srows = argmax ? 1 : 2;
   const long long row_bytes = static_cast<long long>(p.V) * esz;
   // streaming items are single tiles of at most 16 KB per row
@@ -224,7 +232,8 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
   g->C = std::max(C_min, env_int("SPEC_VERIFY_SLICES", C_min, 1, 1 << 16));
   g->stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
   g->fa = argmax ? pick_row_kernel<true>(dtype, tma) : pick_row_kernel<false>(dtype, tma);
-  g->fb = argmax ? reinterpret_cast<const void *>(&finish_kernel) : pick_draw_kernel(dtype, tma);
+  g->fb = argmax ? reinterpret_cast<const void *>(&finish_kernel)
+                 : (p.kind == KIND_TREE_SAMPLE ? pick_tree_draw_kernel(dtype, tma) : pick_draw_kernel(dtype, tma));
   const int per = (p.V + g->C - 1) / g->C;
   g->slice = (per + VE - 1) / VE * VE;
   g->tile = std::min(TILE_MAX_BYTES / esz, g->slice);
@@ -257,7 +266,10 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
   }
   // the draw: clusters of CD CTAs, about 32 KB of each row per CTA; the walk
   // buffer holds one warp range of a CTA slice or of a streaming tile
-  const int base = (4 * (9 * p.K + 2) + 15) / 16 * 16;  // normalisers, logits at x, uniforms, tokens
+  // chain: normalisers, logits at x, uniforms, tokens; tree: parent, tokens,
+  // logits at each token, uniforms, children of the current node
+  const int base = p.kind == KIND_TREE_SAMPLE ? (4 * 6 * p.K + 15) / 16 * 16
+                                              : (4 * (9 * p.K + 2) + 15) / 16 * 16;
   int CD = static_cast<int>(std::min<long long>(
       MAX_CLUSTER, std::max<long long>(1, (row_bytes + DRAW_SLICE_BYTES - 1) / DRAW_SLICE_BYTES)));
   CD = env_int("SPEC_VERIFY_DRAW_CLUSTER", CD, 1, MAX_CLUSTER);
@@ -299,7 +311,7 @@ int launch(Params &p, const Geometry &g, cudaStream_t stream, float4 *partials, 
   p.stages = g.stages;
   p.partials = partials;
   p.status = status;
-  const bool argmax = p.kind != KIND_SAMPLE;
+  const bool argmax = p.kind == KIND_GREEDY_CHAIN || p.kind == KIND_TREE;
   cudaError_t e;
   {
     // a programmatic dependent of whatever precedes it on the stream: its
@@ -483,6 +495,47 @@ int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent,
   p.V = V;
   p.J = N;
   p.kind = KIND_TREE;
+  p.njobs = B * N;
+  p.max_depth = max_depth;
+  p.out_tokens = out_path;
+  p.out_n = out_len;
+  Workspace *w = nullptr;
+  return run_step(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr), &w);
+}
+
+int spec_verify_tree(const void *target_logits, const void *draft_logits, const int32_t *parent,
+                     const int32_t *node_tokens, int B, int N, int V, int dtype, float temperature,
+                     uint64_t seed, int max_depth, int32_t *out_path, int32_t *out_len, void *stream_ptr) {
+  const float T = temperature;
+  if (!(T >= 0.f) || !std::isfinite(T)) return fail(SPEC_ERR_ARG, "temperature must be finite and >= 0");
+  if (T == 0.f)  // greedy matching of the same tree
+    return spec_verify_tree_greedy(target_logits, parent, node_tokens, B, N, V, dtype, max_depth, out_path,
+                                   out_len, stream_ptr);
+  int st = check_common(target_logits, B, V, dtype);
+  if (st) return st;
+  const double cd = 1.4426950408889634 / static_cast<double>(T);
+  if (!(cd < 1e30)) return fail(SPEC_ERR_ARG, "temperature too small");
+  if (N < 1 || N > SPEC_MAX_TREE_NODES) return fail(SPEC_ERR_ARG, "N out of range [1, 1024]");
+  if (max_depth < 0 || max_depth >= N) return fail(SPEC_ERR_ARG, "max_depth out of range [0, N)");
+  if (B == 0) return SPEC_OK;
+  if (!parent || !node_tokens || !out_path || !out_len || !draft_logits)
+    return fail(SPEC_ERR_ARG, "NULL pointer");
+  if (static_cast<long long>(B) * N * MAX_CLUSTER > INT_MAX) return fail(SPEC_ERR_ARG, "B*N too large");
+  const int esz = dtype == SPEC_F32 ? 4 : 2;
+  const bool tma = (static_cast<long long>(V) * esz) % 16 == 0 && aligned16(target_logits) &&
+                   aligned16(draft_logits);
+  Params p = {};
+  p.zt = target_logits;
+  p.zd = draft_logits;
+  p.tokens = node_tokens;
+  p.parent = parent;
+  p.B = B;
+  p.K = N;
+  p.V = V;
+  p.J = N;
+  p.kind = KIND_TREE_SAMPLE;
+  p.c = static_cast<float>(cd);
+  p.seed = seed;
   p.njobs = B * N;
   p.max_depth = max_depth;
   p.out_tokens = out_path;

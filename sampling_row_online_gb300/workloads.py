@@ -67,9 +67,13 @@ class Workload:
     @property
     def rows(self) -> int:
         """Logit rows one call reads: (2K+1) per sequence for a stochastic chain,
-        K+1 for a greedy chain, N for a tree."""
+        K+1 for a greedy chain, N for a tree, N plus one draft row per node with
+        children for a stochastic tree."""
         if self.kind == "tree":
             return self.B * self.K
+        if self.kind == "tree_sample":
+            parent = tree_parents(self.branching, self.K)
+            return self.B * (self.K + len(set(parent[1:])))
         if self.T == 0:
             return self.B * (self.K + 1)
         return self.B * (2 * self.K + 1)
@@ -82,7 +86,7 @@ class Workload:
     @property
     def positions(self) -> int:
         """Verified draft positions per call: B*K (chain), B*(N-1) (tree)."""
-        return self.B * (self.K - 1) if self.kind == "tree" else self.B * self.K
+        return self.B * (self.K - 1) if self.kind in ("tree", "tree_sample") else self.B * self.K
 
     def scaled(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -99,12 +103,19 @@ WORKLOADS = {
                    sigma_t=3.0, data_seed=1003, verify_seed=3),
     "c4": Workload("c4", "chain", B=512, K=4, V=256000, dtype="f32", T=1.0,
                    sigma_t=1.0, sigma_d=1.0, zipf=True, data_seed=1004, verify_seed=4),
+    # not one of the headline configurations: the tree of c3 verified
+    # stochastically, candidates drawn from the draft at their parent
+    "c3s": Workload("c3s", "tree_sample", B=32, K=63, V=128256, dtype="bf16", T=1.0,
+                    sigma_t=3.0, sigma_d=1.0, data_seed=1005, verify_seed=5),
 }
 
 
 def describe(w: Workload) -> str:
     if w.kind == "tree":
         return (f"tree B={w.B} N={w.K} V={w.V} {w.dtype} T=0 "
+                f"branching={'/'.join(map(str, w.branching))}")
+    if w.kind == "tree_sample":
+        return (f"stochastic tree B={w.B} N={w.K} V={w.V} {w.dtype} T={w.T} "
                 f"branching={'/'.join(map(str, w.branching))}")
     return f"chain B={w.B} K={w.K} V={w.V} {w.dtype} T={w.T}"
 
@@ -198,6 +209,29 @@ def make_tree(w: Workload, device="cpu"):
     tok = torch.where(coin, top_of_parent, rnd)
     tok[:, 0] = 0
     return zt, parent, tok.contiguous()
+
+
+def make_tree_sample(w: Workload, device="cpu"):
+    """(target_logits [B,N,V], draft_logits [B,N,V], parent [N] int32,
+    node_tokens [B,N] int32) of a stochastic tree: z_d = z_t + N(0, sigma_d^2),
+    and the candidates of every node drawn independently from
+    softmax(z_d[parent] / T) (what a drafter sampling the tree would do)."""
+    assert w.kind == "tree_sample"
+    g = _gen(device, w.data_seed)
+    B, N, V = w.B, w.K, w.V
+    zt32 = torch.randn((B, N, V), generator=g, device=device) * w.sigma_t
+    zd32 = zt32 + torch.randn((B, N, V), generator=g, device=device) * w.sigma_d
+    zt = zt32.to(w.torch_dtype)
+    del zt32
+    zd = zd32.to(w.torch_dtype)
+    del zd32
+    parent = torch.tensor(tree_parents(w.branching, N), dtype=torch.int32, device=device)
+    tok = torch.zeros((B, N), dtype=torch.int32, device=device)
+    if N > 1:
+        gd = _gen(device, w.data_seed + 7919)
+        rows = zd[:, parent[1:].long()].reshape(B * (N - 1), V).float() / w.T
+        tok[:, 1:] = gumbel_argmax_draws(rows, gd).reshape(B, N - 1)
+    return zt, zd, parent, tok.contiguous()
 
 
 def input_copies_for_cold_l2(bytes_per_copy: int, l2_bytes: int = 129 * 2**20) -> int:

@@ -26,7 +26,7 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = _declared_functions()
-    for required in ("spec_verify", "spec_verify_tree_greedy", "spec_verify_ex", "spec_verify_host",
+    for required in ("spec_verify", "spec_verify_tree_greedy", "spec_verify_tree", "spec_verify_ex", "spec_verify_host",
                      "spec_tree_max_depth", "spec_tree_mask", "spec_get_status",
                      "spec_error_string", "spec_last_error_message", "spec_shutdown"):
         assert required in names
@@ -75,6 +75,14 @@ def test_tree_validation_without_gpu(lib):
     assert lib.spec_verify_tree_greedy(vp, vp, vp, 2, 5, 10, 1, 5, vp, vp, None) == 1     # depth >= N
     assert lib.spec_verify_tree_greedy(vp, vp, vp, 0, 5, 10, 1, 2, vp, vp, None) == 0     # empty
     assert lib.spec_tree_mask(vp, 1, 0, vp, vp, None) == 1
+    # stochastic tree: (zt, zd, parent, tokens, B, N, V, dtype, T, seed, D, path, len, stream)
+    t = lib.spec_verify_tree
+    assert t(vp, vp, vp, vp, 2, 0, 10, 1, 1.0, 0, 0, vp, vp, None) == 1                  # N = 0
+    assert t(vp, vp, vp, vp, 2, 5, 10, 1, 1.0, 0, 5, vp, vp, None) == 1                  # depth >= N
+    assert t(vp, vp, vp, vp, 2, 5, 10, 1, -1.0, 0, 2, vp, vp, None) == 1                 # T < 0
+    assert t(vp, None, vp, vp, 2, 5, 10, 1, 1.0, 0, 2, vp, vp, None) == 1                # no draft rows
+    assert t(vp, vp, vp, vp, 2, 5, 10, 9, 1.0, 0, 2, vp, vp, None) == 2                  # dtype
+    assert t(vp, vp, vp, vp, 0, 5, 10, 1, 1.0, 0, 2, vp, vp, None) == 0                  # empty
 
 
 @pytest.mark.parametrize("parent,depth", [([-1], 0), ([-1, 0, 0, 1, 2], 2),
