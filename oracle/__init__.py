@@ -60,6 +60,8 @@ def _load():
                                                   u64, i32, c_p, c_p, c_p, c_p, c_p, c_p, c_p,
                                                   i32]
         lib.oracle_verify_tree_sample.restype = i32
+        lib.oracle_ngram_propose.argtypes = [c_p, c_p, i32, i32, i32, i32, i32, c_p, c_p]
+        lib.oracle_ngram_propose.restype = i32
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         _lib = lib
@@ -283,3 +285,19 @@ def verify_tree_sample(zt, zd, parent, node_tokens, T: float, seed: int, *, max_
         raise ValueError("oracle_verify_tree_sample: invalid arguments")
     return dict(path=path, length=length, near=near.astype(bool), fallback=fb.astype(bool),
                 status=st)
+
+
+def ngram_propose(tokens, lengths, n_min: int, n_max: int, K: int):
+    """n-gram (prompt-lookup) proposals: (draft [B, K] int32, -1 padded; count [B])."""
+    t = _i32(tokens)
+    if t.ndim == 1:
+        t = t.reshape(1, -1)
+    B, L = t.shape
+    ln = _i32(lengths).reshape(B)
+    draft = np.zeros((B, K), dtype=np.int32)
+    count = np.zeros(B, dtype=np.int32)
+    st = _load().oracle_ngram_propose(_ptr(t), _ptr(ln), B, L, int(n_min), int(n_max), int(K),
+                                      _ptr(draft), _ptr(count))
+    if st != OK:
+        raise ValueError("oracle_ngram_propose: invalid arguments")
+    return draft, count
