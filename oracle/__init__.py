@@ -60,7 +60,7 @@ def _load():
                                                   u64, i32, c_p, c_p, c_p, c_p, c_p, c_p, c_p,
                                                   i32]
         lib.oracle_verify_tree_sample.restype = i32
-        lib.oracle_ngram_propose.argtypes = [c_p, c_p, i32, i32, i32, i32, i32, c_p, c_p]
+        lib.oracle_ngram_propose.argtypes = [c_p, c_p, i32, i32, i32, i32, i32, i32, c_p, c_p]
         lib.oracle_ngram_propose.restype = i32
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
@@ -287,7 +287,7 @@ def verify_tree_sample(zt, zd, parent, node_tokens, T: float, seed: int, *, max_
                 status=st)
 
 
-def ngram_propose(tokens, lengths, n_min: int, n_max: int, K: int):
+def ngram_propose(tokens, lengths, n_min: int, n_max: int, K: int, min_hits: int = 1):
     """n-gram (prompt-lookup) proposals: (draft [B, K] int32, -1 padded; count [B])."""
     t = _i32(tokens)
     if t.ndim == 1:
@@ -296,8 +296,8 @@ def ngram_propose(tokens, lengths, n_min: int, n_max: int, K: int):
     ln = _i32(lengths).reshape(B)
     draft = np.zeros((B, K), dtype=np.int32)
     count = np.zeros(B, dtype=np.int32)
-    st = _load().oracle_ngram_propose(_ptr(t), _ptr(ln), B, L, int(n_min), int(n_max), int(K),
-                                      _ptr(draft), _ptr(count))
+    st = _load().oracle_ngram_propose(_ptr(t), _ptr(ln), B, L, int(n_min), int(n_max), int(min_hits),
+                                      int(K), _ptr(draft), _ptr(count))
     if st != OK:
         raise ValueError("oracle_ngram_propose: invalid arguments")
     return draft, count

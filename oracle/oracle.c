@@ -652,28 +652,32 @@ int oracle_verify_tree_sample(const void *zt, const void *zd,
 /* декодирование на n-граммах": find an earlier occurrence of the current */
 /* n-gram in the context and propose the tokens that followed it;        */
 /* [Anhtu] §"Bật trong production": prompt_lookup_max bounds the n-gram   */
-/* window, num_speculative_tokens is K).  Reading taken: the longest n in */
-/* [n_min, n_max] whose last-n-token suffix occurred earlier wins, and of */
-/* its occurrences the most recent one (the largest start j with          */
-/* j + n <= len - 1, so at least one token follows it); the proposal is   */
-/* the up to K tokens after the occurrence.  Written as the plain search: */
-/* n from n_max down, j from the end down, token by token.                */
+/* window, num_speculative_tokens is K; [Glukhov] §"Настройка            */
+/* параметров" and the llama.cpp flags beside it: min-hits, the number of */
+/* times the pattern must have been seen).  Reading taken: the longest n  */
+/* in [n_min, n_max] whose last-n-token suffix occurred at least min_hits */
+/* times earlier wins, and of its occurrences the most recent one (the    */
+/* largest start j with j + n <= len - 1, so at least one token follows   */
+/* it); the proposal is the up to K tokens after that occurrence.         */
+/* Written as the plain search: n from n_max down, every start j from the */
+/* end down, token by token.                                              */
 /*   tokens: [B, L] int32 (row b holds lengths[b] <= L tokens),           */
 /*   out_draft: [B, K] (proposal, -1 padding), out_count: [B].            */
 /* ------------------------------------------------------------------ */
 int oracle_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B,
-                         int L, int n_min, int n_max, int K,
+                         int L, int n_min, int n_max, int min_hits, int K,
                          int32_t *out_draft, int32_t *out_count) {
-  if (B < 0 || L < 0 || n_min < 1 || n_max < n_min || K < 0) return ORC_ERR_ARG;
+  if (B < 0 || L < 0 || n_min < 1 || n_max < n_min || min_hits < 1 || K < 0) return ORC_ERR_ARG;
   for (int b = 0; b < B; ++b) {
     const int32_t *t = tokens + (size_t)b * L;
     int len = lengths[b];
     if (len < 0 || len > L) return ORC_ERR_ARG;
     int32_t *d = out_draft + (size_t)b * K;
     for (int k = 0; k < K; ++k) d[k] = -1;
-    int count = 0;
-    for (int n = n_max; n >= n_min && count == 0; --n) {
+    int start = -1;
+    for (int n = n_max; n >= n_min && start < 0; --n) {
       if (n > len - 1) continue;
+      int hits = 0, recent = -1;
       for (int j = len - n - 1; j >= 0; --j) {
         int same = 1;
         for (int i = 0; i < n; ++i)
@@ -682,12 +686,16 @@ int oracle_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B,
             break;
           }
         if (same) {
-          int start = j + n;
-          count = len - start < K ? len - start : K;
-          for (int k = 0; k < count; ++k) d[k] = t[start + k];
-          break;
+          if (recent < 0) recent = j;
+          ++hits;
         }
       }
+      if (hits >= min_hits) start = recent + n;
+    }
+    int count = 0;
+    if (start >= 0) {
+      count = len - start < K ? len - start : K;
+      for (int k = 0; k < count; ++k) d[k] = t[start + k];
     }
     out_count[b] = count;
   }
