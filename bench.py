@@ -4,6 +4,9 @@ achieved HBM bandwidth on GB300, one JSON line on stdout (rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c1] [--impl reference]
 
+``--workload ng1`` / ``ng2`` time the n-gram drafter instead (one
+spec_ngram_propose call over a batch of contexts per step).
+
 A step is one call of the verification on one batch of the workload
 (default c1: chain, B=64, K=5, V=128256, bf16 logits, T=0.7), inputs resident
 in HBM.  Consecutive steps rotate through input copies whose total exceeds
@@ -396,17 +399,217 @@ def run_gpu(args, w):
     return 0
 
 
+# ----------------------------------------------------------------------------
+# n-gram drafting workloads (ng1, ng2): one spec_ngram_propose call per step
+# ----------------------------------------------------------------------------
+NGRAM_METRIC = "n-gram drafts/sec (sequences drafted from their context), 1 GPU"
+NGRAM_UNIT = "sequences/s"
+
+
+def _ngram_bytes(lengths_host, K):
+    """Algorithmic bytes of one call: every context token once, the lengths,
+    the drafts and counts."""
+    B = len(lengths_host)
+    return 4 * int(lengths_host.sum()) + 4 * B + 4 * B * (K + 1)
+
+
+def time_ngram_oracle(w, tokens_h, lengths_h, min_seconds):
+    import oracle
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.ngram_propose(tokens_h, lengths_h, w.n_min, w.n_max, w.K, min_hits=w.min_hits)
+        reps += 1
+        secs = time.perf_counter() - t0
+        if secs >= min_seconds:
+            return secs, reps
+
+
+def ngram_describe(w):
+    return (f"n-gram drafting B={w.B} contexts of up to L={w.L} tokens (lengths uniform in [L/2, L]), "
+            f"n in [{w.n_min}, {w.n_max}], min_hits={w.min_hits}, K={w.K}")
+
+
+def run_reference_ngram(args, w):
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    from sampling_row_online_gb300.workloads import make_contexts
+    tokens, lengths = make_contexts(w, "cpu")
+    th, lh = tokens.numpy(), lengths.numpy()
+    for _ in range(max(0, args.warmup)):
+        time_ngram_oracle(w, th, lh, 0.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time_ngram_oracle(w, th, lh, 0.0)
+    secs = time.perf_counter() - t0
+    value = args.steps * w.B / secs
+    line = {
+        "metric": NGRAM_METRIC, "value": value, "unit": NGRAM_UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{w.name}: {ngram_describe(w)}", "step": "the whole batch"},
+        "cpu_baseline": {"value": value, "unit": NGRAM_UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} passes over the {w.B} contexts of {w.name}, oracle, 1 thread"},
+        "e2e": {"value": value, "unit": NGRAM_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu_ngram(args, w):
+    import torch
+    import torch.distributed as dist
+    from sampling_row_online_gb300 import binding
+    from sampling_row_online_gb300.workloads import input_copies_for_cold_l2, make_contexts
+    ws, rank, local = _dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    lib = binding.library()
+    stream = torch.cuda.current_stream()
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    tokens, lengths = make_contexts(w, dev, seed=w.data_seed + 7919 * rank)
+    lengths_h = lengths.cpu().numpy()
+    alg = _ngram_bytes(lengths_h, w.K)
+    ncopies = input_copies_for_cold_l2(alg)
+    copies = [tokens] + [tokens.clone() for _ in range(ncopies - 1)]
+    draft = torch.empty((w.B, w.K), dtype=torch.int32, device=dev)
+    count = torch.empty((w.B,), dtype=torch.int32, device=dev)
+
+    def make_call(t):
+        a = (ctypes.c_void_p(t.data_ptr()), ctypes.c_void_p(lengths.data_ptr()), w.B, w.L, w.n_min, w.n_max,
+             w.min_hits, w.K, ctypes.c_void_p(draft.data_ptr()), ctypes.c_void_p(count.data_ptr()), sp)
+        return lambda: lib.spec_ngram_propose(*a)
+
+    calls = [make_call(t) for t in copies]
+    for k in range(max(3, args.warmup)):
+        st = calls[k % ncopies]()
+        if st != 0:
+            raise SystemExit(f"spec_ngram_propose failed: {st} {lib.spec_last_error_message().decode()}")
+    torch.cuda.synchronize()
+    if lib.spec_get_status(sp) != 0:
+        raise SystemExit("device status error during warm-up")
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.25 if clocks else 0)
+    wall0 = time.perf_counter()
+    t_start.record(stream)
+    for k in range(args.steps):
+        calls[k % ncopies]()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    if lib.spec_get_status(sp) != 0:
+        raise SystemExit("device status error in the timed region")
+    region_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
+    call_ms = region_ms / args.steps
+    # the kernel alone: events around single calls
+    n_one = min(args.steps, 400)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_one)]
+    for k in range(n_one):
+        ev[k][0].record(stream)
+        calls[k % ncopies]()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    avg_launch_ms = max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in ev), dev)
+    value = w.B * args.steps * ws / (region_ms / 1e3)
+
+    # end to end through the binding: contexts copied in from pinned host
+    # memory, drafts and counts copied out, every step
+    e2e = None
+    if not args.no_e2e:
+        th = tokens.cpu().pin_memory()
+        lh = lengths.cpu().pin_memory()
+        dh = torch.empty((w.B, w.K), dtype=torch.int32, pin_memory=True)
+        ch = torch.empty((w.B,), dtype=torch.int32, pin_memory=True)
+        td = torch.empty_like(tokens)
+        ld = torch.empty_like(lengths)
+        e_steps = max(5, min(args.steps, 50))
+
+        def e2e_step():
+            td.copy_(th, non_blocking=True)
+            ld.copy_(lh, non_blocking=True)
+            binding.spec_ngram_propose(td, ld, w.n_min, w.n_max, w.K, min_hits=w.min_hits, out_draft=draft,
+                                       out_count=count)
+            dh.copy_(draft, non_blocking=True)
+            ch.copy_(count, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(3):
+            e2e_step()
+        if ws > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e_steps):
+            e2e_step()
+        e_sec = max_over_ranks(time.perf_counter() - t0, dev)
+        e2e = {"value": w.B * e_steps * ws / e_sec, "unit": NGRAM_UNIT,
+               "h2d_bytes_per_step": th.numel() * 4 + lh.numel() * 4,
+               "d2h_bytes_per_step": dh.numel() * 4 + ch.numel() * 4}
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+    peak, peak_kind = _peaks()
+    kernel = "ngram_kernel"
+    achieved = alg / (avg_launch_ms / 1e3) / 1e9
+    call_achieved = alg / (call_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{peak_kind} hbm_gbs", "traffic": _profile_traffic(kernel, w.name),
+                "kernel": kernel,
+                "timed": f"single calls bracketed by CUDA events on the call's stream, mean of {n_one}",
+                "algorithmic_bytes_per_launch": alg, "avg_launch_us": avg_launch_ms * 1e3,
+                "whole_call": {"achieved": call_achieved, "frac": call_achieved / peak,
+                               "avg_call_us": call_ms * 1e3,
+                               "timed": "region over the steps, calls chained back to back"}}
+    cpu = None
+    if not args.no_cpu_baseline:
+        th_np, lh_np = tokens.cpu().numpy(), lengths_h
+        secs, reps = time_ngram_oracle(w, th_np, lh_np, 3.0)
+        cpu = {"value": w.B * reps / secs, "unit": NGRAM_UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{reps} passes over the {w.B} contexts of {w.name}, oracle, 1 thread"}
+    line = {
+        "metric": NGRAM_METRIC, "value": value, "unit": NGRAM_UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": call_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {ngram_describe(w)}", "per_rank_batch": w.B,
+                   "context_tokens_per_step": int(lengths_h.sum()),
+                   "parallelism": f"replicas x{ws} (sequences sharded, no collective)",
+                   "l2": f"rotating {ncopies} context copies ({ncopies * alg / 1e6:.0f} MB > 2x L2)"},
+        "context_tokens_per_s": int(lengths_h.sum()) * args.steps * ws / (region_ms / 1e3),
+        "roofline": roofline, "achieved_hbm_gbs": achieved, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": args.steps, "clocks": clk, "wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4", "c3s"])
+    ap.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4", "c3s", "ng1", "ng2"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
-    from sampling_row_online_gb300.workloads import WORKLOADS
+    from sampling_row_online_gb300.workloads import NGRAM_WORKLOADS, WORKLOADS
+    if args.workload in NGRAM_WORKLOADS:
+        w = NGRAM_WORKLOADS[args.workload]
+        return run_reference_ngram(args, w) if args.impl == "reference" else run_gpu_ngram(args, w)
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

@@ -69,6 +69,7 @@ enum { SPEC_F32 = 0, SPEC_BF16 = 1 };
 /* Size limits. */
 #define SPEC_MAX_DRAFTS 255      /* K of a chain */
 #define SPEC_MAX_TREE_NODES 1024 /* N of a tree */
+#define SPEC_MAX_NGRAM 64        /* n_max of the n-gram drafter */
 
 /* Counters a caller may ask spec_verify_ex to accumulate (device memory,
  * zeroed by the caller, added to atomically by every call that receives it).
@@ -268,9 +269,39 @@ int spec_tree_mask(const int32_t *parent, int B, int N, uint32_t *out_mask,
                    int32_t *out_depth, void *stream);
 
 /*
+ * spec_ngram_propose — n-gram (prompt-lookup) drafting: for each of B
+ * contexts, the up to K tokens that followed an earlier occurrence of the
+ * context's own last n tokens ([Glukhov] §"Спекулятивное декодирование на
+ * n-граммах"; the window n_max is [Anhtu] §"Bật trong production"'s
+ * prompt_lookup_max, min_hits [Glukhov] §"Настройка параметров"'s min-hits).
+ * The pages leave the choice among several matches open; this reading is
+ * taken: the longest n in [n_min, n_max] whose suffix t[len-n .. len-1]
+ * occurred at least min_hits times at earlier starts j (j + n <= len - 1,
+ * so at least one token follows the occurrence) wins, and of those
+ * occurrences the most recent (largest j); the proposal is
+ * t[j+n .. j+n+count-1] with count = min(K, len - j - n).
+ *   tokens     [B, L] int32 (device): row b holds the context of sequence b
+ *              in its first lengths[b] entries; the rest is not read
+ *   lengths    [B] int32 (device), 0 <= lengths[b] <= L
+ *   n_min, n_max  1 <= n_min <= n_max <= SPEC_MAX_NGRAM
+ *   min_hits   >= 1 (1: any earlier occurrence)
+ *   K          0 <= K <= SPEC_MAX_DRAFTS
+ *   out_draft  [B, K] int32 (device): the proposal, then -1
+ *   out_count  [B] int32 (device): tokens proposed (0: no match)
+ * Token values are compared as plain integers and never range-checked.  A
+ * lengths[b] outside [0, L] sets out_count[b] = -1 and its draft row to -1,
+ * and spec_get_status then returns SPEC_ERR_ARG.  Output is bit-exact and
+ * deterministic (a pure function of the inputs).
+ */
+int spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int L, int n_min,
+                       int n_max, int min_hits, int K, int32_t *out_draft, int32_t *out_count,
+                       void *stream);
+
+/*
  * spec_get_status — waits for `stream`, then returns (and clears) the first
  * device-side error recorded by calls on it: SPEC_OK, SPEC_ERR_TOKEN_RANGE,
- * SPEC_ERR_PARENT, SPEC_ERR_TIMEOUT, or SPEC_ERR_CUDA for an asynchronous
+ * SPEC_ERR_PARENT, SPEC_ERR_TIMEOUT, SPEC_ERR_ARG (a lengths[] entry of
+ * spec_ngram_propose out of range), or SPEC_ERR_CUDA for an asynchronous
  * CUDA error.
  */
 int spec_get_status(void *stream);

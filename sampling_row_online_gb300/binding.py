@@ -55,6 +55,7 @@ def library():
     lib.spec_verify_tree.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, u64, i32, vp, vp, vp]
     lib.spec_tree_max_depth.argtypes = [vp, i32]
     lib.spec_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp]
+    lib.spec_ngram_propose.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.spec_get_status.argtypes = [vp]
     lib.spec_error_string.argtypes = [i32]
     lib.spec_error_string.restype = ctypes.c_char_p
@@ -63,7 +64,7 @@ def library():
     lib.spec_shutdown.argtypes = []
     lib.spec_shutdown.restype = None
     for name in ("spec_verify", "spec_verify_ex", "spec_verify_host", "spec_verify_tree_greedy",
-                 "spec_tree_max_depth", "spec_tree_mask", "spec_get_status"):
+                 "spec_tree_max_depth", "spec_tree_mask", "spec_ngram_propose", "spec_get_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -272,6 +273,36 @@ def spec_tree_mask(parent, *, stream=None):
         st = lib.spec_tree_mask(_ptr(parent), B, N, _ptr(mask), _ptr(depth), _stream(stream))
     _check(st, "spec_tree_mask")
     return mask, depth
+
+
+def spec_ngram_propose(tokens, lengths, n_min, n_max, K, *, min_hits=1, out_draft=None, out_count=None,
+                       stream=None):
+    """n-gram (prompt-lookup) drafts of B contexts.
+
+    tokens: [B, L] int32 CUDA tensor (row b's context in its first lengths[b]
+    entries); lengths: [B] int32.  Returns (draft [B, K] int32, -1 after the
+    proposal; count [B] int32, 0 = no match)."""
+    lib = library()
+    _dev(tokens, "tokens", torch.int32)
+    _dev(lengths, "lengths", torch.int32)
+    if tokens.dim() != 2:
+        raise ValueError("tokens must be [B, L]")
+    B, L = tokens.shape
+    if lengths.shape != (B,):
+        raise ValueError("lengths must be [B]")
+    if out_draft is None:
+        out_draft = torch.empty((B, K), dtype=torch.int32, device=tokens.device)
+    if out_count is None:
+        out_count = torch.empty((B,), dtype=torch.int32, device=tokens.device)
+    _dev(out_draft, "out_draft", torch.int32)
+    _dev(out_count, "out_count", torch.int32)
+    if out_draft.shape != (B, K) or out_count.shape != (B,):
+        raise ValueError("out_draft must be [B, K] and out_count [B]")
+    with torch.cuda.device(tokens.device):
+        st = lib.spec_ngram_propose(_ptr(tokens), _ptr(lengths), B, L, int(n_min), int(n_max), int(min_hits),
+                                    int(K), _ptr(out_draft), _ptr(out_count), _stream(stream))
+    _check(st, "spec_ngram_propose")
+    return out_draft, out_count
 
 
 def spec_get_status(stream=None) -> int:

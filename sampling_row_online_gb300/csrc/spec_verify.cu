@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "kernels.cuh"
+#include "ngram.cuh"
 #include "spec_verify.h"
 
 namespace spec {
@@ -49,6 +50,8 @@ struct Workspace {
   size_t cap_parts = 0;
   unsigned char *stage = nullptr;
   size_t stage_cap = 0;
+  int *ngram_done = nullptr;  // n-gram drafter: finished-CTA counters, zero between calls
+  size_t ngram_cap = 0;
 };
 
 std::mutex g_mu;
@@ -567,6 +570,71 @@ int spec_tree_mask(const int32_t *parent, int B, int N, uint32_t *out_mask, int3
   return SPEC_OK;
 }
 
+int spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int L, int n_min, int n_max,
+                       int min_hits, int K, int32_t *out_draft, int32_t *out_count, void *stream_ptr) {
+  if (B < 0 || L < 0) return fail(SPEC_ERR_ARG, "B and L must be >= 0");
+  if (n_min < 1 || n_max < n_min || n_max > SPEC_MAX_NGRAM)
+    return fail(SPEC_ERR_ARG, "need 1 <= n_min <= n_max <= 64");
+  if (min_hits < 1) return fail(SPEC_ERR_ARG, "min_hits must be >= 1");
+  if (K < 0 || K > SPEC_MAX_DRAFTS) return fail(SPEC_ERR_ARG, "K out of range [0, 255]");
+  if (B == 0) return SPEC_OK;
+  if (!lengths || !out_count || (K > 0 && !out_draft) || (L > 0 && !tokens))
+    return fail(SPEC_ERR_ARG, "NULL pointer");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int mode = min_hits == 1 ? NGRAM_MAXKEY
+                   : n_max - n_min < NGRAM_REG_BINS ? NGRAM_REGHIST : NGRAM_SMEMHIST;
+  // CTAs per sequence: about two waves of resident CTAs (3 per SM, 2 for
+  // the register histogram) over the batch, each with at least one round of
+  // loads (4096 positions)
+  const long long target = 2 * (mode == NGRAM_REGHIST ? 2LL : 3LL) * num_sms();
+  long long G = std::min<long long>((target + B - 1) / B, std::max(1, (L + 4095) / 4096));
+  G = env_int("SPEC_NGRAM_CTAS", static_cast<int>(std::max(1LL, G)), 1, 1 << 16);
+  if (static_cast<long long>(B) * G > INT_MAX) return fail(SPEC_ERR_ARG, "B too large");
+  const size_t part_bytes = static_cast<size_t>(B) * G *
+                            (mode == NGRAM_MAXKEY ? 8 : 8 * static_cast<size_t>(n_max - n_min + 1));
+  Workspace *w = nullptr;
+  int st = get_ws(stream, (part_bytes + 15) / 16, &w);
+  if (st) return st;
+  if (w->ngram_cap < static_cast<size_t>(B)) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    cudaError_t e;
+    if (w->ngram_done) {
+      e = cudaFree(w->ngram_done);  // synchronises the device: no call still uses it
+      w->ngram_done = nullptr;
+      w->ngram_cap = 0;
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFree(ngram counters)");
+    }
+    if ((e = cudaMalloc(&w->ngram_done, sizeof(int) * B)) != cudaSuccess)
+      return cuda_fail(e, "cudaMalloc(ngram counters)");
+    if ((e = cudaMemsetAsync(w->ngram_done, 0, sizeof(int) * B, stream)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemsetAsync(ngram counters)");
+    w->ngram_cap = B;
+  }
+  const bool vec = L % 4 == 0 && aligned16(tokens);
+  static const void *const fns[2][3] = {
+      {reinterpret_cast<const void *>(&ngram_kernel<false, NGRAM_MAXKEY>),
+       reinterpret_cast<const void *>(&ngram_kernel<false, NGRAM_REGHIST>),
+       reinterpret_cast<const void *>(&ngram_kernel<false, NGRAM_SMEMHIST>)},
+      {reinterpret_cast<const void *>(&ngram_kernel<true, NGRAM_MAXKEY>),
+       reinterpret_cast<const void *>(&ngram_kernel<true, NGRAM_REGHIST>),
+       reinterpret_cast<const void *>(&ngram_kernel<true, NGRAM_SMEMHIST>)}};
+  NgramParams p{tokens, lengths, B, L, n_min, n_max, min_hits, K, static_cast<int>(G), out_draft, out_count,
+                w->status, w->partials, w->ngram_done};
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(B * G), 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  void *args[] = {&p};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fns[vec][mode], args);
+  if (e != cudaSuccess) return cuda_fail(e, "ngram_kernel launch");
+  return SPEC_OK;
+}
+
 int spec_arm_rows_event(void *event) {
   g_rows_event = static_cast<cudaEvent_t>(event);
   return SPEC_OK;
@@ -591,6 +659,7 @@ int spec_get_status(void *stream_ptr) {
   if ((e = cudaMemset(w->status, 0, sizeof(int32_t))) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
   if (bits & ST_TIMEOUT) return fail(SPEC_ERR_TIMEOUT, "a bounded wait on the device ran out");
   if (bits & ST_PARENT) return fail(SPEC_ERR_PARENT, "parent[] is not a tree of the given depth");
+  if (bits & ST_LENGTH) return fail(SPEC_ERR_ARG, "lengths[b] outside [0, L]");
   return fail(SPEC_ERR_TOKEN_RANGE, "a draft or node token is outside [0, V)");
 }
 
@@ -675,6 +744,7 @@ void spec_shutdown(void) {
     if (w->status) cudaFree(w->status);
     if (w->partials) cudaFree(w->partials);
     if (w->stage) cudaFree(w->stage);
+    if (w->ngram_done) cudaFree(w->ngram_done);
     delete w;
   }
   g_ws.clear();

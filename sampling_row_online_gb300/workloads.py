@@ -25,6 +25,20 @@ c3    tree       32    63   128256   bf16   0     z_t ~ N(0, 3^2); static tree 4
 c4    chain      512   4    256000   f32    1.0   z_t = 1.5 * (-1.1 ln rank) + N(0, 1);
                                                   z_d = z_t + N(0, 1)
 ====  =========  ====  ===  =======  =====  ====  =======================================
+
+n-gram drafting contexts (``NGRAM_WORKLOADS``, ``make_contexts``): B rows of
+up to L tokens, lengths uniform in [L/2, L].  A row is a sequence of segments
+(geometric lengths, mean ``mean_seg``); a segment either holds fresh tokens
+(log-uniform ranks over V, i.e. Zipf with exponent 1) or, with probability
+``copy_frac``, repeats the span that starts d tokens earlier (d uniform over
+the positions before the segment), as when code or a cited source is edited.
+
+====  ===  =====  ===========  ========  ==
+name  B    L      n_min..n_max  min_hits  K
+====  ===  =====  ===========  ========  ==
+ng1   64   32768  1..4          1         5
+ng2   64   32768  8..8          2         5
+====  ===  =====  ===========  ========  ==
 """
 from __future__ import annotations
 
@@ -238,3 +252,62 @@ def input_copies_for_cold_l2(bytes_per_copy: int, l2_bytes: int = 129 * 2**20) -
     """Number of input copies to rotate so that consecutive calls never find
     their inputs in L2: the copies together exceed twice the L2 size."""
     return max(2, math.ceil(2 * l2_bytes / max(1, bytes_per_copy)) + 1)
+
+
+@dataclass(frozen=True)
+class NgramWorkload:
+    name: str
+    B: int
+    L: int               # row capacity: the longest context
+    n_min: int
+    n_max: int
+    min_hits: int
+    K: int
+    V: int = 128256
+    copy_frac: float = 0.5
+    mean_seg: int = 24
+    data_seed: int = 2000
+
+    @property
+    def context_bytes(self) -> int:
+        return self.B * self.L * 4
+
+
+NGRAM_WORKLOADS = {
+    # vLLM's n-gram settings on the pages: K = 5 speculative tokens, n-gram window up to 4
+    "ng1": NgramWorkload("ng1", B=64, L=32768, n_min=1, n_max=4, min_hits=1, K=5, data_seed=2001),
+    # llama.cpp's setting for text on the pages: n = 8, min-hits 2
+    "ng2": NgramWorkload("ng2", B=64, L=32768, n_min=8, n_max=8, min_hits=2, K=5, data_seed=2002),
+}
+
+
+def make_contexts(w: NgramWorkload, device="cpu", *, B=None, L=None, seed=None):
+    """(tokens [B, L] int32, lengths [B] int32) on ``device``; entries past a
+    row's length are filled too (with the same process), so that nothing
+    depends on them being ignored."""
+    B = w.B if B is None else B
+    L = w.L if L is None else L
+    g = _gen(device, w.data_seed if seed is None else seed)
+    if B == 0 or L == 0:
+        return (torch.zeros((B, L), dtype=torch.int32, device=device),
+                torch.zeros((B,), dtype=torch.int32, device=device))
+    u = torch.rand((B, L), generator=g, device=device, dtype=torch.float64)
+    fresh = torch.floor(torch.exp(u * math.log(w.V))).clamp_(1, w.V).long() - 1
+    pos = torch.arange(L, device=device).expand(B, L)
+    starts = torch.rand((B, L), generator=g, device=device) < 1.0 / w.mean_seg
+    starts[:, 0] = True
+    seg_start = torch.cummax(torch.where(starts, pos, torch.zeros_like(pos)), dim=1).values
+    u_copy = torch.rand((B, L), generator=g, device=device).gather(1, seg_start)
+    u_off = torch.rand((B, L), generator=g, device=device, dtype=torch.float64).gather(1, seg_start)
+    copy = (u_copy < w.copy_frac) & (seg_start > 0)
+    d = 1 + torch.floor(u_off * seg_start).long()           # 1 <= d <= seg_start
+    src = torch.where(copy, pos - d, pos)                  # src[i] < i on copied positions
+    root = src                                              # pointer jumping: reach doubles per step
+    while True:
+        nxt = root.gather(1, root)
+        if torch.equal(nxt, root):
+            break
+        root = nxt
+    tokens = fresh.gather(1, root).to(torch.int32).contiguous()
+    lengths = (L // 2 + torch.randint(0, L - L // 2 + 1, (B,), generator=g, device=device)).to(torch.int32)
+    return tokens, lengths

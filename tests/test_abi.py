@@ -27,7 +27,7 @@ def lib():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for required in ("spec_verify", "spec_verify_tree_greedy", "spec_verify_tree", "spec_verify_ex", "spec_verify_host",
-                     "spec_tree_max_depth", "spec_tree_mask", "spec_get_status",
+                     "spec_tree_max_depth", "spec_tree_mask", "spec_ngram_propose", "spec_get_status",
                      "spec_error_string", "spec_last_error_message", "spec_shutdown"):
         assert required in names
 
@@ -83,6 +83,22 @@ def test_tree_validation_without_gpu(lib):
     assert t(vp, None, vp, vp, 2, 5, 10, 1, 1.0, 0, 2, vp, vp, None) == 1                # no draft rows
     assert t(vp, vp, vp, vp, 2, 5, 10, 9, 1.0, 0, 2, vp, vp, None) == 2                  # dtype
     assert t(vp, vp, vp, vp, 0, 5, 10, 1, 1.0, 0, 2, vp, vp, None) == 0                  # empty
+
+
+def test_ngram_validation_without_gpu(lib):
+    vp = ctypes.c_void_p(16)
+    g = lib.spec_ngram_propose   # (tokens, lengths, B, L, n_min, n_max, min_hits, K, draft, count, stream)
+    assert g(vp, vp, 0, 10, 1, 4, 1, 5, vp, vp, None) == 0        # empty batch
+    assert g(vp, vp, -1, 10, 1, 4, 1, 5, vp, vp, None) == 1       # B < 0
+    assert g(vp, vp, 2, -1, 1, 4, 1, 5, vp, vp, None) == 1        # L < 0
+    assert g(vp, vp, 2, 10, 0, 4, 1, 5, vp, vp, None) == 1        # n_min < 1
+    assert g(vp, vp, 2, 10, 5, 4, 1, 5, vp, vp, None) == 1        # n_max < n_min
+    assert g(vp, vp, 2, 10, 1, 65, 1, 5, vp, vp, None) == 1       # n_max > 64
+    assert g(vp, vp, 2, 10, 1, 4, 0, 5, vp, vp, None) == 1        # min_hits < 1
+    assert g(vp, vp, 2, 10, 1, 4, 1, 256, vp, vp, None) == 1      # K > 255
+    assert g(vp, None, 2, 10, 1, 4, 1, 5, vp, vp, None) == 1      # no lengths
+    assert g(vp, vp, 2, 10, 1, 4, 1, 5, None, vp, None) == 1      # no draft output with K > 0
+    assert g(None, vp, 2, 10, 1, 4, 1, 5, vp, vp, None) == 1      # no tokens with L > 0
 
 
 @pytest.mark.parametrize("parent,depth", [([-1], 0), ([-1, 0, 0, 1, 2], 2),
