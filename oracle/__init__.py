@@ -62,6 +62,12 @@ def _load():
         lib.oracle_verify_tree_sample.restype = i32
         lib.oracle_ngram_propose.argtypes = [c_p, c_p, i32, i32, i32, i32, i32, i32, c_p, c_p]
         lib.oracle_ngram_propose.restype = i32
+        lib.oracle_topk_prob.argtypes = [c_p, i32, i32, i32, ctypes.c_double, i32, c_p, c_p]
+        lib.oracle_topk_prob.restype = i32
+        lib.oracle_eagle2_expand.argtypes = [c_p, i32, i32, i32, c_p, c_p, c_p, c_p, c_p, i32, i32, i32, c_p, c_p]
+        lib.oracle_eagle2_expand.restype = i32
+        lib.oracle_eagle2_rerank.argtypes = [c_p, c_p, c_p, i32, i32, i32, c_p, c_p, c_p, c_p]
+        lib.oracle_eagle2_rerank.restype = i32
         lib.oracle_max_threads.argtypes = []
         lib.oracle_max_threads.restype = i32
         _lib = lib
@@ -301,3 +307,61 @@ def ngram_propose(tokens, lengths, n_min: int, n_max: int, K: int, min_hits: int
     if st != OK:
         raise ValueError("oracle_ngram_propose: invalid arguments")
     return draft, count
+
+
+def topk_prob(z, k: int, T: float = 1.0):
+    """Per row of z [R, V] (or [..., V]): the k tokens of largest logit (ties:
+    lower index first) and their probabilities under softmax(z / T).
+    Returns (tokens [R, k] int32, prob [R, k] float64)."""
+    a, dt = _logits(z)
+    V = a.shape[-1]
+    R = int(a.size // V) if V else 0
+    tok = np.zeros((R, k), dtype=np.int32)
+    prob = np.zeros((R, k), dtype=np.float64)
+    st = _load().oracle_topk_prob(_ptr(a), R, V, dt, float(T), int(k), _ptr(tok), _ptr(prob))
+    if st != OK:
+        raise ValueError("oracle_topk_prob: invalid arguments")
+    return tok, prob
+
+
+def eagle2_expand(frontier, topk_tok, topk_prob_, node_tok, node_val, node_par, offset: int, k_next: int):
+    """One expansion step (updates the node arrays [B, cap] in place).
+    frontier [B, F] node ids; topk_tok / topk_prob_ [B, F, k].  Returns
+    (next frontier [B, k_next] node ids, near [B] bool)."""
+    fr = _i32(frontier)
+    B, F = fr.shape
+    tt = _i32(topk_tok).reshape(B, F, -1)
+    k = tt.shape[2]
+    tp = np.ascontiguousarray(topk_prob_, dtype=np.float64).reshape(B, F, k)
+    for arr, dt in ((node_tok, np.int32), (node_val, np.float64), (node_par, np.int32)):
+        if not (isinstance(arr, np.ndarray) and arr.dtype == dt and arr.flags.c_contiguous):
+            raise TypeError("node arrays must be contiguous numpy arrays (int32, float64, int32)")
+    cap = node_tok.shape[1]
+    out = np.zeros((B, k_next), dtype=np.int32)
+    near = np.zeros(B, dtype=np.uint8)
+    st = _load().oracle_eagle2_expand(_ptr(fr), B, F, k, _ptr(tt), _ptr(tp), _ptr(node_tok), _ptr(node_val),
+                                      _ptr(node_par), cap, int(offset), int(k_next), _ptr(out), _ptr(near))
+    if st != OK:
+        raise ValueError("oracle_eagle2_expand: invalid arguments")
+    return out, near.astype(bool)
+
+
+def eagle2_rerank(node_val, node_par, node_tok, m: int):
+    """Keep the root and the m best nodes of each of B trees [B, M].  Returns
+    (parent [B, m+1] as list positions, tokens [B, m+1], node ids [B, m+1],
+    near [B] bool)."""
+    val = np.ascontiguousarray(node_val, dtype=np.float64)
+    par = _i32(node_par)
+    tok = _i32(node_tok)
+    B, M = val.shape
+    op = np.zeros((B, m + 1), dtype=np.int32)
+    ot = np.zeros((B, m + 1), dtype=np.int32)
+    oi = np.zeros((B, m + 1), dtype=np.int32)
+    near = np.zeros(B, dtype=np.uint8)
+    st = _load().oracle_eagle2_rerank(_ptr(val), _ptr(par), _ptr(tok), B, M, int(m), _ptr(op), _ptr(ot),
+                                      _ptr(oi), _ptr(near))
+    if st == ERR_PARENT:
+        raise ValueError("oracle_eagle2_rerank: malformed tree or a kept node's parent was dropped")
+    if st != OK:
+        raise ValueError("oracle_eagle2_rerank: invalid arguments")
+    return op, ot, oi, near.astype(bool)

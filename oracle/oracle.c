@@ -702,6 +702,204 @@ int oracle_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B,
   return ORC_OK;
 }
 
+/* ------------------------------------------------------------------ */
+/* EAGLE-2 tree budget ([Infra53] §5.1-§5.3: the draft's confidence     */
+/* decides where a limited node budget goes; a node's value is the       */
+/* product of the confidences on its path from the root; an expansion    */
+/* phase grows the few best nodes, a rerank phase keeps the best nodes   */
+/* of all for verification).  Readings taken: a confidence is the        */
+/* draft's probability of the token, softmax(z / T) of the draft row at  */
+/* the parent; every frontier node offers its k most probable tokens as  */
+/* candidates; the k_next candidates of highest value become the next    */
+/* frontier; the rerank keeps the root and the m highest-valued nodes of  */
+/* all candidates.                                                        */
+/* ------------------------------------------------------------------ */
+
+/* Top-k of each of R rows by logit (ties: lower index first), with each
+ * token's probability under softmax(z / T).  Plain selection: k passes,
+ * each taking the largest logit not taken yet. */
+int oracle_topk_prob(const void *z, int R, int V, int dtype, double T, int k,
+                     int32_t *out_tok, double *out_prob) {
+  if (R < 0 || V < 1 || k < 1 || k > V || !(T > 0.0)) return ORC_ERR_ARG;
+  unsigned char *taken = (unsigned char *)malloc((size_t)V);
+  if (!taken) return ORC_ERR_ARG;
+  for (int r = 0; r < R; ++r) {
+    const void *row = row_ptr(z, dtype, r, V);
+    double m, S;
+    oracle_row_stats(row, dtype, V, T, &m, &S);
+    memset(taken, 0, (size_t)V);
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      double bv = 0.0;
+      for (int v = 0; v < V; ++v) {
+        if (taken[v]) continue;
+        double x = logit_at(row, dtype, v);
+        if (best < 0 || x > bv) {
+          best = v;
+          bv = x;
+        }
+      }
+      taken[best] = 1;
+      out_tok[(size_t)r * k + j] = best;
+      out_prob[(size_t)r * k + j] = prob_at(row, dtype, best, T, m, S);
+    }
+  }
+  free(taken);
+  return ORC_OK;
+}
+
+/* Does candidate a rank above candidate b: higher value, ties to the
+ * lower index. */
+static int ranks_above(double va, int ia, double vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+static int near_gap(double a, double b) {
+  double hi = fabs(a) > fabs(b) ? fabs(a) : fabs(b);
+  return fabs(a - b) <= 1e-5 * hi;
+}
+
+/* One expansion step for B trees.  Node arrays per tree ([B, cap]):
+ * node_tok, node_val, node_par.  frontier [B, F] holds node ids; the
+ * candidates of frontier node f are written to nodes offset + f*k + j
+ * (j = 0..k-1, the row's top-k in order) with value
+ * node_val[frontier] * prob and parent frontier.  out_next [B, k_next]
+ * receives the k_next new candidates of highest value (ties: lower node
+ * id), best first.  out_near[b] flags a selection boundary where the
+ * k_next-th and the next value lie within 1e-5 (relative). */
+int oracle_eagle2_expand(const int32_t *frontier, int B, int F, int k,
+                         const int32_t *topk_tok, const double *topk_prob,
+                         int32_t *node_tok, double *node_val, int32_t *node_par,
+                         int cap, int offset, int k_next, int32_t *out_next,
+                         uint8_t *out_near) {
+  if (B < 0 || F < 1 || k < 1 || offset < 1 || offset + F * k > cap ||
+      k_next < 0 || k_next > F * k)
+    return ORC_ERR_ARG;
+  int n = F * k;
+  unsigned char *taken = (unsigned char *)malloc((size_t)n);
+  if (!taken) return ORC_ERR_ARG;
+  for (int b = 0; b < B; ++b) {
+    int32_t *tok = node_tok + (size_t)b * cap;
+    double *val = node_val + (size_t)b * cap;
+    int32_t *par = node_par + (size_t)b * cap;
+    for (int f = 0; f < F; ++f) {
+      int u = frontier[(size_t)b * F + f];
+      if (u < 0 || u >= offset) {
+        free(taken);
+        return ORC_ERR_ARG;
+      }
+      for (int j = 0; j < k; ++j) {
+        int c = offset + f * k + j;
+        tok[c] = topk_tok[((size_t)b * F + f) * k + j];
+        val[c] = val[u] * topk_prob[((size_t)b * F + f) * k + j];
+        par[c] = u;
+      }
+    }
+    memset(taken, 0, (size_t)n);
+    double last = 0.0;
+    for (int s = 0; s < k_next; ++s) {
+      int best = -1;
+      for (int i = 0; i < n; ++i)
+        if (!taken[i] && (best < 0 || ranks_above(val[offset + i], i, val[offset + best], best)))
+          best = i;
+      taken[best] = 1;
+      out_next[(size_t)b * k_next + s] = offset + best;
+      last = val[offset + best];
+    }
+    out_near[b] = 0;
+    if (k_next > 0 && k_next < n) {
+      for (int i = 0; i < n; ++i)
+        if (!taken[i] && near_gap(val[offset + i], last)) out_near[b] = 1;
+    }
+  }
+  free(taken);
+  return ORC_OK;
+}
+
+/* Rerank for B trees of M nodes (node 0 the root, parent[c] < c): keep
+ * the root and the m other nodes of highest value, ties to the smaller
+ * depth, then the lower node id.  A child's value never exceeds its
+ * parent's (a probability is at most 1), so the kept set holds every
+ * ancestor of a kept node.  The kept nodes are listed by depth, then in
+ * rank order; out_par holds parents as positions in that list (-1 for the
+ * root), out_tok their tokens, out_idx their node ids.  out_near[b] flags
+ * a boundary where the m-th kept value and a dropped one lie within 1e-5.
+ * Returns ORC_ERR_PARENT if a tree is malformed or a kept node's parent
+ * was dropped (values that grow along a path). */
+int oracle_eagle2_rerank(const double *node_val, const int32_t *node_par,
+                         const int32_t *node_tok, int B, int M, int m,
+                         int32_t *out_par, int32_t *out_tok, int32_t *out_idx,
+                         uint8_t *out_near) {
+  if (B < 0 || M < 1 || m < 0 || m > M - 1) return ORC_ERR_ARG;
+  int *depth = (int *)malloc(sizeof(int) * (size_t)M);
+  int *rank_of = (int *)malloc(sizeof(int) * (size_t)M);
+  int *order = (int *)malloc(sizeof(int) * (size_t)M);
+  int *pos = (int *)malloc(sizeof(int) * (size_t)M);
+  if (!depth || !rank_of || !order || !pos) {
+    free(depth); free(rank_of); free(order); free(pos);
+    return ORC_ERR_ARG;
+  }
+  int status = ORC_OK;
+  for (int b = 0; b < B && status == ORC_OK; ++b) {
+    const double *val = node_val + (size_t)b * M;
+    const int32_t *par = node_par + (size_t)b * M;
+    const int32_t *tok = node_tok + (size_t)b * M;
+    if (par[0] != -1) { status = ORC_ERR_PARENT; break; }
+    depth[0] = 0;
+    for (int c = 1; c < M; ++c) {
+      if (par[c] < 0 || par[c] >= c) { status = ORC_ERR_PARENT; break; }
+      depth[c] = depth[par[c]] + 1;
+    }
+    if (status != ORC_OK) break;
+    /* selection: rank r = the r-th best non-root node */
+    for (int c = 0; c < M; ++c) rank_of[c] = -1;
+    double last = 0.0;
+    for (int r = 0; r < m; ++r) {
+      int best = -1;
+      for (int c = 1; c < M; ++c) {
+        if (rank_of[c] >= 0) continue;
+        if (best < 0 || val[c] > val[best] ||
+            (val[c] == val[best] && (depth[c] < depth[best] ||
+                                     (depth[c] == depth[best] && c < best))))
+          best = c;
+      }
+      rank_of[best] = r;
+      last = val[best];
+    }
+    out_near[b] = 0;
+    if (m > 0)
+      for (int c = 1; c < M; ++c)
+        if (rank_of[c] < 0 && near_gap(val[c], last)) out_near[b] = 1;
+    /* listing: root, then by depth, then by rank */
+    int n = 0;
+    order[n++] = 0;
+    int maxd = 0;
+    for (int c = 1; c < M; ++c) if (depth[c] > maxd) maxd = depth[c];
+    for (int d = 1; d <= maxd; ++d)
+      for (int r = 0; r < m; ++r)
+        for (int c = 1; c < M; ++c)
+          if (rank_of[c] == r && depth[c] == d) order[n++] = c;
+    for (int c = 0; c < M; ++c) pos[c] = -1;
+    for (int i = 0; i < n; ++i) pos[order[i]] = i;
+    int32_t *op = out_par + (size_t)b * (m + 1);
+    int32_t *ot = out_tok + (size_t)b * (m + 1);
+    int32_t *oi = out_idx + (size_t)b * (m + 1);
+    for (int i = 0; i < n; ++i) {
+      int c = order[i];
+      oi[i] = c;
+      ot[i] = tok[c];
+      if (c == 0) {
+        op[i] = -1;
+      } else {
+        op[i] = pos[par[c]];
+        if (op[i] < 0) status = ORC_ERR_PARENT;
+      }
+    }
+  }
+  free(depth); free(rank_of); free(order); free(pos);
+  return status;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
