@@ -70,6 +70,9 @@ enum { SPEC_F32 = 0, SPEC_BF16 = 1 };
 #define SPEC_MAX_DRAFTS 255      /* K of a chain */
 #define SPEC_MAX_TREE_NODES 1024 /* N of a tree */
 #define SPEC_MAX_NGRAM 64        /* n_max of the n-gram drafter */
+#define SPEC_MAX_TOPK 32         /* k of spec_topk / spec_eagle2_expand */
+#define SPEC_EAGLE_MAX_CANDIDATES 4096 /* F * k of one expansion step */
+#define SPEC_EAGLE_MAX_NODES 8192      /* M of spec_eagle2_rerank */
 
 /* Counters a caller may ask spec_verify_ex to accumulate (device memory,
  * zeroed by the caller, added to atomically by every call that receives it).
@@ -296,6 +299,67 @@ int spec_tree_mask(const int32_t *parent, int B, int N, uint32_t *out_mask,
 int spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int L, int n_min,
                        int n_max, int min_hits, int K, int32_t *out_draft, int32_t *out_count,
                        void *stream);
+
+/*
+ * spec_topk — the k most probable tokens of each of R rows and their
+ * probabilities under softmax(z / T): the confidences of the EAGLE-2 tree
+ * budget ([Infra53] §5.1-§5.2: the draft's confidence decides where the
+ * node budget goes).
+ *   logits      [R, V] SPEC_F32 or SPEC_BF16 (device)
+ *   1 <= k <= min(V, SPEC_MAX_TOPK), T > 0
+ *   out_tokens  [R, k] int32 (device): by decreasing logit, ties to the
+ *               lower index
+ *   out_prob    [R, k] float (device): softmax(z / T) of those tokens
+ * Rows must hold one finite logit (-inf entries allowed).
+ */
+int spec_topk(const void *logits, int R, int V, int dtype, float temperature, int k,
+              int32_t *out_tokens, float *out_prob, void *stream);
+
+/*
+ * spec_eagle2_expand — one expansion step of the EAGLE-2 tree budget for B
+ * trees ([Infra53] §5.2: a node's value is the product of the confidences on
+ * its path; the expansion phase grows the few best nodes).  Reading taken:
+ * each frontier node offers its k most probable tokens (spec_topk of the
+ * draft's row at that node) as candidates; a candidate's value is its
+ * parent's value times its probability; the k_next candidates of highest
+ * value (ties to the lower node id) become the next frontier.
+ *   draft_logits  [B, F, V] (device): the draft's logits at the frontier
+ *   frontier      [B, F] int32 (device): node ids in [0, offset)
+ *   node_tokens, node_values, node_parents  [B, cap] int32 / float / int32
+ *                 (device, caller-owned tree state): node 0 is the root (the
+ *                 caller sets value 1, parent -1 and its token); the step
+ *                 writes the F * k candidates to nodes offset + f * k + j
+ *                 (j = 0..k-1 in decreasing probability), offset >= 1,
+ *                 offset + F * k <= cap, F * k <= SPEC_EAGLE_MAX_CANDIDATES
+ *   out_frontier  [B, k_next] int32 (device): node ids, best first
+ *                 (0 <= k_next <= F * k)
+ * A frontier id outside [0, offset) makes spec_get_status return
+ * SPEC_ERR_PARENT and that tree's out_frontier -1.  Two launches.
+ */
+int spec_eagle2_expand(const void *draft_logits, const int32_t *frontier, int B, int F, int V,
+                       int dtype, float temperature, int k, int32_t *node_tokens,
+                       float *node_values, int32_t *node_parents, int cap, int offset, int k_next,
+                       int32_t *out_frontier, void *stream);
+
+/*
+ * spec_eagle2_rerank — the rerank phase ([Infra53] §5.2: keep the best
+ * nodes of all for verification).  For each of B trees of M nodes (arrays
+ * [B, M] as written by spec_eagle2_expand; parent[0] = -1, parent[c] < c):
+ * keeps the root and the m other nodes of highest value, ties to the
+ * smaller depth, then the lower id (depth < 256).  A child's value never
+ * exceeds its parent's, so the kept set holds every ancestor of a kept node.
+ *   out_parent  [B, m + 1] int32 (device): parents as list positions (-1
+ *               for the root); the list is the root, then the kept nodes by
+ *               depth, then by rank, so parent[c] < c (ready for
+ *               spec_tree_mask and the tree verification)
+ *   out_tokens  [B, m + 1] int32: their tokens; out_index [B, m + 1]: node ids
+ * 1 <= M <= SPEC_EAGLE_MAX_NODES, 0 <= m <= M - 1.  A malformed tree, or a
+ * kept node whose parent was dropped, makes spec_get_status return
+ * SPEC_ERR_PARENT and that tree's outputs -1.
+ */
+int spec_eagle2_rerank(const float *node_values, const int32_t *node_parents,
+                       const int32_t *node_tokens, int B, int M, int m, int32_t *out_parent,
+                       int32_t *out_tokens, int32_t *out_index, void *stream);
 
 /*
  * spec_get_status — waits for `stream`, then returns (and clears) the first

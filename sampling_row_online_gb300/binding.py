@@ -56,6 +56,9 @@ def library():
     lib.spec_tree_max_depth.argtypes = [vp, i32]
     lib.spec_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp]
     lib.spec_ngram_propose.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.spec_topk.argtypes = [vp, i32, i32, i32, f32, i32, vp, vp, vp]
+    lib.spec_eagle2_expand.argtypes = [vp, vp, i32, i32, i32, i32, f32, i32, vp, vp, vp, i32, i32, i32, vp, vp]
+    lib.spec_eagle2_rerank.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
     lib.spec_get_status.argtypes = [vp]
     lib.spec_error_string.argtypes = [i32]
     lib.spec_error_string.restype = ctypes.c_char_p
@@ -64,7 +67,8 @@ def library():
     lib.spec_shutdown.argtypes = []
     lib.spec_shutdown.restype = None
     for name in ("spec_verify", "spec_verify_ex", "spec_verify_host", "spec_verify_tree_greedy",
-                 "spec_tree_max_depth", "spec_tree_mask", "spec_ngram_propose", "spec_get_status"):
+                 "spec_tree_max_depth", "spec_tree_mask", "spec_ngram_propose", "spec_topk",
+                 "spec_eagle2_expand", "spec_eagle2_rerank", "spec_get_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -303,6 +307,72 @@ def spec_ngram_propose(tokens, lengths, n_min, n_max, K, *, min_hits=1, out_draf
                                     int(K), _ptr(out_draft), _ptr(out_count), _stream(stream))
     _check(st, "spec_ngram_propose")
     return out_draft, out_count
+
+
+def spec_topk(logits, k, temperature=1.0, *, out_tokens=None, out_prob=None, stream=None):
+    """Top-k tokens of each row of logits [..., V] (ties to the lower index)
+    and their probabilities under softmax(z / T).  Returns (tokens [R, k]
+    int32, prob [R, k] float32) with R the number of rows."""
+    lib = library()
+    _dev(logits, "logits")
+    V = logits.shape[-1]
+    R = logits.numel() // V if V else 0
+    if out_tokens is None:
+        out_tokens = torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    if out_prob is None:
+        out_prob = torch.empty((R, k), dtype=torch.float32, device=logits.device)
+    with torch.cuda.device(logits.device):
+        st = lib.spec_topk(_ptr(logits), R, V, _dtype_code(logits), float(temperature), int(k), _ptr(out_tokens),
+                           _ptr(out_prob), _stream(stream))
+    _check(st, "spec_topk")
+    return out_tokens, out_prob
+
+
+def spec_eagle2_expand(draft_logits, frontier, node_tokens, node_values, node_parents, k, offset, k_next,
+                       temperature=1.0, *, out_frontier=None, stream=None):
+    """One EAGLE-2 expansion step.  draft_logits [B, F, V]; frontier [B, F]
+    int32 node ids; node arrays [B, cap] (int32 tokens, float32 values, int32
+    parents; node 0 the root), updated in place at nodes offset ..
+    offset + F*k - 1.  Returns the next frontier [B, k_next] int32."""
+    lib = library()
+    _dev(draft_logits, "draft_logits")
+    _dev(frontier, "frontier", torch.int32)
+    _dev(node_tokens, "node_tokens", torch.int32)
+    _dev(node_values, "node_values", torch.float32)
+    _dev(node_parents, "node_parents", torch.int32)
+    if draft_logits.dim() != 3:
+        raise ValueError("draft_logits must be [B, F, V]")
+    B, F, V = draft_logits.shape
+    cap = node_tokens.shape[1]
+    if frontier.shape != (B, F) or node_values.shape != (B, cap) or node_parents.shape != (B, cap):
+        raise ValueError("frontier must be [B, F] and the node arrays [B, cap]")
+    if out_frontier is None:
+        out_frontier = torch.empty((B, k_next), dtype=torch.int32, device=draft_logits.device)
+    with torch.cuda.device(draft_logits.device):
+        st = lib.spec_eagle2_expand(_ptr(draft_logits), _ptr(frontier), B, F, V, _dtype_code(draft_logits),
+                                    float(temperature), int(k), _ptr(node_tokens), _ptr(node_values),
+                                    _ptr(node_parents), cap, int(offset), int(k_next), _ptr(out_frontier),
+                                    _stream(stream))
+    _check(st, "spec_eagle2_expand")
+    return out_frontier
+
+
+def spec_eagle2_rerank(node_values, node_parents, node_tokens, m, *, stream=None):
+    """EAGLE-2 rerank of B trees [B, M]: the root and the m best nodes listed
+    by depth.  Returns (parent [B, m+1] list positions, tokens [B, m+1],
+    node ids [B, m+1]), all int32."""
+    lib = library()
+    _dev(node_values, "node_values", torch.float32)
+    _dev(node_parents, "node_parents", torch.int32)
+    _dev(node_tokens, "node_tokens", torch.int32)
+    B, M = node_values.shape
+    dev = node_values.device
+    out = [torch.empty((B, m + 1), dtype=torch.int32, device=dev) for _ in range(3)]
+    with torch.cuda.device(dev):
+        st = lib.spec_eagle2_rerank(_ptr(node_values), _ptr(node_parents), _ptr(node_tokens), B, M, int(m),
+                                    _ptr(out[0]), _ptr(out[1]), _ptr(out[2]), _stream(stream))
+    _check(st, "spec_eagle2_rerank")
+    return tuple(out)
 
 
 def spec_get_status(stream=None) -> int:

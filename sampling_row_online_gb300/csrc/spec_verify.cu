@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "kernels.cuh"
+#include "eagle2.cuh"
 #include "ngram.cuh"
 #include "spec_verify.h"
 
@@ -455,6 +456,63 @@ int tree_depth_host(const int32_t *parent, int N) {
   return D;
 }
 
+
+// ------------------------------------------------------------ EAGLE-2
+template <int DT, bool VEC>
+const void *pick_topk(int kmax) {
+  if (kmax <= 8) return reinterpret_cast<const void *>(&topk_kernel<DT, VEC, 8>);
+  if (kmax <= 16) return reinterpret_cast<const void *>(&topk_kernel<DT, VEC, 16>);
+  return reinterpret_cast<const void *>(&topk_kernel<DT, VEC, 32>);
+}
+
+int check_topk_args(int R, int V, int dtype, float T, int k) {
+  if (dtype != SPEC_F32 && dtype != SPEC_BF16) return fail(SPEC_ERR_DTYPE, "dtype must be SPEC_F32 or SPEC_BF16");
+  if (R < 0) return fail(SPEC_ERR_ARG, "row count must be >= 0");
+  if (V < 1) return fail(SPEC_ERR_ARG, "V must be >= 1");
+  if (k < 1 || k > SPEC_MAX_TOPK || k > V) return fail(SPEC_ERR_ARG, "need 1 <= k <= min(V, 32)");
+  if (!(T > 0.f) || !std::isfinite(T)) return fail(SPEC_ERR_ARG, "temperature must be finite and > 0");
+  const double c = 1.4426950408889634 / static_cast<double>(T);
+  if (!(c < 1e30)) return fail(SPEC_ERR_ARG, "temperature too small");
+  return SPEC_OK;
+}
+
+// One launch of the top-k kernel (a programmatic dependent of earlier work).
+int launch_topk(TopkParams &p, int dtype, cudaStream_t stream) {
+  const size_t esz = dtype == SPEC_F32 ? 4 : 2;
+  const bool vec = aligned16(p.z) && (static_cast<size_t>(p.V) * esz) % 16 == 0;
+  const void *fn = dtype == SPEC_F32 ? (vec ? pick_topk<0, true>(p.k) : pick_topk<0, false>(p.k))
+                                     : (vec ? pick_topk<1, true>(p.k) : pick_topk<1, false>(p.k));
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.R), 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  void *args[] = {&p};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) return cuda_fail(e, "topk_kernel launch");
+  return SPEC_OK;
+}
+
+int launch_eagle(const void *fn, EagleParams &p, int grid, int smem, cudaStream_t stream, const char *what) {
+  cudaLaunchAttribute pdl;
+  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = &pdl;
+  cfg.numAttrs = 1;
+  void *args[] = {&p};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) return cuda_fail(e, what);
+  return SPEC_OK;
+}
 }  // namespace
 }  // namespace spec
 
@@ -633,6 +691,112 @@ int spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int
   cudaError_t e = cudaLaunchKernelExC(&cfg, fns[vec][mode], args);
   if (e != cudaSuccess) return cuda_fail(e, "ngram_kernel launch");
   return SPEC_OK;
+}
+
+int spec_topk(const void *logits, int R, int V, int dtype, float temperature, int k, int32_t *out_tokens,
+              float *out_prob, void *stream_ptr) {
+  int st = check_topk_args(R, V, dtype, temperature, k);
+  if (st) return st;
+  if (R == 0) return SPEC_OK;
+  if (!logits || !out_tokens || !out_prob) return fail(SPEC_ERR_ARG, "NULL pointer");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  Workspace *w = nullptr;
+  if ((st = get_ws(stream, 1, &w))) return st;
+  TopkParams p{};
+  p.z = logits;
+  p.R = R;
+  p.V = V;
+  p.k = k;
+  p.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  p.out_tok = out_tokens;
+  p.out_prob = out_prob;
+  p.F = 0;
+  p.status = w->status;
+  return launch_topk(p, dtype, stream);
+}
+
+int spec_eagle2_expand(const void *draft_logits, const int32_t *frontier, int B, int F, int V, int dtype,
+                       float temperature, int k, int32_t *node_tokens, float *node_values, int32_t *node_parents,
+                       int cap, int offset, int k_next, int32_t *out_frontier, void *stream_ptr) {
+  if (B < 0 || F < 1) return fail(SPEC_ERR_ARG, "need B >= 0 and F >= 1");
+  int st = check_topk_args(B, V, dtype, temperature, k);
+  if (st) return st;
+  if (static_cast<long long>(F) * k > SPEC_EAGLE_MAX_CANDIDATES)
+    return fail(SPEC_ERR_ARG, "F * k above 4096");
+  if (offset < 1 || static_cast<long long>(offset) + static_cast<long long>(F) * k > cap)
+    return fail(SPEC_ERR_ARG, "need 1 <= offset and offset + F * k <= cap");
+  if (k_next < 0 || k_next > F * k) return fail(SPEC_ERR_ARG, "need 0 <= k_next <= F * k");
+  if (static_cast<long long>(B) * F > INT_MAX || static_cast<long long>(B) * cap > (1LL << 40))
+    return fail(SPEC_ERR_ARG, "B * F too large");
+  if (B == 0) return SPEC_OK;
+  if (!draft_logits || !frontier || !node_tokens || !node_values || !node_parents ||
+      (k_next > 0 && !out_frontier))
+    return fail(SPEC_ERR_ARG, "NULL pointer");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  Workspace *w = nullptr;
+  if ((st = get_ws(stream, 1, &w))) return st;
+  TopkParams tp{};
+  tp.z = draft_logits;
+  tp.R = B * F;
+  tp.V = V;
+  tp.k = k;
+  tp.c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+  tp.out_tok = node_tokens;
+  tp.out_prob = node_values;
+  tp.F = F;
+  tp.cap = cap;
+  tp.offset = offset;
+  tp.frontier = frontier;
+  tp.node_par = node_parents;
+  tp.status = w->status;
+  if ((st = launch_topk(tp, dtype, stream))) return st;
+  EagleParams ep{};
+  ep.B = B;
+  ep.F = F;
+  ep.k = k;
+  ep.cap = cap;
+  ep.offset = offset;
+  ep.k_next = k_next;
+  ep.frontier = frontier;
+  ep.node_tok = node_tokens;
+  ep.node_val = node_values;
+  ep.node_par = node_parents;
+  ep.out_next = out_frontier;
+  ep.status = w->status;
+  return launch_eagle(reinterpret_cast<const void *>(&expand_select_kernel), ep, B, 0, stream,
+                      "expand_select_kernel launch");
+}
+
+int spec_eagle2_rerank(const float *node_values, const int32_t *node_parents, const int32_t *node_tokens, int B,
+                       int M, int m, int32_t *out_parent, int32_t *out_tokens, int32_t *out_index,
+                       void *stream_ptr) {
+  if (B < 0) return fail(SPEC_ERR_ARG, "B must be >= 0");
+  if (M < 1 || M > SPEC_EAGLE_MAX_NODES) return fail(SPEC_ERR_ARG, "M out of range [1, 8192]");
+  if (m < 0 || m > M - 1) return fail(SPEC_ERR_ARG, "need 0 <= m <= M - 1");
+  if (B == 0) return SPEC_OK;
+  if (!node_values || !node_parents || !node_tokens || !out_parent || !out_tokens || !out_index)
+    return fail(SPEC_ERR_ARG, "NULL pointer");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  Workspace *w = nullptr;
+  int st = get_ws(stream, 1, &w);
+  if (st) return st;
+  const void *fn = reinterpret_cast<const void *>(&rerank_kernel);
+  const int smem = 16 * M + 4 * m;
+  int per_sm = 0;
+  if ((st = occupancy(fn, smem, 0, &per_sm))) return st;
+  if (per_sm < 1) return fail(SPEC_ERR_UNSUPPORTED, "rerank kernel does not fit on an SM");
+  EagleParams ep{};
+  ep.B = B;
+  ep.M = M;
+  ep.m = m;
+  ep.node_tok = const_cast<int32_t *>(node_tokens);
+  ep.node_val = const_cast<float *>(node_values);
+  ep.node_par = const_cast<int32_t *>(node_parents);
+  ep.out_par = out_parent;
+  ep.out_tok = out_tokens;
+  ep.out_idx = out_index;
+  ep.status = w->status;
+  return launch_eagle(fn, ep, B, smem, stream, "rerank_kernel launch");
 }
 
 int spec_arm_rows_event(void *event) {

@@ -39,6 +39,12 @@ name  B    L      n_min..n_max  min_hits  K
 ng1   64   32768  1..4          1         5
 ng2   64   32768  8..8          2         5
 ====  ===  =====  ===========  ========  ==
+
+EAGLE-2 tree budget (``EAGLE2_WORKLOADS``): a stand-in draft model whose
+logits at a node are sigma * N(0, 1) over V from a generator seeded by the
+node's token path (``node_key``), so that any two callers that reach the same
+node see the same row; ``eagle2_step_rows`` gives the bench its per-step row
+tensors directly.
 """
 from __future__ import annotations
 
@@ -311,3 +317,76 @@ def make_contexts(w: NgramWorkload, device="cpu", *, B=None, L=None, seed=None):
     tokens = fresh.gather(1, root).to(torch.int32).contiguous()
     lengths = (L // 2 + torch.randint(0, L - L // 2 + 1, (B,), generator=g, device=device)).to(torch.int32)
     return tokens, lengths
+
+
+@dataclass(frozen=True)
+class Eagle2Workload:
+    name: str
+    B: int
+    V: int
+    dtype: str
+    T: float
+    k: int               # candidates per frontier node = nodes expanded per step
+    depth: int           # expansion steps
+    m: int               # nodes kept by the rerank beside the root
+    sigma: float = 3.0
+    data_seed: int = 3000
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    @property
+    def M(self) -> int:
+        """Nodes of a fully grown tree: the root, k at the first step, k*k after."""
+        return 1 + self.k + (self.depth - 1) * self.k * self.k
+
+    def frontier_size(self, step: int) -> int:
+        return 1 if step == 0 else self.k
+
+    def offset(self, step: int) -> int:
+        return 1 if step == 0 else 1 + self.k + (step - 1) * self.k * self.k
+
+
+EAGLE2_WORKLOADS = {
+    # the node budget of the static tree workload (63 nodes, depth 5) spent
+    # dynamically: 8 candidates per node, 8 nodes grown per step
+    "eg1": Eagle2Workload("eg1", B=32, V=128256, dtype="bf16", T=1.0, k=8, depth=5, m=62, data_seed=3001),
+}
+
+_MASK63 = (1 << 63) - 1
+
+
+def _mix64(x: int) -> int:
+    """splitmix64 finaliser (Steele, Lea and Flood, OOPSLA 2014), 63 bits out."""
+    x &= (1 << 64) - 1
+    x = (x + 0x9E3779B97F4A7C15) & ((1 << 64) - 1)
+    x = ((x ^ (x >> 30)) * 0xBF58476D1CE4E5B9) & ((1 << 64) - 1)
+    x = ((x ^ (x >> 27)) * 0x94D049BB133111EB) & ((1 << 64) - 1)
+    return (x ^ (x >> 31)) & _MASK63
+
+
+def root_key(w: Eagle2Workload, b: int) -> int:
+    return _mix64(w.data_seed * 1000003 + b)
+
+
+def node_key(parent_key: int, token: int) -> int:
+    return _mix64(parent_key * 31 + token + 1)
+
+
+def draft_rows(w: Eagle2Workload, keys, device="cpu"):
+    """The stand-in draft's logits at the nodes with these path keys: [len(keys), V]."""
+    out = torch.empty((len(keys), w.V), dtype=torch.float32)
+    g = torch.Generator(device="cpu")
+    for i, key in enumerate(keys):
+        g.manual_seed(int(key))
+        out[i] = torch.randn(w.V, generator=g) * w.sigma
+    return out.to(w.torch_dtype).to(device)
+
+
+def eagle2_step_rows(w: Eagle2Workload, step: int, device="cpu"):
+    """Per-step draft rows [B, F, V] for timing (fresh seeded noise; the row
+    of a frontier slot does not follow a path)."""
+    g = _gen(device, w.data_seed + 7 * step + 1)
+    F = w.frontier_size(step)
+    return (torch.randn((w.B, F, w.V), generator=g, device=device) * w.sigma).to(w.torch_dtype)

@@ -27,7 +27,8 @@ def lib():
 def test_header_declares_the_boundary():
     names = _declared_functions()
     for required in ("spec_verify", "spec_verify_tree_greedy", "spec_verify_tree", "spec_verify_ex", "spec_verify_host",
-                     "spec_tree_max_depth", "spec_tree_mask", "spec_ngram_propose", "spec_get_status",
+                     "spec_tree_max_depth", "spec_tree_mask", "spec_ngram_propose", "spec_topk",
+                     "spec_eagle2_expand", "spec_eagle2_rerank", "spec_get_status",
                      "spec_error_string", "spec_last_error_message", "spec_shutdown"):
         assert required in names
 
@@ -99,6 +100,29 @@ def test_ngram_validation_without_gpu(lib):
     assert g(vp, None, 2, 10, 1, 4, 1, 5, vp, vp, None) == 1      # no lengths
     assert g(vp, vp, 2, 10, 1, 4, 1, 5, None, vp, None) == 1      # no draft output with K > 0
     assert g(None, vp, 2, 10, 1, 4, 1, 5, vp, vp, None) == 1      # no tokens with L > 0
+
+
+def test_eagle2_validation_without_gpu(lib):
+    vp = ctypes.c_void_p(16)
+    t = lib.spec_topk            # (logits, R, V, dtype, T, k, tokens, prob, stream)
+    assert t(vp, 0, 100, 1, 1.0, 5, vp, vp, None) == 0            # no rows
+    assert t(vp, 4, 100, 7, 1.0, 5, vp, vp, None) == 2            # dtype
+    assert t(vp, 4, 100, 1, 1.0, 0, vp, vp, None) == 1            # k < 1
+    assert t(vp, 4, 100, 1, 1.0, 33, vp, vp, None) == 1           # k > 32
+    assert t(vp, 4, 3, 1, 1.0, 4, vp, vp, None) == 1              # k > V
+    assert t(vp, 4, 100, 1, 0.0, 5, vp, vp, None) == 1            # T = 0
+    assert t(None, 4, 100, 1, 1.0, 5, vp, vp, None) == 1          # NULL
+    e = lib.spec_eagle2_expand   # (z, frontier, B, F, V, dtype, T, k, tok, val, par, cap, offset, k_next, next, stream)
+    assert e(vp, vp, 0, 4, 100, 1, 1.0, 4, vp, vp, vp, 40, 1, 4, vp, None) == 0     # empty batch
+    assert e(vp, vp, 2, 4, 100, 1, 1.0, 4, vp, vp, vp, 16, 1, 4, vp, None) == 1     # offset + F*k > cap
+    assert e(vp, vp, 2, 4, 100, 1, 1.0, 4, vp, vp, vp, 40, 0, 4, vp, None) == 1     # offset < 1
+    assert e(vp, vp, 2, 4, 100, 1, 1.0, 4, vp, vp, vp, 40, 1, 17, vp, None) == 1    # k_next > F*k
+    assert e(vp, vp, 2, 200, 100, 1, 1.0, 32, vp, vp, vp, 9000, 1, 4, vp, None) == 1  # F*k > 4096
+    r = lib.spec_eagle2_rerank   # (val, par, tok, B, M, m, par_out, tok_out, idx_out, stream)
+    assert r(vp, vp, vp, 0, 10, 5, vp, vp, vp, None) == 0
+    assert r(vp, vp, vp, 2, 10, 10, vp, vp, vp, None) == 1          # m > M - 1
+    assert r(vp, vp, vp, 2, 9000, 5, vp, vp, vp, None) == 1         # M > 8192
+    assert r(vp, vp, vp, 2, 10, 5, None, vp, vp, None) == 1
 
 
 @pytest.mark.parametrize("parent,depth", [([-1], 0), ([-1, 0, 0, 1, 2], 2),
