@@ -5,7 +5,8 @@ achieved HBM bandwidth on GB300, one JSON line on stdout (rank 0).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c1] [--impl reference]
 
 ``--workload ng1`` / ``ng2`` time the n-gram drafter instead (one
-spec_ngram_propose call over a batch of contexts per step).
+spec_ngram_propose call over a batch of contexts per step); ``--workload eg1``
+times the EAGLE-2 tree budget (one budget build for a batch of trees per step).
 
 A step is one call of the verification on one batch of the workload
 (default c1: chain, B=64, K=5, V=128256, bf16 logits, T=0.7), inputs resident
@@ -596,17 +597,248 @@ def run_gpu_ngram(args, w):
     return 0
 
 
+# ----------------------------------------------------------------------------
+# EAGLE-2 tree budget (eg1): one budget build (all expansion steps and the
+# rerank) for a batch of trees per step
+# ----------------------------------------------------------------------------
+EAGLE_METRIC = "EAGLE-2 draft trees built/sec (expansion steps + rerank, draft rows resident), 1 GPU"
+EAGLE_UNIT = "trees/s"
+
+
+def eagle_describe(w):
+    return (f"EAGLE-2 budget B={w.B} trees, V={w.V} {w.dtype} draft rows, T={w.T}, k={w.k} candidates per node, "
+            f"{w.k} nodes grown per step, depth {w.depth}, rerank keeps {w.m}")
+
+
+def _eagle_bytes(w):
+    rows = sum(w.frontier_size(d) for d in range(w.depth))
+    return w.B * rows * w.V * (4 if w.dtype == "f32" else 2)
+
+
+def _eagle_oracle_build(w, rows, B):
+    """The oracle's budget build over per-step rows [B, F, V] (CPU tensors)."""
+    import numpy as np
+    import oracle
+    tok = np.zeros((B, w.M), np.int32)
+    val = np.zeros((B, w.M), np.float64)
+    par = np.zeros((B, w.M), np.int32)
+    val[:, 0], par[:, 0] = 1.0, -1
+    frontier = np.zeros((B, 1), np.int32)
+    for d in range(w.depth):
+        F = w.frontier_size(d)
+        tt, tp = oracle.topk_prob(rows[d][:B].reshape(B * F, w.V), w.k, w.T)
+        kn = w.k if d < w.depth - 1 else 0
+        frontier, _ = oracle.eagle2_expand(frontier, tt.reshape(B, F, w.k), tp.reshape(B, F, w.k), tok, val, par,
+                                           w.offset(d), kn)
+    return oracle.eagle2_rerank(val, par, tok, w.m)
+
+
+def run_reference_eagle2(args, w):
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    from sampling_row_online_gb300.workloads import eagle2_step_rows
+    nb = 2  # trees per step: a bounded sample of the batch
+    rows = [eagle2_step_rows(w, d, "cpu")[:nb].contiguous() for d in range(w.depth)]
+    for _ in range(max(0, args.warmup)):
+        _eagle_oracle_build(w, rows, nb)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _eagle_oracle_build(w, rows, nb)
+    secs = time.perf_counter() - t0
+    value = args.steps * nb / secs
+    line = {
+        "metric": EAGLE_METRIC, "value": value, "unit": EAGLE_UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": f"{w.name}: {eagle_describe(w)}", "step": f"{nb} trees of the batch"},
+        "cpu_baseline": {"value": value, "unit": EAGLE_UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} builds of {nb} trees of {w.name}, oracle, 1 thread"},
+        "e2e": {"value": value, "unit": EAGLE_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu_eagle2(args, w):
+    import torch
+    import torch.distributed as dist
+    from sampling_row_online_gb300 import binding
+    from sampling_row_online_gb300.workloads import eagle2_step_rows
+    ws, rank, local = _dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    lib = binding.library()
+    stream = torch.cuda.current_stream()
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    vp = ctypes.c_void_p
+    B, M = w.B, w.M
+    rows = [eagle2_step_rows(w, d, dev) for d in range(w.depth)]   # > 2x L2 in total
+    tok = torch.zeros((B, M), dtype=torch.int32, device=dev)
+    val = torch.zeros((B, M), dtype=torch.float32, device=dev)
+    par = torch.zeros((B, M), dtype=torch.int32, device=dev)
+    val[:, 0], par[:, 0] = 1.0, -1
+    fronts = [torch.zeros((B, 1), dtype=torch.int32, device=dev)] + \
+             [torch.empty((B, w.k), dtype=torch.int32, device=dev) for _ in range(w.depth)]
+    out = [torch.empty((B, w.m + 1), dtype=torch.int32, device=dev) for _ in range(3)]
+    dt = 0 if w.dtype == "f32" else 1
+    calls = []
+    for d in range(w.depth):
+        F = w.frontier_size(d)
+        kn = w.k if d < w.depth - 1 else 0
+        a = (vp(rows[d].data_ptr()), vp(fronts[d].data_ptr()), B, F, w.V, dt, ctypes.c_float(w.T), w.k,
+             vp(tok.data_ptr()), vp(val.data_ptr()), vp(par.data_ptr()), M, w.offset(d), kn,
+             vp(fronts[d + 1].data_ptr()), sp)
+        calls.append(lambda a=a: lib.spec_eagle2_expand(*a))
+    ra = (vp(val.data_ptr()), vp(par.data_ptr()), vp(tok.data_ptr()), B, M, w.m, vp(out[0].data_ptr()),
+          vp(out[1].data_ptr()), vp(out[2].data_ptr()), sp)
+    calls.append(lambda: lib.spec_eagle2_rerank(*ra))
+
+    def step():
+        for c in calls:
+            st = c()
+            if st != 0:
+                raise SystemExit(f"EAGLE-2 call failed: {st} {lib.spec_last_error_message().decode()}")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if lib.spec_get_status(sp) != 0:
+        raise SystemExit("device status error during warm-up")
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local) if rank == 0 else None
+    time.sleep(0.25 if clocks else 0)
+    wall0 = time.perf_counter()
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    if lib.spec_get_status(sp) != 0:
+        raise SystemExit("device status error in the timed region")
+    region_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
+    step_ms = region_ms / args.steps
+    value = B * args.steps * ws / (region_ms / 1e3)
+    # the dominant kernel alone: spec_topk over the rows of one full step
+    big = rows[1].view(B * w.k, w.V)
+    ttk = torch.empty((B * w.k, w.k), dtype=torch.int32, device=dev)
+    tpk = torch.empty((B * w.k, w.k), dtype=torch.float32, device=dev)
+    ta = (vp(big.data_ptr()), B * w.k, w.V, dt, ctypes.c_float(w.T), w.k, vp(ttk.data_ptr()), vp(tpk.data_ptr()), sp)
+    n_one = min(args.steps, 200)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_one)]
+    flush = torch.empty(256 * 2**20 // 4, dtype=torch.float32, device=dev)
+    for k in range(n_one):
+        flush.fill_(1.0)   # the rows of one step (33 MB) fit in L2: write 256 MB between calls
+        ev[k][0].record(stream)
+        lib.spec_topk(*ta)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    avg_launch_ms = max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in ev), dev)
+    topk_bytes = B * w.k * w.V * (4 if w.dtype == "f32" else 2)
+
+    e2e = None
+    if not args.no_e2e:
+        hrows = [r.cpu().pin_memory() for r in rows]
+        drows = [torch.empty_like(r) for r in rows]
+        hout = [torch.empty((B, w.m + 1), dtype=torch.int32, pin_memory=True) for _ in range(3)]
+        e_calls = []
+        for d in range(w.depth):
+            F = w.frontier_size(d)
+            kn = w.k if d < w.depth - 1 else 0
+            a = (vp(drows[d].data_ptr()), vp(fronts[d].data_ptr()), B, F, w.V, dt, ctypes.c_float(w.T), w.k,
+                 vp(tok.data_ptr()), vp(val.data_ptr()), vp(par.data_ptr()), M, w.offset(d), kn,
+                 vp(fronts[d + 1].data_ptr()), sp)
+            e_calls.append((d, a))
+
+        def e2e_step():
+            for d, a in e_calls:
+                drows[d].copy_(hrows[d], non_blocking=True)
+                lib.spec_eagle2_expand(*a)
+            lib.spec_eagle2_rerank(*ra)
+            for h, o in zip(hout, out):
+                h.copy_(o, non_blocking=True)
+            stream.synchronize()
+
+        for _ in range(2):
+            e2e_step()
+        e_steps = max(3, min(args.steps, 20))
+        t0 = time.perf_counter()
+        for _ in range(e_steps):
+            e2e_step()
+        e_sec = max_over_ranks(time.perf_counter() - t0, dev)
+        e2e = {"value": B * e_steps * ws / e_sec, "unit": EAGLE_UNIT,
+               "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in hrows),
+               "d2h_bytes_per_step": sum(h.numel() * 4 for h in hout)}
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return 0
+    peak, peak_kind = _peaks()
+    kernel = "topk_kernel"
+    achieved = topk_bytes / (avg_launch_ms / 1e3) / 1e9
+    alg = _eagle_bytes(w)
+    step_achieved = alg / (step_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{peak_kind} hbm_gbs", "traffic": _profile_traffic(kernel, w.name), "kernel": kernel,
+                "timed": (f"spec_topk over one full step's rows ({B * w.k} rows of {w.V}), single calls bracketed "
+                          f"by CUDA events after a 256 MB write, mean of {n_one}"),
+                "algorithmic_bytes_per_launch": topk_bytes, "avg_launch_us": avg_launch_ms * 1e3,
+                "whole_step": {"achieved": step_achieved, "frac": step_achieved / peak, "avg_step_us": step_ms * 1e3,
+                               "algorithmic_bytes": alg,
+                               "timed": "region over the steps (all expansion calls and the rerank), back to back"}}
+    cpu = None
+    if not args.no_cpu_baseline:
+        nb = 2
+        hr = [r[:nb].cpu() for r in rows]
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 3.0:
+            _eagle_oracle_build(w, hr, nb)
+            reps += 1
+        secs = time.perf_counter() - t0
+        cpu = {"value": nb * reps / secs, "unit": EAGLE_UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{reps} builds of {nb} trees of {w.name} on the same rows, oracle, 1 thread"}
+    line = {
+        "metric": EAGLE_METRIC, "value": value, "unit": EAGLE_UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: {eagle_describe(w)}", "per_rank_batch": B,
+                   "parallelism": f"replicas x{ws} (trees sharded, no collective)",
+                   "l2": f"draft rows of one build {alg / 1e6:.0f} MB (> 2x L2), read once per build"},
+        "roofline": roofline, "achieved_hbm_gbs": achieved, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": args.steps * (2 * w.depth + 1), "clocks": clk, "wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4", "c3s", "ng1", "ng2"])
+    ap.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4", "c3s", "ng1", "ng2", "eg1"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args(argv)
-    from sampling_row_online_gb300.workloads import NGRAM_WORKLOADS, WORKLOADS
+    from sampling_row_online_gb300.workloads import EAGLE2_WORKLOADS, NGRAM_WORKLOADS, WORKLOADS
+    if args.workload in EAGLE2_WORKLOADS:
+        w = EAGLE2_WORKLOADS[args.workload]
+        return run_reference_eagle2(args, w) if args.impl == "reference" else run_gpu_eagle2(args, w)
     if args.workload in NGRAM_WORKLOADS:
         w = NGRAM_WORKLOADS[args.workload]
         return run_reference_ngram(args, w) if args.impl == "reference" else run_gpu_ngram(args, w)

@@ -39,43 +39,30 @@ __device__ __forceinline__ unsigned long long topk_key(float x, int i) {
   return (static_cast<unsigned long long>(float_order(x)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(i));
 }
 
-// Sorted (descending) register list of KMAX keys of which the last k are
-// live: the first KMAX - k slots hold a sentinel above every key, which no
-// insertion displaces, so the k-th live key is always key[KMAX - 1] and no
-// slot is ever indexed with a run-time value (the list stays in registers).
-constexpr unsigned long long TOPK_SENTINEL = ~0ull;
+// A warp's sorted (descending) list of its k best keys, k <= 32, one key per
+// lane: lane j holds the j-th best (0 in unused or not yet filled slots).
+// Inserting a key is one shuffle and a select per lane; the k-th key (lane
+// k - 1) is the warp's admission threshold.
+__device__ __forceinline__ unsigned long long warp_list_insert(unsigned long long lk, unsigned long long cand,
+                                                               int lane) {
+  const unsigned long long up = __shfl_up_sync(0xFFFFFFFFu, lk, 1);
+  return lk > cand ? lk : ((lane == 0 || up > cand) ? cand : up);
+}
 
-template <int KMAX>
-struct TopList {
-  unsigned long long key[KMAX];
-  __device__ __forceinline__ void clear(int k) {
+// Sorts one float per lane across the warp, largest in lane 0 (bitonic).
+__device__ __forceinline__ float warp_sort_desc(float v, int lane) {
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) key[j] = j < KMAX - k ? TOPK_SENTINEL : 0ull;
-  }
-  // Inserts c (bubbling the displaced keys down); the last key drops out.
-  __device__ __forceinline__ void insert(unsigned long long c) {
+  for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      const unsigned long long cur = key[j];
-      const bool sw = c > cur;
-      key[j] = sw ? c : cur;
-      c = sw ? cur : c;
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const float o = __shfl_xor_sync(0xFFFFFFFFu, v, stride);
+      const bool up = (lane & size) == 0;        // this block sorts descending
+      const bool low = (lane & stride) == 0;     // the lower lane of the pair
+      v = (low == up) ? fmaxf(v, o) : fminf(v, o);
     }
   }
-  __device__ __forceinline__ unsigned long long last() const { return key[KMAX - 1]; }
-  // The largest live key (0 if none is left).
-  __device__ __forceinline__ unsigned long long head() const {
-    unsigned long long h = 0ull;
-#pragma unroll
-    for (int j = KMAX - 1; j >= 0; --j) h = key[j] != TOPK_SENTINEL ? key[j] : h;
-    return h;
-  }
-  // Retires key h (it becomes a sentinel).
-  __device__ __forceinline__ void retire(unsigned long long h) {
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) key[j] = key[j] == h ? TOPK_SENTINEL : key[j];
-  }
-};
+  return v;
+}
 
 __device__ __forceinline__ unsigned long long warp_max_key(unsigned long long v) {
 #pragma unroll
@@ -100,10 +87,20 @@ struct TopkParams {
   int32_t *status;
 };
 
+constexpr int TOPK_MAX_CLUSTER = 8;  // CTAs sharing one row
+constexpr int TOPK_BUF = 1024;       // candidate keys a CTA collects before falling back
+
 struct TopkShared {
-  unsigned long long wk[NWARP][TOPK_MAX];  // per-warp merged lists
+  unsigned long long buf[TOPK_BUF];                   // candidates (keys >= the threshold)
+  float wmax[NWARP][32];                              // per-warp sorted thread maxima
+  int nbuf;
+  float t;                                            // the CTA's threshold
+  unsigned long long wk[NWARP][TOPK_MAX];             // per-warp lists (fallback path)
+  unsigned long long ctak[TOPK_MAX];                  // this CTA's top k
+  unsigned long long ck[TOPK_MAX_CLUSTER][TOPK_MAX];  // rank 0: the CTA lists of the cluster
   float wm[NWARP], ws[NWARP];
-  float m, s;
+  float cm[TOPK_MAX_CLUSTER], cs[TOPK_MAX_CLUSTER];   // rank 0: the CTA normalisers
+  unsigned long long bar_key;                         // largest k-th key of any warp so far
 };
 
 // Online (max, sum of 2^((x - max) c)) update with one value.
@@ -116,58 +113,144 @@ __device__ __forceinline__ void topk_online(float x, float c, float &m, float &s
   }
 }
 
-// Offers (x, i) to a thread's list; kkey / thr track its k-th key and logit.
-template <int KMAX>
-__device__ __forceinline__ void topk_offer(TopList<KMAX> &L, unsigned long long &kkey, float &thr,
-                                           float x, int i) {
-  if (x >= thr) {
-    const unsigned long long key = topk_key(x, i);
-    if (key > kkey) {
-      L.insert(key);
-      kkey = L.last();
-      thr = kkey ? order_float(static_cast<uint32_t>(kkey >> 32)) : -INFINITY;
+constexpr int TOPK_U = 8;  // 16-byte loads in flight per thread
+
+// Element e (0 <= e < VE, a run-time value) of a packed 16-byte vector.
+template <int DT>
+__device__ __forceinline__ float elem_of(const uint4 &q, int e) {
+  if (DT == 0) {
+    const uint32_t w = e == 0 ? q.x : e == 1 ? q.y : e == 2 ? q.z : q.w;
+    return __uint_as_float(w);
+  }
+  const uint32_t w = e < 2 ? q.x : e < 4 ? q.y : e < 6 ? q.z : q.w;
+  return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+// Warp-wide admission: lanes with candidates (bit e of cm: element e of
+// their vector q, at index base_i + e) insert them one at a time, the lowest
+// lane first; after each insert every lane drops the candidates that no
+// longer beat the bar.  The bar is the largest k-th key of any warp of the
+// CTA (shared in *bar): the CTA's k-th key is at least that, so no key below
+// it can reach the CTA's top k.  Uniform control flow.
+template <int DT>
+__device__ __forceinline__ void warp_admit(uint32_t cm, const uint4 &q, int base_i, int k, int lane,
+                                           unsigned long long &lk, unsigned long long &kkey, float &thr,
+                                           unsigned long long *bar) {
+  constexpr int VE = Elem<DT>::VE;
+  unsigned ballot = __ballot_sync(0xFFFFFFFFu, cm != 0u);
+  while (ballot) {
+    const int src = __ffs(ballot) - 1;
+    unsigned long long key = 0ull;
+    if (lane == src) {
+      const int e = __ffs(cm) - 1;
+      cm &= cm - 1u;
+      key = topk_key(elem_of<DT>(q, e), base_i + e);
     }
+    key = __shfl_sync(0xFFFFFFFFu, key, src);
+    if (key > kkey) {  // uniform
+      lk = warp_list_insert(lk, key, lane);
+      const unsigned long long own = __shfl_sync(0xFFFFFFFFu, lk, k - 1);
+      unsigned long long b = 0ull;
+      if (lane == 0) b = own ? atomicMax(bar, own) : *reinterpret_cast<volatile unsigned long long *>(bar);
+      b = __shfl_sync(0xFFFFFFFFu, b, 0);
+      kkey = own > b ? own : b;
+      thr = kkey ? order_float(static_cast<uint32_t>(kkey >> 32)) : -INFINITY;
+#pragma unroll
+      for (int e = 0; e < VE; ++e)
+        if ((cm >> e) & 1u)
+          if (elem_of<DT>(q, e) < thr) cm &= ~(1u << e);
+    }
+    ballot = __ballot_sync(0xFFFFFFFFu, cm != 0u);
   }
 }
 
-constexpr int TOPK_U = 8;  // 16-byte loads in flight per thread
+// The k best keys of this CTA's slice (vectors [lo, hi) for VEC, else
+// elements [lo, hi)) by lockstep admission: the fallback when too many
+// elements tie at the threshold (flat or masked rows).  Leaves them in
+// sh.ctak[0 .. k-1].
+template <int DT, bool VEC>
+__device__ void topk_slice_by_admission(const unsigned char *row, int lo, int hi, int k, TopkShared &sh) {
+  constexpr int VE = Elem<DT>::VE;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) sh.bar_key = 0ull;
+  __syncthreads();
+  unsigned long long lk = 0ull, kkey = 0ull;
+  float thr = -INFINITY;
+  if (VEC) {
+    const uint4 *rv = reinterpret_cast<const uint4 *>(row);
+    for (int base = lo + warp * 32; base < hi; base += NT) {  // warp-uniform
+      const int vi = base + lane;
+      const uint4 q = vi < hi ? __ldg(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
+      uint32_t cm = 0u;
+      if (vi < hi) {
+        float f[VE];
+        Elem<DT>::unpack(q, f);
+#pragma unroll
+        for (int e = 0; e < VE; ++e) cm |= (f[e] >= thr ? 1u : 0u) << e;
+      }
+      warp_admit<DT>(cm, q, vi * VE, k, lane, lk, kkey, thr, &sh.bar_key);
+    }
+  } else {
+    for (int i0 = lo + warp * 32; i0 < hi; i0 += NT) {  // warp-uniform
+      const int i = i0 + lane;
+      const float x = i < hi ? Elem<DT>::load(row, i) : -INFINITY;
+      const uint4 q = make_uint4(__float_as_uint(x), 0u, 0u, 0u);
+      warp_admit<0>((i < hi && x >= thr) ? 1u : 0u, q, i, k, lane, lk, kkey, thr, &sh.bar_key);
+    }
+  }
+  if (lane < k) sh.wk[warp][lane] = lk;
+  __syncthreads();
+  if (warp == 0) {
+    int head = 0;
+    for (int j = 0; j < k; ++j) {
+      const unsigned long long mine = lane < NWARP && head < k ? sh.wk[lane][head] : 0ull;
+      const unsigned long long best = warp_max_key(mine);
+      if (mine == best && best != 0ull) ++head;
+      if (lane == 0) sh.ctak[j] = best;
+    }
+  }
+  __syncthreads();
+}
 
-template <int DT, bool VEC, int KMAX>
-__global__ void __launch_bounds__(NT, KMAX <= 16 ? 2 : 1) topk_kernel(TopkParams p) {
+template <int DT, bool VEC>
+__global__ void __launch_bounds__(NT, 4) topk_kernel(TopkParams p) {
   __shared__ TopkShared sh;
   constexpr int VE = Elem<DT>::VE;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r = blockIdx.x;
+  const int G = static_cast<int>(cluster_size());  // CTAs per row, each a contiguous slice
+  const int rank = static_cast<int>(cluster_rank());
+  const int r = blockIdx.x / G;
   const int k = p.k;
   pdl_launch_dependents();
+  if (tid == 0) sh.nbuf = 0;
   pdl_wait();
   const unsigned char *row = static_cast<const unsigned char *>(p.z) +
                              static_cast<size_t>(r) * p.V * Elem<DT>::BYTES;
-  TopList<KMAX> L;
-  L.clear(k);
-  float thr = -INFINITY;            // logit of the k-th kept key (-inf while slots are empty)
-  unsigned long long kkey = 0ull;    // the k-th kept key
-  float m = -INFINITY, s = 0.f;
+  const int n = VEC ? p.V / VE : p.V;  // vectors (VEC) or elements
+  const int per = (n + G - 1) / G;
+  const int lo = min(n, rank * per), hi = min(n, lo + per);
+
+  // pass 1: online (max, sum) and the thread's own largest logit
+  float m = -INFINITY, s = 0.f, tmax = -INFINITY;
   if (VEC) {
-    // 16-byte vectors, TOPK_U per thread in flight; a thread's indices increase
-    const int nvec = p.V / VE;
     const uint4 *rv = reinterpret_cast<const uint4 *>(row);
-    for (int base = tid; base < nvec; base += TOPK_U * NT) {
+    for (int base = lo + warp * 32; base < hi; base += TOPK_U * NT) {  // warp-uniform
       uint4 q[TOPK_U];
 #pragma unroll
       for (int u = 0; u < TOPK_U; ++u) {
-        const int vi = base + u * NT;
-        q[u] = vi < nvec ? __ldg(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
+        const int vi = base + u * NT + lane;
+        q[u] = vi < hi ? __ldg(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int u = 0; u < TOPK_U; ++u) {
-        const int vi = base + u * NT;
-        if (vi < nvec) {
+        const int vi = base + u * NT + lane;
+        if (vi < hi) {
           float f[VE];
           Elem<DT>::unpack(q[u], f);
           float vm = f[0];
 #pragma unroll
           for (int e = 1; e < VE; ++e) vm = fmaxf(vm, f[e]);
+          tmax = fmaxf(tmax, vm);
           if (vm > m) {
             s *= ex2((m - vm) * p.c);
             m = vm;
@@ -177,22 +260,95 @@ __global__ void __launch_bounds__(NT, KMAX <= 16 ? 2 : 1) topk_kernel(TopkParams
 #pragma unroll
             for (int e = 0; e < VE; ++e) s += ex2(fmaf(f[e], p.c, -mc));
           }
-          if (vm >= thr) {
-#pragma unroll
-            for (int e = 0; e < VE; ++e) topk_offer(L, kkey, thr, f[e], vi * VE + e);
-          }
         }
       }
     }
   } else {
-    for (int i = tid; i < p.V; i += NT) {
+    for (int i = lo + tid; i < hi; i += NT) {
       const float x = Elem<DT>::load(row, i);
       topk_online(x, p.c, m, s);
-      topk_offer(L, kkey, thr, x, i);
+      tmax = fmaxf(tmax, x);
     }
   }
 
-  // row normalisers: warp, then CTA
+  // the threshold t: the k-th largest thread maximum (at least k elements of
+  // the slice are >= t, so its k best all are)
+  {
+    const float sorted = warp_sort_desc(tmax, lane);
+    sh.wmax[warp][lane] = sorted;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int head = 0;
+    float t = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+      const float mine = lane < NWARP && head < 32 ? sh.wmax[lane][head] : -INFINITY;
+      float best = mine;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+      const unsigned win = __ballot_sync(0xFFFFFFFFu, mine == best && lane < NWARP && head < 32);
+      if (lane == __ffs(win) - 1) ++head;
+      t = best;
+    }
+    if (lane == 0) sh.t = t;
+  }
+  __syncthreads();
+  const float t = sh.t;
+
+  // pass 2: threads holding an element >= t collect those elements' keys
+  if (tmax >= t) {
+    if (VEC) {
+      const uint4 *rv = reinterpret_cast<const uint4 *>(row);
+      for (int v0 = lo + warp * 32 + lane; v0 < hi; v0 += TOPK_U * NT) {  // this thread's vectors
+        uint4 q[TOPK_U];
+#pragma unroll
+        for (int u = 0; u < TOPK_U; ++u) {
+          const int vi = v0 + u * NT;
+          q[u] = vi < hi ? __ldg(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < TOPK_U; ++u) {
+          const int vi = v0 + u * NT;
+          if (vi < hi) {
+            float f[VE];
+            Elem<DT>::unpack(q[u], f);
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+              if (f[e] >= t) {
+                const int slot = atomicAdd(&sh.nbuf, 1);
+                if (slot < TOPK_BUF) sh.buf[slot] = topk_key(f[e], vi * VE + e);
+              }
+            }
+          }
+        }
+      }
+    } else {
+      for (int i = lo + tid; i < hi; i += NT) {
+        const float x = Elem<DT>::load(row, i);
+        if (x >= t) {
+          const int slot = atomicAdd(&sh.nbuf, 1);
+          if (slot < TOPK_BUF) sh.buf[slot] = topk_key(x, i);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int nb = sh.nbuf;
+  if (nb <= TOPK_BUF) {
+    // rank of each candidate among the candidates (keys are distinct)
+    for (int i = tid; i < nb; i += NT) {
+      const unsigned long long key = sh.buf[i];
+      int rk = 0;
+      for (int j = 0; j < nb; ++j) rk += sh.buf[j] > key;
+      if (rk < k) sh.ctak[rk] = key;
+    }
+    for (int j = nb + tid; j < k; j += NT) sh.ctak[j] = 0ull;  // a slice with fewer than k elements
+    __syncthreads();
+  } else {
+    topk_slice_by_admission<DT, VEC>(row, lo, hi, k, sh);
+  }
+
+  // normalisers of the slice; the CTA's list and normalisers go to rank 0
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
@@ -201,22 +357,33 @@ __global__ void __launch_bounds__(NT, KMAX <= 16 ? 2 : 1) topk_kernel(TopkParams
     s = (m == -INFINITY ? 0.f : s * ex2((m - mn) * p.c)) + (m2 == -INFINITY ? 0.f : s2 * ex2((m2 - mn) * p.c));
     m = mn;
   }
-  // warp top-k: k rounds, the lane holding the best head pops it
-  for (int j = 0; j < k; ++j) {
-    const unsigned long long h = L.head();
-    const unsigned long long best = warp_max_key(h);
-    if (lane == 0) sh.wk[warp][j] = best;
-    if (h == best && best != 0ull) L.retire(best);
-  }
   if (lane == 0) {
     sh.wm[warp] = m;
     sh.ws[warp] = s;
   }
   __syncthreads();
-  if (warp != 0) return;
-  // CTA: lanes 0..NWARP-1 hold the warp lists (shared memory heads)
-  m = lane < NWARP ? sh.wm[lane] : -INFINITY;
-  s = lane < NWARP ? sh.ws[lane] : 0.f;
+  if (warp == 0) {
+    m = lane < NWARP ? sh.wm[lane] : -INFINITY;
+    s = lane < NWARP ? sh.ws[lane] : 0.f;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+      const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+      const float mn = fmaxf(m, m2);
+      s = (m == -INFINITY ? 0.f : s * ex2((m - mn) * p.c)) + (m2 == -INFINITY ? 0.f : s2 * ex2((m2 - mn) * p.c));
+      m = mn;
+    }
+    if (lane < k) dsmem_st_u64(dsmem_addr(&sh.ck[rank][lane], 0), sh.ctak[lane]);
+    if (lane == 0) {
+      dsmem_st_f32(dsmem_addr(&sh.cm[rank], 0), m);
+      dsmem_st_f32(dsmem_addr(&sh.cs[rank], 0), s);
+    }
+  }
+  cluster_sync();
+  if (rank != 0 || warp != 0) return;
+  // rank 0: merge the G CTA lists, combine the normalisers, write the row
+  m = lane < G ? sh.cm[lane] : -INFINITY;
+  s = lane < G ? sh.cs[lane] : 0.f;
 #pragma unroll
   for (int o = 16; o; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
@@ -227,7 +394,7 @@ __global__ void __launch_bounds__(NT, KMAX <= 16 ? 2 : 1) topk_kernel(TopkParams
   }
   int head = 0;
   for (int j = 0; j < k; ++j) {
-    const unsigned long long mine = lane < NWARP && head < k ? sh.wk[lane][head] : 0ull;
+    const unsigned long long mine = lane < G && head < k ? sh.ck[lane][head] : 0ull;
     const unsigned long long best = warp_max_key(mine);
     if (mine == best && best != 0ull) ++head;
     if (lane == 0) {

@@ -458,13 +458,6 @@ int tree_depth_host(const int32_t *parent, int N) {
 
 
 // ------------------------------------------------------------ EAGLE-2
-template <int DT, bool VEC>
-const void *pick_topk(int kmax) {
-  if (kmax <= 8) return reinterpret_cast<const void *>(&topk_kernel<DT, VEC, 8>);
-  if (kmax <= 16) return reinterpret_cast<const void *>(&topk_kernel<DT, VEC, 16>);
-  return reinterpret_cast<const void *>(&topk_kernel<DT, VEC, 32>);
-}
-
 int check_topk_args(int R, int V, int dtype, float T, int k) {
   if (dtype != SPEC_F32 && dtype != SPEC_BF16) return fail(SPEC_ERR_DTYPE, "dtype must be SPEC_F32 or SPEC_BF16");
   if (R < 0) return fail(SPEC_ERR_ARG, "row count must be >= 0");
@@ -476,21 +469,38 @@ int check_topk_args(int R, int V, int dtype, float T, int k) {
   return SPEC_OK;
 }
 
-// One launch of the top-k kernel (a programmatic dependent of earlier work).
+// One launch of the top-k kernel (a programmatic dependent of earlier work):
+// G CTAs per row in one cluster, each a contiguous slice of at least 16 KB,
+// G a power of two up to 8 giving about two waves of 3 resident CTAs per SM.
 int launch_topk(TopkParams &p, int dtype, cudaStream_t stream) {
   const size_t esz = dtype == SPEC_F32 ? 4 : 2;
   const bool vec = aligned16(p.z) && (static_cast<size_t>(p.V) * esz) % 16 == 0;
-  const void *fn = dtype == SPEC_F32 ? (vec ? pick_topk<0, true>(p.k) : pick_topk<0, false>(p.k))
-                                     : (vec ? pick_topk<1, true>(p.k) : pick_topk<1, false>(p.k));
-  cudaLaunchAttribute pdl;
-  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl.val.programmaticStreamSerializationAllowed = 1;
+  const void *fn = dtype == SPEC_F32
+                       ? (vec ? reinterpret_cast<const void *>(&topk_kernel<0, true>)
+                              : reinterpret_cast<const void *>(&topk_kernel<0, false>))
+                       : (vec ? reinterpret_cast<const void *>(&topk_kernel<1, true>)
+                              : reinterpret_cast<const void *>(&topk_kernel<1, false>));
+  const long long want = (6LL * num_sms() + p.R - 1) / p.R;
+  const long long by_size = std::max<long long>(1, static_cast<long long>(p.V) * esz / 16384);
+  int G = static_cast<int>(std::min<long long>({static_cast<long long>(TOPK_MAX_CLUSTER), want, by_size}));
+  G = env_int("SPEC_TOPK_CLUSTER", G, 1, TOPK_MAX_CLUSTER);
+  int pow2 = 1;
+  while (pow2 * 2 <= G) pow2 *= 2;
+  G = pow2;
+  if (static_cast<long long>(p.R) * G > INT_MAX) return fail(SPEC_ERR_ARG, "too many rows");
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = G;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.R), 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(p.R * G), 1, 1);
   cfg.blockDim = dim3(NT, 1, 1);
   cfg.stream = stream;
-  cfg.attrs = &pdl;
-  cfg.numAttrs = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   void *args[] = {&p};
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return cuda_fail(e, "topk_kernel launch");

@@ -47,6 +47,19 @@ def test_topk_parity(R, V, k, dtype, T):
     np.testing.assert_allclose(prob.cpu().numpy(), rp, rtol=1e-5, atol=1e-30)
 
 
+@pytest.mark.parametrize("G", [1, 2, 4, 8])
+def test_topk_cluster_sizes(G, monkeypatch):
+    """Rows split over G CTAs of a cluster merge to the same answer
+    (SPEC_TOPK_CLUSTER overrides the choice)."""
+    monkeypatch.setenv("SPEC_TOPK_CLUSTER", str(G))
+    for R, V, k, dtype in ((5, 128256, 10, "bf16"), (3, 40000, 32, "f32"), (4, 1003, 8, "bf16")):
+        z = _rows(R, V, dtype, seed=G * 100 + V)
+        tok, prob = binding.spec_topk(z, k, 1.0)
+        rt, rp = oracle.topk_prob(z.cpu(), k, 1.0)
+        assert np.array_equal(tok.cpu().numpy(), rt)
+        np.testing.assert_allclose(prob.cpu().numpy(), rp, rtol=1e-5, atol=1e-30)
+
+
 def test_topk_unaligned_rows():
     base = _rows(1, 1001 * 6 + 1, "bf16", seed=3, masked=False).reshape(-1)
     z = base[1:].view(6, 1001)                  # odd V, data pointer 2 bytes off: plain loads
