@@ -60,6 +60,25 @@ def test_topk_cluster_sizes(G, monkeypatch):
         np.testing.assert_allclose(prob.cpu().numpy(), rp, rtol=1e-5, atol=1e-30)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_topk_flat_and_masked_rows(dtype):
+    """Rows where thousands of entries reach the threshold (all equal; or all
+    -inf but three) take the lockstep-admission path; ties go to the lowest
+    indices."""
+    V, k = 50000, 8
+    z = torch.zeros((3, V), device="cuda")
+    z[1] = float("-inf")
+    z[1, [7, 20000, 49999]] = torch.tensor([1.0, 3.0, 2.0], device="cuda")
+    z[2, ::2] = 1.5                       # half the row ties at the maximum
+    z = z.to(torch.float32 if dtype == "f32" else torch.bfloat16).contiguous()
+    tok, prob = binding.spec_topk(z, k, 1.0)
+    assert binding.spec_get_status() == 0
+    rt, rp = oracle.topk_prob(z.cpu(), k, 1.0)
+    assert np.array_equal(tok.cpu().numpy(), rt)
+    np.testing.assert_allclose(prob.cpu().numpy(), rp, rtol=1e-5, atol=1e-30)
+    assert tok[0].tolist() == list(range(k)) and tok[2].tolist() == list(range(0, 2 * k, 2))
+
+
 def test_topk_unaligned_rows():
     base = _rows(1, 1001 * 6 + 1, "bf16", seed=3, masked=False).reshape(-1)
     z = base[1:].view(6, 1001)                  # odd V, data pointer 2 bytes off: plain loads
