@@ -295,23 +295,23 @@ __global__ void __launch_bounds__(NT, 4) topk_kernel(TopkParams p) {
   __syncthreads();
   const float t = sh.t;
 
-  // pass 2: threads holding an element >= t collect those elements' keys
-  if (tmax >= t) {
-    if (VEC) {
-      const uint4 *rv = reinterpret_cast<const uint4 *>(row);
-      for (int v0 = lo + warp * 32 + lane; v0 < hi; v0 += TOPK_U * NT) {  // this thread's vectors
-        uint4 q[TOPK_U];
-#pragma unroll
-        for (int u = 0; u < TOPK_U; ++u) {
-          const int vi = v0 + u * NT;
-          q[u] = vi < hi ? __ldg(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int u = 0; u < TOPK_U; ++u) {
-          const int vi = v0 + u * NT;
+  // pass 2: the elements >= t lie in the vectors of "hot" threads (their own
+  // maximum reaches t); each warp re-reads its hot lanes' vectors together,
+  // one vector per lane, and appends the keys of elements >= t
+  {
+    unsigned hot = __ballot_sync(0xFFFFFFFFu, tmax >= t);
+    while (hot) {
+      const int h = __ffs(hot) - 1;
+      hot &= hot - 1u;
+      if (VEC) {
+        const uint4 *rv = reinterpret_cast<const uint4 *>(row);
+        const int first = lo + warp * 32 + h;  // lane h's vectors: first + j * NT
+        for (int j0 = 0; first + j0 * NT < hi; j0 += 32) {  // warp-uniform
+          const int vi = first + (j0 + lane) * NT;
           if (vi < hi) {
+            const uint4 q = __ldg(rv + vi);
             float f[VE];
-            Elem<DT>::unpack(q[u], f);
+            Elem<DT>::unpack(q, f);
 #pragma unroll
             for (int e = 0; e < VE; ++e) {
               if (f[e] >= t) {
@@ -321,13 +321,17 @@ __global__ void __launch_bounds__(NT, 4) topk_kernel(TopkParams p) {
             }
           }
         }
-      }
-    } else {
-      for (int i = lo + tid; i < hi; i += NT) {
-        const float x = Elem<DT>::load(row, i);
-        if (x >= t) {
-          const int slot = atomicAdd(&sh.nbuf, 1);
-          if (slot < TOPK_BUF) sh.buf[slot] = topk_key(x, i);
+      } else {
+        const int first = lo + warp * 32 + h;  // lane h's elements: first + j * NT (see pass 1)
+        for (int j0 = 0; first + j0 * NT < hi; j0 += 32) {
+          const int i = first + (j0 + lane) * NT;
+          if (i < hi) {
+            const float x = Elem<DT>::load(row, i);
+            if (x >= t) {
+              const int slot = atomicAdd(&sh.nbuf, 1);
+              if (slot < TOPK_BUF) sh.buf[slot] = topk_key(x, i);
+            }
+          }
         }
       }
     }
@@ -392,22 +396,24 @@ __global__ void __launch_bounds__(NT, 4) topk_kernel(TopkParams p) {
     s = (m == -INFINITY ? 0.f : s * ex2((m - mn) * p.c)) + (m2 == -INFINITY ? 0.f : s2 * ex2((m2 - mn) * p.c));
     m = mn;
   }
-  int head = 0;
-  for (int j = 0; j < k; ++j) {
-    const unsigned long long mine = lane < G && head < k ? sh.ck[lane][head] : 0ull;
-    const unsigned long long best = warp_max_key(mine);
-    if (mine == best && best != 0ull) ++head;
-    if (lane == 0) {
-      const int i = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(best));
-      const float x = order_float(static_cast<uint32_t>(best >> 32));
+  // rank of every key of the G lists among them (keys are distinct; empty
+  // slots are 0 and rank last), then the k best in parallel
+  for (int i = lane; i < G * k; i += 32) {
+    const unsigned long long key = sh.ck[i / k][i % k];
+    if (key == 0ull) continue;
+    int rk = 0;
+    for (int j = 0; j < G * k; ++j) rk += sh.ck[j / k][j % k] > key;
+    if (rk < k) {
+      const int idx = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+      const float x = order_float(static_cast<uint32_t>(key >> 32));
       const float prob = ex2(fmaf(x, p.c, -m * p.c)) / s;
       if (p.F == 0) {
-        p.out_tok[static_cast<size_t>(r) * k + j] = i;
-        p.out_prob[static_cast<size_t>(r) * k + j] = prob;
+        p.out_tok[static_cast<size_t>(r) * k + rk] = idx;
+        p.out_prob[static_cast<size_t>(r) * k + rk] = prob;
       } else {
         const int b = r / p.F, f = r - b * p.F;
-        const size_t slot = static_cast<size_t>(b) * p.cap + p.offset + f * k + j;
-        p.out_tok[slot] = i;
+        const size_t slot = static_cast<size_t>(b) * p.cap + p.offset + f * k + rk;
+        p.out_tok[slot] = idx;
         p.out_prob[slot] = prob;  // the select step multiplies by the parent's value
         p.node_par[slot] = __ldg(p.frontier + r);
       }
