@@ -251,6 +251,24 @@ int spec_verify_tree(const void *target_logits, const void *draft_logits,
                      int32_t *out_path, int32_t *out_len, void *stream);
 
 /*
+ * spec_verify_trees_greedy, spec_verify_trees — the same two verifications
+ * with one tree per sequence, as a dynamic tree budget builds them
+ * ([Infra53] §5.1: EAGLE-2 grows a different tree for each context; see
+ * spec_eagle2_rerank, whose listing is such a tree):
+ *   parents  [B, N] int32 (device): row b is sequence b's tree (parent[0] =
+ *            -1, parent[c] < c, depth <= max_depth, checked on the device)
+ * Everything else as spec_verify_tree_greedy / spec_verify_tree.  With one
+ * tree per sequence the stochastic form streams every node's draft row (which
+ * nodes have children differs between sequences), so it reads B*2N rows.
+ */
+int spec_verify_trees_greedy(const void *target_logits, const int32_t *parents,
+                             const int32_t *node_tokens, int B, int N, int V, int dtype,
+                             int max_depth, int32_t *out_path, int32_t *out_len, void *stream);
+int spec_verify_trees(const void *target_logits, const void *draft_logits, const int32_t *parents,
+                      const int32_t *node_tokens, int B, int N, int V, int dtype, float temperature,
+                      uint64_t seed, int max_depth, int32_t *out_path, int32_t *out_len, void *stream);
+
+/*
  * spec_tree_max_depth — HOST helper: the largest node depth of parent[]
  * (HOST pointer), or -SPEC_ERR_PARENT if parent[] is not a tree
  * ([Infra53] §3.2: position IDs follow tree depth).

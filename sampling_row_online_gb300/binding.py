@@ -53,6 +53,8 @@ def library():
     lib.spec_arm_rows_event.argtypes = [vp]
     lib.spec_verify_tree_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.spec_verify_tree.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, u64, i32, vp, vp, vp]
+    lib.spec_verify_trees_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.spec_verify_trees.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, u64, i32, vp, vp, vp]
     lib.spec_tree_max_depth.argtypes = [vp, i32]
     lib.spec_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp]
     lib.spec_ngram_propose.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
@@ -200,9 +202,25 @@ def spec_tree_max_depth(parent) -> int:
     return d
 
 
+def _tree_parents(parent, B, N, max_depth):
+    """(one tree per sequence?, max_depth) for a parent tensor [N] (one tree)
+    or [B, N]; a missing max_depth is the deepest node over the trees (read
+    on the host)."""
+    if parent.dim() == 2:
+        if tuple(parent.shape) != (B, N):
+            raise ValueError("parent must be [N] or [B, N]")
+        if max_depth is None:
+            max_depth = max((spec_tree_max_depth(row) for row in parent.cpu()), default=0)
+        return True, max_depth
+    if parent.numel() != N:
+        raise ValueError("parent must be [N] or [B, N]")
+    return False, spec_tree_max_depth(parent.cpu()) if max_depth is None else max_depth
+
+
 def spec_verify_tree_greedy(target_logits, parent, node_tokens, *, max_depth=None,
                             out_path=None, out_len=None, stream=None):
-    """Greedy tree verification; returns (out_path [B, D+1] int32, out_len [B] int32)."""
+    """Greedy tree verification; parent [N] (one tree) or [B, N] (one tree per
+    sequence).  Returns (out_path [B, D+1] int32, out_len [B] int32)."""
     lib = library()
     _dev(target_logits, "target_logits")
     if target_logits.dim() != 3:
@@ -210,17 +228,17 @@ def spec_verify_tree_greedy(target_logits, parent, node_tokens, *, max_depth=Non
     B, N, V = target_logits.shape
     _dev(parent, "parent", torch.int32)
     _dev(node_tokens, "node_tokens", torch.int32)
-    if parent.numel() != N or tuple(node_tokens.shape) != (B, N):
-        raise ValueError("parent must be [N] and node_tokens [B, N]")
-    if max_depth is None:
-        max_depth = spec_tree_max_depth(parent.cpu())
+    if tuple(node_tokens.shape) != (B, N):
+        raise ValueError("node_tokens must be [B, N]")
+    per_seq, max_depth = _tree_parents(parent, B, N, max_depth)
     dev = target_logits.device
     if out_path is None:
         out_path = torch.empty((B, max_depth + 1), dtype=torch.int32, device=dev)
     if out_len is None:
         out_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    fn = lib.spec_verify_trees_greedy if per_seq else lib.spec_verify_tree_greedy
     with torch.cuda.device(dev):
-        st = lib.spec_verify_tree_greedy(_ptr(target_logits), _ptr(parent), _ptr(node_tokens),
+        st = fn(_ptr(target_logits), _ptr(parent), _ptr(node_tokens),
                                          B, N, V, _dtype_code(target_logits), int(max_depth),
                                          _ptr(out_path), _ptr(out_len), _stream(stream))
     _check(st, "spec_verify_tree_greedy")
@@ -229,8 +247,9 @@ def spec_verify_tree_greedy(target_logits, parent, node_tokens, *, max_depth=Non
 
 def spec_verify_tree(target_logits, draft_logits, parent, node_tokens, temperature, seed, *,
                      max_depth=None, out_path=None, out_len=None, stream=None):
-    """Stochastic tree verification (T > 0; T == 0 is greedy matching); returns
-    (out_path [B, D+1] int32, out_len [B] int32)."""
+    """Stochastic tree verification (T > 0; T == 0 is greedy matching); parent
+    [N] (one tree) or [B, N] (one tree per sequence).  Returns (out_path
+    [B, D+1] int32, out_len [B] int32)."""
     lib = library()
     _dev(target_logits, "target_logits")
     if target_logits.dim() != 3:
@@ -242,17 +261,17 @@ def spec_verify_tree(target_logits, draft_logits, parent, node_tokens, temperatu
             raise ValueError("draft_logits must be [B, N, V]")
     _dev(parent, "parent", torch.int32)
     _dev(node_tokens, "node_tokens", torch.int32)
-    if parent.numel() != N or tuple(node_tokens.shape) != (B, N):
-        raise ValueError("parent must be [N] and node_tokens [B, N]")
-    if max_depth is None:
-        max_depth = spec_tree_max_depth(parent.cpu())
+    if tuple(node_tokens.shape) != (B, N):
+        raise ValueError("node_tokens must be [B, N]")
+    per_seq, max_depth = _tree_parents(parent, B, N, max_depth)
     dev = target_logits.device
     if out_path is None:
         out_path = torch.empty((B, max_depth + 1), dtype=torch.int32, device=dev)
     if out_len is None:
         out_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    fn = lib.spec_verify_trees if per_seq else lib.spec_verify_tree
     with torch.cuda.device(dev):
-        st = lib.spec_verify_tree(_ptr(target_logits), _ptr(draft_logits), _ptr(parent),
+        st = fn(_ptr(target_logits), _ptr(draft_logits), _ptr(parent),
                                   _ptr(node_tokens), B, N, V, _dtype_code(target_logits),
                                   ctypes.c_float(temperature), ctypes.c_uint64(int(seed) & ((1 << 64) - 1)),
                                   int(max_depth), _ptr(out_path), _ptr(out_len), _stream(stream))

@@ -477,12 +477,14 @@ __global__ void __launch_bounds__(NT) expand_select_kernel(EagleParams p) {
 
 // Rerank (one CTA per tree of M nodes): keep the root and the m best other
 // nodes by (value, then smaller depth, then lower id); list them by depth,
-// then rank; parents become list positions.  Dynamic shared memory: key[M]
-// (8 B), depth[M], rank[M] (4 B each), byrank[m].
+// then rank; parents become list positions.  The parents and values are read
+// once into shared memory; depths come from walks there.  Dynamic shared
+// memory: key[M] (8 B), parent[M], depth[M], rank[M] (4 B each), byrank[m].
 __global__ void __launch_bounds__(NT) rerank_kernel(EagleParams p) {
   extern __shared__ __align__(128) unsigned char rerank_smem[];
   unsigned long long *key = reinterpret_cast<unsigned long long *>(rerank_smem);
-  int *depth = reinterpret_cast<int *>(key + p.M);
+  int *spar = reinterpret_cast<int *>(key + p.M);
+  int *depth = spar + p.M;
   int *rank = depth + p.M;
   int *byrank = rank + p.M;
   __shared__ int bad;
@@ -497,19 +499,22 @@ __global__ void __launch_bounds__(NT) rerank_kernel(EagleParams p) {
   const int32_t *tok = p.node_tok + static_cast<size_t>(b) * M;
   for (int c = tid; c < M; c += NT) {
     const int u = __ldg(par + c);
+    spar[c] = u;
+    key[c] = __float_as_uint(__ldg(val + c));  // the value's bits, until the depth is known
     if (c == 0 ? u != -1 : (u < 0 || u >= c)) atomicOr(&bad, 1);
   }
   __syncthreads();
   if (!bad) {
     for (int c = tid; c < M; c += NT) {  // parent[c] < c: the walk ends at the root
       int d = 0;
-      for (int u = c; u != 0; u = __ldg(par + u)) ++d;
+      for (int u = c; u != 0; u = spar[u]) ++d;
       depth[c] = d;
     }
     __syncthreads();
     for (int c = tid; c < M; c += NT)
       key[c] = c == 0 ? 0ull
-                      : (static_cast<unsigned long long>(float_order(__ldg(val + c))) << 32) |
+                      : (static_cast<unsigned long long>(float_order(__uint_as_float(static_cast<uint32_t>(key[c]))))
+                         << 32) |
                             (static_cast<unsigned long long>(255 - min(depth[c], 255)) << 24) |
                             (0xFFFFFFu - static_cast<uint32_t>(c));
     __syncthreads();
@@ -525,7 +530,7 @@ __global__ void __launch_bounds__(NT) rerank_kernel(EagleParams p) {
     }
     __syncthreads();
     for (int r = tid; r < m; r += NT) {  // a kept node's parent must be kept
-      const int u = __ldg(par + byrank[r]);
+      const int u = spar[byrank[r]];
       if (u != 0 && rank[u] >= m) atomicOr(&bad, 1);
     }
     __syncthreads();
@@ -559,7 +564,7 @@ __global__ void __launch_bounds__(NT) rerank_kernel(EagleParams p) {
   for (int r = tid; r < m; r += NT) {
     const int c = byrank[r];
     const int q = static_cast<int>(key[c]);
-    const int u = __ldg(par + c);
+    const int u = spar[c];
     op[q] = u == 0 ? 0 : static_cast<int>(key[u]);
     ot[q] = __ldg(tok + c);
     oi[q] = c;

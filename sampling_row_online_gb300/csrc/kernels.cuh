@@ -74,6 +74,7 @@ struct Params {
   const void *zd;           // [B, K, V] draft rows (sampling only)
   const int32_t *tokens;    // chain: draft tokens [B, K]; tree: node tokens [B, N]
   const int32_t *parent;    // tree: [N]
+  int parent_stride;        // 0: one tree for the batch; N: tree b at parent + b * N
   int B, K, V, J;           // K = drafts (chain) or N (tree)
   int kind;
   float c;                  // log2(e) / T
@@ -475,11 +476,15 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
     pc.tree_internal = tree_internal;
     if (!ARGMAX && p.kind == KIND_TREE_SAMPLE) {
       // stochastic tree: nodes with children stream their draft row too
-      for (int w = lane; w < MAX_TREE_NODES / 32; w += 32) tree_internal[w] = 0u;
+      // (one tree per sequence: every node streams its draft row, since which
+      // nodes have children differs between sequences)
+      for (int w = lane; w < MAX_TREE_NODES / 32; w += 32) tree_internal[w] = p.parent_stride ? ~0u : 0u;
       __syncwarp();
-      for (int cn = 1 + lane; cn < p.K; cn += 32) {
-        const int u = __ldg(p.parent + cn);
-        if (u >= 0 && u < p.K) atomicOr(&tree_internal[u >> 5], 1u << (u & 31));
+      if (!p.parent_stride) {
+        for (int cn = 1 + lane; cn < p.K; cn += 32) {
+          const int u = __ldg(p.parent + cn);
+          if (u >= 0 && u < p.K) atomicOr(&tree_internal[u >> 5], 1u << (u & 31));
+        }
       }
       __syncwarp();
     }
@@ -1281,7 +1286,7 @@ __global__ void __launch_bounds__(NT, 4) tree_draw_kernel(const Params p) {
   __syncthreads();
   // ---- inputs: the tree, the node tokens, their logits, the uniforms
   for (int cn = tid; cn < N; cn += NT) {
-    const int pu = __ldg(p.parent + cn);
+    const int pu = __ldg(p.parent + static_cast<size_t>(b) * p.parent_stride + cn);
     const int x = __ldg(p.tokens + static_cast<size_t>(b) * N + cn);
     int bad = 0;
     if (cn == 0) {
@@ -1504,7 +1509,7 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
   int *s_par = ish + 3 * J;
   int *s_depth = s_par + N;
   unsigned char *s_acc = reinterpret_cast<unsigned char *>(s_depth + N);
-  for (int e = tid; e < N; e += NT) s_par[e] = __ldg(p.parent + e);
+  for (int e = tid; e < N; e += NT) s_par[e] = __ldg(p.parent + static_cast<size_t>(b) * p.parent_stride + e);
   __syncthreads();
   if (tid == 0) {
     const int W = p.max_depth + 1;

@@ -545,7 +545,9 @@ int spec_verify_ex(const void *target_logits, const void *draft_logits, const in
                       out_tokens, out_n_accepted, out_row_max, out_row_sumexp, stats, stream);
 }
 
-int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent,
+// Greedy tree verification; parent_stride 0: one tree [N] for the batch,
+// N: tree b at parent + b * N.
+static int tree_greedy_impl(const void *target_logits, const int32_t *parent, int parent_stride,
                             const int32_t *node_tokens, int B, int N, int V, int dtype,
                             int max_depth, int32_t *out_path, int32_t *out_len, void *stream_ptr) {
   int st = check_common(target_logits, B, V, dtype);
@@ -561,6 +563,7 @@ int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent,
   p.zt = target_logits;
   p.tokens = node_tokens;
   p.parent = parent;
+  p.parent_stride = parent_stride;
   p.B = B;
   p.K = N;
   p.V = V;
@@ -574,14 +577,16 @@ int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent,
   return run_step(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr), &w);
 }
 
-int spec_verify_tree(const void *target_logits, const void *draft_logits, const int32_t *parent,
-                     const int32_t *node_tokens, int B, int N, int V, int dtype, float temperature,
-                     uint64_t seed, int max_depth, int32_t *out_path, int32_t *out_len, void *stream_ptr) {
+// Stochastic tree verification; parent_stride as for tree_greedy_impl.
+static int tree_sample_impl(const void *target_logits, const void *draft_logits, const int32_t *parent,
+                            int parent_stride, const int32_t *node_tokens, int B, int N, int V, int dtype,
+                            float temperature, uint64_t seed, int max_depth, int32_t *out_path,
+                            int32_t *out_len, void *stream_ptr) {
   const float T = temperature;
   if (!(T >= 0.f) || !std::isfinite(T)) return fail(SPEC_ERR_ARG, "temperature must be finite and >= 0");
   if (T == 0.f)  // greedy matching of the same tree
-    return spec_verify_tree_greedy(target_logits, parent, node_tokens, B, N, V, dtype, max_depth, out_path,
-                                   out_len, stream_ptr);
+    return tree_greedy_impl(target_logits, parent, parent_stride, node_tokens, B, N, V, dtype, max_depth,
+                            out_path, out_len, stream_ptr);
   int st = check_common(target_logits, B, V, dtype);
   if (st) return st;
   const double cd = 1.4426950408889634 / static_cast<double>(T);
@@ -600,6 +605,7 @@ int spec_verify_tree(const void *target_logits, const void *draft_logits, const 
   p.zd = draft_logits;
   p.tokens = node_tokens;
   p.parent = parent;
+  p.parent_stride = parent_stride;
   p.B = B;
   p.K = N;
   p.V = V;
@@ -613,6 +619,34 @@ int spec_verify_tree(const void *target_logits, const void *draft_logits, const 
   p.out_n = out_len;
   Workspace *w = nullptr;
   return run_step(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr), &w);
+}
+
+int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent, const int32_t *node_tokens,
+                            int B, int N, int V, int dtype, int max_depth, int32_t *out_path,
+                            int32_t *out_len, void *stream_ptr) {
+  return tree_greedy_impl(target_logits, parent, 0, node_tokens, B, N, V, dtype, max_depth, out_path, out_len,
+                          stream_ptr);
+}
+
+int spec_verify_trees_greedy(const void *target_logits, const int32_t *parents, const int32_t *node_tokens,
+                             int B, int N, int V, int dtype, int max_depth, int32_t *out_path,
+                             int32_t *out_len, void *stream_ptr) {
+  return tree_greedy_impl(target_logits, parents, N, node_tokens, B, N, V, dtype, max_depth, out_path, out_len,
+                          stream_ptr);
+}
+
+int spec_verify_tree(const void *target_logits, const void *draft_logits, const int32_t *parent,
+                     const int32_t *node_tokens, int B, int N, int V, int dtype, float temperature,
+                     uint64_t seed, int max_depth, int32_t *out_path, int32_t *out_len, void *stream_ptr) {
+  return tree_sample_impl(target_logits, draft_logits, parent, 0, node_tokens, B, N, V, dtype, temperature, seed,
+                          max_depth, out_path, out_len, stream_ptr);
+}
+
+int spec_verify_trees(const void *target_logits, const void *draft_logits, const int32_t *parents,
+                      const int32_t *node_tokens, int B, int N, int V, int dtype, float temperature,
+                      uint64_t seed, int max_depth, int32_t *out_path, int32_t *out_len, void *stream_ptr) {
+  return tree_sample_impl(target_logits, draft_logits, parents, N, node_tokens, B, N, V, dtype, temperature, seed,
+                          max_depth, out_path, out_len, stream_ptr);
 }
 
 int spec_tree_max_depth(const int32_t *parent_host, int N) {
@@ -791,7 +825,7 @@ int spec_eagle2_rerank(const float *node_values, const int32_t *node_parents, co
   int st = get_ws(stream, 1, &w);
   if (st) return st;
   const void *fn = reinterpret_cast<const void *>(&rerank_kernel);
-  const int smem = 16 * M + 4 * m;
+  const int smem = 20 * M + 4 * m;
   int per_sm = 0;
   if ((st = occupancy(fn, smem, 0, &per_sm))) return st;
   if (per_sm < 1) return fail(SPEC_ERR_UNSUPPORTED, "rerank kernel does not fit on an SM");

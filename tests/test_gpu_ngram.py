@@ -2,8 +2,9 @@
 the oracle: bit-exact drafts and counts on seeded contexts: repetitive
 code-editing-like contexts, tiny alphabets (many overlapping matches), runs
 of one token, the page's worked example, ragged and degenerate lengths,
-unaligned rows (the scalar-load variant), batch sizes that select every
-cluster size, min_hits > 1, and the two full-size drafting workloads."""
+unaligned rows (the scalar-load variant), batch sizes from one sequence
+(hundreds of CTAs each) to a thousand (one CTA each), forced CTA counts,
+min_hits > 1, and the two full-size drafting workloads."""
 import os
 
 import numpy as np
