@@ -62,6 +62,9 @@ def _load():
         lib.oracle_verify_tree_sample.restype = i32
         lib.oracle_ngram_propose.argtypes = [c_p, c_p, i32, i32, i32, i32, i32, i32, c_p, c_p]
         lib.oracle_ngram_propose.restype = i32
+        lib.oracle_verify_points.argtypes = [c_p, c_p, c_p, i32, i32, i32, i32, ctypes.c_double, u64, c_p, c_p, c_p,
+                                             c_p, i32]
+        lib.oracle_verify_points.restype = i32
         lib.oracle_topk_prob.argtypes = [c_p, i32, i32, i32, ctypes.c_double, i32, c_p, c_p]
         lib.oracle_topk_prob.restype = i32
         lib.oracle_eagle2_expand.argtypes = [c_p, i32, i32, i32, c_p, c_p, c_p, c_p, c_p, i32, i32, i32, c_p, c_p]
@@ -365,3 +368,24 @@ def eagle2_rerank(node_val, node_par, node_tok, m: int):
     if st != OK:
         raise ValueError("oracle_eagle2_rerank: invalid arguments")
     return op, ot, oi, near.astype(bool)
+
+
+def verify_points(zt, x, counts, T: float, seed: int, *, b_ids=None, nthreads=1):
+    """Verification of point-mass drafts (a deterministic drafter such as the
+    n-gram drafter): zt [nb, K+1, V], x [nb, K], counts [nb] or None (all K).
+    Returns a dict with tokens [nb, K+1], n [nb], near [nb] bool, status."""
+    zt_a, dt = _logits(zt)
+    nb, K1, V = zt_a.shape
+    K = K1 - 1
+    xs = _i32(x).reshape(nb, K)
+    cn = None if counts is None else _i32(counts).reshape(nb)
+    bi = None if b_ids is None else _i32(b_ids).reshape(nb)
+    tokens = np.zeros((nb, K + 1), dtype=np.int32)
+    n = np.zeros(nb, dtype=np.int32)
+    near = np.zeros(nb, dtype=np.int32)
+    st = _load().oracle_verify_points(_ptr(zt_a), _ptr(xs), _ptr(cn), nb, K, V, dt, float(T),
+                                      int(seed) & ((1 << 64) - 1), _ptr(bi), _ptr(tokens), _ptr(n), _ptr(near),
+                                      int(nthreads))
+    if st == ERR_ARG:
+        raise ValueError("oracle_verify_points: invalid arguments")
+    return dict(tokens=tokens, n=n, near=near.astype(bool), status=st)

@@ -388,6 +388,97 @@ int oracle_verify_chain(const void *zt, const void *zd, const int32_t *x,
 }
 
 /* ------------------------------------------------------------------ */
+/* Verification of drafts from a deterministic drafter: the n-gram        */
+/* drafter ([Glukhov] §"Спекулятивное декодирование на n-граммах")       */
+/* proposes tokens, not a distribution.  Reading taken: the chain rule    */
+/* ([Oscine] §"验收标准的精确数学", §"拒绝之后怎么办？——残差分布") with    */
+/* q_i the point mass at x_i: accept x_i iff u < p_i(x_i); at the first   */
+/* reject j draw from max(0, p_j - q_j), i.e. p_j with x_j removed        */
+/* (weights exp((z_j(v) - m_j)/T) for v != x_j); if all k drafts of the   */
+/* sequence are accepted, the bonus comes from p_k.  Each sequence has    */
+/* its own draft count k = counts[s] in [0, K] (NULL: K); drafts past it  */
+/* are not read.  Uniforms as the chain: (b, i, 0) for the test of x_i,   */
+/* (b, n, 1) for the draw at n.  T == 0: greedy matching of the k drafts. */
+/*   zt: [nb, K+1, V], x: [nb, K], out_tokens: [nb, K+1], out_n: [nb]     */
+/* ------------------------------------------------------------------ */
+int oracle_verify_points(const void *zt, const int32_t *x, const int32_t *counts,
+                         int nb, int K, int V, int dtype, double T, uint64_t seed,
+                         const int32_t *b_ids, int32_t *out_tokens, int32_t *out_n,
+                         int32_t *out_near, int nthreads) {
+  if (nb < 0 || K < 0 || V <= 0 || (dtype != 0 && dtype != 1) || !(T >= 0.0))
+    return ORC_ERR_ARG;
+  int status = ORC_OK;
+  if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads) \
+    reduction(max : status)
+  for (int s = 0; s < nb; ++s) {
+    uint32_t b = b_ids ? (uint32_t)b_ids[s] : (uint32_t)s;
+    const void *zt_seq = row_ptr(zt, dtype, (int64_t)s * (K + 1), V);
+    const int32_t *xs = x + (size_t)s * K;
+    int32_t *tokens = out_tokens + (size_t)s * (K + 1);
+    int k = counts ? counts[s] : K;
+    int near = 0, bad = k < 0 || k > K;
+    for (int i = 0; i <= K; ++i) tokens[i] = -1;
+    for (int i = 0; !bad && i < k; ++i)
+      if (xs[i] < 0 || xs[i] >= V) bad = 1;
+    if (bad) {
+      out_n[s] = -1;
+      if (out_near) out_near[s] = 0;
+      status = ORC_ERR_TOKEN;
+      continue;
+    }
+    int n = k, tok = -1;
+    double *w = T > 0.0 ? (double *)malloc(sizeof(double) * (size_t)V) : NULL;
+    for (int i = 0; i < k; ++i) {
+      const void *row = row_ptr(zt_seq, dtype, i, V);
+      if (T == 0.0) {
+        int a = oracle_argmax(row, dtype, V);
+        if (xs[i] != a) {
+          n = i;
+          tok = a;
+          break;
+        }
+        continue;
+      }
+      double m, S;
+      oracle_row_stats(row, dtype, V, T, &m, &S);
+      double r = prob_at(row, dtype, xs[i], T, m, S); /* p(x) / q(x), q(x) = 1 */
+      double u = oracle_uniform(seed, b, (uint32_t)i, 0u);
+      double scale = r > 1.0 / 16777216.0 ? r : 1.0 / 16777216.0;
+      if (fabs(u - r) <= 1e-5 * scale) near = 1;
+      if (!(u < r)) {
+        double Z = 0.0;
+        for (int v = 0; v < V; ++v) {
+          w[v] = v == xs[i] ? 0.0 : exp((logit_at(row, dtype, v) - m) / T);
+          Z += w[v];
+        }
+        int nr = 0;
+        tok = inverse_cdf(w, V, Z, oracle_uniform(seed, b, (uint32_t)i, 1u), &nr);
+        near |= nr;
+        n = i;
+        break;
+      }
+    }
+    if (n == k) {
+      const void *row = row_ptr(zt_seq, dtype, k, V);
+      if (T == 0.0) {
+        tok = oracle_argmax(row, dtype, V);
+      } else {
+        int nr = 0;
+        tok = oracle_target_sample(row, dtype, V, T, oracle_uniform(seed, b, (uint32_t)k, 1u), &nr);
+        near |= nr;
+      }
+    }
+    free(w);
+    for (int i = 0; i < n; ++i) tokens[i] = xs[i];
+    tokens[n] = tok;
+    out_n[s] = n;
+    if (out_near) out_near[s] = near;
+  }
+  return status;
+}
+
+/* ------------------------------------------------------------------ */
 /* Draft tree ([Infra53] §3 and §8: node 0 is the root, every parent     */
 /* precedes its child, parent[0] = -1; depth = parent's depth + 1).      */
 /* ------------------------------------------------------------------ */
