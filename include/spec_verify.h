@@ -290,6 +290,30 @@ int spec_tree_mask(const int32_t *parent, int B, int N, uint32_t *out_mask,
                    int32_t *out_depth, void *stream);
 
 /*
+ * spec_verify_points — chain verification of drafts from a deterministic
+ * drafter, such as spec_ngram_propose, which proposes tokens but no
+ * distribution ([Glukhov] §"Спекулятивное декодирование на n-граммах").
+ * Reading taken: the chain rule of spec_verify with q_i the point mass at
+ * x_i: x_i is accepted iff u < p_i(x_i); at the first reject j the token is
+ * drawn from max(0, p_j - q_j), i.e. p_j without x_j; if all k drafts are
+ * accepted the bonus comes from p_k.  Equal to spec_verify with draft logits
+ * that are 0 at x_i and -inf elsewhere, without reading any draft rows.
+ *   target_logits [B, K+1, V]; draft_tokens [B, K] (device)
+ *   draft_counts  [B] int32 (device) or NULL: sequence b verifies its first
+ *                 k = draft_counts[b] drafts (0 <= k <= K; the rest are not
+ *                 read, e.g. -1 from spec_ngram_propose) and draws its bonus
+ *                 from p_k (target row k)
+ *   out_tokens [B, K+1]: accepted drafts, the new token, then -1;
+ *   out_n_accepted [B].  T = 0 is greedy matching of the k drafts.
+ * Uniforms, errors and limits as spec_verify; a count outside [0, K] is
+ * reported like an out-of-range token.
+ */
+int spec_verify_points(const void *target_logits, const int32_t *draft_tokens,
+                       const int32_t *draft_counts, int B, int K, int V, int dtype,
+                       float temperature, uint64_t seed, int32_t *out_tokens,
+                       int32_t *out_n_accepted, void *stream);
+
+/*
  * spec_ngram_propose — n-gram (prompt-lookup) drafting: for each of B
  * contexts, the up to K tokens that followed an earlier occurrence of the
  * context's own last n tokens ([Glukhov] §"Спекулятивное декодирование на

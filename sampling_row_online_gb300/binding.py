@@ -59,6 +59,7 @@ def library():
     lib.spec_tree_mask.argtypes = [vp, i32, i32, vp, vp, vp]
     lib.spec_ngram_propose.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.spec_topk.argtypes = [vp, i32, i32, i32, f32, i32, vp, vp, vp]
+    lib.spec_verify_points.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, u64, vp, vp, vp]
     lib.spec_eagle2_expand.argtypes = [vp, vp, i32, i32, i32, i32, f32, i32, vp, vp, vp, i32, i32, i32, vp, vp]
     lib.spec_eagle2_rerank.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]
     lib.spec_get_status.argtypes = [vp]
@@ -296,6 +297,39 @@ def spec_tree_mask(parent, *, stream=None):
         st = lib.spec_tree_mask(_ptr(parent), B, N, _ptr(mask), _ptr(depth), _stream(stream))
     _check(st, "spec_tree_mask")
     return mask, depth
+
+
+def spec_verify_points(target_logits, draft_tokens, temperature, seed, *, draft_counts=None, out_tokens=None,
+                       out_n=None, stream=None):
+    """Chain verification of point-mass drafts (a deterministic drafter such as
+    spec_ngram_propose).  target_logits [B, K+1, V]; draft_tokens [B, K] int32;
+    draft_counts [B] int32 or None (all K).  Returns (out_tokens [B, K+1],
+    n_accepted [B])."""
+    lib = library()
+    _dev(target_logits, "target_logits")
+    _dev(draft_tokens, "draft_tokens", torch.int32)
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, K+1, V]")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    if tuple(draft_tokens.shape) != (B, K):
+        raise ValueError("draft_tokens must be [B, K]")
+    if draft_counts is not None:
+        _dev(draft_counts, "draft_counts", torch.int32)
+        if tuple(draft_counts.shape) != (B,):
+            raise ValueError("draft_counts must be [B]")
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if out_n is None:
+        out_n = torch.empty((B,), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.spec_verify_points(_ptr(target_logits), _ptr(draft_tokens), _ptr(draft_counts), B, K, V,
+                                    _dtype_code(target_logits), ctypes.c_float(temperature),
+                                    ctypes.c_uint64(int(seed) & ((1 << 64) - 1)), _ptr(out_tokens), _ptr(out_n),
+                                    _stream(stream))
+    _check(st, "spec_verify_points")
+    return out_tokens, out_n
 
 
 def spec_ngram_propose(tokens, lengths, n_min, n_max, K, *, min_hits=1, out_draft=None, out_count=None,

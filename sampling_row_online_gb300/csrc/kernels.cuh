@@ -75,6 +75,8 @@ struct Params {
   const int32_t *tokens;    // chain: draft tokens [B, K]; tree: node tokens [B, N]
   const int32_t *parent;    // tree: [N]
   int parent_stride;        // 0: one tree for the batch; N: tree b at parent + b * N
+  const int32_t *counts;    // chain: drafts of each sequence [B] in [0, K] (NULL: K)
+  int point;                // chain: q is the point mass at each draft token (no draft rows)
   int B, K, V, J;           // K = drafts (chain) or N (tree)
   int kind;
   float c;                  // log2(e) / T
@@ -342,7 +344,8 @@ struct ItemCursor {
     int b, i;
     decode_job(p, q, b, i);
     rt = target_row<DT>(p, b, i) + static_cast<size_t>(lo) * E::BYTES;
-    const bool pair = p.kind == KIND_TREE_SAMPLE ? ((tree_internal[i >> 5] >> (i & 31)) & 1u) != 0 : i < p.K;
+    const bool pair = p.kind == KIND_TREE_SAMPLE ? ((tree_internal[i >> 5] >> (i & 31)) & 1u) != 0
+                                                 : (i < p.K && !p.point);
     if (!ARGMAX && pair) {
       rd = draft_row<DT>(p, b, i) + static_cast<size_t>(lo) * E::BYTES;
       nrows = 2;
@@ -681,11 +684,18 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
 struct Weights {
   float c, mtc, mdc, inv_st, inv_sd;
   bool resid;
+  int excl;  // point-mass drafts: the rejected draft token, whose weight is 0
   __device__ __forceinline__ float operator()(float zt, float zd) const {
     const float et = ex2(fmaf(zt, c, -mtc));
     if (!resid) return et;
     const float ed = ex2(fmaf(zd, c, -mdc));
     return fmaxf(__fsub_rn(__fmul_rn(et, inv_st), __fmul_rn(ed, inv_sd)), 0.f);
+  }
+  // Point-mass residual max(0, p - q) with q the point mass at excl: p(v)
+  // rounded as fmul(et, inv_st) for v != excl (exactly the residual of a
+  // one-hot draft row, whose q is 0 there), 0 at excl.
+  __device__ __forceinline__ float at(float zt, float, int v) const {
+    return v == excl ? 0.f : __fmul_rn(ex2(fmaf(zt, c, -mtc)), inv_st);
   }
 };
 
@@ -954,7 +964,7 @@ struct DrawSlice {
 // coalesced 16-byte loads, four per row in flight per lane) into
 // sh.wmass[warp]; each CTA's mass goes into sh.xz[slot][rank] of every CTA;
 // after the cluster barrier every thread of every CTA gets the same total Z.
-template <int DT, bool TMA>
+template <int DT, bool TMA, bool EXCL = false>
 __device__ __forceinline__ float cluster_weigh(const unsigned char *rt, const unsigned char *rd, const Weights &W,
                                                const DrawSlice &ds, int slot, uint32_t rank, uint32_t CD,
                                                DrawShared &sh) {
@@ -981,13 +991,15 @@ __device__ __forceinline__ float cluster_weigh(const unsigned char *rt, const un
         E::unpack(vt[k], ft);
         E::unpack(vd[k], fd);
 #pragma unroll
-        for (int e = 0; e < VE; ++e) acc = __fadd_rn(acc, W(ft[e], fd[e]));
+        for (int e = 0; e < VE; ++e)
+          acc = __fadd_rn(acc, EXCL ? W.at(ft[e], fd[e], ds.lo + (j + 32 * k) * VE + e) : W(ft[e], fd[e]));
       }
     }
   } else {
     const int e0 = min(ds.len, v0 * VE), e1 = min(ds.len, v1 * VE);
     for (int e = e0 + lane; e < e1; e += 32)
-      acc = __fadd_rn(acc, W(E::load(rt, ds.lo + e), W.resid ? E::load(rd, ds.lo + e) : 0.f));
+      acc = __fadd_rn(acc, EXCL ? W.at(E::load(rt, ds.lo + e), W.resid ? E::load(rd, ds.lo + e) : 0.f, ds.lo + e)
+                                : W(E::load(rt, ds.lo + e), W.resid ? E::load(rd, ds.lo + e) : 0.f));
   }
   acc = warp_sum(acc);
   if (lane == 0) sh.wmass[warp] = acc;
@@ -1038,7 +1050,7 @@ __device__ __forceinline__ void find_owner_cta(float u, float Z, int slot, uint3
 // In the owner CTA (after find_owner_cta): the warp range holding t, its
 // weights into wbuf, and the block-wide walk.  Returns the token in every
 // thread.  sh.wmass must still hold this CTA's warp masses of the same W.
-template <int DT>
+template <int DT, bool EXCL = false>
 __device__ __forceinline__ int owner_walk(const unsigned char *rt, const unsigned char *rd, const Weights &W,
                                           const DrawSlice &ds, float *wbuf, DrawShared &sh) {
   using E = Elem<DT>;
@@ -1075,7 +1087,8 @@ __device__ __forceinline__ int owner_walk(const unsigned char *rt, const unsigne
   const int r0 = min(ds.len, ow * ds.nvw * VE);
   const int rlen = min(ds.len, (ow + 1) * ds.nvw * VE) - r0;
   for (int e = tid; e < rlen; e += NT)
-    wbuf[e] = W(E::load(rt, ds.lo + r0 + e), W.resid ? E::load(rd, ds.lo + r0 + e) : 0.f);
+    wbuf[e] = EXCL ? W.at(E::load(rt, ds.lo + r0 + e), W.resid ? E::load(rd, ds.lo + r0 + e) : 0.f, ds.lo + r0 + e)
+                   : W(E::load(rt, ds.lo + r0 + e), W.resid ? E::load(rd, ds.lo + r0 + e) : 0.f);
   const float Pw = sh.bf[2], tw = sh.bf[1];
   const bool lastw = sh.bi[7] != 0;
   __syncthreads();
@@ -1111,14 +1124,19 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   // grid to complete before touching memory)
   pdl_launch_dependents();
 
-  // ---- inputs (not produced by the first launch): tokens, their logits, uniforms
+  // ---- inputs (not produced by the first launch): the draft count, tokens,
+  // their logits, uniforms.  A point-mass draft has draft logit 0 at x and
+  // draft normalisers (0, 1), so q(x) = 1.
+  const int kc = p.counts ? __ldg(p.counts + b) : K;
+  const bool bad_count = kc < 0 || kc > K;
+  const int kb = bad_count ? 0 : kc;  // drafts of this sequence
   for (int i = tid; i < K; i += NT) {
     const int x = __ldg(p.tokens + static_cast<size_t>(b) * K + i);
-    const int ok = x >= 0 && x < p.V;
+    const int ok = i >= kb || (x >= 0 && x < p.V);  // drafts past the count are not read
     gtok[i] = x;
     gok[i] = ok;
-    gx[2 * i] = ok ? E::load(target_row<DT>(p, b, i), x) : 0.f;
-    gx[2 * i + 1] = ok ? E::load(draft_row<DT>(p, b, i), x) : 0.f;
+    gx[2 * i] = (ok && i < kb) ? E::load(target_row<DT>(p, b, i), x) : 0.f;
+    gx[2 * i + 1] = (ok && i < kb && !p.point) ? E::load(draft_row<DT>(p, b, i), x) : 0.f;
     gu[i] = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
   }
   pdl_wait();  // the row partials of the first launch are complete and visible
@@ -1129,23 +1147,24 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   const int nparts = p.C * NCW;
   for (int i = warp; i <= K; i += NWARP) {
     float mt, st, md, sd;
-    warp_job_norms(p.partials + static_cast<size_t>(job_of(p, b, i)) * nparts, nparts, c, i < K, mt, st, md, sd);
+    warp_job_norms(p.partials + static_cast<size_t>(job_of(p, b, i)) * nparts, nparts, c, i < K && !p.point, mt,
+                   st, md, sd);
     if (lane == 0) {
       rmax[i] = mt;
       rsum[i] = st;
       if (i < K) {
-        rmax[K + 1 + i] = md;
-        rsum[K + 1 + i] = sd;
+        rmax[K + 1 + i] = p.point ? 0.f : md;
+        rsum[K + 1 + i] = p.point ? 1.f : sd;
       }
     }
   }
   __syncthreads();
 
-  // ---- the K acceptance tests (one thread each); n = the first reject, or K
-  if (tid == 0) sh.bi[0] = K;
+  // ---- the kb acceptance tests (one thread each); n = the first reject, or kb
+  if (tid == 0) sh.bi[0] = kb;
   __syncthreads();
-  int bad = 0;
-  for (int i = tid; i < K; i += NT) {
+  int bad = bad_count;
+  for (int i = tid; i < kb; i += NT) {
     bad |= !gok[i];
     const float a = fmaf(gx[2 * i], c, -(rmax[i] * c));
     const float d = fmaf(gx[2 * i + 1], c, -(rmax[K + 1 + i] * c));
@@ -1172,21 +1191,22 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   cluster_wait();  // every peer is running (pairs with the arrive above)
   if (err) return;
 
-  if (n == K) {
-    // ---- bonus: rank 0 draws from p_K using the streaming partials
+  if (n == kb) {
+    // ---- bonus: rank 0 draws from p at position kb using the streaming
+    // partials (the target half of a pair job's partials when kb < K)
     if (rank == 0) {
-      const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(K), 1u);
+      const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(kb), 1u);
       const int token = draw_p_from_partials<DT>(
-          p, p.partials + static_cast<size_t>(job_of(p, b, K)) * nparts, target_row<DT>(p, b, K), rmax[K], u,
+          p, p.partials + static_cast<size_t>(job_of(p, b, kb)) * nparts, target_row<DT>(p, b, kb), rmax[kb], u,
           wbuf, sh);
       if (tid < 32) {
         for (int j = lane; j <= K; j += 32)
-          out[j] = j < K ? gtok[j] : token;
+          out[j] = j < kb ? gtok[j] : (j == kb ? token : -1);
         if (lane == 0) {
-          p.out_n[b] = K;
+          p.out_n[b] = kb;
           if (p.stats) {
             atomicAdd(&p.stats->sequences, 1ull);
-            atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(K));
+            atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(kb));
             atomicAdd(&p.stats->bonus, 1ull);
           }
         }
@@ -1196,8 +1216,9 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   }
 
   // ---- the residual draw at position n
+  // (point mass: the residual max(0, p - q) is p without the draft token)
   const unsigned char *rt = target_row<DT>(p, b, n);
-  const unsigned char *rd = draft_row<DT>(p, b, n);
+  const unsigned char *rd = p.point ? rt : draft_row<DT>(p, b, n);
   DrawSlice ds;
   ds.set(static_cast<int>(rank), p.slice_d, p.V, VE);
   Weights W;
@@ -1206,21 +1227,24 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   W.mdc = rmax[K + 1 + n] * c;
   W.inv_st = 1.f / rsum[n];
   W.inv_sd = 1.f / rsum[K + 1 + n];
-  W.resid = true;
+  W.resid = !p.point;
+  W.excl = p.point ? gtok[n] : -1;
   const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(n), 1u);
   int fallback = 0, slot = 0;
-  float Z = cluster_weigh<DT, TMA>(rt, rd, W, ds, slot, rank, CD, sh);
+  float Z = p.point ? cluster_weigh<DT, TMA, true>(rt, rd, W, ds, slot, rank, CD, sh)
+                    : cluster_weigh<DT, TMA>(rt, rd, W, ds, slot, rank, CD, sh);
   if (!(Z > 0.f)) {  // no residual mass in fp32: draw from p at this position
     W.resid = false;
     fallback = 1;
     slot = 1;
-    Z = cluster_weigh<DT, TMA>(rt, rd, W, ds, slot, rank, CD, sh);
+    Z = p.point ? cluster_weigh<DT, TMA, true>(rt, rd, W, ds, slot, rank, CD, sh)
+                : cluster_weigh<DT, TMA>(rt, rd, W, ds, slot, rank, CD, sh);
   }
   if (tid == 0) find_owner_cta(u, Z, slot, CD, sh);
   __syncthreads();
   // No DSMEM access follows the last exchange, so only the owner CTA goes on.
   if (static_cast<int>(rank) != sh.bi[2]) return;
-  const int token = owner_walk<DT>(rt, rd, W, ds, wbuf, sh);
+  const int token = p.point ? owner_walk<DT, true>(rt, rd, W, ds, wbuf, sh) : owner_walk<DT>(rt, rd, W, ds, wbuf, sh);
   if (tid < 32) {
     for (int j = lane; j <= K; j += 32)
       out[j] = j < n ? gtok[j] : (j == n ? token : -1);
@@ -1376,6 +1400,7 @@ __global__ void __launch_bounds__(NT, 4) tree_draw_kernel(const Params p) {
     W.mdc = md * c;
     W.inv_st = 1.f / st;
     W.resid = true;
+    W.excl = -1;
     const float inv_sd = 1.f / sd;
     float a = 0.f, Wk = 1.f;
     int next = -1, vanished = 0, last_slot = 0;
@@ -1480,11 +1505,13 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
         if (p.out_row_sumexp) p.out_row_sumexp[static_cast<size_t>(b) * R + r] = NAN;
       }
     if (tid == 0) {
-      int nacc = K, err = 0;
-      for (int e = 0; e < K; ++e) {
+      const int kc = p.counts ? __ldg(p.counts + b) : K;  // drafts of this sequence
+      const int kb = (kc < 0 || kc > K) ? 0 : kc;
+      int nacc = kb, err = kc < 0 || kc > K;
+      for (int e = 0; e < kb; ++e) {
         const int x = s_tok[e];
         if (x < 0 || x >= p.V) err = 1;
-        if (nacc == K && x != s_amax[e]) nacc = e;
+        if (nacc == kb && x != s_amax[e]) nacc = e;
       }
       int32_t *out = p.out_tokens + static_cast<size_t>(b) * (K + 1);
       for (int e = 0; e <= K; ++e)
@@ -1497,7 +1524,7 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
         } else {
           atomicAdd(&p.stats->sequences, 1ull);
           atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(nacc));
-          atomicAdd(nacc == K ? &p.stats->bonus : &p.stats->resampled, 1ull);
+          atomicAdd(nacc == kb ? &p.stats->bonus : &p.stats->resampled, 1ull);
         }
       }
     }

@@ -402,9 +402,12 @@ int check_common(const void *zt, int B, int V, int dtype) {
   return SPEC_OK;
 }
 
+// Chain verification.  point: q is the point mass at each draft token (no
+// draft rows); counts: drafts per sequence [B] (NULL: K).
 int verify_chain(const void *zt, const void *zd, const int32_t *x, int B, int K, int V, int dtype,
                  float T, uint64_t seed, int32_t *out_tokens, int32_t *out_n, float *row_max,
-                 float *row_sumexp, spec_stats_t *stats, void *stream_ptr) {
+                 float *row_sumexp, spec_stats_t *stats, void *stream_ptr, const int32_t *counts = nullptr,
+                 bool point = false) {
   int st = check_common(zt, B, V, dtype);
   if (st) return st;
   if (K < 0 || K > SPEC_MAX_DRAFTS) return fail(SPEC_ERR_ARG, "K out of range [0, 255]");
@@ -414,18 +417,20 @@ int verify_chain(const void *zt, const void *zd, const int32_t *x, int B, int K,
   if (B == 0) return SPEC_OK;
   if (!out_tokens || !out_n) return fail(SPEC_ERR_ARG, "output pointer is NULL");
   if (K > 0 && !x) return fail(SPEC_ERR_ARG, "draft_tokens is NULL");
-  if (K > 0 && T > 0.f && !zd) return fail(SPEC_ERR_ARG, "draft_logits is NULL with T > 0");
+  if (K > 0 && T > 0.f && !zd && !point) return fail(SPEC_ERR_ARG, "draft_logits is NULL with T > 0");
   if (static_cast<long long>(B) * (K + 1) * MAX_CLUSTER > INT_MAX) return fail(SPEC_ERR_ARG, "B*(K+1) too large");
 
   const int esz = dtype == SPEC_F32 ? 4 : 2;
   const bool sample = T > 0.f;
   const bool tma = (static_cast<long long>(V) * esz) % 16 == 0 && aligned16(zt) &&
-                   (!sample || K == 0 || aligned16(zd));
+                   (!sample || K == 0 || point || aligned16(zd));
   Params p = {};
   p.zt = zt;
-  p.zd = zd;
+  p.zd = point ? nullptr : zd;
   p.tokens = x;
   p.parent = nullptr;
+  p.counts = counts;
+  p.point = point && sample;
   p.B = B;
   p.K = K;
   p.V = V;
@@ -535,6 +540,13 @@ int spec_verify(const void *target_logits, const void *draft_logits, const int32
                 int32_t *out_tokens, int32_t *out_n_accepted, void *stream) {
   return verify_chain(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed,
                       out_tokens, out_n_accepted, nullptr, nullptr, nullptr, stream);
+}
+
+int spec_verify_points(const void *target_logits, const int32_t *draft_tokens, const int32_t *draft_counts, int B,
+                       int K, int V, int dtype, float temperature, uint64_t seed, int32_t *out_tokens,
+                       int32_t *out_n_accepted, void *stream) {
+  return verify_chain(target_logits, nullptr, draft_tokens, B, K, V, dtype, temperature, seed, out_tokens,
+                      out_n_accepted, nullptr, nullptr, nullptr, stream, draft_counts, true);
 }
 
 int spec_verify_ex(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
