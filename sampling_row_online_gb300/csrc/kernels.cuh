@@ -281,9 +281,9 @@ __device__ __forceinline__ float block_exclusive_scan(float v, float *sh, float 
 // Argmax kinds: rows position-major.
 __device__ __forceinline__ void decode_job(const Params &p, int q, int &b, int &i) {
   if (p.kind == KIND_SAMPLE) {
-    const int k = q / p.B;
-    b = q - k * p.B;
-    i = k < p.K ? p.K - 1 - k : p.K;
+    const int k = q / p.B;  // the bonus rows first (never re-read), then pairs K-1 .. 0:
+    b = q - k * p.B;         // the pairs a residual most often re-reads are streamed last
+    i = k == 0 ? p.K : p.K - k;
   } else {
     i = q / p.B;
     b = q - i * p.B;
@@ -291,7 +291,7 @@ __device__ __forceinline__ void decode_job(const Params &p, int q, int &b, int &
 }
 
 __device__ __forceinline__ int job_of(const Params &p, int b, int i) {
-  if (p.kind == KIND_SAMPLE) return (i == p.K ? p.K : p.K - 1 - i) * p.B + b;
+  if (p.kind == KIND_SAMPLE) return (i == p.K ? 0 : p.K - i) * p.B + b;
   return i * p.B + b;
 }
 
