@@ -426,6 +426,16 @@ int spec_get_status(void *stream);
  */
 int spec_arm_rows_event(void *event);
 
+/*
+ * spec_selftest_wait — diagnostic of the bounded waits every kernel uses on
+ * its barriers: one thread waits on a barrier that nothing completes; the
+ * wait gives up after its limit (about one second), the kernel records a
+ * timeout and returns.  The next spec_get_status on `stream` then returns
+ * SPEC_ERR_TIMEOUT, and the stream stays usable.  Returns SPEC_OK once
+ * launched.
+ */
+int spec_selftest_wait(void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *spec_error_string(int status);
 

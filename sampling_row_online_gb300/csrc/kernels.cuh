@@ -1577,6 +1577,21 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
 }
 
 // ======================================================================
+// Self-test of the bounded waits: one thread waits, with the wait the row
+// kernel uses, on an mbarrier that nothing arrives at.  The wait gives up
+// after its limit (about a second), records ST_TIMEOUT and the kernel
+// returns normally, so the context stays usable.
+// ======================================================================
+__global__ void wait_selftest_kernel(int32_t *status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_bounded(&bar, 0)) atomicOr(status, ST_TIMEOUT);  // phase 0 never completes
+  }
+}
+
+// ======================================================================
 // Tree-attention mask and depth position IDs, one CTA per tree.
 // ======================================================================
 __global__ void __launch_bounds__(NT) tree_mask_kernel(const int32_t *parent, int N, int W,

@@ -855,6 +855,17 @@ int spec_eagle2_rerank(const float *node_values, const int32_t *node_parents, co
   return launch_eagle(fn, ep, B, smem, stream, "rerank_kernel launch");
 }
 
+int spec_selftest_wait(void *stream_ptr) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  Workspace *w = nullptr;
+  int st = get_ws(stream, 1, &w);
+  if (st) return st;
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(w->status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "wait_selftest_kernel launch");
+  return SPEC_OK;
+}
+
 int spec_arm_rows_event(void *event) {
   g_rows_event = static_cast<cudaEvent_t>(event);
   return SPEC_OK;

@@ -1,0 +1,35 @@
+"""The bounded waits end: a kernel waiting on a barrier that nothing
+completes gives up after its limit, the library reports SPEC_ERR_TIMEOUT,
+and the stream and context stay usable (a verification call right after
+matches the oracle)."""
+import ctypes
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sampling_row_online_gb300 import binding
+from sampling_row_online_gb300.workloads import Workload, make_chain
+
+pytestmark = pytest.mark.gpu
+
+
+def test_a_wait_that_never_completes_times_out():
+    lib = binding.library()
+    stream = torch.cuda.current_stream()
+    assert binding.spec_get_status() == 0
+    t0 = time.perf_counter()
+    assert lib.spec_selftest_wait(ctypes.c_void_p(stream.cuda_stream)) == 0
+    assert binding.spec_get_status() == 6                      # SPEC_ERR_TIMEOUT
+    waited = time.perf_counter() - t0
+    assert 0.5 < waited < 30.0
+    assert binding.spec_get_status() == 0                      # read once, then cleared
+    w = Workload("after", "chain", B=8, K=4, V=4096, dtype="f32", T=1.0, data_seed=17)
+    zt, zd, x = make_chain(w, device="cuda")
+    out, n = binding.spec_verify(zt, zd, x, 1.0, 5)
+    assert binding.spec_get_status() == 0
+    ref = oracle.verify_chain(zt.cpu(), zd.cpu(), x.cpu(), 1.0, 5)
+    keep = ~ref["near"]
+    assert np.array_equal(n.cpu().numpy()[keep], ref["n_accepted"][keep])
