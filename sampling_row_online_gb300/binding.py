@@ -429,6 +429,14 @@ def spec_eagle2_rerank(node_values, node_parents, node_tokens, m, *, stream=None
     return tuple(out)
 
 
+def spec_selftest_wait(stream=None) -> int:
+    """Launches the bounded-wait self-test on the stream and returns the status
+    the next spec_get_status reports (SPEC_ERR_TIMEOUT when the wait ended by
+    its limit, after about a second)."""
+    _check(library().spec_selftest_wait(_stream(stream)), "spec_selftest_wait")
+    return spec_get_status(stream)
+
+
 def spec_get_status(stream=None) -> int:
     """Waits for the stream; returns (and clears) the device-side status code."""
     return int(library().spec_get_status(_stream(stream)))
