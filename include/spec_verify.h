@@ -429,12 +429,22 @@ int spec_arm_rows_event(void *event);
 /*
  * spec_selftest_wait — diagnostic of the bounded waits every kernel uses on
  * its barriers: one thread waits on a barrier that nothing completes; the
- * wait gives up after its limit (about one second), the kernel records a
+ * wait gives up after one second of global time or 2^17 polls, whichever
+ * comes first (about half a second on GB300), the kernel records a
  * timeout and returns.  The next spec_get_status on `stream` then returns
  * SPEC_ERR_TIMEOUT, and the stream stays usable.  Returns SPEC_OK once
  * launched.
  */
 int spec_selftest_wait(void *stream);
+
+/*
+ * spec_debug_fail_launch — fault injection for tests of the error paths: the
+ * n-th kernel launch from now (counting every launch of this library, n >=
+ * 1) fails with a launch error instead of launching; the call that made it
+ * returns SPEC_ERR_CUDA and leaves the stream's workspace ready for the next
+ * call.  n = 0 switches it off.  No GPU fault is involved.
+ */
+int spec_debug_fail_launch(int n);
 
 /* Static, human-readable name of a status code. */
 const char *spec_error_string(int status);

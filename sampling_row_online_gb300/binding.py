@@ -60,6 +60,7 @@ def library():
     lib.spec_ngram_propose.argtypes = [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.spec_topk.argtypes = [vp, i32, i32, i32, f32, i32, vp, vp, vp]
     lib.spec_selftest_wait.argtypes = [vp]
+    lib.spec_debug_fail_launch.argtypes = [i32]
     lib.spec_verify_points.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, u64, vp, vp, vp]
     lib.spec_eagle2_expand.argtypes = [vp, vp, i32, i32, i32, i32, f32, i32, vp, vp, vp, i32, i32, i32, vp, vp]
     lib.spec_eagle2_rerank.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, vp]

@@ -2,8 +2,10 @@
 // (cluster size, slices, tiles, stages), per-stream workspaces and the C ABI
 // declared in include/spec_verify.h.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdio>
@@ -22,6 +24,25 @@ namespace spec {
 namespace {
 
 thread_local std::string g_last_error;
+
+// Fault injection for tests (spec_debug_fail_launch): the n-th launch from
+// now reports cudaErrorLaunchFailure without launching.  0: off.
+std::atomic<int> g_fail_launch{0};
+
+cudaError_t launch_kernel(const cudaLaunchConfig_t *cfg, const void *fn, void **args) {
+  int n = g_fail_launch.load();
+  while (n > 0 && !g_fail_launch.compare_exchange_weak(n, n - 1)) {
+  }
+  if (n == 1) return cudaErrorLaunchFailure;  // this launch is the injected failure
+  return cudaLaunchKernelExC(cfg, fn, args);
+}
+
+// An NVTX range around each entry point (free when no tool is attached), so
+// that profilers can attribute kernels to calls.
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 int fail(int code, const std::string &msg) {
   g_last_error = msg;
@@ -331,7 +352,7 @@ int launch(Params &p, const Geometry &g, cudaStream_t stream, float4 *partials, 
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
     void *args[] = {&p};
-    e = cudaLaunchKernelExC(&cfg, g.fa, args);
+    e = launch_kernel(&cfg, g.fa, args);
     if (e != cudaSuccess) return cuda_fail(e, "row kernel launch");
   }
   if (ev_rows && (e = cudaEventRecord(ev_rows, stream)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
@@ -359,7 +380,7 @@ int launch(Params &p, const Geometry &g, cudaStream_t stream, float4 *partials, 
   cfg.attrs = attr;
   cfg.numAttrs = na;
   void *args[] = {&p};
-  e = cudaLaunchKernelExC(&cfg, g.fb, args);
+  e = launch_kernel(&cfg, g.fb, args);
   if (e != cudaSuccess) {
     // the decision kernel puts the tickets back to zero; without it, do it here
     cudaMemsetAsync(p.tickets, 0, sizeof(int) * NSHARD * TICKET_STRIDE, stream);
@@ -507,7 +528,7 @@ int launch_topk(TopkParams &p, int dtype, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   void *args[] = {&p};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  cudaError_t e = launch_kernel(&cfg, fn, args);
   if (e != cudaSuccess) return cuda_fail(e, "topk_kernel launch");
   return SPEC_OK;
 }
@@ -524,7 +545,7 @@ int launch_eagle(const void *fn, EagleParams &p, int grid, int smem, cudaStream_
   cfg.attrs = &pdl;
   cfg.numAttrs = 1;
   void *args[] = {&p};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  cudaError_t e = launch_kernel(&cfg, fn, args);
   if (e != cudaSuccess) return cuda_fail(e, what);
   return SPEC_OK;
 }
@@ -538,6 +559,7 @@ extern "C" {
 int spec_verify(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
                 int B, int K, int V, int dtype, float temperature, uint64_t seed,
                 int32_t *out_tokens, int32_t *out_n_accepted, void *stream) {
+  NvtxRange nvtx_range("spec_verify");
   return verify_chain(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed,
                       out_tokens, out_n_accepted, nullptr, nullptr, nullptr, stream);
 }
@@ -545,6 +567,7 @@ int spec_verify(const void *target_logits, const void *draft_logits, const int32
 int spec_verify_points(const void *target_logits, const int32_t *draft_tokens, const int32_t *draft_counts, int B,
                        int K, int V, int dtype, float temperature, uint64_t seed, int32_t *out_tokens,
                        int32_t *out_n_accepted, void *stream) {
+  NvtxRange nvtx_range("spec_verify_points");
   return verify_chain(target_logits, nullptr, draft_tokens, B, K, V, dtype, temperature, seed, out_tokens,
                       out_n_accepted, nullptr, nullptr, nullptr, stream, draft_counts, true);
 }
@@ -553,6 +576,7 @@ int spec_verify_ex(const void *target_logits, const void *draft_logits, const in
                    int B, int K, int V, int dtype, float temperature, uint64_t seed,
                    int32_t *out_tokens, int32_t *out_n_accepted, float *out_row_max,
                    float *out_row_sumexp, spec_stats_t *stats, void *stream) {
+  NvtxRange nvtx_range("spec_verify_ex");
   return verify_chain(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed,
                       out_tokens, out_n_accepted, out_row_max, out_row_sumexp, stats, stream);
 }
@@ -636,6 +660,7 @@ static int tree_sample_impl(const void *target_logits, const void *draft_logits,
 int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent, const int32_t *node_tokens,
                             int B, int N, int V, int dtype, int max_depth, int32_t *out_path,
                             int32_t *out_len, void *stream_ptr) {
+  NvtxRange nvtx_range("spec_verify_tree_greedy");
   return tree_greedy_impl(target_logits, parent, 0, node_tokens, B, N, V, dtype, max_depth, out_path, out_len,
                           stream_ptr);
 }
@@ -643,6 +668,7 @@ int spec_verify_tree_greedy(const void *target_logits, const int32_t *parent, co
 int spec_verify_trees_greedy(const void *target_logits, const int32_t *parents, const int32_t *node_tokens,
                              int B, int N, int V, int dtype, int max_depth, int32_t *out_path,
                              int32_t *out_len, void *stream_ptr) {
+  NvtxRange nvtx_range("spec_verify_trees_greedy");
   return tree_greedy_impl(target_logits, parents, N, node_tokens, B, N, V, dtype, max_depth, out_path, out_len,
                           stream_ptr);
 }
@@ -650,6 +676,7 @@ int spec_verify_trees_greedy(const void *target_logits, const int32_t *parents, 
 int spec_verify_tree(const void *target_logits, const void *draft_logits, const int32_t *parent,
                      const int32_t *node_tokens, int B, int N, int V, int dtype, float temperature,
                      uint64_t seed, int max_depth, int32_t *out_path, int32_t *out_len, void *stream_ptr) {
+  NvtxRange nvtx_range("spec_verify_tree");
   return tree_sample_impl(target_logits, draft_logits, parent, 0, node_tokens, B, N, V, dtype, temperature, seed,
                           max_depth, out_path, out_len, stream_ptr);
 }
@@ -657,6 +684,7 @@ int spec_verify_tree(const void *target_logits, const void *draft_logits, const 
 int spec_verify_trees(const void *target_logits, const void *draft_logits, const int32_t *parents,
                       const int32_t *node_tokens, int B, int N, int V, int dtype, float temperature,
                       uint64_t seed, int max_depth, int32_t *out_path, int32_t *out_len, void *stream_ptr) {
+  NvtxRange nvtx_range("spec_verify_trees");
   return tree_sample_impl(target_logits, draft_logits, parents, N, node_tokens, B, N, V, dtype, temperature, seed,
                           max_depth, out_path, out_len, stream_ptr);
 }
@@ -669,6 +697,7 @@ int spec_tree_max_depth(const int32_t *parent_host, int N) {
 
 int spec_tree_mask(const int32_t *parent, int B, int N, uint32_t *out_mask, int32_t *out_depth,
                    void *stream_ptr) {
+  NvtxRange nvtx_range("spec_tree_mask");
   if (B < 0) return fail(SPEC_ERR_ARG, "B must be >= 0");
   if (N < 1 || N > SPEC_MAX_TREE_NODES) return fail(SPEC_ERR_ARG, "N out of range [1, 1024]");
   if (B == 0) return SPEC_OK;
@@ -678,14 +707,20 @@ int spec_tree_mask(const int32_t *parent, int B, int N, uint32_t *out_mask, int3
   int st = get_ws(stream, 1, &w);
   if (st) return st;
   const int W = (N + 31) / 32;
-  tree_mask_kernel<<<B, NT, 0, stream>>>(parent, N, W, out_mask, out_depth, w->status);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(B), 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.stream = stream;
+  int32_t *status = w->status;
+  void *args[] = {(void *)&parent, (void *)&N, (void *)&W, (void *)&out_mask, (void *)&out_depth, (void *)&status};
+  cudaError_t e = launch_kernel(&cfg, reinterpret_cast<const void *>(&tree_mask_kernel), args);
   if (e != cudaSuccess) return cuda_fail(e, "tree_mask_kernel launch");
   return SPEC_OK;
 }
 
 int spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int L, int n_min, int n_max,
                        int min_hits, int K, int32_t *out_draft, int32_t *out_count, void *stream_ptr) {
+  NvtxRange nvtx_range("spec_ngram_propose");
   if (B < 0 || L < 0) return fail(SPEC_ERR_ARG, "B and L must be >= 0");
   if (n_min < 1 || n_max < n_min || n_max > SPEC_MAX_NGRAM)
     return fail(SPEC_ERR_ARG, "need 1 <= n_min <= n_max <= 64");
@@ -744,13 +779,14 @@ int spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int
   cfg.attrs = &pdl;
   cfg.numAttrs = 1;
   void *args[] = {&p};
-  cudaError_t e = cudaLaunchKernelExC(&cfg, fns[vec][mode], args);
+  cudaError_t e = launch_kernel(&cfg, fns[vec][mode], args);
   if (e != cudaSuccess) return cuda_fail(e, "ngram_kernel launch");
   return SPEC_OK;
 }
 
 int spec_topk(const void *logits, int R, int V, int dtype, float temperature, int k, int32_t *out_tokens,
               float *out_prob, void *stream_ptr) {
+  NvtxRange nvtx_range("spec_topk");
   int st = check_topk_args(R, V, dtype, temperature, k);
   if (st) return st;
   if (R == 0) return SPEC_OK;
@@ -774,6 +810,7 @@ int spec_topk(const void *logits, int R, int V, int dtype, float temperature, in
 int spec_eagle2_expand(const void *draft_logits, const int32_t *frontier, int B, int F, int V, int dtype,
                        float temperature, int k, int32_t *node_tokens, float *node_values, int32_t *node_parents,
                        int cap, int offset, int k_next, int32_t *out_frontier, void *stream_ptr) {
+  NvtxRange nvtx_range("spec_eagle2_expand");
   if (B < 0 || F < 1) return fail(SPEC_ERR_ARG, "need B >= 0 and F >= 1");
   int st = check_topk_args(B, V, dtype, temperature, k);
   if (st) return st;
@@ -826,6 +863,7 @@ int spec_eagle2_expand(const void *draft_logits, const int32_t *frontier, int B,
 int spec_eagle2_rerank(const float *node_values, const int32_t *node_parents, const int32_t *node_tokens, int B,
                        int M, int m, int32_t *out_parent, int32_t *out_tokens, int32_t *out_index,
                        void *stream_ptr) {
+  NvtxRange nvtx_range("spec_eagle2_rerank");
   if (B < 0) return fail(SPEC_ERR_ARG, "B must be >= 0");
   if (M < 1 || M > SPEC_EAGLE_MAX_NODES) return fail(SPEC_ERR_ARG, "M out of range [1, 8192]");
   if (m < 0 || m > M - 1) return fail(SPEC_ERR_ARG, "need 0 <= m <= M - 1");
@@ -856,13 +894,25 @@ int spec_eagle2_rerank(const float *node_values, const int32_t *node_parents, co
 }
 
 int spec_selftest_wait(void *stream_ptr) {
+  NvtxRange nvtx_range("spec_selftest_wait");
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   Workspace *w = nullptr;
   int st = get_ws(stream, 1, &w);
   if (st) return st;
-  wait_selftest_kernel<<<1, 32, 0, stream>>>(w->status);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.stream = stream;
+  int32_t *status = w->status;
+  void *args[] = {&status};
+  cudaError_t e = launch_kernel(&cfg, reinterpret_cast<const void *>(&wait_selftest_kernel), args);
   if (e != cudaSuccess) return cuda_fail(e, "wait_selftest_kernel launch");
+  return SPEC_OK;
+}
+
+int spec_debug_fail_launch(int n) {
+  if (n < 0) return fail(SPEC_ERR_ARG, "n must be >= 0");
+  g_fail_launch.store(n);
   return SPEC_OK;
 }
 
@@ -897,6 +947,7 @@ int spec_get_status(void *stream_ptr) {
 int spec_verify_host(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
                      int B, int K, int V, int dtype, float temperature, uint64_t seed,
                      int32_t *out_tokens, int32_t *out_n_accepted, void *stream_ptr) {
+  NvtxRange nvtx_range("spec_verify_host");
   int st = check_common(target_logits, B, V, dtype);
   if (st) return st;
   if (K < 0 || K > SPEC_MAX_DRAFTS) return fail(SPEC_ERR_ARG, "K out of range [0, 255]");
@@ -1032,6 +1083,7 @@ extern "C" int spec_verify_noalloc(const void *target_logits, const void *draft_
                                    const int32_t *draft_tokens, int B, int K, int V, int dtype,
                                    float temperature, uint64_t seed, int32_t *out_tokens,
                                    int32_t *out_n_accepted, void *stream_ptr) {
+  NvtxRange nvtx_range("spec_verify_noalloc");
   using namespace spec;
   int st = check_common(target_logits, B, V, dtype);
   if (st) return st;

@@ -29,7 +29,7 @@ def test_header_declares_the_boundary():
     for required in ("spec_verify", "spec_verify_tree_greedy", "spec_verify_tree", "spec_verify_ex", "spec_verify_host",
                      "spec_tree_max_depth", "spec_tree_mask", "spec_ngram_propose", "spec_topk",
                      "spec_eagle2_expand", "spec_eagle2_rerank", "spec_verify_trees_greedy",
-                     "spec_verify_trees", "spec_verify_points", "spec_selftest_wait", "spec_get_status",
+                     "spec_verify_trees", "spec_verify_points", "spec_selftest_wait", "spec_debug_fail_launch", "spec_get_status",
                      "spec_error_string", "spec_last_error_message", "spec_shutdown"):
         assert required in names
 

@@ -1,7 +1,9 @@
 """The library's calls inside CUDA graphs: captured once (after a warm-up
 call that sizes the stream's workspace), replayed with new input contents
 copied into the captured tensors, and compared with eager calls on the same
-inputs (bit-identical: the same kernels, the same uniforms)."""
+inputs (bit-identical: the same kernels, the same uniforms).  The side stream
+waits for the default stream before its first call: tensors made there may
+still be in flight, and their blocks may still be in use by queued kernels."""
 import pytest
 import torch
 
@@ -25,6 +27,7 @@ def test_chain_verification_in_a_graph():
     zt, zd, x = make_chain(w, device="cuda")
     out = torch.empty((w.B, w.K + 1), dtype=torch.int32, device="cuda")
     n = torch.empty((w.B,), dtype=torch.int32, device="cuda")
+    s.wait_stream(torch.cuda.current_stream())      # inputs and outputs were made on the default stream
     with torch.cuda.stream(s):
         binding.spec_verify(zt, zd, x, w.T, 9, out_tokens=out, out_n_accepted=n, stream=s)   # sizes the workspace
     s.synchronize()
@@ -56,6 +59,7 @@ def test_ngram_draft_and_point_verification_in_one_graph():
                                    stream=s)
         binding.spec_verify_points(zt, draft, 1.0, 4, draft_counts=count, out_tokens=out, out_n=n, stream=s)
 
+    s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         step()
     s.synchronize()
@@ -96,6 +100,7 @@ def test_eagle2_budget_in_a_graph():
         for dst, src in zip(kept, res):
             dst.copy_(src)
 
+    s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         build()
     s.synchronize()

@@ -20,7 +20,10 @@ def test_a_wait_that_never_completes_times_out():
     t0 = time.perf_counter()
     assert binding.spec_selftest_wait() == 6                   # SPEC_ERR_TIMEOUT
     waited = time.perf_counter() - t0
-    assert 0.5 < waited < 30.0
+    # the wait gives up at 1 s of global time or after 2^17 polls, whichever
+    # comes first; a poll suspends for at most 20 us and may wake sooner, so the
+    # floor only shows that the kernel did wait
+    assert 0.02 < waited < 30.0
     assert binding.spec_get_status() == 0                      # read once, then cleared
     w = Workload("after", "chain", B=8, K=4, V=4096, dtype="f32", T=1.0, data_seed=17)
     zt, zd, x = make_chain(w, device="cuda")
