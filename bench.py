@@ -739,7 +739,7 @@ def run_gpu_eagle2(args, w):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_one)]
     flush = torch.empty(256 * 2**20 // 4, dtype=torch.float32, device=dev)
     for k in range(n_one):
-        flush.fill_(1.0)   # the rows of one step (33 MB) fit in L2: write 256 MB between calls
+        flush.fill_(1.0)   # the rows of one step (65.7 MB) fit in L2: write 256 MB between calls
         ev[k][0].record(stream)
         lib.spec_topk(*ta)
         ev[k][1].record(stream)

@@ -113,7 +113,9 @@ __device__ __forceinline__ void topk_online(float x, float c, float &m, float &s
   }
 }
 
-constexpr int TOPK_U = 8;  // 16-byte loads in flight per thread
+// 16-byte loads per thread per round; pass 1 issues the next round's loads
+// before it weighs the current one, so up to 2 * TOPK_U are in flight
+constexpr int TOPK_U = 4;
 
 // Element e (0 <= e < VE, a run-time value) of a packed 16-byte vector.
 template <int DT>
@@ -233,36 +235,33 @@ __global__ void __launch_bounds__(NT, 4) topk_kernel(TopkParams p) {
   // pass 1: online (max, sum) and the thread's own largest logit
   float m = -INFINITY, s = 0.f, tmax = -INFINITY;
   if (VEC) {
+    // the streaming kernel's per-vector update (packed maxima, paired sums);
+    // the online state's maximum is the thread's own largest logit
+    Online st;
+    st.init();
     const uint4 *rv = reinterpret_cast<const uint4 *>(row);
+    // thread (warp, lane) reads vectors lo + warp * 32 + lane + j * NT
+    auto fetch = [&](uint4 (&d)[TOPK_U], int b) {
+#pragma unroll
+      for (int u = 0; u < TOPK_U; ++u) {
+        const int vi = b + u * NT + lane;
+        d[u] = vi < hi ? __ldg(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    uint4 q[TOPK_U];
+    fetch(q, lo + warp * 32);
     for (int base = lo + warp * 32; base < hi; base += TOPK_U * NT) {  // warp-uniform
-      uint4 q[TOPK_U];
+      uint4 nq[TOPK_U];
+      fetch(nq, base + TOPK_U * NT);  // the next round, in flight while this one is weighed
 #pragma unroll
-      for (int u = 0; u < TOPK_U; ++u) {
-        const int vi = base + u * NT + lane;
-        q[u] = vi < hi ? __ldg(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
-      }
+      for (int u = 0; u < TOPK_U; ++u)
+        if (base + u * NT + lane < hi) online_vec16<DT>(q[u], p.c, st);
 #pragma unroll
-      for (int u = 0; u < TOPK_U; ++u) {
-        const int vi = base + u * NT + lane;
-        if (vi < hi) {
-          float f[VE];
-          Elem<DT>::unpack(q[u], f);
-          float vm = f[0];
-#pragma unroll
-          for (int e = 1; e < VE; ++e) vm = fmaxf(vm, f[e]);
-          tmax = fmaxf(tmax, vm);
-          if (vm > m) {
-            s *= ex2((m - vm) * p.c);
-            m = vm;
-          }
-          if (m != -INFINITY) {
-            const float mc = m * p.c;
-#pragma unroll
-            for (int e = 0; e < VE; ++e) s += ex2(fmaf(f[e], p.c, -mc));
-          }
-        }
-      }
+      for (int u = 0; u < TOPK_U; ++u) q[u] = nq[u];
     }
+    m = st.m;
+    s = st.sum();
+    tmax = st.m;
   } else {
     for (int i = lo + tid; i < hi; i += NT) {
       const float x = Elem<DT>::load(row, i);
@@ -297,31 +296,50 @@ __global__ void __launch_bounds__(NT, 4) topk_kernel(TopkParams p) {
 
   // pass 2: the elements >= t lie in the vectors of "hot" threads (their own
   // maximum reaches t); each warp re-reads its hot lanes' vectors together,
-  // one vector per lane, and appends the keys of elements >= t
+  // one vector per lane, HB hot lanes at a time (their loads in flight
+  // together), and appends the keys of elements >= t
   {
     unsigned hot = __ballot_sync(0xFFFFFFFFu, tmax >= t);
-    while (hot) {
-      const int h = __ffs(hot) - 1;
-      hot &= hot - 1u;
-      if (VEC) {
-        const uint4 *rv = reinterpret_cast<const uint4 *>(row);
-        const int first = lo + warp * 32 + h;  // lane h's vectors: first + j * NT
-        for (int j0 = 0; first + j0 * NT < hi; j0 += 32) {  // warp-uniform
-          const int vi = first + (j0 + lane) * NT;
-          if (vi < hi) {
-            const uint4 q = __ldg(rv + vi);
+    if (VEC) {
+      constexpr int HB = 4;
+      const uint4 *rv = reinterpret_cast<const uint4 *>(row);
+      const int wfirst = lo + warp * 32;  // lane h's vectors: wfirst + h + j * NT
+      while (hot) {  // warp-uniform
+        int first[HB];
+#pragma unroll
+        for (int g = 0; g < HB; ++g) {
+          first[g] = hot ? wfirst + __ffs(hot) - 1 : hi;  // hi: no lane in this slot
+          hot &= hot - 1u;
+        }
+        // first[0] is the smallest, so its vectors bound the others'
+        for (int j0 = 0; first[0] + j0 * NT < hi; j0 += 32) {  // warp-uniform
+          uint4 q[HB];
+          int vi[HB];
+#pragma unroll
+          for (int g = 0; g < HB; ++g) {
+            vi[g] = first[g] + (j0 + lane) * NT;
+            q[g] = vi[g] < hi ? __ldg(rv + vi[g]) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int g = 0; g < HB; ++g) {
+            if (vi[g] >= hi) continue;
             float f[VE];
-            Elem<DT>::unpack(q, f);
+            Elem<DT>::unpack(q[g], f);
 #pragma unroll
             for (int e = 0; e < VE; ++e) {
               if (f[e] >= t) {
                 const int slot = atomicAdd(&sh.nbuf, 1);
-                if (slot < TOPK_BUF) sh.buf[slot] = topk_key(f[e], vi * VE + e);
+                if (slot < TOPK_BUF) sh.buf[slot] = topk_key(f[e], vi[g] * VE + e);
               }
             }
           }
         }
-      } else {
+      }
+    }
+    while (!VEC && hot) {
+      const int h = __ffs(hot) - 1;
+      hot &= hot - 1u;
+      {
         const int first = lo + warp * 32 + h;  // lane h's elements: first + j * NT (see pass 1)
         for (int j0 = 0; first + j0 * NT < hi; j0 += 32) {
           const int i = first + (j0 + lane) * NT;
