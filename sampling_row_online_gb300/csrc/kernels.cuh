@@ -273,11 +273,10 @@ __device__ __forceinline__ float block_exclusive_scan(float v, float *sh, float 
 }
 
 // ------------------------------------------------------------ job layout
-// Job q -> (sequence b, row i).  Stochastic chain: the row pairs from
-// position K-1 down to 0, so the rows a residual draw most often needs (the
-// early positions) are streamed late and are still in L2 when the draw runs,
-// then the B bonus rows (single-row items, half the size, end the stream:
-// the last items finish close together; a bonus draw reads no row again).
+// Job q -> (sequence b, row i).  Stochastic chain: the B bonus rows first (a
+// bonus draw reads no row again), then the row pairs from position K-1 down
+// to 0, so the pairs a residual draw most often re-reads (the early
+// positions) are streamed last and are still in L2 when the draw runs.
 // Argmax kinds: rows position-major.
 __device__ __forceinline__ void decode_job(const Params &p, int q, int &b, int &i) {
   if (p.kind == KIND_SAMPLE) {
