@@ -414,8 +414,8 @@ int spec_get_status(void *stream);
 
 /*
  * spec_arm_rows_event — measurement hook.  The next verification call that
- * launches (spec_verify, spec_verify_ex, spec_verify_noalloc or
- * spec_verify_tree_greedy) made by the calling host thread records `event`
+ * launches (any spec_verify* entry point: chains, point-mass drafts, trees)
+ * made by the calling host thread records `event`
  * (a cudaEvent_t created by the caller, passed as void*) on its stream right
  * after launching its streaming kernel (the row statistics) and before its
  * decision kernel; the hook is then disarmed.  An event the caller records

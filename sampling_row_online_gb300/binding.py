@@ -69,6 +69,7 @@ def library():
     lib.spec_error_string.restype = ctypes.c_char_p
     lib.spec_last_error_message.argtypes = []
     lib.spec_last_error_message.restype = ctypes.c_char_p
+    lib.spec_verify_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, u64, vp, vp, vp]
     lib.spec_shutdown.argtypes = []
     lib.spec_shutdown.restype = None
     for name in ("spec_verify", "spec_verify_ex", "spec_verify_host", "spec_verify_tree_greedy",
@@ -220,6 +221,31 @@ def _tree_parents(parent, B, N, max_depth):
     return False, spec_tree_max_depth(parent.cpu()) if max_depth is None else max_depth
 
 
+def spec_verify_noalloc(target_logits, draft_logits, draft_tokens, temperature, seed, *,
+                        out_tokens=None, out_n_accepted=None, stream=None):
+    """Chain verification on the library's fixed scratch (no device allocation
+    in the call; calls that overlap on the GPU must be serialised).  Returns
+    (out_tokens [B, K+1] int32, n_accepted [B] int32)."""
+    lib = library()
+    _dev(target_logits, "target_logits")
+    B, K, V = _chain_shapes(target_logits, draft_logits, draft_tokens)
+    _dev(draft_logits, "draft_logits")
+    _dev(draft_tokens, "draft_tokens", torch.int32)
+    dev = target_logits.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if out_n_accepted is None:
+        out_n_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    _dev(out_tokens, "out_tokens", torch.int32)
+    _dev(out_n_accepted, "out_n_accepted", torch.int32)
+    with torch.cuda.device(dev):
+        st = lib.spec_verify_noalloc(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, K, V,
+                                     _dtype_code(target_logits), float(temperature), int(seed) & (2 ** 64 - 1),
+                                     _ptr(out_tokens), _ptr(out_n_accepted), _stream(stream))
+    _check(st, "spec_verify_noalloc")
+    return out_tokens, out_n_accepted
+
+
 def spec_verify_tree_greedy(target_logits, parent, node_tokens, *, max_depth=None,
                             out_path=None, out_len=None, stream=None):
     """Greedy tree verification; parent [N] (one tree) or [B, N] (one tree per
@@ -280,6 +306,26 @@ def spec_verify_tree(target_logits, draft_logits, parent, node_tokens, temperatu
                                   int(max_depth), _ptr(out_path), _ptr(out_len), _stream(stream))
     _check(st, "spec_verify_tree")
     return out_path, out_len
+
+
+def spec_verify_trees_greedy(target_logits, parent, node_tokens, *, max_depth=None, out_path=None,
+                             out_len=None, stream=None):
+    """Greedy verification of one tree per sequence: parent [B, N] int32.
+    Returns (out_path [B, D+1] int32, out_len [B] int32)."""
+    if parent.dim() != 2:
+        raise ValueError("parent must be [B, N] (one tree per sequence)")
+    return spec_verify_tree_greedy(target_logits, parent, node_tokens, max_depth=max_depth, out_path=out_path,
+                                   out_len=out_len, stream=stream)
+
+
+def spec_verify_trees(target_logits, draft_logits, parent, node_tokens, temperature, seed, *, max_depth=None,
+                      out_path=None, out_len=None, stream=None):
+    """Stochastic verification of one tree per sequence: parent [B, N] int32.
+    Returns (out_path [B, D+1] int32, out_len [B] int32)."""
+    if parent.dim() != 2:
+        raise ValueError("parent must be [B, N] (one tree per sequence)")
+    return spec_verify_tree(target_logits, draft_logits, parent, node_tokens, temperature, seed,
+                            max_depth=max_depth, out_path=out_path, out_len=out_len, stream=stream)
 
 
 def spec_tree_mask(parent, *, stream=None):
@@ -446,3 +492,29 @@ def spec_get_status(stream=None) -> int:
 def raise_on_device_error(stream=None):
     st = spec_get_status(stream)
     _check(st, "device")
+
+
+def spec_arm_rows_event(event):
+    """Measurement hook: the next verification call made from this thread
+    records `event` (a torch.cuda.Event that has been recorded once, so that
+    it exists) between its streaming and decision kernels."""
+    library().spec_arm_rows_event(ctypes.c_void_p(event.cuda_event))
+
+
+def spec_debug_fail_launch(n):
+    """Fault injection: the n-th next kernel launch of the library fails with a
+    launch error (n = 0 switches it off)."""
+    _check(library().spec_debug_fail_launch(int(n)), "spec_debug_fail_launch")
+
+
+def spec_error_string(status):
+    return library().spec_error_string(int(status)).decode()
+
+
+def spec_last_error_message():
+    return library().spec_last_error_message().decode(errors="replace")
+
+
+def spec_shutdown():
+    """Frees every workspace the library holds (no call may be in flight)."""
+    library().spec_shutdown()

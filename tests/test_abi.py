@@ -39,6 +39,14 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_binding_has_a_wrapper_of_the_same_name_for_every_declared_call():
+    import sampling_row_online_gb300 as pkg
+    from sampling_row_online_gb300 import binding
+    for name in _declared_functions():
+        assert callable(getattr(binding, name, None)), name
+        assert name in pkg.__all__, name
+
+
 def _verify(lib, **kw):
     a = dict(zt=ctypes.c_void_p(16), zd=ctypes.c_void_p(16), x=ctypes.c_void_p(16), B=2, K=3,
              V=100, dtype=1, T=1.0, seed=0, out=ctypes.c_void_p(16), n=ctypes.c_void_p(16),
