@@ -40,6 +40,38 @@ UNIT = "positions/s"
 LAUNCHES_PER_CALL = 2  # the streaming row kernel and the per-sequence decision kernel
 
 
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
+EX2_PER_SM_CLOCK = 16      # MUFU base-2 exponentials per SM per clock, nominal
+
+
+def _quantile(sorted_vals, q):
+    i = min(len(sorted_vals) - 1, max(0, int(round(q * (len(sorted_vals) - 1)))))
+    return sorted_vals[i]
+
+
+def _cpu_model():
+    """The host CPU's name from /proc/cpuinfo (x86: 'model name'; Arm:
+    implementer and part numbers), else the machine type."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        names = {"0xd4f": "Neoverse V2", "0xd40": "Neoverse V1", "0xd49": "Neoverse N2", "0xd0c": "Neoverse N1"}
+        part = fields["CPU part"]
+        return (f"{platform.machine()} {names.get(part, 'part ' + part)} "
+                f"(implementer {fields.get('CPU implementer', '?')}, part {part})")
+    return platform.machine()
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -313,6 +345,18 @@ def run_gpu(args, w):
     if lib.spec_get_status(sp) != 0:
         raise SystemExit("device status error in the kernel-timing loop")
     avg_launch_ms = max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in ev), dev)
+    launch_us = sorted(a.elapsed_time(b) * 1e3 for a, b in ev)
+    # the same kernel with warm L2: calls on one input copy, so the end of the
+    # previous call's stream is still resident
+    n_warm = min(n_rows, 50)
+    evw = ev[:n_warm]
+    calls[0]()
+    for k in range(n_warm):
+        evw[k][0].record(stream)
+        lib.spec_arm_rows_event(ctypes.c_void_p(evw[k][1].cuda_event))
+        calls[0]()
+    torch.cuda.synchronize()
+    warm_ms = max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in evw), dev)
     positions = w.positions * args.steps * ws
     value = positions / (region_ms / 1e3)
 
@@ -362,9 +406,20 @@ def run_gpu(args, w):
                           f"between its two launches (spec_arm_rows_event), mean of {n_rows} calls"),
                 "algorithmic_bytes_per_launch": w.algorithmic_bytes,
                 "avg_launch_us": avg_launch_ms * 1e3,
+                "launch_us_p10_median_p90": [_quantile(launch_us, q) for q in (0.1, 0.5, 0.9)],
+                "warm_avg_launch_us": warm_ms * 1e3,
+                "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                 "whole_call": {"achieved": call_achieved, "frac": call_achieved / peak,
                                "avg_call_us": call_ms * 1e3,
                                "timed": "region over the steps, calls chained back to back"}}
+    if w.T > 0:  # one MUFU ex2 per streamed logit
+        exps = w.algorithmic_bytes / (4 if w.dtype == "f32" else 2)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        mhz = (clk or {}).get("sm_mhz") or (clk or {}).get("sm_max_mhz") or 2070.0
+        exp_peak = sms * EX2_PER_SM_CLOCK * mhz * 1e6
+        roofline["exp"] = {"per_s": exps / (avg_launch_ms / 1e3), "peak_per_s": exp_peak,
+                           "frac": exps / (avg_launch_ms / 1e3) / exp_peak,
+                           "peak_basis": f"{sms} SMs x {EX2_PER_SM_CLOCK} ex2 per clock x {mhz:.0f} MHz"}
     # CPU baseline: the oracle as it stands on the host cores, bounded sample
     cpu = None
     if not args.no_cpu_baseline:
@@ -376,9 +431,14 @@ def run_gpu(args, w):
             secs += more
             reps += 1
         per_seq = w.positions // w.B
+        n1 = min(w.B, 16)
+        secs1, _ = time_oracle(w, n1, nthreads=1)
         cpu = {"value": nseq * reps * per_seq / secs, "unit": UNIT, "cores": threads,
                "kind": "oracle",
-               "sample": f"{reps} pass(es) over the {nseq} sequences of {w.name}, fp64 oracle"}
+               "sample": f"{reps} pass(es) over the {nseq} sequences of {w.name}, fp64 oracle",
+               "one_core": {"value": n1 * per_seq / secs1, "unit": UNIT,
+                            "sample": f"the first {n1} sequences of {w.name}, one thread"},
+               "cpu_model": _cpu_model(), "nproc": os.cpu_count()}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
