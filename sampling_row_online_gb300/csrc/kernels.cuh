@@ -1047,9 +1047,10 @@ __device__ __forceinline__ void find_owner_cta(float u, float Z, int slot, uint3
 }
 
 // In the owner CTA (after find_owner_cta): the warp range holding t, its
-// weights into wbuf, and the block-wide walk.  Returns the token in every
-// thread.  sh.wmass must still hold this CTA's warp masses of the same W.
-template <int DT, bool EXCL = false>
+// weights into wbuf (16-byte loads when the rows allow them, TMA), and the
+// block-wide walk.  Returns the token in every thread.  sh.wmass must still
+// hold this CTA's warp masses of the same W.
+template <int DT, bool TMA, bool EXCL = false>
 __device__ __forceinline__ int owner_walk(const unsigned char *rt, const unsigned char *rd, const Weights &W,
                                           const DrawSlice &ds, float *wbuf, DrawShared &sh) {
   using E = Elem<DT>;
@@ -1085,9 +1086,23 @@ __device__ __forceinline__ int owner_walk(const unsigned char *rt, const unsigne
   const int ow = sh.bi[6];
   const int r0 = min(ds.len, ow * ds.nvw * VE);
   const int rlen = min(ds.len, (ow + 1) * ds.nvw * VE) - r0;
-  for (int e = tid; e < rlen; e += NT)
-    wbuf[e] = EXCL ? W.at(E::load(rt, ds.lo + r0 + e), W.resid ? E::load(rd, ds.lo + r0 + e) : 0.f, ds.lo + r0 + e)
-                   : W(E::load(rt, ds.lo + r0 + e), W.resid ? E::load(rd, ds.lo + r0 + e) : 0.f);
+  if (TMA) {  // r0, rlen and the slice start are multiples of the vector width
+    for (int j = tid; j < rlen / VE; j += NT) {
+      const int e0 = ds.lo + r0 + j * VE;
+      const size_t off = static_cast<size_t>(e0) * E::BYTES;
+      const uint4 vt = __ldcg(reinterpret_cast<const uint4 *>(rt + off));
+      const uint4 vd = W.resid ? __ldcg(reinterpret_cast<const uint4 *>(rd + off)) : make_uint4(0, 0, 0, 0);
+      float ft[VE], fd[VE];
+      E::unpack(vt, ft);
+      E::unpack(vd, fd);
+#pragma unroll
+      for (int e = 0; e < VE; ++e) wbuf[j * VE + e] = EXCL ? W.at(ft[e], fd[e], e0 + e) : W(ft[e], fd[e]);
+    }
+  } else {
+    for (int e = tid; e < rlen; e += NT)
+      wbuf[e] = EXCL ? W.at(E::load(rt, ds.lo + r0 + e), W.resid ? E::load(rd, ds.lo + r0 + e) : 0.f, ds.lo + r0 + e)
+                     : W(E::load(rt, ds.lo + r0 + e), W.resid ? E::load(rd, ds.lo + r0 + e) : 0.f);
+  }
   const float Pw = sh.bf[2], tw = sh.bf[1];
   const bool lastw = sh.bi[7] != 0;
   __syncthreads();
@@ -1243,7 +1258,8 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   __syncthreads();
   // No DSMEM access follows the last exchange, so only the owner CTA goes on.
   if (static_cast<int>(rank) != sh.bi[2]) return;
-  const int token = p.point ? owner_walk<DT, true>(rt, rd, W, ds, wbuf, sh) : owner_walk<DT>(rt, rd, W, ds, wbuf, sh);
+  const int token = p.point ? owner_walk<DT, TMA, true>(rt, rd, W, ds, wbuf, sh)
+                            : owner_walk<DT, TMA>(rt, rd, W, ds, wbuf, sh);
   if (tid < 32) {
     for (int j = lane; j <= K; j += 32)
       out[j] = j < n ? gtok[j] : (j == n ? token : -1);
@@ -1442,7 +1458,7 @@ __global__ void __launch_bounds__(NT, 4) tree_draw_kernel(const Params p) {
       __syncthreads();
       // no DSMEM access follows the last exchange: only the owner CTA goes on
       if (static_cast<int>(rank) != sh.bi[2]) return;
-      token = owner_walk<DT>(rt, rd, W, ds, wbuf, sh);
+      token = owner_walk<DT, TMA>(rt, rd, W, ds, wbuf, sh);
     }
     for (int j = tid; j < W1; j += NT)
       if (j >= len) path[j] = j == len ? token : -1;
