@@ -1109,6 +1109,336 @@ __device__ __forceinline__ int owner_walk(const unsigned char *rt, const unsigne
   return ds.lo + r0 + block_walk(wbuf, rlen, Pw, tw, lastw, sh);
 }
 
+// ---------------------------------------------------------------- chain draw
+// The chain's single draw weighs one row pair (a residual) or one row (a
+// draw from p).  Each row's normaliser is folded into the exponent:
+// p(v) = 2^(z_t(v) c - lt) with lt = m_t c + log2 S_t, and q(v) likewise, so
+// a weight costs two paired FMAs and two MUFU exponentials per entry pair.
+enum WMode : int { W_RESID = 0, W_P = 1, W_P_EXCL = 2 };
+struct FoldedW {
+  float c, lt, ld;
+  int mode;  // W_RESID: max(0, p - q); W_P: p; W_P_EXCL: p, 0 at `excl`
+  int excl;  // point-mass drafts: the rejected draft token
+};
+
+// Weights of the VE entries of one vector whose first entry is e0, with
+// explicit roundings: every recomputation gives the same bits.
+template <int VE>
+__device__ __forceinline__ void vec_weights(const FoldedW &W, const float (&ft)[VE], const float (&fd)[VE],
+                                            int e0, float (&w)[VE]) {
+  const float2 cc = make_float2(W.c, W.c);
+  const float2 nt = make_float2(-W.lt, -W.lt), nd = make_float2(-W.ld, -W.ld);
+#pragma unroll
+  for (int e = 0; e < VE; e += 2) {
+    const float2 a = __ffma2_rn(make_float2(ft[e], ft[e + 1]), cc, nt);
+    const float2 pe = make_float2(ex2(a.x), ex2(a.y));
+    if (W.mode == W_RESID) {
+      const float2 d = __ffma2_rn(make_float2(fd[e], fd[e + 1]), cc, nd);
+      const float2 r = __ffma2_rn(make_float2(ex2(d.x), ex2(d.y)), make_float2(-1.f, -1.f), pe);  // p - q
+      w[e] = fmaxf(r.x, 0.f);
+      w[e + 1] = fmaxf(r.y, 0.f);
+    } else {
+      w[e] = (W.mode == W_P_EXCL && e0 + e == W.excl) ? 0.f : pe.x;
+      w[e + 1] = (W.mode == W_P_EXCL && e0 + e + 1 == W.excl) ? 0.f : pe.y;
+    }
+  }
+}
+
+// Mass of one vector, summed as a pairwise tree.
+template <int VE>
+__device__ __forceinline__ float vec_mass(const float (&w)[VE]) {
+  if constexpr (VE == 8) {
+    const float2 s1 = __fadd2_rn(make_float2(w[0], w[2]), make_float2(w[1], w[3]));  // w0+w1, w2+w3
+    const float2 s2 = __fadd2_rn(make_float2(w[4], w[6]), make_float2(w[5], w[7]));  // w4+w5, w6+w7
+    const float2 s3 = __fadd2_rn(make_float2(s1.x, s2.x), make_float2(s1.y, s2.y));
+    return __fadd_rn(s3.x, s3.y);
+  } else {
+    const float2 s1 = __fadd2_rn(make_float2(w[0], w[2]), make_float2(w[1], w[3]));
+    return __fadd_rn(s1.x, s1.y);
+  }
+}
+
+// Running masses of the entries of one vector along the same tree: pre is
+// non-decreasing, an entry of weight 0 leaves it unchanged, and
+// pre[VE - 1] equals vec_mass(w) bit for bit.
+template <int VE>
+__device__ __forceinline__ void vec_prefix(const float (&w)[VE], float (&pre)[VE]) {
+  const float s01 = __fadd_rn(w[0], w[1]), s23 = __fadd_rn(w[2], w[3]);
+  const float s0123 = __fadd_rn(s01, s23);
+  pre[0] = w[0];
+  pre[1] = s01;
+  pre[2] = __fadd_rn(s01, w[2]);
+  pre[3] = s0123;
+  if constexpr (VE == 8) {
+    const float s45 = __fadd_rn(w[4], w[5]), s67 = __fadd_rn(w[6], w[7]);
+    pre[4] = __fadd_rn(s0123, w[4]);
+    pre[5] = __fadd_rn(s0123, s45);
+    pre[6] = __fadd_rn(s0123, __fadd_rn(s45, w[6]));
+    pre[7] = __fadd_rn(s0123, __fadd_rn(s45, s67));
+  }
+}
+
+// The VE logits of one vector of a row; entries at or past V read as -inf
+// (weight 0).  VEC: the row is 16-byte aligned and e0 a multiple of VE.
+template <int DT, bool VEC>
+__device__ __forceinline__ void load_vec(const unsigned char *row, int e0, int V, float (&f)[Elem<DT>::VE]) {
+  using E = Elem<DT>;
+  if (VEC) {
+    E::unpack(__ldcg(reinterpret_cast<const uint4 *>(row + static_cast<size_t>(e0) * E::BYTES)), f);
+  } else {
+#pragma unroll
+    for (int e = 0; e < E::VE; ++e) f[e] = e0 + e < V ? E::load(row, e0 + e) : -INFINITY;
+  }
+}
+
+// This CTA's weighing of its slice of the draw: the mass of every vector into
+// wv[], each thread's sum over a contiguous chunk of vectors (cs), and a
+// block-wide exclusive scan of those sums (E).  Returns the CTA's mass in
+// every thread.  Loads are block-strided (coalesced) with BATCH vectors per
+// row in flight per thread.
+template <int DT, bool VEC>
+__device__ __forceinline__ float slice_weigh(const unsigned char *rt, const unsigned char *rd, const FoldedW &W,
+                                             const DrawSlice &ds, int V, float *wv, DrawShared &sh, float &E,
+                                             float &cs) {
+  using El = Elem<DT>;
+  constexpr int VE = El::VE;
+  const int tid = threadIdx.x;
+  const bool pair = W.mode == W_RESID;
+  if (VEC) {
+    constexpr int BATCH = 4;
+    for (int j0 = tid; j0 < ds.nv; j0 += NT * BATCH) {
+      uint4 vt[BATCH], vd[BATCH];
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) {
+        const int j = j0 + NT * k;
+        const size_t off = static_cast<size_t>(ds.lo + j * VE) * El::BYTES;
+        vt[k] = j < ds.nv ? __ldcg(reinterpret_cast<const uint4 *>(rt + off)) : make_uint4(0, 0, 0, 0);
+        vd[k] = (j < ds.nv && pair) ? __ldcg(reinterpret_cast<const uint4 *>(rd + off)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) {
+        const int j = j0 + NT * k;
+        if (j >= ds.nv) break;
+        float ft[VE], fd[VE], w[VE];
+        El::unpack(vt[k], ft);
+        El::unpack(vd[k], fd);
+        vec_weights<VE>(W, ft, fd, ds.lo + j * VE, w);
+        wv[j] = vec_mass<VE>(w);
+      }
+    }
+  } else {
+    for (int j = tid; j < ds.nv; j += NT) {
+      float ft[VE], fd[VE], w[VE];
+      load_vec<DT, false>(rt, ds.lo + j * VE, V, ft);
+      if (pair) load_vec<DT, false>(rd, ds.lo + j * VE, V, fd);
+      else
+#pragma unroll
+        for (int e = 0; e < VE; ++e) fd[e] = -INFINITY;
+      vec_weights<VE>(W, ft, fd, ds.lo + j * VE, w);
+      wv[j] = vec_mass<VE>(w);
+    }
+  }
+  __syncthreads();
+  const int cper = (ds.nv + NT - 1) / NT;
+  const int a0 = min(ds.nv, tid * cper), a1 = min(ds.nv, a0 + cper);
+  float s = 0.f;
+  for (int j = a0; j < a1; ++j) s = __fadd_rn(s, wv[j]);
+  cs = s;
+  float total;
+  E = block_exclusive_scan(s, sh.scan, &total);
+  return total;
+}
+
+// The thread whose running mass P + E + cs first passes t (threads with
+// positive mass only); if none does (rounding at the very end of the
+// distribution, or lastmode), the last thread with positive mass and
+// *lastmode = true.  Every thread gets the same answer.
+__device__ __forceinline__ int owner_thread(float P, float t, float E, float cs, bool &lastmode, DrawShared &sh) {
+  const int tid = threadIdx.x;
+  int who = INT_MAX;
+  if (!lastmode)
+    who = block_reduce_min_int((cs > 0.f && __fadd_rn(P, __fadd_rn(E, cs)) > t) ? tid : INT_MAX, sh.ired);
+  if (who == INT_MAX) {
+    lastmode = true;
+    who = max(0, block_reduce_max_int(cs > 0.f ? tid : -1, sh.ired));
+  }
+  return who;
+}
+
+// In the owner thread: the entry of vector (ft, fd, first entry e0) whose
+// running mass base(pre) passes t, where base(x) = P + (E + (cbefore + x));
+// else the last entry of positive weight.  Returns the entry's offset.
+template <int VE>
+__device__ __forceinline__ int vec_walk(const FoldedW &W, const float (&ft)[VE], const float (&fd)[VE], int e0,
+                                        float P, float E, float cbefore, float t, bool lastmode) {
+  float w[VE], pre[VE];
+  vec_weights<VE>(W, ft, fd, e0, w);
+  vec_prefix<VE>(w, pre);
+  int pick = -1, last = -1;
+#pragma unroll
+  for (int e = 0; e < VE; ++e) {
+    if (w[e] > 0.f) {
+      if (!lastmode && pick < 0 && __fadd_rn(P, __fadd_rn(E, __fadd_rn(cbefore, pre[e]))) > t) pick = e;
+      last = e;
+    }
+  }
+  return pick >= 0 ? pick : max(last, 0);
+}
+
+// The owner CTA's part of a cluster-wide draw: the owner thread (by the
+// running masses of the block scan), its vector (by the chunk's vector
+// masses in wv[]), that vector's entries re-read and walked.  Returns the
+// token in thread `who` (set in every thread).
+template <int DT, bool VEC>
+__device__ __forceinline__ int slice_owner_draw(const unsigned char *rt, const unsigned char *rd, const FoldedW &W,
+                                                const DrawSlice &ds, int V, const float *wv, float P, float t,
+                                                bool lastmode, float E, float cs, DrawShared &sh, int &who) {
+  constexpr int VE = Elem<DT>::VE;
+  const int tid = threadIdx.x;
+  who = owner_thread(P, t, E, cs, lastmode, sh);
+  if (tid != who) return -1;
+  const int cper = (ds.nv + NT - 1) / NT;
+  const int a0 = min(ds.nv, tid * cper), a1 = min(ds.nv, a0 + cper);
+  int jv = -1, jlast = -1;
+  float cpre = 0.f, cb = 0.f, cb_last = 0.f;
+  for (int j = a0; j < a1; ++j) {
+    const float before = cpre;
+    cpre = __fadd_rn(cpre, wv[j]);
+    if (wv[j] > 0.f) {
+      if (!lastmode && jv < 0 && __fadd_rn(P, __fadd_rn(E, cpre)) > t) {
+        jv = j;
+        cb = before;
+      }
+      jlast = j;
+      cb_last = before;
+    }
+  }
+  if (jv < 0) {
+    lastmode = true;
+    jv = jlast < 0 ? a0 : jlast;
+    cb = cb_last;
+  }
+  float ft[VE], fd[VE];
+  const int e0 = ds.lo + jv * VE;
+  load_vec<DT, VEC>(rt, e0, V, ft);
+  if (W.mode == W_RESID)
+    load_vec<DT, VEC>(rd, e0, V, fd);
+  else
+#pragma unroll
+    for (int e = 0; e < VE; ++e) fd[e] = -INFINITY;
+  return e0 + vec_walk<VE>(W, ft, fd, e0, P, E, cb, t, lastmode);
+}
+
+// Bonus draw from p (weights 2^(z c - M c)) of one target row by one CTA,
+// from the row's streaming partials: the partial of (slice s, consumer warp
+// w) is the mass of a contiguous vocabulary range, so warp 0 finds the range
+// holding u * Z from the partials alone (their masses kept in pm[]); one
+// thread per 16-byte vector of that range weighs it, a block scan over the
+// vector masses finds the owner thread, and that thread walks its vector
+// from registers.  Returns the token in thread `who` (set in every thread).
+template <int DT, bool VEC>
+__device__ __forceinline__ int bonus_draw(const Params &p, const float4 *parts, const unsigned char *row, float M,
+                                          float u, float *pm, DrawShared &sh, int &who) {
+  using El = Elem<DT>;
+  constexpr int VE = El::VE;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const float c = p.c, Mc = M * c;
+  const int nparts = p.C * NCW;
+  if (tid < 32) {
+    constexpr int BATCH = 4;
+    const int per = (nparts + 31) / 32;
+    const int j0 = min(nparts, lane * per), j1 = min(nparts, j0 + per);
+    float sum = 0.f;
+    for (int j = j0; j < j1; j += BATCH) {
+      float4 v[BATCH];
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) v[k] = j + k < j1 ? __ldcg(parts + j + k) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < BATCH; ++k) {
+        const float m = v[k].x == -INFINITY ? 0.f : __fmul_rn(v[k].y, ex2(fmaf(v[k].x, c, -Mc)));
+        if (j + k < j1) pm[j + k] = m;
+        sum = __fadd_rn(sum, m);
+      }
+    }
+    float Z;
+    const float excl = warp_excl_scan(sum, &Z);
+    const float t = u * Z;
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, sum > 0.f && __fadd_rn(excl, sum) > t);
+    const unsigned pos = __ballot_sync(0xFFFFFFFFu, sum > 0.f);
+    int lastmode = hit == 0;
+    const int wl = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+    if (lane == wl) {
+      float pre = 0.f, P = excl, Plast = excl;
+      int own = -1, lastj = j0;
+      for (int j = j0; j < j1; ++j) {
+        const float before = __fadd_rn(excl, pre);
+        pre = __fadd_rn(pre, pm[j]);
+        if (pm[j] > 0.f) {
+          if (!lastmode && own < 0 && __fadd_rn(excl, pre) > t) {
+            own = j;
+            P = before;
+          }
+          lastj = j;
+          Plast = before;
+        }
+      }
+      if (own < 0) {
+        own = lastj;
+        P = Plast;
+        lastmode = 1;
+      }
+      sh.bi[4] = own;
+      sh.bi[5] = lastmode;
+      sh.bf[4] = P;
+      sh.bf[5] = t;
+    }
+  }
+  __syncthreads();
+  const int own = sh.bi[4];
+  bool lastmode = sh.bi[5] != 0;
+  const float P = sh.bf[4], t = sh.bf[5];
+  // the owner range: slice sl, consumer warp w of the streaming split (its
+  // start is a multiple of VE; at most NT vectors)
+  const int sl = own / NCW, w = own - sl * NCW;
+  const int lo_s = sl * p.slice;
+  const int len_s = max(0, min(p.V, lo_s + p.slice) - lo_s);
+  const int nv = (len_s + VE - 1) / VE, nvw = (nv + NCW - 1) / NCW;
+  const int v0 = min(nv, w * nvw), v1 = min(nv, (w + 1) * nvw);
+  FoldedW W;
+  W.c = c;
+  W.lt = Mc;
+  W.ld = 0.f;
+  W.mode = W_P;
+  W.excl = -1;
+  float ft[VE], fd[VE], wt[VE];
+#pragma unroll
+  for (int e = 0; e < VE; ++e) ft[e] = fd[e] = -INFINITY;
+  float cs = 0.f;
+  const int e0 = lo_s + (v0 + tid) * VE;
+  if (v0 + tid < v1) {
+    load_vec<DT, VEC>(row, e0, p.V, ft);
+    vec_weights<VE>(W, ft, fd, e0, wt);
+    cs = vec_mass<VE>(wt);
+  }
+  float total;
+  const float E = block_exclusive_scan(cs, sh.scan, &total);
+  who = owner_thread(P, t, E, cs, lastmode, sh);
+  if (tid != who) return -1;
+  return e0 + vec_walk<VE>(W, ft, fd, e0, P, E, 0.f, t, lastmode);
+}
+
+// Every CTA's mass into slot `slot` of every CTA of the cluster; after the
+// cluster barrier every thread of every CTA sums them in rank order (the
+// same bits everywhere).
+__device__ __forceinline__ float cluster_exchange(float mass, int slot, uint32_t rank, uint32_t CD, DrawShared &sh) {
+  const int tid = threadIdx.x;
+  if (tid < static_cast<int>(CD)) dsmem_st_f32(dsmem_addr(&sh.xz[slot][rank], static_cast<uint32_t>(tid)), mass);
+  cluster_sync();
+  float Z = 0.f;
+  for (uint32_t r = 0; r < CD; ++r) Z = __fadd_rn(Z, sh.xz[slot][r]);
+  return Z;
+}
+
 template <int DT, bool TMA>
 __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   using E = Elem<DT>;
@@ -1174,18 +1504,31 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   }
   __syncthreads();
 
-  // ---- the kb acceptance tests (one thread each); n = the first reject, or kb
-  if (tid == 0) sh.bi[0] = kb;
-  __syncthreads();
-  int bad = bad_count;
-  for (int i = tid; i < kb; i += NT) {
-    bad |= !gok[i];
-    const float a = fmaf(gx[2 * i], c, -(rmax[i] * c));
-    const float d = fmaf(gx[2 * i + 1], c, -(rmax[K + 1 + i] * c));
-    const float ratio = ex2(a - d) * (rsum[K + 1 + i] / rsum[i]);  // p_i(x_i) / q_i(x_i)
-    if (!(gu[i] < ratio)) atomicMin(&sh.bi[0], i);
+  // ---- the kb acceptance tests by warp 0, one lane per position (ballots):
+  // n = the first reject, or kb; a draft token out of range is an error
+  if (warp == 0) {
+    int nrej = kb, bad = bad_count;
+    for (int i0 = 0; i0 < kb; i0 += 32) {
+      const int i = i0 + lane;
+      bool rej = false, bd = false;
+      if (i < kb) {
+        bd = !gok[i];
+        const float a = fmaf(gx[2 * i], c, -(rmax[i] * c));
+        const float d = fmaf(gx[2 * i + 1], c, -(rmax[K + 1 + i] * c));
+        const float ratio = ex2(a - d) * (rsum[K + 1 + i] / rsum[i]);  // p_i(x_i) / q_i(x_i)
+        rej = !(gu[i] < ratio);
+      }
+      if (__any_sync(0xFFFFFFFFu, bd)) bad = 1;
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, rej);
+      if (m && nrej == kb) nrej = i0 + __ffs(m) - 1;
+    }
+    if (lane == 0) {
+      sh.bi[0] = nrej;
+      sh.bi[1] = bad;
+    }
   }
-  const int err = __syncthreads_or(bad);
+  __syncthreads();
+  const int err = sh.bi[1];
   const int n = sh.bi[0];
   int32_t *out = p.out_tokens + static_cast<size_t>(b) * (K + 1);
   if (rank == 0) {
@@ -1210,12 +1553,12 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
     // partials (the target half of a pair job's partials when kb < K)
     if (rank == 0) {
       const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(kb), 1u);
-      const int token = draw_p_from_partials<DT>(
-          p, p.partials + static_cast<size_t>(job_of(p, b, kb)) * nparts, target_row<DT>(p, b, kb), rmax[kb], u,
-          wbuf, sh);
-      if (tid < 32) {
-        for (int j = lane; j <= K; j += 32)
-          out[j] = j < kb ? gtok[j] : (j == kb ? token : -1);
+      int who;
+      const int token = bonus_draw<DT, TMA>(p, p.partials + static_cast<size_t>(job_of(p, b, kb)) * nparts,
+                                            target_row<DT>(p, b, kb), rmax[kb], u, wbuf, sh, who);
+      if (warp == (who >> 5)) {
+        const int tk = __shfl_sync(0xFFFFFFFFu, token, who & 31);
+        for (int j = lane; j <= K; j += 32) out[j] = j < kb ? gtok[j] : (j == kb ? tk : -1);
         if (lane == 0) {
           p.out_n[b] = kb;
           if (p.stats) {
@@ -1229,48 +1572,45 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
     return;
   }
 
-  // ---- the residual draw at position n
+  // ---- the residual draw at position n over the cluster
   // (point mass: the residual max(0, p - q) is p without the draft token)
   const unsigned char *rt = target_row<DT>(p, b, n);
   const unsigned char *rd = p.point ? rt : draft_row<DT>(p, b, n);
   DrawSlice ds;
   ds.set(static_cast<int>(rank), p.slice_d, p.V, VE);
-  Weights W;
+  FoldedW W;
   W.c = c;
-  W.mtc = rmax[n] * c;
-  W.mdc = rmax[K + 1 + n] * c;
-  W.inv_st = 1.f / rsum[n];
-  W.inv_sd = 1.f / rsum[K + 1 + n];
-  W.resid = !p.point;
+  W.lt = __fadd_rn(__fmul_rn(rmax[n], c), log2f(rsum[n]));
+  W.ld = p.point ? 0.f : __fadd_rn(__fmul_rn(rmax[K + 1 + n], c), log2f(rsum[K + 1 + n]));
+  W.mode = p.point ? W_P_EXCL : W_RESID;
   W.excl = p.point ? gtok[n] : -1;
   const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(n), 1u);
   int fallback = 0, slot = 0;
-  float Z = p.point ? cluster_weigh<DT, TMA, true>(rt, rd, W, ds, slot, rank, CD, sh)
-                    : cluster_weigh<DT, TMA>(rt, rd, W, ds, slot, rank, CD, sh);
+  float Ex, cs;
+  float Z = cluster_exchange(slice_weigh<DT, TMA>(rt, rd, W, ds, p.V, wbuf, sh, Ex, cs), slot, rank, CD, sh);
   if (!(Z > 0.f)) {  // no residual mass in fp32: draw from p at this position
-    W.resid = false;
+    W.mode = p.point ? W_P_EXCL : W_P;
     fallback = 1;
     slot = 1;
-    Z = p.point ? cluster_weigh<DT, TMA, true>(rt, rd, W, ds, slot, rank, CD, sh)
-                : cluster_weigh<DT, TMA>(rt, rd, W, ds, slot, rank, CD, sh);
+    Z = cluster_exchange(slice_weigh<DT, TMA>(rt, rd, W, ds, p.V, wbuf, sh, Ex, cs), slot, rank, CD, sh);
   }
   if (tid == 0) find_owner_cta(u, Z, slot, CD, sh);
   __syncthreads();
   // No DSMEM access follows the last exchange, so only the owner CTA goes on.
   if (static_cast<int>(rank) != sh.bi[2]) return;
-  const int token = p.point ? owner_walk<DT, TMA, true>(rt, rd, W, ds, wbuf, sh)
-                            : owner_walk<DT, TMA>(rt, rd, W, ds, wbuf, sh);
-  if (tid < 32) {
-    for (int j = lane; j <= K; j += 32)
-      out[j] = j < n ? gtok[j] : (j == n ? token : -1);
-    if (lane == 0) {
-      p.out_n[b] = n;
-      if (p.stats) {
-        atomicAdd(&p.stats->sequences, 1ull);
-        atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(n));
-        atomicAdd(&p.stats->resampled, 1ull);
-        if (fallback) atomicAdd(&p.stats->residual_fallbacks, 1ull);
-      }
+  int who;
+  const int token = slice_owner_draw<DT, TMA>(rt, rd, W, ds, p.V, wbuf, sh.bf[0], sh.bf[1], sh.bi[3] != 0, Ex, cs,
+                                              sh, who);
+  if (warp != (who >> 5)) return;
+  const int tk = __shfl_sync(0xFFFFFFFFu, token, who & 31);
+  for (int j = lane; j <= K; j += 32) out[j] = j < n ? gtok[j] : (j == n ? tk : -1);
+  if (lane == 0) {
+    p.out_n[b] = n;
+    if (p.stats) {
+      atomicAdd(&p.stats->sequences, 1ull);
+      atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(n));
+      atomicAdd(&p.stats->resampled, 1ull);
+      if (fallback) atomicAdd(&p.stats->residual_fallbacks, 1ull);
     }
   }
 }

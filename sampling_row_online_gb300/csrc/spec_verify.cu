@@ -303,7 +303,9 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
     const int slice_d = (per_d + VE - 1) / VE * VE;
     if (slice_d > NT * NT) return fail(SPEC_ERR_ARG, "vocabulary too large");
     const auto range = [&](int sl) { return ((sl + VE - 1) / VE + NWARP - 1) / NWARP * VE; };
-    const int wlen = std::max(range(slice_d), range(g->slice));
+    // the walk buffer: a warp range (tree draw), or the vector masses of a
+    // CTA slice and the partials' masses of a row (chain draw)
+    const int wlen = std::max({range(slice_d), range(g->slice), (slice_d + VE - 1) / VE, g->C * NCW});
     g->slice_d = slice_d;
     g->wbuf_off = base;
     g->smem_b = base + 4 * wlen;
