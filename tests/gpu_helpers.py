@@ -5,11 +5,11 @@ Parity rule (stochastic chain): out_n_accepted and every emitted token equal
 the oracle's, except for sequences the oracle flags as near a decision
 boundary (|u - r| <= 1e-5 max(r, 2^-24) at an acceptance test, or t within
 1e-5 Z of a CDF boundary of the draw).  A flagged sequence may differ; such
-excused differences are counted and must stay below 1e-4 of the verified
-positions (a test with fewer than 10^4 positions tolerates one).  Flags
-without a difference are only reported.  Greedy and tree results are
-bit-exact.  Normalisers: the row max exactly, the sum of exponentials to 1e-5
-relative.
+excused differences are counted over the whole session (``record_parity``),
+and the session fails unless their total stays below 1e-4 of all verified
+positions (tests/conftest.py).  A difference in an unflagged sequence fails
+its test at once.  Greedy and tree results are bit-exact.  Normalisers: the
+row max exactly, the sum of exponentials to 1e-5 relative.
 """
 from __future__ import annotations
 
@@ -23,6 +23,46 @@ from sampling_row_online_gb300 import binding
 
 NTHREADS = max(1, os.cpu_count() or 1)
 S_RTOL = 1e-5
+PARITY_BUDGET = 1e-4  # excused differences per verified position, over the session
+
+# kind -> [excused differences, verified positions, near-flagged sequences, sequences]
+TALLY: dict = {}
+
+
+def record_parity(kind, ok, near, positions, where=""):
+    """One stochastic comparison under the parity rule: every unflagged sequence
+    must match (asserted here); flagged sequences that differ are excused and
+    added, with the positions, to the session tally.  Returns the excused count."""
+    ok = np.asarray(ok, bool)
+    near = np.asarray(near, bool)
+    bad = np.where(~ok & ~near)[0]
+    assert bad.size == 0, f"{bad.size} sequences differ from the oracle away from any boundary {where}"
+    excused = int((~ok & near).sum())
+    t = TALLY.setdefault(kind, [0, 0, 0, 0])
+    t[0] += excused
+    t[1] += int(positions)
+    t[2] += int(near.sum())
+    t[3] += int(ok.size)
+    return excused
+
+
+def tally_totals():
+    exc = sum(v[0] for v in TALLY.values())
+    pos = sum(v[1] for v in TALLY.values())
+    return exc, pos
+
+
+def tally_lines():
+    if not TALLY:
+        return []
+    exc, pos = tally_totals()
+    lines = [f"stochastic parity: {exc} excused near-boundary differences in {pos} verified positions "
+             f"(rate {exc / max(pos, 1):.2e}, budget {PARITY_BUDGET:.0e})"]
+    for k in sorted(TALLY):
+        e, p, n, q = TALLY[k]
+        lines.append(f"  {k}: excused {e} / positions {p}; near-flagged sequences {n} of {q} "
+                     f"({n / max(q, 1):.3f})")
+    return lines
 
 
 def gpu_chain(zt, zd, x, T, seed, want_row_stats=True, stats=None):
@@ -39,7 +79,7 @@ def oracle_chain(zt, zd, x, T, seed, b_ids=None, want_stats=True):
                                b_ids=b_ids, want_stats=want_stats, nthreads=NTHREADS)
 
 
-def compare_chain(gpu_tokens, gpu_n, ref, positions, rows=None):
+def compare_chain(gpu_tokens, gpu_n, ref, positions, rows=None, kind="chain"):
     """Asserts the parity rule; returns (excused differences, near-flagged sequences)."""
     near = ref["near"]
     sel = np.arange(len(gpu_n)) if rows is None else np.asarray(rows)
@@ -50,9 +90,7 @@ def compare_chain(gpu_tokens, gpu_n, ref, positions, rows=None):
         f"{bad.size} sequences differ from the oracle away from any boundary; first: "
         f"b={sel[bad[0]]} gpu n={g_n[bad[0]]} tokens={g_tok[bad[0]].tolist()} "
         f"oracle n={ref['n_accepted'][bad[0]]} tokens={ref['tokens'][bad[0]].tolist()}")
-    n_excused = int((~ok & near).sum())
-    assert n_excused <= max(1, 1e-4 * positions), (
-        f"{n_excused} near-boundary differences in {positions} positions")
+    n_excused = record_parity(kind, ok, near, positions)
     return n_excused, int(near.sum())
 
 

@@ -212,7 +212,7 @@ def test_million_identical_rows_distribution_and_near_rate():
     x = gumbel_argmax_draws(zd.reshape(B * K, V) / T, g, chunk_rows=1 << 18).reshape(B, K).contiguous()
     g_tok, g_n, _, _ = gpu_chain(zt, zd, x, T, 31, want_row_stats=False)
     ref = oracle_chain(zt, zd, x, T, 31, want_stats=False)
-    n_excused, n_near = compare_chain(g_tok, g_n, ref, positions=B * K)
+    n_excused, n_near = compare_chain(g_tok, g_n, ref, positions=B * K, kind="chain-1e6")
     assert n_excused < 1e-4 * B * K
     print(f"near-boundary sequences: {n_near} of {B}; excused differences: {n_excused}")
     p = softmax(zt1.astype(np.float64) / T, axis=-1)

@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import oracle
+from gpu_helpers import record_parity
 from sampling_row_online_gb300 import binding
 from sampling_row_online_gb300.workloads import (EAGLE2_WORKLOADS, Eagle2Workload, draft_rows, node_key,
                                                  root_key)
@@ -167,9 +168,7 @@ def _budget_parity(w, B):
     same_keep = ((op.cpu().numpy() == rp).all(1) & (ot.cpu().numpy() == rt).all(1) &
                  (oi.cpu().numpy() == ri).all(1))
     ok = same_tree & same_keep
-    bad = np.where(~ok & ~near)[0]
-    assert bad.size == 0, f"{bad.size} trees differ away from a selection boundary (first b={bad[0]})"
-    assert int((~ok).sum()) <= 1
+    record_parity("eagle2", ok, near, B * w.m, "(EAGLE-2 trees, selection boundary)")
     v = val.cpu().numpy()[same_tree]
     np.testing.assert_allclose(v, oval[same_tree], rtol=1e-5, atol=0)
     return int(near.sum())

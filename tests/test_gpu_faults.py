@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 
 import oracle
+from gpu_helpers import compare_chain
 from sampling_row_online_gb300 import binding
 from sampling_row_online_gb300.workloads import NgramWorkload, Workload, make_chain, make_contexts
 
@@ -19,9 +20,7 @@ def _chain_ok(seed):
     out, n = binding.spec_verify(zt, zd, x, w.T, 3)
     assert binding.spec_get_status() == 0
     ref = oracle.verify_chain(zt.cpu(), zd.cpu(), x.cpu(), w.T, 3)
-    keep = ~ref["near"]
-    assert np.array_equal(n.cpu().numpy()[keep], ref["n_accepted"][keep])
-    assert np.array_equal(out.cpu().numpy()[keep], ref["tokens"][keep])
+    compare_chain(out.cpu().numpy(), n.cpu().numpy(), ref, positions=w.B * w.K)
     return zt, zd, x
 
 

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import NTHREADS, compare_chain
+from gpu_helpers import NTHREADS, compare_chain, record_parity
 from sampling_row_online_gb300 import binding
 
 pytestmark = pytest.mark.gpu
@@ -49,7 +49,7 @@ def chain_case(i, rng):
     st = binding.spec_get_status()
     assert st == 0, f"status {st}"
     ref = oracle.verify_chain(zt.cpu(), zd.cpu() if T > 0 else None, x.cpu(), T, seed, nthreads=NTHREADS)
-    compare_chain(out.cpu().numpy(), n.cpu().numpy(), ref, positions=B * max(K, 1))
+    compare_chain(out.cpu().numpy(), n.cpu().numpy(), ref, positions=B * max(K, 1), kind="random-chain")
     return f"chain B={B} K={K} V={V} {tdt} T={T} unaligned={un}"
 
 
@@ -118,8 +118,7 @@ def tree_sample_case(i, rng):
     assert binding.spec_get_status() == 0
     ref = oracle.verify_tree_sample(zt.cpu(), zd.cpu(), par.cpu(), tok.cpu(), T, seed, nthreads=NTHREADS)
     ok = (ln.cpu().numpy() == ref["length"]) & np.all(path.cpu().numpy() == ref["path"], axis=1)
-    bad = np.where(~ok & ~ref["near"])[0]
-    assert bad.size == 0, f"{bad.size} trees differ away from a boundary"
+    record_parity("random-tree_sample", ok, ref["near"], B * max(1, N - 1), "(trees)")
     return f"tree_sample B={B} N={N} V={V}"
 
 
@@ -145,8 +144,7 @@ def points_case(i, rng):
     ref = oracle.verify_points(zt.cpu(), x.cpu(), None if counts is None else counts.cpu(), T, seed,
                                nthreads=NTHREADS)
     ok = (n.cpu().numpy() == ref["n"]) & np.all(out.cpu().numpy() == ref["tokens"], axis=1)
-    bad = np.where(~ok & ~ref["near"])[0]
-    assert bad.size == 0, f"{bad.size} sequences differ away from a boundary"
+    record_parity("random-points", ok, ref["near"], B * max(K, 1))
     return f"points B={B} K={K} V={V}"
 
 

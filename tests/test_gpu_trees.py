@@ -11,7 +11,7 @@ import oracle
 from sampling_row_online_gb300 import binding
 from sampling_row_online_gb300.workloads import Eagle2Workload, gumbel_argmax_draws
 
-from gpu_helpers import NTHREADS
+from gpu_helpers import NTHREADS, record_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -59,11 +59,13 @@ def _oracle_per_seq(zt, zd, par, tok, T, seed, D):
     return np.stack(paths), np.array(lens), np.array(near)
 
 
-def _compare(path, length, rpath, rlen, near, positions):
+def _compare(path, length, rpath, rlen, near, positions, T):
     ok = (length == rlen) & np.all(path == rpath, axis=1)
-    bad = np.where(~ok & ~near)[0]
-    assert bad.size == 0, f"{bad.size} sequences differ away from a boundary (first b={bad[0]})"
-    assert int((~ok).sum()) <= max(1, 1e-4 * positions)
+    if T > 0:
+        record_parity("trees", ok, near, positions)
+    else:  # greedy: bit-exact
+        bad = np.where(~ok)[0]
+        assert bad.size == 0, f"{bad.size} greedy trees differ (first b={bad[0]})"
 
 
 CASES = [(6, 9, 1000, "f32", 0.0), (5, 31, 4096, "bf16", 0.0), (4, 63, 32000, "bf16", 0.0),
@@ -82,7 +84,7 @@ def test_trees_that_differ_per_sequence(B, N, V, dtype, T):
         path, length = binding.spec_verify_tree(zt, zd, par, tok, T, 77, max_depth=D)
     assert binding.spec_get_status() == 0
     rpath, rlen, near = _oracle_per_seq(zt, zd, par, tok, T, 77, D)
-    _compare(path.cpu().numpy(), length.cpu().numpy(), rpath, rlen, near, B * (N - 1))
+    _compare(path.cpu().numpy(), length.cpu().numpy(), rpath, rlen, near, B * (N - 1), T)
 
 
 def test_shared_tree_as_rows_matches_the_shared_call():
@@ -127,4 +129,4 @@ def test_eagle2_trees_are_verified():
         path, length = binding.spec_verify_tree(zt, zd, op, ot, T, 13, max_depth=D)
         assert binding.spec_get_status() == 0
         rpath, rlen, near = _oracle_per_seq(zt, zd, op, ot, T, 13, D)
-        _compare(path.cpu().numpy(), length.cpu().numpy(), rpath, rlen, near, w.B * w.m)
+        _compare(path.cpu().numpy(), length.cpu().numpy(), rpath, rlen, near, w.B * w.m, T)

@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle
+from gpu_helpers import compare_chain
 from sampling_row_online_gb300 import binding
 from sampling_row_online_gb300.workloads import Workload, make_chain
 
@@ -30,5 +31,4 @@ def test_a_wait_that_never_completes_times_out():
     out, n = binding.spec_verify(zt, zd, x, 1.0, 5)
     assert binding.spec_get_status() == 0
     ref = oracle.verify_chain(zt.cpu(), zd.cpu(), x.cpu(), 1.0, 5)
-    keep = ~ref["near"]
-    assert np.array_equal(n.cpu().numpy()[keep], ref["n_accepted"][keep])
+    compare_chain(out.cpu().numpy(), n.cpu().numpy(), ref, positions=w.B * w.K)

@@ -28,7 +28,7 @@ def test_chain_workload(name, nsample):
                                                                   replace=False)]))
     idx = torch.from_numpy(rows).cuda()
     ref = oracle_chain(zt[idx], zd[idx], x[idx], w.T, w.verify_seed, b_ids=rows)
-    compare_chain(g_tok, g_n, ref, positions=len(rows) * w.K, rows=rows)
+    compare_chain(g_tok, g_n, ref, positions=len(rows) * w.K, rows=rows, kind=f"chain-{w.name}")
     compare_row_stats(g_max, g_sum, ref, w.T, rows=rows)
     # outputs are well formed everywhere, also outside the sample
     assert np.all((g_n >= 0) & (g_n <= w.K))
