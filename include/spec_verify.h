@@ -85,6 +85,12 @@ typedef struct {
   unsigned long long resampled;          /* sequences that stopped at a reject */
   unsigned long long residual_fallbacks; /* rejects whose residual mass was 0 in fp32 */
   unsigned long long errors;             /* sequences with an out-of-range token */
+  unsigned long long near_boundary;      /* sequences with a decision near its boundary: an
+                                            acceptance test with |u - p/q| <= 1e-5 max(p/q, 2^-24),
+                                            or a draw whose t = u Z lies within 1e-5 Z of either end
+                                            of the drawn token's CDF interval (fp32, as computed);
+                                            such decisions are where another rounding of the same
+                                            arithmetic could choose differently */
 } spec_stats_t;
 
 /*
@@ -177,14 +183,28 @@ int spec_verify_host(const void *target_logits, const void *draft_logits,
  *   - Every call shares the one array: two calls that overlap on the GPU
  *     (different streams, or different host threads) race and corrupt each
  *     other's results.  Serialise them.
- *   - Errors found on the device (a draft token outside [0, V)) show in the
- *     outputs (n_accepted = -1, tokens -1); they are not reported by
- *     spec_get_status.
+ *   - Errors found on the device show in the outputs: a draft token outside
+ *     [0, V) marks its sequence (n_accepted = -1, tokens -1); a bounded wait
+ *     that ran out marks every sequence of the call, and of every later
+ *     call, until spec_noalloc_get_status reads and clears the array's
+ *     status word (spec_get_status does not read it).
+ *   - After a device reset (cudaDeviceReset) call spec_shutdown before the
+ *     next call: it forgets the array's cached device addresses.
  */
 int spec_verify_noalloc(const void *target_logits, const void *draft_logits,
                         const int32_t *draft_tokens, int B, int K, int V, int dtype,
                         float temperature, uint64_t seed, int32_t *out_tokens,
                         int32_t *out_n_accepted, void *stream);
+
+/*
+ * spec_noalloc_get_status — spec_get_status for the status word of
+ * spec_verify_noalloc's fixed array: waits for `stream` (the stream the calls
+ * ran on), then returns and clears the first device-side error recorded by
+ * those calls (SPEC_OK, SPEC_ERR_TOKEN_RANGE or SPEC_ERR_TIMEOUT).
+ * Allocates nothing; like the first spec_verify_noalloc call on a device,
+ * its first call looks up the array's device address.
+ */
+int spec_noalloc_get_status(void *stream);
 
 /*
  * spec_verify_tree_greedy — greedy verification of a draft tree
@@ -337,6 +357,10 @@ int spec_verify_points(const void *target_logits, const int32_t *draft_tokens,
  * lengths[b] outside [0, L] sets out_count[b] = -1 and its draft row to -1,
  * and spec_get_status then returns SPEC_ERR_ARG.  Output is bit-exact and
  * deterministic (a pure function of the inputs).
+ * Launch geometry: G CTAs share each context's end positions (about two
+ * waves of resident CTAs over the batch, at least 4096 positions each); the
+ * environment variable SPEC_NGRAM_CTAS, read at each call, sets G instead
+ * (any G >= 1 gives the same outputs).
  */
 int spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int L, int n_min,
                        int n_max, int min_hits, int K, int32_t *out_draft, int32_t *out_count,
@@ -353,6 +377,11 @@ int spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int
  *               lower index
  *   out_prob    [R, k] float (device): softmax(z / T) of those tokens
  * Rows must hold one finite logit (-inf entries allowed).
+ * Launch geometry: each row is split over a cluster of G CTAs (G a power of
+ * two up to 8, about one wave of 3 CTAs per SM); the environment variable
+ * SPEC_TOPK_CLUSTER, read at each call, sets G instead (rounded down to a
+ * power of two; any G gives the same outputs).  No other environment
+ * variable changes this library's launches.
  */
 int spec_topk(const void *logits, int R, int V, int dtype, float temperature, int k,
               int32_t *out_tokens, float *out_prob, void *stream);
@@ -408,7 +437,10 @@ int spec_eagle2_rerank(const float *node_values, const int32_t *node_parents,
  * device-side error recorded by calls on it: SPEC_OK, SPEC_ERR_TOKEN_RANGE,
  * SPEC_ERR_PARENT, SPEC_ERR_TIMEOUT, SPEC_ERR_ARG (a lengths[] entry of
  * spec_ngram_propose out of range), or SPEC_ERR_CUDA for an asynchronous
- * CUDA error.
+ * CUDA error.  While a SPEC_ERR_TIMEOUT is recorded and not yet read, every
+ * verification on the stream (chains, point-mass drafts, trees) writes -1
+ * for its outputs (n_accepted or length -1, tokens -1) instead of values
+ * drawn from statistics a stopped wait may have left incomplete.
  */
 int spec_get_status(void *stream);
 
@@ -445,6 +477,15 @@ int spec_selftest_wait(void *stream);
  * call.  n = 0 switches it off.  No GPU fault is involved.
  */
 int spec_debug_fail_launch(int n);
+
+/*
+ * spec_debug_noalloc_status — test hook of spec_verify_noalloc's error path:
+ * ORs the device status bits `bits` (1: token out of range, 4: a wait ran
+ * out) into the status word of its fixed array, as a kernel would, so that
+ * a test can check the outputs and spec_noalloc_get_status without faulting
+ * or stalling a GPU.  Synchronous; allocates nothing.
+ */
+int spec_debug_noalloc_status(int bits);
 
 /* Static, human-readable name of a status code. */
 const char *spec_error_string(int status);

@@ -34,7 +34,10 @@ class SpecError(RuntimeError):
 
 class StatsStruct(ctypes.Structure):
     _fields_ = [(n, ctypes.c_ulonglong) for n in
-                ("sequences", "accepted", "bonus", "resampled", "residual_fallbacks", "errors")]
+                ("sequences", "accepted", "bonus", "resampled", "residual_fallbacks", "errors",
+                 "near_boundary")]
+
+STATS_COUNTERS = len(StatsStruct._fields_)
 
 
 def library():
@@ -70,11 +73,14 @@ def library():
     lib.spec_last_error_message.argtypes = []
     lib.spec_last_error_message.restype = ctypes.c_char_p
     lib.spec_verify_noalloc.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, u64, vp, vp, vp]
+    lib.spec_noalloc_get_status.argtypes = [vp]
+    lib.spec_debug_noalloc_status.argtypes = [i32]
     lib.spec_shutdown.argtypes = []
     lib.spec_shutdown.restype = None
     for name in ("spec_verify", "spec_verify_ex", "spec_verify_host", "spec_verify_tree_greedy",
                  "spec_tree_max_depth", "spec_tree_mask", "spec_ngram_propose", "spec_topk",
-                 "spec_eagle2_expand", "spec_eagle2_rerank", "spec_get_status"):
+                 "spec_eagle2_expand", "spec_eagle2_rerank", "spec_get_status", "spec_verify_noalloc",
+                 "spec_noalloc_get_status", "spec_debug_noalloc_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -141,7 +147,7 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature, seed,
                    out_tokens=None, out_n_accepted=None, want_row_stats=False, stats=None,
                    stream=None):
     """Chain verification with optional per-row (max, sumexp) [B, 2K+1] outputs and a
-    device ``stats`` tensor (6 int64 counters, accumulated).  Returns
+    device ``stats`` tensor (STATS_COUNTERS int64 counters, accumulated).  Returns
     (out_tokens, n_accepted, row_max or None, row_sumexp or None)."""
     lib = library()
     _dev(target_logits, "target_logits")
@@ -161,8 +167,8 @@ def spec_verify_ex(target_logits, draft_logits, draft_tokens, temperature, seed,
         row_sumexp = torch.empty((B, 2 * K + 1), dtype=torch.float32, device=dev)
     if stats is not None:
         _dev(stats, "stats", torch.int64)
-        if stats.numel() != 6:
-            raise ValueError("stats must hold 6 int64 counters")
+        if stats.numel() != STATS_COUNTERS:
+            raise ValueError(f"stats must hold {STATS_COUNTERS} int64 counters")
     with torch.cuda.device(dev):
         st = lib.spec_verify_ex(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens),
                                 B, K, V, _dtype_code(target_logits), float(temperature),
@@ -487,6 +493,18 @@ def spec_selftest_wait(stream=None) -> int:
 def spec_get_status(stream=None) -> int:
     """Waits for the stream; returns (and clears) the device-side status code."""
     return int(library().spec_get_status(_stream(stream)))
+
+
+def spec_noalloc_get_status(stream=None) -> int:
+    """Waits for the stream; returns (and clears) the status code recorded in
+    the fixed array of spec_verify_noalloc."""
+    return int(library().spec_noalloc_get_status(_stream(stream)))
+
+
+def spec_debug_noalloc_status(bits):
+    """Test hook: ORs device status bits (1 token out of range, 4 a wait ran
+    out) into the status word of spec_verify_noalloc's fixed array."""
+    _check(library().spec_debug_noalloc_status(int(bits)), "spec_debug_noalloc_status")
 
 
 def raise_on_device_error(stream=None):

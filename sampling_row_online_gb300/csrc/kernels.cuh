@@ -66,8 +66,13 @@ enum Kind : int { KIND_SAMPLE = 0, KIND_GREEDY_CHAIN = 1, KIND_TREE = 2, KIND_TR
 constexpr int MAX_TREE_NODES = 1024;
 
 struct Stats {  // layout-compatible with spec_stats_t
-  unsigned long long sequences, accepted, bonus, resampled, residual_fallbacks, errors;
+  unsigned long long sequences, accepted, bonus, resampled, residual_fallbacks, errors, near_boundary;
 };
+
+// A decision within this relative distance of its boundary counts as near
+// (the acceptance test |u - r| <= NEAR_REL max(r, 2^-24), the draw
+// |t - C| <= NEAR_REL Z at either end of the drawn token's interval).
+constexpr float NEAR_REL = 1e-5f;
 
 struct Params {
   const void *zt;           // [B, J, V] target rows (J = K+1 chain, N tree)
@@ -307,6 +312,14 @@ __device__ __forceinline__ const unsigned char *draft_row(const Params &p, int b
 }
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// After the dependent-launch wait: a bounded wait of this call's streaming
+// kernel (or of any earlier call on the same status word not yet read) ran
+// out, so the row statistics may be incomplete; the call's outputs are then
+// -1 rather than values drawn from them.
+__device__ __forceinline__ bool stream_timed_out(const Params &p) {
+  return (*reinterpret_cast<const volatile int32_t *>(p.status) & ST_TIMEOUT) != 0;
+}
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
@@ -706,6 +719,8 @@ struct DrawShared {
   float scan[NWARP + 1];     // block scan scratch
   int ired[NWARP];           // block reduction scratch
   int pick;                  // walk result
+  int near_acc;              // an acceptance test of the sequence was near its boundary
+  float zdraw;               // the draw's total mass Z (bonus draw)
 };
 
 constexpr int PARTS_PER_LANE = 4;
@@ -1267,10 +1282,12 @@ __device__ __forceinline__ int owner_thread(float P, float t, float E, float cs,
 
 // In the owner thread: the entry of vector (ft, fd, first entry e0) whose
 // running mass base(pre) passes t, where base(x) = P + (E + (cbefore + x));
-// else the last entry of positive weight.  Returns the entry's offset.
+// else the last entry of positive weight.  Returns the entry's offset; *near
+// is set when t lies within NEAR_REL Z of either end of that entry's interval.
 template <int VE>
 __device__ __forceinline__ int vec_walk(const FoldedW &W, const float (&ft)[VE], const float (&fd)[VE], int e0,
-                                        float P, float E, float cbefore, float t, bool lastmode) {
+                                        float P, float E, float cbefore, float t, bool lastmode, float Z,
+                                        bool *near) {
   float w[VE], pre[VE];
   vec_weights<VE>(W, ft, fd, e0, w);
   vec_prefix<VE>(w, pre);
@@ -1282,7 +1299,16 @@ __device__ __forceinline__ int vec_walk(const FoldedW &W, const float (&ft)[VE],
       last = e;
     }
   }
-  return pick >= 0 ? pick : max(last, 0);
+  const int sel = pick >= 0 ? pick : max(last, 0);
+  float hi = __fadd_rn(P, __fadd_rn(E, cbefore)), lo = hi;
+#pragma unroll
+  for (int e = 0; e < VE; ++e) {
+    const float x = __fadd_rn(P, __fadd_rn(E, __fadd_rn(cbefore, pre[e])));
+    if (e < sel) lo = x;
+    if (e == sel) hi = x;
+  }
+  *near = fabsf(t - hi) <= NEAR_REL * Z || fabsf(t - lo) <= NEAR_REL * Z;
+  return sel;
 }
 
 // The owner CTA's part of a cluster-wide draw: the owner thread (by the
@@ -1292,7 +1318,8 @@ __device__ __forceinline__ int vec_walk(const FoldedW &W, const float (&ft)[VE],
 template <int DT, bool VEC>
 __device__ __forceinline__ int slice_owner_draw(const unsigned char *rt, const unsigned char *rd, const FoldedW &W,
                                                 const DrawSlice &ds, int V, const float *wv, float P, float t,
-                                                bool lastmode, float E, float cs, DrawShared &sh, int &who) {
+                                                bool lastmode, float E, float cs, float Z, DrawShared &sh, int &who,
+                                                bool *near) {
   constexpr int VE = Elem<DT>::VE;
   const int tid = threadIdx.x;
   who = owner_thread(P, t, E, cs, lastmode, sh);
@@ -1326,7 +1353,7 @@ __device__ __forceinline__ int slice_owner_draw(const unsigned char *rt, const u
   else
 #pragma unroll
     for (int e = 0; e < VE; ++e) fd[e] = -INFINITY;
-  return e0 + vec_walk<VE>(W, ft, fd, e0, P, E, cb, t, lastmode);
+  return e0 + vec_walk<VE>(W, ft, fd, e0, P, E, cb, t, lastmode, Z, near);
 }
 
 // Bonus draw from p (weights 2^(z c - M c)) of one target row by one CTA,
@@ -1338,7 +1365,7 @@ __device__ __forceinline__ int slice_owner_draw(const unsigned char *rt, const u
 // from registers.  Returns the token in thread `who` (set in every thread).
 template <int DT, bool VEC>
 __device__ __forceinline__ int bonus_draw(const Params &p, const float4 *parts, const unsigned char *row, float M,
-                                          float u, float *pm, DrawShared &sh, int &who) {
+                                          float u, float *pm, DrawShared &sh, int &who, bool *near) {
   using El = Elem<DT>;
   constexpr int VE = El::VE;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -1391,12 +1418,13 @@ __device__ __forceinline__ int bonus_draw(const Params &p, const float4 *parts, 
       sh.bi[5] = lastmode;
       sh.bf[4] = P;
       sh.bf[5] = t;
+      sh.zdraw = Z;
     }
   }
   __syncthreads();
   const int own = sh.bi[4];
   bool lastmode = sh.bi[5] != 0;
-  const float P = sh.bf[4], t = sh.bf[5];
+  const float P = sh.bf[4], t = sh.bf[5], Zd = sh.zdraw;
   // the owner range: slice sl, consumer warp w of the streaming split (its
   // start is a multiple of VE; at most NT vectors)
   const int sl = own / NCW, w = own - sl * NCW;
@@ -1424,7 +1452,7 @@ __device__ __forceinline__ int bonus_draw(const Params &p, const float4 *parts, 
   const float E = block_exclusive_scan(cs, sh.scan, &total);
   who = owner_thread(P, t, E, cs, lastmode, sh);
   if (tid != who) return -1;
-  return e0 + vec_walk<VE>(W, ft, fd, e0, P, E, 0.f, t, lastmode);
+  return e0 + vec_walk<VE>(W, ft, fd, e0, P, E, 0.f, t, lastmode, Zd, near);
 }
 
 // Every CTA's mass into slot `slot` of every CTA of the cluster; after the
@@ -1507,24 +1535,31 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   // ---- the kb acceptance tests by warp 0, one lane per position (ballots):
   // n = the first reject, or kb; a draft token out of range is an error
   if (warp == 0) {
-    int nrej = kb, bad = bad_count;
+    int nrej = kb, bad = bad_count, near = 0;
     for (int i0 = 0; i0 < kb; i0 += 32) {
       const int i = i0 + lane;
-      bool rej = false, bd = false;
+      bool rej = false, bd = false, nr = false;
       if (i < kb) {
         bd = !gok[i];
         const float a = fmaf(gx[2 * i], c, -(rmax[i] * c));
         const float d = fmaf(gx[2 * i + 1], c, -(rmax[K + 1 + i] * c));
         const float ratio = ex2(a - d) * (rsum[K + 1 + i] / rsum[i]);  // p_i(x_i) / q_i(x_i)
         rej = !(gu[i] < ratio);
+        nr = isfinite(ratio) && fabsf(gu[i] - ratio) <= NEAR_REL * fmaxf(ratio, 0x1p-24f);
       }
       if (__any_sync(0xFFFFFFFFu, bd)) bad = 1;
       const unsigned m = __ballot_sync(0xFFFFFFFFu, rej);
-      if (m && nrej == kb) nrej = i0 + __ffs(m) - 1;
+      const unsigned nm = __ballot_sync(0xFFFFFFFFu, nr);
+      if (nrej == kb) {  // tests up to and including the first reject
+        const int f = m ? __ffs(m) - 1 : 31;
+        if (nm & (f == 31 ? 0xFFFFFFFFu : ((2u << f) - 1u))) near = 1;
+        if (m) nrej = i0 + f;
+      }
     }
     if (lane == 0) {
       sh.bi[0] = nrej;
       sh.bi[1] = bad;
+      sh.near_acc = near;
     }
   }
   __syncthreads();
@@ -1547,6 +1582,13 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   }
   cluster_wait();  // every peer is running (pairs with the arrive above)
   if (err) return;
+  if (stream_timed_out(p)) {
+    if (rank == 0) {
+      for (int e = tid; e <= K; e += NT) out[e] = -1;
+      if (tid == 0) p.out_n[b] = -1;
+    }
+    return;
+  }
 
   if (n == kb) {
     // ---- bonus: rank 0 draws from p at position kb using the streaming
@@ -1554,10 +1596,12 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
     if (rank == 0) {
       const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(kb), 1u);
       int who;
+      bool nd = false;
       const int token = bonus_draw<DT, TMA>(p, p.partials + static_cast<size_t>(job_of(p, b, kb)) * nparts,
-                                            target_row<DT>(p, b, kb), rmax[kb], u, wbuf, sh, who);
+                                            target_row<DT>(p, b, kb), rmax[kb], u, wbuf, sh, who, &nd);
       if (warp == (who >> 5)) {
         const int tk = __shfl_sync(0xFFFFFFFFu, token, who & 31);
+        const bool near = __shfl_sync(0xFFFFFFFFu, static_cast<int>(nd), who & 31) || sh.near_acc;
         for (int j = lane; j <= K; j += 32) out[j] = j < kb ? gtok[j] : (j == kb ? tk : -1);
         if (lane == 0) {
           p.out_n[b] = kb;
@@ -1565,6 +1609,7 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
             atomicAdd(&p.stats->sequences, 1ull);
             atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(kb));
             atomicAdd(&p.stats->bonus, 1ull);
+            if (near) atomicAdd(&p.stats->near_boundary, 1ull);
           }
         }
       }
@@ -1599,10 +1644,12 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   // No DSMEM access follows the last exchange, so only the owner CTA goes on.
   if (static_cast<int>(rank) != sh.bi[2]) return;
   int who;
+  bool nd = false;
   const int token = slice_owner_draw<DT, TMA>(rt, rd, W, ds, p.V, wbuf, sh.bf[0], sh.bf[1], sh.bi[3] != 0, Ex, cs,
-                                              sh, who);
+                                              Z, sh, who, &nd);
   if (warp != (who >> 5)) return;
   const int tk = __shfl_sync(0xFFFFFFFFu, token, who & 31);
+  const bool near = __shfl_sync(0xFFFFFFFFu, static_cast<int>(nd), who & 31) || sh.near_acc;
   for (int j = lane; j <= K; j += 32) out[j] = j < n ? gtok[j] : (j == n ? tk : -1);
   if (lane == 0) {
     p.out_n[b] = n;
@@ -1611,6 +1658,7 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
       atomicAdd(&p.stats->accepted, static_cast<unsigned long long>(n));
       atomicAdd(&p.stats->resampled, 1ull);
       if (fallback) atomicAdd(&p.stats->residual_fallbacks, 1ull);
+      if (near) atomicAdd(&p.stats->near_boundary, 1ull);
     }
   }
 }
@@ -1696,6 +1744,13 @@ __global__ void __launch_bounds__(NT, 4) tree_draw_kernel(const Params p) {
   const int W1 = p.max_depth + 1;
   int32_t *path = p.out_tokens + static_cast<size_t>(b) * W1;
   cluster_wait();  // pairs with the arrive above
+  if (!err && stream_timed_out(p)) {
+    if (rank == 0) {
+      for (int j = tid; j < W1; j += NT) path[j] = -1;
+      if (tid == 0) p.out_n[b] = -1;
+    }
+    return;
+  }
   if (err) {
     if (rank == 0) {
       for (int j = tid; j < W1; j += NT) path[j] = -1;
@@ -1824,6 +1879,12 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
   for (int e = tid; e < ntok; e += NT) s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * ntok + e);
   pdl_wait();
   if (b == 0 && tid < p.nshard) p.tickets[tid * TICKET_STRIDE] = 0;  // for the next call
+  if (stream_timed_out(p)) {
+    const int W = p.kind == KIND_TREE ? p.max_depth + 1 : p.K + 1;
+    for (int e = tid; e < W; e += NT) p.out_tokens[static_cast<size_t>(b) * W + e] = -1;
+    if (tid == 0) p.out_n[b] = -1;
+    return;
+  }
   const int nparts = p.C * NCW;
   for (int r = warp; r < J; r += NWARP) {
     float v = -INFINITY;

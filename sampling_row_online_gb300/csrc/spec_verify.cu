@@ -25,6 +25,8 @@ namespace {
 
 thread_local std::string g_last_error;
 
+void noalloc_forget();  // spec_verify_noalloc's cached device addresses (defined with it)
+
 // Fault injection for tests (spec_debug_fail_launch): the n-th launch from
 // now reports cudaErrorLaunchFailure without launching.  0: off.
 std::atomic<int> g_fail_launch{0};
@@ -254,8 +256,8 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
   const long long row_bytes = static_cast<long long>(p.V) * esz;
   // streaming items are single tiles of at most 16 KB per row
   const int C_min = static_cast<int>(std::max<long long>(1, (row_bytes + TILE_MAX_BYTES - 1) / TILE_MAX_BYTES));
-  g->C = std::max(C_min, env_int("SPEC_VERIFY_SLICES", C_min, 1, 1 << 16));
-  g->stages = env_int("SPEC_VERIFY_STAGES", DEFAULT_STAGES, 1, MAX_STAGES);
+  g->C = C_min;
+  g->stages = DEFAULT_STAGES;
   g->fa = argmax ? pick_row_kernel<true>(dtype, tma) : pick_row_kernel<false>(dtype, tma);
   g->fb = argmax ? reinterpret_cast<const void *>(&finish_kernel)
                  : (p.kind == KIND_TREE_SAMPLE ? pick_tree_draw_kernel(dtype, tma) : pick_draw_kernel(dtype, tma));
@@ -297,7 +299,6 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
                                               : (4 * (9 * p.K + 2) + 15) / 16 * 16;
   int CD = static_cast<int>(std::min<long long>(
       MAX_CLUSTER, std::max<long long>(1, (row_bytes + DRAW_SLICE_BYTES - 1) / DRAW_SLICE_BYTES)));
-  CD = env_int("SPEC_VERIFY_DRAW_CLUSTER", CD, 1, MAX_CLUSTER);
   for (;;) {
     const int per_d = (p.V + CD - 1) / CD;
     const int slice_d = (per_d + VE - 1) / VE * VE;
@@ -923,6 +924,29 @@ int spec_arm_rows_event(void *event) {
   return SPEC_OK;
 }
 
+}  // extern "C"
+
+namespace spec {
+namespace {
+// Reads the device status word at `word` (after the stream has drained),
+// clears it, and maps its bits to a status code.
+int read_status_word(int32_t *word) {
+  int32_t bits = 0;
+  cudaError_t e;
+  if ((e = cudaMemcpy(&bits, word, sizeof bits, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemcpy(status)");
+  if (bits == 0) return SPEC_OK;
+  if ((e = cudaMemset(word, 0, sizeof(int32_t))) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+  if (bits & ST_TIMEOUT) return fail(SPEC_ERR_TIMEOUT, "a bounded wait on the device ran out");
+  if (bits & ST_PARENT) return fail(SPEC_ERR_PARENT, "parent[] is not a tree of the given depth");
+  if (bits & ST_LENGTH) return fail(SPEC_ERR_ARG, "lengths[b] outside [0, L]");
+  return fail(SPEC_ERR_TOKEN_RANGE, "a draft or node token is outside [0, V)");
+}
+}  // namespace
+}  // namespace spec
+
+extern "C" {
+
 int spec_get_status(void *stream_ptr) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   cudaError_t e = cudaStreamSynchronize(stream);
@@ -935,15 +959,7 @@ int spec_get_status(void *stream_ptr) {
     w = find_ws(dev, stream, false);
   }
   if (!w || !w->status) return SPEC_OK;
-  int32_t bits = 0;
-  if ((e = cudaMemcpy(&bits, w->status, sizeof bits, cudaMemcpyDeviceToHost)) != cudaSuccess)
-    return cuda_fail(e, "cudaMemcpy(status)");
-  if (bits == 0) return SPEC_OK;
-  if ((e = cudaMemset(w->status, 0, sizeof(int32_t))) != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
-  if (bits & ST_TIMEOUT) return fail(SPEC_ERR_TIMEOUT, "a bounded wait on the device ran out");
-  if (bits & ST_PARENT) return fail(SPEC_ERR_PARENT, "parent[] is not a tree of the given depth");
-  if (bits & ST_LENGTH) return fail(SPEC_ERR_ARG, "lengths[b] outside [0, L]");
-  return fail(SPEC_ERR_TOKEN_RANGE, "a draft or node token is outside [0, V)");
+  return read_status_word(w->status);
 }
 
 int spec_verify_host(const void *target_logits, const void *draft_logits, const int32_t *draft_tokens,
@@ -1020,6 +1036,7 @@ const char *spec_error_string(int status) {
 const char *spec_last_error_message(void) { return g_last_error.c_str(); }
 
 void spec_shutdown(void) {
+  noalloc_forget();
   std::lock_guard<std::mutex> lock(g_mu);
   int cur = 0;
   cudaGetDevice(&cur);
@@ -1059,6 +1076,11 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_BYTES];
 constexpr int NOALLOC_MAX_DEVICES = 64;
 std::mutex g_noalloc_mu;
 unsigned char *g_noalloc_ptr[NOALLOC_MAX_DEVICES] = {nullptr};
+
+void noalloc_forget() {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  for (auto &ptr : g_noalloc_ptr) ptr = nullptr;
+}
 
 // Device address of the scratch array on the current device, looked up once
 // per device (the array's host-side name is only a stand-in).
@@ -1122,4 +1144,29 @@ extern "C" int spec_verify_noalloc(const void *target_logits, const void *draft_
   return run_step_on(p, dtype, tma, static_cast<cudaStream_t>(stream_ptr),
                      reinterpret_cast<float4 *>(scratch + NOALLOC_PARTS_OFF), NOALLOC_MAX_PARTIALS,
                      reinterpret_cast<int32_t *>(scratch));
+}
+
+extern "C" int spec_noalloc_get_status(void *stream_ptr) {
+  using namespace spec;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream_ptr));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned char *scratch = nullptr;
+  int st = noalloc_scratch(&scratch);
+  if (st) return st;
+  return read_status_word(reinterpret_cast<int32_t *>(scratch));
+}
+
+extern "C" int spec_debug_noalloc_status(int bits) {
+  using namespace spec;
+  unsigned char *scratch = nullptr;
+  int st = noalloc_scratch(&scratch);
+  if (st) return st;
+  int32_t cur = 0;
+  cudaError_t e;
+  if ((e = cudaMemcpy(&cur, scratch, sizeof cur, cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemcpy(status)");
+  cur |= bits & (ST_TOKEN | ST_PARENT | ST_TIMEOUT);
+  if ((e = cudaMemcpy(scratch, &cur, sizeof cur, cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_fail(e, "cudaMemcpy(status)");
+  return SPEC_OK;
 }

@@ -174,7 +174,7 @@ def test_empty_batch_is_a_no_op():
 
 def test_stats_counters():
     zt, zd, x = _inputs(64, 5, 8000, "bf16", 1.0, sigma_d=1.0, seed=4)
-    stats = torch.zeros(6, dtype=torch.int64, device="cuda")
+    stats = torch.zeros(binding.STATS_COUNTERS, dtype=torch.int64, device="cuda")
     out, n, _, _ = binding.spec_verify_ex(zt, zd, x, 1.0, 17, stats=stats)
     binding.spec_verify_ex(zt, zd, x, 1.0, 17, stats=stats)
     s = stats.cpu().numpy()
@@ -184,6 +184,24 @@ def test_stats_counters():
     assert s[2] == 2 * (nn == 5).sum()         # bonus
     assert s[3] == 2 * (nn < 5).sum()          # resampled
     assert s[5] == 0
+
+
+NEAR_CASES = [(64, 5, 128256, "bf16", 0.7, 0.5, 1001, 0), (256, 4, 4096, "f32", 1.0, 1.0, 7, 3),
+              (400, 3, 16, "f32", 1.0, 1.0, 9, 11), (128, 8, 32000, "bf16", 1.0, 2.0, 13, 5)]
+
+
+@pytest.mark.parametrize("B,K,V,dtype,T,sd,dseed,seed", NEAR_CASES,
+                         ids=[f"B{c[0]}K{c[1]}V{c[2]}{c[3]}" for c in NEAR_CASES])
+def test_near_boundary_counter_matches_the_oracle_flags(B, K, V, dtype, T, sd, dseed, seed):
+    """The near_boundary counter counts the sequences the oracle flags near an
+    acceptance or CDF boundary (same 1e-5 window; fp32 here, fp64 there: the
+    cases are ones where no decision sits at the window's own edge)."""
+    zt, zd, x = _inputs(B, K, V, dtype, T, sigma_d=sd, seed=dseed)
+    stats = torch.zeros(binding.STATS_COUNTERS, dtype=torch.int64, device="cuda")
+    binding.spec_verify_ex(zt, zd, x, T, seed, stats=stats)
+    s = stats.cpu().numpy()
+    ref = oracle_chain(zt, zd, x, T, seed, want_stats=False)
+    assert s[6] == int(ref["near"].sum()), (s[6], int(ref["near"].sum()))
 
 
 def test_host_buffer_entry_point_matches_device_path():

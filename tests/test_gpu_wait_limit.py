@@ -2,6 +2,7 @@
 completes gives up after its limit, the library reports SPEC_ERR_TIMEOUT,
 and the stream and context stay usable (a verification call right after
 matches the oracle)."""
+import ctypes
 import time
 
 import numpy as np
@@ -32,3 +33,28 @@ def test_a_wait_that_never_completes_times_out():
     assert binding.spec_get_status() == 0
     ref = oracle.verify_chain(zt.cpu(), zd.cpu(), x.cpu(), 1.0, 5)
     compare_chain(out.cpu().numpy(), n.cpu().numpy(), ref, positions=w.B * w.K)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_calls_after_an_unread_timeout_output_minus_one(T):
+    """While a timeout is recorded and not yet read, a verification on the stream
+    writes -1 (its statistics may be incomplete); reading the status clears it
+    and the next call matches the oracle again."""
+    lib = binding.library()
+    assert binding.spec_get_status() == 0
+    w = Workload("poison", "chain", B=6, K=3, V=2048, dtype="bf16", T=T, data_seed=23)
+    zt, zd, x = make_chain(w, device="cuda")
+    stream = torch.cuda.current_stream()
+    assert lib.spec_selftest_wait(ctypes.c_void_p(stream.cuda_stream)) == 0   # records a timeout
+    out, n = binding.spec_verify(zt, zd if T > 0 else None, x, T, 3)
+    torch.cuda.synchronize()
+    assert np.all(n.cpu().numpy() == -1) and np.all(out.cpu().numpy() == -1)
+    assert binding.spec_get_status() == 6                      # SPEC_ERR_TIMEOUT, now cleared
+    out, n = binding.spec_verify(zt, zd if T > 0 else None, x, T, 3)
+    assert binding.spec_get_status() == 0
+    ref = oracle.verify_chain(zt.cpu(), zd.cpu() if T > 0 else None, x.cpu(), T, 3)
+    if T > 0:
+        compare_chain(out.cpu().numpy(), n.cpu().numpy(), ref, positions=w.B * w.K)
+    else:
+        assert np.array_equal(n.cpu().numpy(), ref["n_accepted"])
+        assert np.array_equal(out.cpu().numpy(), ref["tokens"])
