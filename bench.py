@@ -42,6 +42,7 @@ LAUNCHES_PER_CALL = 2  # the streaming row kernel and the per-sequence decision 
 
 NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal
 EX2_PER_SM_CLOCK = 16      # MUFU base-2 exponentials per SM per clock, nominal
+STAT_CALLS = 200           # calls behind every per-call percentile (independent of --steps)
 
 
 def _quantile(sorted_vals, q):
@@ -241,6 +242,7 @@ def run_reference(args, w):
 # GPU arm
 # ----------------------------------------------------------------------------
 def run_gpu(args, w):
+    import numpy as np
     import torch
     import torch.distributed as dist
     from sampling_row_online_gb300 import binding
@@ -330,8 +332,9 @@ def run_gpu(args, w):
     # time is the region over the steps
     call_ms = region_ms / args.steps
     # the dominant kernel alone: an event before each call and one the library
-    # records between its two launches (spec_arm_rows_event)
-    n_rows = min(args.steps, 400)
+    # records between its two launches (spec_arm_rows_event); a fixed sample
+    # of STAT_CALLS calls, whatever --steps is
+    n_rows = STAT_CALLS
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rows)]
     for a, b in ev:
         a.record(stream)
@@ -357,6 +360,24 @@ def run_gpu(args, w):
         calls[0]()
     torch.cuda.synchronize()
     warm_ms = max_over_ranks(statistics.fmean(a.elapsed_time(b) for a, b in evw), dev)
+    # the same calls chained back to back (as in the timed region), each with
+    # device stamps (spec_arm_timer: no stream operation between launches):
+    # the dominant kernel's time as it runs there, the call's device time, and
+    # the start-to-start period of consecutive calls
+    stamps = torch.empty((STAT_CALLS, 3), dtype=torch.int64, device=dev)
+    stamps[:, 0] = -1
+    stamps[:, 1:] = 0
+    torch.cuda.synchronize()
+    for k in range(STAT_CALLS):
+        lib.spec_arm_timer(ctypes.c_void_p(stamps[k].data_ptr()))
+        calls[k % ncopies]()
+    torch.cuda.synchronize()
+    if lib.spec_get_status(sp) != 0:
+        raise SystemExit("device status error in the chained-stamps loop")
+    st_np = stamps.cpu().numpy().view(np.uint64).astype(np.float64)
+    chained_row_us = sorted(((st_np[:, 1] - st_np[:, 0]) / 1e3).tolist())
+    chained_call_us = sorted(((st_np[:, 2] - st_np[:, 0]) / 1e3).tolist())
+    chained_period_us = sorted(((st_np[1:, 0] - st_np[:-1, 0]) / 1e3).tolist())
     positions = w.positions * args.steps * ws
     value = positions / (region_ms / 1e3)
 
@@ -399,11 +420,18 @@ def run_gpu(args, w):
     kernel = "row_kernel"
     achieved = w.algorithmic_bytes / (avg_launch_ms / 1e3) / 1e9
     call_achieved = w.algorithmic_bytes / (call_ms / 1e3) / 1e9
+    med_launch_ms = _quantile(launch_us, 0.5) / 1e3
+    achieved_med = w.algorithmic_bytes / (med_launch_ms / 1e3) / 1e9
+    q3 = lambda v: [_quantile(v, q) for q in (0.1, 0.5, 0.9)]
+    row_med = _quantile(chained_row_us, 0.5)
+    period_med = _quantile(chained_period_us, 0.5)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                "frac": achieved / peak, "frac_median": achieved_med / peak,
+                "peak_source": f"{peak_kind} hbm_gbs",
                 "traffic": _profile_traffic(kernel, w.name), "kernel": kernel,
                 "timed": (f"{kernel} alone: CUDA events on the call's stream before the call and "
-                          f"between its two launches (spec_arm_rows_event), mean of {n_rows} calls"),
+                          f"between its two launches (spec_arm_rows_event), mean of {n_rows} calls "
+                          f"(frac_median: their median)"),
                 "algorithmic_bytes_per_launch": w.algorithmic_bytes,
                 "avg_launch_us": avg_launch_ms * 1e3,
                 "launch_us_p10_median_p90": [_quantile(launch_us, q) for q in (0.1, 0.5, 0.9)],
@@ -411,7 +439,17 @@ def run_gpu(args, w):
                 "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                 "whole_call": {"achieved": call_achieved, "frac": call_achieved / peak,
                                "avg_call_us": call_ms * 1e3,
-                               "timed": "region over the steps, calls chained back to back"}}
+                               "timed": "region over the steps, calls chained back to back",
+                               "period_us_p10_median_p90": q3(chained_period_us),
+                               "frac_median_period": w.algorithmic_bytes / (period_med / 1e6) / 1e9 / peak},
+                "chained": {"calls": STAT_CALLS,
+                            "timed": ("device global-timer stamps of calls chained back to back "
+                                      "(spec_arm_timer): first streaming-CTA start, last streaming-CTA "
+                                      "end, last output"),
+                            "row_kernel_us_p10_median_p90": q3(chained_row_us),
+                            "row_kernel_frac_median": w.algorithmic_bytes / (row_med / 1e6) / 1e9 / peak,
+                            "call_device_us_p10_median_p90": q3(chained_call_us),
+                            "period_us_p10_median_p90": q3(chained_period_us)}}
     if w.T > 0:  # one MUFU ex2 per streamed logit
         exps = w.algorithmic_bytes / (4 if w.dtype == "f32" else 2)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count

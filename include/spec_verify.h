@@ -459,6 +459,20 @@ int spec_get_status(void *stream);
 int spec_arm_rows_event(void *event);
 
 /*
+ * spec_arm_timer — measurement hook that leaves the stream untouched: the
+ * next verification call (any spec_verify* entry point) made by the calling
+ * host thread records global-timer stamps (%globaltimer, ns) into `stamps`,
+ * three unsigned 64-bit words in device memory that the caller has set to
+ * (UINT64_MAX, 0, 0): [0] the earliest start of a streaming CTA (after its
+ * wait on the preceding work), [1] the latest end of one, [2] the latest
+ * output written by the decision kernel.  No event or other operation is
+ * put between the call's launches, so calls made back to back still chain
+ * by programmatic dependent launch, and [1] - [0] is the streaming kernel's
+ * time as it runs there.  The hook is then disarmed.  Always returns SPEC_OK.
+ */
+int spec_arm_timer(unsigned long long *stamps);
+
+/*
  * spec_selftest_wait — diagnostic of the bounded waits every kernel uses on
  * its barriers: one thread waits on a barrier that nothing completes; the
  * wait gives up after one second of global time or 2^17 polls, whichever

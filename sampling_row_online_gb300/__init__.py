@@ -10,7 +10,7 @@ from __future__ import annotations
 __all__ = ["spec_verify", "spec_verify_ex", "spec_verify_host", "spec_verify_noalloc", "spec_verify_points",
            "spec_verify_tree_greedy", "spec_verify_tree", "spec_verify_trees_greedy", "spec_verify_trees",
            "spec_tree_mask", "spec_tree_max_depth", "spec_ngram_propose", "spec_topk", "spec_eagle2_expand",
-           "spec_eagle2_rerank", "spec_selftest_wait", "spec_get_status", "spec_arm_rows_event",
+           "spec_eagle2_rerank", "spec_selftest_wait", "spec_get_status", "spec_arm_rows_event", "spec_arm_timer",
            "spec_debug_fail_launch", "spec_noalloc_get_status", "spec_debug_noalloc_status",
            "spec_error_string", "spec_last_error_message", "spec_shutdown",
            "SpecError", "library"]

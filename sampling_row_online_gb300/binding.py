@@ -54,6 +54,7 @@ def library():
     lib.spec_verify_ex.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, u64, vp, vp, vp, vp, vp, vp]
     lib.spec_verify_host.argtypes = [vp, vp, vp, i32, i32, i32, i32, f32, u64, vp, vp, vp]
     lib.spec_arm_rows_event.argtypes = [vp]
+    lib.spec_arm_timer.argtypes = [vp]
     lib.spec_verify_tree_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.spec_verify_tree.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, f32, u64, i32, vp, vp, vp]
     lib.spec_verify_trees_greedy.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]
@@ -517,6 +518,17 @@ def spec_arm_rows_event(event):
     records `event` (a torch.cuda.Event that has been recorded once, so that
     it exists) between its streaming and decision kernels."""
     library().spec_arm_rows_event(ctypes.c_void_p(event.cuda_event))
+
+
+def spec_arm_timer(stamps):
+    """Measurement hook: the next verification call made from this thread
+    records global-timer stamps into `stamps` (a CUDA int64 tensor of 3 words
+    set to (-1, 0, 0), read as unsigned): first streaming-CTA start, last
+    streaming-CTA end, last output."""
+    _dev(stamps, "stamps", torch.int64)
+    if stamps.numel() < 3:
+        raise ValueError("stamps must hold 3 int64 words")
+    library().spec_arm_timer(_ptr(stamps))
 
 
 def spec_debug_fail_launch(n):

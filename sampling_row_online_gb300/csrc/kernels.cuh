@@ -104,7 +104,17 @@ struct Params {
   int *tickets;             // item tickets, shard k at tickets[k * TICKET_STRIDE]; zero
                             // between calls (the decision kernel puts them back)
   int nshard;               // ticket shards in use
+  unsigned long long *timer;  // measurement (or null): global-timer ns of the first row CTA's
+                              // start [0], the last row CTA's end [1], the last output [2]
 };
+
+// Measurement stamps (spec_arm_timer): the earliest start and the latest end.
+__device__ __forceinline__ void timer_min(const Params &p, int k) {
+  if (p.timer) atomicMin(p.timer + k, static_cast<unsigned long long>(clock_ns()));
+}
+__device__ __forceinline__ void timer_max(const Params &p, int k) {
+  if (p.timer) atomicMax(p.timer + k, static_cast<unsigned long long>(clock_ns()));
+}
 
 // ------------------------------------------------------------------ elements
 template <int DT>
@@ -482,6 +492,7 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
   // CTAs above were set up while that kernel finished; nothing in global
   // memory is touched before it has completed.
   pdl_wait();
+  if (tid == 0) timer_min(p, 0);
 
   if (warp == NCW) {
     // ------------------------------------------------------------ producer
@@ -666,6 +677,7 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
     }
     if (lane == 0) p.partials[static_cast<size_t>(m.item) * NCW + warp] = out;
   }
+  if (lane == 0) timer_max(p, 1);
   pdl_launch_dependents();
   if (tmo) atomicOr(p.status, ST_TIMEOUT);
 }
@@ -1604,6 +1616,7 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
         const bool near = __shfl_sync(0xFFFFFFFFu, static_cast<int>(nd), who & 31) || sh.near_acc;
         for (int j = lane; j <= K; j += 32) out[j] = j < kb ? gtok[j] : (j == kb ? tk : -1);
         if (lane == 0) {
+          timer_max(p, 2);
           p.out_n[b] = kb;
           if (p.stats) {
             atomicAdd(&p.stats->sequences, 1ull);
@@ -1652,6 +1665,7 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   const bool near = __shfl_sync(0xFFFFFFFFu, static_cast<int>(nd), who & 31) || sh.near_acc;
   for (int j = lane; j <= K; j += 32) out[j] = j < n ? gtok[j] : (j == n ? tk : -1);
   if (lane == 0) {
+    timer_max(p, 2);
     p.out_n[b] = n;
     if (p.stats) {
       atomicAdd(&p.stats->sequences, 1ull);
@@ -1799,7 +1813,10 @@ __global__ void __launch_bounds__(NT, 4) tree_draw_kernel(const Params p) {
             wbuf, sh);
         for (int j = tid; j < W1; j += NT)
           if (j >= len) path[j] = j == len ? token : -1;
-        if (tid == 0) p.out_n[b] = len + 1;
+        if (tid == 0) {
+          p.out_n[b] = len + 1;
+          timer_max(p, 2);
+        }
       }
       return;
     }
@@ -1857,7 +1874,10 @@ __global__ void __launch_bounds__(NT, 4) tree_draw_kernel(const Params p) {
     }
     for (int j = tid; j < W1; j += NT)
       if (j >= len) path[j] = j == len ? token : -1;
-    if (tid == 0) p.out_n[b] = len + 1;
+    if (tid == 0) {
+      p.out_n[b] = len + 1;
+      timer_max(p, 2);
+    }
     return;
   }
 }
@@ -1933,6 +1953,7 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
       for (int e = 0; e <= K; ++e)
         out[e] = err ? -1 : (e < nacc ? s_tok[e] : (e == nacc ? s_amax[nacc] : -1));
       p.out_n[b] = err ? -1 : nacc;
+      timer_max(p, 2);
       if (err) atomicOr(p.status, ST_TOKEN);
       if (p.stats) {
         if (err) {
@@ -1988,6 +2009,7 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
       path[d] = s_amax[bestn];
       for (int n2 = bestn, e = d - 1; n2 != 0; n2 = s_par[n2], --e) path[e] = s_tok[n2];
       p.out_n[b] = d + 1;
+      timer_max(p, 2);
     }
   }
 }

@@ -325,10 +325,14 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
 // One-shot measurement hook (spec_arm_rows_event): recorded on the stream
 // between the two launches of the next call on this host thread.
 thread_local cudaEvent_t g_rows_event = nullptr;
+// One-shot measurement hook (spec_arm_timer): device stamps of the next call.
+thread_local unsigned long long *g_timer = nullptr;
 
 int launch(Params &p, const Geometry &g, cudaStream_t stream, float4 *partials, int32_t *status) {
   const cudaEvent_t ev_rows = g_rows_event;
   g_rows_event = nullptr;
+  p.timer = g_timer;
+  g_timer = nullptr;
   p.tickets = tickets_of(status);
   p.nshard = g.nshard;
   p.C = g.C;
@@ -916,6 +920,11 @@ int spec_selftest_wait(void *stream_ptr) {
 int spec_debug_fail_launch(int n) {
   if (n < 0) return fail(SPEC_ERR_ARG, "n must be >= 0");
   g_fail_launch.store(n);
+  return SPEC_OK;
+}
+
+int spec_arm_timer(unsigned long long *stamps) {
+  g_timer = stamps;
   return SPEC_OK;
 }
 
