@@ -377,11 +377,12 @@ int spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int
  *               lower index
  *   out_prob    [R, k] float (device): softmax(z / T) of those tokens
  * Rows must hold one finite logit (-inf entries allowed).
- * Launch geometry: each row is split over a cluster of G CTAs (G a power of
- * two up to 8, about one wave of 3 CTAs per SM); the environment variable
- * SPEC_TOPK_CLUSTER, read at each call, sets G instead (rounded down to a
- * power of two; any G gives the same outputs).  No other environment
- * variable changes this library's launches.
+ * Launch geometry: each row is split over a cluster of G CTAs of 512
+ * threads (G a power of two up to 8, about one wave of 1.5 CTAs per SM, each
+ * slice at least 32 KB; G = 1 when the rows alone fill that wave); the
+ * environment variable SPEC_TOPK_CLUSTER, read at each call, sets G instead
+ * (rounded down to a power of two; any G gives the same outputs).  No other
+ * environment variable changes this library's launches.
  */
 int spec_topk(const void *logits, int R, int V, int dtype, float temperature, int k,
               int32_t *out_tokens, float *out_prob, void *stream);
@@ -460,15 +461,18 @@ int spec_arm_rows_event(void *event);
 
 /*
  * spec_arm_timer — measurement hook that leaves the stream untouched: the
- * next verification call (any spec_verify* entry point) made by the calling
- * host thread records global-timer stamps (%globaltimer, ns) into `stamps`,
- * three unsigned 64-bit words in device memory that the caller has set to
- * (UINT64_MAX, 0, 0): [0] the earliest start of a streaming CTA (after its
- * wait on the preceding work), [1] the latest end of one, [2] the latest
- * output written by the decision kernel.  No event or other operation is
- * put between the call's launches, so calls made back to back still chain
- * by programmatic dependent launch, and [1] - [0] is the streaming kernel's
- * time as it runs there.  The hook is then disarmed.  Always returns SPEC_OK.
+ * next verification call (any spec_verify* entry point) or top-k launch
+ * (spec_topk, or the top-k of spec_eagle2_expand) made by the calling host
+ * thread records global-timer stamps (%globaltimer, ns) into `stamps`, three
+ * unsigned 64-bit words in device memory that the caller has set to
+ * (UINT64_MAX, 0, 0).  Verification: [0] the earliest start of a streaming
+ * CTA (after its wait on the preceding work), [1] the latest end of one, [2]
+ * the latest output written by the decision kernel.  Top-k: [0] the earliest
+ * CTA start (after the wait), [1] the latest CTA end, [2] the latest row
+ * written.  No event or other operation is put between the launches, so
+ * calls made back to back still chain by programmatic dependent launch, and
+ * [1] - [0] is the kernel's time as it runs there.  The hook is then
+ * disarmed.  Always returns SPEC_OK.
  */
 int spec_arm_timer(unsigned long long *stamps);
 

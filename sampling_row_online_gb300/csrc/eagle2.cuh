@@ -85,20 +85,35 @@ struct TopkParams {
   const int32_t *frontier;
   int32_t *node_par;
   int32_t *status;
+  unsigned long long *timer;  // measurement (or null): [0] earliest CTA start, [1] latest CTA end,
+                              // [2] latest row written (global-timer ns)
 };
 
+__device__ __forceinline__ void topk_stamp(const TopkParams &p, int k, bool first) {
+  if (!p.timer) return;
+  const unsigned long long t = clock_ns();
+  if (first)
+    atomicMin(p.timer + k, t);
+  else
+    atomicMax(p.timer + k, t);
+}
+
 constexpr int TOPK_MAX_CLUSTER = 8;  // CTAs sharing one row
+constexpr int TOPK_NT = 512;         // threads of a top-k CTA
+constexpr int TOPK_NWARP = TOPK_NT / 32;
+constexpr int TOPK_GS = TOPK_NT / 32;  // threads per group of the threshold (32 groups)
+static_assert(TOPK_GS <= 32 && 32 % TOPK_GS == 0, "threshold groups lie within a warp");
 constexpr int TOPK_BUF = 1024;       // candidate keys a CTA collects before falling back
 
 struct TopkShared {
   unsigned long long buf[TOPK_BUF];                   // candidates (keys >= the threshold)
-  float wmax[NWARP][32];                              // per-warp sorted thread maxima
+  uint4 pv[TOPK_NT];                                       // each thread's best vector, fetched again
+  float gmax[32];                                     // maxima of the threshold's groups
   int nbuf;
-  float t;                                            // the CTA's threshold
-  unsigned long long wk[NWARP][TOPK_MAX];             // per-warp lists (fallback path)
+  unsigned long long wk[TOPK_NWARP][TOPK_MAX];             // per-warp lists (fallback path)
   unsigned long long ctak[TOPK_MAX];                  // this CTA's top k
   unsigned long long ck[TOPK_MAX_CLUSTER][TOPK_MAX];  // rank 0: the CTA lists of the cluster
-  float wm[NWARP], ws[NWARP];
+  float wm[TOPK_NWARP], ws[TOPK_NWARP];
   float cm[TOPK_MAX_CLUSTER], cs[TOPK_MAX_CLUSTER];   // rank 0: the CTA normalisers
   unsigned long long bar_key;                         // largest k-th key of any warp so far
 };
@@ -180,7 +195,7 @@ __device__ void topk_slice_by_admission(const unsigned char *row, int lo, int hi
   float thr = -INFINITY;
   if (VEC) {
     const uint4 *rv = reinterpret_cast<const uint4 *>(row);
-    for (int base = lo + warp * 32; base < hi; base += NT) {  // warp-uniform
+    for (int base = lo + warp * 32; base < hi; base += TOPK_NT) {  // warp-uniform
       const int vi = base + lane;
       const uint4 q = vi < hi ? __ldg(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
       uint32_t cm = 0u;
@@ -193,7 +208,7 @@ __device__ void topk_slice_by_admission(const unsigned char *row, int lo, int hi
       warp_admit<DT>(cm, q, vi * VE, k, lane, lk, kkey, thr, &sh.bar_key);
     }
   } else {
-    for (int i0 = lo + warp * 32; i0 < hi; i0 += NT) {  // warp-uniform
+    for (int i0 = lo + warp * 32; i0 < hi; i0 += TOPK_NT) {  // warp-uniform
       const int i = i0 + lane;
       const float x = i < hi ? Elem<DT>::load(row, i) : -INFINITY;
       const uint4 q = make_uint4(__float_as_uint(x), 0u, 0u, 0u);
@@ -205,7 +220,7 @@ __device__ void topk_slice_by_admission(const unsigned char *row, int lo, int hi
   if (warp == 0) {
     int head = 0;
     for (int j = 0; j < k; ++j) {
-      const unsigned long long mine = lane < NWARP && head < k ? sh.wk[lane][head] : 0ull;
+      const unsigned long long mine = lane < TOPK_NWARP && head < k ? sh.wk[lane][head] : 0ull;
       const unsigned long long best = warp_max_key(mine);
       if (mine == best && best != 0ull) ++head;
       if (lane == 0) sh.ctak[j] = best;
@@ -214,8 +229,71 @@ __device__ void topk_slice_by_admission(const unsigned char *row, int lo, int hi
   __syncthreads();
 }
 
+// (max, sum of 2^((z - max) c)) of the states held by lanes 0 .. n-1 (n a
+// power of two up to 32), into every one of those lanes: the maximum first,
+// then one rescale per lane and the sum, so the dependent chain holds one
+// exponential.
+__device__ __forceinline__ void group_ms(float &m, float &s, float c, int n) {
+  float M = m;
+  for (int o = 1; o < n; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+  float t = (M == -INFINITY || m == -INFINITY) ? 0.f : s * ex2((m - M) * c);
+  for (int o = 1; o < n; o <<= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+  m = M;
+  s = t;
+}
+
+// Rank 0 of a row's cluster, one warp: merges the G CTA lists (each sorted,
+// best first; keys distinct, empty slots 0), combines the G slice
+// normalisers, and writes the row's k tokens and probabilities (the
+// expansion layout writes straight into the node arrays).  `poisoned`: a
+// wait of the row ran out; the row is written as tokens -1 with probability
+// 0 (parents -1).
+__device__ __forceinline__ void topk_write_row(const TopkParams &p, int r, int G, int k,
+                                               const unsigned long long (*ck)[TOPK_MAX], const float *cm,
+                                               const float *cs, int lane, bool poisoned) {
+  float m = lane < G ? cm[lane] : -INFINITY;
+  float s = lane < G ? cs[lane] : 0.f;
+  group_ms(m, s, p.c, G);
+  m = __shfl_sync(0xFFFFFFFFu, m, 0);
+  const float inv_s = 1.f / __shfl_sync(0xFFFFFFFFu, s, 0);
+  auto put = [&](int j, int idx, float prob, int par) {
+    if (p.F == 0) {
+      p.out_tok[static_cast<size_t>(r) * k + j] = idx;
+      p.out_prob[static_cast<size_t>(r) * k + j] = prob;
+    } else {
+      const int b = r / p.F, f = r - b * p.F;
+      const size_t slot = static_cast<size_t>(b) * p.cap + p.offset + f * k + j;
+      p.out_tok[slot] = idx;
+      p.out_prob[slot] = prob;  // the select step multiplies by the parent's value
+      p.node_par[slot] = par;
+    }
+  };
+  if (poisoned) {
+    for (int j = lane; j < k; j += 32) put(j, -1, 0.f, -1);
+    return;
+  }
+  // slot (g, j) of the lists: its rank is j plus the keys above it in the
+  // other lists; the k best are written in parallel
+  for (int l = lane; l < G * k; l += 32) {
+    const int g = l / k, j = l - g * k;
+    const unsigned long long key = ck[g][j];
+    if (key == 0ull) continue;
+    int rk = j;
+    for (int g2 = 0; g2 < G; ++g2) {
+      if (g2 == g) continue;
+#pragma unroll
+      for (int j2 = 0; j2 < TOPK_MAX; ++j2) rk += j2 < k && ck[g2][j2] > key;
+    }
+    if (rk < k) {
+      const int idx = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
+      const float x = order_float(static_cast<uint32_t>(key >> 32));
+      put(rk, idx, ex2(fmaf(x, p.c, -m * p.c)) * inv_s, p.F == 0 ? 0 : __ldg(p.frontier + r));
+    }
+  }
+}
+
 template <int DT, bool VEC>
-__global__ void __launch_bounds__(NT, 4) topk_kernel(TopkParams p) {
+__global__ void __launch_bounds__(TOPK_NT, 2) topk_kernel(TopkParams p) {
   __shared__ TopkShared sh;
   constexpr int VE = Elem<DT>::VE;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -226,84 +304,114 @@ __global__ void __launch_bounds__(NT, 4) topk_kernel(TopkParams p) {
   pdl_launch_dependents();
   if (tid == 0) sh.nbuf = 0;
   pdl_wait();
+  if (tid == 0) topk_stamp(p, 0, true);
   const unsigned char *row = static_cast<const unsigned char *>(p.z) +
                              static_cast<size_t>(r) * p.V * Elem<DT>::BYTES;
   const int n = VEC ? p.V / VE : p.V;  // vectors (VEC) or elements
   const int per = (n + G - 1) / G;
   const int lo = min(n, rank * per), hi = min(n, lo + per);
 
-  // pass 1: online (max, sum) and the thread's own largest logit
+  // pass 1: online (max, sum) and the thread's own largest logit; with
+  // vector loads, also the index of the thread's best vector (the first to
+  // reach the maximum; -1: no vector with a finite maximum) and the largest
+  // maximum of its other vectors
   float m = -INFINITY, s = 0.f, tmax = -INFINITY;
+  float vm2 = -INFINITY;
+  int j1 = -1;
   if (VEC) {
     // the streaming kernel's per-vector update (packed maxima, paired sums);
     // the online state's maximum is the thread's own largest logit
-    Online st;
+    Online st;  // st.m is also the best vector's maximum
     st.init();
     const uint4 *rv = reinterpret_cast<const uint4 *>(row);
-    // thread (warp, lane) reads vectors lo + warp * 32 + lane + j * NT
+    // thread (warp, lane) reads vectors lo + warp * 32 + lane + j * TOPK_NT
     auto fetch = [&](uint4 (&d)[TOPK_U], int b) {
 #pragma unroll
       for (int u = 0; u < TOPK_U; ++u) {
-        const int vi = b + u * NT + lane;
+        const int vi = b + u * TOPK_NT + lane;
         d[u] = vi < hi ? __ldg(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
       }
     };
     uint4 q[TOPK_U];
     fetch(q, lo + warp * 32);
-    for (int base = lo + warp * 32; base < hi; base += TOPK_U * NT) {  // warp-uniform
+    for (int base = lo + warp * 32; base < hi; base += TOPK_U * TOPK_NT) {  // warp-uniform
       uint4 nq[TOPK_U];
-      fetch(nq, base + TOPK_U * NT);  // the next round, in flight while this one is weighed
+      fetch(nq, base + TOPK_U * TOPK_NT);  // the next round, in flight while this one is weighed
 #pragma unroll
-      for (int u = 0; u < TOPK_U; ++u)
-        if (base + u * NT + lane < hi) online_vec16<DT>(q[u], p.c, st);
+      for (int u = 0; u < TOPK_U; ++u) {
+        const int vi = base + u * TOPK_NT + lane;
+        if (vi < hi) {
+          const float vm1 = st.m;
+          const float vm = online_vec16<DT>(q[u], p.c, st);
+          const bool a1 = vm > vm1;
+          vm2 = a1 ? vm1 : fmaxf(vm2, vm);
+          j1 = a1 ? vi : j1;
+        }
+      }
 #pragma unroll
       for (int u = 0; u < TOPK_U; ++u) q[u] = nq[u];
     }
     m = st.m;
     s = st.sum();
     tmax = st.m;
+    // the best vector again (from L2) into the thread's shared slot, an
+    // asynchronous copy in flight while the threshold is found
+    if (j1 >= 0) cp_async16(&sh.pv[tid], rv + j1);
+    cp_async_commit();
   } else {
-    for (int i = lo + tid; i < hi; i += NT) {
+    for (int i = lo + tid; i < hi; i += TOPK_NT) {
       const float x = Elem<DT>::load(row, i);
       topk_online(x, p.c, m, s);
       tmax = fmaxf(tmax, x);
     }
   }
 
-  // the threshold t: the k-th largest thread maximum (at least k elements of
-  // the slice are >= t, so its k best all are)
+  // the threshold t: a lower bound of the slice's k-th best element.  The
+  // 32 groups of TOPK_GS consecutive threads each have a maximum, an element
+  // of the group; k groups have a maximum >= the k-th largest group maximum,
+  // so at least k elements are >= it.  Every warp sorts the 32 group maxima
+  // itself and takes the k-th: one barrier.
   {
-    const float sorted = warp_sort_desc(tmax, lane);
-    sh.wmax[warp][lane] = sorted;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    int head = 0;
-    float t = -INFINITY;
-    for (int j = 0; j < k; ++j) {
-      const float mine = lane < NWARP && head < 32 ? sh.wmax[lane][head] : -INFINITY;
-      float best = mine;
+    float g = tmax;
 #pragma unroll
-      for (int o = 16; o; o >>= 1) best = fmaxf(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
-      const unsigned win = __ballot_sync(0xFFFFFFFFu, mine == best && lane < NWARP && head < 32);
-      if (lane == __ffs(win) - 1) ++head;
-      t = best;
-    }
-    if (lane == 0) sh.t = t;
+    for (int o = 1; o < TOPK_GS; o <<= 1) g = fmaxf(g, __shfl_xor_sync(0xFFFFFFFFu, g, o));
+    if (lane % TOPK_GS == 0) sh.gmax[tid / TOPK_GS] = g;
   }
   __syncthreads();
-  const float t = sh.t;
+  const float t = __shfl_sync(0xFFFFFFFFu, warp_sort_desc(sh.gmax[lane], lane), k - 1);
 
-  // pass 2: the elements >= t lie in the vectors of "hot" threads (their own
-  // maximum reaches t); each warp re-reads its hot lanes' vectors together,
-  // one vector per lane, HB hot lanes at a time (their loads in flight
-  // together), and appends the keys of elements >= t
+  // candidates: the elements >= t.  They lie in the vectors of "hot" threads
+  // (their own maximum reaches t).  With vector loads a hot thread whose
+  // other vectors all stay below t offers the elements of its best vector
+  // (fetched above); one whose other vectors may reach t too (always so
+  // when t = -inf) re-reads all its vectors instead: the warp loads such a
+  // lane's vectors together, one per lane, HB lanes at a time.  Keys >= t
+  // are appended to a shared buffer.
   {
-    unsigned hot = __ballot_sync(0xFFFFFFFFu, tmax >= t);
+    unsigned hot;
+    if (VEC) {
+      cp_async_wait_all();  // every thread: no copy outlives this step
+      const bool mine = lo + warp * 32 + lane < hi && tmax >= t;
+      const bool reread = mine && (j1 < 0 || vm2 >= t);
+      if (mine && !reread) {
+        float f[VE];
+        Elem<DT>::unpack(sh.pv[tid], f);
+#pragma unroll
+        for (int e = 0; e < VE; ++e) {
+          if (f[e] >= t) {
+            const int slot = atomicAdd(&sh.nbuf, 1);
+            if (slot < TOPK_BUF) sh.buf[slot] = topk_key(f[e], j1 * VE + e);
+          }
+        }
+      }
+      hot = __ballot_sync(0xFFFFFFFFu, reread);
+    } else {
+      hot = __ballot_sync(0xFFFFFFFFu, tmax >= t);
+    }
     if (VEC) {
       constexpr int HB = 4;
       const uint4 *rv = reinterpret_cast<const uint4 *>(row);
-      const int wfirst = lo + warp * 32;  // lane h's vectors: wfirst + h + j * NT
+      const int wfirst = lo + warp * 32;  // lane h's vectors: wfirst + h + j * TOPK_NT
       while (hot) {  // warp-uniform
         int first[HB];
 #pragma unroll
@@ -312,12 +420,12 @@ __global__ void __launch_bounds__(NT, 4) topk_kernel(TopkParams p) {
           hot &= hot - 1u;
         }
         // first[0] is the smallest, so its vectors bound the others'
-        for (int j0 = 0; first[0] + j0 * NT < hi; j0 += 32) {  // warp-uniform
+        for (int j0 = 0; first[0] + j0 * TOPK_NT < hi; j0 += 32) {  // warp-uniform
           uint4 q[HB];
           int vi[HB];
 #pragma unroll
           for (int g = 0; g < HB; ++g) {
-            vi[g] = first[g] + (j0 + lane) * NT;
+            vi[g] = first[g] + (j0 + lane) * TOPK_NT;
             q[g] = vi[g] < hi ? __ldg(rv + vi[g]) : make_uint4(0u, 0u, 0u, 0u);
           }
 #pragma unroll
@@ -340,9 +448,9 @@ __global__ void __launch_bounds__(NT, 4) topk_kernel(TopkParams p) {
       const int h = __ffs(hot) - 1;
       hot &= hot - 1u;
       {
-        const int first = lo + warp * 32 + h;  // lane h's elements: first + j * NT (see pass 1)
-        for (int j0 = 0; first + j0 * NT < hi; j0 += 32) {
-          const int i = first + (j0 + lane) * NT;
+        const int first = lo + warp * 32 + h;  // lane h's elements: first + j * TOPK_NT (see pass 1)
+        for (int j0 = 0; first + j0 * TOPK_NT < hi; j0 += 32) {
+          const int i = first + (j0 + lane) * TOPK_NT;
           if (i < hi) {
             const float x = Elem<DT>::load(row, i);
             if (x >= t) {
@@ -354,89 +462,68 @@ __global__ void __launch_bounds__(NT, 4) topk_kernel(TopkParams p) {
       }
     }
   }
-  __syncthreads();
-  const int nb = sh.nbuf;
-  if (nb <= TOPK_BUF) {
-    // rank of each candidate among the candidates (keys are distinct)
-    for (int i = tid; i < nb; i += NT) {
-      const unsigned long long key = sh.buf[i];
-      int rk = 0;
-      for (int j = 0; j < nb; ++j) rk += sh.buf[j] > key;
-      if (rk < k) sh.ctak[rk] = key;
-    }
-    for (int j = nb + tid; j < k; j += NT) sh.ctak[j] = 0ull;  // a slice with fewer than k elements
-    __syncthreads();
-  } else {
-    topk_slice_by_admission<DT, VEC>(row, lo, hi, k, sh);
-  }
 
-  // normalisers of the slice; the CTA's list and normalisers go to rank 0
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
-    const float mn = fmaxf(m, m2);
-    s = (m == -INFINITY ? 0.f : s * ex2((m - mn) * p.c)) + (m2 == -INFINITY ? 0.f : s2 * ex2((m2 - mn) * p.c));
-    m = mn;
-  }
+  // the slice's normalisers: each warp's (their latency overlaps the
+  // barrier's wait), then warp 0 combines the warps'
+  group_ms(m, s, p.c, 32);
   if (lane == 0) {
     sh.wm[warp] = m;
     sh.ws[warp] = s;
   }
   __syncthreads();
-  if (warp == 0) {
-    m = lane < NWARP ? sh.wm[lane] : -INFINITY;
-    s = lane < NWARP ? sh.ws[lane] : 0.f;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-      const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
-      const float mn = fmaxf(m, m2);
-      s = (m == -INFINITY ? 0.f : s * ex2((m - mn) * p.c)) + (m2 == -INFINITY ? 0.f : s2 * ex2((m2 - mn) * p.c));
-      m = mn;
+
+  // the CTA's k best: at most 32 candidates (the usual case) are ranked by
+  // warp 0 alone, which stores them straight into rank 0's list; more are
+  // ranked by the whole CTA into sh.ctak (or, past the buffer, found by
+  // lockstep admission)
+  const int nb = sh.nbuf;
+  const bool few = nb <= 32;
+  if (!few) {
+    if (nb <= TOPK_BUF) {
+      for (int i = tid; i < nb; i += TOPK_NT) {
+        const unsigned long long key = sh.buf[i];
+        int rk = 0;
+        for (int j = 0; j < nb; ++j) rk += sh.buf[j] > key;
+        if (rk < k) sh.ctak[rk] = key;
+      }
+      __syncthreads();
+    } else {
+      topk_slice_by_admission<DT, VEC>(row, lo, hi, k, sh);
     }
-    if (lane < k) dsmem_st_u64(dsmem_addr(&sh.ck[rank][lane], 0), sh.ctak[lane]);
+  }
+  if (warp == 0) {
+    unsigned long long key;
+    int rk;
+    if (few) {
+      key = lane < nb ? sh.buf[lane] : 0ull;
+      rk = lane;  // lanes >= nb: empty slots (key 0) after the nb real keys
+      if (lane < nb) {
+        rk = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) rk += j < nb && sh.buf[j] > key;
+      }
+    } else {
+      key = lane < k ? sh.ctak[lane] : 0ull;
+      rk = lane;
+    }
+    if (rk < k) dsmem_st_u64(dsmem_addr(&sh.ck[rank][rk], 0), key);
+    m = lane < TOPK_NWARP ? sh.wm[lane] : -INFINITY;
+    s = lane < TOPK_NWARP ? sh.ws[lane] : 0.f;
+    group_ms(m, s, p.c, TOPK_NWARP);
     if (lane == 0) {
       dsmem_st_f32(dsmem_addr(&sh.cm[rank], 0), m);
       dsmem_st_f32(dsmem_addr(&sh.cs[rank], 0), s);
     }
   }
-  cluster_sync();
+  if (G > 1)
+    cluster_sync();  // G is the same for every CTA of the grid
+  else
+    __syncwarp();  // one CTA per row: warp 0 stored its own list above
+  if (tid == 0) topk_stamp(p, 1, false);
   if (rank != 0 || warp != 0) return;
-  // rank 0: merge the G CTA lists, combine the normalisers, write the row
-  m = lane < G ? sh.cm[lane] : -INFINITY;
-  s = lane < G ? sh.cs[lane] : 0.f;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-    const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
-    const float mn = fmaxf(m, m2);
-    s = (m == -INFINITY ? 0.f : s * ex2((m - mn) * p.c)) + (m2 == -INFINITY ? 0.f : s2 * ex2((m2 - mn) * p.c));
-    m = mn;
-  }
-  // rank of every key of the G lists among them (keys are distinct; empty
-  // slots are 0 and rank last), then the k best in parallel
-  for (int i = lane; i < G * k; i += 32) {
-    const unsigned long long key = sh.ck[i / k][i % k];
-    if (key == 0ull) continue;
-    int rk = 0;
-    for (int j = 0; j < G * k; ++j) rk += sh.ck[j / k][j % k] > key;
-    if (rk < k) {
-      const int idx = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(key));
-      const float x = order_float(static_cast<uint32_t>(key >> 32));
-      const float prob = ex2(fmaf(x, p.c, -m * p.c)) / s;
-      if (p.F == 0) {
-        p.out_tok[static_cast<size_t>(r) * k + rk] = idx;
-        p.out_prob[static_cast<size_t>(r) * k + rk] = prob;
-      } else {
-        const int b = r / p.F, f = r - b * p.F;
-        const size_t slot = static_cast<size_t>(b) * p.cap + p.offset + f * k + rk;
-        p.out_tok[slot] = idx;
-        p.out_prob[slot] = prob;  // the select step multiplies by the parent's value
-        p.node_par[slot] = __ldg(p.frontier + r);
-      }
-    }
-  }
+  topk_write_row(p, r, G, k, sh.ck, sh.cm, sh.cs, lane, false);
+  __syncwarp();
+  if (lane == 0) topk_stamp(p, 2, false);
 }
 
 struct EagleParams {

@@ -424,9 +424,10 @@ struct Online {
   __device__ __forceinline__ float sum() const { return s.x + s.y; }
 };
 
-// One 16-byte vector of logits into the online state.
+// One 16-byte vector of logits into the online state; returns the vector's
+// largest logit.
 template <int DT>
-__device__ __forceinline__ void online_vec16(const uint4 w, float c, Online &st) {
+__device__ __forceinline__ float online_vec16(const uint4 w, float c, Online &st) {
   float f[Elem<DT>::VE];
   Elem<DT>::unpack(w, f);
   float vm;
@@ -438,6 +439,7 @@ __device__ __forceinline__ void online_vec16(const uint4 w, float c, Online &st)
   }
   st.rescale(vm, c);
   st.accumulate(f, c);
+  return vm;
 }
 
 // What the producer tells the consumers about the tile in a stage.
@@ -530,21 +532,30 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
     };
     // Items come from this CTA's ticket shard (the grid is a multiple of the
     // shard count, so every shard has as many CTAs as items / ns needs):
-    // CTAs that run ahead take more items and all CTAs end together.  Lane 0
-    // holds the next ticket, fetched one item ahead so its latency hides
-    // behind the current item.
+    // CTAs that run ahead take more items and all CTAs end together.  The
+    // first item of CTA i is item i (no ticket, so the first copy is issued
+    // at once); the shard's tickets then count from the shard's CTAs onward.
+    // Lane 0 holds the next ticket, fetched one item ahead so its latency
+    // hides behind the current item.
     const int ns = p.nshard;
     const int shard = static_cast<int>(blockIdx.x) % ns;
+    const int per_shard = static_cast<int>(gridDim.x) / ns;
     int tk = 0;
-    if (lane == 0) tk = atomicAdd(&p.tickets[shard * TICKET_STRIDE], 1);
+    bool first = true;
+    if (lane == 0) tk = atomicAdd(&p.tickets[shard * TICKET_STRIDE], 1) + per_shard;
     for (;;) {
       int it = nitems;
       if (lane == 0) {
-        const long long cand = static_cast<long long>(tk) * ns + shard;
-        if (cand < nitems) {
-          it = static_cast<int>(cand);
-          tk = atomicAdd(&p.tickets[shard * TICKET_STRIDE], 1);
+        if (first) {
+          it = static_cast<int>(blockIdx.x);  // the grid never exceeds the items
+        } else {
+          const long long cand = static_cast<long long>(tk) * ns + shard;
+          if (cand < nitems) {
+            it = static_cast<int>(cand);
+            tk = atomicAdd(&p.tickets[shard * TICKET_STRIDE], 1) + per_shard;
+          }
         }
+        first = false;
       }
       it = __shfl_sync(0xFFFFFFFFu, it, 0);
       if (it >= nitems || tmo) break;

@@ -79,6 +79,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// Asynchronous 16-byte copy global -> this thread's shared memory slot (both
+// 16-byte aligned).  Barriers do not wait for it: the issuing thread waits
+// with cp_async_wait_all before it reads the slot.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;

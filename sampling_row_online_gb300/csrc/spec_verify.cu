@@ -503,9 +503,12 @@ int check_topk_args(int R, int V, int dtype, float T, int k) {
 }
 
 // One launch of the top-k kernel (a programmatic dependent of earlier work):
-// G CTAs per row in one cluster, each a contiguous slice of at least 16 KB,
-// G a power of two up to 8 giving about one wave of 3 CTAs per SM.
+// G CTAs per row in one cluster, each a contiguous slice of at least 32 KB,
+// G a power of two up to 8 giving about one wave of 1.5 CTAs (of 512
+// threads) per SM; rows enough for that wave take one CTA each.
 int launch_topk(TopkParams &p, int dtype, cudaStream_t stream) {
+  p.timer = g_timer;
+  g_timer = nullptr;
   const size_t esz = dtype == SPEC_F32 ? 4 : 2;
   const bool vec = aligned16(p.z) && (static_cast<size_t>(p.V) * esz) % 16 == 0;
   const void *fn = dtype == SPEC_F32
@@ -513,8 +516,8 @@ int launch_topk(TopkParams &p, int dtype, cudaStream_t stream) {
                               : reinterpret_cast<const void *>(&topk_kernel<0, false>))
                        : (vec ? reinterpret_cast<const void *>(&topk_kernel<1, true>)
                               : reinterpret_cast<const void *>(&topk_kernel<1, false>));
-  const long long want = (3LL * num_sms() + p.R - 1) / p.R;
-  const long long by_size = std::max<long long>(1, static_cast<long long>(p.V) * esz / 16384);
+  const long long want = (3LL * num_sms() / 2 + p.R - 1) / p.R;
+  const long long by_size = std::max<long long>(1, static_cast<long long>(p.V) * esz / 32768);
   int G = static_cast<int>(std::min<long long>({static_cast<long long>(TOPK_MAX_CLUSTER), want, by_size}));
   G = env_int("SPEC_TOPK_CLUSTER", G, 1, TOPK_MAX_CLUSTER);
   int pow2 = 1;
@@ -530,7 +533,7 @@ int launch_topk(TopkParams &p, int dtype, cudaStream_t stream) {
   attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.R * G), 1, 1);
-  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.blockDim = dim3(TOPK_NT, 1, 1);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
