@@ -504,7 +504,7 @@ def run_gpu(args, w):
 NGRAM_METRIC = "n-gram drafts/sec (sequences drafted from their context), 1 GPU"
 NGRAM_UNIT = "sequences/s"
 NGRAM_BATCH = 10          # calls per chained-latency sample
-NGRAM_FLOOR_US = 3.0      # 5 dependent round trips x ~0.6 us
+NGRAM_FLOOR_US = 2.0      # 3 dependent round trips x ~0.6 us, plus one cluster barrier
 
 
 def _ngram_bytes(lengths_host, K):
@@ -695,9 +695,9 @@ def run_gpu_ngram(args, w):
                "chained_p10_median_p90": q3(chained_us),
                "standalone_p10_median_p90": q3(one_us),
                "floor_us": NGRAM_FLOOR_US,
-               "floor_basis": ("5 dependent global round trips of the kernel (lengths, context and "
-                               "suffix, partial and finished-CTA counter, the G partials, the draft) "
-                               "x ~0.6 us idle L2/HBM round trip on GB300"),
+               "floor_basis": ("3 dependent global round trips of the kernel (lengths; context and "
+                               "suffix; the draft's tokens) x ~0.6 us idle L2/HBM round trip on GB300, "
+                               "plus one cluster barrier (the G <= 8 CTAs of a sequence combine on chip)"),
                "timed": (f"chained: {n_one} batches of {NGRAM_BATCH} calls back to back between CUDA "
                          f"events; standalone: {n_one} calls each between CUDA events (includes "
                          f"the ~4 us fixed cost of a launch between two events)")}

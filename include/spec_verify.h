@@ -358,9 +358,11 @@ int spec_verify_points(const void *target_logits, const int32_t *draft_tokens,
  * and spec_get_status then returns SPEC_ERR_ARG.  Output is bit-exact and
  * deterministic (a pure function of the inputs).
  * Launch geometry: G CTAs share each context's end positions (about two
- * waves of resident CTAs over the batch, at least 4096 positions each); the
- * environment variable SPEC_NGRAM_CTAS, read at each call, sets G instead
- * (any G >= 1 gives the same outputs).
+ * waves of resident CTAs over the batch, at least 4096 positions each),
+ * combining their partials through one thread-block cluster when G <= 8 and
+ * through global memory otherwise; the environment variable
+ * SPEC_NGRAM_CTAS, read at each call, sets G instead (any G >= 1 gives the
+ * same outputs).
  */
 int spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int L, int n_min,
                        int n_max, int min_hits, int K, int32_t *out_draft, int32_t *out_count,

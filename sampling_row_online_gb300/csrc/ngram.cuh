@@ -22,9 +22,13 @@
 // tokens per lane per round, the next round in flight while one is
 // compared; the first round is issued before the suffix is in shared
 // memory).  t[e] is compared with the last token; only a hit walks back.
-// Each CTA reduces its threads' state and stores it as a partial; the last
-// CTA of the sequence to finish (a per-sequence counter, put back to zero by
-// that CTA) combines the G partials and writes the draft.  One launch.
+// Each CTA reduces its threads' state to a partial.  With G <= 8 the
+// sequence's CTAs form one thread-block cluster: the partials go into rank
+// 0's shared memory (distributed shared memory stores) and, after one
+// cluster barrier, rank 0 combines them and writes the draft.  With larger G
+// the partials go to global memory and the last CTA of the sequence to
+// finish (a per-sequence counter, put back to zero by that CTA) combines
+// them.  One launch.
 #pragma once
 
 #include <cstdint>
@@ -53,6 +57,8 @@ struct NgramParams {
   int *done;               // [B] finished-CTA counters, zero between calls
 };
 
+constexpr int NGRAM_MAX_CLUSTER = 8;  // CTAs per sequence that combine through a cluster
+
 struct NgramShared {
   int suf[NGRAM_MAX_N];                 // suf[i] = t[len - 1 - i]
   int cnt[NGRAM_MAX_N + 1];             // histogram: #e with m(e) == k
@@ -60,6 +66,10 @@ struct NgramShared {
   unsigned long long wkey[NWARP];
   int is_last;
   int start, count;
+  // rank 0 of a cluster: the CTAs' partials (key; or counts and latest e per bin)
+  unsigned long long ckey[NGRAM_MAX_CLUSTER];
+  int ccnt[NGRAM_MAX_CLUSTER][NGRAM_MAX_N];
+  int clast[NGRAM_MAX_CLUSTER][NGRAM_MAX_N];
 };
 
 // Four tokens t[4g .. 4g+3]; positions at or past e_end are never compared,
@@ -91,7 +101,7 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
   return v;
 }
 
-template <bool VEC, int MODE>
+template <bool VEC, int MODE, bool CLUSTER>
 __global__ void __launch_bounds__(NT, MODE == NGRAM_REGHIST ? 2 : 3) ngram_kernel(NgramParams p) {
   __shared__ NgramShared sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -221,7 +231,10 @@ __global__ void __launch_bounds__(NT, MODE == NGRAM_REGHIST ? 2 : 3) ngram_kerne
     if (tid == 0) {
       unsigned long long m = 0;
       for (int w = 0; w < NWARP; ++w) m = sh.wkey[w] > m ? sh.wkey[w] : m;
-      static_cast<unsigned long long *>(p.partials)[blockIdx.x] = m;
+      if (CLUSTER)
+        dsmem_st_u64(dsmem_addr(&sh.ckey[rank], 0), m);
+      else
+        static_cast<unsigned long long *>(p.partials)[blockIdx.x] = m;
     }
   } else {
     if (MODE == NGRAM_REGHIST) {
@@ -243,20 +256,33 @@ __global__ void __launch_bounds__(NT, MODE == NGRAM_REGHIST ? 2 : 3) ngram_kerne
       }
     }
     __syncthreads();
-    int *part = static_cast<int *>(p.partials) + static_cast<size_t>(blockIdx.x) * 2 * nb;
-    for (int k = tid; k < nb; k += NT) {
-      part[k] = sh.cnt[p.n_min + k];
-      part[nb + k] = sh.last[p.n_min + k];
+    if (CLUSTER) {
+      for (int k = tid; k < nb; k += NT) {
+        dsmem_st_s32(dsmem_addr(&sh.ccnt[rank][k], 0), sh.cnt[p.n_min + k]);
+        dsmem_st_s32(dsmem_addr(&sh.clast[rank][k], 0), sh.last[p.n_min + k]);
+      }
+    } else {
+      int *part = static_cast<int *>(p.partials) + static_cast<size_t>(blockIdx.x) * 2 * nb;
+      for (int k = tid; k < nb; k += NT) {
+        part[k] = sh.cnt[p.n_min + k];
+        part[nb + k] = sh.last[p.n_min + k];
+      }
     }
   }
-  // the last CTA of the sequence to finish combines the partials
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) sh.is_last = atomicAdd(p.done + b, 1) == G - 1;
-  __syncthreads();
-  if (!sh.is_last) return;
-  __threadfence();
-  if (tid == 0) p.done[b] = 0;  // ready for the next call on this workspace
+  if (CLUSTER) {
+    // rank 0 of the cluster combines the G partials in its shared memory
+    cluster_sync();
+    if (rank != 0) return;
+  } else {
+    // the last CTA of the sequence to finish combines the partials
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) sh.is_last = atomicAdd(p.done + b, 1) == G - 1;
+    __syncthreads();
+    if (!sh.is_last) return;
+    __threadfence();
+    if (tid == 0) p.done[b] = 0;  // ready for the next call on this workspace
+  }
 
   int start = -1;
   if (MODE == NGRAM_MAXKEY) {
@@ -264,7 +290,7 @@ __global__ void __launch_bounds__(NT, MODE == NGRAM_REGHIST ? 2 : 3) ngram_kerne
         static_cast<const unsigned long long *>(p.partials) + static_cast<size_t>(b) * G;
     unsigned long long m = 0;
     for (int r = tid; r < G; r += NT) {
-      const unsigned long long x = __ldcg(parts + r);
+      const unsigned long long x = CLUSTER ? sh.ckey[r] : __ldcg(parts + r);
       m = x > m ? x : m;
     }
     m = warp_max_u64(m);
@@ -275,18 +301,31 @@ __global__ void __launch_bounds__(NT, MODE == NGRAM_REGHIST ? 2 : 3) ngram_kerne
       if (m != 0) start = static_cast<int>(m & 0xFFFFFFFFu) + 1;
     }
   } else {
-    for (int k = tid; k <= p.n_max; k += NT) {
-      sh.cnt[k] = 0;
-      sh.last[k] = -1;
-    }
-    __syncthreads();
-    const int *parts = static_cast<const int *>(p.partials) + static_cast<size_t>(b) * G * 2 * nb;
-    for (int i = tid; i < G * nb; i += NT) {
-      const int r = i / nb, k = i - r * nb;
-      const int c = __ldcg(parts + static_cast<size_t>(r) * 2 * nb + k);
-      if (c > 0) {
-        atomicAdd(&sh.cnt[p.n_min + k], c);
-        atomicMax(&sh.last[p.n_min + k], __ldcg(parts + static_cast<size_t>(r) * 2 * nb + nb + k));
+    if (CLUSTER) {
+      // bin by bin over the G CTAs: the sequence's totals into sh.cnt / sh.last
+      for (int k = tid; k < nb; k += NT) {
+        int c = 0, l = -1;
+        for (int r = 0; r < G; ++r) {
+          c += sh.ccnt[r][k];
+          l = max(l, sh.clast[r][k]);
+        }
+        sh.cnt[p.n_min + k] = c;
+        sh.last[p.n_min + k] = l;
+      }
+    } else {
+      for (int k = tid; k <= p.n_max; k += NT) {
+        sh.cnt[k] = 0;
+        sh.last[k] = -1;
+      }
+      __syncthreads();
+      const int *parts = static_cast<const int *>(p.partials) + static_cast<size_t>(b) * G * 2 * nb;
+      for (int i = tid; i < G * nb; i += NT) {
+        const int r = i / nb, k = i - r * nb;
+        const int c = __ldcg(parts + static_cast<size_t>(r) * 2 * nb + k);
+        if (c > 0) {
+          atomicAdd(&sh.cnt[p.n_min + k], c);
+          atomicMax(&sh.last[p.n_min + k], __ldcg(parts + static_cast<size_t>(r) * 2 * nb + nb + k));
+        }
       }
     }
     __syncthreads();

@@ -770,26 +770,32 @@ int spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int
     w->ngram_cap = B;
   }
   const bool vec = L % 4 == 0 && aligned16(tokens);
-  static const void *const fns[2][3] = {
-      {reinterpret_cast<const void *>(&ngram_kernel<false, NGRAM_MAXKEY>),
-       reinterpret_cast<const void *>(&ngram_kernel<false, NGRAM_REGHIST>),
-       reinterpret_cast<const void *>(&ngram_kernel<false, NGRAM_SMEMHIST>)},
-      {reinterpret_cast<const void *>(&ngram_kernel<true, NGRAM_MAXKEY>),
-       reinterpret_cast<const void *>(&ngram_kernel<true, NGRAM_REGHIST>),
-       reinterpret_cast<const void *>(&ngram_kernel<true, NGRAM_SMEMHIST>)}};
+  // G <= 8: the sequence's CTAs form a cluster and combine on chip
+  const bool cl = G <= NGRAM_MAX_CLUSTER;
+#define SPEC_NGRAM_FNS(V, C)                                                 \
+  {reinterpret_cast<const void *>(&ngram_kernel<V, NGRAM_MAXKEY, C>),        \
+   reinterpret_cast<const void *>(&ngram_kernel<V, NGRAM_REGHIST, C>),       \
+   reinterpret_cast<const void *>(&ngram_kernel<V, NGRAM_SMEMHIST, C>)}
+  static const void *const fns[2][2][3] = {{SPEC_NGRAM_FNS(false, false), SPEC_NGRAM_FNS(false, true)},
+                                           {SPEC_NGRAM_FNS(true, false), SPEC_NGRAM_FNS(true, true)}};
+#undef SPEC_NGRAM_FNS
   NgramParams p{tokens, lengths, B, L, n_min, n_max, min_hits, K, static_cast<int>(G), out_draft, out_count,
                 w->status, w->partials, w->ngram_done};
-  cudaLaunchAttribute pdl;
-  pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cl ? static_cast<unsigned>(G) : 1u;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(B * G), 1, 1);
   cfg.blockDim = dim3(NT, 1, 1);
   cfg.stream = stream;
-  cfg.attrs = &pdl;
-  cfg.numAttrs = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   void *args[] = {&p};
-  cudaError_t e = launch_kernel(&cfg, fns[vec][mode], args);
+  cudaError_t e = launch_kernel(&cfg, fns[vec][cl][mode], args);
   if (e != cudaSuccess) return cuda_fail(e, "ngram_kernel launch");
   return SPEC_OK;
 }

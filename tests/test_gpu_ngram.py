@@ -103,10 +103,12 @@ def test_batch_sizes():
         _check(tokens, lengths, 1, 4, 5)
 
 
-@pytest.mark.parametrize("ctas", [1, 3, 37, 600])
+@pytest.mark.parametrize("ctas", [1, 3, 8, 9, 37, 600])
 def test_forced_ctas_per_sequence(ctas, monkeypatch):
     """Every mode combines its per-CTA partials the same way whatever the
-    number of CTAs per sequence (SPEC_NGRAM_CTAS overrides the choice)."""
+    number of CTAs per sequence (SPEC_NGRAM_CTAS overrides the choice): up to
+    8 through one cluster's shared memory, beyond that through global
+    memory and the last CTA to finish."""
     monkeypatch.setenv("SPEC_NGRAM_CTAS", str(ctas))
     w = NgramWorkload("t", B=7, L=20000, n_min=1, n_max=4, min_hits=1, K=5)
     tokens, lengths = make_contexts(w, device="cuda", seed=ctas)
