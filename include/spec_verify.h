@@ -357,10 +357,11 @@ int spec_verify_points(const void *target_logits, const int32_t *draft_tokens,
  * lengths[b] outside [0, L] sets out_count[b] = -1 and its draft row to -1,
  * and spec_get_status then returns SPEC_ERR_ARG.  Output is bit-exact and
  * deterministic (a pure function of the inputs).
- * Launch geometry: G CTAs share each context's end positions (about two
- * waves of resident CTAs over the batch, at least 4096 positions each),
- * combining their partials through one thread-block cluster when G <= 8 and
- * through global memory otherwise; the environment variable
+ * Launch geometry: G CTAs share each context's end positions: one round of
+ * loads each (4096 positions) when the batch then fits in about one wave of
+ * resident CTAs (up to 1.25 waves), else as many as one wave holds.  They
+ * combine their partials through one thread-block cluster when G <= 8 and
+ * through global memory otherwise.  The environment variable
  * SPEC_NGRAM_CTAS, read at each call, sets G instead (any G >= 1 gives the
  * same outputs).
  */

@@ -742,12 +742,29 @@ int spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const int mode = min_hits == 1 ? NGRAM_MAXKEY
                    : n_max - n_min < NGRAM_REG_BINS ? NGRAM_REGHIST : NGRAM_SMEMHIST;
-  // CTAs per sequence: about two waves of resident CTAs (3 per SM, 2 for
-  // the register histogram) over the batch, each with at least one round of
-  // loads (4096 positions)
-  const long long target = 2 * (mode == NGRAM_REGHIST ? 2LL : 3LL) * num_sms();
-  long long G = std::min<long long>((target + B - 1) / B, std::max(1, (L + 4095) / 4096));
-  G = env_int("SPEC_NGRAM_CTAS", static_cast<int>(std::max(1LL, G)), 1, 1 << 16);
+  const bool vec = L % 4 == 0 && aligned16(tokens);
+  // CTAs per sequence: one round of loads each (4096 positions) if the
+  // batch then fits in about one wave of resident CTAs (up to 1.25 waves),
+  // else as many as one wave holds: the call is a chain of dependent memory
+  // round trips, and a second round or a second wave each add one
+  int per_sm = 0;
+  {
+    const void *probe = vec ? reinterpret_cast<const void *>(&ngram_kernel<true, NGRAM_MAXKEY, true>)
+                            : reinterpret_cast<const void *>(&ngram_kernel<false, NGRAM_MAXKEY, true>);
+    if (mode == NGRAM_REGHIST)
+      probe = vec ? reinterpret_cast<const void *>(&ngram_kernel<true, NGRAM_REGHIST, true>)
+                  : reinterpret_cast<const void *>(&ngram_kernel<false, NGRAM_REGHIST, true>);
+    else if (mode == NGRAM_SMEMHIST)
+      probe = vec ? reinterpret_cast<const void *>(&ngram_kernel<true, NGRAM_SMEMHIST, true>)
+                  : reinterpret_cast<const void *>(&ngram_kernel<false, NGRAM_SMEMHIST, true>);
+    int st0 = occupancy(probe, 0, 0, &per_sm);
+    if (st0) return st0;
+  }
+  const long long slots = std::max(1LL, static_cast<long long>(per_sm) * num_sms());
+  const long long g_round = std::max(1, (L + 4095) / 4096);
+  long long G = static_cast<long long>(B) * g_round * 4 <= slots * 5 ? g_round
+                                                                      : std::max(1LL, std::min(g_round, slots / B));
+  G = env_int("SPEC_NGRAM_CTAS", static_cast<int>(G), 1, 1 << 16);
   if (static_cast<long long>(B) * G > INT_MAX) return fail(SPEC_ERR_ARG, "B too large");
   const size_t part_bytes = static_cast<size_t>(B) * G *
                             (mode == NGRAM_MAXKEY ? 8 : 8 * static_cast<size_t>(n_max - n_min + 1));
@@ -769,7 +786,6 @@ int spec_ngram_propose(const int32_t *tokens, const int32_t *lengths, int B, int
       return cuda_fail(e, "cudaMemsetAsync(ngram counters)");
     w->ngram_cap = B;
   }
-  const bool vec = L % 4 == 0 && aligned16(tokens);
   // G <= 8: the sequence's CTAs form a cluster and combine on chip
   const bool cl = G <= NGRAM_MAX_CLUSTER;
 #define SPEC_NGRAM_FNS(V, C)                                                 \
