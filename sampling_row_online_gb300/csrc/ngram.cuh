@@ -17,7 +17,9 @@
 //     held in registers per thread when n_max - n_min < 8, else in shared
 //     memory.
 //
-// Grid: G CTAs per sequence (G sized to fill the GPU), each scanning a
+// Grid: G CTAs per sequence (G sized from the resident CTAs per SM: 4 for
+// the maximum key, at most 64 registers, so that a batch of long contexts
+// fits in one wave; 2 for the register histogram; 3 otherwise), each scanning a
 // contiguous slice of the end positions with 16-byte loads (U groups of four
 // tokens per lane per round, the next round in flight while one is
 // compared; the first round is issued before the suffix is in shared
@@ -102,7 +104,7 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
 }
 
 template <bool VEC, int MODE, bool CLUSTER>
-__global__ void __launch_bounds__(NT, MODE == NGRAM_REGHIST ? 2 : 3) ngram_kernel(NgramParams p) {
+__global__ void __launch_bounds__(NT, MODE == NGRAM_REGHIST ? 2 : (MODE == NGRAM_MAXKEY ? 4 : 3)) ngram_kernel(NgramParams p) {
   __shared__ NgramShared sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = p.G;
