@@ -212,6 +212,16 @@ def time_oracle(w, n_sequences: int, host_inputs=None, nthreads=None):
     return time.perf_counter() - t0, nthreads
 
 
+def chain_config(w, ws):
+    """The config of a verification workload's line, the same for both arms."""
+    from sampling_row_online_gb300.workloads import describe, input_copies_for_cold_l2
+    per_copy = w.algorithmic_bytes
+    ncopies = input_copies_for_cold_l2(per_copy)
+    return {"workload": f"{w.name}: {describe(w)}", "logits": w.dtype,
+            "per_rank_batch": w.B, "parallelism": f"replicas x{ws} (sequences sharded, no collective)",
+            "l2": f"rotating {ncopies} input copies ({ncopies * per_copy / 1e6:.0f} MB > 2x L2)"}
+
+
 def run_reference(args, w):
     ws, rank, _ = _dist_env()
     if rank != 0:
@@ -228,7 +238,7 @@ def run_reference(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": f"{w.name}: {describe(w)}", "step": "one sequence of the batch"},
+        "config": chain_config(w, ws),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"{args.steps} sequences of {w.name} (cycling through its "
                                    f"batch of {w.B}), fp64 oracle, {threads} OpenMP threads"},
@@ -481,9 +491,7 @@ def run_gpu(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": region_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{w.name}: {describe(w)}", "logits": w.dtype,
-                   "per_rank_batch": w.B, "parallelism": f"replicas x{ws} (sequences sharded, no collective)",
-                   "l2": f"rotating {ncopies} input copies ({ncopies * per_copy / 1e6:.0f} MB > 2x L2)"},
+        "config": chain_config(w, ws),
         "roofline": roofline,
         "achieved_hbm_gbs": achieved,
         "cpu_baseline": cpu,
@@ -530,6 +538,17 @@ def ngram_describe(w):
             f"n in [{w.n_min}, {w.n_max}], min_hits={w.min_hits}, K={w.K}")
 
 
+def ngram_config(w, ws, lengths_h):
+    """The config of an n-gram workload's line, the same for both arms."""
+    from sampling_row_online_gb300.workloads import input_copies_for_cold_l2
+    alg = _ngram_bytes(lengths_h, w.K)
+    ncopies = input_copies_for_cold_l2(alg)
+    return {"workload": f"{w.name}: {ngram_describe(w)}", "per_rank_batch": w.B,
+            "context_tokens_per_step": int(lengths_h.sum()),
+            "parallelism": f"replicas x{ws} (sequences sharded, no collective)",
+            "l2": f"rotating {ncopies} context copies ({ncopies * alg / 1e6:.0f} MB > 2x L2)"}
+
+
 def run_reference_ngram(args, w):
     ws, rank, _ = _dist_env()
     if rank != 0:
@@ -549,7 +568,7 @@ def run_reference_ngram(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": f"{w.name}: {ngram_describe(w)}", "step": "the whole batch"},
+        "config": ngram_config(w, ws, lh),
         "cpu_baseline": {"value": value, "unit": NGRAM_UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} passes over the {w.B} contexts of {w.name}, oracle, 1 thread"},
         "e2e": {"value": value, "unit": NGRAM_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -573,7 +592,9 @@ def run_gpu_ngram(args, w):
     lib = binding.library()
     stream = torch.cuda.current_stream()
     sp = ctypes.c_void_p(stream.cuda_stream)
-    tokens, lengths = make_contexts(w, dev, seed=w.data_seed + 7919 * rank)
+    # generated on the host (the reference arm's contexts, bit for bit), then copied
+    tokens, lengths = make_contexts(w, "cpu", seed=w.data_seed + 7919 * rank)
+    tokens, lengths = tokens.to(dev), lengths.to(dev)
     lengths_h = lengths.cpu().numpy()
     alg = _ngram_bytes(lengths_h, w.K)
     ncopies = input_copies_for_cold_l2(alg)
@@ -706,10 +727,7 @@ def run_gpu_ngram(args, w):
         "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": call_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-        "config": {"workload": f"{w.name}: {ngram_describe(w)}", "per_rank_batch": w.B,
-                   "context_tokens_per_step": int(lengths_h.sum()),
-                   "parallelism": f"replicas x{ws} (sequences sharded, no collective)",
-                   "l2": f"rotating {ncopies} context copies ({ncopies * alg / 1e6:.0f} MB > 2x L2)"},
+        "config": ngram_config(w, ws, lengths_h),
         "context_tokens_per_s": int(lengths_h.sum()) * args.steps * ws / (region_ms / 1e3),
         "roofline": roofline, "achieved_hbm_gbs": achieved, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": args.steps, "clocks": clk, "wall_s": wall,
@@ -756,6 +774,14 @@ def _eagle_oracle_build(w, rows, B):
     return oracle.eagle2_rerank(val, par, tok, w.m)
 
 
+def eagle_config(w, ws):
+    """The config of an EAGLE-2 workload's line, the same for both arms."""
+    alg = _eagle_bytes(w)
+    return {"workload": f"{w.name}: {eagle_describe(w)}", "per_rank_batch": w.B,
+            "parallelism": f"replicas x{ws} (trees sharded, no collective)",
+            "l2": f"draft rows of one build {alg / 1e6:.0f} MB (> 2x L2), read once per build"}
+
+
 def run_reference_eagle2(args, w):
     ws, rank, _ = _dist_env()
     if rank != 0:
@@ -774,7 +800,7 @@ def run_reference_eagle2(args, w):
         "metric": EAGLE_METRIC, "value": value, "unit": EAGLE_UNIT, "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-        "config": {"workload": f"{w.name}: {eagle_describe(w)}", "step": f"{nb} trees of the batch"},
+        "config": eagle_config(w, ws),
         "cpu_baseline": {"value": value, "unit": EAGLE_UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"{args.steps} builds of {nb} trees of {w.name}, oracle, 1 thread"},
         "e2e": {"value": value, "unit": EAGLE_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -972,9 +998,7 @@ def run_gpu_eagle2(args, w):
         "metric": EAGLE_METRIC, "value": value, "unit": EAGLE_UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{w.name}: {eagle_describe(w)}", "per_rank_batch": B,
-                   "parallelism": f"replicas x{ws} (trees sharded, no collective)",
-                   "l2": f"draft rows of one build {alg / 1e6:.0f} MB (> 2x L2), read once per build"},
+        "config": eagle_config(w, ws),
         "roofline": roofline, "achieved_hbm_gbs": achieved, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": args.steps * (2 * w.depth + 1), "clocks": clk, "wall_s": wall,
     }
