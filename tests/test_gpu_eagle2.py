@@ -61,6 +61,29 @@ def test_topk_cluster_sizes(G, monkeypatch):
         np.testing.assert_allclose(prob.cpu().numpy(), rp, rtol=1e-5, atol=1e-30)
 
 
+@pytest.mark.parametrize("dtype,spread", [("bf16", 3), ("bf16", 9), ("f32", 5)])
+def test_topk_best_elements_in_one_thread(dtype, spread, monkeypatch):
+    """A thread reads every 512th 16-byte vector of its CTA's slice.  Put the
+    row's best elements in vectors 512 apart (one thread's) and that
+    thread's other vectors reach the threshold too, so it re-reads all of
+    them instead of offering its best vector alone; the results must not
+    change."""
+    monkeypatch.setenv("SPEC_TOPK_CLUSTER", "1")  # one CTA per row: the slice starts at 0
+    R, V, k = 6, 128256, 8
+    z = _rows(R, V, dtype, seed=spread, ties=False, masked=False).float()
+    ve = 4 if dtype == "f32" else 8
+    for r in range(R):
+        v0 = 17 + 29 * r
+        for j in range(spread):
+            z[r, (v0 + 512 * j) * ve + (j % ve)] = 60.0 - j
+    z = z.to(torch.float32 if dtype == "f32" else torch.bfloat16).contiguous()
+    tok, prob = binding.spec_topk(z, k, 1.0)
+    assert binding.spec_get_status() == 0
+    rt, rp = oracle.topk_prob(z.cpu(), k, 1.0)
+    assert np.array_equal(tok.cpu().numpy(), rt)
+    np.testing.assert_allclose(prob.cpu().numpy(), rp, rtol=1e-5, atol=1e-30)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_topk_flat_and_masked_rows(dtype):
     """Rows where thousands of entries reach the threshold (all equal; or all
