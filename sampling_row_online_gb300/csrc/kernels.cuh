@@ -746,7 +746,7 @@ struct DrawShared {
   float zdraw;               // the draw's total mass Z (bonus draw)
 };
 
-constexpr int PARTS_PER_LANE = 4;
+constexpr int PARTS_PER_LANE = 8;
 
 // (max, sumexp) of the target row (and of the draft row if `pair`) of one job
 // from its C x NCW partials, by one warp: lane l folds partials l, l + 32, ...
