@@ -41,6 +41,22 @@ def test_chain_parity(B, K, V, dtype, T):
     compare_row_stats(g_max, g_sum, ref, T)
 
 
+@pytest.mark.parametrize("B,V,dtype", [(400, 32000, "f32"), (300, 128256, "bf16")])
+def test_large_batches_use_fewer_decision_ctas(B, V, dtype):
+    """A batch too large for one wave of decision CTAs at ~32 KB of each row
+    per CTA takes fewer CTAs per sequence (wider slices of the residual
+    weighing): B = 400 at V = 32000 fp32 and B = 300 at V = 128256 bf16
+    run with 2 and 3 CTAs per sequence instead of 4 and 8."""
+    K, T = 2, 1.0
+    zt, zd, x = _inputs(B, K, V, dtype, T, seed=B + V)
+    seed = 77 + B
+    g_tok, g_n, g_max, g_sum = gpu_chain(zt, zd, x, T, seed)
+    ref = oracle_chain(zt, zd, x, T, seed)
+    compare_chain(g_tok, g_n, ref, positions=B * K)
+    compare_row_stats(g_max, g_sum, ref, T)
+    assert (g_n < K).sum() > B // 4  # enough residual draws to exercise the weighing
+
+
 @pytest.mark.parametrize("V,dtype", [(33, "f32"), (4096, "bf16"), (32000, "bf16"), (128256, "bf16")])
 def test_high_and_low_agreement(V, dtype):
     for sd in (0.05, 3.0):          # near-identical draft (mostly accepted) / unrelated draft
