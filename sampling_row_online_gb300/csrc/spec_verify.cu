@@ -123,6 +123,8 @@ int get_ws(cudaStream_t stream, size_t nparts, Workspace **out) {
 constexpr int DEFAULT_STAGES = 2;               // tile ring depth
 constexpr int TILE_MAX_BYTES = 16 * 1024;       // tile width per row
 constexpr int DRAW_SLICE_BYTES = 32 * 1024;     // draw: bytes of each row per CTA (one wave)
+constexpr int DRAW_SLICE_BYTES_TREE = 16 * 1024;  // the same for a stochastic tree, whose draw weighs
+                                                  // one row pair per rejected candidate, in sequence
 constexpr int DRAW_CTAS_PER_SM = 4;             // draw: resident CTAs per SM (its launch bound)
 
 int env_int(const char *name, int dflt, int lo, int hi) {
@@ -298,12 +300,14 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
   // logits at each token, uniforms, children of the current node
   const int base = p.kind == KIND_TREE_SAMPLE ? (4 * 6 * p.K + 15) / 16 * 16
                                               : (4 * (9 * p.K + 2) + 15) / 16 * 16;
-  // CTAs per sequence: slices of DRAW_SLICE_BYTES of each row, but no more
+  // CTAs per sequence: slices of DRAW_SLICE_BYTES of each row (a stochastic
+  // tree's draw, a chain of weighings, takes more and narrower ones), but no more
   // CTAs than one wave of the batch holds (a grid of many waves pays each
   // CTA's fixed steps -- dependency wait, normalisers, decisions, exchange --
   // once per CTA), and at least enough that a slice stays within the walk's
   // NT * NT entries
-  const long long cd_size = std::max<long long>(1, (row_bytes + DRAW_SLICE_BYTES - 1) / DRAW_SLICE_BYTES);
+  const long long slice_bytes = p.kind == KIND_TREE_SAMPLE ? DRAW_SLICE_BYTES_TREE : DRAW_SLICE_BYTES;
+  const long long cd_size = std::max<long long>(1, (row_bytes + slice_bytes - 1) / slice_bytes);
   const long long cd_wave = std::max<long long>(1, (static_cast<long long>(DRAW_CTAS_PER_SM) * num_sms() + p.B - 1) / p.B);
   const long long cd_walk = (static_cast<long long>(p.V) + NT * NT - 1) / (NT * NT);
   int CD = static_cast<int>(std::min<long long>(MAX_CLUSTER, std::max(cd_walk, std::min(cd_size, cd_wave))));
