@@ -1917,7 +1917,43 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
     return;
   }
   const int nparts = p.C * NCW;
-  for (int r = warp; r < J; r += NWARP) {
+  // rows of at most 4 partials per lane: a warp loads up to FIN_ROWS of its
+  // rows at once (one round trip for all), then folds each in the same order
+  constexpr int FIN_ROWS = 8;
+  for (int r0 = warp; nparts <= 32 * 4 && r0 < J; r0 += NWARP * FIN_ROWS) {
+    float4 a[FIN_ROWS][4];
+#pragma unroll
+    for (int q = 0; q < FIN_ROWS; ++q) {
+      const int r = r0 + q * NWARP;
+      const float4 *parts = p.partials + static_cast<size_t>(r < J ? job_of(p, b, r) : 0) * nparts;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = lane + 32 * k;
+        a[q][k] = (r < J && j < nparts) ? __ldcg(parts + j)
+                                        : make_float4(-INFINITY, __int_as_float(INT_MAX), 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < FIN_ROWS; ++q) {
+      const int r = r0 + q * NWARP;
+      if (r >= J) break;  // warp-uniform
+      float v = -INFINITY;
+      int idx = INT_MAX;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) am_combine(v, idx, a[q][k].x, __float_as_int(a[q][k].y));
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float v2 = __shfl_xor_sync(0xFFFFFFFFu, v, off);
+        const int i2 = __shfl_xor_sync(0xFFFFFFFFu, idx, off);
+        am_combine(v, idx, v2, i2);
+      }
+      if (lane == 0) {
+        s_amax[r] = idx == INT_MAX ? 0 : idx;  // every logit -inf: first index
+        s_vmax[r] = v;
+      }
+    }
+  }
+  for (int r = warp; nparts > 32 * 4 && r < J; r += NWARP) {
     float v = -INFINITY;
     int idx = INT_MAX;
     const float4 *parts = p.partials + static_cast<size_t>(job_of(p, b, r)) * nparts;
