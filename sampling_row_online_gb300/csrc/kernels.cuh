@@ -1535,6 +1535,9 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
     gu[i] = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
   }
   pdl_wait();  // the row partials of the first launch are complete and visible
+  // the status word is final now (only the first launch sets its timeout
+  // bit); read here, its latency hides behind the partials' loads
+  const bool timed_out = stream_timed_out(p);
   if (blockIdx.x == 0 && tid < p.nshard) p.tickets[tid * TICKET_STRIDE] = 0;  // for the next call
 
   // ---- normalisers of all 2K+1 rows (target 0..K, draft 0..K-1), one job
@@ -1605,7 +1608,7 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   }
   cluster_wait();  // every peer is running (pairs with the arrive above)
   if (err) return;
-  if (stream_timed_out(p)) {
+  if (timed_out) {
     if (rank == 0) {
       for (int e = tid; e <= K; e += NT) out[e] = -1;
       if (tid == 0) p.out_n[b] = -1;
@@ -1764,12 +1767,15 @@ __global__ void __launch_bounds__(NT, 4) tree_draw_kernel(const Params p) {
   }
   __syncthreads();
   pdl_wait();  // the row partials of the first launch are complete and visible
+  // final now (only the first launch sets the timeout bit); read before the
+  // cluster barrier, so its latency hides behind it
+  const bool timed_out = stream_timed_out(p);
   if (blockIdx.x == 0 && tid < p.nshard) p.tickets[tid * TICKET_STRIDE] = 0;  // for the next call
   const int err = tst[0];
   const int W1 = p.max_depth + 1;
   int32_t *path = p.out_tokens + static_cast<size_t>(b) * W1;
   cluster_wait();  // pairs with the arrive above
-  if (!err && stream_timed_out(p)) {
+  if (!err && timed_out) {
     if (rank == 0) {
       for (int j = tid; j < W1; j += NT) path[j] = -1;
       if (tid == 0) p.out_n[b] = -1;
@@ -1909,13 +1915,10 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
   pdl_launch_dependents();  // the next kernel may start its set-up
   for (int e = tid; e < ntok; e += NT) s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * ntok + e);
   pdl_wait();
+  // final now (only the first launch sets the timeout bit); consulted after
+  // the partials' folds, so its latency hides behind their loads
+  const bool timed_out = stream_timed_out(p);
   if (b == 0 && tid < p.nshard) p.tickets[tid * TICKET_STRIDE] = 0;  // for the next call
-  if (stream_timed_out(p)) {
-    const int W = p.kind == KIND_TREE ? p.max_depth + 1 : p.K + 1;
-    for (int e = tid; e < W; e += NT) p.out_tokens[static_cast<size_t>(b) * W + e] = -1;
-    if (tid == 0) p.out_n[b] = -1;
-    return;
-  }
   const int nparts = p.C * NCW;
   // rows of at most 4 partials per lane: a warp loads up to FIN_ROWS of its
   // rows at once (one round trip for all), then folds each in the same order
@@ -1979,6 +1982,12 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
     }
   }
   __syncthreads();
+  if (timed_out) {  // the partials may be incomplete: no outputs drawn from them
+    const int W = p.kind == KIND_TREE ? p.max_depth + 1 : p.K + 1;
+    for (int e = tid; e < W; e += NT) p.out_tokens[static_cast<size_t>(b) * W + e] = -1;
+    if (tid == 0) p.out_n[b] = -1;
+    return;
+  }
 
   if (p.kind == KIND_GREEDY_CHAIN) {
     const int K = p.K, R = 2 * K + 1;
