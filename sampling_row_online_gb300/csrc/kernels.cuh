@@ -1912,8 +1912,12 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
   float *s_vmax = reinterpret_cast<float *>(ish + 2 * J);  // [J]
 
   const int ntok = p.kind == KIND_TREE ? J : p.K;
+  int *s_par = ish + 3 * J;  // tree: parents [N]
   pdl_launch_dependents();  // the next kernel may start its set-up
+  // inputs the first launch does not write: tokens (and parents)
   for (int e = tid; e < ntok; e += NT) s_tok[e] = __ldg(p.tokens + static_cast<size_t>(b) * ntok + e);
+  if (p.kind == KIND_TREE)
+    for (int e = tid; e < J; e += NT) s_par[e] = __ldg(p.parent + static_cast<size_t>(b) * p.parent_stride + e);
   pdl_wait();
   // final now (only the first launch sets the timeout bit); consulted after
   // the partials' folds, so its latency hides behind their loads
@@ -2024,43 +2028,55 @@ __global__ void __launch_bounds__(NT) finish_kernel(const Params p) {
     return;
   }
 
-  // tree: J = N nodes
+  // tree: J = N nodes.  Node c (c >= 1) is accepted iff every edge on its
+  // path to the root is: its token equals the argmax of its parent's row.
+  // Every thread takes its nodes and walks their ancestors (parent < child,
+  // so a walk ends at the root within max_depth steps, else the tree is too
+  // deep); the deepest accepted node, lowest index first, is the largest
+  // key (depth, inverted index) of a block-wide maximum.
   const int N = J;
-  int *s_par = ish + 3 * J;
-  int *s_depth = s_par + N;
-  unsigned char *s_acc = reinterpret_cast<unsigned char *>(s_depth + N);
-  for (int e = tid; e < N; e += NT) s_par[e] = __ldg(p.parent + static_cast<size_t>(b) * p.parent_stride + e);
+  __shared__ int s_bad[2];  // a malformed parent (or too deep a tree), a token out of range
+  __shared__ unsigned long long s_best;
+  if (tid == 0) {
+    s_bad[0] = s_par[0] != -1;
+    s_bad[1] = 0;
+    s_best = 0ull;
+  }
+  __syncthreads();
+  for (int c2 = 1 + tid; c2 < N; c2 += NT) {
+    const int pc = s_par[c2], x = s_tok[c2];
+    if (pc < 0 || pc >= c2) s_bad[0] = 1;
+    if (x < 0 || x >= p.V) s_bad[1] = 1;
+  }
+  __syncthreads();
+  if (!s_bad[0]) {
+    unsigned long long best = 0ull;
+    for (int c2 = tid; c2 < N; c2 += NT) {
+      int d = 0;
+      bool acc = true;
+      for (int a = c2; a != 0 && d <= p.max_depth; ++d) {
+        const int pa = s_par[a];
+        acc = acc && s_tok[a] == s_amax[pa];
+        a = pa;
+      }
+      if (d > p.max_depth) s_bad[0] = 1;
+      else if (acc) best = max(best, (static_cast<unsigned long long>(d) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(c2)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+    if (lane == 0) atomicMax(&s_best, best);
+  }
   __syncthreads();
   if (tid == 0) {
     const int W = p.max_depth + 1;
     int32_t *path = p.out_tokens + static_cast<size_t>(b) * W;
-    int bad_parent = s_par[0] != -1, bad_tok = 0;
-    s_depth[0] = 0;
-    s_acc[0] = 1;
-    int bestn = 0;
-    for (int c2 = 1; c2 < N && !bad_parent; ++c2) {
-      const int pc = s_par[c2];
-      if (pc < 0 || pc >= c2) {
-        bad_parent = 1;
-        break;
-      }
-      const int d = s_depth[pc] + 1;
-      if (d > p.max_depth) {
-        bad_parent = 1;
-        break;
-      }
-      const int x = s_tok[c2];
-      if (x < 0 || x >= p.V) bad_tok = 1;
-      s_depth[c2] = d;
-      s_acc[c2] = s_acc[pc] && x == s_amax[pc];
-      if (s_acc[c2] && d > s_depth[bestn]) bestn = c2;
-    }
-    if (bad_parent || bad_tok) {
+    if (s_bad[0] || s_bad[1]) {
       for (int e = 0; e < W; ++e) path[e] = -1;
       p.out_n[b] = -1;
-      atomicOr(p.status, bad_parent ? ST_PARENT : ST_TOKEN);
+      atomicOr(p.status, s_bad[0] ? ST_PARENT : ST_TOKEN);
     } else {
-      const int d = s_depth[bestn];
+      const int bestn = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(s_best));
+      const int d = static_cast<int>(s_best >> 32);
       for (int e = d + 1; e < W; ++e) path[e] = -1;
       path[d] = s_amax[bestn];
       for (int n2 = bestn, e = d - 1; n2 != 0; n2 = s_par[n2], --e) path[e] = s_tok[n2];
