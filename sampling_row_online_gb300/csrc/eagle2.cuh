@@ -640,6 +640,15 @@ __global__ void __launch_bounds__(NT) rerank_kernel(EagleParams p) {
     }
     __syncthreads();
   }
+  // the kept nodes' tokens, fetched now so that the loads overlap the list
+  // positions below (ranks r = tid + i * NT; the rest is read at the end)
+  constexpr int TOK_REGS = 4;
+  int tkr[TOK_REGS];
+#pragma unroll
+  for (int i = 0; i < TOK_REGS; ++i) {
+    const int r = tid + i * NT;
+    tkr[i] = (!bad && r < m) ? __ldg(tok + byrank[r]) : -1;
+  }
   int32_t *op = p.out_par + static_cast<size_t>(b) * (m + 1);
   int32_t *ot = p.out_tok + static_cast<size_t>(b) * (m + 1);
   int32_t *oi = p.out_idx + static_cast<size_t>(b) * (m + 1);
@@ -649,16 +658,19 @@ __global__ void __launch_bounds__(NT) rerank_kernel(EagleParams p) {
     return;
   }
   // list position of the kept node of rank r: 1 + kept nodes before it by
-  // (depth, rank); written to rank[] of that node for the parent remap
+  // (depth, rank); written to key[] of that node for the parent remap.  The
+  // depths by rank go to rank[] first (its ranks are no longer needed).
+  __syncthreads();
+  for (int r = tid; r < m; r += NT) rank[r] = depth[byrank[r]];
   __syncthreads();
   for (int r = tid; r < m; r += NT) {
-    const int c = byrank[r], d = depth[c];
+    const int d = rank[r];
     int q = 1;
     for (int r2 = 0; r2 < m; ++r2) {
-      const int d2 = depth[byrank[r2]];
+      const int d2 = rank[r2];
       q += d2 < d || (d2 == d && r2 < r);
     }
-    key[c] = static_cast<unsigned long long>(q);  // key[] reused: list position
+    key[byrank[r]] = static_cast<unsigned long long>(q);  // key[] reused: list position
   }
   __syncthreads();
   if (tid == 0) {
@@ -666,12 +678,16 @@ __global__ void __launch_bounds__(NT) rerank_kernel(EagleParams p) {
     ot[0] = __ldg(tok);
     oi[0] = 0;
   }
-  for (int r = tid; r < m; r += NT) {
+  for (int r = tid, i = 0; r < m; r += NT, ++i) {
     const int c = byrank[r];
     const int q = static_cast<int>(key[c]);
     const int u = spar[c];
     op[q] = u == 0 ? 0 : static_cast<int>(key[u]);
-    ot[q] = __ldg(tok + c);
+    int t = -1;
+#pragma unroll
+    for (int i2 = 0; i2 < TOK_REGS; ++i2)
+      if (i2 == i) t = tkr[i2];
+    ot[q] = i < TOK_REGS ? t : __ldg(tok + c);
     oi[q] = c;
   }
 }
