@@ -518,6 +518,8 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
     }
     int pseq = 0;
     bool tmo = false;
+    // every logit is streamed once: its lines are the first that L2 evicts
+    const uint64_t pol = policy_evict_first();
     auto next_stage = [&]() -> int {  // wait until the next stage is free
       // Lane 0 alone waits (it alone issues the copies) and the warp learns
       // the outcome through the shuffle.  Were every lane to wait, a lane
@@ -578,8 +580,8 @@ __global__ void __launch_bounds__(NT_ROW, 2) row_kernel(const Params p) {
           if (lane == 0) {
             const uint32_t bytes = static_cast<uint32_t>(n) * E::BYTES;
             mbar_arrive_expect_tx(&full[s], bytes * pc.nrows);
-            bulk_g2s(stage_row(s, 0), pc.rt + off, bytes, &full[s]);
-            if (pc.nrows == 2) bulk_g2s(stage_row(s, 1), pc.rd + off, bytes, &full[s]);
+            bulk_g2s_hint(stage_row(s, 0), pc.rt + off, bytes, &full[s], pol);
+            if (pc.nrows == 2) bulk_g2s_hint(stage_row(s, 1), pc.rd + off, bytes, &full[s], pol);
           }
         } else {
           const int npad = (n + VE - 1) / VE * VE;
