@@ -744,8 +744,8 @@ struct DrawShared {
   float scan[NWARP + 1];     // block scan scratch
   int ired[NWARP];           // block reduction scratch
   int pick;                  // walk result
-  int near_acc;              // an acceptance test of the sequence was near its boundary
   float zdraw;               // the draw's total mass Z (bonus draw)
+  unsigned long long mrej, mnear, mbad;  // chain: positions rejected / near a boundary / with a bad token
 };
 
 constexpr int PARTS_PER_LANE = 8;
@@ -1497,7 +1497,8 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VE = E::VE;
   // dynamic: row max [R], row sumexp [R], logits at x [2K], ok [K], u [K],
-  // tokens [K], then (16-byte aligned) the walk buffer
+  // tokens [K], folded normalisers m c + log2 S of target and draft [K+1]
+  // each, draw uniforms [K+1], then (16-byte aligned) the walk buffer
   extern __shared__ __align__(16) float dsh[];
   __shared__ DrawShared sh;
 
@@ -1512,6 +1513,7 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   int *gok = reinterpret_cast<int *>(dsh + 2 * R + 2 * K);
   float *gu = dsh + 2 * R + 3 * K;
   int *gtok = reinterpret_cast<int *>(dsh + 2 * R + 4 * K);
+  float *glt = dsh + 2 * R + 5 * K, *gld = glt + K + 1, *gw = gld + K + 1;
   float *wbuf = dsh + p.wbuf_off / 4;
 
   // every CTA of the cluster must be running before any DSMEM store: arrive
@@ -1522,11 +1524,17 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   pdl_launch_dependents();
 
   // ---- inputs (not produced by the first launch): the draft count, tokens,
-  // their logits, uniforms.  A point-mass draft has draft logit 0 at x and
+  // their logits, the uniforms of the tests (slot 0) and of the draw at
+  // every position (slot 1).  A point-mass draft has draft logit 0 at x and
   // draft normalisers (0, 1), so q(x) = 1.
   const int kc = p.counts ? __ldg(p.counts + b) : K;
   const bool bad_count = kc < 0 || kc > K;
   const int kb = bad_count ? 0 : kc;  // drafts of this sequence
+  if (tid == 0) {
+    sh.mrej = 0ull;
+    sh.mnear = 0ull;
+    sh.mbad = 0ull;
+  }
   for (int i = tid; i < K; i += NT) {
     const int x = __ldg(p.tokens + static_cast<size_t>(b) * K + i);
     const int ok = i >= kb || (x >= 0 && x < p.V);  // drafts past the count are not read
@@ -1536,6 +1544,9 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
     gx[2 * i + 1] = (ok && i < kb && !p.point) ? E::load(draft_row<DT>(p, b, i), x) : 0.f;
     gu[i] = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 0u);
   }
+  for (int i = tid; i <= K; i += NT)
+    gw[i] = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i), 1u);
+  __syncthreads();  // the inputs, for the warps that take the tests below
   pdl_wait();  // the row partials of the first launch are complete and visible
   // the status word is final now (only the first launch sets its timeout
   // bit); read here, its latency hides behind the partials' loads
@@ -1543,56 +1554,42 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   if (blockIdx.x == 0 && tid < p.nshard) p.tickets[tid * TICKET_STRIDE] = 0;  // for the next call
 
   // ---- normalisers of all 2K+1 rows (target 0..K, draft 0..K-1), one job
-  // (row pair, or the bonus row) per warp
+  // (row pair, or the bonus row) per warp; the warp of position i < kb also
+  // takes its acceptance test and records it in the sequence's bit masks
   const int nparts = p.C * NCW;
   for (int i = warp; i <= K; i += NWARP) {
     float mt, st, md, sd;
     warp_job_norms(p.partials + static_cast<size_t>(job_of(p, b, i)) * nparts, nparts, c, i < K && !p.point, mt,
                    st, md, sd);
     if (lane == 0) {
+      const float mdr = p.point ? 0.f : md, sdr = p.point ? 1.f : sd;
       rmax[i] = mt;
       rsum[i] = st;
+      glt[i] = __fadd_rn(__fmul_rn(mt, c), log2f(st));
+      gld[i] = (i < K && !p.point) ? __fadd_rn(__fmul_rn(md, c), log2f(sd)) : 0.f;
       if (i < K) {
-        rmax[K + 1 + i] = p.point ? 0.f : md;
-        rsum[K + 1 + i] = p.point ? 1.f : sd;
+        rmax[K + 1 + i] = mdr;
+        rsum[K + 1 + i] = sdr;
+      }
+      if (i < kb) {
+        const unsigned long long bit = 1ull << i;
+        const float a = fmaf(gx[2 * i], c, -(mt * c));
+        const float d = fmaf(gx[2 * i + 1], c, -(mdr * c));
+        const float ratio = ex2(a - d) * (sdr / st);  // p_i(x_i) / q_i(x_i)
+        if (!gok[i]) atomicOr(&sh.mbad, bit);
+        if (!(gu[i] < ratio)) atomicOr(&sh.mrej, bit);
+        if (isfinite(ratio) && fabsf(gu[i] - ratio) <= NEAR_REL * fmaxf(ratio, 0x1p-24f)) atomicOr(&sh.mnear, bit);
       }
     }
   }
   __syncthreads();
 
-  // ---- the kb acceptance tests by warp 0, one lane per position (ballots):
-  // n = the first reject, or kb; a draft token out of range is an error
-  if (warp == 0) {
-    int nrej = kb, bad = bad_count, near = 0;
-    for (int i0 = 0; i0 < kb; i0 += 32) {
-      const int i = i0 + lane;
-      bool rej = false, bd = false, nr = false;
-      if (i < kb) {
-        bd = !gok[i];
-        const float a = fmaf(gx[2 * i], c, -(rmax[i] * c));
-        const float d = fmaf(gx[2 * i + 1], c, -(rmax[K + 1 + i] * c));
-        const float ratio = ex2(a - d) * (rsum[K + 1 + i] / rsum[i]);  // p_i(x_i) / q_i(x_i)
-        rej = !(gu[i] < ratio);
-        nr = isfinite(ratio) && fabsf(gu[i] - ratio) <= NEAR_REL * fmaxf(ratio, 0x1p-24f);
-      }
-      if (__any_sync(0xFFFFFFFFu, bd)) bad = 1;
-      const unsigned m = __ballot_sync(0xFFFFFFFFu, rej);
-      const unsigned nm = __ballot_sync(0xFFFFFFFFu, nr);
-      if (nrej == kb) {  // tests up to and including the first reject
-        const int f = m ? __ffs(m) - 1 : 31;
-        if (nm & (f == 31 ? 0xFFFFFFFFu : ((2u << f) - 1u))) near = 1;
-        if (m) nrej = i0 + f;
-      }
-    }
-    if (lane == 0) {
-      sh.bi[0] = nrej;
-      sh.bi[1] = bad;
-      sh.near_acc = near;
-    }
-  }
-  __syncthreads();
-  const int err = sh.bi[1];
-  const int n = sh.bi[0];
+  // ---- n = the first reject, or kb; a draft token out of range is an
+  // error; a test up to n near its boundary is counted
+  const unsigned long long mrej = sh.mrej;
+  const int err = bad_count || sh.mbad != 0ull;
+  const int n = mrej ? __ffsll(static_cast<long long>(mrej)) - 1 : kb;
+  const bool near_acc = (sh.mnear & (n >= 63 ? ~0ull : (2ull << n) - 1ull)) != 0ull;
   int32_t *out = p.out_tokens + static_cast<size_t>(b) * (K + 1);
   if (rank == 0) {
     for (int r = tid; r < R; r += NT) {
@@ -1622,14 +1619,14 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
     // ---- bonus: rank 0 draws from p at position kb using the streaming
     // partials (the target half of a pair job's partials when kb < K)
     if (rank == 0) {
-      const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(kb), 1u);
+      const float u = gw[kb];
       int who;
       bool nd = false;
       const int token = bonus_draw<DT, TMA>(p, p.partials + static_cast<size_t>(job_of(p, b, kb)) * nparts,
                                             target_row<DT>(p, b, kb), rmax[kb], u, wbuf, sh, who, &nd);
       if (warp == (who >> 5)) {
         const int tk = __shfl_sync(0xFFFFFFFFu, token, who & 31);
-        const bool near = __shfl_sync(0xFFFFFFFFu, static_cast<int>(nd), who & 31) || sh.near_acc;
+        const bool near = __shfl_sync(0xFFFFFFFFu, static_cast<int>(nd), who & 31) || near_acc;
         for (int j = lane; j <= K; j += 32) out[j] = j < kb ? gtok[j] : (j == kb ? tk : -1);
         if (lane == 0) {
           timer_max(p, 2);
@@ -1654,11 +1651,11 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   ds.set(static_cast<int>(rank), p.slice_d, p.V, VE);
   FoldedW W;
   W.c = c;
-  W.lt = __fadd_rn(__fmul_rn(rmax[n], c), log2f(rsum[n]));
-  W.ld = p.point ? 0.f : __fadd_rn(__fmul_rn(rmax[K + 1 + n], c), log2f(rsum[K + 1 + n]));
+  W.lt = glt[n];
+  W.ld = gld[n];
   W.mode = p.point ? W_P_EXCL : W_RESID;
   W.excl = p.point ? gtok[n] : -1;
-  const float u = philox_uniform(p.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(n), 1u);
+  const float u = gw[n];
   int fallback = 0, slot = 0;
   float Ex, cs;
   float Z = cluster_exchange(slice_weigh<DT, TMA>(rt, rd, W, ds, p.V, wbuf, sh, Ex, cs), slot, rank, CD, sh);
@@ -1678,7 +1675,7 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
                                               Z, sh, who, &nd);
   if (warp != (who >> 5)) return;
   const int tk = __shfl_sync(0xFFFFFFFFu, token, who & 31);
-  const bool near = __shfl_sync(0xFFFFFFFFu, static_cast<int>(nd), who & 31) || sh.near_acc;
+  const bool near = __shfl_sync(0xFFFFFFFFu, static_cast<int>(nd), who & 31) || near_acc;
   for (int j = lane; j <= K; j += 32) out[j] = j < n ? gtok[j] : (j == n ? tk : -1);
   if (lane == 0) {
     timer_max(p, 2);

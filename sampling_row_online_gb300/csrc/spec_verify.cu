@@ -296,10 +296,11 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
   }
   // the draw: clusters of CD CTAs, about 32 KB of each row per CTA; the walk
   // buffer holds one warp range of a CTA slice or of a streaming tile
-  // chain: normalisers, logits at x, uniforms, tokens; tree: parent, tokens,
+  // chain: normalisers, logits at x, uniforms, tokens, folded normalisers,
+  // draw uniforms; tree: parent, tokens,
   // logits at each token, uniforms, children of the current node
   const int base = p.kind == KIND_TREE_SAMPLE ? (4 * 6 * p.K + 15) / 16 * 16
-                                              : (4 * (9 * p.K + 2) + 15) / 16 * 16;
+                                              : (4 * (12 * p.K + 5) + 15) / 16 * 16;
   // CTAs per sequence: slices of DRAW_SLICE_BYTES of each row (a stochastic
   // tree's draw, a chain of weighings, takes more and narrower ones), but no more
   // CTAs than one wave of the batch holds (a grid of many waves pays each
