@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(TOPK_NT, 2) topk_kernel(TopkParams p) {
 #pragma unroll
       for (int u = 0; u < TOPK_U; ++u) {
         const int vi = b + u * TOPK_NT + lane;
-        d[u] = vi < hi ? __ldg(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
+        d[u] = vi < hi ? ldg_na(rv + vi) : make_uint4(0u, 0u, 0u, 0u);
       }
     };
     uint4 q[TOPK_U];

@@ -89,6 +89,16 @@ __device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32
       : "memory");
 }
 
+// 16-byte read-only load that does not allocate in L1 (data streamed once
+// per thread; what is read again comes back from L2).
+__device__ __forceinline__ uint4 ldg_na(const uint4 *p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
 // Asynchronous 16-byte copy global -> this thread's shared memory slot (both
 // 16-byte aligned).  Barriers do not wait for it: the issuing thread waits
 // with cp_async_wait_all before it reads the slot.
