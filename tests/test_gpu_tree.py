@@ -74,6 +74,38 @@ def test_malformed_tree_reports_parent_error():
     assert np.all(length.cpu().numpy() == -1)
 
 
+def test_tree_deeper_than_max_depth_reports_parent_error():
+    # a chain of depth 5 verified with max_depth 3: every node's ancestor walk
+    # must stop at the limit and mark the tree malformed
+    parent = [-1, 0, 1, 2, 3, 4]
+    zt, par, tok, _ = _tree_case(2, 6, 40, "f32", seed=3, parent=parent, p_correct=1.0)
+    path, length = binding.spec_verify_tree_greedy(zt, par, tok, max_depth=3)
+    assert binding.spec_get_status() == 7
+    assert np.all(length.cpu().numpy() == -1)
+    assert np.all(path.cpu().numpy() == -1)
+
+
+def test_equal_depth_accepted_siblings_take_the_lowest_index():
+    # nodes 1 and 2 carry the same token (the root row's argmax), and so do
+    # their children 3 and 4 under their own rows: both depth-2 nodes are
+    # accepted, and the path must run through the lower index (1, then 3)
+    parent = [-1, 0, 0, 1, 2, 0]
+    V = 16
+    zt = torch.zeros((1, 6, V), device="cuda")
+    zt[0, 0, 5] = 2.0       # root row: argmax 5
+    zt[0, 1, 7] = 2.0       # node 1's row: argmax 7
+    zt[0, 2, 7] = 2.0       # node 2's row: argmax 7
+    zt[0, 3, 9] = 2.0       # node 3's row: argmax 9 (the bonus)
+    zt[0, 4, 11] = 2.0      # node 4's row: argmax 11
+    tok = torch.tensor([[0, 5, 5, 7, 7, 3]], dtype=torch.int32, device="cuda")
+    par = torch.tensor(parent, dtype=torch.int32, device="cuda")
+    path, length = binding.spec_verify_tree_greedy(zt, par, tok)
+    assert binding.spec_get_status() == 0
+    assert length.item() == 3 and path[0].tolist() == [5, 7, 9]
+    rpath, rlen, st = oracle.verify_tree_greedy(zt.cpu(), parent, tok.cpu())
+    assert st == oracle.OK and rlen.tolist() == [3] and rpath[0].tolist() == [5, 7, 9]
+
+
 def test_node_token_out_of_range():
     zt, par, tok, parent = _tree_case(3, 8, 50, "f32", seed=2)
     tok[1, 3] = 50
