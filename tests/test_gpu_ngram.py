@@ -41,7 +41,9 @@ def _check(tokens, lengths, n_min, n_max, K, min_hits=1):
 SHAPES = [(1, 7, 1, 4, 5, 1), (3, 64, 1, 4, 5, 1), (8, 1000, 2, 6, 8, 1), (16, 4097, 1, 3, 5, 2),
           (5, 30001, 1, 12, 6, 1), (2, 200000, 1, 4, 5, 1), (1, 1 << 20, 3, 8, 48, 1), (300, 2048, 1, 4, 5, 3),
           (4, 4096, 8, 8, 5, 2), (2, 5000, 1, 64, 255, 1), (64, 10000, 1, 4, 0, 1), (8, 8192, 1, 16, 5, 2),
-          (6, 12003, 2, 40, 7, 2), (1, 300000, 1, 8, 5, 4)]
+          (6, 12003, 2, 40, 7, 2), (1, 300000, 1, 8, 5, 4),
+          # min_hits == 1 in a cluster, drafts longer than a warp's lanes
+          (8, 3001, 1, 4, 32, 1), (8, 3001, 1, 4, 33, 1)]
 
 
 @pytest.mark.parametrize("B,L,n_min,n_max,K,min_hits", SHAPES,
