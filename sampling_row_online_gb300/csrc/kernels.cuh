@@ -745,7 +745,9 @@ struct DrawShared {
   int ired[NWARP];           // block reduction scratch
   int pick;                  // walk result
   float zdraw;               // the draw's total mass Z (bonus draw)
-  unsigned long long mrej, mnear, mbad;  // chain: positions rejected / near a boundary / with a bad token
+  // chain: bit i of word i / 64: position i rejected / near its boundary /
+  // with a bad token (K <= 255)
+  unsigned long long mrej[4], mnear[4], mbad[4];
 };
 
 constexpr int PARTS_PER_LANE = 8;
@@ -1530,10 +1532,10 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
   const int kc = p.counts ? __ldg(p.counts + b) : K;
   const bool bad_count = kc < 0 || kc > K;
   const int kb = bad_count ? 0 : kc;  // drafts of this sequence
-  if (tid == 0) {
-    sh.mrej = 0ull;
-    sh.mnear = 0ull;
-    sh.mbad = 0ull;
+  if (tid < 4) {
+    sh.mrej[tid] = 0ull;
+    sh.mnear[tid] = 0ull;
+    sh.mbad[tid] = 0ull;
   }
   for (int i = tid; i < K; i += NT) {
     const int x = __ldg(p.tokens + static_cast<size_t>(b) * K + i);
@@ -1572,13 +1574,15 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
         rsum[K + 1 + i] = sdr;
       }
       if (i < kb) {
-        const unsigned long long bit = 1ull << i;
+        const int wd = i >> 6;
+        const unsigned long long bit = 1ull << (i & 63);
         const float a = fmaf(gx[2 * i], c, -(mt * c));
         const float d = fmaf(gx[2 * i + 1], c, -(mdr * c));
         const float ratio = ex2(a - d) * (sdr / st);  // p_i(x_i) / q_i(x_i)
-        if (!gok[i]) atomicOr(&sh.mbad, bit);
-        if (!(gu[i] < ratio)) atomicOr(&sh.mrej, bit);
-        if (isfinite(ratio) && fabsf(gu[i] - ratio) <= NEAR_REL * fmaxf(ratio, 0x1p-24f)) atomicOr(&sh.mnear, bit);
+        if (!gok[i]) atomicOr(&sh.mbad[wd], bit);
+        if (!(gu[i] < ratio)) atomicOr(&sh.mrej[wd], bit);
+        if (isfinite(ratio) && fabsf(gu[i] - ratio) <= NEAR_REL * fmaxf(ratio, 0x1p-24f))
+          atomicOr(&sh.mnear[wd], bit);
       }
     }
   }
@@ -1586,10 +1590,25 @@ __global__ void __launch_bounds__(NT, 4) draw_kernel(const Params p) {
 
   // ---- n = the first reject, or kb; a draft token out of range is an
   // error; a test up to n near its boundary is counted
-  const unsigned long long mrej = sh.mrej;
-  const int err = bad_count || sh.mbad != 0ull;
-  const int n = mrej ? __ffsll(static_cast<long long>(mrej)) - 1 : kb;
-  const bool near_acc = (sh.mnear & (n >= 63 ? ~0ull : (2ull << n) - 1ull)) != 0ull;
+  int n = kb, err = bad_count;
+  bool near_acc = false;
+  if (kb <= 64) {  // one word (uniform in the CTA)
+    const unsigned long long r = sh.mrej[0];
+    if (r) n = __ffsll(static_cast<long long>(r)) - 1;
+    if (sh.mbad[0]) err = 1;
+    near_acc = (sh.mnear[0] & (n >= 63 ? ~0ull : (2ull << n) - 1ull)) != 0ull;
+  } else {
+    for (int wd = 3; wd >= 0; --wd) {
+      const unsigned long long r = sh.mrej[wd];
+      if (r) n = wd * 64 + __ffsll(static_cast<long long>(r)) - 1;
+      if (sh.mbad[wd]) err = 1;
+    }
+    for (int wd = 0; wd < 4; ++wd) {  // the tests up to and including position n
+      const int hi = n - wd * 64;       // highest bit of this word that counts
+      const unsigned long long upto = hi >= 63 ? ~0ull : (hi < 0 ? 0ull : (2ull << hi) - 1ull);
+      if (sh.mnear[wd] & upto) near_acc = true;
+    }
+  }
   int32_t *out = p.out_tokens + static_cast<size_t>(b) * (K + 1);
   if (rank == 0) {
     for (int r = tid; r < R; r += NT) {

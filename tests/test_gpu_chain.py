@@ -57,6 +57,22 @@ def test_large_batches_use_fewer_decision_ctas(B, V, dtype):
     assert (g_n < K).sum() > B // 4  # enough residual draws to exercise the weighing
 
 
+@pytest.mark.parametrize("K,V,dtype,sd", [(100, 64, "f32", 0.03), (255, 33, "bf16", 0.05), (70, 4096, "f32", 0.02),
+                                          (255, 64, "f32", 0.01)])
+def test_long_chains_decide_past_position_64(K, V, dtype, sd):
+    """Drafts that agree closely with the target (draft logits = target +
+    N(0, sd)): the first reject falls anywhere up to K = 255, past the first
+    64 positions' decision word."""
+    B, T = 24, 1.0
+    zt, zd, x = _inputs(B, K, V, dtype, T, sigma_d=sd, seed=K + V)
+    seed = 99 + K
+    g_tok, g_n, g_max, g_sum = gpu_chain(zt, zd, x, T, seed)
+    ref = oracle_chain(zt, zd, x, T, seed)
+    compare_chain(g_tok, g_n, ref, positions=B * K)
+    compare_row_stats(g_max, g_sum, ref, T)
+    assert (ref["n_accepted"] >= 64).any()
+
+
 @pytest.mark.parametrize("V,dtype", [(33, "f32"), (4096, "bf16"), (32000, "bf16"), (128256, "bf16")])
 def test_high_and_low_agreement(V, dtype):
     for sd in (0.05, 3.0):          # near-identical draft (mostly accepted) / unrelated draft
