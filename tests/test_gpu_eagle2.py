@@ -213,6 +213,31 @@ def test_budget_workload_full_size():
     _budget_parity(w, w.B)
 
 
+@pytest.mark.parametrize("M,m", [(3000, 1500), (8192, 4000)])
+def test_rerank_keeps_more_nodes_than_a_thread_holds(M, m):
+    """Large synthetic budgets: values are products of confidences along the
+    path (a child never above its parent), so the m best nodes form a tree;
+    m beyond 1024 kept nodes takes the rerank's tokens from memory for the
+    ranks its threads do not hold."""
+    B = 2
+    rng = np.random.default_rng(M + m)
+    par = np.zeros((B, M), np.int32)
+    val = np.zeros((B, M), np.float32)
+    tok = rng.integers(0, 50000, (B, M)).astype(np.int32)
+    par[:, 0], val[:, 0] = -1, 1.0
+    for b in range(B):
+        for c in range(1, M):
+            u = int(rng.integers(max(0, c - 40), c))
+            par[b, c] = u
+            val[b, c] = np.float32(val[b, u] * np.float32(rng.uniform(0.3, 1.0)))
+    g_val, g_par, g_tok = (torch.from_numpy(a).cuda() for a in (val, par, tok))
+    op, ot, oi = binding.spec_eagle2_rerank(g_val, g_par, g_tok, m)
+    assert binding.spec_get_status() == 0
+    rp, rt, ri, near = oracle.eagle2_rerank(val.astype(np.float64), par, tok, m)
+    ok = (op.cpu().numpy() == rp).all(1) & (ot.cpu().numpy() == rt).all(1) & (oi.cpu().numpy() == ri).all(1)
+    assert ok.all()
+
+
 def test_kept_tree_feeds_the_tree_mask():
     """The rerank's listing is a valid tree (parent[c] < c) whose mask and
     depths the tree-mask kernel builds."""
