@@ -50,6 +50,20 @@ def test_parity(B, K, V, dtype, T, ragged):
     _compare(out.cpu().numpy(), n.cpu().numpy(), ref, B * max(K, 1))
 
 
+def test_long_point_mass_chains():
+    """K = 150 drafts, nearly all the target's argmax with a dominant logit:
+    first rejects past position 64 (and some chains accepted whole)."""
+    B, K, V, T = 16, 150, 1000, 1.0
+    zt, x = _case(B, K, V, "f32", seed=77, p_good=0.99)
+    top = zt[:, :K].argmax(-1, keepdim=True)
+    zt[:, :K].scatter_add_(2, top, torch.full((B, K, 1), 20.0, device="cuda"))
+    out, n = binding.spec_verify_points(zt, x, T, 31)
+    assert binding.spec_get_status() == 0
+    ref = oracle.verify_points(zt.cpu(), x.cpu(), None, T, 31, nthreads=NTHREADS)
+    _compare(out.cpu().numpy(), n.cpu().numpy(), ref, B * K)
+    assert (ref["n"] >= 64).any()
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_equals_spec_verify_on_one_hot_draft_rows(dtype):
     B, K, V = 48, 5, 50257
