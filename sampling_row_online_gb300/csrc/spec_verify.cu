@@ -123,6 +123,7 @@ int get_ws(cudaStream_t stream, size_t nparts, Workspace **out) {
 constexpr int DEFAULT_STAGES = 2;               // tile ring depth
 constexpr int TILE_MAX_BYTES = 16 * 1024;       // tile width per row
 constexpr int DRAW_SLICE_BYTES = 32 * 1024;     // draw: bytes of each row per CTA (one wave)
+constexpr int DRAW_MAX_VECTORS = 16384;         // chain draw: vectors per CTA slice (64 KB of masses)
 constexpr int DRAW_SLICE_BYTES_TREE = 16 * 1024;  // the same for a stochastic tree, whose draw weighs
                                                   // one row pair per rejected candidate, in sequence
 constexpr int DRAW_CTAS_PER_SM = 4;             // draw: resident CTAs per SM (its launch bound)
@@ -305,17 +306,22 @@ int plan(Params &p, int dtype, bool tma, Geometry *g) {
   // tree's draw, a chain of weighings, takes more and narrower ones), but no more
   // CTAs than one wave of the batch holds (a grid of many waves pays each
   // CTA's fixed steps -- dependency wait, normalisers, decisions, exchange --
-  // once per CTA), and at least enough that a slice stays within the walk's
-  // NT * NT entries
-  const long long slice_bytes = p.kind == KIND_TREE_SAMPLE ? DRAW_SLICE_BYTES_TREE : DRAW_SLICE_BYTES;
+  // once per CTA), and at least enough that a slice stays within what its
+  // walk holds: the vector masses of a chain draw's slice in the walk buffer
+  // (DRAW_MAX_VECTORS), a stochastic tree's warp ranges within NT * NT entries
+  const bool chain = p.kind == KIND_SAMPLE;
+  const long long slice_bytes = chain ? DRAW_SLICE_BYTES : DRAW_SLICE_BYTES_TREE;
   const long long cd_size = std::max<long long>(1, (row_bytes + slice_bytes - 1) / slice_bytes);
-  const long long cd_wave = std::max<long long>(1, (static_cast<long long>(DRAW_CTAS_PER_SM) * num_sms() + p.B - 1) / p.B);
-  const long long cd_walk = (static_cast<long long>(p.V) + NT * NT - 1) / (NT * NT);
+  const long long cd_wave = std::max<long long>(1, (static_cast<long long>(DRAW_CTAS_PER_SM) * num_sms()) / p.B);
+  const long long nvec = (static_cast<long long>(p.V) + VE - 1) / VE;
+  const long long cd_walk = chain ? (nvec + DRAW_MAX_VECTORS - 1) / DRAW_MAX_VECTORS
+                                  : (static_cast<long long>(p.V) + NT * NT - 1) / (NT * NT);
   int CD = static_cast<int>(std::min<long long>(MAX_CLUSTER, std::max(cd_walk, std::min(cd_size, cd_wave))));
   for (;;) {
     const int per_d = (p.V + CD - 1) / CD;
     const int slice_d = (per_d + VE - 1) / VE * VE;
-    if (slice_d > NT * NT) return fail(SPEC_ERR_ARG, "vocabulary too large");
+    if (chain ? (slice_d + VE - 1) / VE > DRAW_MAX_VECTORS : slice_d > NT * NT)
+      return fail(SPEC_ERR_ARG, "vocabulary too large");
     const auto range = [&](int sl) { return ((sl + VE - 1) / VE + NWARP - 1) / NWARP * VE; };
     // the walk buffer: a warp range (tree draw), or the vector masses of a
     // CTA slice and the partials' masses of a row (chain draw)

@@ -46,7 +46,7 @@ def test_large_batches_use_fewer_decision_ctas(B, V, dtype):
     """A batch too large for one wave of decision CTAs at ~32 KB of each row
     per CTA takes fewer CTAs per sequence (wider slices of the residual
     weighing): B = 400 at V = 32000 fp32 and B = 300 at V = 128256 bf16
-    run with 2 and 3 CTAs per sequence instead of 4 and 8."""
+    run with 1 and 2 CTAs per sequence instead of 4 and 8."""
     K, T = 2, 1.0
     zt, zd, x = _inputs(B, K, V, dtype, T, seed=B + V)
     seed = 77 + B
